@@ -1,0 +1,398 @@
+"""Benchmark of the streaming Sinkhorn hot path on one GB300 (or N replicas).
+
+One step = the whole hot path over one synthetic problem: preparation,
+every Sinkhorn iteration of the workload's eps schedule (from a cold start),
+then its plan operator (barycentric projection, grad_x or P V).  Prints one
+JSON line on rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the float64 CPU oracle, bounded sample
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
+on the stream the library launches on; a 256 MB buffer is written between
+steps to flush the 129 MB L2.  The half-update kernel is also timed launch by
+launch with the library's own events (fs_timing_*) over the same region; that
+gives the roofline numbers.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from streaming_sinkhorn_solver_gb300.workloads import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "Sinkhorn iters/s and score-pairs/s at n=m=50k (d=3/64/512); % of roofline"
+DEFAULT_WORKLOAD = "c4_n50k_d512"
+PROFILES = os.path.join(ROOT, "profiles")
+# ex2 issue rate of the special-function units on sm_103 (per SM per clock);
+# the ALU roofline is this times the SM count times the SM clock.
+EX2_PER_CLK_SM = 32
+
+
+def _rank_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        d["source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "streaming_sinkhorn_solver_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as fh:
+                h.update(name.encode())
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_from_profiles(workload: str):
+    """DRAM bytes per launch of the half-update kernel from the committed ncu
+    summary for this workload, or None if absent or taken on other sources."""
+    path = os.path.join(PROFILES, f"half_update_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if line.startswith("- ") and "=" in line:
+            k, v = line[2:].split("=", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_hash") != _kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def _work(w, n, m, d):
+    """Algorithmic work of one step."""
+    iters = w.n_iter
+    pairs = 2 * n * m * iters + (n * m if w.apply else 0)
+    return iters, pairs
+
+
+def _step_fn(fs, w, t, path):
+    import torch
+
+    def step(host=None):
+        src = host if host is not None else t
+        g0 = src["g0"]
+        if host is None:
+            g0.zero_()
+        f, g = src["f"], g0
+        for eps, iters in w.stages:
+            fs.fs_sinkhorn_solve(src["X"], src["a"], src["Y"], src["b"], eps, iters, f, g, path=path)
+        eps_last = w.stages[-1][0]
+        if w.apply == "barycentric":
+            fs.fs_barycentric(src["X"], src["a"], src["Y"], src["b"], eps_last, f, g, src["out"],
+                              path=path)
+        elif w.apply == "grad_x":
+            fs.fs_grad_x(src["X"], src["a"], src["Y"], src["b"], eps_last, f, g, src["out"], path=path)
+        elif w.apply == "pv":
+            fs.fs_apply_plan(src["X"], src["a"], src["Y"], src["b"], eps_last, f, g, src["V"],
+                             src["out"], path=path)
+        return f, g
+    return step
+
+
+def _cpu_baseline(w, inp, seconds: float):
+    """The float64 oracle as it stands, on a bounded sample of this workload:
+    f-updates of a stated number of rows against all m columns."""
+    import oracle as orc
+    n, m, d = w.n, w.m, w.d
+    eps = w.stages[0][0]
+    g = np.zeros(m)
+    # size the sample from a short probe so the timed part takes ~`seconds`
+    probe_rows = np.arange(min(n, max(4, orc.num_threads())), dtype=np.int64)
+    t0 = time.perf_counter()
+    orc.f_update_rows(inp["X"], inp["Y"], inp["b"], eps, g, probe_rows)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    rows_n = int(min(n, max(len(probe_rows), len(probe_rows) * seconds / dt)))
+    rows = np.linspace(0, n - 1, rows_n).astype(np.int64)
+    t0 = time.perf_counter()
+    orc.f_update_rows(inp["X"], inp["Y"], inp["b"], eps, g, rows)
+    dt = time.perf_counter() - t0
+    pairs = rows_n * m
+    return {"value": pairs / dt, "unit": "score-pairs/s", "cores": orc.num_threads(),
+            "kind": "oracle",
+            "sample": f"float64 f-update of {rows_n} evenly spaced rows against all {m} columns "
+                      f"(d={d}), {dt:.1f} s; the full step is {_work(w, n, m, d)[1]:.3e} pairs"}
+
+
+def run_reference(args, w):
+    """The reference arm: the oracle, timed on the host cores."""
+    rank, world, _ = _rank_info()
+    if rank != 0:
+        return
+    import oracle as orc
+    inp = make_inputs(w.name)
+    n, m, d = w.n, w.m, w.d
+    eps = w.stages[0][0]
+    g = np.zeros(m)
+    rows_per_step = max(orc.num_threads(), int(args.ref_rows))
+    times = []
+    rows_all = np.random.default_rng(0).permutation(n)
+    for s in range(args.warmup + args.steps):
+        rows = np.sort(rows_all[(s * rows_per_step) % n:][:rows_per_step]).astype(np.int64)
+        t0 = time.perf_counter()
+        orc.f_update_rows(inp["X"], inp["Y"], inp["b"], eps, g, rows)
+        if s >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    pairs = rows_per_step * m * args.steps
+    value = pairs / tot
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "score-pairs/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "n": n, "m": m, "d": d, "eps": eps},
+            "cpu_baseline": {"value": value, "unit": "score-pairs/s", "cores": orc.num_threads(),
+                             "kind": "oracle",
+                             "sample": f"per step: float64 f-update of {rows_per_step} rows "
+                                       f"against all {m} columns"},
+            "e2e": {"value": value, "unit": "score-pairs/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gb300(args, w):
+    import torch
+    from streaming_sinkhorn_solver_gb300 import binding as fs
+
+    rank, world, local = _rank_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    fs.load_library()
+    n, m, d = w.n, w.m, w.d
+    # weak scaling: every rank solves its own replica of the workload
+    inp = make_inputs(w.name, seed=WORKLOADS[w.name].seed + rank)
+    t = {k: torch.from_numpy(v).to(dev) for k, v in inp.items()}
+    k_out = w.k if w.apply == "pv" else d
+    t["f"] = torch.empty(n, device=dev)
+    t["g0"] = torch.zeros(m, device=dev)
+    t["out"] = torch.empty(n, k_out, device=dev) if w.apply else None
+    path = args.path
+    step = _step_fn(fs, w, t, path)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MB > L2
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+
+    sampler = ClockSampler(dev.index) if rank == 0 or True else None
+    sampler.start()
+    fs.fs_timing_read()
+    fs.fs_timing_enable(True)
+    l0 = fs.fs_launch_count()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for s in range(args.steps):
+        flush.fill_(float(s))
+        ev[s][0].record(stream)
+        step()
+        ev[s][1].record(stream)
+    torch.cuda.synchronize()
+    launches = fs.fs_launch_count() - l0
+    fs.fs_timing_enable(False)
+    (half_ms, apply_ms), (half_n, apply_n) = fs.fs_timing_read()
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    iters, pairs = _work(w, n, m, d)
+    value = world * pairs * args.steps / (total_ms * 1e-3)
+    iters_per_s = world * iters * args.steps / (total_ms * 1e-3)
+
+    # roofline of the dominant kernel (the half-update), from its own events
+    peaks = _peaks()
+    tensor_path = (path == "tensor") or (path == "auto" and d > 16)
+    avg_half_ms = half_ms / max(half_n, 1)
+    pairs_per_half = None
+    # both halves process n*m pairs; the launch count is split evenly f/g
+    pairs_per_half = n * m
+    if tensor_path:
+        flops = 2.0 * pairs_per_half * d
+        achieved = flops / (avg_half_ms * 1e-3) / 1e12
+        peak = float(peaks["bf16_tflops_sustained"])
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak,
+                "peak_source": f"{peaks['source']} bf16 sustained x1 (f16 operands, same nominal rate)"}
+    else:
+        clk = (clocks or {}).get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        peak = EX2_PER_CLK_SM * sms * clk * 1e6 / 1e9  # G ex2/s
+        achieved = pairs_per_half / (avg_half_ms * 1e-3) / 1e9
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Gex2/s",
+                "frac": achieved / peak,
+                "peak_source": f"derived: {EX2_PER_CLK_SM} ex2/clk/SM x {sms} SMs x {clk:.0f} MHz "
+                               f"(median SM clock under load)"}
+    roof["traffic"] = _traffic_from_profiles(w.name)
+    roof["kernel"] = "half_update"
+    roof["avg_launch_ms"] = avg_half_ms
+    roof["launches"] = half_n
+
+    line = {"metric": METRIC, "value": value, "unit": "score-pairs/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16xf16->f32" if tensor_path else "f32", "data": "synthetic",
+            "config": {"workload": w.name, "n": n, "m": m, "d": d,
+                       "stages": [list(s) for s in w.stages], "apply": w.apply,
+                       "l2": "256 MB write between timed steps; inputs also > L2"
+                             if (n + m) * d * 4 > 129e6 else "256 MB write between timed steps"},
+            "iters_per_s": iters_per_s, "roofline": roof, "gpu_launches": int(launches),
+            "clocks": clocks,
+            "apply_ms": apply_ms / max(apply_n, 1) if apply_n else None}
+
+    # end to end through the C ABI with pinned host buffers
+    if not args.no_e2e:
+        host = {k: torch.from_numpy(v).pin_memory() for k, v in inp.items()}
+        host["f"] = torch.empty(n).pin_memory()
+        host["g0"] = torch.zeros(m).pin_memory()
+        host["out"] = torch.empty(n, k_out).pin_memory() if w.apply else None
+        estep = _step_fn(fs, w, host, path)
+        estep(host)
+        torch.cuda.synchronize()
+        e2e_ms = []
+        for s in range(max(1, min(args.steps, 3))):
+            host["g0"].zero_()
+            flush.fill_(float(s))
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            estep(host)
+            torch.cuda.synchronize()
+            e2e_ms.append(1e3 * (time.perf_counter() - t0))
+        # bytes the library copies per step: every call stages its host inputs
+        fb = 4
+        per_solve_h2d = fb * (n * d + n + m * d + m + m)
+        per_solve_d2h = fb * (n + m)
+        n_solves = len(w.stages)
+        h2d = n_solves * per_solve_h2d
+        d2h = n_solves * per_solve_d2h
+        if w.apply:
+            h2d += fb * (n * d + n + m * d + m + n + m + (m * w.k if w.apply == "pv" else 0))
+            d2h += fb * n * k_out
+        e2e_total = sum(e2e_ms)
+        line["e2e"] = {"value": world * pairs * len(e2e_ms) / (e2e_total * 1e-3),
+                       "unit": "score-pairs/s", "h2d_bytes_per_step": int(h2d),
+                       "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_total / len(e2e_ms),
+                       "timer": "host wall clock around the C-ABI calls, stream synchronised"}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = _cpu_baseline(w, inp, args.cpu_seconds)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default=os.environ.get("FS_BENCH_WORKLOAD", DEFAULT_WORKLOAD),
+                    choices=sorted(WORKLOADS))
+    ap.add_argument("--path", choices=["auto", "fma", "tensor"], default="auto")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-rows", type=int, default=64)
+    args = ap.parse_args()
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_gb300(args, w)
+
+
+if __name__ == "__main__":
+    main()

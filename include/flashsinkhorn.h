@@ -1,0 +1,199 @@
+/*
+ * flashsinkhorn.h -- C ABI of the GB300 (sm_103a) streaming Sinkhorn library.
+ *
+ * The method is the one described in "FlashSinkhorn: IO-Aware Entropic
+ * Optimal Transport on GPU" (gist.science technical summary):
+ *   - Problem statement: entropic optimal transport between weighted point
+ *     clouds X (n x d, weights a) and Y (m x d, weights b) with the squared
+ *     Euclidean cost C_ij = ||x_i - y_j||^2, solved by Sinkhorn iterations.
+ *   - Method 1 (attention-form reformulation, Proposition 1): the stabilised
+ *     log-domain update
+ *         f_i <- -eps * LSE_j[ (g_j - C_ij)/eps + log b_j ]
+ *     equals a row LogSumExp of the biased dot-product score matrix
+ *         S_X = (Q K^T + 1 (g_hat + delta)^T) / eps,  Q = sqrt(2) X, K = sqrt(2) Y,
+ *     with g_hat_j = g_j - ||y_j||^2 and delta_j = eps log b_j.  The
+ *     g-update is the symmetric one over K^T with gamma_i = eps log a_i.
+ *   - Method 2 (streaming kernels and tiling): the n x m cost or plan is never
+ *     written to memory; score tiles are formed on chip, reduced with an
+ *     online max / sum-exp and fused with the potential write-back.
+ *   - Method 3 (differentiation): the transport plan
+ *         P_ij = a_i b_j exp((f_i + g_j - C_ij)/eps)
+ *     is applied to vectors without being materialised (barycentric
+ *     projection, gradient with respect to X).
+ *
+ * Conventions shared by every entry point
+ *   - Arrays are float32, row-major and contiguous: X is n x d (row i is
+ *     x_i), Y is m x d, V is m x k, out is n x k (or n x d).
+ *   - A pointer may address device memory of the current device or host
+ *     memory (pinned or pageable).  The library finds out which with
+ *     cudaPointerGetAttributes and stages host arrays through its device
+ *     workspace; host outputs are written back with cudaMemcpyAsync on
+ *     `stream` and are valid once that stream has been synchronised.  The
+ *     caller owns every array; the library never frees or keeps a pointer.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  All device work is enqueued on it; the call returns without
+ *     synchronising unless a host array had to be read or written through
+ *     pageable memory.
+ *   - Weights must be positive and finite; they are used as given (no
+ *     renormalisation).  eps must be positive and finite; both sides of any
+ *     comparison use its float32 value.
+ *   - The library keeps one device workspace per device, grown on demand
+ *     with cudaMalloc and freed by fs_release().  Calls on different
+ *     streams are ordered through an event on that workspace, so they do
+ *     not race, but they do not overlap either.
+ *   - Results are bitwise deterministic for the same inputs, sizes and
+ *     options: partial reductions are merged in a fixed order, with no
+ *     floating-point atomics.
+ *   - Errors are returned as fs_status codes, never as C++ exceptions.  A
+ *     human-readable message for the last non-OK status of the calling
+ *     thread is available from fs_last_error().
+ */
+#ifndef FLASHSINKHORN_H
+#define FLASHSINKHORN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FS_OK = 0,
+    FS_ERR_INVALID_ARG = 1,   /* a size, pointer, eps or option is out of range */
+    FS_ERR_CUDA = 2,          /* a CUDA runtime call failed (message has details) */
+    FS_ERR_OOM = 3,           /* the workspace could not be allocated */
+    FS_ERR_NONFINITE = 4,     /* opt->check_finite found a NaN or Inf in f or g */
+    FS_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up (error word set) */
+    FS_ERR_UNSUPPORTED = 6    /* the requested path cannot run these sizes */
+} fs_status;
+
+/* Compute path.  AUTO picks the FP32-FMA path for d <= 16 and the tcgen05
+ * tensor-core path (fp16 operands with per-tensor power-of-two scaling,
+ * fp32 accumulation) above. */
+typedef enum {
+    FS_PATH_AUTO = 0,
+    FS_PATH_FMA = 1,
+    FS_PATH_TENSOR = 2
+} fs_path;
+
+/* Optional tuning and checking knobs; pass NULL for the defaults (all zero). */
+typedef struct fs_options {
+    int32_t path;          /* fs_path */
+    int32_t splits;        /* column splits per half-update; 0 = choose from the SM count */
+    int32_t check_finite;  /* nonzero: after the call, scan the outputs and return
+                              FS_ERR_NONFINITE if any is NaN/Inf (synchronises) */
+    int32_t reserved[5];   /* must be zero */
+} fs_options;
+
+/*
+ * fs_sinkhorn_solve -- n_iter stabilised log-domain Sinkhorn iterations.
+ *
+ * Method 1 of the pages: one iteration is the f-update from g
+ *     f_i = -eps LSE_j[(g_j - C_ij)/eps + log b_j]          (i < n)
+ * followed by the symmetric g-update from the new f
+ *     g_j = -eps LSE_i[(f_i - C_ij)/eps + log a_i]          (j < m),
+ * each evaluated as a streamed row LSE of the biased dot-product scores
+ * (Proposition 1); the n x m matrix is never stored.
+ *
+ *   X  [n*d], a [n]     source points and weights (host or device)
+ *   Y  [m*d], b [m]     target points and weights
+ *   eps                 entropic regularisation, > 0
+ *   n_iter              iterations, >= 1
+ *   f  [n]   in/out     ignored on entry (the first f-update overwrites it)
+ *   g  [m]   in/out     on entry seeds the first f-update (zeros = cold
+ *                       start); warm starts and eps schedules pass the
+ *                       previous call's g back in
+ *   opt                 NULL or options
+ *   stream              cudaStream_t as void*
+ *
+ * Limits: 1 <= n, m <= 2^31 - 1; 1 <= d <= 4096.
+ * Errors: FS_ERR_INVALID_ARG for sizes out of range, null pointers,
+ * eps <= 0 or not finite, n_iter < 1, nonzero reserved options;
+ * FS_ERR_OOM, FS_ERR_CUDA, FS_ERR_TIMEOUT, FS_ERR_NONFINITE as above.
+ * On error f and g are unspecified.
+ */
+fs_status fs_sinkhorn_solve(const float* X, const float* a, int64_t n,
+                            const float* Y, const float* b, int64_t m, int32_t d,
+                            float eps, int32_t n_iter,
+                            float* f, float* g,
+                            const fs_options* opt, void* stream);
+
+/*
+ * fs_apply_plan -- out = P V without materialising P (Method 3).
+ *
+ *     out_i = sum_j P_ij V_j,   P_ij = a_i b_j exp((f_i + g_j - C_ij)/eps)
+ *
+ *   f [n], g [m]        potentials (any values; typically from fs_sinkhorn_solve)
+ *   V [m*k]             m x k values, row j attached to y_j; 1 <= k <= 4096
+ *   out [n*k]           written
+ * Swapping the roles (Y, b, m, X, a, n, g, f) applies P^T instead, which
+ * gives column marginals (V = ones) and the Y-side barycentric map.
+ * Errors as fs_sinkhorn_solve, plus FS_ERR_INVALID_ARG for k out of range.
+ */
+fs_status fs_apply_plan(const float* X, const float* a, int64_t n,
+                        const float* Y, const float* b, int64_t m, int32_t d,
+                        float eps, const float* f, const float* g,
+                        const float* V, int32_t k, float* out,
+                        const fs_options* opt, void* stream);
+
+/*
+ * fs_barycentric -- the barycentric projection T_i = (P Y)_i / a_i (Method 3:
+ * "barycentric projection ... as an attention-like weighted mean").  The
+ * denominator is the weight a_i, not the realised row sum of P.
+ *   out [n*d]           written
+ */
+fs_status fs_barycentric(const float* X, const float* a, int64_t n,
+                         const float* Y, const float* b, int64_t m, int32_t d,
+                         float eps, const float* f, const float* g, float* out,
+                         const fs_options* opt, void* stream);
+
+/*
+ * fs_grad_x -- gradient of the entropic OT value with respect to X
+ * (Method 3: "gradient computation by the same streaming kernels"):
+ *
+ *     grad_i = 2 (a_i x_i - (P Y)_i)
+ *
+ * which at a Sinkhorn fixed point is the derivative of <a,f> + <b,g>.
+ *   out [n*d]           written
+ */
+fs_status fs_grad_x(const float* X, const float* a, int64_t n,
+                    const float* Y, const float* b, int64_t m, int32_t d,
+                    float eps, const float* f, const float* g, float* out,
+                    const fs_options* opt, void* stream);
+
+/* Device bytes the library's workspace needs for these sizes (k = 0 for a
+ * solve).  The workspace is O((n + m) d): no n x m buffer exists. */
+int64_t fs_workspace_bytes(int64_t n, int64_t m, int32_t d, int32_t k, const fs_options* opt);
+
+/* Synchronise `stream`, read and clear the device error word of the current
+ * device.  Returns FS_OK, FS_ERR_TIMEOUT or FS_ERR_CUDA. */
+fs_status fs_check(void* stream);
+
+/* Free the workspaces of every device (synchronises each). */
+fs_status fs_release(void);
+
+/* Message for the calling thread's last non-OK status ("" if none). */
+const char* fs_last_error(void);
+
+/* Library version, "major.minor.patch". */
+const char* fs_version(void);
+
+/* Number of kernel launches the library has issued since load (all devices);
+ * used by the benchmark to count launches in a timed region. */
+int64_t fs_launch_count(void);
+
+/* Kernel timing, a benchmarking aid.  While enabled (on != 0), the library
+ * records a pair of CUDA events on the launching stream around every launch
+ * of its half-update kernel (kind 0) and plan-application kernel (kind 1).
+ * fs_timing_read synchronises those events and returns, per kind, the summed
+ * elapsed milliseconds and the number of launches since the previous read,
+ * then starts a new count.  Either output pointer may be NULL.  Enabling
+ * adds two event records per timed launch and nothing else. */
+fs_status fs_timing_enable(int32_t on);
+fs_status fs_timing_read(double* ms_by_kind /* [2] */, int64_t* launches_by_kind /* [2] */);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLASHSINKHORN_H */

@@ -1,0 +1,275 @@
+"""ctypes binding of libflashsinkhorn (include/flashsinkhorn.h).
+
+Argument marshalling only: every function passes pointers, sizes and the
+current CUDA stream to the C ABI function of the same name, and every step
+of the computation runs in the library's CUDA kernels.  Arrays are float32,
+C-contiguous torch tensors (CUDA or CPU) or numpy arrays; CPU arrays are
+staged by the library itself.  Nothing is converted silently: a wrong dtype,
+layout or shape raises before the call.
+
+The library must have been built (``python -m streaming_sinkhorn_solver_gb300.build``
+or ``__graft_entry__.build()``); if it is missing the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libflashsinkhorn.so")
+
+FS_OK, FS_ERR_INVALID_ARG, FS_ERR_CUDA, FS_ERR_OOM = 0, 1, 2, 3
+FS_ERR_NONFINITE, FS_ERR_TIMEOUT, FS_ERR_UNSUPPORTED = 4, 5, 6
+_STATUS = {0: "FS_OK", 1: "FS_ERR_INVALID_ARG", 2: "FS_ERR_CUDA", 3: "FS_ERR_OOM",
+           4: "FS_ERR_NONFINITE", 5: "FS_ERR_TIMEOUT", 6: "FS_ERR_UNSUPPORTED"}
+PATHS = {"auto": 0, "fma": 1, "tensor": 2}
+
+EXPORTED = ("fs_sinkhorn_solve", "fs_apply_plan", "fs_barycentric", "fs_grad_x",
+            "fs_workspace_bytes", "fs_check", "fs_release", "fs_last_error", "fs_version",
+            "fs_launch_count", "fs_timing_enable", "fs_timing_read")
+
+
+class FlashSinkhornError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class fs_options(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("splits", ctypes.c_int32),
+                ("check_finite", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library(path: Optional[str] = None):
+    """Load (once) and return the ctypes handle; raises if the .so is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise ImportError(f"{p} is missing: build it with "
+                              "'python -m streaming_sinkhorn_solver_gb300.build'")
+        lib = ctypes.CDLL(p)
+        vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+        opt = ctypes.POINTER(fs_options)
+        lib.fs_sinkhorn_solve.argtypes = [vp, vp, i64, vp, vp, i64, i32, f32, i32, vp, vp, opt, vp]
+        lib.fs_apply_plan.argtypes = [vp, vp, i64, vp, vp, i64, i32, f32, vp, vp, vp, i32, vp, opt, vp]
+        lib.fs_barycentric.argtypes = [vp, vp, i64, vp, vp, i64, i32, f32, vp, vp, vp, opt, vp]
+        lib.fs_grad_x.argtypes = [vp, vp, i64, vp, vp, i64, i32, f32, vp, vp, vp, opt, vp]
+        for fn in ("fs_sinkhorn_solve", "fs_apply_plan", "fs_barycentric", "fs_grad_x",
+                   "fs_check", "fs_release"):
+            getattr(lib, fn).restype = ctypes.c_int
+        lib.fs_workspace_bytes.argtypes = [i64, i64, i32, i32, opt]
+        lib.fs_workspace_bytes.restype = i64
+        lib.fs_check.argtypes = [vp]
+        lib.fs_release.argtypes = []
+        lib.fs_last_error.restype = ctypes.c_char_p
+        lib.fs_version.restype = ctypes.c_char_p
+        lib.fs_launch_count.restype = i64
+        lib.fs_timing_enable.argtypes = [i32]
+        lib.fs_timing_enable.restype = ctypes.c_int
+        lib.fs_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]
+        lib.fs_timing_read.restype = ctypes.c_int
+        if path is None:
+            _lib = lib
+        return lib
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+
+def _is_torch(x) -> bool:
+    return type(x).__module__.startswith("torch")
+
+
+def _ptr(x, name: str, shape) -> int:
+    """Pointer of a float32 C-contiguous tensor/array with the given shape."""
+    if _is_torch(x):
+        import torch
+        if x.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32, got {x.dtype}")
+        if not x.is_contiguous():
+            raise TypeError(f"{name} must be contiguous")
+        if tuple(x.shape) != tuple(shape):
+            raise ValueError(f"{name} has shape {tuple(x.shape)}, expected {tuple(shape)}")
+        return x.data_ptr()
+    if isinstance(x, np.ndarray):
+        if x.dtype != np.float32:
+            raise TypeError(f"{name} must be float32, got {x.dtype}")
+        if not x.flags.c_contiguous:
+            raise TypeError(f"{name} must be C-contiguous")
+        if tuple(x.shape) != tuple(shape):
+            raise ValueError(f"{name} has shape {tuple(x.shape)}, expected {tuple(shape)}")
+        return x.ctypes.data
+    raise TypeError(f"{name} must be a torch tensor or numpy array, got {type(x).__name__}")
+
+
+def _on_cuda(*xs) -> bool:
+    return any(_is_torch(x) and x.is_cuda for x in xs)
+
+
+def _stream(stream, *xs):
+    """The cudaStream_t to use: explicit, else torch's current stream."""
+    if stream is not None:
+        return ctypes.c_void_p(int(getattr(stream, "cuda_stream", stream)))
+    try:
+        import torch
+        if torch.cuda.is_available():
+            return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    except Exception:
+        pass
+    return ctypes.c_void_p(0)
+
+
+def _opts(path: str, splits: int, check_finite: bool):
+    o = fs_options()
+    o.path = PATHS[path]
+    o.splits = int(splits)
+    o.check_finite = 1 if check_finite else 0
+    return ctypes.byref(o)
+
+
+def _raise(status: int):
+    if status != FS_OK:
+        msg = load_library().fs_last_error().decode(errors="replace")
+        raise FlashSinkhornError(status, msg)
+
+
+def _host_sync(stream, *xs):
+    """Host outputs are valid once the stream is synchronised."""
+    if not _on_cuda(*xs):
+        try:
+            import torch
+            if torch.cuda.is_available():
+                torch.cuda.synchronize()
+        except Exception:
+            pass
+
+
+def _new_like(ref, shape):
+    if _is_torch(ref):
+        import torch
+        return torch.empty(shape, dtype=torch.float32, device=ref.device)
+    return np.empty(shape, dtype=np.float32)
+
+
+def _zeros_like(ref, shape):
+    if _is_torch(ref):
+        import torch
+        return torch.zeros(shape, dtype=torch.float32, device=ref.device)
+    return np.zeros(shape, dtype=np.float32)
+
+
+# ---------------------------------------------------------------------------
+# the C ABI, one function each
+
+def fs_sinkhorn_solve(X, a, Y, b, eps: float, n_iter: int, f=None, g=None, *, path: str = "auto",
+                      splits: int = 0, check_finite: bool = False, stream=None) -> Tuple:
+    """n_iter log-domain Sinkhorn iterations; f, g are in/out (g seeds the first
+    f-update, zeros if None).  Returns (f, g)."""
+    n, d = X.shape
+    m = Y.shape[0]
+    f = _new_like(X, (n,)) if f is None else f
+    g = _zeros_like(X, (m,)) if g is None else g
+    st = load_library().fs_sinkhorn_solve(
+        _ptr(X, "X", (n, d)), _ptr(a, "a", (n,)), n, _ptr(Y, "Y", (m, d)), _ptr(b, "b", (m,)), m, d,
+        float(eps), int(n_iter), _ptr(f, "f", (n,)), _ptr(g, "g", (m,)),
+        _opts(path, splits, check_finite), _stream(stream, X))
+    _raise(st)
+    _host_sync(stream, X, f, g)
+    return f, g
+
+
+def fs_apply_plan(X, a, Y, b, eps: float, f, g, V, out=None, *, path: str = "auto",
+                  splits: int = 0, check_finite: bool = False, stream=None):
+    """out = P V with P_ij = a_i b_j exp((f_i + g_j - C_ij)/eps); V is m x k."""
+    n, d = X.shape
+    m = Y.shape[0]
+    squeeze = len(V.shape) == 1
+    k = 1 if squeeze else V.shape[1]
+    out = _new_like(X, (n, k) if not squeeze else (n,)) if out is None else out
+    st = load_library().fs_apply_plan(
+        _ptr(X, "X", (n, d)), _ptr(a, "a", (n,)), n, _ptr(Y, "Y", (m, d)), _ptr(b, "b", (m,)), m, d,
+        float(eps), _ptr(f, "f", (n,)), _ptr(g, "g", (m,)),
+        _ptr(V, "V", (m,) if squeeze else (m, k)), k,
+        _ptr(out, "out", (n,) if squeeze else (n, k)),
+        _opts(path, splits, check_finite), _stream(stream, X))
+    _raise(st)
+    _host_sync(stream, X, out)
+    return out
+
+
+def fs_barycentric(X, a, Y, b, eps: float, f, g, out=None, *, path: str = "auto",
+                   splits: int = 0, check_finite: bool = False, stream=None):
+    """T_i = (P Y)_i / a_i."""
+    n, d = X.shape
+    m = Y.shape[0]
+    out = _new_like(X, (n, d)) if out is None else out
+    st = load_library().fs_barycentric(
+        _ptr(X, "X", (n, d)), _ptr(a, "a", (n,)), n, _ptr(Y, "Y", (m, d)), _ptr(b, "b", (m,)), m, d,
+        float(eps), _ptr(f, "f", (n,)), _ptr(g, "g", (m,)), _ptr(out, "out", (n, d)),
+        _opts(path, splits, check_finite), _stream(stream, X))
+    _raise(st)
+    _host_sync(stream, X, out)
+    return out
+
+
+def fs_grad_x(X, a, Y, b, eps: float, f, g, out=None, *, path: str = "auto", splits: int = 0,
+              check_finite: bool = False, stream=None):
+    """grad_i = 2 (a_i x_i - (P Y)_i)."""
+    n, d = X.shape
+    m = Y.shape[0]
+    out = _new_like(X, (n, d)) if out is None else out
+    st = load_library().fs_grad_x(
+        _ptr(X, "X", (n, d)), _ptr(a, "a", (n,)), n, _ptr(Y, "Y", (m, d)), _ptr(b, "b", (m,)), m, d,
+        float(eps), _ptr(f, "f", (n,)), _ptr(g, "g", (m,)), _ptr(out, "out", (n, d)),
+        _opts(path, splits, check_finite), _stream(stream, X))
+    _raise(st)
+    _host_sync(stream, X, out)
+    return out
+
+
+def fs_workspace_bytes(n: int, m: int, d: int, k: int = 0, *, path: str = "auto",
+                       splits: int = 0) -> int:
+    return int(load_library().fs_workspace_bytes(n, m, d, k, _opts(path, splits, False)))
+
+
+def fs_check(stream=None) -> None:
+    _raise(load_library().fs_check(_stream(stream)))
+
+
+def fs_release() -> None:
+    _raise(load_library().fs_release())
+
+
+def fs_last_error() -> str:
+    return load_library().fs_last_error().decode(errors="replace")
+
+
+def fs_version() -> str:
+    return load_library().fs_version().decode()
+
+
+def fs_launch_count() -> int:
+    return int(load_library().fs_launch_count())
+
+
+def fs_timing_enable(on: bool = True) -> None:
+    _raise(load_library().fs_timing_enable(1 if on else 0))
+
+
+def fs_timing_read():
+    """Returns ((half_ms, apply_ms), (half_launches, apply_launches)) since the last read."""
+    ms = (ctypes.c_double * 2)()
+    cnt = (ctypes.c_int64 * 2)()
+    _raise(load_library().fs_timing_read(ms, cnt))
+    return (ms[0], ms[1]), (int(cnt[0]), int(cnt[1]))

@@ -1,0 +1,178 @@
+// Host orchestration of the FP32-FMA path (d <= 16): buffer layout,
+// preparation, the alternating half-update loop and plan application.
+#include "fs_host.cuh"
+
+#include <algorithm>
+
+namespace fs {
+
+namespace {
+
+struct FmaPlan {
+    int D, DS;
+    int splits_f, splits_g;
+    int64_t cps_f, cps_g;
+};
+
+FmaPlan plan_fma(int64_t n, int64_t m, int32_t d, int sms, const fs_options* opt) {
+    FmaPlan p;
+    p.D = fma_pad_dim(d);
+    p.DS = fma_stride(p.D);
+    const int rpt = p.D <= 4 ? 4 : (p.D <= 8 ? 2 : 1);
+    const int64_t rows_per_block = 256 * rpt;
+    p.splits_f = choose_splits((n + rows_per_block - 1) / rows_per_block, m, sms, 4, 256, opt, &p.cps_f);
+    p.splits_g = choose_splits((m + rows_per_block - 1) / rows_per_block, n, sms, 4, 256, opt, &p.cps_g);
+    return p;
+}
+
+struct FmaBufs {
+    size_t shift_part, shift, PX, PY, nx, ny, lax, lby, partial, phi, apply_part, counter;
+};
+
+void layout_fma(Layout& L, FmaBufs& B, int64_t n, int64_t m, int32_t d, const FmaPlan& p,
+                int apply_k, int apply_splits) {
+    B.shift_part = L.take(sizeof(double) * (size_t)kShiftBlocks * d);
+    B.shift = L.take(sizeof(float) * d);
+    B.PX = L.take(sizeof(float) * (size_t)n * p.DS);
+    B.PY = L.take(sizeof(float) * (size_t)m * p.DS);
+    B.nx = L.take(sizeof(float) * n);
+    B.ny = L.take(sizeof(float) * m);
+    B.lax = L.take(sizeof(float) * n);
+    B.lby = L.take(sizeof(float) * m);
+    const int64_t part = std::max((int64_t)n * p.splits_f, (int64_t)m * p.splits_g);
+    B.partial = L.take(sizeof(float2) * (size_t)part);
+    B.phi = L.take(sizeof(float) * n);
+    B.apply_part =
+        apply_splits > 1 ? L.take(sizeof(float) * (size_t)apply_splits * n * (apply_k + 1)) : 0;
+    B.counter = L.take(sizeof(unsigned int) * 4);
+}
+
+int apply_splits_for(int64_t n, int64_t m, int32_t k, int sms, const fs_options* opt, int64_t* cps) {
+    const int64_t row_blocks = (n + 127) / 128;
+    const int kchunks = k <= 4 ? 1 : (k + 15) / 16;
+    return choose_splits(row_blocks * kchunks, m, sms, 4, 256, opt, cps);
+}
+
+}  // namespace
+
+int64_t workspace_bytes_fma(int64_t n, int64_t m, int32_t d, int32_t k, int sms,
+                            const fs_options* opt) {
+    const FmaPlan p = plan_fma(n, m, d, sms, opt);
+    int64_t cps;
+    const int splits = k > 0 ? apply_splits_for(n, m, k, sms, opt, &cps) : 1;
+    Layout L;
+    FmaBufs B;
+    layout_fma(L, B, n, m, d, p, k, splits);
+    return (int64_t)L.off;
+}
+
+fs_status solve_fma(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) {
+    const int64_t n = P.n, m = P.m;
+    const int32_t d = P.d;
+    const FmaPlan p = plan_fma(n, m, d, c.ws->sms, opt);
+    FmaBufs B;
+    layout_fma(c.L, B, n, m, d, p, 0, 1);
+    FS_TRY(ensure_capacity(c));
+    for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g}) bind(c, *A);
+    for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.g}) FS_TRY(upload(c, *A));
+
+    const double eps = (double)P.eps;
+    const float l_over_eps = (float)(kLog2e / eps);
+    const float kappa = (float)(2.0 * kLog2e / eps);
+    const float eps_ln2 = (float)(eps * kLn2);
+    float* shift = c.at<float>(B.shift);
+    float* PX = c.at<float>(B.PX);
+    float* PY = c.at<float>(B.PY);
+    float* nx = c.at<float>(B.nx);
+    float* ny = c.at<float>(B.ny);
+    float* lax = c.at<float>(B.lax);
+    float* lby = c.at<float>(B.lby);
+    float2* part = c.at<float2>(B.partial);
+
+    FS_CUDA(launch_shift(P.X.dev, n, P.Y.dev, m, d, c.at<double>(B.shift_part), kShiftBlocks, shift,
+                         c.stream));
+    FS_CUDA(launch_pack_fma(P.X.dev, P.a.dev, nullptr, n, d, p.D, shift, l_over_eps, PX, nx, lax,
+                            c.stream));
+    FS_CUDA(launch_pack_fma(P.Y.dev, P.b.dev, P.g.dev, m, d, p.D, shift, l_over_eps, PY, ny, lby,
+                            c.stream));
+
+    HalfArgs hf{PX, PY, n, m, kappa, eps_ln2, nx, lax, P.f.dev, part, p.splits_f, p.cps_f};
+    HalfArgs hg{PY, PX, m, n, kappa, eps_ln2, ny, lby, P.g.dev, part, p.splits_g, p.cps_g};
+    for (int32_t it = 0; it < n_iter; ++it) {
+        int ts = timing_begin(c.stream);
+        FS_CUDA(launch_half_fma(p.D, hf, c.stream));
+        timing_end(ts, TIME_HALF, c.stream);
+        if (p.splits_f > 1)
+            FS_CUDA(launch_merge_lse(part, p.splits_f, n, nx, lax, eps_ln2, P.f.dev, PX + p.D, p.DS,
+                                     c.stream));
+        ts = timing_begin(c.stream);
+        FS_CUDA(launch_half_fma(p.D, hg, c.stream));
+        timing_end(ts, TIME_HALF, c.stream);
+        if (p.splits_g > 1)
+            FS_CUDA(launch_merge_lse(part, p.splits_g, m, ny, lby, eps_ln2, P.g.dev, PY + p.D, p.DS,
+                                     c.stream));
+    }
+    if (opt && opt->check_finite) {
+        FS_TRY(scan_finite(c, P.f.dev, n, c.at<unsigned int>(B.counter)));
+        FS_TRY(scan_finite(c, P.g.dev, m, c.at<unsigned int>(B.counter)));
+    }
+    FS_TRY(download(c, P.f));
+    FS_TRY(download(c, P.g));
+    return FS_OK;
+}
+
+fs_status apply_fma(Call& c, Problem& P, int mode, const fs_options* opt) {
+    const int64_t n = P.n, m = P.m;
+    const int32_t d = P.d, k = P.k;
+    const FmaPlan p = plan_fma(n, m, d, c.ws->sms, opt);
+    int64_t cps;
+    const int splits = apply_splits_for(n, m, k, c.ws->sms, opt, &cps);
+    FmaBufs B;
+    layout_fma(c.L, B, n, m, d, p, k, splits);
+    FS_TRY(ensure_capacity(c));
+    for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g, &P.V, &P.out}) bind(c, *A);
+    for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g, &P.V}) FS_TRY(upload(c, *A));
+
+    const double eps = (double)P.eps;
+    const float l_over_eps = (float)(kLog2e / eps);
+    const float kappa = (float)(2.0 * kLog2e / eps);
+    float* shift = c.at<float>(B.shift);
+    float* PX = c.at<float>(B.PX);
+    float* PY = c.at<float>(B.PY);
+    float* phi = c.at<float>(B.phi);
+    FS_CUDA(launch_shift(P.X.dev, n, P.Y.dev, m, d, c.at<double>(B.shift_part), kShiftBlocks, shift,
+                         c.stream));
+    FS_CUDA(launch_pack_fma(P.X.dev, P.a.dev, nullptr, n, d, p.D, shift, l_over_eps, PX,
+                            c.at<float>(B.nx), c.at<float>(B.lax), c.stream));
+    FS_CUDA(launch_pack_fma(P.Y.dev, P.b.dev, P.g.dev, m, d, p.D, shift, l_over_eps, PY,
+                            c.at<float>(B.ny), c.at<float>(B.lby), c.stream));
+    FS_CUDA(launch_phi(P.f.dev, c.at<float>(B.nx), n, l_over_eps, phi, c.stream));
+
+    ApplyArgs A;
+    A.rows = PX;
+    A.cols = PY;
+    A.phi = phi;
+    A.V = P.V.dev;
+    A.k = k;
+    A.n = n;
+    A.m = m;
+    A.kappa = kappa;
+    A.a = P.a.dev;
+    A.X = P.X.dev;
+    A.d = d;
+    A.out = P.out.dev;
+    A.partial = splits > 1 ? c.at<float>(B.apply_part) : nullptr;
+    A.splits = splits;
+    A.cols_per_split = cps;
+    A.mode = mode;
+    const int ts = timing_begin(c.stream);
+    FS_CUDA(launch_apply_fma(p.D, A, c.stream));
+    timing_end(ts, TIME_APPLY, c.stream);
+    if (splits > 1) FS_CUDA(launch_merge_apply(A, c.stream));
+    if (opt && opt->check_finite)
+        FS_TRY(scan_finite(c, P.out.dev, n * (int64_t)k, c.at<unsigned int>(B.counter)));
+    FS_TRY(download(c, P.out));
+    return FS_OK;
+}
+
+}  // namespace fs

@@ -1,0 +1,113 @@
+// Host-side infrastructure shared by the entry points and the two compute
+// paths: error reporting, the per-device workspace, staging of host arrays.
+#pragma once
+
+#include "flashsinkhorn.h"
+#include "fs_internal.cuh"
+
+#include <mutex>
+#include <string>
+
+namespace fs {
+
+fs_status fail(fs_status st, const char* fmt, ...);
+
+#define FS_CUDA(call)                                                                       \
+    do {                                                                                    \
+        cudaError_t e_ = (call);                                                            \
+        if (e_ != cudaSuccess)                                                              \
+            return ::fs::fail(e_ == cudaErrorMemoryAllocation ? FS_ERR_OOM : FS_ERR_CUDA,  \
+                              "%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_),       \
+                              __FILE__, __LINE__);                                          \
+    } while (0)
+
+#define FS_TRY(expr)                    \
+    do {                                \
+        fs_status s_ = (expr);          \
+        if (s_ != FS_OK) return s_;     \
+    } while (0)
+
+constexpr int kMaxDevices = 64;
+constexpr int kShiftBlocks = 1024;
+
+// One workspace per device: a single cudaMalloc'd arena carved per call.
+struct Workspace {
+    std::mutex mu;
+    char* base = nullptr;
+    size_t cap = 0;
+    cudaEvent_t done = nullptr;        // recorded at the end of every call
+    cudaStream_t last_stream = nullptr;
+    bool used = false;
+    uint32_t* err_word = nullptr;      // device error word (own allocation)
+    int sms = 0;
+};
+
+// Bump layout: offsets are computed first (for sizing), then bound to a base.
+struct Layout {
+    size_t off = 0;
+    size_t take(size_t bytes) {
+        const size_t o = off;
+        off += (bytes + 255) & ~size_t(255);
+        return o;
+    }
+};
+
+// A caller array: used in place (device memory) or staged through the
+// workspace (host memory).  `alias` shares another array's device copy.
+struct Arr {
+    const float* user = nullptr;
+    size_t count = 0;
+    bool host = false;
+    size_t off = 0;
+    float* dev = nullptr;
+    const Arr* alias = nullptr;
+};
+
+struct Call {
+    int dev = 0;
+    cudaStream_t stream = nullptr;
+    Workspace* ws = nullptr;
+    std::unique_lock<std::mutex> lock;
+    Layout L;
+
+    template <typename T>
+    T* at(size_t off) const { return reinterpret_cast<T*>(ws->base + off); }
+};
+
+fs_status begin_call(Call& c, void* stream);
+fs_status end_call(Call& c);
+fs_status ensure_capacity(Call& c);                 // grows to c.L.off bytes
+fs_status classify(Call& c, Arr& a, const float* p, size_t count);
+void bind(Call& c, Arr& a);
+fs_status upload(Call& c, const Arr& a);
+fs_status download(Call& c, const Arr& a);
+fs_status scan_finite(Call& c, const float* v, int64_t len, unsigned int* counter);
+
+// Kernel timing (fs_timing_enable / fs_timing_read).  timing_begin returns a
+// slot (or -1 when timing is off); timing_end closes it.
+enum TimingKind : int { TIME_HALF = 0, TIME_APPLY = 1 };
+int timing_begin(cudaStream_t s);
+void timing_end(int slot, int kind, cudaStream_t s);
+
+int choose_splits(int64_t row_blocks, int64_t nc, int sms, int per_sm, int64_t min_cols,
+                  const fs_options* opt, int64_t* cols_per_split);
+
+// The arrays of one call, staged.
+struct Problem {
+    Arr X, a, Y, b, f, g, V, out;
+    int64_t n = 0, m = 0;
+    int32_t d = 0, k = 0;
+    float eps = 0.f;
+};
+
+// Path entry points.  Each one lays out its buffers after the staging area
+// already in c.L, grows the workspace, binds and uploads the staged arrays,
+// runs, and downloads host outputs.
+fs_status solve_fma(Call& c, Problem& P, int32_t n_iter, const fs_options* opt);
+fs_status apply_fma(Call& c, Problem& P, int mode, const fs_options* opt);
+fs_status solve_tc(Call& c, Problem& P, int32_t n_iter, const fs_options* opt);
+fs_status apply_tc(Call& c, Problem& P, int mode, const fs_options* opt);
+int64_t workspace_bytes_fma(int64_t n, int64_t m, int32_t d, int32_t k, int sms, const fs_options* opt);
+int64_t workspace_bytes_tc(int64_t n, int64_t m, int32_t d, int32_t k, int sms, const fs_options* opt);
+
+}  // namespace fs

@@ -1,0 +1,128 @@
+// Internal declarations shared by the translation units of libflashsinkhorn.
+//
+// Notation (base-2 folded form of the pages' Proposition 1).  With centred
+// points x~ = x - t, y~ = y - t (t is any common shift; the cost is invariant),
+// L = log2(e) and kappa = 2 L / eps, the f-update of the pages,
+//     f_i = -eps LSE_j[(g_j - C_ij)/eps + log b_j],
+// becomes
+//     s_ij  = kappa x~_i . y~_j + beta_j,    beta_j = (g_j - |y~_j|^2) L/eps + log2 b_j
+//     f_i   = |x~_i|^2 - eps ln2 * log2 sum_j 2^{s_ij}
+// and the bias the following g-update needs is
+//     alpha_i = (f_i - |x~_i|^2) L/eps + log2 a_i = log2 a_i - log2 sum_j 2^{s_ij}.
+// The g-update is the same computation with the roles of (X, a, f, alpha) and
+// (Y, b, g, beta) exchanged.  beta and alpha are the pages' g_hat + delta and
+// f_hat + gamma, divided by eps and written in base 2.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include <atomic>
+
+namespace fs {
+
+constexpr double kLog2e = 1.4426950408889634074;   // log2(e)
+constexpr double kLn2 = 0.69314718055994530942;    // ln(2)
+
+// Kernel launches issued by the library (reported by fs_launch_count).
+extern std::atomic<int64_t> g_launches;
+inline void count_launch(int64_t k = 1) { g_launches.fetch_add(k, std::memory_order_relaxed); }
+
+// Device error word bits (set by bounded waits; read by fs_check).
+enum : uint32_t { ERR_TIMEOUT_PRODUCER = 1u, ERR_TIMEOUT_MMA = 2u, ERR_TIMEOUT_EPILOGUE = 4u };
+
+// ---------------------------------------------------------------------------
+// device helpers
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ---------------------------------------------------------------------------
+// FMA path: packed operand arrays.  Row r of a packed array holds the centred
+// coordinates of a point, zero-padded to D, then its current bias (alpha or
+// beta) at index D, padded to a stride DS that is a multiple of 4 floats.
+
+__host__ __device__ constexpr int fma_pad_dim(int d) { return d <= 2 ? 2 : d <= 3 ? 3 : d <= 4 ? 4 : d <= 8 ? 8 : 16; }
+__host__ __device__ constexpr int fma_stride(int D) { return ((D + 1) + 3) / 4 * 4; }
+constexpr int kFmaMaxDim = 16;
+
+// Half-update on the FMA path.  rows: packed array of the side being
+// updated (nr rows); cols: packed array of the other side (nc rows) whose
+// bias slot holds beta (or alpha).  Writes pot[i] and the row bias into
+// rows[i*DS + D] (splits == 1), or (max, sum) partials (splits > 1).
+struct HalfArgs {
+    float* rows;            // packed [nr x DS]; bias slot written
+    const float* cols;      // packed [nc x DS]
+    int64_t nr, nc;
+    float kappa;            // 2 log2(e) / eps
+    float eps_ln2;          // eps * ln 2
+    const float* rnorm;     // |x~_i|^2 [nr]
+    const float* rlogw2;    // log2 of the row weights [nr]
+    float* pot;             // potential out [nr]
+    float2* partial;        // [splits x nr] or nullptr
+    int splits;
+    int64_t cols_per_split;
+};
+cudaError_t launch_half_fma(int D, const HalfArgs& a, cudaStream_t s);
+
+// Merge of split partials: LSE2 = M + log2 sum_s S_s 2^{M_s - M} in split
+// order, then pot = rnorm - eps ln2 LSE2 and bias = rlogw2 - LSE2.
+cudaError_t launch_merge_lse(const float2* partial, int splits, int64_t nr, const float* rnorm,
+                             const float* rlogw2, float eps_ln2, float* pot, float* bias,
+                             int64_t bias_stride, cudaStream_t s);
+
+// Plan application on the FMA path.
+enum ApplyMode : int { APPLY_PV = 0, APPLY_BARY = 1, APPLY_GRAD = 2 };
+struct ApplyArgs {
+    const float* rows;      // packed [n x DS] (centred x~)
+    const float* cols;      // packed [m x DS] with beta from the given g
+    const float* phi;       // (f_i - |x~_i|^2) L/eps  [n]
+    const float* V;         // [m x k]
+    int k;
+    int64_t n, m;
+    float kappa;
+    const float* a;         // weights [n]
+    const float* X;         // raw X [n x d] (grad mode)
+    int d;
+    float* out;             // [n x k]
+    float* partial;         // [splits x n x (k+1)] or nullptr
+    int splits;
+    int64_t cols_per_split;
+    int mode;
+};
+cudaError_t launch_apply_fma(int D, const ApplyArgs& a, cudaStream_t s);
+cudaError_t launch_merge_apply(const ApplyArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Preparation kernels.
+
+// Per-dimension sums of the rows of X and Y in double, in a fixed order:
+// partial[blk * d + k] over row blocks, then shift[k] = total / (n + m).
+cudaError_t launch_shift(const float* X, int64_t n, const float* Y, int64_t m, int d,
+                         double* partial, int nblk_max, float* shift, cudaStream_t s);
+
+// FMA path: centre, pack, norms and log2-weights of one side.  If `pot` is
+// non-null the bias slot is filled from it: bias = (pot - |p~|^2) L/eps + log2 w.
+cudaError_t launch_pack_fma(const float* P, const float* w, const float* pot, int64_t rows, int d,
+                            int D, const float* shift, float l_over_eps, float* packed,
+                            float* norm, float* logw2, cudaStream_t s);
+
+// phi_i = (f_i - |x~_i|^2) L/eps (apply).
+cudaError_t launch_phi(const float* f, const float* norm, int64_t n, float l_over_eps, float* phi,
+                       cudaStream_t s);
+
+// Count NaN/Inf in v (atomic counter, integer).
+cudaError_t launch_count_nonfinite(const float* v, int64_t len, unsigned int* counter,
+                                   cudaStream_t s);
+
+}  // namespace fs

@@ -1,0 +1,135 @@
+"""The C-ABI library loads, exports every symbol include/*.h declares, and
+rejects bad arguments on the host before touching the GPU (no compute calls
+here: these run without a GPU)."""
+import ctypes
+import glob
+import os
+import re
+
+import numpy as np
+import pytest
+
+from streaming_sinkhorn_solver_gb300 import binding as fs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for mname in re.finditer(r"\b(fs_[a-z0-9_]+)\s*\(", text):
+            names.add(mname.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from streaming_sinkhorn_solver_gb300.build import build
+    build()
+    return fs.load_library()
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("fs_sinkhorn_solve", "fs_apply_plan", "fs_grad_x", "fs_barycentric",
+                     "fs_last_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+    assert set(_declared_functions()) <= set(fs.EXPORTED)
+
+
+def test_version_and_launch_counter(lib):
+    assert re.match(r"^\d+\.\d+\.\d+$", fs.fs_version())
+    assert fs.fs_launch_count() >= 0
+
+
+def _small():
+    X = np.zeros((4, 2), np.float32)
+    Y = np.zeros((5, 2), np.float32)
+    a = np.full(4, 0.25, np.float32)
+    b = np.full(5, 0.2, np.float32)
+    return X, a, Y, b
+
+
+@pytest.mark.parametrize("bad", ["eps0", "epsnan", "iters0", "path", "reserved", "splits"])
+def test_invalid_arguments_rejected_on_host(lib, bad):
+    X, a, Y, b = _small()
+    f = np.zeros(4, np.float32)
+    g = np.zeros(5, np.float32)
+    opt = fs.fs_options()
+    eps, iters = 0.1, 3
+    if bad == "eps0":
+        eps = 0.0
+    elif bad == "epsnan":
+        eps = float("nan")
+    elif bad == "iters0":
+        iters = 0
+    elif bad == "path":
+        opt.path = 7
+    elif bad == "reserved":
+        opt.reserved[2] = 1
+    elif bad == "splits":
+        opt.splits = -1
+    st = lib.fs_sinkhorn_solve(X.ctypes.data, a.ctypes.data, 4, Y.ctypes.data, b.ctypes.data, 5, 2,
+                               eps, iters, f.ctypes.data, g.ctypes.data, ctypes.byref(opt), None)
+    assert st == fs.FS_ERR_INVALID_ARG
+    assert fs.fs_last_error()
+
+
+def test_bad_sizes_and_null_pointers(lib):
+    X, a, Y, b = _small()
+    f = np.zeros(4, np.float32)
+    g = np.zeros(5, np.float32)
+    for n, m, d in [(0, 5, 2), (4, 0, 2), (4, 5, 0), (4, 5, 5000)]:
+        st = lib.fs_sinkhorn_solve(X.ctypes.data, a.ctypes.data, n, Y.ctypes.data, b.ctypes.data,
+                                   m, d, 0.1, 1, f.ctypes.data, g.ctypes.data, None, None)
+        assert st == fs.FS_ERR_INVALID_ARG
+    st = lib.fs_sinkhorn_solve(None, a.ctypes.data, 4, Y.ctypes.data, b.ctypes.data, 5, 2, 0.1, 1,
+                               f.ctypes.data, g.ctypes.data, None, None)
+    assert st == fs.FS_ERR_INVALID_ARG
+    out = np.zeros((4, 3), np.float32)
+    V = np.zeros((5, 3), np.float32)
+    st = lib.fs_apply_plan(X.ctypes.data, a.ctypes.data, 4, Y.ctypes.data, b.ctypes.data, 5, 2,
+                           0.1, f.ctypes.data, g.ctypes.data, V.ctypes.data, 0, out.ctypes.data,
+                           None, None)
+    assert st == fs.FS_ERR_INVALID_ARG
+
+
+def test_fma_path_rejects_large_d(lib):
+    X = np.zeros((4, 17), np.float32)
+    Y = np.zeros((5, 17), np.float32)
+    a = np.full(4, 0.25, np.float32)
+    b = np.full(5, 0.2, np.float32)
+    with pytest.raises(fs.FlashSinkhornError) as ei:
+        fs.fs_sinkhorn_solve(X, a, Y, b, 0.1, 1, path="fma")
+    assert ei.value.status == fs.FS_ERR_UNSUPPORTED
+
+
+def test_binding_rejects_wrong_dtype_and_layout(lib):
+    X, a, Y, b = _small()
+    with pytest.raises(TypeError):
+        fs.fs_sinkhorn_solve(X.astype(np.float64), a, Y, b, 0.1, 1)
+    with pytest.raises(TypeError):
+        fs.fs_sinkhorn_solve(np.asfortranarray(np.zeros((4, 3), np.float32)), a,
+                             np.zeros((5, 3), np.float32), b, 0.1, 1)
+    with pytest.raises(ValueError):
+        fs.fs_sinkhorn_solve(X, a[:3], Y, b, 0.1, 1)
+
+
+def test_workspace_is_linear_in_sizes(lib):
+    w1 = fs.fs_workspace_bytes(10_000, 10_000, 3)
+    w2 = fs.fs_workspace_bytes(20_000, 20_000, 3)
+    assert 0 < w1 < w2 < 3 * w1
+    # no n x m buffer: far below n*m*4 bytes at 50k
+    assert fs.fs_workspace_bytes(50_000, 50_000, 3) < 50_000 * 50_000 * 4 // 100
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(ImportError):
+        fs.load_library(str(tmp_path / "nope.so"))
