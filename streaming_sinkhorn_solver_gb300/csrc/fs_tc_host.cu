@@ -1,17 +1,199 @@
-// Host orchestration of the tcgen05 tensor-core path (placeholder until the
-// kernels land).
+// Host orchestration of the tcgen05 tensor-core path (d > 16): buffer
+// layout, preparation, the alternating half-update loop, plan application.
 #include "fs_host.cuh"
+#include "fs_tc_kernels.cuh"
+
+#include <algorithm>
 
 namespace fs {
 
-int64_t workspace_bytes_tc(int64_t, int64_t, int32_t, int32_t, int, const fs_options*) { return -1; }
+namespace {
 
-fs_status solve_tc(Call&, Problem&, int32_t, const fs_options*) {
-    return fail(FS_ERR_UNSUPPORTED, "tensor-core path not built");
+using namespace tc;
+
+struct TcPlan {
+    int nch;
+    bool qres;
+    int64_t rtx, rty;           // row tiles of X and Y
+    int splits_f, splits_g;
+    int tps_f, tps_g;           // column tiles per split
+};
+
+// Pick the split count that best fills whole waves of one CTA per SM.
+void choose_tc_splits(int64_t row_tiles, int64_t col_tiles, int sms, const fs_options* opt,
+                      int* splits, int* tps) {
+    if (opt && opt->splits > 0) {
+        int64_t sp = std::min<int64_t>(opt->splits, col_tiles);
+        sp = std::min<int64_t>(sp, 65535);
+        const int64_t t = (col_tiles + sp - 1) / sp;
+        *tps = (int)t;
+        *splits = (int)((col_tiles + t - 1) / t);
+        return;
+    }
+    double best = -1.0;
+    int best_sp = 1, best_tps = (int)col_tiles;
+    const int64_t max_sp = std::min<int64_t>(col_tiles, 64);
+    for (int64_t sp = 1; sp <= max_sp; ++sp) {
+        const int64_t t = (col_tiles + sp - 1) / sp;
+        const int64_t spe = (col_tiles + t - 1) / t;
+        const int64_t ctas = row_tiles * spe;
+        const int64_t waves = (ctas + sms - 1) / sms;
+        const double eff = (double)(row_tiles * col_tiles) / (double)(waves * sms * t);
+        if (eff > best + 0.01) {
+            best = eff;
+            best_sp = (int)spe;
+            best_tps = (int)t;
+        }
+    }
+    *splits = best_sp;
+    *tps = best_tps;
+}
+
+TcPlan plan_tc(int64_t n, int64_t m, int32_t d, int sms, const fs_options* opt) {
+    TcPlan p;
+    p.nch = (d + BK - 1) / BK;
+    p.qres = p.nch <= kMaxResidentChunks;
+    p.rtx = (n + BM - 1) / BM;
+    p.rty = (m + BM - 1) / BM;
+    choose_tc_splits(p.rtx, p.rty, sms, opt, &p.splits_f, &p.tps_f);
+    choose_tc_splits(p.rty, p.rtx, sms, opt, &p.splits_g, &p.tps_g);
+    return p;
+}
+
+struct TcBufs {
+    size_t shift_part, shift, nx, ny, lax, lby, absmax, params, X16, Y16, alpha, beta, partial;
+};
+
+void layout_tc(Layout& L, TcBufs& B, int64_t n, int64_t m, int32_t d, const TcPlan& p) {
+    B.shift_part = L.take(sizeof(double) * (size_t)kShiftBlocks * d);
+    B.shift = L.take(sizeof(float) * d);
+    B.nx = L.take(sizeof(float) * n);
+    B.ny = L.take(sizeof(float) * m);
+    B.lax = L.take(sizeof(float) * n);
+    B.lby = L.take(sizeof(float) * m);
+    B.absmax = L.take(sizeof(unsigned int) * 2);
+    B.params = L.take(sizeof(float) * 4);
+    B.X16 = L.take((size_t)p.rtx * p.nch * CHUNK_BYTES);
+    B.Y16 = L.take((size_t)p.rty * p.nch * CHUNK_BYTES);
+    B.alpha = L.take(sizeof(float) * (size_t)p.rtx * BM);
+    B.beta = L.take(sizeof(float) * (size_t)p.rty * BM);
+    const int64_t part = std::max((int64_t)n * p.splits_f, (int64_t)m * p.splits_g);
+    B.partial = L.take(sizeof(float2) * (size_t)part);
+}
+
+// centring, norms, log-weights, fp16 tiles of both clouds; beta from g
+fs_status prep_tc(Call& c, Problem& P, const TcPlan& p, const TcBufs& B, bool beta_from_g) {
+    const int64_t n = P.n, m = P.m;
+    const int32_t d = P.d;
+    const double eps = (double)P.eps;
+    const float l_over_eps = (float)(kLog2e / eps);
+    const float kappa = (float)(2.0 * kLog2e / eps);
+    float* shift = c.at<float>(B.shift);
+    unsigned int* absmax = c.at<unsigned int>(B.absmax);
+    float* params = c.at<float>(B.params);
+    FS_CUDA(launch_shift(P.X.dev, n, P.Y.dev, m, d, c.at<double>(B.shift_part), kShiftBlocks, shift,
+                         c.stream));
+    FS_CUDA(cudaMemsetAsync(absmax, 0, 2 * sizeof(unsigned int), c.stream));
+    FS_CUDA(launch_prep_side(P.X.dev, P.a.dev, n, d, shift, c.at<float>(B.nx), c.at<float>(B.lax),
+                             absmax, c.stream));
+    FS_CUDA(launch_prep_side(P.Y.dev, P.b.dev, m, d, shift, c.at<float>(B.ny), c.at<float>(B.lby),
+                             absmax + 1, c.stream));
+    FS_CUDA(launch_scales(absmax, kappa, params, c.stream));
+    FS_CUDA(launch_to_tiles(P.X.dev, n, d, shift, params + 0, p.nch, p.rtx, c.at<void>(B.X16),
+                            c.stream));
+    FS_CUDA(launch_to_tiles(P.Y.dev, m, d, shift, params + 1, p.nch, p.rty, c.at<void>(B.Y16),
+                            c.stream));
+    FS_CUDA(launch_bias_init(beta_from_g ? P.g.dev : nullptr, c.at<float>(B.ny), c.at<float>(B.lby),
+                             l_over_eps, m, p.rty * BM, c.at<float>(B.beta), c.stream));
+    FS_CUDA(launch_bias_init(nullptr, c.at<float>(B.nx), c.at<float>(B.lax), l_over_eps, n,
+                             p.rtx * BM, c.at<float>(B.alpha), c.stream));
+    return FS_OK;
+}
+
+}  // namespace
+
+int64_t workspace_bytes_tc(int64_t n, int64_t m, int32_t d, int32_t k, int sms,
+                           const fs_options* opt) {
+    (void)k;
+    const TcPlan p = plan_tc(n, m, d, sms, opt);
+    Layout L;
+    TcBufs B;
+    layout_tc(L, B, n, m, d, p);
+    return (int64_t)L.off;
+}
+
+fs_status solve_tc(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) {
+    const int64_t n = P.n, m = P.m;
+    const int32_t d = P.d;
+    const TcPlan p = plan_tc(n, m, d, c.ws->sms, opt);
+    TcBufs B;
+    layout_tc(c.L, B, n, m, d, p);
+    FS_TRY(ensure_capacity(c));
+    for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g}) bind(c, *A);
+    for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.g}) FS_TRY(upload(c, *A));
+    FS_TRY(prep_tc(c, P, p, B, true));
+
+    const float eps_ln2 = (float)((double)P.eps * kLn2);
+    float2* part = c.at<float2>(B.partial);
+    TcHalfArgs hf{};
+    hf.Q = c.at<void>(B.X16);
+    hf.K = c.at<void>(B.Y16);
+    hf.cbias = c.at<float>(B.beta);
+    hf.kscale = c.at<float>(B.params) + 2;
+    hf.nr = n;
+    hf.nc = m;
+    hf.nch = p.nch;
+    hf.col_tiles = (int)p.rty;
+    hf.tiles_per_split = p.tps_f;
+    hf.splits = p.splits_f;
+    hf.eps_ln2 = eps_ln2;
+    hf.rnorm = c.at<float>(B.nx);
+    hf.rlogw2 = c.at<float>(B.lax);
+    hf.pot = P.f.dev;
+    hf.rbias = c.at<float>(B.alpha);
+    hf.partial = part;
+    hf.err = c.ws->err_word;
+
+    TcHalfArgs hg = hf;
+    hg.Q = c.at<void>(B.Y16);
+    hg.K = c.at<void>(B.X16);
+    hg.cbias = c.at<float>(B.alpha);
+    hg.nr = m;
+    hg.nc = n;
+    hg.col_tiles = (int)p.rtx;
+    hg.tiles_per_split = p.tps_g;
+    hg.splits = p.splits_g;
+    hg.rnorm = c.at<float>(B.ny);
+    hg.rlogw2 = c.at<float>(B.lby);
+    hg.pot = P.g.dev;
+    hg.rbias = c.at<float>(B.beta);
+
+    for (int32_t it = 0; it < n_iter; ++it) {
+        int ts = timing_begin(c.stream);
+        FS_CUDA(launch_half_tc(hf, (int)p.rtx, p.qres, c.stream));
+        timing_end(ts, TIME_HALF, c.stream);
+        if (p.splits_f > 1)
+            FS_CUDA(launch_merge_lse(part, p.splits_f, n, hf.rnorm, hf.rlogw2, eps_ln2, P.f.dev,
+                                     hf.rbias, 1, c.stream));
+        ts = timing_begin(c.stream);
+        FS_CUDA(launch_half_tc(hg, (int)p.rty, p.qres, c.stream));
+        timing_end(ts, TIME_HALF, c.stream);
+        if (p.splits_g > 1)
+            FS_CUDA(launch_merge_lse(part, p.splits_g, m, hg.rnorm, hg.rlogw2, eps_ln2, P.g.dev,
+                                     hg.rbias, 1, c.stream));
+    }
+    if (opt && opt->check_finite) {
+        unsigned int* counter = c.at<unsigned int>(B.absmax);
+        FS_TRY(scan_finite(c, P.f.dev, n, counter));
+        FS_TRY(scan_finite(c, P.g.dev, m, counter));
+    }
+    FS_TRY(download(c, P.f));
+    FS_TRY(download(c, P.g));
+    return FS_OK;
 }
 
 fs_status apply_tc(Call&, Problem&, int, const fs_options*) {
-    return fail(FS_ERR_UNSUPPORTED, "tensor-core path not built");
+    return fail(FS_ERR_UNSUPPORTED, "tensor-core plan application not built yet");
 }
 
 }  // namespace fs

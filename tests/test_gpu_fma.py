@@ -140,7 +140,9 @@ def test_column_marginal_after_g_update_via_transposed_apply():
     f, g = fs.fs_sinkhorn_solve(t["X"], t["a"], t["Y"], t["b"], 0.05, 25)
     ones = t["X"].new_ones((1500, 1))
     col = fs.fs_apply_plan(t["Y"], t["b"], t["X"], t["a"], 0.05, g, f, ones)
-    np.testing.assert_allclose(np64(col)[:, 0], inp["b"].astype(np.float64), rtol=2e-5)
+    # base-2 scores reach |s| ~ 600 here; float32 rounds them to ~4e-5 (relative
+    # error of each plan entry), and the row scale 2^{phi + M} adds as much again
+    np.testing.assert_allclose(np64(col)[:, 0], inp["b"].astype(np.float64), rtol=2e-4)
 
 
 def test_translation_invariance_far_shift():
