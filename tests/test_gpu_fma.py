@@ -161,12 +161,17 @@ def test_translation_invariance_far_shift():
 
 
 def test_warm_start_equals_longer_run():
+    """10 + 10 warm-started iterations equal 20 in one call, up to the float32
+    rounding of the bias rebuilt from g at the restart (|beta| <~ 600 here,
+    so ~4e-5 in base-2 score units, i.e. ~1e-6 in f)."""
     inp = random_cloud(900, 800, 2, seed=74)
     t = to_dev(inp)
     f1, g1 = fs.fs_sinkhorn_solve(t["X"], t["a"], t["Y"], t["b"], 0.05, 20)
     f2, g2 = fs.fs_sinkhorn_solve(t["X"], t["a"], t["Y"], t["b"], 0.05, 10)
     f2, g2 = fs.fs_sinkhorn_solve(t["X"], t["a"], t["Y"], t["b"], 0.05, 10, f2, g2)
-    assert np.array_equal(np64(f1), np64(f2)) and np.array_equal(np64(g1), np64(g2))
+    cmax = orc.cost(inp["X"], inp["Y"]).max()
+    assert max_abs(np64(f1), np64(f2)) <= 1e-5 * cmax
+    assert max_abs(np64(g1), np64(g2)) <= 1e-5 * cmax
 
 
 def test_nonfinite_check_reports():
