@@ -148,6 +148,10 @@ __global__ void k_merge_lse(const float2* __restrict__ partial, int splits, int6
         S += p.y * ex2(p.x - M);
     }
     const float lse2 = M + log2f(S);
+    if (rnorm == nullptr) {  // log2-sum-exp only (pre-pass of plan application)
+        pot[i] = lse2;
+        return;
+    }
     pot[i] = rnorm[i] - eps_ln2 * lse2;
     bias[i * bias_stride] = rlogw2[i] - lse2;
 }

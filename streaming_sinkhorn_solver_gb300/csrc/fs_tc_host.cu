@@ -110,15 +110,36 @@ fs_status prep_tc(Call& c, Problem& P, const TcPlan& p, const TcBufs& B, bool be
     return FS_OK;
 }
 
+struct TcApplyBufs {
+    size_t lse2, phi, VT, vabs, vparams, partial;
+    int splits, tps, kpad;
+};
+
+void layout_apply(Layout& L, TcApplyBufs& A, const TcPlan& p, int64_t n, int32_t k, int sms,
+                  const fs_options* opt) {
+    A.kpad = (k + 15) / 16 * 16;
+    const int64_t nkv = (A.kpad + kApplyKV - 1) / kApplyKV;
+    choose_tc_splits(p.rtx * nkv, p.rty, sms, opt, &A.splits, &A.tps);
+    A.lse2 = L.take(sizeof(float) * n);
+    A.phi = L.take(sizeof(float) * n);
+    A.VT = L.take((size_t)p.rty * 2 * A.kpad * 128);
+    A.vabs = L.take(sizeof(unsigned int) * 2);
+    A.vparams = L.take(sizeof(float) * 2);
+    A.partial = A.splits > 1 ? L.take(sizeof(float) * (size_t)A.splits * n * k) : 0;
+}
+
 }  // namespace
 
 int64_t workspace_bytes_tc(int64_t n, int64_t m, int32_t d, int32_t k, int sms,
                            const fs_options* opt) {
-    (void)k;
     const TcPlan p = plan_tc(n, m, d, sms, opt);
     Layout L;
     TcBufs B;
     layout_tc(L, B, n, m, d, p);
+    if (k > 0) {
+        TcApplyBufs A;
+        layout_apply(L, A, p, n, k, sms, opt);
+    }
     return (int64_t)L.off;
 }
 
@@ -192,8 +213,97 @@ fs_status solve_tc(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) {
     return FS_OK;
 }
 
-fs_status apply_tc(Call&, Problem&, int, const fs_options*) {
-    return fail(FS_ERR_UNSUPPORTED, "tensor-core plan application not built yet");
+fs_status apply_tc(Call& c, Problem& P, int mode, const fs_options* opt) {
+    const int64_t n = P.n, m = P.m;
+    const int32_t d = P.d, k = P.k;
+    const TcPlan p = plan_tc(n, m, d, c.ws->sms, opt);
+    TcBufs B;
+    layout_tc(c.L, B, n, m, d, p);
+    TcApplyBufs A;
+    layout_apply(c.L, A, p, n, k, c.ws->sms, opt);
+    FS_TRY(ensure_capacity(c));
+    for (Arr* X : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g, &P.V, &P.out}) bind(c, *X);
+    for (Arr* X : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g, &P.V}) FS_TRY(upload(c, *X));
+    FS_TRY(prep_tc(c, P, p, B, true));
+
+    const double eps = (double)P.eps;
+    const float l_over_eps = (float)(kLog2e / eps);
+    float* lse2 = c.at<float>(A.lse2);
+    float* phi = c.at<float>(A.phi);
+    FS_CUDA(launch_phi(P.f.dev, c.at<float>(B.nx), n, l_over_eps, phi, c.stream));
+
+    // pass 1: exact row log2-sum-exp of the scores built from g
+    TcHalfArgs h{};
+    h.Q = c.at<void>(B.X16);
+    h.K = c.at<void>(B.Y16);
+    h.cbias = c.at<float>(B.beta);
+    h.kscale = c.at<float>(B.params) + 2;
+    h.nr = n;
+    h.nc = m;
+    h.nch = p.nch;
+    h.col_tiles = (int)p.rty;
+    h.tiles_per_split = p.tps_f;
+    h.splits = p.splits_f;
+    h.eps_ln2 = (float)(eps * kLn2);
+    h.rnorm = nullptr;
+    h.pot = lse2;
+    h.partial = c.at<float2>(B.partial);
+    h.err = c.ws->err_word;
+    FS_CUDA(launch_half_tc(h, (int)p.rtx, p.qres, c.stream));
+    if (p.splits_f > 1)
+        FS_CUDA(launch_merge_lse(h.partial, p.splits_f, n, nullptr, nullptr, 0.f, lse2, nullptr, 1,
+                                 c.stream));
+
+    // values: transposed fp16 tiles with a power-of-two scale
+    unsigned int* vabs = c.at<unsigned int>(A.vabs);
+    float* vparams = c.at<float>(A.vparams);
+    float* shift = c.at<float>(B.shift);
+    if (mode == APPLY_PV) {
+        FS_CUDA(cudaMemsetAsync(vabs, 0, sizeof(unsigned int), c.stream));
+        FS_CUDA(launch_absmax(P.V.dev, m * (int64_t)k, vabs, c.stream));
+        FS_CUDA(launch_value_scale(vabs, vparams, c.stream));
+        FS_CUDA(launch_vt_tiles(P.V.dev, m, k, A.kpad, nullptr, vparams, p.rty, c.at<void>(A.VT),
+                                c.stream));
+    } else {
+        // V = Y: centred coordinates, whose max |.| the preparation already found
+        FS_CUDA(launch_value_scale(c.at<unsigned int>(B.absmax) + 1, vparams, c.stream));
+        FS_CUDA(launch_vt_tiles(P.Y.dev, m, d, A.kpad, shift, vparams, p.rty, c.at<void>(A.VT),
+                                c.stream));
+    }
+
+    // pass 2: O = sum_j p_ij V_j on the tensor cores
+    TcApplyArgs ap{};
+    ap.Q = h.Q;
+    ap.K = h.K;
+    ap.VT = c.at<void>(A.VT);
+    ap.cbias = h.cbias;
+    ap.kscale = h.kscale;
+    ap.lse2 = lse2;
+    ap.phi = phi;
+    ap.vinv = vparams + 1;
+    ap.shift = shift;
+    ap.a = P.a.dev;
+    ap.X = P.X.dev;
+    ap.nr = n;
+    ap.nc = m;
+    ap.nch = p.nch;
+    ap.col_tiles = (int)p.rty;
+    ap.tiles_per_split = A.tps;
+    ap.splits = A.splits;
+    ap.k = k;
+    ap.kpad = A.kpad;
+    ap.mode = mode;
+    ap.out = P.out.dev;
+    ap.partial = A.splits > 1 ? c.at<float>(A.partial) : nullptr;
+    ap.err = c.ws->err_word;
+    const int ts = timing_begin(c.stream);
+    FS_CUDA(launch_apply_tc(ap, (int)p.rtx, c.stream));
+    timing_end(ts, TIME_APPLY, c.stream);
+    if (A.splits > 1) FS_CUDA(launch_merge_apply_tc(ap, c.stream));
+    if (opt && opt->check_finite)
+        FS_TRY(scan_finite(c, P.out.dev, n * (int64_t)k, c.at<unsigned int>(A.vabs) + 1));
+    FS_TRY(download(c, P.out));
+    return FS_OK;
 }
 
 }  // namespace fs

@@ -53,5 +53,48 @@ cudaError_t launch_bias_init(const float* pot, const float* norm, const float* l
 size_t half_smem_bytes(int nch, bool qres);
 cudaError_t launch_half_tc(const TcHalfArgs& a, int row_tiles, bool qres, cudaStream_t s);
 
+// ---------------------------------------------------------------------------
+// Plan application.  Values V (m x k) are stored transposed per column tile:
+// tile j holds, for each of its two 64-point halves kq, kpad rows (one per
+// output column n) of 64 fp16 values in the K-major 128-byte-swizzled order,
+// i.e. byte ((j*2 + kq)*kpad + n)*128 + swizzled offset of point p.
+constexpr int kApplyStages = 3;         // (K chunk, Q chunk) pairs in flight
+constexpr int kApplyKV = 128;           // output columns per CTA (TMEM columns of O)
+constexpr int kApplyThreads = kHalfThreads;
+constexpr int kApplyTmemCols = 512;     // 2 score buffers + O, rounded to a power of two
+
+struct TcApplyArgs {
+    const void* Q;          // row-side tiles
+    const void* K;          // column-side tiles
+    const void* VT;         // transposed value tiles
+    const float* cbias;     // beta built from g, padding -inf
+    const float* kscale;    // device scalar: kappa 2^-(ex+ey)
+    const float* lse2;      // log2 sum_j 2^{s_ij} per row (pre-pass)
+    const float* phi;       // (f_i - |x~_i|^2) L/eps per row
+    const float* vinv;      // device scalar: 1 / (power-of-two scale of V)
+    const float* shift;     // centring shift (barycentric / gradient modes)
+    const float* a;         // row weights
+    const float* X;         // raw rows (gradient mode), n x d
+    int64_t nr, nc;
+    int nch, col_tiles, tiles_per_split, splits;
+    int k, kpad;
+    int mode;               // APPLY_PV / APPLY_BARY / APPLY_GRAD
+    float* out;             // n x k
+    float* partial;         // splits x n x k unscaled sums when splits > 1
+    uint32_t* err;
+};
+
+size_t apply_smem_bytes();
+cudaError_t launch_apply_tc(const TcApplyArgs& a, int row_tiles, cudaStream_t s);
+cudaError_t launch_merge_apply_tc(const TcApplyArgs& a, cudaStream_t s);
+// transposed value tiles from V (m x k, row-major); shift subtracted if given
+cudaError_t launch_vt_tiles(const float* V, int64_t m, int k, int kpad, const float* shift,
+                            const float* scale_ptr, int64_t col_tiles, void* out,
+                            cudaStream_t s);
+// max |V| as ordered float bits (atomicMax)
+cudaError_t launch_absmax(const float* V, int64_t len, unsigned int* bits, cudaStream_t s);
+// params[0] = 2^e with max|V| 2^e in [2^14, 2^15), params[1] = 2^-e
+cudaError_t launch_value_scale(const unsigned int* bits, float* params, cudaStream_t s);
+
 }  // namespace tc
 }  // namespace fs

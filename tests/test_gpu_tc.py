@@ -108,3 +108,89 @@ def test_tensor_path_host_buffers():
     fh, gh = fs.fs_sinkhorn_solve(inp["X"], inp["a"], inp["Y"], inp["b"], 0.05, 5, path="tensor")
     np.testing.assert_array_equal(fd, fh.astype(np.float64))
     np.testing.assert_array_equal(gd, gh.astype(np.float64))
+
+
+# --- plan application on the tensor path ------------------------------------
+
+def _potentials(inp, eps, iters):
+    C = orc.cost(inp["X"], inp["Y"])
+    fr, gr = orc.sinkhorn(C, inp["a"], inp["b"], eps, iters)
+    return C, fr.astype(np.float32), gr.astype(np.float32)
+
+
+@pytest.mark.parametrize("n,m,d,k", [(300, 400, 64, 1), (257, 383, 64, 16), (129, 700, 32, 17),
+                                     (400, 300, 100, 64), (200, 260, 512, 130),
+                                     (150, 170, 600, 300), (140, 129, 1024, 64)])
+def test_apply_plan_tensor_matches_oracle(n, m, d, k):
+    inp = random_cloud(n, m, d, seed=300 + k + d, spread=1.0 / np.sqrt(d), weights="lognormal")
+    C = orc.cost(inp["X"], inp["Y"])
+    eps = 0.05 * C.max()
+    _, f32, g32 = _potentials(inp, eps, 5)
+    V = np.random.default_rng(k).standard_normal((m, k)).astype(np.float32)
+    t = to_dev(dict(inp, V=V, f=f32, g=g32))
+    out = fs.fs_apply_plan(t["X"], t["a"], t["Y"], t["b"], eps, t["f"], t["g"], t["V"], path="tensor")
+    ref = orc.apply_plan(C, inp["a"], inp["b"], eps, f32, g32, V)
+    assert rel_l2(np64(out), ref) <= APPLY_TOL
+
+
+@pytest.mark.parametrize("d", [64, 512])
+def test_grad_and_barycentric_tensor_match_oracle(d):
+    inp = make_inputs("c4_n50k_d512", n=900, m=1000, d=d)
+    C, f32, g32 = _potentials(inp, 0.05, 30)
+    t = to_dev(dict(inp, f=f32, g=g32))
+    grad = fs.fs_grad_x(t["X"], t["a"], t["Y"], t["b"], 0.05, t["f"], t["g"], path="tensor")
+    ref = orc.grad_x(C, inp["X"], inp["a"], inp["b"], 0.05, f32, g32, inp["Y"])
+    assert rel_l2(np64(grad), ref) <= APPLY_TOL
+    T = fs.fs_barycentric(t["X"], t["a"], t["Y"], t["b"], 0.05, t["f"], t["g"], path="tensor")
+    Tr = orc.barycentric(C, inp["a"], inp["b"], 0.05, f32, g32, inp["Y"])
+    assert rel_l2(np64(T), Tr) <= APPLY_TOL
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_apply_forced_splits(splits):
+    inp = random_cloud(500, 650, 64, seed=13, spread=0.125, weights="lognormal")
+    C, f32, g32 = _potentials(inp, 0.1, 10)
+    V = np.random.default_rng(2).standard_normal((650, 40)).astype(np.float32)
+    t = to_dev(dict(inp, V=V, f=f32, g=g32))
+    out = fs.fs_apply_plan(t["X"], t["a"], t["Y"], t["b"], 0.1, t["f"], t["g"], t["V"],
+                           path="tensor", splits=splits)
+    ref = orc.apply_plan(C, inp["a"], inp["b"], 0.1, f32, g32, V)
+    assert rel_l2(np64(out), ref) <= APPLY_TOL
+
+
+def test_column_marginal_tensor_path():
+    """After a tensor-path solve, the last half-update (the g-update) makes
+    the column sums equal b; the transposed apply measures them on the GPU."""
+    inp = make_inputs("c3_n50k_d64", n=3000, m=2700)
+    t = to_dev(inp)
+    f, g = fs.fs_sinkhorn_solve(t["X"], t["a"], t["Y"], t["b"], 0.1, 30, path="tensor")
+    ones = t["X"].new_ones((3000, 1))
+    col = fs.fs_apply_plan(t["Y"], t["b"], t["X"], t["a"], 0.1, g, f, ones, path="tensor")
+    # fp16 plan entries (relative 2^-11 each) averaged over many rows
+    assert rel_l2(np64(col)[:, 0], inp["b"]) <= APPLY_TOL
+
+
+@pytest.mark.parametrize("name", ["c4_n50k_d512", "c5_n20k_m30k_d1024"])
+def test_full_size_plan_application_on_sampled_rows(name):
+    """Full-size workload: potentials from the oracle on 24 sampled rows (g = 0,
+    f = the oracle's f-update there), the workload's plan operator on the GPU,
+    compared with the oracle's point-by-point application on those rows."""
+    w = WORKLOADS[name]
+    inp = make_inputs(name)
+    eps = w.stages[-1][0]
+    rows = np.random.default_rng(3).choice(w.n, 24, replace=False)
+    rows[:2] = [0, w.n - 1]
+    g = np.zeros(w.m)
+    fr = orc.f_update_rows(inp["X"], inp["Y"], inp["b"], eps, g, rows)
+    f = np.zeros(w.n, np.float32)
+    f[rows] = fr.astype(np.float32)
+    V = inp["V"] if w.apply == "pv" else inp["Y"]
+    t = to_dev(dict(inp, f=f, g=g.astype(np.float32)))
+    if w.apply == "pv":
+        out = fs.fs_apply_plan(t["X"], t["a"], t["Y"], t["b"], eps, t["f"], t["g"], t["V"])
+        ref = orc.apply_plan_rows(inp["X"], inp["a"], inp["Y"], inp["b"], eps, f, g, V, rows)
+    else:
+        out = fs.fs_grad_x(t["X"], t["a"], t["Y"], t["b"], eps, t["f"], t["g"])
+        PY = orc.apply_plan_rows(inp["X"], inp["a"], inp["Y"], inp["b"], eps, f, g, V, rows)
+        ref = 2.0 * (inp["a"][rows, None].astype(np.float64) * inp["X"][rows] - PY)
+    assert rel_l2(np64(out)[rows], ref) <= APPLY_TOL
