@@ -70,10 +70,13 @@ __global__ void k_scales(const unsigned int* __restrict__ absmax_bits, float kap
     params[2] = ldexpf(kappa, -(ex + ey));
 }
 
-// One thread per 16-byte unit (8 fp16) of the tiled, swizzled operand.
+// One thread per 16-byte unit (8 fp16) of the tiled, swizzled operand.  If
+// `out_lo` is given it receives the rounding remainder fp16(v - fp16(v)), so
+// that hi + lo carries about 22 significant bits.
 __global__ void k_to_tiles(const float* __restrict__ P, int64_t rows, int d,
                            const float* __restrict__ shift, const float* __restrict__ scale_ptr,
-                           int nch, int64_t row_tiles, uint4* __restrict__ out) {
+                           int nch, int64_t row_tiles, uint4* __restrict__ out,
+                           uint4* __restrict__ out_lo) {
     const int64_t unit = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t units = row_tiles * BM * nch * 8;
     if (unit >= units) return;
@@ -87,15 +90,20 @@ __global__ void k_to_tiles(const float* __restrict__ P, int64_t rows, int d,
     const float scale = *scale_ptr;
     const int k0 = chunk * BK + u * 8;
     __align__(16) __half h[8];
+    __align__(16) __half l[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
         const int k = k0 + q;
         float v = 0.f;
         if (row < rows && k < d) v = (P[row * d + k] - shift[k]) * scale;
         h[q] = __float2half_rn(v);
+        l[q] = __float2half_rn(v - __half2float(h[q]));
     }
-    char* base = reinterpret_cast<char*>(out) + ((tile * nch + chunk) * (int64_t)CHUNK_BYTES);
-    *reinterpret_cast<uint4*>(base + swz_offset(r, u * 8)) = *reinterpret_cast<const uint4*>(h);
+    const int64_t off = (tile * nch + chunk) * (int64_t)CHUNK_BYTES + swz_offset(r, u * 8);
+    *reinterpret_cast<uint4*>(reinterpret_cast<char*>(out) + off) = *reinterpret_cast<const uint4*>(h);
+    if (out_lo != nullptr)
+        *reinterpret_cast<uint4*>(reinterpret_cast<char*>(out_lo) + off) =
+            *reinterpret_cast<const uint4*>(l);
 }
 
 // bias[j] = (pot_j - norm_j) L/eps + logw2_j for j < rows, -inf for padding;
@@ -128,10 +136,11 @@ cudaError_t launch_scales(const unsigned int* absmax_bits, float kappa, float* p
 
 cudaError_t launch_to_tiles(const float* P, int64_t rows, int d, const float* shift,
                             const float* scale_ptr, int nch, int64_t row_tiles, void* out,
-                            cudaStream_t s) {
+                            void* out_lo, cudaStream_t s) {
     const int64_t units = row_tiles * BM * nch * 8;
     k_to_tiles<<<(unsigned)((units + 255) / 256), 256, 0, s>>>(P, rows, d, shift, scale_ptr, nch,
-                                                               row_tiles, (uint4*)out);
+                                                               row_tiles, (uint4*)out,
+                                                               (uint4*)out_lo);
     count_launch();
     return cudaGetLastError();
 }

@@ -98,14 +98,16 @@ cudaError_t launch_vt_tiles(const float* V, int64_t m, int k, int kpad, const fl
 }
 
 // ---------------------------------------------------------------------------
-// output of one row: o = sum_j p_ij V_j (already unscaled)
+// output of one row from o = sum_j p_ij V~_j (already unscaled) and
+// sigma = sum_j p_ij (the same rounded p the tensor core summed).  For V = Y
+// the values are centred, y = y~ + t, so sum_j p_ij y_j = o + t sigma.
 
 __device__ __forceinline__ float apply_out(const TcApplyArgs& a, int64_t row, int col, float W,
-                                           float o) {
+                                           float o, float sigma) {
     if (a.mode == APPLY_PV) return a.a[row] * W * o;
-    const float t = o + a.shift[col];              // centred values + shift = raw values
-    if (a.mode == APPLY_BARY) return W * t;
-    return 2.f * a.a[row] * (a.X[row * (int64_t)a.k + col] - W * t);
+    const float py = o + a.shift[col] * sigma;     // sum_j p_ij y_j
+    if (a.mode == APPLY_BARY) return W * py;
+    return 2.f * a.a[row] * (a.X[row * (int64_t)a.k + col] - W * py);
 }
 
 __global__ void k_merge_apply_tc(TcApplyArgs a) {
@@ -113,10 +115,15 @@ __global__ void k_merge_apply_tc(TcApplyArgs a) {
     if (idx >= a.nr * (int64_t)a.k) return;
     const int64_t row = idx / a.k;
     const int col = (int)(idx - row * a.k);
-    float o = 0.f;
-    for (int sp = 0; sp < a.splits; ++sp) o += a.partial[(int64_t)sp * a.nr * a.k + idx];
+    const int64_t stride = a.nr * (int64_t)(a.k + 1);
+    const int64_t base = row * (a.k + 1);
+    float o = 0.f, sigma = 0.f;
+    for (int sp = 0; sp < a.splits; ++sp) {
+        o += a.partial[sp * stride + base + col];
+        sigma += a.partial[sp * stride + base + a.k];
+    }
     const float W = exp2f(a.phi[row] + a.lse2[row]);
-    a.out[idx] = apply_out(a, row, col, W, o);
+    a.out[idx] = apply_out(a, row, col, W, o, sigma);
 }
 
 cudaError_t launch_merge_apply_tc(const TcApplyArgs& a, cudaStream_t s) {
@@ -135,7 +142,7 @@ cudaError_t launch_merge_apply_tc(const TcApplyArgs& a, cudaStream_t s) {
 // warps 2-5: epilogue, one thread per row
 
 namespace {
-constexpr int kStageA = 2 * CHUNK_BYTES;          // K chunk, then Q chunk
+constexpr int kStageA = 4 * CHUNK_BYTES;          // K hi, K lo, Q hi, Q lo
 constexpr int kVtSlot = kApplyKV * 2 * 128;       // 2 halves x 128 rows x 128 B
 constexpr int kOCol = 2 * BN;                     // TMEM column of the O accumulator
 }  // namespace
@@ -194,23 +201,30 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
 
     if (warp == 0) {
         if (lane == 0) {
-            const char* Qg = reinterpret_cast<const char*>(a.Q) + rt * nch * (int64_t)CHUNK_BYTES;
+            const int64_t qoff = rt * nch * (int64_t)CHUNK_BYTES;
+            const char* Qg = reinterpret_cast<const char*>(a.Q) + qoff;
+            const char* Qlg = reinterpret_cast<const char*>(a.Qlo) + qoff;
             const char* VTg = reinterpret_cast<const char*>(a.VT);
             int s = 0, issued = 0, vissued = 0;
             uint32_t ph = 0;
             bool ok = true;
             for (int t = 0; t < ntiles && ok; ++t) {
                 const int64_t j = j0 + t;
-                const char* Kg = reinterpret_cast<const char*>(a.K) + j * nch * (int64_t)CHUNK_BYTES;
+                const int64_t koff = j * nch * (int64_t)CHUNK_BYTES;
+                const char* Kg = reinterpret_cast<const char*>(a.K) + koff;
+                const char* Klg = reinterpret_cast<const char*>(a.Klo) + koff;
                 for (int c = 0; c < nch; ++c) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, a.err, ERR_TIMEOUT_PRODUCER)) {
                         ok = false;
                         break;
                     }
                     uint8_t* st = sStage + s * kStageA;
+                    const int64_t co = c * (int64_t)CHUNK_BYTES;
                     mbar_arrive_expect_tx(&full[s], kStageA);
-                    bulk_g2s(st, Kg + c * (int64_t)CHUNK_BYTES, CHUNK_BYTES, &full[s]);
-                    bulk_g2s(st + CHUNK_BYTES, Qg + c * (int64_t)CHUNK_BYTES, CHUNK_BYTES, &full[s]);
+                    bulk_g2s(st, Kg + co, CHUNK_BYTES, &full[s]);
+                    bulk_g2s(st + CHUNK_BYTES, Klg + co, CHUNK_BYTES, &full[s]);
+                    bulk_g2s(st + 2 * CHUNK_BYTES, Qg + co, CHUNK_BYTES, &full[s]);
+                    bulk_g2s(st + 3 * CHUNK_BYTES, Qlg + co, CHUNK_BYTES, &full[s]);
                     ++issued;
                     if (++s == kApplyStages) {
                         s = 0;
@@ -263,12 +277,15 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
                     if (!mbar_wait(&full[s], ph, a.err, ERR_TIMEOUT_MMA)) return false;
                     tc_fence_after();
                     const uint8_t* st = sStage + s * kStageA;
-                    const uint32_t aaddr = smem_u32(st + CHUNK_BYTES);
-                    const uint32_t baddr = smem_u32(st);
+                    const uint32_t kh = smem_u32(st), kl = kh + CHUNK_BYTES;
+                    const uint32_t qh = kh + 2 * CHUNK_BYTES, ql = kh + 3 * CHUNK_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        mma_f16(d_tmem, sdesc_sw128(aaddr + kk * 32), sdesc_sw128(baddr + kk * 32),
-                                idescS, (c | kk) != 0);
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint32_t o = kk * 32;
+                        mma_f16(d_tmem, sdesc_sw128(qh + o), sdesc_sw128(kh + o), idescS, (c | kk) != 0);
+                        mma_f16(d_tmem, sdesc_sw128(qh + o), sdesc_sw128(kl + o), idescS, 1);
+                        mma_f16(d_tmem, sdesc_sw128(ql + o), sdesc_sw128(kh + o), idescS, 1);
+                    }
                     mma_commit(&empty[s]);
                     if (++s == kApplyStages) {
                         s = 0;
@@ -312,6 +329,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
         const float ks = *a.kscale;
         const float L = a.lse2[rowc];
         const uint32_t lofs = (uint32_t)(quarter * 32) << 16;
+        float sigma = 0.f;
         bool ok = true;
         for (int t = 0; t < ntiles; ++t) {
             const int b = t & 1;
@@ -349,8 +367,11 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
                 p[7] = ex2(fmaf(w[7], ks, b1.w) - L);
                 __align__(16) __half2 h[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
+                for (int q = 0; q < 4; ++q) {
                     h[q] = live ? __floats2half2_rn(p[2 * q], p[2 * q + 1]) : __floats2half2_rn(0.f, 0.f);
+                    const float2 r = __half22float2(h[q]);
+                    sigma += r.x + r.y;
+                }
                 const int kq = u16 >> 3, u = u16 & 7;
                 *reinterpret_cast<uint4*>(sP + kq * CHUNK_BYTES + swz_offset(rloc, u * 8)) =
                     *reinterpret_cast<const uint4*>(h);
@@ -363,6 +384,10 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
             tc_fence_after();
             const float vinv = *a.vinv;
             const float W = exp2f(a.phi[rowc] + L);
+            float* prow = a.splits > 1
+                              ? a.partial + ((int64_t)blockIdx.z * a.nr + row) * (a.k + 1)
+                              : nullptr;
+            if (live && a.splits > 1 && blockIdx.y == 0) prow[a.k] = sigma;
             for (int q = 0; q < (kvN + 31) / 32; ++q) {
                 float o[32];
                 tmem_ld32(tmem + kOCol + lofs + q * 32, o);
@@ -373,9 +398,9 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
                     if (q * 32 + cc >= kvN || col >= a.k) break;
                     const float ov = o[cc] * vinv;
                     if (a.splits > 1)
-                        a.partial[((int64_t)blockIdx.z * a.nr + row) * a.k + col] = ov;
+                        prow[col] = ov;
                     else
-                        a.out[row * (int64_t)a.k + col] = apply_out(a, row, col, W, ov);
+                        a.out[row * (int64_t)a.k + col] = apply_out(a, row, col, W, ov, sigma);
                 }
             }
         }

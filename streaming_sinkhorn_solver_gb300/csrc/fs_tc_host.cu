@@ -82,7 +82,9 @@ void layout_tc(Layout& L, TcBufs& B, int64_t n, int64_t m, int32_t d, const TcPl
 }
 
 // centring, norms, log-weights, fp16 tiles of both clouds; beta from g
-fs_status prep_tc(Call& c, Problem& P, const TcPlan& p, const TcBufs& B, bool beta_from_g) {
+// (xlo, ylo: optional fp16 rounding remainders of the tiles, for split precision)
+fs_status prep_tc(Call& c, Problem& P, const TcPlan& p, const TcBufs& B, bool beta_from_g,
+                  void* xlo = nullptr, void* ylo = nullptr) {
     const int64_t n = P.n, m = P.m;
     const int32_t d = P.d;
     const double eps = (double)P.eps;
@@ -100,9 +102,9 @@ fs_status prep_tc(Call& c, Problem& P, const TcPlan& p, const TcBufs& B, bool be
                              absmax + 1, c.stream));
     FS_CUDA(launch_scales(absmax, kappa, params, c.stream));
     FS_CUDA(launch_to_tiles(P.X.dev, n, d, shift, params + 0, p.nch, p.rtx, c.at<void>(B.X16),
-                            c.stream));
+                            xlo, c.stream));
     FS_CUDA(launch_to_tiles(P.Y.dev, m, d, shift, params + 1, p.nch, p.rty, c.at<void>(B.Y16),
-                            c.stream));
+                            ylo, c.stream));
     FS_CUDA(launch_bias_init(beta_from_g ? P.g.dev : nullptr, c.at<float>(B.ny), c.at<float>(B.lby),
                              l_over_eps, m, p.rty * BM, c.at<float>(B.beta), c.stream));
     FS_CUDA(launch_bias_init(nullptr, c.at<float>(B.nx), c.at<float>(B.lax), l_over_eps, n,
@@ -111,7 +113,7 @@ fs_status prep_tc(Call& c, Problem& P, const TcPlan& p, const TcBufs& B, bool be
 }
 
 struct TcApplyBufs {
-    size_t lse2, phi, VT, vabs, vparams, partial;
+    size_t lse2, phi, VT, vabs, vparams, partial, Xlo, Ylo;
     int splits, tps, kpad;
 };
 
@@ -125,7 +127,9 @@ void layout_apply(Layout& L, TcApplyBufs& A, const TcPlan& p, int64_t n, int32_t
     A.VT = L.take((size_t)p.rty * 2 * A.kpad * 128);
     A.vabs = L.take(sizeof(unsigned int) * 2);
     A.vparams = L.take(sizeof(float) * 2);
-    A.partial = A.splits > 1 ? L.take(sizeof(float) * (size_t)A.splits * n * k) : 0;
+    A.partial = A.splits > 1 ? L.take(sizeof(float) * (size_t)A.splits * n * (k + 1)) : 0;
+    A.Xlo = L.take((size_t)p.rtx * p.nch * CHUNK_BYTES);
+    A.Ylo = L.take((size_t)p.rty * p.nch * CHUNK_BYTES);
 }
 
 }  // namespace
@@ -224,7 +228,7 @@ fs_status apply_tc(Call& c, Problem& P, int mode, const fs_options* opt) {
     FS_TRY(ensure_capacity(c));
     for (Arr* X : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g, &P.V, &P.out}) bind(c, *X);
     for (Arr* X : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g, &P.V}) FS_TRY(upload(c, *X));
-    FS_TRY(prep_tc(c, P, p, B, true));
+    FS_TRY(prep_tc(c, P, p, B, true, c.at<void>(A.Xlo), c.at<void>(A.Ylo)));
 
     const double eps = (double)P.eps;
     const float l_over_eps = (float)(kLog2e / eps);
@@ -275,6 +279,8 @@ fs_status apply_tc(Call& c, Problem& P, int mode, const fs_options* opt) {
     TcApplyArgs ap{};
     ap.Q = h.Q;
     ap.K = h.K;
+    ap.Qlo = c.at<void>(A.Xlo);
+    ap.Klo = c.at<void>(A.Ylo);
     ap.VT = c.at<void>(A.VT);
     ap.cbias = h.cbias;
     ap.kscale = h.kscale;

@@ -46,7 +46,7 @@ cudaError_t launch_scales(const unsigned int* absmax_bits, float kappa, float* p
                           cudaStream_t s);
 cudaError_t launch_to_tiles(const float* P, int64_t rows, int d, const float* shift,
                             const float* scale_ptr, int nch, int64_t row_tiles, void* out,
-                            cudaStream_t s);
+                            void* out_lo, cudaStream_t s);
 cudaError_t launch_bias_init(const float* pot, const float* norm, const float* logw2,
                              float l_over_eps, int64_t rows, int64_t rows_pad, float* bias,
                              cudaStream_t s);
@@ -58,14 +58,19 @@ cudaError_t launch_half_tc(const TcHalfArgs& a, int row_tiles, bool qres, cudaSt
 // tile j holds, for each of its two 64-point halves kq, kpad rows (one per
 // output column n) of 64 fp16 values in the K-major 128-byte-swizzled order,
 // i.e. byte ((j*2 + kq)*kpad + n)*128 + swizzled offset of point p.
-constexpr int kApplyStages = 3;         // (K chunk, Q chunk) pairs in flight
+constexpr int kApplyStages = 2;         // (K hi, K lo, Q hi, Q lo) chunk sets in flight
 constexpr int kApplyKV = 128;           // output columns per CTA (TMEM columns of O)
 constexpr int kApplyThreads = kHalfThreads;
 constexpr int kApplyTmemCols = 512;     // 2 score buffers + O, rounded to a power of two
 
+// Scores are formed in split precision, S = Qh Kh^T + Qh Kl^T + Ql Kh^T with
+// hi = fp16(v) and lo = fp16(v - hi): an error near 2^-22 instead of 2^-11,
+// because a plan entry carries the score's absolute error as a relative one.
 struct TcApplyArgs {
-    const void* Q;          // row-side tiles
-    const void* K;          // column-side tiles
+    const void* Q;          // row-side tiles (hi part)
+    const void* K;          // column-side tiles (hi part)
+    const void* Qlo;        // row-side remainders
+    const void* Klo;        // column-side remainders
     const void* VT;         // transposed value tiles
     const float* cbias;     // beta built from g, padding -inf
     const float* kscale;    // device scalar: kappa 2^-(ex+ey)
@@ -80,7 +85,7 @@ struct TcApplyArgs {
     int k, kpad;
     int mode;               // APPLY_PV / APPLY_BARY / APPLY_GRAD
     float* out;             // n x k
-    float* partial;         // splits x n x k unscaled sums when splits > 1
+    float* partial;         // splits x n x (k+1): unscaled sums, then sum_j p_ij
     uint32_t* err;
 };
 
