@@ -1,0 +1,318 @@
+// Fused half-update on the tcgen05 tensor cores (d > 16).
+//
+// "FlashSinkhorn: IO-Aware Entropic Optimal Transport on GPU", Method 1
+// (Proposition 1: the f-update is a row LSE of the biased dot-product score
+// matrix (Q K^T + bias)/eps) and Method 2 (streaming kernels and tiling: the
+// n x m matrix never reaches HBM; a Q row block stays on chip while every K
+// block streams past; running row max and sum-exp on chip; score, bias, LSE
+// and potential write-back fused in one pass).
+//
+// One CTA owns a 128-row tile of Q and a range of 128-column tiles of K.
+//   warp 0     producer: Q once (resident in shared memory up to d = 512,
+//              otherwise streamed beside K), then for every column tile its
+//              512-byte bias slice and its K chunks (128 x 64 fp16, 16 KB,
+//              pre-swizzled in HBM) into a ring sized to the free space, all
+//              with cp.async.bulk;
+//   warp 1     one thread issues tcgen05.mma (M = 128, N = 128, K = 16 steps)
+//              into TMEM buffer t mod 4;
+//   warps 2-9  two epilogue groups of four warps, tile t going to group
+//              t mod 2; a thread owns one row: it reads its 128 scores from
+//              TMEM, forms s = acc kappa' + bias (packed f32x2 FMA), and
+//              folds them into the row's running max M and sum S of 2^{s-M}.
+// At the end the two groups' (M, S) are merged in a fixed order and the row
+// potential and next bias are written (or (M, S) partials per split).
+#include "fs_tc.cuh"
+
+namespace fs {
+namespace tc {
+
+namespace {
+
+constexpr int kBiasBytes = BN * 4;
+
+__host__ __device__ constexpr int half_fixed_bytes(int nch, bool qres) {
+    return 1024 /* alignment slack */ + (qres ? nch * CHUNK_BYTES : 0) + kTmemBufs * kBiasBytes +
+           BM * 8 /* group merge */ + 8 * (2 * kMaxStages + 4 * kTmemBufs + 2) + 16;
+}
+
+__device__ __forceinline__ void epi_bar_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kHalfGroups * kEpiWarps * 32) : "memory");
+}
+
+}  // namespace
+
+int half_stages(int nch, bool qres) {
+    const int stage = qres ? CHUNK_BYTES : 2 * CHUNK_BYTES;
+    const int s = (kSmemLimit - half_fixed_bytes(nch, qres)) / stage;
+    return s < kMaxStages ? s : kMaxStages;
+}
+
+size_t half_smem_bytes(int nch, bool qres, int stages) {
+    const size_t stage = qres ? CHUNK_BYTES : 2 * CHUNK_BYTES;
+    return (size_t)half_fixed_bytes(nch, qres) + (size_t)stages * stage;
+}
+
+template <bool QRES>
+__global__ void __launch_bounds__(kHalfThreads, 1) k_half_tc(TcHalfArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t rt = blockIdx.x;
+    const int j0 = blockIdx.y * a.tiles_per_split;
+    const int j1 = min(a.col_tiles, j0 + a.tiles_per_split);
+    const int ntiles = j1 - j0;
+    const int nch = a.nch;
+    const int stages = a.stages;
+
+    constexpr int STAGE_BYTES = QRES ? CHUNK_BYTES : 2 * CHUNK_BYTES;
+    uint8_t* sQ = smem;
+    uint8_t* sStage = smem + (QRES ? nch * CHUNK_BYTES : 0);
+    uint8_t* sBias = sStage + stages * STAGE_BYTES;
+    float2* sMerge = reinterpret_cast<float2*>(sBias + kTmemBufs * kBiasBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sMerge + BM);
+    uint64_t* empty = full + kMaxStages;
+    uint64_t* tfull = empty + kMaxStages;
+    uint64_t* tempty = tfull + kTmemBufs;
+    uint64_t* bfull = tempty + kTmemBufs;
+    uint64_t* bempty = bfull + kTmemBufs;
+    uint64_t* qfull = bempty + kTmemBufs;
+    uint64_t* drain = qfull + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < kTmemBufs; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], kEpiWarps);
+            mbar_init(&bfull[b], 1);
+            mbar_init(&bempty[b], kEpiWarps);
+        }
+        mbar_init(qfull, 1);
+        mbar_init(drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            const char* Qg = reinterpret_cast<const char*>(a.Q) + rt * nch * (int64_t)CHUNK_BYTES;
+            if (QRES) {
+                mbar_arrive_expect_tx(qfull, (uint32_t)(nch * CHUNK_BYTES));
+                for (int c = 0; c < nch; ++c)
+                    bulk_g2s(sQ + c * CHUNK_BYTES, Qg + c * (int64_t)CHUNK_BYTES, CHUNK_BYTES, qfull);
+            }
+            int s = 0, issued = 0, bissued = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int t = 0; t < ntiles && ok; ++t) {
+                const int b = t & (kTmemBufs - 1);
+                if (!mbar_wait(&bempty[b], (uint32_t)((t >> 2) & 1) ^ 1u, a.err, ERR_TIMEOUT_PRODUCER)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&bfull[b], kBiasBytes);
+                bulk_g2s(sBias + b * kBiasBytes, a.cbias + (int64_t)(j0 + t) * BN, kBiasBytes, &bfull[b]);
+                ++bissued;
+                const char* Kg =
+                    reinterpret_cast<const char*>(a.K) + (int64_t)(j0 + t) * nch * CHUNK_BYTES;
+                for (int c = 0; c < nch; ++c) {
+                    if (!mbar_wait(&empty[s], ph ^ 1u, a.err, ERR_TIMEOUT_PRODUCER)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = sStage + s * STAGE_BYTES;
+                    mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+                    bulk_g2s(st, Kg + c * (int64_t)CHUNK_BYTES, CHUNK_BYTES, &full[s]);
+                    if (!QRES)
+                        bulk_g2s(st + CHUNK_BYTES, Qg + c * (int64_t)CHUNK_BYTES, CHUNK_BYTES,
+                                 &full[s]);
+                    ++issued;
+                    if (++s == stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // let every copy already issued land before the CTA can exit
+                int s2 = 0;
+                uint32_t ph2 = 0;
+                const int skip = issued > stages ? issued - stages : 0;
+                for (int i = 0; i < issued; ++i) {
+                    if (i >= skip) mbar_wait(&full[s2], ph2, a.err, ERR_TIMEOUT_PRODUCER);
+                    if (++s2 == stages) {
+                        s2 = 0;
+                        ph2 ^= 1u;
+                    }
+                }
+                for (int i = bissued > kTmemBufs ? bissued - kTmemBufs : 0; i < bissued; ++i)
+                    mbar_wait(&bfull[i & (kTmemBufs - 1)], (uint32_t)((i >> 2) & 1), a.err,
+                              ERR_TIMEOUT_PRODUCER);
+                if (QRES) mbar_wait(qfull, 0, a.err, ERR_TIMEOUT_PRODUCER);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
+            bool ok = true;
+            if (QRES) ok = mbar_wait(qfull, 0, a.err, ERR_TIMEOUT_MMA);
+            tc_fence_after();
+            int s = 0;
+            uint32_t ph = 0;
+            for (int t = 0; t < ntiles && ok; ++t) {
+                const int b = t & (kTmemBufs - 1);
+                if (!mbar_wait(&tempty[b], (uint32_t)((t >> 2) & 1) ^ 1u, a.err, ERR_TIMEOUT_MMA)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + (uint32_t)(b * BN);
+                for (int c = 0; c < nch; ++c) {
+                    if (!mbar_wait(&full[s], ph, a.err, ERR_TIMEOUT_MMA)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t* st = sStage + s * STAGE_BYTES;
+                    const uint32_t aaddr = smem_u32(QRES ? sQ + c * CHUNK_BYTES : st + CHUNK_BYTES);
+                    const uint32_t baddr = smem_u32(st);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_f16(d_tmem, sdesc_sw128(aaddr + kk * 32), sdesc_sw128(baddr + kk * 32),
+                                idesc, (c | kk) != 0);
+                    mma_commit(&empty[s]);
+                    if (++s == stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&tfull[b]);
+            }
+            // every MMA issued has completed once `drain` fires
+            mma_commit(drain);
+            mbar_wait(drain, 0, a.err, ERR_TIMEOUT_MMA);
+        }
+    } else {
+        // ---------------- epilogue groups: one thread per row ----------------
+        const int grp = (warp - 2) / kEpiWarps;
+        const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
+        const int rloc = quarter * 32 + lane;
+        const int64_t row = rt * BM + rloc;
+        const float ks = *a.kscale;
+        const uint64_t ks2 = pk(ks, ks);
+        const uint32_t lofs = (uint32_t)(quarter * 32) << 16;
+        float M = -INFINITY, S = 0.f;
+        for (int t = grp; t < ntiles; t += kHalfGroups) {
+            const int b = t & (kTmemBufs - 1);
+            const uint32_t ph = (uint32_t)((t >> 2) & 1);
+            if (!mbar_wait(&tfull[b], ph, a.err, ERR_TIMEOUT_EPILOGUE)) break;
+            tc_fence_after();
+            float v[BN];
+#pragma unroll
+            for (int q = 0; q < BN / 32; ++q) tmem_ld32(tmem + (uint32_t)(b * BN) + lofs + q * 32, v + q * 32);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[b]);
+            if (!mbar_wait(&bfull[b], ph, a.err, ERR_TIMEOUT_EPILOGUE)) break;
+
+            // s = acc kappa' + bias, row max (two chains)
+            const float4* sb = reinterpret_cast<const float4*>(sBias + b * kBiasBytes);
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < BN / 4; ++q) {
+                const float4 bb = sb[q];
+                upk(fma2(pk(v[4 * q], v[4 * q + 1]), ks2, pk(bb.x, bb.y)), v[4 * q], v[4 * q + 1]);
+                upk(fma2(pk(v[4 * q + 2], v[4 * q + 3]), ks2, pk(bb.z, bb.w)), v[4 * q + 2],
+                    v[4 * q + 3]);
+                mx0 = max3(mx0, v[4 * q], v[4 * q + 1]);
+                mx1 = max3(mx1, v[4 * q + 2], v[4 * q + 3]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bempty[b]);
+            const float mx = fmaxf(mx0, mx1);
+            if (mx > M) {
+                S *= ex2(M - mx);
+                M = mx;
+            }
+            // S += sum 2^{s - M}
+            const uint64_t nm = pk(-M, -M);
+            uint64_t acc0 = pk(0.f, 0.f), acc1 = pk(0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < BN / 4; ++q) {
+                float x0, x1, x2, x3;
+                upk(add2(pk(v[4 * q], v[4 * q + 1]), nm), x0, x1);
+                upk(add2(pk(v[4 * q + 2], v[4 * q + 3]), nm), x2, x3);
+                acc0 = add2(acc0, pk(ex2(x0), ex2(x1)));
+                acc1 = add2(acc1, pk(ex2(x2), ex2(x3)));
+            }
+            float s0, s1, s2, s3;
+            upk(acc0, s0, s1);
+            upk(acc1, s2, s3);
+            S += (s0 + s1) + (s2 + s3);
+        }
+
+        // merge the groups in a fixed order: group 0 absorbs group 1
+        if (grp == 1) sMerge[rloc] = make_float2(M, S);
+        epi_bar_sync();
+        if (grp == 0) {
+            const float2 o = sMerge[rloc];
+            const float Mt = fmaxf(M, o.x);
+            const float St = S * ex2(M - Mt) + o.y * ex2(o.x - Mt);
+            if (row < a.nr) {
+                if (a.splits > 1) {
+                    a.partial[(int64_t)blockIdx.y * a.nr + row] = make_float2(Mt, St);
+                } else {
+                    const float lse2 = Mt + log2f(St);
+                    if (a.rnorm != nullptr) {
+                        a.pot[row] = a.rnorm[row] - a.eps_ln2 * lse2;
+                        a.rbias[row] = a.rlogw2[row] - lse2;
+                    } else {
+                        a.pot[row] = lse2;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+cudaError_t launch_half_tc(const TcHalfArgs& a, int row_tiles, bool qres, cudaStream_t s) {
+    const size_t smem = half_smem_bytes(a.nch, qres, a.stages);
+    dim3 grid((unsigned)row_tiles, (unsigned)a.splits);
+    cudaError_t e;
+    if (qres) {
+        e = cudaFuncSetAttribute(k_half_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        k_half_tc<true><<<grid, kHalfThreads, smem, s>>>(a);
+    } else {
+        e = cudaFuncSetAttribute(k_half_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        k_half_tc<false><<<grid, kHalfThreads, smem, s>>>(a);
+    }
+    count_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace tc
+}  // namespace fs

@@ -171,6 +171,7 @@ fs_status solve_tc(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) {
     hf.col_tiles = (int)p.rty;
     hf.tiles_per_split = p.tps_f;
     hf.splits = p.splits_f;
+    hf.stages = half_stages(p.nch, p.qres);
     hf.eps_ln2 = eps_ln2;
     hf.rnorm = c.at<float>(B.nx);
     hf.rlogw2 = c.at<float>(B.lax);
@@ -248,6 +249,7 @@ fs_status apply_tc(Call& c, Problem& P, int mode, const fs_options* opt) {
     h.col_tiles = (int)p.rty;
     h.tiles_per_split = p.tps_f;
     h.splits = p.splits_f;
+    h.stages = half_stages(p.nch, p.qres);
     h.eps_ln2 = (float)(eps * kLn2);
     h.rnorm = nullptr;
     h.pot = lse2;

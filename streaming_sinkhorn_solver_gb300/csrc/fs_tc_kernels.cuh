@@ -10,11 +10,14 @@ constexpr int BM = 128;                 // rows of a tile (TMEM lanes)
 constexpr int BK = 64;                  // fp16 elements per 128-byte swizzled row
 constexpr int CHUNK_BYTES = BM * BK * 2;  // one 128 x 64 fp16 chunk = 16 KB
 constexpr int BN = 128;                 // columns of a score tile (TMEM columns per buffer)
-constexpr int kStages = 4;              // shared-memory ring depth (chunks)
-constexpr int kTmemBufs = 2;            // score tiles in flight in TMEM
-constexpr int kEpiWarps = 4;            // epilogue warps (one thread per tile row)
-constexpr int kHalfThreads = 32 * (2 + kEpiWarps);
+constexpr int kEpiWarps = 4;            // warps of one epilogue group (one thread per tile row)
+// half-update kernel
+constexpr int kHalfGroups = 2;          // epilogue groups, alternating score tiles
+constexpr int kTmemBufs = 4;            // score tiles in flight in TMEM (tile t -> t mod 4)
+constexpr int kHalfThreads = 32 * (2 + kHalfGroups * kEpiWarps);
 constexpr int kTmemCols = kTmemBufs * BN;
+constexpr int kMaxStages = 8;           // shared-memory ring depth is set by the free space
+constexpr int kSmemLimit = 232448;      // dynamic shared memory per block on sm_103
 constexpr int kMaxResidentChunks = 8;   // Q stays in shared memory up to d = 512
 
 // Operand tiles: a cloud of `rows` points becomes ceil(rows/128) tiles of
@@ -30,6 +33,7 @@ struct TcHalfArgs {
     int col_tiles;
     int tiles_per_split;
     int splits;
+    int stages;             // ring depth (from half_stages)
     float eps_ln2;
     const float* rnorm;     // |x~|^2 of the rows; nullptr = write log2-sum-exp only
     const float* rlogw2;    // log2 of the row weights
@@ -50,7 +54,8 @@ cudaError_t launch_to_tiles(const float* P, int64_t rows, int d, const float* sh
 cudaError_t launch_bias_init(const float* pot, const float* norm, const float* logw2,
                              float l_over_eps, int64_t rows, int64_t rows_pad, float* bias,
                              cudaStream_t s);
-size_t half_smem_bytes(int nch, bool qres);
+int half_stages(int nch, bool qres);    // deepest ring that fits next to resident Q
+size_t half_smem_bytes(int nch, bool qres, int stages);
 cudaError_t launch_half_tc(const TcHalfArgs& a, int row_tiles, bool qres, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
@@ -60,7 +65,7 @@ cudaError_t launch_half_tc(const TcHalfArgs& a, int row_tiles, bool qres, cudaSt
 // i.e. byte ((j*2 + kq)*kpad + n)*128 + swizzled offset of point p.
 constexpr int kApplyStages = 2;         // (K hi, K lo, Q hi, Q lo) chunk sets in flight
 constexpr int kApplyKV = 128;           // output columns per CTA (TMEM columns of O)
-constexpr int kApplyThreads = kHalfThreads;
+constexpr int kApplyThreads = 32 * (2 + kEpiWarps);   // producer, MMA, one epilogue group
 constexpr int kApplyTmemCols = 512;     // 2 score buffers + O, rounded to a power of two
 
 // Scores are formed in split precision, S = Qh Kh^T + Qh Kl^T + Ql Kh^T with
