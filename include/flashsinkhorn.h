@@ -161,6 +161,34 @@ fs_status fs_grad_x(const float* X, const float* a, int64_t n,
                     float eps, const float* f, const float* g, float* out,
                     const fs_options* opt, void* stream);
 
+/*
+ * fs_sinkhorn_solve_noalloc -- the same iterations as fs_sinkhorn_solve on the
+ * FP32-FMA path, for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart: this entry point exists for callers that
+ * must not call cudaMalloc (a process whose device memory is budgeted by
+ * someone else, a latency-critical loop where an allocation or the device
+ * synchronisation of a cudaFree is not allowed).  All scratch comes from one
+ * static array of about 10 MB inside the library's device image, present on
+ * every device that loads the library until the process exits; nothing is
+ * allocated, ever.
+ *
+ *   Arguments as fs_sinkhorn_solve, except: every pointer must be device
+ *   memory of the current device; 1 <= d <= 16; 1 <= n, m <= 32768; no
+ *   options.  Sizes beyond these limits return FS_ERR_INVALID_ARG with a
+ *   message naming the limit.
+ *   The first call on a device looks the scratch array's address up
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   Calls share the one scratch array: calls whose GPU work overlaps (other
+ *   streams, other threads) race and produce wrong results; calls on one
+ *   stream are ordered and safe.  No scratch state carries from one call to
+ *   the next.
+ */
+fs_status fs_sinkhorn_solve_noalloc(const float* X, const float* a, int64_t n,
+                                    const float* Y, const float* b, int64_t m, int32_t d,
+                                    float eps, int32_t n_iter, float* f, float* g,
+                                    void* stream);
+
 /* Device bytes the library's workspace needs for these sizes (k = 0 for a
  * solve).  The workspace is O((n + m) d): no n x m buffer exists. */
 int64_t fs_workspace_bytes(int64_t n, int64_t m, int32_t d, int32_t k, const fs_options* opt);

@@ -30,7 +30,8 @@ PATHS = {"auto": 0, "fma": 1, "tensor": 2}
 
 EXPORTED = ("fs_sinkhorn_solve", "fs_apply_plan", "fs_barycentric", "fs_grad_x",
             "fs_workspace_bytes", "fs_check", "fs_release", "fs_last_error", "fs_version",
-            "fs_launch_count", "fs_timing_enable", "fs_timing_read")
+            "fs_launch_count", "fs_timing_enable", "fs_timing_read",
+            "fs_sinkhorn_solve_noalloc")
 
 
 class FlashSinkhornError(RuntimeError):
@@ -79,6 +80,8 @@ def load_library(path: Optional[str] = None):
         lib.fs_timing_enable.restype = ctypes.c_int
         lib.fs_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]
         lib.fs_timing_read.restype = ctypes.c_int
+        lib.fs_sinkhorn_solve_noalloc.argtypes = [vp, vp, i64, vp, vp, i64, i32, f32, i32, vp, vp, vp]
+        lib.fs_sinkhorn_solve_noalloc.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -273,3 +276,16 @@ def fs_timing_read():
     cnt = (ctypes.c_int64 * 2)()
     _raise(load_library().fs_timing_read(ms, cnt))
     return (ms[0], ms[1]), (int(cnt[0]), int(cnt[1]))
+
+
+def fs_sinkhorn_solve_noalloc(X, a, Y, b, eps: float, n_iter: int, f, g, *, stream=None):
+    """The FMA-path solve with no device allocation (see the C header for
+    who needs it and its limits).  Every array must be a CUDA tensor; f and g
+    are in/out as in fs_sinkhorn_solve.  Returns (f, g)."""
+    n, d = X.shape
+    m = Y.shape[0]
+    st = load_library().fs_sinkhorn_solve_noalloc(
+        _ptr(X, "X", (n, d)), _ptr(a, "a", (n,)), n, _ptr(Y, "Y", (m, d)), _ptr(b, "b", (m,)), m, d,
+        float(eps), int(n_iter), _ptr(f, "f", (n,)), _ptr(g, "g", (m,)), _stream(stream, X))
+    _raise(st)
+    return f, g
