@@ -53,10 +53,13 @@ TcPlan plan_tc(int64_t n, int64_t m, int32_t d, int sms, const fs_options* opt) 
     TcPlan p;
     p.nch = (d + BK - 1) / BK;
     p.qres = p.nch <= kMaxResidentChunks;
-    p.rtx = (n + BM - 1) / BM;
-    p.rty = (m + BM - 1) / BM;
-    choose_tc_splits(p.rtx, p.rty, sms, opt, &p.splits_f, &p.tps_f);
-    choose_tc_splits(p.rty, p.rtx, sms, opt, &p.splits_g, &p.tps_g);
+    // tile counts are even: the solve runs on CTA pairs (two 128-row tiles of
+    // the updated side, 256-column tiles of the other); padding rows are zero
+    // and padding biases -inf
+    p.rtx = (n + 2 * BM - 1) / (2 * BM) * 2;
+    p.rty = (m + 2 * BM - 1) / (2 * BM) * 2;
+    choose_tc_splits(p.rtx, p.rty / 2, sms, opt, &p.splits_f, &p.tps_f);
+    choose_tc_splits(p.rty, p.rtx / 2, sms, opt, &p.splits_g, &p.tps_g);
     return p;
 }
 
@@ -113,8 +116,9 @@ fs_status prep_tc(Call& c, Problem& P, const TcPlan& p, const TcBufs& B, bool be
 }
 
 struct TcApplyBufs {
-    size_t lse2, phi, VT, vabs, vparams, partial, Xlo, Ylo;
+    size_t lse2, phi, VT, vabs, vparams, partial, Xlo, Ylo, lse_partial;
     int splits, tps, kpad;
+    int lse_splits, lse_tps;    // the log2-sum-exp pre-pass (one-CTA kernel, 128-column tiles)
 };
 
 void layout_apply(Layout& L, TcApplyBufs& A, const TcPlan& p, int64_t n, int32_t k, int sms,
@@ -130,6 +134,8 @@ void layout_apply(Layout& L, TcApplyBufs& A, const TcPlan& p, int64_t n, int32_t
     A.partial = A.splits > 1 ? L.take(sizeof(float) * (size_t)A.splits * n * (k + 1)) : 0;
     A.Xlo = L.take((size_t)p.rtx * p.nch * CHUNK_BYTES);
     A.Ylo = L.take((size_t)p.rty * p.nch * CHUNK_BYTES);
+    choose_tc_splits(p.rtx, p.rty, sms, opt, &A.lse_splits, &A.lse_tps);
+    A.lse_partial = L.take(sizeof(float2) * (size_t)n * A.lse_splits);
 }
 
 }  // namespace
@@ -168,10 +174,10 @@ fs_status solve_tc(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) {
     hf.nr = n;
     hf.nc = m;
     hf.nch = p.nch;
-    hf.col_tiles = (int)p.rty;
+    hf.col_tiles = (int)(p.rty / 2);
     hf.tiles_per_split = p.tps_f;
     hf.splits = p.splits_f;
-    hf.stages = half_stages(p.nch, p.qres);
+    hf.stages = pair_stages(p.nch, p.qres);
     hf.eps_ln2 = eps_ln2;
     hf.rnorm = c.at<float>(B.nx);
     hf.rlogw2 = c.at<float>(B.lax);
@@ -186,7 +192,7 @@ fs_status solve_tc(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) {
     hg.cbias = c.at<float>(B.alpha);
     hg.nr = m;
     hg.nc = n;
-    hg.col_tiles = (int)p.rtx;
+    hg.col_tiles = (int)(p.rtx / 2);
     hg.tiles_per_split = p.tps_g;
     hg.splits = p.splits_g;
     hg.rnorm = c.at<float>(B.ny);
@@ -196,13 +202,13 @@ fs_status solve_tc(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) {
 
     for (int32_t it = 0; it < n_iter; ++it) {
         int ts = timing_begin(c.stream);
-        FS_CUDA(launch_half_tc(hf, (int)p.rtx, p.qres, c.stream));
+        FS_CUDA(launch_half_pair(hf, (int)p.rtx, p.qres, c.stream));
         timing_end(ts, TIME_HALF, c.stream);
         if (p.splits_f > 1)
             FS_CUDA(launch_merge_lse(part, p.splits_f, n, hf.rnorm, hf.rlogw2, eps_ln2, P.f.dev,
                                      hf.rbias, 1, c.stream));
         ts = timing_begin(c.stream);
-        FS_CUDA(launch_half_tc(hg, (int)p.rty, p.qres, c.stream));
+        FS_CUDA(launch_half_pair(hg, (int)p.rty, p.qres, c.stream));
         timing_end(ts, TIME_HALF, c.stream);
         if (p.splits_g > 1)
             FS_CUDA(launch_merge_lse(part, p.splits_g, m, hg.rnorm, hg.rlogw2, eps_ln2, P.g.dev,
@@ -247,17 +253,17 @@ fs_status apply_tc(Call& c, Problem& P, int mode, const fs_options* opt) {
     h.nc = m;
     h.nch = p.nch;
     h.col_tiles = (int)p.rty;
-    h.tiles_per_split = p.tps_f;
-    h.splits = p.splits_f;
+    h.tiles_per_split = A.lse_tps;
+    h.splits = A.lse_splits;
     h.stages = half_stages(p.nch, p.qres);
     h.eps_ln2 = (float)(eps * kLn2);
     h.rnorm = nullptr;
     h.pot = lse2;
-    h.partial = c.at<float2>(B.partial);
+    h.partial = c.at<float2>(A.lse_partial);
     h.err = c.ws->err_word;
     FS_CUDA(launch_half_tc(h, (int)p.rtx, p.qres, c.stream));
-    if (p.splits_f > 1)
-        FS_CUDA(launch_merge_lse(h.partial, p.splits_f, n, nullptr, nullptr, 0.f, lse2, nullptr, 1,
+    if (A.lse_splits > 1)
+        FS_CUDA(launch_merge_lse(h.partial, A.lse_splits, n, nullptr, nullptr, 0.f, lse2, nullptr, 1,
                                  c.stream));
 
     // values: transposed fp16 tiles with a power-of-two scale

@@ -54,6 +54,13 @@ cudaError_t launch_to_tiles(const float* P, int64_t rows, int d, const float* sh
 cudaError_t launch_bias_init(const float* pot, const float* norm, const float* logw2,
                              float l_over_eps, int64_t rows, int64_t rows_pad, float* bias,
                              cudaStream_t s);
+// CTA-pair variant (fs_tc_pair.cu): M = 256 over two CTAs, 256-column tiles
+// (col_tiles / tiles_per_split count 256-column tiles; row_tiles even; K has
+// an even number of 128-row tiles and the bias 256 entries per tile).
+int pair_stages(int nch, bool qres);
+size_t pair_smem_bytes(int nch, bool qres, int stages);
+cudaError_t launch_half_pair(const TcHalfArgs& a, int row_tiles, bool qres, cudaStream_t s);
+
 int half_stages(int nch, bool qres);    // deepest ring that fits next to resident Q
 size_t half_smem_bytes(int nch, bool qres, int stages);
 cudaError_t launch_half_tc(const TcHalfArgs& a, int row_tiles, bool qres, cudaStream_t s);

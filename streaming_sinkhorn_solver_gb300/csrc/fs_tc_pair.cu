@@ -1,0 +1,369 @@
+// Fused half-update on CTA pairs: tcgen05.mma.cta_group::2 with M = 256
+// (the pair's two 128-row tiles of Q) and N = 256 columns of K.
+//
+// "FlashSinkhorn: IO-Aware Entropic Optimal Transport on GPU", Method 1
+// (Proposition 1) and Method 2 (streaming kernels, row-stationary traversal,
+// online max/sum-exp, fused write-back) -- the same computation as
+// fs_tc_half.cu, mapped onto two SMs.
+//
+// Why pairs.  With one CTA, an M = N = 128 MMA step reads 4 KB of A and 4 KB
+// of B from shared memory and the bulk copies write another 4 KB of B: about
+// 192 B/clk at the f16 MMA rate, well above the ~128 B/clk an SM's shared
+// memory delivers.  In a pair each SM keeps its own 128 Q rows and supplies
+// half of each 256-row K tile, so an MMA step costs it 4 KB of A, 4 KB of B
+// read and 4 KB of B written per 128 clocks (~96 B/clk), and its copy ring
+// covers twice the latency for the same bytes.
+//
+// Roles (320 threads per CTA, clusters of 2 along x):
+//   warp 0     producer, both CTAs: own Q tile once, then per 256-column tile
+//              the 1 KB bias slice and its own 128-row half of every K chunk;
+//   warp 1     even CTA: issues the pair MMAs into TMEM buffer t mod 2 and
+//              commits with multicast to both CTAs' barriers;
+//              odd CTA: relays "my half of this stage has landed" (and "my Q
+//              has landed") to the even CTA's barriers with remote arrives;
+//   warps 2-9  two epilogue groups per CTA, tile t going to group t mod 2,
+//              one thread per row reading its 256 scores from its own TMEM in
+//              two halves; the TMEM buffer is released to the even CTA's
+//              barrier (local and remote arrivals).
+#include "fs_tc.cuh"
+
+namespace fs {
+namespace tc {
+
+namespace {
+
+constexpr int BNP = 256;                    // columns of a pair score tile
+constexpr int kPairBufs = 2;                // TMEM buffers of BNP columns
+constexpr int kPairTmemCols = kPairBufs * BNP;
+constexpr int kPairBiasBytes = BNP * 4;
+
+__host__ __device__ constexpr int pair_fixed_bytes(int nch, bool qres) {
+    return 1024 + (qres ? nch * CHUNK_BYTES : 0) + kPairBufs * kPairBiasBytes + BM * 8 +
+           8 * (2 * kMaxStages + 4 * kPairBufs + 2) + 16;
+}
+
+__device__ __forceinline__ void epi_bar_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kHalfGroups * kEpiWarps * 32) : "memory");
+}
+
+// one row's 128 scores: s = acc kappa' + bias, folded into (M, S)
+__device__ __forceinline__ void fold128(float* v, const float4* sb, uint64_t ks2, float& M,
+                                        float& S) {
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < 32; ++q) {
+        const float4 bb = sb[q];
+        upk(fma2(pk(v[4 * q], v[4 * q + 1]), ks2, pk(bb.x, bb.y)), v[4 * q], v[4 * q + 1]);
+        upk(fma2(pk(v[4 * q + 2], v[4 * q + 3]), ks2, pk(bb.z, bb.w)), v[4 * q + 2], v[4 * q + 3]);
+        mx0 = max3(mx0, v[4 * q], v[4 * q + 1]);
+        mx1 = max3(mx1, v[4 * q + 2], v[4 * q + 3]);
+    }
+    const float mx = fmaxf(mx0, mx1);
+    if (mx > M) {
+        S *= ex2(M - mx);
+        M = mx;
+    }
+    const uint64_t nm = pk(-M, -M);
+    uint64_t acc0 = pk(0.f, 0.f), acc1 = pk(0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < 32; ++q) {
+        float x0, x1, x2, x3;
+        upk(add2(pk(v[4 * q], v[4 * q + 1]), nm), x0, x1);
+        upk(add2(pk(v[4 * q + 2], v[4 * q + 3]), nm), x2, x3);
+        acc0 = add2(acc0, pk(ex2(x0), ex2(x1)));
+        acc1 = add2(acc1, pk(ex2(x2), ex2(x3)));
+    }
+    float s0, s1, s2, s3;
+    upk(acc0, s0, s1);
+    upk(acc1, s2, s3);
+    S += (s0 + s1) + (s2 + s3);
+}
+
+}  // namespace
+
+int pair_stages(int nch, bool qres) {
+    const int stage = qres ? CHUNK_BYTES : 2 * CHUNK_BYTES;
+    const int s = (kSmemLimit - pair_fixed_bytes(nch, qres)) / stage;
+    return s < kMaxStages ? s : kMaxStages;
+}
+
+size_t pair_smem_bytes(int nch, bool qres, int stages) {
+    const size_t stage = qres ? CHUNK_BYTES : 2 * CHUNK_BYTES;
+    return (size_t)pair_fixed_bytes(nch, qres) + (size_t)stages * stage;
+}
+
+// a.col_tiles and a.tiles_per_split count 256-column tiles; a.K holds an even
+// number of 128-row tiles; a.cbias has 256 entries per column tile.
+template <bool QRES>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHalfThreads, 1)
+    k_half_pair(TcHalfArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int64_t rt = blockIdx.x;
+    const int j0 = blockIdx.y * a.tiles_per_split;
+    const int j1 = min(a.col_tiles, j0 + a.tiles_per_split);
+    const int ntiles = j1 - j0;
+    const int nch = a.nch;
+    const int stages = a.stages;
+
+    constexpr int STAGE_BYTES = QRES ? CHUNK_BYTES : 2 * CHUNK_BYTES;
+    uint8_t* sQ = smem;
+    uint8_t* sStage = smem + (QRES ? nch * CHUNK_BYTES : 0);
+    uint8_t* sBias = sStage + stages * STAGE_BYTES;
+    float2* sMerge = reinterpret_cast<float2*>(sBias + kPairBufs * kPairBiasBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sMerge + BM);
+    uint64_t* empty = full + kMaxStages;
+    uint64_t* tfull = empty + kMaxStages;
+    uint64_t* tempty = tfull + kPairBufs;
+    uint64_t* bfull = tempty + kPairBufs;
+    uint64_t* bempty = bfull + kPairBufs;
+    uint64_t* qfull = bempty + kPairBufs;
+    uint64_t* drain = qfull + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+
+    if (threadIdx.x == 0) {
+        // the even CTA's full/qfull also count the odd CTA's relay arrival,
+        // its tempty the odd CTA's epilogue warps
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], leader ? 2 : 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < kPairBufs; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 2 * kEpiWarps);
+            mbar_init(&bfull[b], 1);
+            mbar_init(&bempty[b], kEpiWarps);
+        }
+        mbar_init(qfull, leader ? 2 : 1);
+        mbar_init(drain, 1);
+        fence_mbar_init();
+    }
+    cluster_sync();   // every barrier of both CTAs exists before any remote arrival
+    if (warp == 1) tmem_alloc_pair(tmem_slot, kPairTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- producer (both CTAs) ----------------
+        if (lane == 0) {
+            const char* Qg = reinterpret_cast<const char*>(a.Q) + rt * nch * (int64_t)CHUNK_BYTES;
+            if (QRES) {
+                mbar_arrive_expect_tx(qfull, (uint32_t)(nch * CHUNK_BYTES));
+                for (int c = 0; c < nch; ++c)
+                    bulk_g2s(sQ + c * CHUNK_BYTES, Qg + c * (int64_t)CHUNK_BYTES, CHUNK_BYTES, qfull);
+            }
+            int s = 0, issued = 0, bissued = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int t = 0; t < ntiles && ok; ++t) {
+                const int b = t & 1;
+                if (!mbar_wait(&bempty[b], (uint32_t)((t >> 1) & 1) ^ 1u, a.err, ERR_TIMEOUT_PRODUCER)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&bfull[b], kPairBiasBytes);
+                bulk_g2s(sBias + b * kPairBiasBytes, a.cbias + (int64_t)(j0 + t) * BNP,
+                         kPairBiasBytes, &bfull[b]);
+                ++bissued;
+                const char* Kg = reinterpret_cast<const char*>(a.K) +
+                                 (2 * (int64_t)(j0 + t) + rank) * nch * (int64_t)CHUNK_BYTES;
+                for (int c = 0; c < nch; ++c) {
+                    if (!mbar_wait(&empty[s], ph ^ 1u, a.err, ERR_TIMEOUT_PRODUCER)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = sStage + s * STAGE_BYTES;
+                    mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+                    bulk_g2s(st, Kg + c * (int64_t)CHUNK_BYTES, CHUNK_BYTES, &full[s]);
+                    if (!QRES)
+                        bulk_g2s(st + CHUNK_BYTES, Qg + c * (int64_t)CHUNK_BYTES, CHUNK_BYTES,
+                                 &full[s]);
+                    ++issued;
+                    if (++s == stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // let every copy already issued land before the CTA can exit; the
+                // copies complete the local transaction count whatever the peer does
+                int s2 = 0;
+                uint32_t ph2 = 0;
+                const int skip = issued > stages ? issued - stages : 0;
+                for (int i = 0; i < issued; ++i) {
+                    if (i >= skip) mbar_wait_cluster(&full[s2], ph2, a.err, ERR_TIMEOUT_PRODUCER);
+                    if (++s2 == stages) {
+                        s2 = 0;
+                        ph2 ^= 1u;
+                    }
+                }
+                for (int i = bissued > kPairBufs ? bissued - kPairBufs : 0; i < bissued; ++i)
+                    mbar_wait(&bfull[i & 1], (uint32_t)((i >> 1) & 1), a.err, ERR_TIMEOUT_PRODUCER);
+                if (QRES) mbar_wait_cluster(qfull, 0, a.err, ERR_TIMEOUT_PRODUCER);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // ---------------- MMA issuer (even CTA) ----------------
+            constexpr uint32_t idesc = idesc_f16_f32(2 * BM, BNP);
+            bool ok = true;
+            if (QRES) ok = mbar_wait_cluster(qfull, 0, a.err, ERR_TIMEOUT_MMA);
+            tc_fence_after();
+            int s = 0;
+            uint32_t ph = 0;
+            for (int t = 0; t < ntiles && ok; ++t) {
+                const int b = t & 1;
+                if (!mbar_wait_cluster(&tempty[b], (uint32_t)((t >> 1) & 1) ^ 1u, a.err,
+                                       ERR_TIMEOUT_MMA)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + (uint32_t)(b * BNP);
+                for (int c = 0; c < nch; ++c) {
+                    if (!mbar_wait_cluster(&full[s], ph, a.err, ERR_TIMEOUT_MMA)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t* st = sStage + s * STAGE_BYTES;
+                    const uint32_t aaddr = smem_u32(QRES ? sQ + c * CHUNK_BYTES : st + CHUNK_BYTES);
+                    const uint32_t baddr = smem_u32(st);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_f16_pair(d_tmem, sdesc_sw128(aaddr + kk * 32),
+                                     sdesc_sw128(baddr + kk * 32), idesc, (c | kk) != 0);
+                    mma_commit_pair(&empty[s], 3);
+                    if (++s == stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit_pair(&tfull[b], 3);
+            }
+            mma_commit_pair(drain, 3);
+            mbar_wait(drain, 0, a.err, ERR_TIMEOUT_MMA);
+        } else if (lane == 0) {
+            // ---------------- relay (odd CTA) ----------------
+            bool ok = true;
+            if (QRES) {
+                ok = mbar_wait(qfull, 0, a.err, ERR_TIMEOUT_MMA);
+                if (ok) mbar_arrive_remote(mapa_shared(smem_u32(qfull), 0));
+            }
+            int s = 0;
+            uint32_t ph = 0;
+            for (int t = 0; t < ntiles && ok; ++t) {
+                for (int c = 0; c < nch; ++c) {
+                    if (!mbar_wait(&full[s], ph, a.err, ERR_TIMEOUT_MMA)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_remote(mapa_shared(smem_u32(&full[s]), 0));
+                    if (++s == stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+        }
+    } else {
+        // ---------------- epilogue groups: one thread per row ----------------
+        const int grp = (warp - 2) / kEpiWarps;
+        const int quarter = warp & 3;
+        const int rloc = quarter * 32 + lane;
+        const int64_t row = rt * BM + rloc;
+        const float ks = *a.kscale;
+        const uint64_t ks2 = pk(ks, ks);
+        const uint32_t lofs = (uint32_t)(quarter * 32) << 16;
+        float M = -INFINITY, S = 0.f;
+        for (int t = grp; t < ntiles; t += kHalfGroups) {
+            const int b = t & 1;
+            const uint32_t ph = (uint32_t)((t >> 1) & 1);
+            if (!mbar_wait_cluster(&tfull[b], ph, a.err, ERR_TIMEOUT_EPILOGUE)) break;
+            tc_fence_after();
+            if (!mbar_wait(&bfull[b], ph, a.err, ERR_TIMEOUT_EPILOGUE)) break;
+            const float4* sb = reinterpret_cast<const float4*>(sBias + b * kPairBiasBytes);
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                float v[128];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    tmem_ld32(tmem + (uint32_t)(b * BNP + h * 128) + lofs + q * 32, v + q * 32);
+                tmem_wait_ld();
+                if (h == 1) {
+                    // both halves are in registers: hand the buffer back to the MMA
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[b]), 0));
+                }
+                fold128(v, sb + h * 32, ks2, M, S);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bempty[b]);
+        }
+
+        // merge the groups in a fixed order: group 0 absorbs group 1
+        if (grp == 1) sMerge[rloc] = make_float2(M, S);
+        epi_bar_sync();
+        if (grp == 0) {
+            const float2 o = sMerge[rloc];
+            const float Mt = fmaxf(M, o.x);
+            const float St = S * ex2(M - Mt) + o.y * ex2(o.x - Mt);
+            if (row < a.nr) {
+                if (a.splits > 1) {
+                    a.partial[(int64_t)blockIdx.y * a.nr + row] = make_float2(Mt, St);
+                } else {
+                    const float lse2 = Mt + log2f(St);
+                    if (a.rnorm != nullptr) {
+                        a.pot[row] = a.rnorm[row] - a.eps_ln2 * lse2;
+                        a.rbias[row] = a.rlogw2[row] - lse2;
+                    } else {
+                        a.pot[row] = lse2;
+                    }
+                }
+            }
+        }
+    }
+
+    // no MMA of the pair is in flight past this point (the even CTA drained
+    // them); neither CTA frees TMEM or leaves while the other may still use it
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, kPairTmemCols);
+    }
+}
+
+cudaError_t launch_half_pair(const TcHalfArgs& a, int row_tiles, bool qres, cudaStream_t s) {
+    if (row_tiles % 2 != 0) return cudaErrorInvalidValue;
+    const size_t smem = pair_smem_bytes(a.nch, qres, a.stages);
+    dim3 grid((unsigned)row_tiles, (unsigned)a.splits);
+    cudaError_t e;
+    if (qres) {
+        e = cudaFuncSetAttribute(k_half_pair<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        k_half_pair<true><<<grid, kHalfThreads, smem, s>>>(a);
+    } else {
+        e = cudaFuncSetAttribute(k_half_pair<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        k_half_pair<false><<<grid, kHalfThreads, smem, s>>>(a);
+    }
+    count_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace tc
+}  // namespace fs
