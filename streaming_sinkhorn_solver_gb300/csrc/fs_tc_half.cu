@@ -247,6 +247,7 @@ __global__ void __launch_bounds__(kHalfThreads, 1) k_half_tc(TcHalfArgs a) {
                 S *= ex2(M - mx);
                 M = mx;
             }
+            if (M == -INFINITY) continue;   // only padding columns so far: nothing to add
             // S += sum 2^{s - M}
             const uint64_t nm = pk(-M, -M);
             uint64_t acc0 = pk(0.f, 0.f), acc1 = pk(0.f, 0.f);

@@ -63,6 +63,7 @@ __device__ __forceinline__ void fold128(float* v, const float4* sb, uint64_t ks2
         S *= ex2(M - mx);
         M = mx;
     }
+    if (M == -INFINITY) return;   // only padding columns so far: nothing to add
     const uint64_t nm = pk(-M, -M);
     uint64_t acc0 = pk(0.f, 0.f), acc1 = pk(0.f, 0.f);
 #pragma unroll
