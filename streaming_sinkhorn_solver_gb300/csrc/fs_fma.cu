@@ -145,7 +145,7 @@ __global__ void k_merge_lse(const float2* __restrict__ partial, int splits, int6
     float S = 0.f;
     for (int sp = 0; sp < splits; ++sp) {
         const float2 p = partial[(int64_t)sp * nr + i];
-        S += p.y * ex2(p.x - M);
+        if (p.x != -INFINITY) S += p.y * ex2(p.x - M);   // a padding-only split adds nothing
     }
     const float lse2 = M + log2f(S);
     if (rnorm == nullptr) {  // log2-sum-exp only (pre-pass of plan application)

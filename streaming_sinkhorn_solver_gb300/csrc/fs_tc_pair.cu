@@ -318,7 +318,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHalfThreads, 1)
         if (grp == 0) {
             const float2 o = sMerge[rloc];
             const float Mt = fmaxf(M, o.x);
-            const float St = S * ex2(M - Mt) + o.y * ex2(o.x - Mt);
+            // a group that saw only padding has (M, S) = (-inf, 0) and adds nothing
+            const float St = (M == -INFINITY ? 0.f : S * ex2(M - Mt)) +
+                             (o.x == -INFINITY ? 0.f : o.y * ex2(o.x - Mt));
             if (row < a.nr) {
                 if (a.splits > 1) {
                     a.partial[(int64_t)blockIdx.y * a.nr + row] = make_float2(Mt, St);
