@@ -98,17 +98,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Wait for the phase of parity `parity` to complete.  Gives up after
 // kTimeoutNs, ORs `code` into the device error word and returns false.
+//
+// The whole spin (try_wait, then %globaltimer against the deadline) is one
+// inline-PTX block with brace-scoped labels: with the retry loop written in
+// C++ instead, the thread issuing tcgen05.mma ran its MMA stream at about a
+// quarter of the tensor rate (measured on sm_103a), with the loop in PTX it
+// runs at full rate.
+#define FS_MBAR_WAIT_PTX(SEM)                                                     \
+    "{\n\t.reg .pred p;\n\t.reg .u64 t0, t;\n\t"                                  \
+    "mbarrier.try_wait.parity" SEM ".shared::cta.b64 p, [%1], %2;\n\t"            \
+    "@p bra.uni LAB_DONE;\n\t"                                                    \
+    "mov.u64 t0, %%globaltimer;\n"                                                \
+    "LAB_WAIT:\n\t"                                                               \
+    "mbarrier.try_wait.parity" SEM ".shared::cta.b64 p, [%1], %2;\n\t"            \
+    "@p bra.uni LAB_DONE;\n\t"                                                    \
+    "mov.u64 t, %%globaltimer;\n\t"                                               \
+    "sub.u64 t, t, t0;\n\t"                                                       \
+    "setp.lt.u64 p, t, %3;\n\t"                                                   \
+    "@p bra.uni LAB_WAIT;\n\t"                                                    \
+    "selp.u32 %0, 0, 0, p;\n\t"                                                   \
+    "bra.uni LAB_END;\n"                                                          \
+    "LAB_DONE:\n\t"                                                               \
+    "mov.u32 %0, 1;\n"                                                            \
+    "LAB_END:\n\t}"
+
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
                                           uint32_t code) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer() - t0 > kTimeoutNs) {
-            atomicOr(err, code);
-            return false;
-        }
-    }
+    uint32_t ok;
+    asm volatile(FS_MBAR_WAIT_PTX("")
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity), "l"(kTimeoutNs)
+                 : "memory");
+    if (!ok) atomicOr(err, code);
+    return ok != 0;
 }
 
 // --- bulk copy global -> shared (async proxy, completes on an mbarrier) -------
@@ -218,15 +240,13 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
 // bounded wait on a barrier that also receives arrivals from the peer CTA
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t* err,
                                                   uint32_t code) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    while (true) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
-        if (globaltimer() - t0 > kTimeoutNs) {
-            atomicOr(err, code);
-            return false;
-        }
-    }
+    uint32_t ok;
+    asm volatile(FS_MBAR_WAIT_PTX(".acquire.cluster")
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity), "l"(kTimeoutNs)
+                 : "memory");
+    if (!ok) atomicOr(err, code);
+    return ok != 0;
 }
 
 // all threads of both CTAs
