@@ -89,6 +89,9 @@ enum TimingKind : int { TIME_HALF = 0, TIME_APPLY = 1 };
 int timing_begin(cudaStream_t s);
 void timing_end(int slot, int kind, cudaStream_t s);
 
+// TMA tensor map (128 bytes) over `rows` rows of 64 fp16 at `base`, box 64 x 128.
+fs_status make_chunk_tmap(void* map128, const void* base, uint64_t rows);
+
 int choose_splits(int64_t row_blocks, int64_t nc, int sms, int per_sm, int64_t min_cols,
                   const fs_options* opt, int64_t* cols_per_split);
 

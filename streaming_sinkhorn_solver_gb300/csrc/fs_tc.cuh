@@ -255,6 +255,18 @@ __device__ __forceinline__ void cluster_sync() {
                      : "memory");
 }
 
+// TMA copy of one 128 x 64 fp16 chunk (a 2-D box {64, 128} at x = 0, y = row)
+// into this CTA's shared memory, completing its bytes on an mbarrier of
+// either CTA of the pair (`bar_cluster` is a shared::cluster address).
+__device__ __forceinline__ void tma_chunk_pair(void* dst_smem, const void* tmap, uint32_t row,
+                                               uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst_smem)),
+        "l"(tmap), "r"(0), "r"(row), "r"(bar_cluster)
+        : "memory");
+}
+
 // one warp in each CTA of the pair, collectively
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(

@@ -200,15 +200,20 @@ fs_status solve_tc(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) {
     hg.pot = P.g.dev;
     hg.rbias = c.at<float>(B.beta);
 
+    // TMA chunk maps over the two operand arrays (host-side encoding only)
+    TensorMap128 tmX, tmY;
+    FS_TRY(make_chunk_tmap(&tmX, hf.Q, (uint64_t)p.rtx * p.nch * BM));
+    FS_TRY(make_chunk_tmap(&tmY, hf.K, (uint64_t)p.rty * p.nch * BM));
+
     for (int32_t it = 0; it < n_iter; ++it) {
         int ts = timing_begin(c.stream);
-        FS_CUDA(launch_half_pair(hf, (int)p.rtx, p.qres, c.stream));
+        FS_CUDA(launch_half_pair(hf, tmX, tmY, (int)p.rtx, p.qres, c.stream));
         timing_end(ts, TIME_HALF, c.stream);
         if (p.splits_f > 1)
             FS_CUDA(launch_merge_lse(part, p.splits_f, n, hf.rnorm, hf.rlogw2, eps_ln2, P.f.dev,
                                      hf.rbias, 1, c.stream));
         ts = timing_begin(c.stream);
-        FS_CUDA(launch_half_pair(hg, (int)p.rty, p.qres, c.stream));
+        FS_CUDA(launch_half_pair(hg, tmY, tmX, (int)p.rty, p.qres, c.stream));
         timing_end(ts, TIME_HALF, c.stream);
         if (p.splits_g > 1)
             FS_CUDA(launch_merge_lse(part, p.splits_g, m, hg.rnorm, hg.rlogw2, eps_ln2, P.g.dev,

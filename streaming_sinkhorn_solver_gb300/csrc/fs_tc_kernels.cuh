@@ -54,12 +54,19 @@ cudaError_t launch_to_tiles(const float* P, int64_t rows, int d, const float* sh
 cudaError_t launch_bias_init(const float* pot, const float* norm, const float* logw2,
                              float l_over_eps, int64_t rows, int64_t rows_pad, float* bias,
                              cudaStream_t s);
+// An opaque 128-byte TMA descriptor (CUtensorMap), passed by value to kernels.
+struct alignas(64) TensorMap128 {
+    unsigned char bytes[128];
+};
+
 // CTA-pair variant (fs_tc_pair.cu): M = 256 over two CTAs, 256-column tiles
 // (col_tiles / tiles_per_split count 256-column tiles; row_tiles even; K has
-// an even number of 128-row tiles and the bias 256 entries per tile).
+// an even number of 128-row tiles and the bias 256 entries per tile).  tmQ /
+// tmK are chunk maps (make_chunk_tmap) over a.Q / a.K.
 int pair_stages(int nch, bool qres);
 size_t pair_smem_bytes(int nch, bool qres, int stages);
-cudaError_t launch_half_pair(const TcHalfArgs& a, int row_tiles, bool qres, cudaStream_t s);
+cudaError_t launch_half_pair(const TcHalfArgs& a, const TensorMap128& tmQ,
+                             const TensorMap128& tmK, int row_tiles, bool qres, cudaStream_t s);
 
 int half_stages(int nch, bool qres);    // deepest ring that fits next to resident Q
 size_t half_smem_bytes(int nch, bool qres, int stages);

@@ -97,7 +97,8 @@ size_t pair_smem_bytes(int nch, bool qres, int stages) {
 // number of 128-row tiles; a.cbias has 256 entries per column tile.
 template <bool QRES>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHalfThreads, 1)
-    k_half_pair(TcHalfArgs a) {
+    k_half_pair(const __grid_constant__ TensorMap128 tmQ, const __grid_constant__ TensorMap128 tmK,
+                TcHalfArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -128,10 +129,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHalfThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
 
     if (threadIdx.x == 0) {
-        // the even CTA's full/qfull also count the odd CTA's relay arrival,
-        // its tempty the odd CTA's epilogue warps
+        // the even CTA's full/qfull collect the bytes of both CTAs' copies (the
+        // even producer's expect_tx covers both); its tempty also counts the
+        // odd CTA's epilogue warps.  The odd CTA's full/qfull stay unused.
         for (int s = 0; s < stages; ++s) {
-            mbar_init(&full[s], leader ? 2 : 1);
+            mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < kPairBufs; ++b) {
@@ -140,7 +142,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHalfThreads, 1)
             mbar_init(&bfull[b], 1);
             mbar_init(&bempty[b], kEpiWarps);
         }
-        mbar_init(qfull, leader ? 2 : 1);
+        mbar_init(qfull, 1);
         mbar_init(drain, 1);
         fence_mbar_init();
     }
@@ -154,11 +156,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHalfThreads, 1)
     if (warp == 0) {
         // ---------------- producer (both CTAs) ----------------
         if (lane == 0) {
-            const char* Qg = reinterpret_cast<const char*>(a.Q) + rt * nch * (int64_t)CHUNK_BYTES;
+            // both CTAs' copies complete their bytes on the even CTA's barriers
+            const uint32_t qfull_lead = mapa_shared(smem_u32(qfull), 0);
+            const uint32_t qrow0 = (uint32_t)(rt * nch) * BM;
             if (QRES) {
-                mbar_arrive_expect_tx(qfull, (uint32_t)(nch * CHUNK_BYTES));
+                if (leader) mbar_arrive_expect_tx(qfull, (uint32_t)(2 * nch * CHUNK_BYTES));
                 for (int c = 0; c < nch; ++c)
-                    bulk_g2s(sQ + c * CHUNK_BYTES, Qg + c * (int64_t)CHUNK_BYTES, CHUNK_BYTES, qfull);
+                    tma_chunk_pair(sQ + c * CHUNK_BYTES, &tmQ, qrow0 + c * BM, qfull_lead);
             }
             int s = 0, issued = 0, bissued = 0;
             uint32_t ph = 0;
@@ -173,19 +177,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHalfThreads, 1)
                 bulk_g2s(sBias + b * kPairBiasBytes, a.cbias + (int64_t)(j0 + t) * BNP,
                          kPairBiasBytes, &bfull[b]);
                 ++bissued;
-                const char* Kg = reinterpret_cast<const char*>(a.K) +
-                                 (2 * (int64_t)(j0 + t) + rank) * nch * (int64_t)CHUNK_BYTES;
+                const uint32_t krow0 = (uint32_t)((2 * (j0 + t) + (int)rank) * nch) * BM;
                 for (int c = 0; c < nch; ++c) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, a.err, ERR_TIMEOUT_PRODUCER)) {
                         ok = false;
                         break;
                     }
                     uint8_t* st = sStage + s * STAGE_BYTES;
-                    mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-                    bulk_g2s(st, Kg + c * (int64_t)CHUNK_BYTES, CHUNK_BYTES, &full[s]);
-                    if (!QRES)
-                        bulk_g2s(st + CHUNK_BYTES, Qg + c * (int64_t)CHUNK_BYTES, CHUNK_BYTES,
-                                 &full[s]);
+                    const uint32_t full_lead = mapa_shared(smem_u32(&full[s]), 0);
+                    if (leader) mbar_arrive_expect_tx(&full[s], 2 * STAGE_BYTES);
+                    tma_chunk_pair(st, &tmK, krow0 + c * BM, full_lead);
+                    if (!QRES) tma_chunk_pair(st + CHUNK_BYTES, &tmQ, qrow0 + c * BM, full_lead);
                     ++issued;
                     if (++s == stages) {
                         s = 0;
@@ -194,21 +196,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHalfThreads, 1)
                 }
             }
             if (!ok) {
-                // let every copy already issued land before the CTA can exit; the
-                // copies complete the local transaction count whatever the peer does
-                int s2 = 0;
-                uint32_t ph2 = 0;
-                const int skip = issued > stages ? issued - stages : 0;
-                for (int i = 0; i < issued; ++i) {
-                    if (i >= skip) mbar_wait_cluster(&full[s2], ph2, a.err, ERR_TIMEOUT_PRODUCER);
-                    if (++s2 == stages) {
-                        s2 = 0;
-                        ph2 ^= 1u;
+                // let the copies already issued land before the pair can exit: the
+                // even CTA's barriers count both CTAs' bytes, and the final cluster
+                // barrier holds the odd CTA until the even one has drained them
+                if (leader) {
+                    int s2 = 0;
+                    uint32_t ph2 = 0;
+                    const int skip = issued > stages ? issued - stages : 0;
+                    for (int i = 0; i < issued; ++i) {
+                        if (i >= skip) mbar_wait_cluster(&full[s2], ph2, a.err, ERR_TIMEOUT_PRODUCER);
+                        if (++s2 == stages) {
+                            s2 = 0;
+                            ph2 ^= 1u;
+                        }
                     }
+                    if (QRES) mbar_wait_cluster(qfull, 0, a.err, ERR_TIMEOUT_PRODUCER);
                 }
                 for (int i = bissued > kPairBufs ? bissued - kPairBufs : 0; i < bissued; ++i)
                     mbar_wait(&bfull[i & 1], (uint32_t)((i >> 1) & 1), a.err, ERR_TIMEOUT_PRODUCER);
-                if (QRES) mbar_wait_cluster(qfull, 0, a.err, ERR_TIMEOUT_PRODUCER);
             }
         }
     } else if (warp == 1) {
@@ -253,28 +258,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHalfThreads, 1)
             }
             mma_commit_pair(drain, 3);
             mbar_wait(drain, 0, a.err, ERR_TIMEOUT_MMA);
-        } else if (lane == 0) {
-            // ---------------- relay (odd CTA) ----------------
-            bool ok = true;
-            if (QRES) {
-                ok = mbar_wait(qfull, 0, a.err, ERR_TIMEOUT_MMA);
-                if (ok) mbar_arrive_remote(mapa_shared(smem_u32(qfull), 0));
-            }
-            int s = 0;
-            uint32_t ph = 0;
-            for (int t = 0; t < ntiles && ok; ++t) {
-                for (int c = 0; c < nch; ++c) {
-                    if (!mbar_wait(&full[s], ph, a.err, ERR_TIMEOUT_MMA)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_remote(mapa_shared(smem_u32(&full[s]), 0));
-                    if (++s == stages) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
-                }
-            }
         }
     } else {
         // ---------------- epilogue groups: one thread per row ----------------
@@ -348,7 +331,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHalfThreads, 1)
     }
 }
 
-cudaError_t launch_half_pair(const TcHalfArgs& a, int row_tiles, bool qres, cudaStream_t s) {
+cudaError_t launch_half_pair(const TcHalfArgs& a, const TensorMap128& tmQ,
+                             const TensorMap128& tmK, int row_tiles, bool qres, cudaStream_t s) {
     if (row_tiles % 2 != 0) return cudaErrorInvalidValue;
     const size_t smem = pair_smem_bytes(a.nch, qres, a.stages);
     dim3 grid((unsigned)row_tiles, (unsigned)a.splits);
@@ -357,12 +341,12 @@ cudaError_t launch_half_pair(const TcHalfArgs& a, int row_tiles, bool qres, cuda
         e = cudaFuncSetAttribute(k_half_pair<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
-        k_half_pair<true><<<grid, kHalfThreads, smem, s>>>(a);
+        k_half_pair<true><<<grid, kHalfThreads, smem, s>>>(tmQ, tmK, a);
     } else {
         e = cudaFuncSetAttribute(k_half_pair<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
-        k_half_pair<false><<<grid, kHalfThreads, smem, s>>>(a);
+        k_half_pair<false><<<grid, kHalfThreads, smem, s>>>(tmQ, tmK, a);
     }
     count_launch();
     return cudaGetLastError();
