@@ -14,6 +14,7 @@ using namespace tc;
 struct TcPlan {
     int nch;
     bool qres;
+    bool pair;                  // CTA-pair kernel (d > 128); else one CTA per row tile
     int64_t rtx, rty;           // row tiles of X and Y
     int splits_f, splits_g;
     int tps_f, tps_g;           // column tiles per split
@@ -58,8 +59,13 @@ TcPlan plan_tc(int64_t n, int64_t m, int32_t d, int sms, const fs_options* opt) 
     // and padding biases -inf
     p.rtx = (n + 2 * BM - 1) / (2 * BM) * 2;
     p.rty = (m + 2 * BM - 1) / (2 * BM) * 2;
-    choose_tc_splits(p.rtx, p.rty / 2, sms, opt, &p.splits_f, &p.tps_f);
-    choose_tc_splits(p.rty, p.rtx / 2, sms, opt, &p.splits_g, &p.tps_g);
+    // Pairs pay off once a score tile carries enough MMA work (d > 128); for
+    // small d the exponentials bind, and the one-CTA kernel's four TMEM
+    // buffers keep both epilogue groups busier.
+    p.pair = p.nch > 2;
+    const int64_t ct = p.pair ? 2 : 1;   // 128-row tiles per column tile
+    choose_tc_splits(p.rtx, p.rty / ct, sms, opt, &p.splits_f, &p.tps_f);
+    choose_tc_splits(p.rty, p.rtx / ct, sms, opt, &p.splits_g, &p.tps_g);
     return p;
 }
 
@@ -174,10 +180,10 @@ fs_status solve_tc(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) {
     hf.nr = n;
     hf.nc = m;
     hf.nch = p.nch;
-    hf.col_tiles = (int)(p.rty / 2);
+    hf.col_tiles = (int)(p.pair ? p.rty / 2 : p.rty);
     hf.tiles_per_split = p.tps_f;
     hf.splits = p.splits_f;
-    hf.stages = pair_stages(p.nch, p.qres);
+    hf.stages = p.pair ? pair_stages(p.nch, p.qres) : half_stages(p.nch, p.qres);
     hf.eps_ln2 = eps_ln2;
     hf.rnorm = c.at<float>(B.nx);
     hf.rlogw2 = c.at<float>(B.lax);
@@ -192,7 +198,7 @@ fs_status solve_tc(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) {
     hg.cbias = c.at<float>(B.alpha);
     hg.nr = m;
     hg.nc = n;
-    hg.col_tiles = (int)(p.rtx / 2);
+    hg.col_tiles = (int)(p.pair ? p.rtx / 2 : p.rtx);
     hg.tiles_per_split = p.tps_g;
     hg.splits = p.splits_g;
     hg.rnorm = c.at<float>(B.ny);
@@ -205,15 +211,20 @@ fs_status solve_tc(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) {
     FS_TRY(make_chunk_tmap(&tmX, hf.Q, (uint64_t)p.rtx * p.nch * BM));
     FS_TRY(make_chunk_tmap(&tmY, hf.K, (uint64_t)p.rty * p.nch * BM));
 
+    auto half = [&](const TcHalfArgs& h, const TensorMap128& tq, const TensorMap128& tk,
+                    int64_t row_tiles) -> cudaError_t {
+        return p.pair ? launch_half_pair(h, tq, tk, (int)row_tiles, p.qres, c.stream)
+                      : launch_half_tc(h, (int)row_tiles, p.qres, c.stream);
+    };
     for (int32_t it = 0; it < n_iter; ++it) {
         int ts = timing_begin(c.stream);
-        FS_CUDA(launch_half_pair(hf, tmX, tmY, (int)p.rtx, p.qres, c.stream));
+        FS_CUDA(half(hf, tmX, tmY, p.rtx));
         timing_end(ts, TIME_HALF, c.stream);
         if (p.splits_f > 1)
             FS_CUDA(launch_merge_lse(part, p.splits_f, n, hf.rnorm, hf.rlogw2, eps_ln2, P.f.dev,
                                      hf.rbias, 1, c.stream));
         ts = timing_begin(c.stream);
-        FS_CUDA(launch_half_pair(hg, tmY, tmX, (int)p.rty, p.qres, c.stream));
+        FS_CUDA(half(hg, tmY, tmX, p.rty));
         timing_end(ts, TIME_HALF, c.stream);
         if (p.splits_g > 1)
             FS_CUDA(launch_merge_lse(part, p.splits_g, m, hg.rnorm, hg.rlogw2, eps_ln2, P.g.dev,
