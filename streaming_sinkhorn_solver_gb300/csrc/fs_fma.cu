@@ -18,7 +18,6 @@ namespace fs {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kChunk = 512;   // columns staged in shared memory per pass
 constexpr int kGroup = 8;     // columns scored before one max/rescale check
 
 template <int D>
@@ -35,89 +34,128 @@ __device__ __forceinline__ void load_cols(const float4* __restrict__ sc, int j, 
     for (int k = 0; k <= D; ++k) c[k] = t[k];
 }
 
-template <int D, int RPT>
+// Shared-memory column records are stored duplicated, (y0, y0, y1, y1, ...,
+// bias, bias), so that one packed fma.rn.f32x2 scores a column against two
+// rows at once with no register shuffling.
+__host__ __device__ constexpr int fma_dup_stride(int D) { return (2 * (D + 1) + 3) / 4 * 4; }
+__host__ __device__ constexpr int fma_chunk(int D) { return D <= 4 ? 512 : 256; }
+
+// Score G columns starting at shared record j against RP row pairs and fold
+// them into the rows' running max M and sum S of 2^{s - M}.
+template <int D, int RP, int G>
+__device__ __forceinline__ void fma_group(const float4* __restrict__ sc, int j,
+                                          const uint64_t (&q)[RP][D], float (&M)[2 * RP],
+                                          float (&S)[2 * RP]) {
+    constexpr int DD = fma_dup_stride(D);
+    uint64_t s[RP][G];
+#pragma unroll
+    for (int u = 0; u < G; ++u) {
+        const float4* p = sc + (j + u) * (DD / 4);
+        uint64_t c[DD / 2];
+#pragma unroll
+        for (int w = 0; w < DD / 4; ++w) {
+            const float4 v = p[w];
+            c[2 * w] = pk(v.x, v.y);
+            c[2 * w + 1] = pk(v.z, v.w);
+        }
+#pragma unroll
+        for (int r = 0; r < RP; ++r) {
+            uint64_t acc = c[D];
+#pragma unroll
+            for (int k = 0; k < D; ++k) acc = fma2(q[r][k], c[k], acc);
+            s[r][u] = acc;
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < RP; ++r) {
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < G; u += 2) {
+            float a0, a1, b0 = -INFINITY, b1 = -INFINITY;
+            upk(s[r][u], a0, a1);
+            if (u + 1 < G) upk(s[r][u + 1], b0, b1);
+            mx0 = max3(mx0, a0, b0);
+            mx1 = max3(mx1, a1, b1);
+        }
+        if (mx0 > M[2 * r]) {
+            S[2 * r] *= ex2(M[2 * r] - mx0);
+            M[2 * r] = mx0;
+        }
+        if (mx1 > M[2 * r + 1]) {
+            S[2 * r + 1] *= ex2(M[2 * r + 1] - mx1);
+            M[2 * r + 1] = mx1;
+        }
+        const uint64_t nm = pk(-M[2 * r], -M[2 * r + 1]);
+        uint64_t acc = pk(0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < G; ++u) {
+            float x0, x1;
+            upk(add2(s[r][u], nm), x0, x1);
+            acc = add2(acc, pk(ex2(x0), ex2(x1)));
+        }
+        float e0, e1;
+        upk(acc, e0, e1);
+        S[2 * r] += e0;
+        S[2 * r + 1] += e1;
+    }
+}
+
+// RP row pairs per thread: rows row0 + tid + i * kThreads, i < 2 RP.
+template <int D, int RP>
 __global__ void __launch_bounds__(kThreads) k_half_fma(HalfArgs a) {
     constexpr int DS = fma_stride(D);
-    __shared__ float4 sc[kChunk * DS / 4];
+    constexpr int DD = fma_dup_stride(D);
+    constexpr int CH = fma_chunk(D);
+    constexpr int RPT = 2 * RP;
+    __shared__ float4 sc[CH * DD / 4];
 
     const int tid = threadIdx.x;
     const int64_t row0 = (int64_t)blockIdx.x * (kThreads * RPT);
     const int64_t c0 = (int64_t)blockIdx.y * a.cols_per_split;
     const int64_t c1 = min(a.nc, c0 + a.cols_per_split);
 
-    float q[RPT][D], M[RPT], S[RPT];
+    uint64_t q[RP][D];
+    float M[RPT], S[RPT];
 #pragma unroll
-    for (int r = 0; r < RPT; ++r) {
-        int64_t row = row0 + tid + r * kThreads;
-        row = row < a.nr ? row : a.nr - 1;
+    for (int r = 0; r < RP; ++r) {
+        int64_t ra = row0 + tid + (2 * r) * kThreads, rb = ra + kThreads;
+        ra = ra < a.nr ? ra : a.nr - 1;
+        rb = rb < a.nr ? rb : a.nr - 1;
 #pragma unroll
-        for (int k = 0; k < D; ++k) q[r][k] = a.rows[row * DS + k] * a.kappa;
-        M[r] = -INFINITY;
-        S[r] = 0.f;
+        for (int k = 0; k < D; ++k)
+            q[r][k] = pk(a.rows[ra * DS + k] * a.kappa, a.rows[rb * DS + k] * a.kappa);
+    }
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+        M[i] = -INFINITY;
+        S[i] = 0.f;
     }
 
-    for (int64_t cb = c0; cb < c1; cb += kChunk) {
-        const int ncol = (int)min((int64_t)kChunk, c1 - cb);
+    float* sf = reinterpret_cast<float*>(sc);
+    for (int64_t cb = c0; cb < c1; cb += CH) {
+        const int ncol = (int)min((int64_t)CH, c1 - cb);
         __syncthreads();
-        const float4* src = reinterpret_cast<const float4*>(a.cols + cb * DS);
-        for (int e = tid; e < ncol * (DS / 4); e += kThreads) sc[e] = src[e];
+        // stage (coordinates, bias) records, each value written twice
+        for (int e = tid; e < ncol * (D + 1); e += kThreads) {
+            const int jj = e / (D + 1), k = e - jj * (D + 1);
+            const float v = a.cols[(cb + jj) * DS + k];
+            sf[jj * DD + 2 * k] = v;
+            sf[jj * DD + 2 * k + 1] = v;
+        }
         __syncthreads();
-
         int j = 0;
-        for (; j + kGroup <= ncol; j += kGroup) {
-            float s[RPT][kGroup];
-#pragma unroll
-            for (int u = 0; u < kGroup; ++u) {
-                float c[D + 1];
-                load_cols<D>(sc, j + u, c);
-#pragma unroll
-                for (int r = 0; r < RPT; ++r) {
-                    float acc = c[D];
-#pragma unroll
-                    for (int k = 0; k < D; ++k) acc = fmaf(q[r][k], c[k], acc);
-                    s[r][u] = acc;
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < RPT; ++r) {
-                float mx = s[r][0];
-#pragma unroll
-                for (int u = 1; u < kGroup; ++u) mx = fmaxf(mx, s[r][u]);
-                if (mx > M[r]) {
-                    S[r] *= ex2(M[r] - mx);
-                    M[r] = mx;
-                }
-                float acc = 0.f;
-#pragma unroll
-                for (int u = 0; u < kGroup; ++u) acc += ex2(s[r][u] - M[r]);
-                S[r] += acc;
-            }
-        }
-        for (; j < ncol; ++j) {
-            float c[D + 1];
-            load_cols<D>(sc, j, c);
-#pragma unroll
-            for (int r = 0; r < RPT; ++r) {
-                float acc = c[D];
-#pragma unroll
-                for (int k = 0; k < D; ++k) acc = fmaf(q[r][k], c[k], acc);
-                if (acc > M[r]) {
-                    S[r] *= ex2(M[r] - acc);
-                    M[r] = acc;
-                }
-                S[r] += ex2(acc - M[r]);
-            }
-        }
+        for (; j + kGroup <= ncol; j += kGroup) fma_group<D, RP, kGroup>(sc, j, q, M, S);
+        for (; j < ncol; ++j) fma_group<D, RP, 1>(sc, j, q, M, S);
     }
 
 #pragma unroll
-    for (int r = 0; r < RPT; ++r) {
-        const int64_t row = row0 + tid + r * kThreads;
+    for (int i = 0; i < RPT; ++i) {
+        const int64_t row = row0 + tid + i * kThreads;
         if (row >= a.nr) continue;
         if (a.splits > 1) {
-            a.partial[(int64_t)blockIdx.y * a.nr + row] = make_float2(M[r], S[r]);
+            a.partial[(int64_t)blockIdx.y * a.nr + row] = make_float2(M[i], S[i]);
         } else {
-            const float lse2 = M[r] + log2f(S[r]);
+            const float lse2 = M[i] + log2f(S[i]);
             a.pot[row] = a.rnorm[row] - a.eps_ln2 * lse2;
             a.rows[row * DS + D] = a.rlogw2[row] - lse2;
         }
@@ -126,10 +164,11 @@ __global__ void __launch_bounds__(kThreads) k_half_fma(HalfArgs a) {
 
 template <int D>
 cudaError_t launch_half_fma_t(const HalfArgs& a, cudaStream_t s) {
-    constexpr int RPT = D <= 4 ? 4 : (D <= 8 ? 2 : 1);
-    const int64_t rows_per_block = (int64_t)kThreads * RPT;
+    constexpr int RP = fma_row_pairs(D);
+    const int64_t rows_per_block = (int64_t)kThreads * 2 * RP;
+    static_assert(kThreads * 2 * RP == fma_rows_per_block(D), "row blocking");
     dim3 grid((unsigned)((a.nr + rows_per_block - 1) / rows_per_block), (unsigned)a.splits);
-    k_half_fma<D, RPT><<<grid, kThreads, 0, s>>>(a);
+    k_half_fma<D, RP><<<grid, kThreads, 0, s>>>(a);
     count_launch();
     return cudaGetLastError();
 }

@@ -18,8 +18,7 @@ FmaPlan plan_fma(int64_t n, int64_t m, int32_t d, int sms, const fs_options* opt
     FmaPlan p;
     p.D = fma_pad_dim(d);
     p.DS = fma_stride(p.D);
-    const int rpt = p.D <= 4 ? 4 : (p.D <= 8 ? 2 : 1);
-    const int64_t rows_per_block = 256 * rpt;
+    const int64_t rows_per_block = fma_rows_per_block(p.D);
     p.splits_f = choose_splits((n + rows_per_block - 1) / rows_per_block, m, sms, 4, 256, opt, &p.cps_f);
     p.splits_g = choose_splits((m + rows_per_block - 1) / rows_per_block, n, sms, 4, 256, opt, &p.cps_g);
     return p;

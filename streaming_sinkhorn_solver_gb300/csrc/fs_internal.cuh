@@ -47,6 +47,31 @@ __device__ __forceinline__ float lg2(float x) {
     return y;
 }
 
+// packed fp32 arithmetic: two lanes per instruction (sm_100 family)
+__device__ __forceinline__ uint64_t pk(float x, float y) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ void upk(uint64_t r, float& x, float& y) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // ---------------------------------------------------------------------------
 // FMA path: packed operand arrays.  Row r of a packed array holds the centred
 // coordinates of a point, zero-padded to D, then its current bias (alpha or
@@ -55,6 +80,10 @@ __device__ __forceinline__ float lg2(float x) {
 __host__ __device__ constexpr int fma_pad_dim(int d) { return d <= 2 ? 2 : d <= 3 ? 3 : d <= 4 ? 4 : d <= 8 ? 8 : 16; }
 __host__ __device__ constexpr int fma_stride(int D) { return ((D + 1) + 3) / 4 * 4; }
 constexpr int kFmaMaxDim = 16;
+// Half-update rows per thread come in pairs (packed f32x2 lanes); blocks are
+// 256 threads, so a block covers 512 * fma_row_pairs(D) rows.
+__host__ __device__ constexpr int fma_row_pairs(int D) { return D <= 4 ? 2 : 1; }
+constexpr int64_t fma_rows_per_block(int D) { return 512 * fma_row_pairs(D); }
 
 // Half-update on the FMA path.  rows: packed array of the side being
 // updated (nr rows); cols: packed array of the other side (nc rows) whose

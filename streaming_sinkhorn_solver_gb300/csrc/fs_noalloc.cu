@@ -119,8 +119,7 @@ fs_status solve_noalloc(const float* X, const float* a, int64_t n, const float* 
 
     const int D = fma_pad_dim(d);
     const int DS = fma_stride(D);
-    const int rpt = D <= 4 ? 4 : (D <= 8 ? 2 : 1);
-    const int64_t rows_per_block = 256 * rpt;
+    const int64_t rows_per_block = fma_rows_per_block(D);
     int64_t cps_f, cps_g;
     int sp_f = choose_splits((n + rows_per_block - 1) / rows_per_block, m, sc->sms, 4, 256, nullptr, &cps_f);
     int sp_g = choose_splits((m + rows_per_block - 1) / rows_per_block, n, sc->sms, 4, 256, nullptr, &cps_g);

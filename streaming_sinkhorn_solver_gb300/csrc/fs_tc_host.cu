@@ -20,7 +20,11 @@ struct TcPlan {
     int tps_f, tps_g;           // column tiles per split
 };
 
-// Pick the split count that best fills whole waves of one CTA per SM.
+// Pick the split count that best fills whole waves of one CTA per SM, charging
+// every CTA about two tiles of fixed cost (TMEM allocation, barrier set-up,
+// the Q load, filling and draining its pipeline).
+constexpr double kCtaOverheadTiles = 2.0;
+
 void choose_tc_splits(int64_t row_tiles, int64_t col_tiles, int sms, const fs_options* opt,
                       int* splits, int* tps) {
     if (opt && opt->splits > 0) {
@@ -39,7 +43,8 @@ void choose_tc_splits(int64_t row_tiles, int64_t col_tiles, int sms, const fs_op
         const int64_t spe = (col_tiles + t - 1) / t;
         const int64_t ctas = row_tiles * spe;
         const int64_t waves = (ctas + sms - 1) / sms;
-        const double eff = (double)(row_tiles * col_tiles) / (double)(waves * sms * t);
+        const double eff =
+            (double)(row_tiles * col_tiles) / ((double)(waves * sms) * ((double)t + kCtaOverheadTiles));
         if (eff > best + 0.01) {
             best = eff;
             best_sp = (int)spe;

@@ -59,6 +59,12 @@ WORKLOADS: Dict[str, Workload] = {
         "c2_n10k_d3", 10_000, 10_000, 3, ((0.01, 200),), "barycentric", seed=1002,
         about="X~U[0,1]^3, Y 4-component isotropic GMM (sigma 0.1), uniform weights, "
               "eps=0.01, 200 iterations, barycentric projection P.Y/a"),
+    # The n=m=50,000, d=3 point of the throughput metric: the 10k recipe above
+    # (same distributions, eps and plan operator) at the 50k size.
+    "c2_n50k_d3": Workload(
+        "c2_n50k_d3", 50_000, 50_000, 3, ((0.01, 100),), "barycentric", seed=1006,
+        about="X~U[0,1]^3, Y 4-component isotropic GMM (sigma 0.1), uniform weights, "
+              "eps=0.01, 100 iterations at n=m=50k, barycentric projection P.Y/a"),
     "c3_n50k_d64": Workload(
         "c3_n50k_d64", 50_000, 50_000, 64, ((0.1, 100),), None, seed=1003,
         about="X,Y~N(0,I/d), Y shifted 0.5 along e1, Dirichlet(1) weights, eps=0.1, "

@@ -183,3 +183,29 @@ def test_nonfinite_check_reports():
         fs.fs_sinkhorn_solve(t["X"], t["a"], t["Y"], t["b"], 0.1, 2, None, g, check_finite=True)
     assert ei.value.status == fs.FS_ERR_NONFINITE
     fs.fs_check()
+
+
+def test_full_size_d3_converged_update_on_sampled_rows():
+    """n = m = 50,000, d = 3, in the benchmark's launch configuration: after
+    the workload's 100 iterations, one more warm-started f-update equals the
+    oracle's point-by-point f-update from the GPU's g on 48 sampled rows, and
+    the barycentric projection equals the oracle's on those rows."""
+    w = WORKLOADS["c2_n50k_d3"]
+    inp = make_inputs(w.name)
+    eps, iters = w.stages[0]
+    t = to_dev(inp)
+    f, g = fs.fs_sinkhorn_solve(t["X"], t["a"], t["Y"], t["b"], eps, iters, path="auto")
+    g_prev = np64(g)
+    f1, _ = fs.fs_sinkhorn_solve(t["X"], t["a"], t["Y"], t["b"], eps, 1, f.clone(), g.clone(),
+                                 path="auto")
+    rows = np.random.default_rng(5).choice(w.n, 48, replace=False)
+    rows[:2] = [0, w.n - 1]
+    ref = orc.f_update_rows(inp["X"], inp["Y"], inp["b"], eps, g_prev, rows)
+    cmax = float(np.max(np.sum((inp["X"][rows, None, :].astype(np.float64)
+                                - inp["Y"][None, :, :].astype(np.float64)) ** 2, axis=2)))
+    assert max_abs(np64(f1)[rows], ref) <= F_TOL_FMA * cmax
+    T = fs.fs_barycentric(t["X"], t["a"], t["Y"], t["b"], eps, f, g)
+    f32, g32 = np64(f).astype(np.float32), g_prev.astype(np.float32)
+    PY = orc.apply_plan_rows(inp["X"], inp["a"], inp["Y"], inp["b"], eps, f32, g32, inp["Y"], rows)
+    Tr = PY / inp["a"][rows, None].astype(np.float64)
+    assert rel_l2(np64(T)[rows], Tr) <= APPLY_TOL
