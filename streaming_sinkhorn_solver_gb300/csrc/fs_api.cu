@@ -7,6 +7,7 @@
 // kernels, O((n+m)d) memory) and Method 3 (plan application).
 #include "fs_host.cuh"
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -181,16 +182,34 @@ void timing_end(int slot, int kind, cudaStream_t s) {
     g_timing.kind[slot] = kind;
 }
 
+// Column splits for a grid of row_blocks x splits blocks, per_sm of which
+// are resident on an SM at once.  A block costs its columns plus a fixed
+// overhead (start-up, partial write, its share of the merge) counted in
+// columns; the split count minimising (waves x per-block cost) wins, so a
+// grid that would spill a thin last wave takes fewer, longer blocks.
 int choose_splits(int64_t row_blocks, int64_t nc, int sms, int per_sm, int64_t min_cols,
                   const fs_options* opt, int64_t* cols_per_split) {
+    constexpr double kBlockOverheadCols = 64.0;
     int64_t sp;
     if (opt && opt->splits > 0) {
         sp = opt->splits;
     } else {
-        const int64_t target = (int64_t)sms * per_sm;
-        sp = (target + row_blocks - 1) / row_blocks;
-        const int64_t max_sp = (nc + min_cols - 1) / min_cols;
-        if (sp > max_sp) sp = max_sp;
+        const int64_t slots = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+        int64_t max_sp = (nc + min_cols - 1) / min_cols;
+        max_sp = std::min<int64_t>(max_sp, 4 * ((slots + row_blocks - 1) / row_blocks) + 1);
+        max_sp = std::max<int64_t>(1, std::min<int64_t>(max_sp, 65535));
+        sp = 1;
+        double best = 0.0;
+        for (int64_t s = 1; s <= max_sp; ++s) {
+            const int64_t cps = (nc + s - 1) / s;
+            const int64_t used = (nc + cps - 1) / cps;
+            const int64_t waves = (row_blocks * used + slots - 1) / slots;
+            const double cost = (double)waves * ((double)cps + kBlockOverheadCols);
+            if (s == 1 || cost < best * (1.0 - 1e-9)) {
+                best = cost;
+                sp = used;
+            }
+        }
     }
     if (sp < 1) sp = 1;
     if (sp > nc) sp = nc;

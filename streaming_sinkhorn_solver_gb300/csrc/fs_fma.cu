@@ -18,7 +18,14 @@ namespace fs {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kGroup = 8;     // columns scored before one max/rescale check
+constexpr int kGroup = 8;     // columns scored per max check
+
+// Guarded range of a row's sum S = sum_j 2^{s_ij - M_ref} when the offset is
+// the previous LSE instead of the running max: below 2^-64 the terms that
+// underflowed could matter, above 2^126 the sum could overflow.  Outside the
+// range the row is recomputed with the online max.
+constexpr float kMinRefSum = 5.421010862427522e-20f;   // 2^-64
+constexpr float kMaxRefSum = 8.507059173023462e+37f;   // 2^126
 
 template <int D>
 __device__ __forceinline__ void load_cols(const float4* __restrict__ sc, int j, float (&c)[D + 1]) {
@@ -40,14 +47,26 @@ __device__ __forceinline__ void load_cols(const float4* __restrict__ sc, int j, 
 __host__ __device__ constexpr int fma_dup_stride(int D) { return (2 * (D + 1) + 3) / 4 * 4; }
 __host__ __device__ constexpr int fma_chunk(int D) { return D <= 4 ? 512 : 256; }
 
-// Score G columns starting at shared record j against RP row pairs and fold
-// them into the rows' running max M and sum S of 2^{s - M}.
+// max(m, v[0], ..., v[G-1]) as a depth-2 tree of 3-input maxima.
+template <int G>
+__device__ __forceinline__ float max_tree(const float (&v)[G], float m) {
+    static_assert(G == 1 || G == 8, "group sizes 1 and 8");
+    if constexpr (G == 1) {
+        return fmaxf(m, v[0]);
+    } else {
+        return max3(max3(v[0], v[1], v[2]), max3(v[3], v[4], v[5]), max3(v[6], v[7], m));
+    }
+}
+
+// A row's reference M moves only when its max exceeds M by more than this
+// (log2 units), so terms 2^{s - M} stay below 2^8 and the rescale is rare.
+constexpr float kMaxSlack = 8.f;
+
+// Scores of G columns (shared records j .. j+G-1) against RP row pairs.
 template <int D, int RP, int G>
-__device__ __forceinline__ void fma_group(const float4* __restrict__ sc, int j,
-                                          const uint64_t (&q)[RP][D], float (&M)[2 * RP],
-                                          float (&S)[2 * RP]) {
+__device__ __forceinline__ void fma_scores(const float4* __restrict__ sc, int j,
+                                           const uint64_t (&q)[RP][D], uint64_t (&s)[RP][G]) {
     constexpr int DD = fma_dup_stride(D);
-    uint64_t s[RP][G];
 #pragma unroll
     for (int u = 0; u < G; ++u) {
         const float4* p = sc + (j + u) * (DD / 4);
@@ -66,43 +85,79 @@ __device__ __forceinline__ void fma_group(const float4* __restrict__ sc, int j,
             s[r][u] = acc;
         }
     }
+}
+
+// S[r] += sum_u 2^{s[r][u] - M} (nm = packed -M), summed as a tree.
+template <int RP, int G>
+__device__ __forceinline__ void fma_sum_exp(const uint64_t (&s)[RP][G], const uint64_t (&nm)[RP],
+                                            uint64_t (&S)[RP]) {
 #pragma unroll
     for (int r = 0; r < RP; ++r) {
-        float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int u = 0; u < G; u += 2) {
-            float a0, a1, b0 = -INFINITY, b1 = -INFINITY;
-            upk(s[r][u], a0, a1);
-            if (u + 1 < G) upk(s[r][u + 1], b0, b1);
-            mx0 = max3(mx0, a0, b0);
-            mx1 = max3(mx1, a1, b1);
-        }
-        if (mx0 > M[2 * r]) {
-            S[2 * r] *= ex2(M[2 * r] - mx0);
-            M[2 * r] = mx0;
-        }
-        if (mx1 > M[2 * r + 1]) {
-            S[2 * r + 1] *= ex2(M[2 * r + 1] - mx1);
-            M[2 * r + 1] = mx1;
-        }
-        const uint64_t nm = pk(-M[2 * r], -M[2 * r + 1]);
-        uint64_t acc = pk(0.f, 0.f);
+        uint64_t e[G];
 #pragma unroll
         for (int u = 0; u < G; ++u) {
             float x0, x1;
-            upk(add2(s[r][u], nm), x0, x1);
-            acc = add2(acc, pk(ex2(x0), ex2(x1)));
+            upk(add2(s[r][u], nm[r]), x0, x1);
+            e[u] = pk(ex2(x0), ex2(x1));
         }
-        float e0, e1;
-        upk(acc, e0, e1);
-        S[2 * r] += e0;
-        S[2 * r + 1] += e1;
+#pragma unroll
+        for (int w = 1; w < G; w *= 2) {
+#pragma unroll
+            for (int u = 0; u + w < G; u += 2 * w) e[u] = add2(e[u], e[u + w]);
+        }
+        S[r] = add2(S[r], e[0]);
     }
 }
 
-// RP row pairs per thread: rows row0 + tid + i * kThreads, i < 2 RP.
-template <int D, int RP>
-__global__ void __launch_bounds__(kThreads) k_half_fma(HalfArgs a) {
+// Online fold of G scores per row into (M, S): S = sum 2^{s - M}.  Mt = M +
+// slack is the threshold a new max must pass to move M; nm holds the packed
+// -M of each row pair.  The check is warp-uniform, so the rescale branch
+// never diverges.
+template <int RP, int G>
+__device__ __forceinline__ void fma_fold(const uint64_t (&s)[RP][G], float (&M)[2 * RP],
+                                         float (&Mt)[2 * RP], uint64_t (&nm)[RP],
+                                         uint64_t (&S)[RP]) {
+    float m[2 * RP];
+    bool grow = false;
+#pragma unroll
+    for (int r = 0; r < RP; ++r) {
+        float lo[G], hi[G];
+#pragma unroll
+        for (int u = 0; u < G; ++u) upk(s[r][u], lo[u], hi[u]);
+        m[2 * r] = max_tree<G>(lo, Mt[2 * r]);
+        m[2 * r + 1] = max_tree<G>(hi, Mt[2 * r + 1]);
+        grow |= (m[2 * r] > Mt[2 * r]) | (m[2 * r + 1] > Mt[2 * r + 1]);
+    }
+    if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+        for (int i = 0; i < 2 * RP; ++i) {
+            const float n = m[i] > Mt[i] ? m[i] : M[i];
+            m[i] = ex2(M[i] - n);   // rescale factor (1 where M stays)
+            M[i] = n;
+            Mt[i] = n + kMaxSlack;
+        }
+#pragma unroll
+        for (int r = 0; r < RP; ++r) {
+            S[r] = fma2(S[r], pk(m[2 * r], m[2 * r + 1]), pk(0.f, 0.f));
+            nm[r] = pk(-M[2 * r], -M[2 * r + 1]);
+        }
+    }
+    fma_sum_exp<RP, G>(s, nm, S);
+}
+
+// Append `row` to the list of rows the fixup kernel recomputes.
+__device__ __forceinline__ void push_fix(const HalfArgs& a, int64_t row) {
+    const unsigned int slot = atomicAdd(&a.fix_count[0], 1u);
+    if (slot < (unsigned int)a.nr) a.fix_list[slot] = (int)row;
+}
+
+// Half-update, RP row pairs per thread (rows row0 + tid + i * kThreads,
+// i < 2 RP).  REF = false: online max.  REF = true: each row's offset is the
+// LSE of its previous half-update, log2 w_i - (bias slot), so no max is
+// tracked; the sum is range-checked at the end (here when the split is the
+// whole row, else in the merge).
+template <int D, int RP, bool REF>
+__global__ void __launch_bounds__(kThreads, D <= 8 ? 3 : 2) k_half_fma(HalfArgs a) {
     constexpr int DS = fma_stride(D);
     constexpr int DD = fma_dup_stride(D);
     constexpr int CH = fma_chunk(D);
@@ -115,7 +170,8 @@ __global__ void __launch_bounds__(kThreads) k_half_fma(HalfArgs a) {
     const int64_t c1 = min(a.nc, c0 + a.cols_per_split);
 
     uint64_t q[RP][D];
-    float M[RPT], S[RPT];
+    float M[RPT], Mt[RPT];
+    uint64_t S[RP], nm[RP];
 #pragma unroll
     for (int r = 0; r < RP; ++r) {
         int64_t ra = row0 + tid + (2 * r) * kThreads, rb = ra + kThreads;
@@ -124,11 +180,15 @@ __global__ void __launch_bounds__(kThreads) k_half_fma(HalfArgs a) {
 #pragma unroll
         for (int k = 0; k < D; ++k)
             q[r][k] = pk(a.rows[ra * DS + k] * a.kappa, a.rows[rb * DS + k] * a.kappa);
-    }
-#pragma unroll
-    for (int i = 0; i < RPT; ++i) {
-        M[i] = -INFINITY;
-        S[i] = 0.f;
+        if (REF) {
+            M[2 * r] = a.rlogw2[ra] - a.rows[ra * DS + D];
+            M[2 * r + 1] = a.rlogw2[rb] - a.rows[rb * DS + D];
+        } else {
+            M[2 * r] = M[2 * r + 1] = -INFINITY;
+        }
+        Mt[2 * r] = Mt[2 * r + 1] = -INFINITY;
+        S[r] = pk(0.f, 0.f);
+        nm[r] = REF ? pk(-M[2 * r], -M[2 * r + 1]) : pk(INFINITY, INFINITY);
     }
 
     float* sf = reinterpret_cast<float*>(sc);
@@ -144,18 +204,32 @@ __global__ void __launch_bounds__(kThreads) k_half_fma(HalfArgs a) {
         }
         __syncthreads();
         int j = 0;
-        for (; j + kGroup <= ncol; j += kGroup) fma_group<D, RP, kGroup>(sc, j, q, M, S);
-        for (; j < ncol; ++j) fma_group<D, RP, 1>(sc, j, q, M, S);
+        for (; j + kGroup <= ncol; j += kGroup) {
+            uint64_t s[RP][kGroup];
+            fma_scores<D, RP, kGroup>(sc, j, q, s);
+            if (REF) fma_sum_exp<RP, kGroup>(s, nm, S);
+            else fma_fold<RP, kGroup>(s, M, Mt, nm, S);
+        }
+        for (; j < ncol; ++j) {
+            uint64_t s[RP][1];
+            fma_scores<D, RP, 1>(sc, j, q, s);
+            if (REF) fma_sum_exp<RP, 1>(s, nm, S);
+            else fma_fold<RP, 1>(s, M, Mt, nm, S);
+        }
     }
 
+    float Sf[RPT];
+#pragma unroll
+    for (int r = 0; r < RP; ++r) upk(S[r], Sf[2 * r], Sf[2 * r + 1]);
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
         const int64_t row = row0 + tid + i * kThreads;
         if (row >= a.nr) continue;
         if (a.splits > 1) {
-            a.partial[(int64_t)blockIdx.y * a.nr + row] = make_float2(M[i], S[i]);
+            a.partial[(int64_t)blockIdx.y * a.nr + row] = make_float2(M[i], Sf[i]);
         } else {
-            const float lse2 = M[i] + log2f(S[i]);
+            if (REF && !(Sf[i] >= kMinRefSum && Sf[i] <= kMaxRefSum)) push_fix(a, row);
+            const float lse2 = M[i] + log2f(Sf[i]);
             a.pot[row] = a.rnorm[row] - a.eps_ln2 * lse2;
             a.rows[row * DS + D] = a.rlogw2[row] - lse2;
         }
@@ -168,7 +242,8 @@ cudaError_t launch_half_fma_t(const HalfArgs& a, cudaStream_t s) {
     const int64_t rows_per_block = (int64_t)kThreads * 2 * RP;
     static_assert(kThreads * 2 * RP == fma_rows_per_block(D), "row blocking");
     dim3 grid((unsigned)((a.nr + rows_per_block - 1) / rows_per_block), (unsigned)a.splits);
-    k_half_fma<D, RP><<<grid, kThreads, 0, s>>>(a);
+    if (a.use_ref) k_half_fma<D, RP, true><<<grid, kThreads, 0, s>>>(a);
+    else k_half_fma<D, RP, false><<<grid, kThreads, 0, s>>>(a);
     count_launch();
     return cudaGetLastError();
 }
@@ -176,7 +251,8 @@ cudaError_t launch_half_fma_t(const HalfArgs& a, cudaStream_t s) {
 __global__ void k_merge_lse(const float2* __restrict__ partial, int splits, int64_t nr,
                             const float* __restrict__ rnorm, const float* __restrict__ rlogw2,
                             float eps_ln2, float* __restrict__ pot, float* __restrict__ bias,
-                            int64_t bias_stride) {
+                            int64_t bias_stride, int* __restrict__ fix_list,
+                            unsigned int* __restrict__ fix_count) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= nr) return;
     float M = -INFINITY;
@@ -186,6 +262,10 @@ __global__ void k_merge_lse(const float2* __restrict__ partial, int splits, int6
         const float2 p = partial[(int64_t)sp * nr + i];
         if (p.x != -INFINITY) S += p.y * ex2(p.x - M);   // a padding-only split adds nothing
     }
+    if (fix_list != nullptr && !(S >= kMinRefSum && S <= kMaxRefSum)) {
+        const unsigned int slot = atomicAdd(&fix_count[0], 1u);
+        if (slot < (unsigned int)nr) fix_list[slot] = (int)i;
+    }
     const float lse2 = M + log2f(S);
     if (rnorm == nullptr) {  // log2-sum-exp only (pre-pass of plan application)
         pot[i] = lse2;
@@ -193,6 +273,69 @@ __global__ void k_merge_lse(const float2* __restrict__ partial, int splits, int6
     }
     pot[i] = rnorm[i] - eps_ln2 * lse2;
     bias[i * bias_stride] = rlogw2[i] - lse2;
+}
+
+// Recompute, with the online max, the rows listed by a guarded half-update:
+// one warp per listed row, lanes striding over all columns, then a shuffle
+// merge of the lanes' (max, sum).  The list length is read once per block;
+// the last block to finish resets the list for the next half-update.
+constexpr int kFixBlocks = 64;
+
+template <int D>
+__global__ void __launch_bounds__(256) k_fix_fma(HalfArgs a) {
+    constexpr int DS = fma_stride(D);
+    __shared__ unsigned int s_cnt;
+    if (threadIdx.x == 0) s_cnt = min(*(volatile unsigned int*)&a.fix_count[0], (unsigned int)a.nr);
+    __syncthreads();
+    const unsigned int cnt = s_cnt;
+    const int lane = threadIdx.x & 31;
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    for (unsigned int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < cnt; w += warps) {
+        const int64_t row = a.fix_list[w];
+        float q[D];
+#pragma unroll
+        for (int k = 0; k < D; ++k) q[k] = a.rows[row * DS + k] * a.kappa;
+        float M = -INFINITY, S = 0.f;
+        for (int64_t j = lane; j < a.nc; j += 32) {
+            float s = a.cols[j * DS + D];
+#pragma unroll
+            for (int k = 0; k < D; ++k) s = fmaf(q[k], a.cols[j * DS + k], s);
+            if (s > M) {
+                S *= ex2(M - s);
+                M = s;
+            }
+            S += ex2(s - M);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float Mo = __shfl_xor_sync(0xffffffffu, M, o);
+            const float So = __shfl_xor_sync(0xffffffffu, S, o);
+            const float Mn = fmaxf(M, Mo);
+            S = (M == -INFINITY ? 0.f : S * ex2(M - Mn)) + (Mo == -INFINITY ? 0.f : So * ex2(Mo - Mn));
+            M = Mn;
+        }
+        if (lane == 0) {
+            const float lse2 = M + log2f(S);
+            a.pot[row] = a.rnorm[row] - a.eps_ln2 * lse2;
+            a.rows[row * DS + D] = a.rlogw2[row] - lse2;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(&a.fix_count[1], 1u) == gridDim.x - 1) {
+            a.fix_count[0] = 0;
+            a.fix_count[1] = 0;
+            __threadfence();
+        }
+    }
+}
+
+template <int D>
+cudaError_t launch_fix_fma_t(const HalfArgs& a, cudaStream_t s) {
+    k_fix_fma<D><<<kFixBlocks, 256, 0, s>>>(a);
+    count_launch();
+    return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
@@ -322,13 +465,50 @@ cudaError_t launch_half_fma(int D, const HalfArgs& a, cudaStream_t s) {
     }
 }
 
+namespace {
+template <int D>
+int half_fma_residency() {
+    static std::atomic<int> cached{0};
+    int v = cached.load(std::memory_order_relaxed);
+    if (v == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, k_half_fma<D, fma_row_pairs(D), true>,
+                                                          kThreads, 0) != cudaSuccess || v < 1)
+            v = 1;
+        cached.store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+}  // namespace
+
+int fma_half_blocks_per_sm(int D) {
+    switch (D) {
+        case 2: return half_fma_residency<2>();
+        case 3: return half_fma_residency<3>();
+        case 4: return half_fma_residency<4>();
+        case 8: return half_fma_residency<8>();
+        default: return half_fma_residency<16>();
+    }
+}
+
 cudaError_t launch_merge_lse(const float2* partial, int splits, int64_t nr, const float* rnorm,
                              const float* rlogw2, float eps_ln2, float* pot, float* bias,
-                             int64_t bias_stride, cudaStream_t s) {
-    k_merge_lse<<<(unsigned)((nr + 255) / 256), 256, 0, s>>>(partial, splits, nr, rnorm, rlogw2,
-                                                             eps_ln2, pot, bias, bias_stride);
+                             int64_t bias_stride, cudaStream_t s, int* fix_list,
+                             unsigned int* fix_count) {
+    k_merge_lse<<<(unsigned)((nr + 255) / 256), 256, 0, s>>>(
+        partial, splits, nr, rnorm, rlogw2, eps_ln2, pot, bias, bias_stride, fix_list, fix_count);
     count_launch();
     return cudaGetLastError();
+}
+
+cudaError_t launch_fix_fma(int D, const HalfArgs& a, cudaStream_t s) {
+    switch (D) {
+        case 2: return launch_fix_fma_t<2>(a, s);
+        case 3: return launch_fix_fma_t<3>(a, s);
+        case 4: return launch_fix_fma_t<4>(a, s);
+        case 8: return launch_fix_fma_t<8>(a, s);
+        case 16: return launch_fix_fma_t<16>(a, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_apply_fma(int D, const ApplyArgs& a, cudaStream_t s) {

@@ -19,14 +19,23 @@ FmaPlan plan_fma(int64_t n, int64_t m, int32_t d, int sms, const fs_options* opt
     p.D = fma_pad_dim(d);
     p.DS = fma_stride(p.D);
     const int64_t rows_per_block = fma_rows_per_block(p.D);
-    p.splits_f = choose_splits((n + rows_per_block - 1) / rows_per_block, m, sms, 4, 256, opt, &p.cps_f);
-    p.splits_g = choose_splits((m + rows_per_block - 1) / rows_per_block, n, sms, 4, 256, opt, &p.cps_g);
+    const int per_sm = fma_half_blocks_per_sm(p.D);
+    p.splits_f = choose_splits((n + rows_per_block - 1) / rows_per_block, m, sms, per_sm, 128, opt,
+                               &p.cps_f);
+    p.splits_g = choose_splits((m + rows_per_block - 1) / rows_per_block, n, sms, per_sm, 128, opt,
+                               &p.cps_g);
     return p;
 }
 
 struct FmaBufs {
-    size_t shift_part, shift, PX, PY, nx, ny, lax, lby, partial, phi, apply_part, counter;
+    size_t shift_part, shift, PX, PY, nx, ny, lax, lby, partial, phi, apply_part, counter, fix_list,
+        fix_count;
 };
+
+// Problems from this many score pairs up use reference offsets after the
+// first iteration: below it the fixup launch costs more than the online max.
+constexpr double kRefMinPairs = 67108864.0;   // 2^26
+constexpr int kOnlineIters = 2;
 
 void layout_fma(Layout& L, FmaBufs& B, int64_t n, int64_t m, int32_t d, const FmaPlan& p,
                 int apply_k, int apply_splits) {
@@ -44,6 +53,8 @@ void layout_fma(Layout& L, FmaBufs& B, int64_t n, int64_t m, int32_t d, const Fm
     B.apply_part =
         apply_splits > 1 ? L.take(sizeof(float) * (size_t)apply_splits * n * (apply_k + 1)) : 0;
     B.counter = L.take(sizeof(unsigned int) * 4);
+    B.fix_list = L.take(sizeof(int) * (size_t)std::max(n, m));
+    B.fix_count = L.take(sizeof(unsigned int) * 2);
 }
 
 int apply_splits_for(int64_t n, int64_t m, int32_t k, int sms, const fs_options* opt, int64_t* cps) {
@@ -95,21 +106,35 @@ fs_status solve_fma(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) 
     FS_CUDA(launch_pack_fma(P.Y.dev, P.b.dev, P.g.dev, m, d, p.D, shift, l_over_eps, PY, ny, lby,
                             c.stream));
 
-    HalfArgs hf{PX, PY, n, m, kappa, eps_ln2, nx, lax, P.f.dev, part, p.splits_f, p.cps_f};
-    HalfArgs hg{PY, PX, m, n, kappa, eps_ln2, ny, lby, P.g.dev, part, p.splits_g, p.cps_g};
+    int* fix_list = c.at<int>(B.fix_list);
+    unsigned int* fix_count = c.at<unsigned int>(B.fix_count);
+    FS_CUDA(cudaMemsetAsync(fix_count, 0, 2 * sizeof(unsigned int), c.stream));
+    HalfArgs hf{PX, PY, n, m, kappa, eps_ln2, nx, lax, P.f.dev, part, p.splits_f, p.cps_f,
+                0, fix_list, fix_count};
+    HalfArgs hg{PY, PX, m, n, kappa, eps_ln2, ny, lby, P.g.dev, part, p.splits_g, p.cps_g,
+                0, fix_list, fix_count};
+    // The first iterations take the online max: the initial potentials may be
+    // arbitrary and the first updates move the LSEs by large amounts.  Later
+    // ones use reference offsets, with a guarded sum and a fixup of the rows
+    // that fail it.
+    const bool ref_ok = (double)n * (double)m >= kRefMinPairs;
+    auto half = [&](HalfArgs& h, int splits, int64_t nr, const float* rnorm, const float* rlogw2,
+                    float* pot, float* packed, bool ref) -> fs_status {
+        h.use_ref = ref ? 1 : 0;
+        const int ts = timing_begin(c.stream);
+        FS_CUDA(launch_half_fma(p.D, h, c.stream));
+        timing_end(ts, TIME_HALF, c.stream);
+        if (splits > 1)
+            FS_CUDA(launch_merge_lse(part, splits, nr, rnorm, rlogw2, eps_ln2, pot, packed + p.D,
+                                     p.DS, c.stream, ref ? fix_list : nullptr,
+                                     ref ? fix_count : nullptr));
+        if (ref) FS_CUDA(launch_fix_fma(p.D, h, c.stream));
+        return FS_OK;
+    };
     for (int32_t it = 0; it < n_iter; ++it) {
-        int ts = timing_begin(c.stream);
-        FS_CUDA(launch_half_fma(p.D, hf, c.stream));
-        timing_end(ts, TIME_HALF, c.stream);
-        if (p.splits_f > 1)
-            FS_CUDA(launch_merge_lse(part, p.splits_f, n, nx, lax, eps_ln2, P.f.dev, PX + p.D, p.DS,
-                                     c.stream));
-        ts = timing_begin(c.stream);
-        FS_CUDA(launch_half_fma(p.D, hg, c.stream));
-        timing_end(ts, TIME_HALF, c.stream);
-        if (p.splits_g > 1)
-            FS_CUDA(launch_merge_lse(part, p.splits_g, m, ny, lby, eps_ln2, P.g.dev, PY + p.D, p.DS,
-                                     c.stream));
+        const bool ref = ref_ok && it >= kOnlineIters;
+        FS_TRY(half(hf, p.splits_f, n, nx, lax, P.f.dev, PX, ref));
+        FS_TRY(half(hg, p.splits_g, m, ny, lby, P.g.dev, PY, ref));
     }
     if (opt && opt->check_finite) {
         FS_TRY(scan_finite(c, P.f.dev, n, c.at<unsigned int>(B.counter)));

@@ -101,14 +101,28 @@ struct HalfArgs {
     float2* partial;        // [splits x nr] or nullptr
     int splits;
     int64_t cols_per_split;
+    // Reference offsets: with use_ref set, each row's exponent offset is the
+    // LSE of its previous half-update (log2 w_i minus its bias slot) instead
+    // of an online max; rows whose sum leaves the guarded range are appended
+    // to fix_list (fix_count[0] entries) for launch_fix_fma.
+    int use_ref;
+    int* fix_list;            // [nr]
+    unsigned int* fix_count;  // [2], zero before the first guarded half-update
 };
 cudaError_t launch_half_fma(int D, const HalfArgs& a, cudaStream_t s);
+// Recompute the listed rows with the online max; resets the list.
+cudaError_t launch_fix_fma(int D, const HalfArgs& a, cudaStream_t s);
+// Blocks of the half-update kernel for padded dimension D resident per SM.
+int fma_half_blocks_per_sm(int D);
 
 // Merge of split partials: LSE2 = M + log2 sum_s S_s 2^{M_s - M} in split
 // order, then pot = rnorm - eps ln2 LSE2 and bias = rlogw2 - LSE2.
+// With fix_list set, rows whose merged sum leaves the guarded range of a
+// reference-offset half-update are appended to it.
 cudaError_t launch_merge_lse(const float2* partial, int splits, int64_t nr, const float* rnorm,
                              const float* rlogw2, float eps_ln2, float* pot, float* bias,
-                             int64_t bias_stride, cudaStream_t s);
+                             int64_t bias_stride, cudaStream_t s, int* fix_list = nullptr,
+                             unsigned int* fix_count = nullptr);
 
 // Plan application on the FMA path.
 enum ApplyMode : int { APPLY_PV = 0, APPLY_BARY = 1, APPLY_GRAD = 2 };

@@ -121,8 +121,11 @@ fs_status solve_noalloc(const float* X, const float* a, int64_t n, const float* 
     const int DS = fma_stride(D);
     const int64_t rows_per_block = fma_rows_per_block(D);
     int64_t cps_f, cps_g;
-    int sp_f = choose_splits((n + rows_per_block - 1) / rows_per_block, m, sc->sms, 4, 256, nullptr, &cps_f);
-    int sp_g = choose_splits((m + rows_per_block - 1) / rows_per_block, n, sc->sms, 4, 256, nullptr, &cps_g);
+    const int per_sm = fma_half_blocks_per_sm(D);
+    int sp_f = choose_splits((n + rows_per_block - 1) / rows_per_block, m, sc->sms, per_sm, 128, nullptr,
+                             &cps_f);
+    int sp_g = choose_splits((m + rows_per_block - 1) / rows_per_block, n, sc->sms, per_sm, 128, nullptr,
+                             &cps_g);
     if (sp_f > kNoAllocMaxSplits) {
         cps_f = (m + kNoAllocMaxSplits - 1) / kNoAllocMaxSplits;
         sp_f = (int)((m + cps_f - 1) / cps_f);

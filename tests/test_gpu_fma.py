@@ -209,3 +209,15 @@ def test_full_size_d3_converged_update_on_sampled_rows():
     PY = orc.apply_plan_rows(inp["X"], inp["a"], inp["Y"], inp["b"], eps, f32, g32, inp["Y"], rows)
     Tr = PY / inp["a"][rows, None].astype(np.float64)
     assert rel_l2(np64(T)[rows], Tr) <= APPLY_TOL
+
+
+@pytest.mark.parametrize("eps,iters", [(0.005, 6), (0.05, 12)])
+def test_reference_offset_path_with_fixups(eps, iters):
+    """n*m = 2^26 takes reference offsets after the first iterations; a cold
+    start at small eps moves the LSEs by hundreds of log2 units between
+    iterations, so many rows fail the guarded range and are recomputed by the
+    fixup kernel.  The potentials must still match the oracle."""
+    inp = make_inputs("c2_n10k_d3", n=8192, m=8192, seed=91)
+    f, g, fr, gr, C, _ = _solve_both(inp, eps, iters, path="auto")
+    assert max_abs(f, fr) <= F_TOL_FMA * C.max()
+    assert max_abs(g, gr) <= F_TOL_FMA * C.max()
