@@ -35,9 +35,19 @@ from streaming_sinkhorn_solver_gb300.workloads import WORKLOADS, make_inputs  # 
 METRIC = "Sinkhorn iters/s and score-pairs/s at n=m=50k (d=3/64/512); % of roofline"
 DEFAULT_WORKLOAD = "c4_n50k_d512"
 PROFILES = os.path.join(ROOT, "profiles")
-# ex2 issue rate of the special-function units on sm_103 (per SM per clock);
-# the ALU roofline is this times the SM count times the SM clock.
+# ex2 rate of the special-function units on sm_103 (per SM per clock, measured)
+# and the FP32 lanes per SM per clock; the ALU roofline is the slower of the
+# two limits, times the SM count and the SM clock.
 EX2_PER_CLK_SM = 32
+FP32_LANES_PER_CLK_SM = 128
+
+
+def fp32_ops_per_pair(d: int, tensor_path: bool) -> int:
+    """FP32 lane-ops one score pair needs at the least: on the FMA path d
+    fused multiply-adds (the bias is the chain's first addend), one offset
+    subtraction and one accumulation; on the tensor path the dot product is
+    on the tensor pipe and the epilogue keeps the subtraction and the sum."""
+    return 2 if tensor_path else d + 2
 
 
 def _rank_info():
@@ -307,11 +317,14 @@ def run_gb300(args, w):
     clk = (clocks or {}).get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     ex2_peak = EX2_PER_CLK_SM * sms * clk * 1e6                       # ex2 / s
+    fp32_ops = fp32_ops_per_pair(d, tensor_path)
+    fp32_pair_peak = FP32_LANES_PER_CLK_SM / fp32_ops * sms * clk * 1e6  # pairs / s
     tflops_peak = float(peaks["bf16_tflops_sustained"])
     hbm_peak = float(peaks["hbm_gbs"])
     op_bytes = 2 if tensor_path else 4
     alg_bytes = op_bytes * (n + m) * d + 4 * 3 * (n + m)                # operands + biases/outputs
-    terms = {"alu_s": pairs_per_half / ex2_peak, "hbm_s": alg_bytes / (hbm_peak * 1e9)}
+    alu_peak = min(ex2_peak, fp32_pair_peak)                           # pairs / s
+    terms = {"alu_s": pairs_per_half / alu_peak, "hbm_s": alg_bytes / (hbm_peak * 1e9)}
     if tensor_path:
         terms["tensor_s"] = 2.0 * pairs_per_half * d / (tflops_peak * 1e12)
     bound = max(terms, key=terms.get)[:-2]
@@ -322,9 +335,14 @@ def run_gb300(args, w):
                                f"same nominal rate"}
     elif bound == "alu":
         achieved = pairs_per_half / t_launch / 1e9
-        roof = {"bound": "alu", "achieved": achieved, "peak": ex2_peak / 1e9, "unit": "Gex2/s",
-                "peak_source": f"derived: {EX2_PER_CLK_SM} ex2/clk/SM x {sms} SMs x {clk:.0f} MHz "
-                               f"(median SM clock sampled in the timed region)"}
+        per_clk = min(EX2_PER_CLK_SM, FP32_LANES_PER_CLK_SM / fp32_ops)
+        roof = {"bound": "alu", "achieved": achieved, "peak": alu_peak / 1e9, "unit": "Gpair/s",
+                "peak_source": f"derived: min(MUFU {EX2_PER_CLK_SM} ex2/clk/SM, FP32 "
+                               f"{FP32_LANES_PER_CLK_SM} lanes/clk/SM / {fp32_ops} lane-ops per "
+                               f"pair) = {per_clk:.1f} pairs/clk/SM x {sms} SMs x {clk:.0f} MHz "
+                               f"(median SM clock sampled in the timed region)",
+                "mufu_frac": achieved * 1e9 / ex2_peak,
+                "fp32_frac": achieved * 1e9 / fp32_pair_peak}
     else:
         achieved = alg_bytes / t_launch / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",

@@ -14,6 +14,11 @@ namespace fs {
 namespace tc {
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;   // any single wait: 2 s
+// Suspend-time hint of every try_wait: a waiting thread sleeps until the phase
+// completes (or this long) instead of returning at once and spinning, which
+// took issue slots from the producer and MMA threads on the same SM
+// sub-partition (measured on sm_103a).
+constexpr uint32_t kSuspendHintNs = 1000000u;
 
 // byte offset of element (r, e) of a 128 x 64 chunk in the K-major
 // 128-byte-swizzled layout: row r occupies bytes [128 r, 128 r + 128); its
@@ -80,11 +85,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // runs at full rate.
 #define FS_MBAR_WAIT_PTX(SEM)                                                     \
     "{\n\t.reg .pred p;\n\t.reg .u64 t0, t;\n\t"                                  \
-    "mbarrier.try_wait.parity" SEM ".shared::cta.b64 p, [%1], %2;\n\t"            \
+    "mbarrier.try_wait.parity" SEM ".shared::cta.b64 p, [%1], %2, %4;\n\t"        \
     "@p bra.uni LAB_DONE;\n\t"                                                    \
     "mov.u64 t0, %%globaltimer;\n"                                                \
     "LAB_WAIT:\n\t"                                                               \
-    "mbarrier.try_wait.parity" SEM ".shared::cta.b64 p, [%1], %2;\n\t"            \
+    "mbarrier.try_wait.parity" SEM ".shared::cta.b64 p, [%1], %2, %4;\n\t"        \
     "@p bra.uni LAB_DONE;\n\t"                                                    \
     "mov.u64 t, %%globaltimer;\n\t"                                               \
     "sub.u64 t, t, t0;\n\t"                                                       \
@@ -101,7 +106,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
     uint32_t ok;
     asm volatile(FS_MBAR_WAIT_PTX("")
                  : "=r"(ok)
-                 : "r"(smem_u32(bar)), "r"(parity), "l"(kTimeoutNs)
+                 : "r"(smem_u32(bar)), "r"(parity), "l"(kTimeoutNs), "r"(kSuspendHintNs)
                  : "memory");
     if (!ok) atomicOr(err, code);
     return ok != 0;
@@ -179,6 +184,30 @@ __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Order later uses of v after a tcgen05.wait::ld: the empty asm statements
+// (volatile, so they stay after the wait) redefine every register of v.
+template <int N>
+__device__ __forceinline__ void tmem_reg_fence(float (&v)[N]) {
+    static_assert(N % 8 == 0, "multiples of 8 registers");
+#pragma unroll
+    for (int i = 0; i < N; i += 8)
+        asm volatile("" : "+f"(v[i]), "+f"(v[i + 1]), "+f"(v[i + 2]), "+f"(v[i + 3]), "+f"(v[i + 4]),
+                     "+f"(v[i + 5]), "+f"(v[i + 6]), "+f"(v[i + 7]));
+}
+
+// warp: the same value x into 32 consecutive columns of the warp's 32 lanes
+__device__ __forceinline__ void tmem_fill32(uint32_t taddr, float x) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, "
+        "%1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1};" ::"r"(taddr),
+        "f"(x)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // --- CTA pairs (cluster of 2, tcgen05 cta_group::2) ---------------------------
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -217,7 +246,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     uint32_t ok;
     asm volatile(FS_MBAR_WAIT_PTX(".acquire.cluster")
                  : "=r"(ok)
-                 : "r"(smem_u32(bar)), "r"(parity), "l"(kTimeoutNs)
+                 : "r"(smem_u32(bar)), "r"(parity), "l"(kTimeoutNs), "r"(kSuspendHintNs)
                  : "memory");
     if (!ok) atomicOr(err, code);
     return ok != 0;

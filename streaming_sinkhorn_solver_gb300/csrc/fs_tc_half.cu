@@ -10,16 +10,25 @@
 // One CTA owns a 128-row tile of Q and a range of 128-column tiles of K.
 //   warp 0     producer: Q once (resident in shared memory up to d = 512,
 //              otherwise streamed beside K), then for every column tile its
-//              512-byte bias slice and its K chunks (128 x 64 fp16, 16 KB,
-//              pre-swizzled in HBM) into a ring sized to the free space, all
-//              with cp.async.bulk;
+//              512-byte bias slice (a ring of 16) and its K chunks (128 x 64
+//              fp16, 16 KB, pre-swizzled in HBM) into a ring sized to the free
+//              space, all with cp.async.bulk;
 //   warp 1     one thread issues tcgen05.mma (M = 128, N = 128, K = 16 steps)
 //              into TMEM buffer t mod 4;
-//   warps 2-9  two epilogue groups of four warps, tile t going to group
-//              t mod 2; a thread owns one row: it reads its 128 scores from
-//              TMEM, forms s = acc kappa' + bias (packed f32x2 FMA), and
-//              folds them into the row's running max M and sum S of 2^{s-M}.
-// At the end the two groups' (M, S) are merged in a fixed order and the row
+//   warps 2-   epilogue groups of four warps, tile t going to group t mod G;
+//              a thread owns one row.
+// Two epilogue modes:
+//   online     (G = 2) the thread reads its 128 scores, forms s = acc kappa'
+//              + bias (packed f32x2 FMA) and folds them into the row's running
+//              max M and sum S of 2^{s-M};
+//   reference  (G = 4, one group per TMEM buffer) the row's offset M is its
+//              LSE from the previous half-update.  The group pre-loads every
+//              accumulator column of its buffer with -M / kappa' (tcgen05.st),
+//              the MMAs accumulate onto it, and the epilogue only forms
+//              2^{acc kappa' + bias} and sums it, 32 columns at a time, the
+//              next slice's TMEM load in flight.  The sum is range-checked at
+//              the end; a row outside the range is recomputed later.
+// At the end the groups' (M, S) are merged in a fixed order and the row
 // potential and next bias are written (or (M, S) partials per split).
 #include "fs_tc.cuh"
 
@@ -29,14 +38,35 @@ namespace tc {
 namespace {
 
 constexpr int kBiasBytes = BN * 4;
+// Bias slices in flight: deeper than the K ring (in tiles), so the producer's
+// wait for a free bias slot never holds back the next K chunks.
+constexpr int kBiasSlots = 16;
+constexpr int kMaxGroups = kRefGroups > kHalfGroups ? kRefGroups : kHalfGroups;
 
 __host__ __device__ constexpr int half_fixed_bytes(int nch, bool qres) {
-    return 1024 /* alignment slack */ + (qres ? nch * CHUNK_BYTES : 0) + kTmemBufs * kBiasBytes +
-           BM * 8 /* group merge */ + 8 * (2 * kMaxStages + 4 * kTmemBufs + 2) + 16;
+    return 1024 /* alignment slack */ + (qres ? nch * CHUNK_BYTES : 0) + kBiasSlots * kBiasBytes +
+           BM * 8 * (kMaxGroups - 1) /* group merge */ +
+           8 * (2 * kMaxStages + 2 * kTmemBufs + 2 * kBiasSlots + 2) + 16;
 }
 
+template <int GROUPS>
 __device__ __forceinline__ void epi_bar_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kHalfGroups * kEpiWarps * 32) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(GROUPS * kEpiWarps * 32) : "memory");
+}
+
+// One 32-column slice in reference mode: acc[] += 2^{v kappa' + bias}
+// (bias already holds the row offset through the accumulator pre-load).
+__device__ __forceinline__ void ref_slice(const float (&v)[32], const float4* __restrict__ sb,
+                                          uint64_t ks2, uint64_t (&acc)[4]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 bb = sb[q];
+        float x0, x1, x2, x3;
+        upk(fma2(pk(v[4 * q], v[4 * q + 1]), ks2, pk(bb.x, bb.y)), x0, x1);
+        upk(fma2(pk(v[4 * q + 2], v[4 * q + 3]), ks2, pk(bb.z, bb.w)), x2, x3);
+        acc[(2 * q) & 3] = add2(acc[(2 * q) & 3], pk(ex2(x0), ex2(x1)));
+        acc[(2 * q + 1) & 3] = add2(acc[(2 * q + 1) & 3], pk(ex2(x2), ex2(x3)));
+    }
 }
 
 }  // namespace
@@ -52,8 +82,10 @@ size_t half_smem_bytes(int nch, bool qres, int stages) {
     return (size_t)half_fixed_bytes(nch, qres) + (size_t)stages * stage;
 }
 
-template <bool QRES>
-__global__ void __launch_bounds__(kHalfThreads, 1) k_half_tc(TcHalfArgs a) {
+template <bool QRES, bool REF>
+__global__ void __launch_bounds__(half_threads(REF), 1) k_half_tc(TcHalfArgs a) {
+    constexpr int GROUPS = REF ? kRefGroups : kHalfGroups;
+    static_assert(!REF || GROUPS == kTmemBufs, "reference mode: one group per TMEM buffer");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -70,14 +102,14 @@ __global__ void __launch_bounds__(kHalfThreads, 1) k_half_tc(TcHalfArgs a) {
     uint8_t* sQ = smem;
     uint8_t* sStage = smem + (QRES ? nch * CHUNK_BYTES : 0);
     uint8_t* sBias = sStage + stages * STAGE_BYTES;
-    float2* sMerge = reinterpret_cast<float2*>(sBias + kTmemBufs * kBiasBytes);
-    uint64_t* full = reinterpret_cast<uint64_t*>(sMerge + BM);
+    float2* sMerge = reinterpret_cast<float2*>(sBias + kBiasSlots * kBiasBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sMerge + BM * (kMaxGroups - 1));
     uint64_t* empty = full + kMaxStages;
     uint64_t* tfull = empty + kMaxStages;
     uint64_t* tempty = tfull + kTmemBufs;
     uint64_t* bfull = tempty + kTmemBufs;
-    uint64_t* bempty = bfull + kTmemBufs;
-    uint64_t* qfull = bempty + kTmemBufs;
+    uint64_t* bempty = bfull + kBiasSlots;
+    uint64_t* qfull = bempty + kBiasSlots;
     uint64_t* drain = qfull + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
 
@@ -89,6 +121,8 @@ __global__ void __launch_bounds__(kHalfThreads, 1) k_half_tc(TcHalfArgs a) {
         for (int b = 0; b < kTmemBufs; ++b) {
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], kEpiWarps);
+        }
+        for (int b = 0; b < kBiasSlots; ++b) {
             mbar_init(&bfull[b], 1);
             mbar_init(&bempty[b], kEpiWarps);
         }
@@ -115,8 +149,9 @@ __global__ void __launch_bounds__(kHalfThreads, 1) k_half_tc(TcHalfArgs a) {
             uint32_t ph = 0;
             bool ok = true;
             for (int t = 0; t < ntiles && ok; ++t) {
-                const int b = t & (kTmemBufs - 1);
-                if (!mbar_wait(&bempty[b], (uint32_t)((t >> 2) & 1) ^ 1u, a.err, ERR_TIMEOUT_PRODUCER)) {
+                const int b = t % kBiasSlots;
+                if (!mbar_wait(&bempty[b], (uint32_t)((t / kBiasSlots) & 1) ^ 1u, a.err,
+                               ERR_TIMEOUT_PRODUCER)) {
                     ok = false;
                     break;
                 }
@@ -155,14 +190,18 @@ __global__ void __launch_bounds__(kHalfThreads, 1) k_half_tc(TcHalfArgs a) {
                         ph2 ^= 1u;
                     }
                 }
-                for (int i = bissued > kTmemBufs ? bissued - kTmemBufs : 0; i < bissued; ++i)
-                    mbar_wait(&bfull[i & (kTmemBufs - 1)], (uint32_t)((i >> 2) & 1), a.err,
+                for (int i = bissued > kBiasSlots ? bissued - kBiasSlots : 0; i < bissued; ++i)
+                    mbar_wait(&bfull[i % kBiasSlots], (uint32_t)((i / kBiasSlots) & 1), a.err,
                               ERR_TIMEOUT_PRODUCER);
                 if (QRES) mbar_wait(qfull, 0, a.err, ERR_TIMEOUT_PRODUCER);
             }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
+        // Online mode: buffer use u waits for the epilogue's release of use
+        // u - 1 (the first use passes at once).  Reference mode: the epilogue
+        // also releases each buffer once before its first use, after filling
+        // it with the row offsets, so use u waits for release u.
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
             bool ok = true;
@@ -172,7 +211,8 @@ __global__ void __launch_bounds__(kHalfThreads, 1) k_half_tc(TcHalfArgs a) {
             uint32_t ph = 0;
             for (int t = 0; t < ntiles && ok; ++t) {
                 const int b = t & (kTmemBufs - 1);
-                if (!mbar_wait(&tempty[b], (uint32_t)((t >> 2) & 1) ^ 1u, a.err, ERR_TIMEOUT_MMA)) {
+                const uint32_t use_ph = (uint32_t)((t >> 2) & 1) ^ (REF ? 0u : 1u);
+                if (!mbar_wait(&tempty[b], use_ph, a.err, ERR_TIMEOUT_MMA)) {
                     ok = false;
                     break;
                 }
@@ -190,7 +230,7 @@ __global__ void __launch_bounds__(kHalfThreads, 1) k_half_tc(TcHalfArgs a) {
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
                         mma_f16(d_tmem, sdesc_sw128(aaddr + kk * 32), sdesc_sw128(baddr + kk * 32),
-                                idesc, (c | kk) != 0);
+                                idesc, REF || (c | kk) != 0);
                     mma_commit(&empty[s]);
                     if (++s == stages) {
                         s = 0;
@@ -214,70 +254,141 @@ __global__ void __launch_bounds__(kHalfThreads, 1) k_half_tc(TcHalfArgs a) {
         const uint64_t ks2 = pk(ks, ks);
         const uint32_t lofs = (uint32_t)(quarter * 32) << 16;
         float M = -INFINITY, S = 0.f;
-        for (int t = grp; t < ntiles; t += kHalfGroups) {
-            const int b = t & (kTmemBufs - 1);
-            const uint32_t ph = (uint32_t)((t >> 2) & 1);
-            if (!mbar_wait(&tfull[b], ph, a.err, ERR_TIMEOUT_EPILOGUE)) break;
-            tc_fence_after();
-            float v[BN];
+        if constexpr (REF) {
+            // the group's own TMEM buffer holds -M / kappa' before every use
+            const int64_t rr = row < a.nr ? row : a.nr - 1;
+            M = a.rlogw2[rr] - a.rbias[rr];
+            const float fill = -M / ks;
+            const uint32_t buf = tmem + (uint32_t)(grp * BN) + lofs;
 #pragma unroll
-            for (int q = 0; q < BN / 32; ++q) tmem_ld32(tmem + (uint32_t)(b * BN) + lofs + q * 32, v + q * 32);
-            tmem_wait_ld();
+            for (int q = 0; q < BN / 32; ++q) tmem_fill32(buf + q * 32, fill);
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[b]);
-            if (!mbar_wait(&bfull[b], ph, a.err, ERR_TIMEOUT_EPILOGUE)) break;
+            if (lane == 0) mbar_arrive(&tempty[grp]);
+            uint64_t acc[4] = {pk(0.f, 0.f), pk(0.f, 0.f), pk(0.f, 0.f), pk(0.f, 0.f)};
+            for (int t = grp; t < ntiles; t += GROUPS) {
+                const uint32_t ph = (uint32_t)((t >> 2) & 1);
+                if (!mbar_wait(&tfull[grp], ph, a.err, ERR_TIMEOUT_EPILOGUE)) break;
+                tc_fence_after();
+                const int bs = t % kBiasSlots;
+                if (!mbar_wait(&bfull[bs], (uint32_t)((t / kBiasSlots) & 1), a.err,
+                               ERR_TIMEOUT_EPILOGUE))
+                    break;
+                const float4* sb = reinterpret_cast<const float4*>(sBias + bs * kBiasBytes);
+                float va[32], vb[32];
+                tmem_ld32(buf, va);
+                tmem_wait_ld();
+                tmem_reg_fence(va);
+                tmem_ld32(buf + 32, vb);
+                ref_slice(va, sb, ks2, acc);
+                tmem_wait_ld();
+                tmem_reg_fence(vb);
+                tmem_ld32(buf + 64, va);
+                ref_slice(vb, sb + 8, ks2, acc);
+                tmem_wait_ld();
+                tmem_reg_fence(va);
+                tmem_ld32(buf + 96, vb);
+                ref_slice(va, sb + 16, ks2, acc);
+                tmem_wait_ld();
+                tmem_reg_fence(vb);
+                // every score of the tile is in registers: refill, release
+#pragma unroll
+                for (int q = 0; q < BN / 32; ++q) tmem_fill32(buf + q * 32, fill);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[grp]);
+                ref_slice(vb, sb + 24, ks2, acc);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bempty[bs]);
+            }
+            float s0, s1, s2, s3, s4, s5, s6, s7;
+            upk(acc[0], s0, s1);
+            upk(acc[1], s2, s3);
+            upk(acc[2], s4, s5);
+            upk(acc[3], s6, s7);
+            S = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+        } else {
+            for (int t = grp; t < ntiles; t += GROUPS) {
+                const int b = t & (kTmemBufs - 1);
+                const uint32_t ph = (uint32_t)((t >> 2) & 1);
+                if (!mbar_wait(&tfull[b], ph, a.err, ERR_TIMEOUT_EPILOGUE)) break;
+                tc_fence_after();
+                float v[BN];
+#pragma unroll
+                for (int q = 0; q < BN / 32; ++q)
+                    tmem_ld32(tmem + (uint32_t)(b * BN) + lofs + q * 32, v + q * 32);
+                tmem_wait_ld();
+                tmem_reg_fence(v);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[b]);
+                const int bs = t % kBiasSlots;
+                if (!mbar_wait(&bfull[bs], (uint32_t)((t / kBiasSlots) & 1), a.err,
+                               ERR_TIMEOUT_EPILOGUE))
+                    break;
 
-            // s = acc kappa' + bias, row max (two chains)
-            const float4* sb = reinterpret_cast<const float4*>(sBias + b * kBiasBytes);
-            float mx0 = -INFINITY, mx1 = -INFINITY;
+                // s = acc kappa' + bias, row max (two chains)
+                const float4* sb = reinterpret_cast<const float4*>(sBias + bs * kBiasBytes);
+                float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int q = 0; q < BN / 4; ++q) {
-                const float4 bb = sb[q];
-                upk(fma2(pk(v[4 * q], v[4 * q + 1]), ks2, pk(bb.x, bb.y)), v[4 * q], v[4 * q + 1]);
-                upk(fma2(pk(v[4 * q + 2], v[4 * q + 3]), ks2, pk(bb.z, bb.w)), v[4 * q + 2],
-                    v[4 * q + 3]);
-                mx0 = max3(mx0, v[4 * q], v[4 * q + 1]);
-                mx1 = max3(mx1, v[4 * q + 2], v[4 * q + 3]);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bempty[b]);
-            const float mx = fmaxf(mx0, mx1);
-            if (mx > M) {
-                S *= ex2(M - mx);
-                M = mx;
-            }
-            if (M == -INFINITY) continue;   // only padding columns so far: nothing to add
-            // S += sum 2^{s - M}
-            const uint64_t nm = pk(-M, -M);
-            uint64_t acc0 = pk(0.f, 0.f), acc1 = pk(0.f, 0.f);
+                for (int q = 0; q < BN / 4; ++q) {
+                    const float4 bb = sb[q];
+                    upk(fma2(pk(v[4 * q], v[4 * q + 1]), ks2, pk(bb.x, bb.y)), v[4 * q], v[4 * q + 1]);
+                    upk(fma2(pk(v[4 * q + 2], v[4 * q + 3]), ks2, pk(bb.z, bb.w)), v[4 * q + 2],
+                        v[4 * q + 3]);
+                    mx0 = max3(mx0, v[4 * q], v[4 * q + 1]);
+                    mx1 = max3(mx1, v[4 * q + 2], v[4 * q + 3]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bempty[bs]);
+                const float mx = fmaxf(mx0, mx1);
+                if (mx > M) {
+                    S *= ex2(M - mx);
+                    M = mx;
+                }
+                if (M == -INFINITY) continue;   // only padding columns so far: nothing to add
+                // S += sum 2^{s - M}
+                const uint64_t nm = pk(-M, -M);
+                uint64_t acc0 = pk(0.f, 0.f), acc1 = pk(0.f, 0.f);
 #pragma unroll
-            for (int q = 0; q < BN / 4; ++q) {
-                float x0, x1, x2, x3;
-                upk(add2(pk(v[4 * q], v[4 * q + 1]), nm), x0, x1);
-                upk(add2(pk(v[4 * q + 2], v[4 * q + 3]), nm), x2, x3);
-                acc0 = add2(acc0, pk(ex2(x0), ex2(x1)));
-                acc1 = add2(acc1, pk(ex2(x2), ex2(x3)));
+                for (int q = 0; q < BN / 4; ++q) {
+                    float x0, x1, x2, x3;
+                    upk(add2(pk(v[4 * q], v[4 * q + 1]), nm), x0, x1);
+                    upk(add2(pk(v[4 * q + 2], v[4 * q + 3]), nm), x2, x3);
+                    acc0 = add2(acc0, pk(ex2(x0), ex2(x1)));
+                    acc1 = add2(acc1, pk(ex2(x2), ex2(x3)));
+                }
+                float s0, s1, s2, s3;
+                upk(acc0, s0, s1);
+                upk(acc1, s2, s3);
+                S += (s0 + s1) + (s2 + s3);
             }
-            float s0, s1, s2, s3;
-            upk(acc0, s0, s1);
-            upk(acc1, s2, s3);
-            S += (s0 + s1) + (s2 + s3);
         }
 
-        // merge the groups in a fixed order: group 0 absorbs group 1
-        if (grp == 1) sMerge[rloc] = make_float2(M, S);
-        epi_bar_sync();
+        // merge the groups in a fixed order: group 0 absorbs groups 1, 2, ...
+        if (grp > 0) sMerge[(grp - 1) * BM + rloc] = make_float2(M, S);
+        epi_bar_sync<GROUPS>();
         if (grp == 0) {
-            const float2 o = sMerge[rloc];
-            const float Mt = fmaxf(M, o.x);
-            // a group that saw only padding has (M, S) = (-inf, 0) and adds nothing
-            const float St = (M == -INFINITY ? 0.f : S * ex2(M - Mt)) +
-                             (o.x == -INFINITY ? 0.f : o.y * ex2(o.x - Mt));
+            float Mt = M, St = S;
+#pragma unroll
+            for (int g = 1; g < GROUPS; ++g) {
+                const float2 o = sMerge[(g - 1) * BM + rloc];
+                const float Mn = fmaxf(Mt, o.x);
+                // a group that saw only padding has (M, S) = (-inf, 0) and adds nothing
+                St = (Mt == -INFINITY ? 0.f : St * ex2(Mt - Mn)) +
+                     (o.x == -INFINITY ? 0.f : o.y * ex2(o.x - Mn));
+                Mt = Mn;
+            }
             if (row < a.nr) {
                 if (a.splits > 1) {
                     a.partial[(int64_t)blockIdx.y * a.nr + row] = make_float2(Mt, St);
                 } else {
+                    if (REF && !(St >= kTcMinRefSum && St <= kTcMaxRefSum)) {
+                        const unsigned int slot = atomicAdd(&a.fix_count[0], 1u);
+                        if (slot < (unsigned int)a.nr) a.fix_list[slot] = (int)row;
+                    }
                     const float lse2 = Mt + log2f(St);
                     if (a.rnorm != nullptr) {
                         a.pot[row] = a.rnorm[row] - a.eps_ln2 * lse2;
@@ -298,21 +409,94 @@ __global__ void __launch_bounds__(kHalfThreads, 1) k_half_tc(TcHalfArgs a) {
     }
 }
 
+template <bool QRES, bool REF>
+cudaError_t launch_half_tc_t(const TcHalfArgs& a, int row_tiles, size_t smem, cudaStream_t s) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        k_half_tc<QRES, REF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_half_tc<QRES, REF><<<dim3((unsigned)row_tiles, (unsigned)a.splits), half_threads(REF), smem, s>>>(a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_half_tc(const TcHalfArgs& a, int row_tiles, bool qres, cudaStream_t s) {
     const size_t smem = half_smem_bytes(a.nch, qres, a.stages);
-    dim3 grid((unsigned)row_tiles, (unsigned)a.splits);
     cudaError_t e;
-    if (qres) {
-        e = cudaFuncSetAttribute(k_half_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess) return e;
-        k_half_tc<true><<<grid, kHalfThreads, smem, s>>>(a);
-    } else {
-        e = cudaFuncSetAttribute(k_half_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess) return e;
-        k_half_tc<false><<<grid, kHalfThreads, smem, s>>>(a);
+    if (a.use_ref)
+        e = qres ? launch_half_tc_t<true, true>(a, row_tiles, smem, s)
+                 : launch_half_tc_t<false, true>(a, row_tiles, smem, s);
+    else
+        e = qres ? launch_half_tc_t<true, false>(a, row_tiles, smem, s)
+                 : launch_half_tc_t<false, false>(a, row_tiles, smem, s);
+    count_launch();
+    return e;
+}
+
+// ---------------------------------------------------------------------------
+// Fixup of guarded rows: one warp per listed row.  The row's centred
+// coordinates times kappa sit in shared memory; each lane scores columns
+// lane, lane + 32, ... in FP32 from the raw, centred coordinates, folds them
+// into an online (max, sum), and the lanes merge by shuffles.  The list
+// length is read once per block; the last block to finish resets the list.
+namespace {
+constexpr int kFixBlocks = 64;
+constexpr int kFixWarps = 8;
+}  // namespace
+
+__global__ void __launch_bounds__(kFixWarps * 32) k_fix_tc(TcFixArgs a) {
+    __shared__ float sx[kFixWarps][kFixMaxDim];
+    __shared__ float st[kFixMaxDim];
+    __shared__ unsigned int s_cnt;
+    const int d = a.d;
+    for (int k = threadIdx.x; k < d; k += blockDim.x) st[k] = a.shift[k];
+    if (threadIdx.x == 0) s_cnt = min(*(volatile unsigned int*)&a.fix_count[0], (unsigned int)a.nr);
+    __syncthreads();
+    const unsigned int cnt = s_cnt;
+    const int wl = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const unsigned int warps = gridDim.x * kFixWarps;
+    for (unsigned int w = blockIdx.x * kFixWarps + wl; w < cnt; w += warps) {
+        const int64_t row = a.fix_list[w];
+        for (int k = lane; k < d; k += 32) sx[wl][k] = (a.R[row * d + k] - st[k]) * a.kappa;
+        __syncwarp();
+        float M = -INFINITY, S = 0.f;
+        for (int64_t j = lane; j < a.nc; j += 32) {
+            const float* y = a.C + j * d;
+            float s = a.cbias[j];
+            for (int k = 0; k < d; ++k) s = fmaf(sx[wl][k], y[k] - st[k], s);
+            if (s > M) {
+                S *= ex2(M - s);
+                M = s;
+            }
+            if (M != -INFINITY) S += ex2(s - M);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float Mo = __shfl_xor_sync(0xffffffffu, M, o);
+            const float So = __shfl_xor_sync(0xffffffffu, S, o);
+            const float Mn = fmaxf(M, Mo);
+            S = (M == -INFINITY ? 0.f : S * ex2(M - Mn)) + (Mo == -INFINITY ? 0.f : So * ex2(Mo - Mn));
+            M = Mn;
+        }
+        if (lane == 0) {
+            const float lse2 = M + log2f(S);
+            a.pot[row] = a.rnorm[row] - a.eps_ln2 * lse2;
+            a.rbias[row] = a.rlogw2[row] - lse2;
+        }
+        __syncwarp();
     }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(&a.fix_count[1], 1u) == gridDim.x - 1) {
+            a.fix_count[0] = 0;
+            a.fix_count[1] = 0;
+            __threadfence();
+        }
+    }
+}
+
+cudaError_t launch_fix_tc(const TcFixArgs& a, cudaStream_t s) {
+    if (a.d > kFixMaxDim) return cudaErrorInvalidValue;
+    k_fix_tc<<<kFixBlocks, kFixWarps * 32, 0, s>>>(a);
     count_launch();
     return cudaGetLastError();
 }

@@ -75,8 +75,15 @@ TcPlan plan_tc(int64_t n, int64_t m, int32_t d, int sms, const fs_options* opt) 
 }
 
 struct TcBufs {
-    size_t shift_part, shift, nx, ny, lax, lby, absmax, params, X16, Y16, alpha, beta, partial;
+    size_t shift_part, shift, nx, ny, lax, lby, absmax, params, X16, Y16, alpha, beta, partial,
+        fix_list, fix_count;
 };
+
+// Reference offsets from this many score pairs up, after the first
+// iterations: below it the fixup launch costs more than it saves; the first
+// updates move the LSEs too far.
+constexpr double kTcRefMinPairs = 67108864.0;   // 2^26
+constexpr int kTcOnlineIters = 2;
 
 void layout_tc(Layout& L, TcBufs& B, int64_t n, int64_t m, int32_t d, const TcPlan& p) {
     B.shift_part = L.take(sizeof(double) * (size_t)kShiftBlocks * d);
@@ -93,6 +100,8 @@ void layout_tc(Layout& L, TcBufs& B, int64_t n, int64_t m, int32_t d, const TcPl
     B.beta = L.take(sizeof(float) * (size_t)p.rty * BM);
     const int64_t part = std::max((int64_t)n * p.splits_f, (int64_t)m * p.splits_g);
     B.partial = L.take(sizeof(float2) * (size_t)part);
+    B.fix_list = L.take(sizeof(int) * (size_t)std::max(n, m));
+    B.fix_count = L.take(sizeof(unsigned int) * 2);
 }
 
 // centring, norms, log-weights, fp16 tiles of both clouds; beta from g
@@ -216,24 +225,36 @@ fs_status solve_tc(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) {
     FS_TRY(make_chunk_tmap(&tmX, hf.Q, (uint64_t)p.rtx * p.nch * BM));
     FS_TRY(make_chunk_tmap(&tmY, hf.K, (uint64_t)p.rty * p.nch * BM));
 
-    auto half = [&](const TcHalfArgs& h, const TensorMap128& tq, const TensorMap128& tk,
-                    int64_t row_tiles) -> cudaError_t {
-        return p.pair ? launch_half_pair(h, tq, tk, (int)row_tiles, p.qres, c.stream)
-                      : launch_half_tc(h, (int)row_tiles, p.qres, c.stream);
+    int* fix_list = c.at<int>(B.fix_list);
+    unsigned int* fix_count = c.at<unsigned int>(B.fix_count);
+    FS_CUDA(cudaMemsetAsync(fix_count, 0, 2 * sizeof(unsigned int), c.stream));
+    hf.fix_list = hg.fix_list = fix_list;
+    hf.fix_count = hg.fix_count = fix_count;
+    TcFixArgs ff{P.X.dev, P.Y.dev, c.at<float>(B.shift), d, (float)(2.0 * kLog2e / (double)P.eps),
+                 hf.cbias, n, m, eps_ln2, hf.rnorm, hf.rlogw2, P.f.dev, hf.rbias, fix_list,
+                 fix_count};
+    TcFixArgs fg{P.Y.dev, P.X.dev, c.at<float>(B.shift), d, ff.kappa, hg.cbias, m, n, eps_ln2,
+                 hg.rnorm, hg.rlogw2, P.g.dev, hg.rbias, fix_list, fix_count};
+    const bool ref_ok = d <= kFixMaxDim && (double)n * (double)m >= kTcRefMinPairs;
+
+    auto half = [&](TcHalfArgs& h, const TcFixArgs& fx, const TensorMap128& tq,
+                    const TensorMap128& tk, int64_t row_tiles, int splits, int64_t nr, float* pot,
+                    bool ref) -> fs_status {
+        h.use_ref = ref ? 1 : 0;
+        const int ts = timing_begin(c.stream);
+        FS_CUDA(p.pair ? launch_half_pair(h, tq, tk, (int)row_tiles, p.qres, c.stream)
+                       : launch_half_tc(h, (int)row_tiles, p.qres, c.stream));
+        timing_end(ts, TIME_HALF, c.stream);
+        if (splits > 1)
+            FS_CUDA(launch_merge_lse(part, splits, nr, h.rnorm, h.rlogw2, eps_ln2, pot, h.rbias, 1,
+                                     c.stream, ref ? fix_list : nullptr, ref ? fix_count : nullptr));
+        if (ref) FS_CUDA(launch_fix_tc(fx, c.stream));
+        return FS_OK;
     };
     for (int32_t it = 0; it < n_iter; ++it) {
-        int ts = timing_begin(c.stream);
-        FS_CUDA(half(hf, tmX, tmY, p.rtx));
-        timing_end(ts, TIME_HALF, c.stream);
-        if (p.splits_f > 1)
-            FS_CUDA(launch_merge_lse(part, p.splits_f, n, hf.rnorm, hf.rlogw2, eps_ln2, P.f.dev,
-                                     hf.rbias, 1, c.stream));
-        ts = timing_begin(c.stream);
-        FS_CUDA(half(hg, tmY, tmX, p.rty));
-        timing_end(ts, TIME_HALF, c.stream);
-        if (p.splits_g > 1)
-            FS_CUDA(launch_merge_lse(part, p.splits_g, m, hg.rnorm, hg.rlogw2, eps_ln2, P.g.dev,
-                                     hg.rbias, 1, c.stream));
+        const bool ref = ref_ok && it >= kTcOnlineIters;
+        FS_TRY(half(hf, ff, tmX, tmY, p.rtx, p.splits_f, n, P.f.dev, ref));
+        FS_TRY(half(hg, fg, tmY, tmX, p.rty, p.splits_g, m, P.g.dev, ref));
     }
     if (opt && opt->check_finite) {
         unsigned int* counter = c.at<unsigned int>(B.absmax);

@@ -41,7 +41,45 @@ struct TcHalfArgs {
     float* rbias;           // bias of the rows for the next half-update
     float2* partial;        // (max, sum) per split and row when splits > 1
     uint32_t* err;          // device error word
+    // Reference offsets (one-CTA kernel): with use_ref set, a row's exponent
+    // offset is its previous LSE, rlogw2 - rbias, instead of a running max;
+    // rows whose sum leaves the guarded range go to fix_list for
+    // launch_fix_tc.
+    int use_ref;
+    int* fix_list;            // [nr]
+    unsigned int* fix_count;  // [2], zero before the first guarded half-update
 };
+
+// Epilogue groups of the one-CTA half-update: two with the online max (a
+// thread holds a whole 128-score tile row), four with reference offsets
+// (32-column slices streamed from TMEM; one group per TMEM buffer).
+constexpr int kRefGroups = 4;
+constexpr int half_threads(bool ref) { return 32 * (2 + (ref ? kRefGroups : kHalfGroups) * kEpiWarps); }
+
+// Guarded range of a reference-offset sum (see the FMA path).
+constexpr float kTcMinRefSum = 5.421010862427522e-20f;   // 2^-64
+constexpr float kTcMaxRefSum = 8.507059173023462e+37f;   // 2^126
+
+// FP32 recomputation of the rows a guarded half-update listed: one warp per
+// row over all columns, centred coordinates, online max.
+struct TcFixArgs {
+    const float* R;           // raw coordinates of the updated side [nr x d]
+    const float* C;           // raw coordinates of the other side [nc x d]
+    const float* shift;       // [d]
+    int d;
+    float kappa;              // 2 log2(e) / eps
+    const float* cbias;       // column bias [nc] (beta or alpha)
+    int64_t nr, nc;
+    float eps_ln2;
+    const float* rnorm;
+    const float* rlogw2;
+    float* pot;
+    float* rbias;
+    int* fix_list;
+    unsigned int* fix_count;
+};
+constexpr int kFixMaxDim = 512;
+cudaError_t launch_fix_tc(const TcFixArgs& a, cudaStream_t s);
 
 cudaError_t launch_prep_side(const float* P, const float* w, int64_t rows, int d,
                              const float* shift, float* norm, float* logw2,

@@ -21,10 +21,17 @@
 //              commits with multicast to both CTAs' barriers;
 //              odd CTA: relays "my half of this stage has landed" (and "my Q
 //              has landed") to the even CTA's barriers with remote arrives;
-//   warps 2-9  two epilogue groups per CTA, tile t going to group t mod 2,
-//              one thread per row reading its 256 scores from its own TMEM in
-//              two halves; the TMEM buffer is released to the even CTA's
-//              barrier (local and remote arrivals).
+//   warps 2-   epilogue groups, one thread per row, releasing TMEM buffers
+//              to the even CTA's barrier (local and remote arrivals):
+//              online mode: two groups, tile t going to group t mod 2, a
+//              thread reading its 256 scores in two halves and folding them
+//              into a running max and sum;
+//              reference mode: four groups, two per TMEM buffer, each owning
+//              one 128-column half: the group pre-loads its accumulators
+//              with -M / kappa' (M = the row's previous LSE), then streams its
+//              half in 32-column slices and only sums 2^{acc kappa' + bias}.
+// Bias slices go through a ring of 8, so the producer never waits on them
+// before issuing K chunks.
 #include "fs_tc.cuh"
 
 namespace fs {
@@ -36,14 +43,32 @@ constexpr int BNP = 256;                    // columns of a pair score tile
 constexpr int kPairBufs = 2;                // TMEM buffers of BNP columns
 constexpr int kPairTmemCols = kPairBufs * BNP;
 constexpr int kPairBiasBytes = BNP * 4;
+constexpr int kPairBiasSlots = 8;
+constexpr int kPairMaxGroups = kRefGroups;
 
 __host__ __device__ constexpr int pair_fixed_bytes(int nch, bool qres) {
-    return 1024 + (qres ? nch * CHUNK_BYTES : 0) + kPairBufs * kPairBiasBytes + BM * 8 +
-           8 * (2 * kMaxStages + 4 * kPairBufs + 2) + 16;
+    return 1024 + (qres ? nch * CHUNK_BYTES : 0) + kPairBiasSlots * kPairBiasBytes +
+           BM * 8 * (kPairMaxGroups - 1) +
+           8 * (2 * kMaxStages + 2 * kPairBufs + 2 * kPairBiasSlots + 2) + 16;
 }
 
+template <int GROUPS>
 __device__ __forceinline__ void epi_bar_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kHalfGroups * kEpiWarps * 32) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(GROUPS * kEpiWarps * 32) : "memory");
+}
+
+// One 32-column slice in reference mode: acc[] += 2^{v kappa' + bias}.
+__device__ __forceinline__ void ref_slice(const float (&v)[32], const float4* __restrict__ sb,
+                                          uint64_t ks2, uint64_t (&acc)[4]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 bb = sb[q];
+        float x0, x1, x2, x3;
+        upk(fma2(pk(v[4 * q], v[4 * q + 1]), ks2, pk(bb.x, bb.y)), x0, x1);
+        upk(fma2(pk(v[4 * q + 2], v[4 * q + 3]), ks2, pk(bb.z, bb.w)), x2, x3);
+        acc[(2 * q) & 3] = add2(acc[(2 * q) & 3], pk(ex2(x0), ex2(x1)));
+        acc[(2 * q + 1) & 3] = add2(acc[(2 * q + 1) & 3], pk(ex2(x2), ex2(x3)));
+    }
 }
 
 // one row's 128 scores: s = acc kappa' + bias, folded into (M, S)
@@ -95,10 +120,12 @@ size_t pair_smem_bytes(int nch, bool qres, int stages) {
 
 // a.col_tiles and a.tiles_per_split count 256-column tiles; a.K holds an even
 // number of 128-row tiles; a.cbias has 256 entries per column tile.
-template <bool QRES>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHalfThreads, 1)
+template <bool QRES, bool REF>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(half_threads(REF), 1)
     k_half_pair(const __grid_constant__ TensorMap128 tmQ, const __grid_constant__ TensorMap128 tmK,
                 TcHalfArgs a) {
+    constexpr int GROUPS = REF ? kRefGroups : kHalfGroups;
+    static_assert(!REF || GROUPS == 2 * kPairBufs, "reference mode: two groups per TMEM buffer");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -117,14 +144,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHalfThreads, 1)
     uint8_t* sQ = smem;
     uint8_t* sStage = smem + (QRES ? nch * CHUNK_BYTES : 0);
     uint8_t* sBias = sStage + stages * STAGE_BYTES;
-    float2* sMerge = reinterpret_cast<float2*>(sBias + kPairBufs * kPairBiasBytes);
-    uint64_t* full = reinterpret_cast<uint64_t*>(sMerge + BM);
+    float2* sMerge = reinterpret_cast<float2*>(sBias + kPairBiasSlots * kPairBiasBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sMerge + BM * (kPairMaxGroups - 1));
     uint64_t* empty = full + kMaxStages;
     uint64_t* tfull = empty + kMaxStages;
     uint64_t* tempty = tfull + kPairBufs;
     uint64_t* bfull = tempty + kPairBufs;
-    uint64_t* bempty = bfull + kPairBufs;
-    uint64_t* qfull = bempty + kPairBufs;
+    uint64_t* bempty = bfull + kPairBiasSlots;
+    uint64_t* qfull = bempty + kPairBiasSlots;
     uint64_t* drain = qfull + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
 
@@ -136,11 +163,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHalfThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
+        // a TMEM buffer is released by every epilogue warp that reads it, in
+        // both CTAs: one group per CTA (online), two (reference)
+        constexpr int readers = (REF ? 2 : 1) * kEpiWarps;
         for (int b = 0; b < kPairBufs; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 2 * kEpiWarps);
+            mbar_init(&tempty[b], 2 * readers);
+        }
+        for (int b = 0; b < kPairBiasSlots; ++b) {
             mbar_init(&bfull[b], 1);
-            mbar_init(&bempty[b], kEpiWarps);
+            mbar_init(&bempty[b], readers);
         }
         mbar_init(qfull, 1);
         mbar_init(drain, 1);
@@ -168,8 +200,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHalfThreads, 1)
             uint32_t ph = 0;
             bool ok = true;
             for (int t = 0; t < ntiles && ok; ++t) {
-                const int b = t & 1;
-                if (!mbar_wait(&bempty[b], (uint32_t)((t >> 1) & 1) ^ 1u, a.err, ERR_TIMEOUT_PRODUCER)) {
+                const int b = t % kPairBiasSlots;
+                if (!mbar_wait(&bempty[b], (uint32_t)((t / kPairBiasSlots) & 1) ^ 1u, a.err,
+                               ERR_TIMEOUT_PRODUCER)) {
                     ok = false;
                     break;
                 }
@@ -212,8 +245,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHalfThreads, 1)
                     }
                     if (QRES) mbar_wait_cluster(qfull, 0, a.err, ERR_TIMEOUT_PRODUCER);
                 }
-                for (int i = bissued > kPairBufs ? bissued - kPairBufs : 0; i < bissued; ++i)
-                    mbar_wait(&bfull[i & 1], (uint32_t)((i >> 1) & 1), a.err, ERR_TIMEOUT_PRODUCER);
+                for (int i = bissued > kPairBiasSlots ? bissued - kPairBiasSlots : 0; i < bissued; ++i)
+                    mbar_wait(&bfull[i % kPairBiasSlots], (uint32_t)((i / kPairBiasSlots) & 1), a.err,
+                              ERR_TIMEOUT_PRODUCER);
             }
         }
     } else if (warp == 1) {
@@ -225,9 +259,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHalfThreads, 1)
             tc_fence_after();
             int s = 0;
             uint32_t ph = 0;
+            // online: use u of a buffer waits for the release of use u - 1 (the
+            // first passes at once); reference: the epilogue releases every
+            // buffer once before its first use, after pre-loading it
             for (int t = 0; t < ntiles && ok; ++t) {
                 const int b = t & 1;
-                if (!mbar_wait_cluster(&tempty[b], (uint32_t)((t >> 1) & 1) ^ 1u, a.err,
+                if (!mbar_wait_cluster(&tempty[b], (uint32_t)((t >> 1) & 1) ^ (REF ? 0u : 1u), a.err,
                                        ERR_TIMEOUT_MMA)) {
                     ok = false;
                     break;
@@ -246,7 +283,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHalfThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
                         mma_f16_pair(d_tmem, sdesc_sw128(aaddr + kk * 32),
-                                     sdesc_sw128(baddr + kk * 32), idesc, (c | kk) != 0);
+                                     sdesc_sw128(baddr + kk * 32), idesc, REF || (c | kk) != 0);
                     mma_commit_pair(&empty[s], 3);
                     if (++s == stages) {
                         s = 0;
@@ -269,45 +306,118 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHalfThreads, 1)
         const uint64_t ks2 = pk(ks, ks);
         const uint32_t lofs = (uint32_t)(quarter * 32) << 16;
         float M = -INFINITY, S = 0.f;
-        for (int t = grp; t < ntiles; t += kHalfGroups) {
-            const int b = t & 1;
-            const uint32_t ph = (uint32_t)((t >> 1) & 1);
-            if (!mbar_wait_cluster(&tfull[b], ph, a.err, ERR_TIMEOUT_EPILOGUE)) break;
-            tc_fence_after();
-            if (!mbar_wait(&bfull[b], ph, a.err, ERR_TIMEOUT_EPILOGUE)) break;
-            const float4* sb = reinterpret_cast<const float4*>(sBias + b * kPairBiasBytes);
-#pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                float v[128];
+        if constexpr (REF) {
+            // group g: TMEM buffer g / 2 (tiles t = g / 2 mod 2), column half g % 2
+            const int b = grp >> 1, h = grp & 1;
+            const int64_t rr = row < a.nr ? row : a.nr - 1;
+            M = a.rlogw2[rr] - a.rbias[rr];
+            const float fill = -M / ks;
+            const uint32_t buf = tmem + (uint32_t)(b * BNP + h * 128) + lofs;
+            const uint32_t tempty_lead = mapa_shared(smem_u32(&tempty[b]), 0);
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    tmem_ld32(tmem + (uint32_t)(b * BNP + h * 128) + lofs + q * 32, v + q * 32);
-                tmem_wait_ld();
-                if (h == 1) {
-                    // both halves are in registers: hand the buffer back to the MMA
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[b]), 0));
-                }
-                fold128(v, sb + h * 32, ks2, M, S);
-            }
+            for (int q = 0; q < 4; ++q) tmem_fill32(buf + q * 32, fill);
+            tmem_wait_st();
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bempty[b]);
+            if (lane == 0) mbar_arrive_remote(tempty_lead);
+            uint64_t acc[4] = {pk(0.f, 0.f), pk(0.f, 0.f), pk(0.f, 0.f), pk(0.f, 0.f)};
+            for (int t = b; t < ntiles; t += kPairBufs) {
+                if (!mbar_wait_cluster(&tfull[b], (uint32_t)((t >> 1) & 1), a.err, ERR_TIMEOUT_EPILOGUE))
+                    break;
+                tc_fence_after();
+                const int bs = t % kPairBiasSlots;
+                if (!mbar_wait(&bfull[bs], (uint32_t)((t / kPairBiasSlots) & 1), a.err,
+                               ERR_TIMEOUT_EPILOGUE))
+                    break;
+                const float4* sb =
+                    reinterpret_cast<const float4*>(sBias + bs * kPairBiasBytes) + h * 32;
+                float va[32], vb[32];
+                tmem_ld32(buf, va);
+                tmem_wait_ld();
+                tmem_reg_fence(va);
+                tmem_ld32(buf + 32, vb);
+                ref_slice(va, sb, ks2, acc);
+                tmem_wait_ld();
+                tmem_reg_fence(vb);
+                tmem_ld32(buf + 64, va);
+                ref_slice(vb, sb + 8, ks2, acc);
+                tmem_wait_ld();
+                tmem_reg_fence(va);
+                tmem_ld32(buf + 96, vb);
+                ref_slice(va, sb + 16, ks2, acc);
+                tmem_wait_ld();
+                tmem_reg_fence(vb);
+                // the half is in registers: pre-load it again, hand it back
+#pragma unroll
+                for (int q = 0; q < 4; ++q) tmem_fill32(buf + q * 32, fill);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(tempty_lead);
+                ref_slice(vb, sb + 24, ks2, acc);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bempty[bs]);
+            }
+            float s0, s1, s2, s3, s4, s5, s6, s7;
+            upk(acc[0], s0, s1);
+            upk(acc[1], s2, s3);
+            upk(acc[2], s4, s5);
+            upk(acc[3], s6, s7);
+            S = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+        } else {
+            for (int t = grp; t < ntiles; t += GROUPS) {
+                const int b = t & 1;
+                const uint32_t ph = (uint32_t)((t >> 1) & 1);
+                if (!mbar_wait_cluster(&tfull[b], ph, a.err, ERR_TIMEOUT_EPILOGUE)) break;
+                tc_fence_after();
+                const int bs = t % kPairBiasSlots;
+                if (!mbar_wait(&bfull[bs], (uint32_t)((t / kPairBiasSlots) & 1), a.err,
+                               ERR_TIMEOUT_EPILOGUE))
+                    break;
+                const float4* sb = reinterpret_cast<const float4*>(sBias + bs * kPairBiasBytes);
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    float v[128];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        tmem_ld32(tmem + (uint32_t)(b * BNP + h * 128) + lofs + q * 32, v + q * 32);
+                    tmem_wait_ld();
+                    tmem_reg_fence(v);
+                    if (h == 1) {
+                        // both halves are in registers: hand the buffer back to the MMA
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[b]), 0));
+                    }
+                    fold128(v, sb + h * 32, ks2, M, S);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bempty[bs]);
+            }
         }
 
-        // merge the groups in a fixed order: group 0 absorbs group 1
-        if (grp == 1) sMerge[rloc] = make_float2(M, S);
-        epi_bar_sync();
+        // merge the groups in a fixed order: group 0 absorbs groups 1, 2, ...
+        if (grp > 0) sMerge[(grp - 1) * BM + rloc] = make_float2(M, S);
+        epi_bar_sync<GROUPS>();
         if (grp == 0) {
-            const float2 o = sMerge[rloc];
-            const float Mt = fmaxf(M, o.x);
-            // a group that saw only padding has (M, S) = (-inf, 0) and adds nothing
-            const float St = (M == -INFINITY ? 0.f : S * ex2(M - Mt)) +
-                             (o.x == -INFINITY ? 0.f : o.y * ex2(o.x - Mt));
+            float Mt = M, St = S;
+#pragma unroll
+            for (int g = 1; g < GROUPS; ++g) {
+                const float2 o = sMerge[(g - 1) * BM + rloc];
+                const float Mn = fmaxf(Mt, o.x);
+                // a group that saw only padding has (M, S) = (-inf, 0) and adds nothing
+                St = (Mt == -INFINITY ? 0.f : St * ex2(Mt - Mn)) +
+                     (o.x == -INFINITY ? 0.f : o.y * ex2(o.x - Mn));
+                Mt = Mn;
+            }
             if (row < a.nr) {
                 if (a.splits > 1) {
                     a.partial[(int64_t)blockIdx.y * a.nr + row] = make_float2(Mt, St);
                 } else {
+                    if (REF && !(St >= kTcMinRefSum && St <= kTcMaxRefSum)) {
+                        const unsigned int slot = atomicAdd(&a.fix_count[0], 1u);
+                        if (slot < (unsigned int)a.nr) a.fix_list[slot] = (int)row;
+                    }
                     const float lse2 = Mt + log2f(St);
                     if (a.rnorm != nullptr) {
                         a.pot[row] = a.rnorm[row] - a.eps_ln2 * lse2;
@@ -331,25 +441,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHalfThreads, 1)
     }
 }
 
+template <bool QRES, bool REF>
+cudaError_t launch_half_pair_t(const TcHalfArgs& a, const TensorMap128& tmQ, const TensorMap128& tmK,
+                               int row_tiles, size_t smem, cudaStream_t s) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        k_half_pair<QRES, REF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_half_pair<QRES, REF><<<dim3((unsigned)row_tiles, (unsigned)a.splits), half_threads(REF), smem,
+                             s>>>(tmQ, tmK, a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_half_pair(const TcHalfArgs& a, const TensorMap128& tmQ,
                              const TensorMap128& tmK, int row_tiles, bool qres, cudaStream_t s) {
     if (row_tiles % 2 != 0) return cudaErrorInvalidValue;
     const size_t smem = pair_smem_bytes(a.nch, qres, a.stages);
-    dim3 grid((unsigned)row_tiles, (unsigned)a.splits);
     cudaError_t e;
-    if (qres) {
-        e = cudaFuncSetAttribute(k_half_pair<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess) return e;
-        k_half_pair<true><<<grid, kHalfThreads, smem, s>>>(tmQ, tmK, a);
-    } else {
-        e = cudaFuncSetAttribute(k_half_pair<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess) return e;
-        k_half_pair<false><<<grid, kHalfThreads, smem, s>>>(tmQ, tmK, a);
-    }
+    if (a.use_ref)
+        e = qres ? launch_half_pair_t<true, true>(a, tmQ, tmK, row_tiles, smem, s)
+                 : launch_half_pair_t<false, true>(a, tmQ, tmK, row_tiles, smem, s);
+    else
+        e = qres ? launch_half_pair_t<true, false>(a, tmQ, tmK, row_tiles, smem, s)
+                 : launch_half_pair_t<false, false>(a, tmQ, tmK, row_tiles, smem, s);
     count_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace tc
