@@ -194,3 +194,17 @@ def test_full_size_plan_application_on_sampled_rows(name):
         PY = orc.apply_plan_rows(inp["X"], inp["a"], inp["Y"], inp["b"], eps, f, g, V, rows)
         ref = 2.0 * (inp["a"][rows, None].astype(np.float64) * inp["X"][rows] - PY)
     assert rel_l2(np64(out)[rows], ref) <= APPLY_TOL
+
+
+@pytest.mark.parametrize("d,eps,iters", [(64, 0.01, 6), (64, 0.1, 10), (256, 0.02, 6)])
+def test_reference_offset_path_with_fixups(d, eps, iters):
+    """n*m = 2^26 takes reference offsets after the first iterations (one-CTA
+    kernel at d = 64, CTA pairs at d = 256).  A cold start at small eps moves
+    the LSEs far between iterations, so many rows fail the guarded range and
+    are recomputed by the FP32 fixup; the potentials must still match."""
+    inp = make_inputs("c3_n50k_d64", n=8192, m=8192, d=d, seed=93)
+    C = orc.cost(inp["X"], inp["Y"])
+    f, g, _ = _solve(inp, [(eps, iters)], path="auto")
+    fr, gr = orc.sinkhorn(C, inp["a"], inp["b"], eps, iters)
+    assert max_abs(f, fr) <= F_TOL_TENSOR * C.max()
+    assert max_abs(g, gr) <= F_TOL_TENSOR * C.max()
