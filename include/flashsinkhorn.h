@@ -162,6 +162,55 @@ fs_status fs_grad_x(const float* X, const float* a, int64_t n,
                     const fs_options* opt, void* stream);
 
 /*
+ * The Y side of the plan.  P^T_ji = P_ij, so these are the calls above with
+ * the roles of (X, a, f) and (Y, b, g) exchanged (Method 3's projection and
+ * gradient are attention-like in either direction):
+ *   fs_apply_plan_t    out_j = sum_i P_ij U_i         U [n*k], out [m*k]
+ *   fs_barycentric_y   T_j = (P^T X)_j / b_j          out [m*d]
+ *   fs_grad_y          grad_j = 2 (b_j y_j - (P^T X)_j)   out [m*d]
+ * Arguments, pointers and errors as fs_apply_plan (k bounds apply to U).
+ */
+fs_status fs_apply_plan_t(const float* X, const float* a, int64_t n,
+                          const float* Y, const float* b, int64_t m, int32_t d,
+                          float eps, const float* f, const float* g,
+                          const float* U, int32_t k, float* out,
+                          const fs_options* opt, void* stream);
+fs_status fs_barycentric_y(const float* X, const float* a, int64_t n,
+                           const float* Y, const float* b, int64_t m, int32_t d,
+                           float eps, const float* f, const float* g, float* out,
+                           const fs_options* opt, void* stream);
+fs_status fs_grad_y(const float* X, const float* a, int64_t n,
+                    const float* Y, const float* b, int64_t m, int32_t d,
+                    float eps, const float* f, const float* g, float* out,
+                    const fs_options* opt, void* stream);
+
+/*
+ * fs_dual_value -- the dual objective <a, f> + <b, g> (Method 1; at a fixed
+ * point the entropic OT value, whose gradient fs_grad_x returns).
+ *   a [n], f [n], b [m], g [m]   host or device
+ *   out                          HOST pointer to one double, written
+ * Summed on the GPU in double, in a fixed order (bitwise reproducible).
+ * Synchronises `stream`.  FS_ERR_INVALID_ARG for null pointers or sizes < 1.
+ */
+fs_status fs_dual_value(const float* a, int64_t n, const float* b, int64_t m,
+                        const float* f, const float* g, double* out, void* stream);
+
+/*
+ * fs_marginal_residuals -- the constraint violations of the plan P(f, g)
+ * (Method 1: P 1 = a, P^T 1 = b at convergence):
+ *     out[0] = || P 1 - a ||_1,   out[1] = || P^T 1 - b ||_1
+ * The row and column sums are two plan applications on the GPU (V = 1), the
+ * norms fixed-order double reductions.  Arguments as fs_apply_plan; `out` is
+ * a HOST pointer to two doubles.  Scratch is stream-ordered device memory
+ * (cudaMallocAsync/cudaFreeAsync on `stream`).  Synchronises `stream`.
+ * Errors as fs_apply_plan.
+ */
+fs_status fs_marginal_residuals(const float* X, const float* a, int64_t n,
+                                const float* Y, const float* b, int64_t m, int32_t d,
+                                float eps, const float* f, const float* g, double* out,
+                                const fs_options* opt, void* stream);
+
+/*
  * fs_sinkhorn_solve_noalloc -- the same iterations as fs_sinkhorn_solve on the
  * FP32-FMA path, for callers that cannot allocate device memory.
  *

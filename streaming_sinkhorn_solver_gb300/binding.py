@@ -29,9 +29,10 @@ _STATUS = {0: "FS_OK", 1: "FS_ERR_INVALID_ARG", 2: "FS_ERR_CUDA", 3: "FS_ERR_OOM
 PATHS = {"auto": 0, "fma": 1, "tensor": 2}
 
 EXPORTED = ("fs_sinkhorn_solve", "fs_apply_plan", "fs_barycentric", "fs_grad_x",
-            "fs_workspace_bytes", "fs_check", "fs_release", "fs_last_error", "fs_version",
-            "fs_launch_count", "fs_timing_enable", "fs_timing_read",
-            "fs_sinkhorn_solve_noalloc")
+            "fs_apply_plan_t", "fs_barycentric_y", "fs_grad_y", "fs_dual_value",
+            "fs_marginal_residuals", "fs_workspace_bytes", "fs_check", "fs_release",
+            "fs_last_error", "fs_version", "fs_launch_count", "fs_timing_enable",
+            "fs_timing_read", "fs_sinkhorn_solve_noalloc")
 
 
 class FlashSinkhornError(RuntimeError):
@@ -66,8 +67,15 @@ def load_library(path: Optional[str] = None):
         lib.fs_apply_plan.argtypes = [vp, vp, i64, vp, vp, i64, i32, f32, vp, vp, vp, i32, vp, opt, vp]
         lib.fs_barycentric.argtypes = [vp, vp, i64, vp, vp, i64, i32, f32, vp, vp, vp, opt, vp]
         lib.fs_grad_x.argtypes = [vp, vp, i64, vp, vp, i64, i32, f32, vp, vp, vp, opt, vp]
+        lib.fs_apply_plan_t.argtypes = lib.fs_apply_plan.argtypes
+        lib.fs_barycentric_y.argtypes = lib.fs_barycentric.argtypes
+        lib.fs_grad_y.argtypes = lib.fs_grad_x.argtypes
+        lib.fs_dual_value.argtypes = [vp, i64, vp, i64, vp, vp, ctypes.POINTER(ctypes.c_double), vp]
+        lib.fs_marginal_residuals.argtypes = [vp, vp, i64, vp, vp, i64, i32, f32, vp, vp,
+                                              ctypes.POINTER(ctypes.c_double), opt, vp]
         for fn in ("fs_sinkhorn_solve", "fs_apply_plan", "fs_barycentric", "fs_grad_x",
-                   "fs_check", "fs_release"):
+                   "fs_apply_plan_t", "fs_barycentric_y", "fs_grad_y", "fs_dual_value",
+                   "fs_marginal_residuals", "fs_check", "fs_release"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.fs_workspace_bytes.argtypes = [i64, i64, i32, i32, opt]
         lib.fs_workspace_bytes.restype = i64
@@ -239,6 +247,76 @@ def fs_grad_x(X, a, Y, b, eps: float, f, g, out=None, *, path: str = "auto", spl
     _raise(st)
     _host_sync(stream, X, out)
     return out
+
+
+def fs_apply_plan_t(X, a, Y, b, eps: float, f, g, U, out=None, *, path: str = "auto",
+                    splits: int = 0, check_finite: bool = False, stream=None):
+    """out = P^T U (m x k); U is n x k."""
+    n, d = X.shape
+    m = Y.shape[0]
+    squeeze = len(U.shape) == 1
+    k = 1 if squeeze else U.shape[1]
+    out = _new_like(Y, (m, k) if not squeeze else (m,)) if out is None else out
+    st = load_library().fs_apply_plan_t(
+        _ptr(X, "X", (n, d)), _ptr(a, "a", (n,)), n, _ptr(Y, "Y", (m, d)), _ptr(b, "b", (m,)), m, d,
+        float(eps), _ptr(f, "f", (n,)), _ptr(g, "g", (m,)),
+        _ptr(U, "U", (n,) if squeeze else (n, k)), k,
+        _ptr(out, "out", (m,) if squeeze else (m, k)),
+        _opts(path, splits, check_finite), _stream(stream, X))
+    _raise(st)
+    _host_sync(stream, X, out)
+    return out
+
+
+def _y_side(fn, X, a, Y, b, eps, f, g, out, path, splits, check_finite, stream):
+    n, d = X.shape
+    m = Y.shape[0]
+    out = _new_like(Y, (m, d)) if out is None else out
+    st = getattr(load_library(), fn)(
+        _ptr(X, "X", (n, d)), _ptr(a, "a", (n,)), n, _ptr(Y, "Y", (m, d)), _ptr(b, "b", (m,)), m, d,
+        float(eps), _ptr(f, "f", (n,)), _ptr(g, "g", (m,)), _ptr(out, "out", (m, d)),
+        _opts(path, splits, check_finite), _stream(stream, X))
+    _raise(st)
+    _host_sync(stream, X, out)
+    return out
+
+
+def fs_barycentric_y(X, a, Y, b, eps: float, f, g, out=None, *, path: str = "auto",
+                     splits: int = 0, check_finite: bool = False, stream=None):
+    """T_j = (P^T X)_j / b_j."""
+    return _y_side("fs_barycentric_y", X, a, Y, b, eps, f, g, out, path, splits, check_finite,
+                   stream)
+
+
+def fs_grad_y(X, a, Y, b, eps: float, f, g, out=None, *, path: str = "auto", splits: int = 0,
+              check_finite: bool = False, stream=None):
+    """grad_j = 2 (b_j y_j - (P^T X)_j)."""
+    return _y_side("fs_grad_y", X, a, Y, b, eps, f, g, out, path, splits, check_finite, stream)
+
+
+def fs_dual_value(a, b, f, g, *, stream=None) -> float:
+    """<a, f> + <b, g>, summed on the GPU in double."""
+    n, m = a.shape[0], b.shape[0]
+    out = ctypes.c_double(0.0)
+    st = load_library().fs_dual_value(_ptr(a, "a", (n,)), n, _ptr(b, "b", (m,)), m,
+                                      _ptr(f, "f", (n,)), _ptr(g, "g", (m,)), ctypes.byref(out),
+                                      _stream(stream, a))
+    _raise(st)
+    return float(out.value)
+
+
+def fs_marginal_residuals(X, a, Y, b, eps: float, f, g, *, path: str = "auto", splits: int = 0,
+                          stream=None):
+    """(||P 1 - a||_1, ||P^T 1 - b||_1)."""
+    n, d = X.shape
+    m = Y.shape[0]
+    out = (ctypes.c_double * 2)()
+    st = load_library().fs_marginal_residuals(
+        _ptr(X, "X", (n, d)), _ptr(a, "a", (n,)), n, _ptr(Y, "Y", (m, d)), _ptr(b, "b", (m,)), m, d,
+        float(eps), _ptr(f, "f", (n,)), _ptr(g, "g", (m,)), out, _opts(path, splits, False),
+        _stream(stream, X))
+    _raise(st)
+    return float(out[0]), float(out[1])
 
 
 def fs_workspace_bytes(n: int, m: int, d: int, k: int = 0, *, path: str = "auto",

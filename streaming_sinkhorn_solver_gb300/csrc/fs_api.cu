@@ -354,6 +354,39 @@ fs_status fs_grad_x(const float* X, const float* a, int64_t n, const float* Y, c
     }
 }
 
+// The Y side: P^T with the roles of (X, a, f) and (Y, b, g) exchanged, since
+// P^T_ji = b_j a_i exp((g_j + f_i - C_ji)/eps) is the same plan.
+fs_status fs_apply_plan_t(const float* X, const float* a, int64_t n, const float* Y,
+                          const float* b, int64_t m, int32_t d, float eps, const float* f,
+                          const float* g, const float* U, int32_t k, float* out,
+                          const fs_options* opt, void* stream) {
+    try {
+        return apply_entry(APPLY_PV, Y, b, m, X, a, n, d, eps, g, f, U, k, out, opt, stream);
+    } catch (...) {
+        return fail(FS_ERR_CUDA, "unexpected host exception");
+    }
+}
+
+fs_status fs_barycentric_y(const float* X, const float* a, int64_t n, const float* Y,
+                           const float* b, int64_t m, int32_t d, float eps, const float* f,
+                           const float* g, float* out, const fs_options* opt, void* stream) {
+    try {
+        return apply_entry(APPLY_BARY, Y, b, m, X, a, n, d, eps, g, f, X, d, out, opt, stream);
+    } catch (...) {
+        return fail(FS_ERR_CUDA, "unexpected host exception");
+    }
+}
+
+fs_status fs_grad_y(const float* X, const float* a, int64_t n, const float* Y, const float* b,
+                    int64_t m, int32_t d, float eps, const float* f, const float* g, float* out,
+                    const fs_options* opt, void* stream) {
+    try {
+        return apply_entry(APPLY_GRAD, Y, b, m, X, a, n, d, eps, g, f, X, d, out, opt, stream);
+    } catch (...) {
+        return fail(FS_ERR_CUDA, "unexpected host exception");
+    }
+}
+
 int64_t fs_workspace_bytes(int64_t n, int64_t m, int32_t d, int32_t k, const fs_options* opt) {
     if (n < 1 || m < 1 || d < 1 || d > kMaxDim || k < 0 || k > kMaxK) return -1;
     int dev = 0, sms = 152;

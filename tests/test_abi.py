@@ -133,3 +133,27 @@ def test_workspace_is_linear_in_sizes(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(ImportError):
         fs.load_library(str(tmp_path / "nope.so"))
+
+
+def test_y_side_and_reports_reject_bad_arguments(lib):
+    X, a, Y, b = _small()
+    f = np.zeros(4, np.float32)
+    g = np.zeros(5, np.float32)
+    U = np.zeros((4, 3), np.float32)
+    out = np.zeros((5, 3), np.float32)
+    st = lib.fs_apply_plan_t(X.ctypes.data, a.ctypes.data, 4, Y.ctypes.data, b.ctypes.data, 5, 2,
+                             0.1, f.ctypes.data, g.ctypes.data, U.ctypes.data, 0, out.ctypes.data,
+                             None, None)
+    assert st == fs.FS_ERR_INVALID_ARG
+    st = lib.fs_grad_y(X.ctypes.data, a.ctypes.data, 4, Y.ctypes.data, b.ctypes.data, 5, 2, 0.0,
+                       f.ctypes.data, g.ctypes.data, out.ctypes.data, None, None)
+    assert st == fs.FS_ERR_INVALID_ARG
+    res = (ctypes.c_double * 2)()
+    st = lib.fs_dual_value(None, 4, b.ctypes.data, 5, f.ctypes.data, g.ctypes.data, res, None)
+    assert st == fs.FS_ERR_INVALID_ARG
+    st = lib.fs_dual_value(a.ctypes.data, 0, b.ctypes.data, 5, f.ctypes.data, g.ctypes.data, res,
+                           None)
+    assert st == fs.FS_ERR_INVALID_ARG
+    st = lib.fs_marginal_residuals(X.ctypes.data, a.ctypes.data, 4, Y.ctypes.data, b.ctypes.data,
+                                   5, 2, 0.1, f.ctypes.data, g.ctypes.data, None, None, None)
+    assert st == fs.FS_ERR_INVALID_ARG
