@@ -150,6 +150,28 @@ def _traffic_from_profiles(workload: str):
         return None
 
 
+def replica_seed(w, rank: int) -> int:
+    """Weak scaling: rank r solves its own replica, drawn with seed + r."""
+    return WORKLOADS[w.name].seed + rank
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest value over the ranks of the default process group (the job
+    is as slow as its slowest rank); x itself outside a group of > 1 ranks."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(world: int, units_per_rank_step: float, steps: int, total_ms: float) -> float:
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    return world * units_per_rank_step * steps / (total_ms * 1e-3)
+
+
 def _work(w, n, m, d):
     """Algorithmic work of one step."""
     iters = w.n_iter
@@ -260,7 +282,7 @@ def run_gb300(args, w):
     fs.load_library()
     n, m, d = w.n, w.m, w.d
     # weak scaling: every rank solves its own replica of the workload
-    inp = make_inputs(w.name, seed=WORKLOADS[w.name].seed + rank)
+    inp = make_inputs(w.name, seed=replica_seed(w, rank))
     t = {k: torch.from_numpy(v).to(dev) for k, v in inp.items()}
     k_out = w.k if w.apply == "pv" else d
     t["f"] = torch.empty(n, device=dev)
@@ -271,6 +293,10 @@ def run_gb300(args, w):
     flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MB > L2
 
     stream = torch.cuda.current_stream()
+    try:
+        rates = fs.fs_unit_rates()
+    except Exception as exc:  # pragma: no cover - reported, nominal rates used
+        rates = {"error": str(exc)}
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -293,17 +319,14 @@ def run_gb300(args, w):
     torch.cuda.synchronize()
     launches = fs.fs_launch_count() - l0
     fs.fs_timing_enable(False)
-    (half_ms, apply_ms), (half_n, apply_n) = fs.fs_timing_read()
+    (half_ms, apply_ms, prep_ms), (half_n, apply_n, prep_n) = fs.fs_timing_read()
     clocks = sampler.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(step_ms)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, dev if world > 1 else None)
     iters, pairs = _work(w, n, m, d)
-    value = world * pairs * args.steps / (total_ms * 1e-3)
-    iters_per_s = world * iters * args.steps / (total_ms * 1e-3)
+    value = aggregate_rate(world, pairs, args.steps, total_ms)
+    iters_per_s = aggregate_rate(world, iters, args.steps, total_ms)
 
     # roofline of the dominant kernel (the half-update), from its own events.
     # Per launch (one f- or g-update) the algorithmic work is n*m score pairs:
@@ -316,9 +339,12 @@ def run_gb300(args, w):
     pairs_per_half = n * m
     clk = (clocks or {}).get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    ex2_peak = EX2_PER_CLK_SM * sms * clk * 1e6                       # ex2 / s
+    ex2_clk = rates.get("ex2_per_clk_sm") or EX2_PER_CLK_SM
+    fp32_clk = rates.get("fma2_lanes_per_clk_sm") or FP32_LANES_PER_CLK_SM
+    rate_src = "measured by fs_unit_rates" if "ex2_per_clk_sm" in rates else "nominal"
+    ex2_peak = ex2_clk * sms * clk * 1e6                               # ex2 / s
     fp32_ops = fp32_ops_per_pair(d, tensor_path)
-    fp32_pair_peak = FP32_LANES_PER_CLK_SM / fp32_ops * sms * clk * 1e6  # pairs / s
+    fp32_pair_peak = fp32_clk / fp32_ops * sms * clk * 1e6             # pairs / s
     tflops_peak = float(peaks["bf16_tflops_sustained"])
     hbm_peak = float(peaks["hbm_gbs"])
     op_bytes = 2 if tensor_path else 4
@@ -335,12 +361,12 @@ def run_gb300(args, w):
                                f"same nominal rate"}
     elif bound == "alu":
         achieved = pairs_per_half / t_launch / 1e9
-        per_clk = min(EX2_PER_CLK_SM, FP32_LANES_PER_CLK_SM / fp32_ops)
+        per_clk = min(ex2_clk, fp32_clk / fp32_ops)
         roof = {"bound": "alu", "achieved": achieved, "peak": alu_peak / 1e9, "unit": "Gpair/s",
-                "peak_source": f"derived: min(MUFU {EX2_PER_CLK_SM} ex2/clk/SM, FP32 "
-                               f"{FP32_LANES_PER_CLK_SM} lanes/clk/SM / {fp32_ops} lane-ops per "
-                               f"pair) = {per_clk:.1f} pairs/clk/SM x {sms} SMs x {clk:.0f} MHz "
-                               f"(median SM clock sampled in the timed region)",
+                "peak_source": f"derived: min(MUFU {ex2_clk:.1f} ex2/clk/SM, FP32 "
+                               f"{fp32_clk:.1f} lanes/clk/SM / {fp32_ops} lane-ops per "
+                               f"pair) = {per_clk:.1f} pairs/clk/SM ({rate_src}) x {sms} SMs x "
+                               f"{clk:.0f} MHz (median SM clock sampled in the timed region)",
                 "mufu_frac": achieved * 1e9 / ex2_peak,
                 "fp32_frac": achieved * 1e9 / fp32_pair_peak}
     else:
@@ -354,6 +380,7 @@ def run_gb300(args, w):
     roof["launches"] = half_n
     roof["roofline_ms"] = {k[:-2]: v * 1e3 for k, v in terms.items()}
     roof["algorithmic_bytes_per_launch"] = alg_bytes
+    roof["unit_rates"] = dict(rates, source=rate_src)
 
     line = {"metric": METRIC, "value": value, "unit": "score-pairs/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
@@ -365,7 +392,13 @@ def run_gb300(args, w):
                              if (n + m) * d * 4 > 129e6 else "256 MB write between timed steps"},
             "iters_per_s": iters_per_s, "roofline": roof, "gpu_launches": int(launches),
             "clocks": clocks,
-            "apply_ms": apply_ms / max(apply_n, 1) if apply_n else None}
+            "apply_ms": apply_ms / max(apply_n, 1) if apply_n else None,
+            # preparation (centring, norms, operand packing/tiling) per solve call,
+            # included in ms_per_step; and the device workspace the calls use
+            "prep_ms_per_step": prep_ms / args.steps,
+            "workspace_bytes": int(max(fs.fs_workspace_bytes(n, m, d, 0, path=path),
+                                       fs.fs_workspace_bytes(n, m, d, k_out, path=path)
+                                       if w.apply else 0))}
 
     # end to end through the C ABI with pinned host buffers
     if not args.no_e2e:
@@ -395,8 +428,8 @@ def run_gb300(args, w):
         if w.apply:
             h2d += fb * (n * d + n + m * d + m + n + m + (m * w.k if w.apply == "pv" else 0))
             d2h += fb * n * k_out
-        e2e_total = sum(e2e_ms)
-        line["e2e"] = {"value": world * pairs * len(e2e_ms) / (e2e_total * 1e-3),
+        e2e_total = max_over_ranks(sum(e2e_ms), dev if world > 1 else None)
+        line["e2e"] = {"value": aggregate_rate(world, pairs, len(e2e_ms), e2e_total),
                        "unit": "score-pairs/s", "h2d_bytes_per_step": int(h2d),
                        "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_total / len(e2e_ms),
                        "timer": "host wall clock around the C-ABI calls, stream synchronised"}

@@ -238,6 +238,22 @@ fs_status fs_sinkhorn_solve_noalloc(const float* X, const float* a, int64_t n,
                                     float eps, int32_t n_iter, float* f, float* g,
                                     void* stream);
 
+/*
+ * fs_unit_rates -- measure, on the current GPU, the per-SM issue rates that
+ * bound the exponent-heavy half-updates (no counterpart on the pages: it
+ * supplies the denominators of the ALU roofline).  Throughput kernels with
+ * independent dependency chains, four 256-thread blocks per SM, counted in
+ * SM cycles (clock64), so the rates do not depend on the clock:
+ *   out[0]  ex2.approx.ftz.f32 results per clock per SM (MUFU)
+ *   out[1]  fma.rn.f32x2 lane results per clock per SM (packed FP32)
+ *   out[2]  fma.rn.f32 results per clock per SM (scalar FP32)
+ *   out[3]  3-input max.f32 results per clock per SM
+ *   out[4]  SM count
+ * `out` is a HOST pointer to five doubles.  Takes a few milliseconds; uses a
+ * little stream-ordered scratch; synchronises `stream`.
+ */
+fs_status fs_unit_rates(double* out, void* stream);
+
 /* Device bytes the library's workspace needs for these sizes (k = 0 for a
  * solve).  The workspace is O((n + m) d): no n x m buffer exists. */
 int64_t fs_workspace_bytes(int64_t n, int64_t m, int32_t d, int32_t k, const fs_options* opt);
@@ -261,13 +277,15 @@ int64_t fs_launch_count(void);
 
 /* Kernel timing, a benchmarking aid.  While enabled (on != 0), the library
  * records a pair of CUDA events on the launching stream around every launch
- * of its half-update kernel (kind 0) and plan-application kernel (kind 1).
- * fs_timing_read synchronises those events and returns, per kind, the summed
- * elapsed milliseconds and the number of launches since the previous read,
- * then starts a new count.  Either output pointer may be NULL.  Enabling
- * adds two event records per timed launch and nothing else. */
+ * of its half-update kernel (kind 0), its plan-application kernel (kind 1)
+ * and the preparation of a call (kind 2: centring, norms, operand packing or
+ * tiling, initial biases).  fs_timing_read synchronises those events and
+ * returns, per kind, the summed elapsed milliseconds and the number of timed
+ * regions since the previous read, then starts a new count.  Either output
+ * pointer may be NULL.  Enabling adds two event records per timed region and
+ * nothing else. */
 fs_status fs_timing_enable(int32_t on);
-fs_status fs_timing_read(double* ms_by_kind /* [2] */, int64_t* launches_by_kind /* [2] */);
+fs_status fs_timing_read(double* ms_by_kind /* [3] */, int64_t* launches_by_kind /* [3] */);
 
 #ifdef __cplusplus
 }

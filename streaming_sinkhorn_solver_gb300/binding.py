@@ -32,7 +32,7 @@ EXPORTED = ("fs_sinkhorn_solve", "fs_apply_plan", "fs_barycentric", "fs_grad_x",
             "fs_apply_plan_t", "fs_barycentric_y", "fs_grad_y", "fs_dual_value",
             "fs_marginal_residuals", "fs_workspace_bytes", "fs_check", "fs_release",
             "fs_last_error", "fs_version", "fs_launch_count", "fs_timing_enable",
-            "fs_timing_read", "fs_sinkhorn_solve_noalloc")
+            "fs_timing_read", "fs_sinkhorn_solve_noalloc", "fs_unit_rates")
 
 
 class FlashSinkhornError(RuntimeError):
@@ -90,6 +90,8 @@ def load_library(path: Optional[str] = None):
         lib.fs_timing_read.restype = ctypes.c_int
         lib.fs_sinkhorn_solve_noalloc.argtypes = [vp, vp, i64, vp, vp, i64, i32, f32, i32, vp, vp, vp]
         lib.fs_sinkhorn_solve_noalloc.restype = ctypes.c_int
+        lib.fs_unit_rates.argtypes = [ctypes.POINTER(ctypes.c_double), vp]
+        lib.fs_unit_rates.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -319,6 +321,14 @@ def fs_marginal_residuals(X, a, Y, b, eps: float, f, g, *, path: str = "auto", s
     return float(out[0]), float(out[1])
 
 
+def fs_unit_rates(stream=None) -> dict:
+    """Measured per-SM rates (results per clock per SM) and the SM count."""
+    out = (ctypes.c_double * 5)()
+    _raise(load_library().fs_unit_rates(out, _stream(stream)))
+    return {"ex2_per_clk_sm": out[0], "fma2_lanes_per_clk_sm": out[1],
+            "fma_per_clk_sm": out[2], "max3_per_clk_sm": out[3], "sms": int(out[4])}
+
+
 def fs_workspace_bytes(n: int, m: int, d: int, k: int = 0, *, path: str = "auto",
                        splits: int = 0) -> int:
     return int(load_library().fs_workspace_bytes(n, m, d, k, _opts(path, splits, False)))
@@ -349,11 +359,11 @@ def fs_timing_enable(on: bool = True) -> None:
 
 
 def fs_timing_read():
-    """Returns ((half_ms, apply_ms), (half_launches, apply_launches)) since the last read."""
-    ms = (ctypes.c_double * 2)()
-    cnt = (ctypes.c_int64 * 2)()
+    """Returns ((half_ms, apply_ms, prep_ms), (half_n, apply_n, prep_n)) since the last read."""
+    ms = (ctypes.c_double * 3)()
+    cnt = (ctypes.c_int64 * 3)()
     _raise(load_library().fs_timing_read(ms, cnt))
-    return (ms[0], ms[1]), (int(cnt[0]), int(cnt[1]))
+    return (ms[0], ms[1], ms[2]), (int(cnt[0]), int(cnt[1]), int(cnt[2]))
 
 
 def fs_sinkhorn_solve_noalloc(X, a, Y, b, eps: float, n_iter: int, f, g, *, stream=None):

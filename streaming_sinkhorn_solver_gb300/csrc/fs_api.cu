@@ -449,11 +449,11 @@ fs_status fs_timing_enable(int32_t on) {
 
 fs_status fs_timing_read(double* ms_by_kind, int64_t* launches_by_kind) {
     std::lock_guard<std::mutex> lk(g_timing.mu);
-    double ms[2] = {0.0, 0.0};
-    int64_t cnt[2] = {0, 0};
+    double ms[TIME_KINDS] = {};
+    int64_t cnt[TIME_KINDS] = {};
     for (size_t i = 0; i < g_timing.used; ++i) {
         const int k = g_timing.kind[i];
-        if (k < 0 || k > 1) continue;
+        if (k < 0 || k >= TIME_KINDS) continue;
         FS_CUDA(cudaEventSynchronize(g_timing.pool[2 * i + 1]));
         float t = 0.f;
         FS_CUDA(cudaEventElapsedTime(&t, g_timing.pool[2 * i], g_timing.pool[2 * i + 1]));
@@ -461,8 +461,10 @@ fs_status fs_timing_read(double* ms_by_kind, int64_t* launches_by_kind) {
         cnt[k] += 1;
     }
     g_timing.used = 0;
-    if (ms_by_kind) { ms_by_kind[0] = ms[0]; ms_by_kind[1] = ms[1]; }
-    if (launches_by_kind) { launches_by_kind[0] = cnt[0]; launches_by_kind[1] = cnt[1]; }
+    for (int k = 0; k < TIME_KINDS; ++k) {
+        if (ms_by_kind) ms_by_kind[k] = ms[k];
+        if (launches_by_kind) launches_by_kind[k] = cnt[k];
+    }
     return FS_OK;
 }
 

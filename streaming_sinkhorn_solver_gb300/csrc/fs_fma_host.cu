@@ -99,12 +99,14 @@ fs_status solve_fma(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) 
     float* lby = c.at<float>(B.lby);
     float2* part = c.at<float2>(B.partial);
 
+    const int tp = timing_begin(c.stream);
     FS_CUDA(launch_shift(P.X.dev, n, P.Y.dev, m, d, c.at<double>(B.shift_part), kShiftBlocks, shift,
                          c.stream));
     FS_CUDA(launch_pack_fma(P.X.dev, P.a.dev, nullptr, n, d, p.D, shift, l_over_eps, PX, nx, lax,
                             c.stream));
     FS_CUDA(launch_pack_fma(P.Y.dev, P.b.dev, P.g.dev, m, d, p.D, shift, l_over_eps, PY, ny, lby,
                             c.stream));
+    timing_end(tp, TIME_PREP, c.stream);
 
     int* fix_list = c.at<int>(B.fix_list);
     unsigned int* fix_count = c.at<unsigned int>(B.fix_count);

@@ -85,7 +85,7 @@ fs_status scan_finite(Call& c, const float* v, int64_t len, unsigned int* counte
 
 // Kernel timing (fs_timing_enable / fs_timing_read).  timing_begin returns a
 // slot (or -1 when timing is off); timing_end closes it.
-enum TimingKind : int { TIME_HALF = 0, TIME_APPLY = 1 };
+enum TimingKind : int { TIME_HALF = 0, TIME_APPLY = 1, TIME_PREP = 2, TIME_KINDS = 3 };
 int timing_begin(cudaStream_t s);
 void timing_end(int slot, int kind, cudaStream_t s);
 

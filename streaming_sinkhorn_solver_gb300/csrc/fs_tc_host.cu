@@ -182,7 +182,9 @@ fs_status solve_tc(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) {
     FS_TRY(ensure_capacity(c));
     for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g}) bind(c, *A);
     for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.g}) FS_TRY(upload(c, *A));
+    const int tp = timing_begin(c.stream);
     FS_TRY(prep_tc(c, P, p, B, true));
+    timing_end(tp, TIME_PREP, c.stream);
 
     const float eps_ln2 = (float)((double)P.eps * kLn2);
     float2* part = c.at<float2>(B.partial);
