@@ -77,6 +77,7 @@ def _load():
     lib.orc_num_threads.restype = _INT
     lib.orc_set_num_threads.argtypes = [_INT]
     lib.orc_cost.argtypes = [_f32, _I64, _f32, _I64, _INT, _f64]
+    lib.orc_cost_cosine.argtypes = [_f32, _I64, _f32, _I64, _INT, _f64]
     lib.orc_f_update.argtypes = [_f64, _I64, _I64, _f32, _DBL, _f64, _f64]
     lib.orc_g_update.argtypes = [_f64, _I64, _I64, _f32, _DBL, _f64, _f64]
     lib.orc_sinkhorn.argtypes = [_f64, _I64, _I64, _f32, _f32, _DBL, _INT, _f64, _f64]
@@ -164,6 +165,16 @@ def cost(X, Y) -> np.ndarray:
     m = Y.shape[0]
     C = np.empty((n, m), dtype=np.float64)
     _load().orc_cost(X, n, Y, m, d, C)
+    return C
+
+
+def cost_cosine(X, Y) -> np.ndarray:
+    """C_ij = 2 - 2 cos(x_i, y_j), from its definition (zero rows: see the C source)."""
+    X, Y = _c32(X), _c32(Y)
+    n, d = X.shape
+    m = Y.shape[0]
+    C = np.empty((n, m), dtype=np.float64)
+    _load().orc_cost_cosine(X, n, Y, m, d, C)
     return C
 
 
@@ -256,6 +267,22 @@ def grad_x(C, X, a, b, eps, f, g, Y) -> np.ndarray:
     """grad_i = 2 (a_i x_i - (P Y)_i)."""
     PY = apply_plan(C, a, b, eps, f, g, Y)
     return 2.0 * (np.asarray(a, dtype=np.float64)[:, None] * np.asarray(X, dtype=np.float64) - PY)
+
+
+def grad_x_cosine(C, X, a, b, eps, f, g, Y) -> np.ndarray:
+    """Gradient with respect to the raw x_i under the cosine cost: the chain
+    rule through x^_i = x_i / |x_i| applied to 2 (a_i x^_i - (P Y^)_i), i.e.
+    J_i^T of it with J_i = (I - x^_i x^_i^T) / |x_i| (zero rows: 0)."""
+    X = np.asarray(X, dtype=np.float64)
+    Y = np.asarray(Y, dtype=np.float64)
+    nx = np.linalg.norm(X, axis=1)
+    ny = np.linalg.norm(Y, axis=1)
+    Xh = np.where(nx[:, None] > 0, X / np.where(nx > 0, nx, 1.0)[:, None], 0.0)
+    Yh = np.where(ny[:, None] > 0, Y / np.where(ny > 0, ny, 1.0)[:, None], 0.0)
+    G = 2.0 * (np.asarray(a, dtype=np.float64)[:, None] * Xh
+               - apply_plan(C, a, b, eps, f, g, Yh.astype(np.float32)))
+    G = G - np.sum(Xh * G, axis=1, keepdims=True) * Xh
+    return np.where(nx[:, None] > 0, G / np.where(nx > 0, nx, 1.0)[:, None], 0.0)
 
 
 def marginals(C, a, b, eps, f, g) -> Tuple[np.ndarray, np.ndarray]:

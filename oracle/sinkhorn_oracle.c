@@ -71,6 +71,35 @@ void orc_cost(const float* X, int64_t n, const float* Y, int64_t m, int d, doubl
             C[i * m + j] = sqdist(X + i * d, Y + j * d, d);
 }
 
+/* C (n x m, double) = cosine cost, written from its definition
+ * C_ij = 2 - 2 cos(x_i, y_j) = 2 - 2 x_i.y_j / (|x_i| |y_j|)
+ * (the pages' Discussion: the cosine cost is the squared-Euclidean cost of
+ * the normalised points).  A zero row is taken as the zero vector after
+ * normalisation, so its cost to a nonzero point is 1 and to a zero point 0:
+ * C_ij = [x_i != 0] + [y_j != 0] - 2 x_i.y_j / (|x_i| |y_j|), the last term
+ * 0 when either norm is 0. */
+void orc_cost_cosine(const float* X, int64_t n, const float* Y, int64_t m, int d, double* C) {
+    double* ny = (double*)malloc(sizeof(double) * (size_t)(m > 0 ? m : 1));
+    for (int64_t j = 0; j < m; ++j) {
+        double s = 0.0;
+        for (int k = 0; k < d; ++k) s += (double)Y[j * d + k] * (double)Y[j * d + k];
+        ny[j] = sqrt(s);
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        double s = 0.0;
+        for (int k = 0; k < d; ++k) s += (double)X[i * d + k] * (double)X[i * d + k];
+        const double nx = sqrt(s);
+        for (int64_t j = 0; j < m; ++j) {
+            double dot = 0.0;
+            for (int k = 0; k < d; ++k) dot += (double)X[i * d + k] * (double)Y[j * d + k];
+            const double cosv = (nx > 0.0 && ny[j] > 0.0) ? dot / (nx * ny[j]) : 0.0;
+            C[i * m + j] = (nx > 0.0 ? 1.0 : 0.0) + (ny[j] > 0.0 ? 1.0 : 0.0) - 2.0 * cosv;
+        }
+    }
+    free(ny);
+}
+
 /* log sum_j exp(z_j), shifted by the maximum; sums in index order. */
 static double lse(const double* z, int64_t len) {
     double M = -INFINITY;

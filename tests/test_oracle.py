@@ -339,3 +339,62 @@ def test_workload_inputs_have_recipe_shapes():
         assert (inp["a"] > 0).all() and (inp["b"] > 0).all()
     c4 = make_inputs("c4_n50k_d512", n=20, m=30)
     np.testing.assert_allclose(np.linalg.norm(c4["X"], axis=1), 1, atol=1e-6)
+
+
+# --- cosine cost (the pages' Discussion: cosine as squared-Euclidean on
+# normalised points, C = 2 - 2 cos) ---------------------------------------
+
+def test_cosine_cost_special_values():
+    """Same direction 0, orthogonal 2, opposite 4, whatever the lengths; a zero
+    row costs 1 against a nonzero point and 0 against another zero row."""
+    X = np.array([[2.0, 0.0], [0.0, 0.0]], np.float32)
+    Y = np.array([[5.0, 0.0], [0.0, 0.3], [-1.0, 0.0], [0.0, 0.0]], np.float32)
+    C = orc.cost_cosine(X, Y)
+    np.testing.assert_allclose(C, [[0.0, 2.0, 4.0, 1.0], [1.0, 1.0, 1.0, 0.0]], atol=1e-15)
+
+
+def test_cosine_cost_equals_squared_euclidean_on_unit_rows():
+    """On unit rows 2 - 2 cos(x, y) = |x - y|^2: the definition against the
+    squared-Euclidean oracle cost (a different formula)."""
+    rng = np.random.default_rng(5)
+    X = rng.standard_normal((40, 7))
+    Y = rng.standard_normal((30, 7))
+    X = (X / np.linalg.norm(X, axis=1, keepdims=True)).astype(np.float32)
+    Y = (Y / np.linalg.norm(Y, axis=1, keepdims=True)).astype(np.float32)
+    np.testing.assert_allclose(orc.cost_cosine(X, Y), orc.cost(X, Y), atol=2e-7)
+
+
+def test_cosine_cost_invariant_to_positive_row_scaling():
+    rng = np.random.default_rng(6)
+    X = rng.standard_normal((25, 5)).astype(np.float32)
+    Y = rng.standard_normal((20, 5)).astype(np.float32)
+    s = rng.uniform(0.1, 10.0, (25, 1)).astype(np.float32)
+    t = rng.uniform(0.1, 10.0, (20, 1)).astype(np.float32)
+    np.testing.assert_allclose(orc.cost_cosine(X * s, Y * t), orc.cost_cosine(X, Y), atol=1e-6)
+
+
+def test_grad_x_cosine_matches_finite_differences():
+    """At convergence under the cosine cost, d/dx_i (<a,f*> + <b,g*>) equals
+    the chain rule through the normalisation (envelope theorem)."""
+    c = _cloud(6, 7, 3, 37, weights="lognormal")
+    X, Y, a, b = c["X"], c["Y"], c["a"], c["b"]
+    eps, iters = 0.3, 600
+
+    def dual_cos(Xv):
+        C = orc.cost_cosine(Xv, Y)
+        f, g = orc.sinkhorn(C, a, b, eps, iters)
+        return orc.dual(a, b, f, g), C, f, g
+
+    _, C, f, g = dual_cos(X)
+    grad = orc.grad_x_cosine(C, X, a, b, eps, f, g, Y)
+    fd = np.zeros_like(grad)
+    for i in range(X.shape[0]):
+        for k in range(X.shape[1]):
+            Xp = X.copy(); Xm = X.copy()
+            Xp[i, k] = np.float32(X[i, k] + np.float32(2e-3))
+            Xm[i, k] = np.float32(X[i, k] - np.float32(2e-3))
+            h = float(Xp[i, k]) - float(Xm[i, k])
+            fd[i, k] = (dual_cos(Xp)[0] - dual_cos(Xm)[0]) / h
+    np.testing.assert_allclose(grad, fd, rtol=2e-4, atol=2e-5 * np.abs(grad).max())
+    # the gradient is orthogonal to x_i (a cosine cost cannot change along it)
+    assert np.abs(np.sum(grad * X.astype(np.float64), axis=1)).max() <= 1e-12 * np.abs(grad).max() * 10

@@ -29,6 +29,8 @@ MUTANTS = [
     ("plan_no_a", "orc_apply_plan", "double p = (double)a[i] * (double)b[j]",
      "double p = (double)b[j]"),
     ("prop1_no_ynorm", "orc_f_update_prop1", "double ghat = g[j] - yy;", "double ghat = g[j];"),
+    ("cosine_no_factor2", "orc_cost_cosine", "- 2.0 * cosv;", "- cosv;"),
+    ("cosine_no_ynorm", "orc_cost_cosine", "dot / (nx * ny[j])", "dot / nx"),
 ]
 
 PINS = [
@@ -43,6 +45,8 @@ PINS = [
     lambda: pins.test_gauge_invariance_of_plan_and_update_equivariance(),
     lambda: pins.test_large_eps_plan_is_product_measure(),
     lambda: pins.test_grad_x_matches_finite_differences(),
+    lambda: pins.test_cosine_cost_special_values(),
+    lambda: pins.test_cosine_cost_equals_squared_euclidean_on_unit_rows(),
 ]
 
 
