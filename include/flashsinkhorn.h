@@ -77,12 +77,28 @@ typedef enum {
 } fs_path;
 
 /* Optional tuning and checking knobs; pass NULL for the defaults (all zero). */
+
+/* Ground cost.  FS_COST_COSINE is the pages' cosine cost (Discussion):
+ * C_ij = 2 - 2 cos(x_i, y_j), evaluated as the squared-Euclidean cost of the
+ * normalised rows x_i / |x_i|, y_j / |y_j| (a zero row stays zero: its cost
+ * is 1 to a nonzero point).  Plan applications use that plan with the
+ * caller's V; fs_barycentric (and fs_barycentric_y) average the normalised
+ * points; fs_grad_x (fs_grad_y) returns the gradient with respect to the
+ * caller's x_i (y_j): the squared-Euclidean gradient at the normalised points
+ * multiplied by (I - x^ x^T) / |x| (zero for a zero row).  The normalised
+ * copies take (n + m) d floats of workspace more. */
+typedef enum {
+    FS_COST_SQEUCLIDEAN = 0,
+    FS_COST_COSINE = 1
+} fs_cost;
+
 typedef struct fs_options {
     int32_t path;          /* fs_path */
     int32_t splits;        /* column splits per half-update; 0 = choose from the SM count */
     int32_t check_finite;  /* nonzero: after the call, scan the outputs and return
                               FS_ERR_NONFINITE if any is NaN/Inf (synchronises) */
-    int32_t reserved[5];   /* must be zero */
+    int32_t cost;          /* fs_cost; 0 = squared Euclidean */
+    int32_t reserved[4];   /* must be zero */
 } fs_options;
 
 /*

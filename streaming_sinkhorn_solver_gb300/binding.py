@@ -41,9 +41,13 @@ class FlashSinkhornError(RuntimeError):
         self.status = status
 
 
+COSTS = {"sqeuclidean": 0, "cosine": 1}
+
+
 class fs_options(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("splits", ctypes.c_int32),
-                ("check_finite", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5)]
+                ("check_finite", ctypes.c_int32), ("cost", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 4)]
 
 
 _lib = None
@@ -143,11 +147,12 @@ def _stream(stream, *xs):
     return ctypes.c_void_p(0)
 
 
-def _opts(path: str, splits: int, check_finite: bool):
+def _opts(path: str, splits: int, check_finite: bool, cost: str = "sqeuclidean"):
     o = fs_options()
     o.path = PATHS[path]
     o.splits = int(splits)
     o.check_finite = 1 if check_finite else 0
+    o.cost = COSTS[cost]
     return ctypes.byref(o)
 
 
@@ -185,7 +190,7 @@ def _zeros_like(ref, shape):
 # ---------------------------------------------------------------------------
 # the C ABI, one function each
 
-def fs_sinkhorn_solve(X, a, Y, b, eps: float, n_iter: int, f=None, g=None, *, path: str = "auto",
+def fs_sinkhorn_solve(X, a, Y, b, eps: float, n_iter: int, f=None, g=None, *, path: str = "auto", cost: str = "sqeuclidean",
                       splits: int = 0, check_finite: bool = False, stream=None) -> Tuple:
     """n_iter log-domain Sinkhorn iterations; f, g are in/out (g seeds the first
     f-update, zeros if None).  Returns (f, g)."""
@@ -196,13 +201,13 @@ def fs_sinkhorn_solve(X, a, Y, b, eps: float, n_iter: int, f=None, g=None, *, pa
     st = load_library().fs_sinkhorn_solve(
         _ptr(X, "X", (n, d)), _ptr(a, "a", (n,)), n, _ptr(Y, "Y", (m, d)), _ptr(b, "b", (m,)), m, d,
         float(eps), int(n_iter), _ptr(f, "f", (n,)), _ptr(g, "g", (m,)),
-        _opts(path, splits, check_finite), _stream(stream, X))
+        _opts(path, splits, check_finite, cost), _stream(stream, X))
     _raise(st)
     _host_sync(stream, X, f, g)
     return f, g
 
 
-def fs_apply_plan(X, a, Y, b, eps: float, f, g, V, out=None, *, path: str = "auto",
+def fs_apply_plan(X, a, Y, b, eps: float, f, g, V, out=None, *, path: str = "auto", cost: str = "sqeuclidean",
                   splits: int = 0, check_finite: bool = False, stream=None):
     """out = P V with P_ij = a_i b_j exp((f_i + g_j - C_ij)/eps); V is m x k."""
     n, d = X.shape
@@ -215,13 +220,13 @@ def fs_apply_plan(X, a, Y, b, eps: float, f, g, V, out=None, *, path: str = "aut
         float(eps), _ptr(f, "f", (n,)), _ptr(g, "g", (m,)),
         _ptr(V, "V", (m,) if squeeze else (m, k)), k,
         _ptr(out, "out", (n,) if squeeze else (n, k)),
-        _opts(path, splits, check_finite), _stream(stream, X))
+        _opts(path, splits, check_finite, cost), _stream(stream, X))
     _raise(st)
     _host_sync(stream, X, out)
     return out
 
 
-def fs_barycentric(X, a, Y, b, eps: float, f, g, out=None, *, path: str = "auto",
+def fs_barycentric(X, a, Y, b, eps: float, f, g, out=None, *, path: str = "auto", cost: str = "sqeuclidean",
                    splits: int = 0, check_finite: bool = False, stream=None):
     """T_i = (P Y)_i / a_i."""
     n, d = X.shape
@@ -230,13 +235,13 @@ def fs_barycentric(X, a, Y, b, eps: float, f, g, out=None, *, path: str = "auto"
     st = load_library().fs_barycentric(
         _ptr(X, "X", (n, d)), _ptr(a, "a", (n,)), n, _ptr(Y, "Y", (m, d)), _ptr(b, "b", (m,)), m, d,
         float(eps), _ptr(f, "f", (n,)), _ptr(g, "g", (m,)), _ptr(out, "out", (n, d)),
-        _opts(path, splits, check_finite), _stream(stream, X))
+        _opts(path, splits, check_finite, cost), _stream(stream, X))
     _raise(st)
     _host_sync(stream, X, out)
     return out
 
 
-def fs_grad_x(X, a, Y, b, eps: float, f, g, out=None, *, path: str = "auto", splits: int = 0,
+def fs_grad_x(X, a, Y, b, eps: float, f, g, out=None, *, path: str = "auto", cost: str = "sqeuclidean", splits: int = 0,
               check_finite: bool = False, stream=None):
     """grad_i = 2 (a_i x_i - (P Y)_i)."""
     n, d = X.shape
@@ -245,13 +250,13 @@ def fs_grad_x(X, a, Y, b, eps: float, f, g, out=None, *, path: str = "auto", spl
     st = load_library().fs_grad_x(
         _ptr(X, "X", (n, d)), _ptr(a, "a", (n,)), n, _ptr(Y, "Y", (m, d)), _ptr(b, "b", (m,)), m, d,
         float(eps), _ptr(f, "f", (n,)), _ptr(g, "g", (m,)), _ptr(out, "out", (n, d)),
-        _opts(path, splits, check_finite), _stream(stream, X))
+        _opts(path, splits, check_finite, cost), _stream(stream, X))
     _raise(st)
     _host_sync(stream, X, out)
     return out
 
 
-def fs_apply_plan_t(X, a, Y, b, eps: float, f, g, U, out=None, *, path: str = "auto",
+def fs_apply_plan_t(X, a, Y, b, eps: float, f, g, U, out=None, *, path: str = "auto", cost: str = "sqeuclidean",
                     splits: int = 0, check_finite: bool = False, stream=None):
     """out = P^T U (m x k); U is n x k."""
     n, d = X.shape
@@ -264,36 +269,37 @@ def fs_apply_plan_t(X, a, Y, b, eps: float, f, g, U, out=None, *, path: str = "a
         float(eps), _ptr(f, "f", (n,)), _ptr(g, "g", (m,)),
         _ptr(U, "U", (n,) if squeeze else (n, k)), k,
         _ptr(out, "out", (m,) if squeeze else (m, k)),
-        _opts(path, splits, check_finite), _stream(stream, X))
+        _opts(path, splits, check_finite, cost), _stream(stream, X))
     _raise(st)
     _host_sync(stream, X, out)
     return out
 
 
-def _y_side(fn, X, a, Y, b, eps, f, g, out, path, splits, check_finite, stream):
+def _y_side(fn, X, a, Y, b, eps, f, g, out, path, splits, check_finite, stream, cost="sqeuclidean"):
     n, d = X.shape
     m = Y.shape[0]
     out = _new_like(Y, (m, d)) if out is None else out
     st = getattr(load_library(), fn)(
         _ptr(X, "X", (n, d)), _ptr(a, "a", (n,)), n, _ptr(Y, "Y", (m, d)), _ptr(b, "b", (m,)), m, d,
         float(eps), _ptr(f, "f", (n,)), _ptr(g, "g", (m,)), _ptr(out, "out", (m, d)),
-        _opts(path, splits, check_finite), _stream(stream, X))
+        _opts(path, splits, check_finite, cost), _stream(stream, X))
     _raise(st)
     _host_sync(stream, X, out)
     return out
 
 
-def fs_barycentric_y(X, a, Y, b, eps: float, f, g, out=None, *, path: str = "auto",
+def fs_barycentric_y(X, a, Y, b, eps: float, f, g, out=None, *, path: str = "auto", cost: str = "sqeuclidean",
                      splits: int = 0, check_finite: bool = False, stream=None):
     """T_j = (P^T X)_j / b_j."""
     return _y_side("fs_barycentric_y", X, a, Y, b, eps, f, g, out, path, splits, check_finite,
-                   stream)
+                   stream, cost)
 
 
-def fs_grad_y(X, a, Y, b, eps: float, f, g, out=None, *, path: str = "auto", splits: int = 0,
+def fs_grad_y(X, a, Y, b, eps: float, f, g, out=None, *, path: str = "auto", cost: str = "sqeuclidean", splits: int = 0,
               check_finite: bool = False, stream=None):
     """grad_j = 2 (b_j y_j - (P^T X)_j)."""
-    return _y_side("fs_grad_y", X, a, Y, b, eps, f, g, out, path, splits, check_finite, stream)
+    return _y_side("fs_grad_y", X, a, Y, b, eps, f, g, out, path, splits, check_finite, stream,
+                   cost)
 
 
 def fs_dual_value(a, b, f, g, *, stream=None) -> float:
@@ -307,7 +313,7 @@ def fs_dual_value(a, b, f, g, *, stream=None) -> float:
     return float(out.value)
 
 
-def fs_marginal_residuals(X, a, Y, b, eps: float, f, g, *, path: str = "auto", splits: int = 0,
+def fs_marginal_residuals(X, a, Y, b, eps: float, f, g, *, path: str = "auto", cost: str = "sqeuclidean", splits: int = 0,
                           stream=None):
     """(||P 1 - a||_1, ||P^T 1 - b||_1)."""
     n, d = X.shape
@@ -315,7 +321,7 @@ def fs_marginal_residuals(X, a, Y, b, eps: float, f, g, *, path: str = "auto", s
     out = (ctypes.c_double * 2)()
     st = load_library().fs_marginal_residuals(
         _ptr(X, "X", (n, d)), _ptr(a, "a", (n,)), n, _ptr(Y, "Y", (m, d)), _ptr(b, "b", (m,)), m, d,
-        float(eps), _ptr(f, "f", (n,)), _ptr(g, "g", (m,)), out, _opts(path, splits, False),
+        float(eps), _ptr(f, "f", (n,)), _ptr(g, "g", (m,)), out, _opts(path, splits, False, cost),
         _stream(stream, X))
     _raise(st)
     return float(out[0]), float(out[1])
@@ -329,9 +335,9 @@ def fs_unit_rates(stream=None) -> dict:
             "fma_per_clk_sm": out[2], "max3_per_clk_sm": out[3], "sms": int(out[4])}
 
 
-def fs_workspace_bytes(n: int, m: int, d: int, k: int = 0, *, path: str = "auto",
+def fs_workspace_bytes(n: int, m: int, d: int, k: int = 0, *, path: str = "auto", cost: str = "sqeuclidean",
                        splits: int = 0) -> int:
-    return int(load_library().fs_workspace_bytes(n, m, d, k, _opts(path, splits, False)))
+    return int(load_library().fs_workspace_bytes(n, m, d, k, _opts(path, splits, False, cost)))
 
 
 def fs_check(stream=None) -> None:

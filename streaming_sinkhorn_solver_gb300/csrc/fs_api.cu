@@ -232,8 +232,10 @@ fs_status check_common(const float* X, const float* a, int64_t n, const float* Y
     if (!(eps > 0.f) || !std::isfinite(eps))
         return fail(FS_ERR_INVALID_ARG, "eps must be positive and finite (got %g)", (double)eps);
     if (opt) {
-        for (int i = 0; i < 5; ++i)
+        for (int i = 0; i < 4; ++i)
             if (opt->reserved[i]) return fail(FS_ERR_INVALID_ARG, "fs_options.reserved must be zero");
+        if (opt->cost < FS_COST_SQEUCLIDEAN || opt->cost > FS_COST_COSINE)
+            return fail(FS_ERR_INVALID_ARG, "fs_options.cost=%d", opt->cost);
         if (opt->path < FS_PATH_AUTO || opt->path > FS_PATH_TENSOR)
             return fail(FS_ERR_INVALID_ARG, "fs_options.path=%d", opt->path);
         if (opt->splits < 0) return fail(FS_ERR_INVALID_ARG, "fs_options.splits=%d", opt->splits);
@@ -265,6 +267,7 @@ fs_status solve_entry(const float* X, const float* a, int64_t n, const float* Y,
     FS_TRY(begin_call(c, stream));
     Problem P;
     P.n = n; P.m = m; P.d = d; P.eps = eps;
+    P.cost = opt ? opt->cost : FS_COST_SQEUCLIDEAN;
     FS_TRY(classify(c, P.X, X, (size_t)n * d));
     FS_TRY(classify(c, P.a, a, (size_t)n));
     FS_TRY(classify(c, P.Y, Y, (size_t)m * d));
@@ -288,6 +291,7 @@ fs_status apply_entry(int mode, const float* X, const float* a, int64_t n, const
     FS_TRY(begin_call(c, stream));
     Problem P;
     P.n = n; P.m = m; P.d = d; P.k = k; P.eps = eps;
+    P.cost = opt ? opt->cost : FS_COST_SQEUCLIDEAN;
     FS_TRY(classify(c, P.X, X, (size_t)n * d));
     FS_TRY(classify(c, P.a, a, (size_t)n));
     FS_TRY(classify(c, P.Y, Y, (size_t)m * d));
@@ -395,8 +399,9 @@ int64_t fs_workspace_bytes(int64_t n, int64_t m, int32_t d, int32_t k, const fs_
     cudaGetLastError();
     const int path = choose_path(d, opt);
     if (path == FS_PATH_FMA && d > kFmaMaxDim) return -1;
-    return path == FS_PATH_FMA ? workspace_bytes_fma(n, m, d, k, sms, opt)
-                               : workspace_bytes_tc(n, m, d, k, sms, opt);
+    return (path == FS_PATH_FMA ? workspace_bytes_fma(n, m, d, k, sms, opt)
+                                : workspace_bytes_tc(n, m, d, k, sms, opt)) +
+           cos_workspace_bytes(n, m, d, opt);
 }
 
 fs_status fs_check(void* stream) {

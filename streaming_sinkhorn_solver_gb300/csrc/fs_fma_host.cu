@@ -82,9 +82,12 @@ fs_status solve_fma(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) 
     const FmaPlan p = plan_fma(n, m, d, c.ws->sms, opt);
     FmaBufs B;
     layout_fma(c.L, B, n, m, d, p, 0, 1);
+    CosBufs cb;
+    layout_cos(c.L, cb, P);
     FS_TRY(ensure_capacity(c));
     for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g}) bind(c, *A);
     for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.g}) FS_TRY(upload(c, *A));
+    FS_TRY(prepare_cos(c, P, cb));
 
     const double eps = (double)P.eps;
     const float l_over_eps = (float)(kLog2e / eps);
@@ -155,9 +158,12 @@ fs_status apply_fma(Call& c, Problem& P, int mode, const fs_options* opt) {
     const int splits = apply_splits_for(n, m, k, c.ws->sms, opt, &cps);
     FmaBufs B;
     layout_fma(c.L, B, n, m, d, p, k, splits);
+    CosBufs cb;
+    layout_cos(c.L, cb, P);
     FS_TRY(ensure_capacity(c));
     for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g, &P.V, &P.out}) bind(c, *A);
     for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g, &P.V}) FS_TRY(upload(c, *A));
+    FS_TRY(prepare_cos(c, P, cb, mode != APPLY_PV));
 
     const double eps = (double)P.eps;
     const float l_over_eps = (float)(kLog2e / eps);
@@ -195,6 +201,7 @@ fs_status apply_fma(Call& c, Problem& P, int mode, const fs_options* opt) {
     FS_CUDA(launch_apply_fma(p.D, A, c.stream));
     timing_end(ts, TIME_APPLY, c.stream);
     if (splits > 1) FS_CUDA(launch_merge_apply(A, c.stream));
+    if (mode == APPLY_GRAD) FS_TRY(finish_grad_cos(c, P, cb));
     if (opt && opt->check_finite)
         FS_TRY(scan_finite(c, P.out.dev, n * (int64_t)k, c.at<unsigned int>(B.counter)));
     FS_TRY(download(c, P.out));

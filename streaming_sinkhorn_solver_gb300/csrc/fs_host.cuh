@@ -101,7 +101,23 @@ struct Problem {
     int64_t n = 0, m = 0;
     int32_t d = 0, k = 0;
     float eps = 0.f;
+    int32_t cost = FS_COST_SQEUCLIDEAN;
 };
+
+// Cosine cost: normalised copies of X and Y in the workspace (laid out with
+// the path's buffers, before the capacity check); prepare_cos fills them
+// after staging and points the problem at them (and, for the barycentric
+// map and the gradient, the V that is Y);
+// finish_grad_cos turns a gradient at the normalised points into one with
+// respect to the caller's X.  All are no-ops for the squared-Euclidean cost.
+struct CosBufs {
+    size_t xn = 0, yn = 0, nx = 0;
+    bool used = false;
+};
+void layout_cos(Layout& L, CosBufs& cb, const Problem& P);
+int64_t cos_workspace_bytes(int64_t n, int64_t m, int32_t d, const fs_options* opt);
+fs_status prepare_cos(Call& c, Problem& P, const CosBufs& cb, bool v_is_points = false);
+fs_status finish_grad_cos(Call& c, Problem& P, const CosBufs& cb);
 
 // Path entry points.  Each one lays out its buffers after the staging area
 // already in c.L, grows the workspace, binds and uploads the staged arrays,

@@ -179,9 +179,12 @@ fs_status solve_tc(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) {
     const TcPlan p = plan_tc(n, m, d, c.ws->sms, opt);
     TcBufs B;
     layout_tc(c.L, B, n, m, d, p);
+    CosBufs cb;
+    layout_cos(c.L, cb, P);
     FS_TRY(ensure_capacity(c));
     for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g}) bind(c, *A);
     for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.g}) FS_TRY(upload(c, *A));
+    FS_TRY(prepare_cos(c, P, cb));
     const int tp = timing_begin(c.stream);
     FS_TRY(prep_tc(c, P, p, B, true));
     timing_end(tp, TIME_PREP, c.stream);
@@ -276,9 +279,12 @@ fs_status apply_tc(Call& c, Problem& P, int mode, const fs_options* opt) {
     layout_tc(c.L, B, n, m, d, p);
     TcApplyBufs A;
     layout_apply(c.L, A, p, n, k, c.ws->sms, opt);
+    CosBufs cb;
+    layout_cos(c.L, cb, P);
     FS_TRY(ensure_capacity(c));
     for (Arr* X : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g, &P.V, &P.out}) bind(c, *X);
     for (Arr* X : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g, &P.V}) FS_TRY(upload(c, *X));
+    FS_TRY(prepare_cos(c, P, cb, mode != APPLY_PV));
     FS_TRY(prep_tc(c, P, p, B, true, c.at<void>(A.Xlo), c.at<void>(A.Ylo)));
 
     const double eps = (double)P.eps;
@@ -358,6 +364,7 @@ fs_status apply_tc(Call& c, Problem& P, int mode, const fs_options* opt) {
     FS_CUDA(launch_apply_tc(ap, (int)p.rtx, c.stream));
     timing_end(ts, TIME_APPLY, c.stream);
     if (A.splits > 1) FS_CUDA(launch_merge_apply_tc(ap, c.stream));
+    if (mode == APPLY_GRAD) FS_TRY(finish_grad_cos(c, P, cb));
     if (opt && opt->check_finite)
         FS_TRY(scan_finite(c, P.out.dev, n * (int64_t)k, c.at<unsigned int>(A.vabs) + 1));
     FS_TRY(download(c, P.out));
