@@ -398,3 +398,60 @@ def test_grad_x_cosine_matches_finite_differences():
     np.testing.assert_allclose(grad, fd, rtol=2e-4, atol=2e-5 * np.abs(grad).max())
     # the gradient is orthogonal to x_i (a cosine cost cannot change along it)
     assert np.abs(np.sum(grad * X.astype(np.float64), axis=1)).max() <= 1e-12 * np.abs(grad).max() * 10
+
+
+# --- Hessian-vector product of the converged OT value (derived here; the
+# pages name a streaming HVP without a formula) ---------------------------
+
+def test_hvp_single_pair_closed_form():
+    """n = m = 1: F = |x - y|^2, so H = 2 I at any eps."""
+    X = np.array([[0.3, -1.2, 0.5]], np.float32)
+    Y = np.array([[1.0, 0.25, -0.5]], np.float32)
+    a = b = np.ones(1, np.float32)
+    C = orc.cost(X, Y)
+    f, g = orc.sinkhorn(C, a, b, 0.7, 3)
+    V = np.array([[0.2, 1.5, -0.4]])
+    np.testing.assert_allclose(orc.hvp_x(C, X, a, b, 0.7, f, g, Y, V), 2.0 * V, atol=1e-12)
+
+
+def test_hvp_matches_finite_differences_of_the_gradient():
+    c = _cloud(6, 7, 2, 41, weights="lognormal")
+    X, Y, a, b = c["X"], c["Y"], c["a"], c["b"]
+    eps, iters = 0.5, 800
+    V = np.random.default_rng(3).standard_normal(X.shape)
+
+    def grad_at(Xv):
+        C = orc.cost(Xv, Y)
+        f, g = orc.sinkhorn(C, a, b, eps, iters)
+        return orc.grad_x(C, Xv, a, b, eps, f, g, Y)
+
+    C = orc.cost(X, Y)
+    f, g = orc.sinkhorn(C, a, b, eps, iters)
+    hv = orc.hvp_x(C, X, a, b, eps, f, g, Y, V)
+    h = 1e-3
+    Xp = (X.astype(np.float64) + h * V).astype(np.float32)
+    Xm = (X.astype(np.float64) - h * V).astype(np.float32)
+    # the float32 rounding of X +- hV is part of the step actually taken
+    dX = Xp.astype(np.float64) - Xm.astype(np.float64)
+    fd = (grad_at(Xp) - grad_at(Xm)) / (2 * h)
+    hv_taken = orc.hvp_x(C, X, a, b, eps, f, g, Y, dX / (2 * h))
+    np.testing.assert_allclose(hv_taken, fd, rtol=1e-3, atol=1e-4 * np.abs(fd).max())
+    assert np.abs(hv - hv_taken).max() <= 1e-2 * np.abs(hv).max()
+
+
+def test_hvp_is_symmetric():
+    """<U, H V> = <V, H U>: a Hessian is symmetric.  Exactly so only at an exact
+    fixed point, which needs equal masses: dyadic uniform weights (1/8, 1/16)
+    sum to 1 exactly in float32."""
+    c = _cloud(8, 16, 3, 43)
+    X, Y, a, b = c["X"], c["Y"], c["a"], c["b"]
+    assert float(a.astype(np.float64).sum()) == float(b.astype(np.float64).sum()) == 1.0
+    eps = 0.3
+    C = orc.cost(X, Y)
+    f, g = orc.sinkhorn(C, a, b, eps, 2000)
+    rng = np.random.default_rng(4)
+    U = rng.standard_normal(X.shape)
+    V = rng.standard_normal(X.shape)
+    lhs = float(np.sum(U * orc.hvp_x(C, X, a, b, eps, f, g, Y, V)))
+    rhs = float(np.sum(V * orc.hvp_x(C, X, a, b, eps, f, g, Y, U)))
+    assert abs(lhs - rhs) <= 1e-8 * max(abs(lhs), 1.0)
