@@ -255,6 +255,35 @@ fs_status fs_sinkhorn_solve_noalloc(const float* X, const float* a, int64_t n,
                                     void* stream);
 
 /*
+ * fs_hvp_x -- Hessian of the converged entropic OT value F(X) = <a, f> + <b, g>
+ * with respect to X, applied to a direction V (the pages' streaming HVP of
+ * Method 3 and the Discussion, which they describe as transport-vector and
+ * transport-matrix products in O((n + m) d) memory without a formula).
+ * Derived from the fixed point P 1 = a, P^T 1 = b: along X + t V the
+ * potentials move by (fdot, gdot) with
+ *     diag(b) gdot - P^T diag(1/a) P gdot = c - P^T (r / a)
+ *     r_i = sum_j P_ij Cdot_ij,  c_j = sum_i P_ij Cdot_ij,  Cdot_ij = 2 (x_i - y_j).v_i
+ * (solved by conjugate gradients in the complement of the gauge direction 1),
+ * fdot = (r - P gdot) / a, and
+ *     (H V)_i = 2 a_i v_i - (2/eps) sum_j P_ij (fdot_i + gdot_j - Cdot_ij) y_j.
+ * Every product with P is a plan application (never stored); the last term
+ * applies P to the d^2 products y_j y_j^T.
+ *   f, g          converged potentials (from fs_sinkhorn_solve); the formula
+ *                 assumes both marginals hold, so its accuracy follows the
+ *                 marginal residuals (fs_marginal_residuals)
+ *   V [n*d], out [n*d]   direction and result (host or device)
+ *   cg_max_iter   CG iteration limit, 0 = 200;  cg_tol  relative residual, 0 = 1e-6
+ * Squared-Euclidean cost, 1 <= d <= 64 (FS_ERR_UNSUPPORTED otherwise).
+ * Stream-ordered scratch of O((n + m) d^2) floats; synchronises `stream`
+ * (each CG step reads two dot products on the host).
+ */
+fs_status fs_hvp_x(const float* X, const float* a, int64_t n,
+                   const float* Y, const float* b, int64_t m, int32_t d,
+                   float eps, const float* f, const float* g,
+                   const float* V, float* out, int32_t cg_max_iter, float cg_tol,
+                   const fs_options* opt, void* stream);
+
+/*
  * fs_unit_rates -- measure, on the current GPU, the per-SM issue rates that
  * bound the exponent-heavy half-updates (no counterpart on the pages: it
  * supplies the denominators of the ALU roofline).  Throughput kernels with

@@ -32,7 +32,7 @@ EXPORTED = ("fs_sinkhorn_solve", "fs_apply_plan", "fs_barycentric", "fs_grad_x",
             "fs_apply_plan_t", "fs_barycentric_y", "fs_grad_y", "fs_dual_value",
             "fs_marginal_residuals", "fs_workspace_bytes", "fs_check", "fs_release",
             "fs_last_error", "fs_version", "fs_launch_count", "fs_timing_enable",
-            "fs_timing_read", "fs_sinkhorn_solve_noalloc", "fs_unit_rates")
+            "fs_timing_read", "fs_sinkhorn_solve_noalloc", "fs_unit_rates", "fs_hvp_x")
 
 
 class FlashSinkhornError(RuntimeError):
@@ -94,6 +94,9 @@ def load_library(path: Optional[str] = None):
         lib.fs_timing_read.restype = ctypes.c_int
         lib.fs_sinkhorn_solve_noalloc.argtypes = [vp, vp, i64, vp, vp, i64, i32, f32, i32, vp, vp, vp]
         lib.fs_sinkhorn_solve_noalloc.restype = ctypes.c_int
+        lib.fs_hvp_x.argtypes = [vp, vp, i64, vp, vp, i64, i32, f32, vp, vp, vp, vp, i32, f32,
+                                 opt, vp]
+        lib.fs_hvp_x.restype = ctypes.c_int
         lib.fs_unit_rates.argtypes = [ctypes.POINTER(ctypes.c_double), vp]
         lib.fs_unit_rates.restype = ctypes.c_int
         if path is None:
@@ -325,6 +328,21 @@ def fs_marginal_residuals(X, a, Y, b, eps: float, f, g, *, path: str = "auto", c
         _stream(stream, X))
     _raise(st)
     return float(out[0]), float(out[1])
+
+
+def fs_hvp_x(X, a, Y, b, eps: float, f, g, V, out=None, *, cg_max_iter: int = 0,
+             cg_tol: float = 0.0, path: str = "auto", splits: int = 0, stream=None):
+    """(H V), H the Hessian of the converged OT value with respect to X."""
+    n, d = X.shape
+    m = Y.shape[0]
+    out = _new_like(X, (n, d)) if out is None else out
+    st = load_library().fs_hvp_x(
+        _ptr(X, "X", (n, d)), _ptr(a, "a", (n,)), n, _ptr(Y, "Y", (m, d)), _ptr(b, "b", (m,)), m, d,
+        float(eps), _ptr(f, "f", (n,)), _ptr(g, "g", (m,)), _ptr(V, "V", (n, d)),
+        _ptr(out, "out", (n, d)), int(cg_max_iter), float(cg_tol), _opts(path, splits, False),
+        _stream(stream, X))
+    _raise(st)
+    return out
 
 
 def fs_unit_rates(stream=None) -> dict:

@@ -18,7 +18,7 @@ namespace fs {
 namespace {
 
 constexpr int kRedThreads = 256;
-constexpr int kRedMaxBlocks = 512;
+constexpr int kRedMaxBlocks = kRedPartials;
 
 // MODE 0: sum x_i y_i; MODE 1: sum |x_i - y_i|
 template <int MODE>
@@ -75,45 +75,19 @@ cudaError_t reduce_into(const float* x, const float* y, int64_t len, double* par
     return cudaGetLastError();
 }
 
-bool is_device_ptr(const void* p) {
-    cudaPointerAttributes attr;
-    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    return attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged;
+}  // namespace
+
+cudaError_t launch_dot_double(const float* x, const float* y, int64_t len, double* partial,
+                              double* out, int add, cudaStream_t s) {
+    return reduce_into<0>(x, y, len, partial, out, add, s);
 }
 
-// Stream-ordered scratch for the composite reports (freed on the stream).
-struct Scratch {
-    cudaStream_t s;
-    std::vector<void*> ptrs;
-    explicit Scratch(cudaStream_t st) : s(st) {}
-    ~Scratch() {
-        for (void* p : ptrs) cudaFreeAsync(p, s);
-    }
-    template <typename T>
-    cudaError_t get(T** p, size_t count) {
-        void* q = nullptr;
-        const cudaError_t e = cudaMallocAsync(&q, std::max<size_t>(count, 1) * sizeof(T), s);
-        if (e == cudaSuccess) ptrs.push_back(q);
-        *p = static_cast<T*>(q);
-        return e;
-    }
-    // a device copy of `p` (or `p` itself when it is device memory)
-    cudaError_t device_view(const float* p, size_t count, const float** out) {
-        if (is_device_ptr(p)) {
-            *out = p;
-            return cudaSuccess;
-        }
-        float* d = nullptr;
-        cudaError_t e = get(&d, count);
-        if (e != cudaSuccess) return e;
-        e = cudaMemcpyAsync(d, p, count * sizeof(float), cudaMemcpyHostToDevice, s);
-        *out = d;
-        return e;
-    }
-};
+cudaError_t launch_l1_double(const float* x, const float* y, int64_t len, double* partial,
+                             double* out, int add, cudaStream_t s) {
+    return reduce_into<1>(x, y, len, partial, out, add, s);
+}
+
+namespace {
 
 fs_status dual_entry(const float* a, int64_t n, const float* b, int64_t m, const float* f,
                      const float* g, double* out, void* stream) {

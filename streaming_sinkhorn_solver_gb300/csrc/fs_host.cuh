@@ -6,6 +6,7 @@
 #include "fs_internal.cuh"
 
 #include <mutex>
+#include <vector>
 #include <string>
 
 namespace fs {
@@ -102,6 +103,57 @@ struct Problem {
     int32_t d = 0, k = 0;
     float eps = 0.f;
     int32_t cost = FS_COST_SQEUCLIDEAN;
+};
+
+// Composite calls (reports, HVP): stream-ordered scratch, freed on the stream
+// when the helper goes out of scope, and fixed-order double reductions
+// (sum x_i y_i, sum |x_i - y_i| into out[0], or added to it when add != 0;
+// `partial` holds at least kRedPartials doubles).
+constexpr int kRedPartials = 512;
+cudaError_t launch_dot_double(const float* x, const float* y, int64_t len, double* partial,
+                              double* out, int add, cudaStream_t s);
+cudaError_t launch_l1_double(const float* x, const float* y, int64_t len, double* partial,
+                             double* out, int add, cudaStream_t s);
+
+inline bool is_device_ptr(const void* p) {
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged;
+}
+
+struct Scratch {
+    cudaStream_t s;
+    std::vector<void*> ptrs;
+    explicit Scratch(cudaStream_t st) : s(st) {}
+    Scratch(const Scratch&) = delete;
+    Scratch& operator=(const Scratch&) = delete;
+    ~Scratch() {
+        for (void* p : ptrs) cudaFreeAsync(p, s);
+    }
+    template <typename T>
+    cudaError_t get(T** p, size_t count) {
+        void* q = nullptr;
+        const cudaError_t e = cudaMallocAsync(&q, (count > 0 ? count : 1) * sizeof(T), s);
+        if (e == cudaSuccess) ptrs.push_back(q);
+        *p = static_cast<T*>(q);
+        return e;
+    }
+    // a device copy of `p` (or `p` itself when it is device memory)
+    cudaError_t device_view(const float* p, size_t count, const float** out) {
+        if (is_device_ptr(p)) {
+            *out = p;
+            return cudaSuccess;
+        }
+        float* d = nullptr;
+        cudaError_t e = get(&d, count);
+        if (e != cudaSuccess) return e;
+        e = cudaMemcpyAsync(d, p, count * sizeof(float), cudaMemcpyHostToDevice, s);
+        *out = d;
+        return e;
+    }
 };
 
 // Cosine cost: normalised copies of X and Y in the workspace (laid out with

@@ -157,3 +157,18 @@ def test_y_side_and_reports_reject_bad_arguments(lib):
     st = lib.fs_marginal_residuals(X.ctypes.data, a.ctypes.data, 4, Y.ctypes.data, b.ctypes.data,
                                    5, 2, 0.1, f.ctypes.data, g.ctypes.data, None, None, None)
     assert st == fs.FS_ERR_INVALID_ARG
+
+
+def test_hvp_rejects_bad_arguments(lib):
+    X, a, Y, b = _small()
+    f = np.zeros(4, np.float32)
+    g = np.zeros(5, np.float32)
+    V = np.zeros((4, 2), np.float32)
+    out = np.zeros((4, 2), np.float32)
+    st = lib.fs_hvp_x(X.ctypes.data, a.ctypes.data, 4, Y.ctypes.data, b.ctypes.data, 5, 2, 0.1,
+                      f.ctypes.data, g.ctypes.data, None, out.ctypes.data, 0, 0.0, None, None)
+    assert st == fs.FS_ERR_INVALID_ARG
+    st = lib.fs_hvp_x(X.ctypes.data, a.ctypes.data, 4, Y.ctypes.data, b.ctypes.data, 5, 100, 0.1,
+                      f.ctypes.data, g.ctypes.data, V.ctypes.data, out.ctypes.data, 0, 0.0, None,
+                      None)
+    assert st == fs.FS_ERR_UNSUPPORTED
