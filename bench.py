@@ -303,7 +303,7 @@ def run_gb300(args, w):
     if world > 1:
         torch.distributed.barrier()
 
-    sampler = ClockSampler(dev.index) if rank == 0 or True else None
+    sampler = ClockSampler(dev.index)   # every rank samples its own GPU
     sampler.start()
     fs.fs_timing_read()
     fs.fs_timing_enable(True)

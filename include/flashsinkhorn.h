@@ -102,6 +102,18 @@ typedef struct fs_options {
 } fs_options;
 
 /*
+ * CUDA graphs.  fs_sinkhorn_solve, fs_apply_plan, fs_barycentric, fs_grad_x
+ * and the _t / _y variants can be captured into a CUDA graph on the stream
+ * they are given, once a call with the same sizes has run outside the capture
+ * (it sizes the workspace; a capture never allocates).  Inside a capture all
+ * arrays must be device memory and check_finite must be off
+ * (FS_ERR_UNSUPPORTED otherwise), and the library does not order the
+ * captured work against its other calls: replays share the workspace with
+ * every call on the device, so the caller orders them (one stream, or events).
+ * The reports, fs_hvp_x and fs_check synchronise and cannot be captured.
+ */
+
+/*
  * fs_sinkhorn_solve -- n_iter stabilised log-domain Sinkhorn iterations.
  *
  * Method 1 of the pages: one iteration is the f-update from g

@@ -39,9 +39,14 @@ fs_status begin_call(Call& c, void* stream) {
     FS_CUDA(cudaGetDevice(&c.dev));
     if (c.dev < 0 || c.dev >= kMaxDevices) return fail(FS_ERR_UNSUPPORTED, "device index %d", c.dev);
     c.stream = static_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    FS_CUDA(cudaStreamIsCapturing(c.stream, &cs));
+    c.capturing = cs == cudaStreamCaptureStatusActive;
     c.ws = &g_ws[c.dev];
     c.lock = std::unique_lock<std::mutex>(c.ws->mu);
     Workspace& w = *c.ws;
+    if (w.done == nullptr && c.capturing)
+        return fail(FS_ERR_UNSUPPORTED, "make one call on this device before capturing a graph");
     if (w.done == nullptr) {
         FS_CUDA(cudaDeviceGetAttribute(&w.sms, cudaDevAttrMultiProcessorCount, c.dev));
         FS_CUDA(cudaMalloc(&w.err_word, sizeof(uint32_t)));
@@ -49,13 +54,16 @@ fs_status begin_call(Call& c, void* stream) {
         FS_CUDA(cudaDeviceSynchronize());
         FS_CUDA(cudaEventCreateWithFlags(&w.done, cudaEventDisableTiming));
     }
-    // order this call after the previous one if that ran on another stream
-    if (w.used && w.last_stream != c.stream) FS_CUDA(cudaStreamWaitEvent(c.stream, w.done, 0));
+    // order this call after the previous one if that ran on another stream (a
+    // captured call is ordered by the graph's user instead)
+    if (!c.capturing && w.used && w.last_stream != c.stream)
+        FS_CUDA(cudaStreamWaitEvent(c.stream, w.done, 0));
     return FS_OK;
 }
 
 fs_status end_call(Call& c) {
     Workspace& w = *c.ws;
+    if (c.capturing) return FS_OK;
     FS_CUDA(cudaEventRecord(w.done, c.stream));
     w.last_stream = c.stream;
     w.used = true;
@@ -66,6 +74,10 @@ fs_status ensure_capacity(Call& c) {
     Workspace& w = *c.ws;
     const size_t bytes = c.L.off;
     if (bytes <= w.cap) return FS_OK;
+    if (c.capturing)
+        return fail(FS_ERR_UNSUPPORTED,
+                    "the workspace (%zu bytes) must be grown before graph capture: make one call "
+                    "with these sizes outside the capture first", bytes);
     // grow: wait for every user of the old arena, then replace it
     if (w.base) {
         FS_CUDA(cudaDeviceSynchronize());
@@ -107,6 +119,8 @@ fs_status classify(Call& c, Arr& a, const float* p, size_t count) {
             a.host = true;  // pinned or pageable host memory
             break;
     }
+    if (a.host && c.capturing)
+        return fail(FS_ERR_UNSUPPORTED, "host arrays cannot be staged inside a graph capture");
     if (a.host) a.off = c.L.take(count * sizeof(float));
     return FS_OK;
 }
@@ -134,6 +148,9 @@ fs_status download(Call& c, const Arr& a) {
 }
 
 fs_status scan_finite(Call& c, const float* v, int64_t len, unsigned int* counter) {
+    if (c.capturing)
+        return fail(FS_ERR_UNSUPPORTED, "check_finite reads a count on the host: not inside a "
+                                        "graph capture");
     FS_CUDA(cudaMemsetAsync(counter, 0, sizeof(unsigned int), c.stream));
     FS_CUDA(launch_count_nonfinite(v, len, counter, c.stream));
     unsigned int h = 0;
@@ -157,6 +174,11 @@ TimingState g_timing;
 int timing_begin(cudaStream_t s) {
     std::lock_guard<std::mutex> lk(g_timing.mu);
     if (!g_timing.on) return -1;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+        cudaGetLastError();
+        return -1;   // events inside a graph are not timed
+    }
     const size_t slot = g_timing.used;
     if (2 * slot + 2 > g_timing.pool.size()) {
         for (int i = 0; i < 2; ++i) {

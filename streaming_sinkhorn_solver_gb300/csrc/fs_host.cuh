@@ -67,6 +67,7 @@ struct Arr {
 struct Call {
     int dev = 0;
     cudaStream_t stream = nullptr;
+    bool capturing = false;            // the stream is being captured into a CUDA graph
     Workspace* ws = nullptr;
     std::unique_lock<std::mutex> lock;
     Layout L;
