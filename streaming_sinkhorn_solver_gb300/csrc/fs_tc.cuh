@@ -204,6 +204,14 @@ __device__ __forceinline__ void tmem_fill32(uint32_t taddr, float x) {
         "f"(x)
         : "memory");
 }
+// warp: 8 registers into 8 consecutive columns of the warp's 32 lanes
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+                     taddr),
+                 "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]),
+                 "f"(v[7])
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }

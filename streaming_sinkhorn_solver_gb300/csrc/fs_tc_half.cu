@@ -1,4 +1,4 @@
-// Fused half-update on the tcgen05 tensor cores (d > 16).
+// Fused half-update on the tcgen05 tensor cores (d > 16), online-max form.
 //
 // "FlashSinkhorn: IO-Aware Entropic Optimal Transport on GPU", Method 1
 // (Proposition 1: the f-update is a row LSE of the biased dot-product score
@@ -15,21 +15,15 @@
 //              space, all with cp.async.bulk;
 //   warp 1     one thread issues tcgen05.mma (M = 128, N = 128, K = 16 steps)
 //              into TMEM buffer t mod 4;
-//   warps 2-   epilogue groups of four warps, tile t going to group t mod G;
-//              a thread owns one row.
-// Two epilogue modes:
-//   online     (G = 2) the thread reads its 128 scores, forms s = acc kappa'
-//              + bias (packed f32x2 FMA) and folds them into the row's running
-//              max M and sum S of 2^{s-M};
-//   reference  (G = 4, one group per TMEM buffer) the row's offset M is its
-//              LSE from the previous half-update.  The group pre-loads every
-//              accumulator column of its buffer with -M / kappa' (tcgen05.st),
-//              the MMAs accumulate onto it, and the epilogue only forms
-//              2^{acc kappa' + bias} and sums it, 32 columns at a time, the
-//              next slice's TMEM load in flight.  The sum is range-checked at
-//              the end; a row outside the range is recomputed later.
+//   warps 2-9  two epilogue groups of four warps, tile t going to group
+//              t mod 2; a thread owns one row, reads its 128 scores, forms
+//              s = acc kappa' + bias (packed f32x2 FMA) and folds them into the
+//              row's running max M and sum S of 2^{s-M}.
 // At the end the groups' (M, S) are merged in a fixed order and the row
-// potential and next bias are written (or (M, S) partials per split).
+// potential and next bias are written (or (M, S) partials per split).  This
+// kernel serves the first iterations and the log2-sum-exp pre-pass of the
+// plan operators; settled iterations with d <= 128 use the reference-offset
+// kernel (k_half_ref), which needs no running max.
 #include "fs_tc.cuh"
 
 namespace fs {
@@ -41,32 +35,16 @@ constexpr int kBiasBytes = BN * 4;
 // Bias slices in flight: deeper than the K ring (in tiles), so the producer's
 // wait for a free bias slot never holds back the next K chunks.
 constexpr int kBiasSlots = 16;
-constexpr int kMaxGroups = kRefGroups > kHalfGroups ? kRefGroups : kHalfGroups;
 
 __host__ __device__ constexpr int half_fixed_bytes(int nch, bool qres) {
     return 1024 /* alignment slack */ + (qres ? nch * CHUNK_BYTES : 0) + kBiasSlots * kBiasBytes +
-           BM * 8 * (kMaxGroups - 1) /* group merge */ +
+           BM * 8 * (kHalfGroups - 1) /* group merge */ +
            8 * (2 * kMaxStages + 2 * kTmemBufs + 2 * kBiasSlots + 2) + 16;
 }
 
 template <int GROUPS>
 __device__ __forceinline__ void epi_bar_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(GROUPS * kEpiWarps * 32) : "memory");
-}
-
-// One 32-column slice in reference mode: acc[] += 2^{v kappa' + bias}
-// (bias already holds the row offset through the accumulator pre-load).
-__device__ __forceinline__ void ref_slice(const float (&v)[32], const float4* __restrict__ sb,
-                                          uint64_t ks2, uint64_t (&acc)[4]) {
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const float4 bb = sb[q];
-        float x0, x1, x2, x3;
-        upk(fma2(pk(v[4 * q], v[4 * q + 1]), ks2, pk(bb.x, bb.y)), x0, x1);
-        upk(fma2(pk(v[4 * q + 2], v[4 * q + 3]), ks2, pk(bb.z, bb.w)), x2, x3);
-        acc[(2 * q) & 3] = add2(acc[(2 * q) & 3], pk(ex2(x0), ex2(x1)));
-        acc[(2 * q + 1) & 3] = add2(acc[(2 * q + 1) & 3], pk(ex2(x2), ex2(x3)));
-    }
 }
 
 }  // namespace
@@ -82,10 +60,9 @@ size_t half_smem_bytes(int nch, bool qres, int stages) {
     return (size_t)half_fixed_bytes(nch, qres) + (size_t)stages * stage;
 }
 
-template <bool QRES, bool REF>
-__global__ void __launch_bounds__(half_threads(REF), 1) k_half_tc(TcHalfArgs a) {
-    constexpr int GROUPS = REF ? kRefGroups : kHalfGroups;
-    static_assert(!REF || GROUPS == kTmemBufs, "reference mode: one group per TMEM buffer");
+template <bool QRES>
+__global__ void __launch_bounds__(kHalfThreads, 1) k_half_tc(TcHalfArgs a) {
+    constexpr int GROUPS = kHalfGroups;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -103,7 +80,7 @@ __global__ void __launch_bounds__(half_threads(REF), 1) k_half_tc(TcHalfArgs a) 
     uint8_t* sStage = smem + (QRES ? nch * CHUNK_BYTES : 0);
     uint8_t* sBias = sStage + stages * STAGE_BYTES;
     float2* sMerge = reinterpret_cast<float2*>(sBias + kBiasSlots * kBiasBytes);
-    uint64_t* full = reinterpret_cast<uint64_t*>(sMerge + BM * (kMaxGroups - 1));
+    uint64_t* full = reinterpret_cast<uint64_t*>(sMerge + BM * (kHalfGroups - 1));
     uint64_t* empty = full + kMaxStages;
     uint64_t* tfull = empty + kMaxStages;
     uint64_t* tempty = tfull + kTmemBufs;
@@ -198,10 +175,8 @@ __global__ void __launch_bounds__(half_threads(REF), 1) k_half_tc(TcHalfArgs a) 
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
-        // Online mode: buffer use u waits for the epilogue's release of use
-        // u - 1 (the first use passes at once).  Reference mode: the epilogue
-        // also releases each buffer once before its first use, after filling
-        // it with the row offsets, so use u waits for release u.
+        // Buffer use u waits for the epilogue's release of use u - 1 (the
+        // first use passes at once).
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
             bool ok = true;
@@ -211,7 +186,7 @@ __global__ void __launch_bounds__(half_threads(REF), 1) k_half_tc(TcHalfArgs a) 
             uint32_t ph = 0;
             for (int t = 0; t < ntiles && ok; ++t) {
                 const int b = t & (kTmemBufs - 1);
-                const uint32_t use_ph = (uint32_t)((t >> 2) & 1) ^ (REF ? 0u : 1u);
+                const uint32_t use_ph = (uint32_t)((t >> 2) & 1) ^ 1u;
                 if (!mbar_wait(&tempty[b], use_ph, a.err, ERR_TIMEOUT_MMA)) {
                     ok = false;
                     break;
@@ -230,7 +205,7 @@ __global__ void __launch_bounds__(half_threads(REF), 1) k_half_tc(TcHalfArgs a) 
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
                         mma_f16(d_tmem, sdesc_sw128(aaddr + kk * 32), sdesc_sw128(baddr + kk * 32),
-                                idesc, REF || (c | kk) != 0);
+                                idesc, (c | kk) != 0);
                     mma_commit(&empty[s]);
                     if (++s == stages) {
                         s = 0;
@@ -254,117 +229,60 @@ __global__ void __launch_bounds__(half_threads(REF), 1) k_half_tc(TcHalfArgs a) 
         const uint64_t ks2 = pk(ks, ks);
         const uint32_t lofs = (uint32_t)(quarter * 32) << 16;
         float M = -INFINITY, S = 0.f;
-        if constexpr (REF) {
-            // the group's own TMEM buffer holds -M / kappa' before every use
-            const int64_t rr = row < a.nr ? row : a.nr - 1;
-            M = a.rlogw2[rr] - a.rbias[rr];
-            const float fill = -M / ks;
-            const uint32_t buf = tmem + (uint32_t)(grp * BN) + lofs;
+        for (int t = grp; t < ntiles; t += GROUPS) {
+            const int b = t & (kTmemBufs - 1);
+            const uint32_t ph = (uint32_t)((t >> 2) & 1);
+            if (!mbar_wait(&tfull[b], ph, a.err, ERR_TIMEOUT_EPILOGUE)) break;
+            tc_fence_after();
+            float v[BN];
 #pragma unroll
-            for (int q = 0; q < BN / 32; ++q) tmem_fill32(buf + q * 32, fill);
-            tmem_wait_st();
+            for (int q = 0; q < BN / 32; ++q)
+                tmem_ld32(tmem + (uint32_t)(b * BN) + lofs + q * 32, v + q * 32);
+            tmem_wait_ld();
+            tmem_reg_fence(v);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[grp]);
-            uint64_t acc[4] = {pk(0.f, 0.f), pk(0.f, 0.f), pk(0.f, 0.f), pk(0.f, 0.f)};
-            for (int t = grp; t < ntiles; t += GROUPS) {
-                const uint32_t ph = (uint32_t)((t >> 2) & 1);
-                if (!mbar_wait(&tfull[grp], ph, a.err, ERR_TIMEOUT_EPILOGUE)) break;
-                tc_fence_after();
-                const int bs = t % kBiasSlots;
-                if (!mbar_wait(&bfull[bs], (uint32_t)((t / kBiasSlots) & 1), a.err,
-                               ERR_TIMEOUT_EPILOGUE))
-                    break;
-                const float4* sb = reinterpret_cast<const float4*>(sBias + bs * kBiasBytes);
-                float va[32], vb[32];
-                tmem_ld32(buf, va);
-                tmem_wait_ld();
-                tmem_reg_fence(va);
-                tmem_ld32(buf + 32, vb);
-                ref_slice(va, sb, ks2, acc);
-                tmem_wait_ld();
-                tmem_reg_fence(vb);
-                tmem_ld32(buf + 64, va);
-                ref_slice(vb, sb + 8, ks2, acc);
-                tmem_wait_ld();
-                tmem_reg_fence(va);
-                tmem_ld32(buf + 96, vb);
-                ref_slice(va, sb + 16, ks2, acc);
-                tmem_wait_ld();
-                tmem_reg_fence(vb);
-                // every score of the tile is in registers: refill, release
-#pragma unroll
-                for (int q = 0; q < BN / 32; ++q) tmem_fill32(buf + q * 32, fill);
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[grp]);
-                ref_slice(vb, sb + 24, ks2, acc);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bempty[bs]);
-            }
-            float s0, s1, s2, s3, s4, s5, s6, s7;
-            upk(acc[0], s0, s1);
-            upk(acc[1], s2, s3);
-            upk(acc[2], s4, s5);
-            upk(acc[3], s6, s7);
-            S = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
-        } else {
-            for (int t = grp; t < ntiles; t += GROUPS) {
-                const int b = t & (kTmemBufs - 1);
-                const uint32_t ph = (uint32_t)((t >> 2) & 1);
-                if (!mbar_wait(&tfull[b], ph, a.err, ERR_TIMEOUT_EPILOGUE)) break;
-                tc_fence_after();
-                float v[BN];
-#pragma unroll
-                for (int q = 0; q < BN / 32; ++q)
-                    tmem_ld32(tmem + (uint32_t)(b * BN) + lofs + q * 32, v + q * 32);
-                tmem_wait_ld();
-                tmem_reg_fence(v);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[b]);
-                const int bs = t % kBiasSlots;
-                if (!mbar_wait(&bfull[bs], (uint32_t)((t / kBiasSlots) & 1), a.err,
-                               ERR_TIMEOUT_EPILOGUE))
-                    break;
+            if (lane == 0) mbar_arrive(&tempty[b]);
+            const int bs = t % kBiasSlots;
+            if (!mbar_wait(&bfull[bs], (uint32_t)((t / kBiasSlots) & 1), a.err,
+                           ERR_TIMEOUT_EPILOGUE))
+                break;
 
-                // s = acc kappa' + bias, row max (two chains)
-                const float4* sb = reinterpret_cast<const float4*>(sBias + bs * kBiasBytes);
-                float mx0 = -INFINITY, mx1 = -INFINITY;
+            // s = acc kappa' + bias, row max (two chains)
+            const float4* sb = reinterpret_cast<const float4*>(sBias + bs * kBiasBytes);
+            float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-                for (int q = 0; q < BN / 4; ++q) {
-                    const float4 bb = sb[q];
-                    upk(fma2(pk(v[4 * q], v[4 * q + 1]), ks2, pk(bb.x, bb.y)), v[4 * q], v[4 * q + 1]);
-                    upk(fma2(pk(v[4 * q + 2], v[4 * q + 3]), ks2, pk(bb.z, bb.w)), v[4 * q + 2],
-                        v[4 * q + 3]);
-                    mx0 = max3(mx0, v[4 * q], v[4 * q + 1]);
-                    mx1 = max3(mx1, v[4 * q + 2], v[4 * q + 3]);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bempty[bs]);
-                const float mx = fmaxf(mx0, mx1);
-                if (mx > M) {
-                    S *= ex2(M - mx);
-                    M = mx;
-                }
-                if (M == -INFINITY) continue;   // only padding columns so far: nothing to add
-                // S += sum 2^{s - M}
-                const uint64_t nm = pk(-M, -M);
-                uint64_t acc0 = pk(0.f, 0.f), acc1 = pk(0.f, 0.f);
-#pragma unroll
-                for (int q = 0; q < BN / 4; ++q) {
-                    float x0, x1, x2, x3;
-                    upk(add2(pk(v[4 * q], v[4 * q + 1]), nm), x0, x1);
-                    upk(add2(pk(v[4 * q + 2], v[4 * q + 3]), nm), x2, x3);
-                    acc0 = add2(acc0, pk(ex2(x0), ex2(x1)));
-                    acc1 = add2(acc1, pk(ex2(x2), ex2(x3)));
-                }
-                float s0, s1, s2, s3;
-                upk(acc0, s0, s1);
-                upk(acc1, s2, s3);
-                S += (s0 + s1) + (s2 + s3);
+            for (int q = 0; q < BN / 4; ++q) {
+                const float4 bb = sb[q];
+                upk(fma2(pk(v[4 * q], v[4 * q + 1]), ks2, pk(bb.x, bb.y)), v[4 * q], v[4 * q + 1]);
+                upk(fma2(pk(v[4 * q + 2], v[4 * q + 3]), ks2, pk(bb.z, bb.w)), v[4 * q + 2],
+                    v[4 * q + 3]);
+                mx0 = max3(mx0, v[4 * q], v[4 * q + 1]);
+                mx1 = max3(mx1, v[4 * q + 2], v[4 * q + 3]);
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bempty[bs]);
+            const float mx = fmaxf(mx0, mx1);
+            if (mx > M) {
+                S *= ex2(M - mx);
+                M = mx;
+            }
+            if (M == -INFINITY) continue;   // only padding columns so far: nothing to add
+            // S += sum 2^{s - M}
+            const uint64_t nm = pk(-M, -M);
+            uint64_t acc0 = pk(0.f, 0.f), acc1 = pk(0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < BN / 4; ++q) {
+                float x0, x1, x2, x3;
+                upk(add2(pk(v[4 * q], v[4 * q + 1]), nm), x0, x1);
+                upk(add2(pk(v[4 * q + 2], v[4 * q + 3]), nm), x2, x3);
+                acc0 = add2(acc0, pk(ex2(x0), ex2(x1)));
+                acc1 = add2(acc1, pk(ex2(x2), ex2(x3)));
+            }
+            float s0, s1, s2, s3;
+            upk(acc0, s0, s1);
+            upk(acc1, s2, s3);
+            S += (s0 + s1) + (s2 + s3);
         }
 
         // merge the groups in a fixed order: group 0 absorbs groups 1, 2, ...
@@ -385,10 +303,6 @@ __global__ void __launch_bounds__(half_threads(REF), 1) k_half_tc(TcHalfArgs a) 
                 if (a.splits > 1) {
                     a.partial[(int64_t)blockIdx.y * a.nr + row] = make_float2(Mt, St);
                 } else {
-                    if (REF && !(St >= kTcMinRefSum && St <= kTcMaxRefSum)) {
-                        const unsigned int slot = atomicAdd(&a.fix_count[0], 1u);
-                        if (slot < (unsigned int)a.nr) a.fix_list[slot] = (int)row;
-                    }
                     const float lse2 = Mt + log2f(St);
                     if (a.rnorm != nullptr) {
                         a.pot[row] = a.rnorm[row] - a.eps_ln2 * lse2;
@@ -409,24 +323,24 @@ __global__ void __launch_bounds__(half_threads(REF), 1) k_half_tc(TcHalfArgs a) 
     }
 }
 
-template <bool QRES, bool REF>
+template <bool QRES>
 cudaError_t launch_half_tc_t(const TcHalfArgs& a, int row_tiles, size_t smem, cudaStream_t s) {
     const cudaError_t e = cudaFuncSetAttribute(
-        k_half_tc<QRES, REF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        k_half_tc<QRES>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_half_tc<QRES, REF><<<dim3((unsigned)row_tiles, (unsigned)a.splits), half_threads(REF), smem, s>>>(a);
+    k_half_tc<QRES><<<dim3((unsigned)row_tiles, (unsigned)a.splits), kHalfThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_half_tc(const TcHalfArgs& a, int row_tiles, bool qres, cudaStream_t s) {
+    // settled iterations: the reference-offset kernel (Q resident, d <= 128)
+    if (a.use_ref) {
+        if (!qres || a.nch > 2) return cudaErrorInvalidValue;
+        return launch_half_ref(a, row_tiles, s);
+    }
     const size_t smem = half_smem_bytes(a.nch, qres, a.stages);
-    cudaError_t e;
-    if (a.use_ref)
-        e = qres ? launch_half_tc_t<true, true>(a, row_tiles, smem, s)
-                 : launch_half_tc_t<false, true>(a, row_tiles, smem, s);
-    else
-        e = qres ? launch_half_tc_t<true, false>(a, row_tiles, smem, s)
-                 : launch_half_tc_t<false, false>(a, row_tiles, smem, s);
+    const cudaError_t e = qres ? launch_half_tc_t<true>(a, row_tiles, smem, s)
+                               : launch_half_tc_t<false>(a, row_tiles, smem, s);
     count_launch();
     return e;
 }

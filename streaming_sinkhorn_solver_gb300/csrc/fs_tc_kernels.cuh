@@ -41,7 +41,7 @@ struct TcHalfArgs {
     float* rbias;           // bias of the rows for the next half-update
     float2* partial;        // (max, sum) per split and row when splits > 1
     uint32_t* err;          // device error word
-    // Reference offsets (one-CTA kernel): with use_ref set, a row's exponent
+    // Reference offsets: with use_ref set, a row's exponent
     // offset is its previous LSE, rlogw2 - rbias, instead of a running max;
     // rows whose sum leaves the guarded range go to fix_list for
     // launch_fix_tc.
@@ -50,10 +50,11 @@ struct TcHalfArgs {
     unsigned int* fix_count;  // [2], zero before the first guarded half-update
 };
 
-// Epilogue groups of the one-CTA half-update: two with the online max (a
-// thread holds a whole 128-score tile row), four with reference offsets
-// (32-column slices streamed from TMEM; one group per TMEM buffer).
+// Groups of the reference-offset half-update (fs_tc_ref.cu): four groups of
+// four warps, one per TMEM buffer, each issuing its own copies and MMAs.
 constexpr int kRefGroups = 4;
+// Threads of the CTA-pair half-update: producer, MMA warp and two (online)
+// or four (reference offsets) epilogue groups.
 constexpr int half_threads(bool ref) { return 32 * (2 + (ref ? kRefGroups : kHalfGroups) * kEpiWarps); }
 
 // Guarded range of a reference-offset sum (see the FMA path).
@@ -108,7 +109,10 @@ cudaError_t launch_half_pair(const TcHalfArgs& a, const TensorMap128& tmQ,
 
 int half_stages(int nch, bool qres);    // deepest ring that fits next to resident Q
 size_t half_smem_bytes(int nch, bool qres, int stages);
+// online-max kernel, or with a.use_ref set the reference-offset kernel
+// (requires qres and nch <= 2)
 cudaError_t launch_half_tc(const TcHalfArgs& a, int row_tiles, bool qres, cudaStream_t s);
+cudaError_t launch_half_ref(const TcHalfArgs& a, int row_tiles, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Plan application.  Values V (m x k) are stored transposed per column tile:

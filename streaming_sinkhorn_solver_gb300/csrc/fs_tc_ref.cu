@@ -1,0 +1,309 @@
+// Reference-offset half-update on the tcgen05 tensor cores (one CTA per
+// 128-row tile, d <= 128).
+//
+// "FlashSinkhorn: IO-Aware Entropic Optimal Transport on GPU", Method 1
+// (Proposition 1: the f-update is a row LSE of the biased dot-product score
+// matrix (Q K^T + bias)/eps) and Method 2 (streaming kernels and tiling: a Q
+// row block stays on chip while every K block streams past; score, bias,
+// exponent, sum and potential write-back fused in one pass).
+//
+// Once the potentials have settled, a row's previous LSE is a fixed exponent
+// offset M for the whole pass: no running max, so every score costs one
+// multiply-add, one exp2 and one add.  The accumulator of each score tile is
+// pre-loaded with -M / kappa' (tcgen05.st), the MMAs accumulate onto it, and
+// the epilogue forms 2^{acc kappa' + bias} directly.  The row's sum is
+// range-checked at the end; a row outside the range goes to the fixup list.
+//
+// One CTA owns a 128-row tile of Q (resident in shared memory) and a range
+// of 128-column tiles of K; tile t lives in TMEM buffer t mod 4.
+//   warp 0     producer: Q once; per tile its 512-byte bias slice (a ring of
+//              16) and its K tile into K slot t mod 4, all with cp.async.bulk;
+//   warp 1     one thread issues the tile's tcgen05.mma (M = 128, N = 128,
+//              K = 16 steps) and one commit;
+//   warps 2-17 four epilogue groups of four warps, group g owning buffer g
+//              and the tiles t = g (mod 4); a thread owns one row.
+// The K slots are tied to the TMEM buffers so that the MMA thread, whose
+// serial work per tile bounds the kernel once the epilogue is cheap, waits on
+// a single barrier per tile: tempty[b] completes when the group has re-filled
+// buffer b (four arrivals), the producer has armed it (one arrival with the
+// K tile's byte count) and the K tile has landed.  The producer re-uses slot
+// b once the MMAs of the tile before have completed (tfull[b]), so the MMA
+// thread commits once per tile.  Its descriptors are formed before the loop;
+// a K step is a 32-byte advance of both start addresses.
+#include "fs_tc.cuh"
+
+namespace fs {
+namespace tc {
+
+namespace {
+
+constexpr int kRefThreads = 32 * (2 + kRefGroups * kEpiWarps);
+constexpr int kRefBiasSlots = 16;
+constexpr int kBiasBytes = BN * 4;
+static_assert(kRefGroups == kTmemBufs, "one epilogue group per TMEM buffer");
+
+__host__ __device__ constexpr int ref_smem_bytes(int nch) {
+    return 1024 /* alignment slack */ + (1 + kTmemBufs) * nch * CHUNK_BYTES +
+           kRefBiasSlots * kBiasBytes + BM * 4 * (kRefGroups - 1) /* group merge */ +
+           8 * (1 + 2 * kTmemBufs + 2 * kRefBiasSlots + 1) + 16;
+}
+
+// One 32-column slice: acc[] += 2^{v kappa' + bias} (the accumulator already
+// holds -M / kappa').
+__device__ __forceinline__ void ref_slice(const float (&v)[32], const float4* __restrict__ sb,
+                                          uint64_t ks2, uint64_t (&acc)[4]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 bb = sb[q];
+        float x0, x1, x2, x3;
+        upk(fma2(pk(v[4 * q], v[4 * q + 1]), ks2, pk(bb.x, bb.y)), x0, x1);
+        upk(fma2(pk(v[4 * q + 2], v[4 * q + 3]), ks2, pk(bb.z, bb.w)), x2, x3);
+        acc[(2 * q) & 3] = add2(acc[(2 * q) & 3], pk(ex2(x0), ex2(x1)));
+        acc[(2 * q + 1) & 3] = add2(acc[(2 * q + 1) & 3], pk(ex2(x2), ex2(x3)));
+    }
+}
+
+// the row offset into 128 accumulator columns, 8 at a time from 8 opaque
+// registers (so that no block of copies of `fill` stays live over a loop)
+__device__ __forceinline__ void fill_buffer(uint32_t buf, float fill) {
+    float f8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f8[i] = fill;
+    tmem_reg_fence(f8);
+#pragma unroll
+    for (int q = 0; q < BN / 8; ++q) tmem_st8(buf + q * 8, f8);
+    tmem_wait_st();
+}
+
+template <int NCH>
+__global__ void __launch_bounds__(kRefThreads, 1) k_half_ref(TcHalfArgs a) {
+    constexpr int TILE_BYTES = NCH * CHUNK_BYTES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t rt = blockIdx.x;
+    const int j0 = blockIdx.y * a.tiles_per_split;
+    const int ntiles = min(a.col_tiles, j0 + a.tiles_per_split) - j0;
+
+    uint8_t* sQ = smem;
+    uint8_t* sK = smem + TILE_BYTES;                       // slot b at sK + b * TILE_BYTES
+    uint8_t* sBias = sK + kTmemBufs * TILE_BYTES;
+    float* sMerge = reinterpret_cast<float*>(sBias + kRefBiasSlots * kBiasBytes);
+    uint64_t* qfull = reinterpret_cast<uint64_t*>(sMerge + BM * (kRefGroups - 1));
+    uint64_t* tfull = qfull + 1;                 // MMAs of the buffer's tile complete
+    uint64_t* tempty = tfull + kTmemBufs;        // buffer re-filled and its K tile landed
+    uint64_t* bfull = tempty + kTmemBufs;
+    uint64_t* bempty = bfull + kRefBiasSlots;
+    uint64_t* drain = bempty + kRefBiasSlots;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+
+    if (threadIdx.x == 0) {
+        mbar_init(qfull, 1);
+        for (int b = 0; b < kTmemBufs; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], kEpiWarps + 1);
+        }
+        for (int s = 0; s < kRefBiasSlots; ++s) {
+            mbar_init(&bfull[s], 1);
+            mbar_init(&bempty[s], kEpiWarps);
+        }
+        mbar_init(drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            mbar_arrive_expect_tx(qfull, (uint32_t)TILE_BYTES);
+            const char* Qg = reinterpret_cast<const char*>(a.Q) + rt * (int64_t)TILE_BYTES;
+#pragma unroll
+            for (int c = 0; c < NCH; ++c)
+                bulk_g2s(sQ + c * CHUNK_BYTES, Qg + c * CHUNK_BYTES, CHUNK_BYTES, qfull);
+            const char* Kg = reinterpret_cast<const char*>(a.K) + (int64_t)j0 * TILE_BYTES;
+            int kiss = 0, biss = 0;
+            bool ok = true;
+            for (int t = 0; t < ntiles; ++t) {
+                const int bs = t % kRefBiasSlots;
+                ok = mbar_wait(&bempty[bs], (uint32_t)((t / kRefBiasSlots) & 1) ^ 1u, a.err,
+                               ERR_TIMEOUT_PRODUCER);
+                if (!ok) break;
+                mbar_arrive_expect_tx(&bfull[bs], kBiasBytes);
+                bulk_g2s(sBias + bs * kBiasBytes, a.cbias + (int64_t)(j0 + t) * BN, kBiasBytes,
+                         &bfull[bs]);
+                biss = t + 1;
+                const int b = t & (kTmemBufs - 1);
+                const int u = t >> 2;
+                // slot b is free once the MMAs of tile t - 4 have completed
+                if (u > 0) {
+                    ok = mbar_wait(&tfull[b], (uint32_t)((u - 1) & 1), a.err, ERR_TIMEOUT_PRODUCER);
+                    if (!ok) break;
+                }
+                uint8_t* slot = sK + b * TILE_BYTES;
+                mbar_arrive_expect_tx(&tempty[b], (uint32_t)TILE_BYTES);
+#pragma unroll
+                for (int c = 0; c < NCH; ++c)
+                    bulk_g2s(slot + c * CHUNK_BYTES, Kg + (int64_t)t * TILE_BYTES + c * CHUNK_BYTES,
+                             CHUNK_BYTES, &tempty[b]);
+                kiss = t + 1;
+            }
+            if (!ok) {
+                // let every copy already issued land before the CTA can exit
+                for (int t = kiss > kTmemBufs ? kiss - kTmemBufs : 0; t < kiss; ++t)
+                    mbar_wait(&tempty[t & (kTmemBufs - 1)], (uint32_t)((t >> 2) & 1), a.err,
+                              ERR_TIMEOUT_PRODUCER);
+                for (int t = biss > kRefBiasSlots ? biss - kRefBiasSlots : 0; t < biss; ++t)
+                    mbar_wait(&bfull[t % kRefBiasSlots], (uint32_t)((t / kRefBiasSlots) & 1),
+                              a.err, ERR_TIMEOUT_PRODUCER);
+            }
+            mbar_wait(qfull, 0, a.err, ERR_TIMEOUT_PRODUCER);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
+            uint64_t qd[NCH];
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) qd[c] = sdesc_sw128(smem_u32(sQ + c * CHUNK_BYTES));
+            const uint64_t kd0 = sdesc_sw128(smem_u32(sK));
+            bool ok = mbar_wait(qfull, 0, a.err, ERR_TIMEOUT_MMA);
+            for (int t = 0; t < ntiles && ok; ++t) {
+                const int b = t & (kTmemBufs - 1);
+                if (!mbar_wait(&tempty[b], (uint32_t)((t >> 2) & 1), a.err, ERR_TIMEOUT_MMA)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + (uint32_t)(b * BN);
+                const uint64_t kd = kd0 + (uint64_t)((b * TILE_BYTES) >> 4);
+#pragma unroll
+                for (int c = 0; c < NCH; ++c)
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_f16(d_tmem, qd[c] + (uint64_t)(2 * kk),
+                                kd + (uint64_t)((c * CHUNK_BYTES) >> 4) + (uint64_t)(2 * kk), idesc,
+                                1u);
+                mma_commit(&tfull[b]);
+            }
+            // every MMA issued has completed once `drain` fires
+            mma_commit(drain);
+            mbar_wait(drain, 0, a.err, ERR_TIMEOUT_MMA);
+        }
+    } else {
+        // ---------------- epilogue groups: one thread per row ----------------
+        const int grp = (warp - 2) / kEpiWarps;
+        const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
+        const int rloc = quarter * 32 + lane;
+        const int64_t row = rt * BM + rloc;
+        const float ks = *a.kscale;
+        const uint64_t ks2 = pk(ks, ks);
+        const int64_t rr = row < a.nr ? row : a.nr - 1;
+        const float M = a.rlogw2[rr] - a.rbias[rr];
+        const float fill = -M / ks;
+        const uint32_t buf = tmem + (uint32_t)(grp * BN) + ((uint32_t)(quarter * 32) << 16);
+        fill_buffer(buf, fill);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[grp]);
+
+        uint64_t acc[4] = {pk(0.f, 0.f), pk(0.f, 0.f), pk(0.f, 0.f), pk(0.f, 0.f)};
+        for (int t = grp; t < ntiles; t += kRefGroups) {
+            if (!mbar_wait(&tfull[grp], (uint32_t)((t >> 2) & 1), a.err, ERR_TIMEOUT_EPILOGUE))
+                break;
+            tc_fence_after();
+            const int bs = t % kRefBiasSlots;
+            if (!mbar_wait(&bfull[bs], (uint32_t)((t / kRefBiasSlots) & 1), a.err,
+                           ERR_TIMEOUT_EPILOGUE))
+                break;
+            const float4* sb = reinterpret_cast<const float4*>(sBias + bs * kBiasBytes);
+            float va[32], vb[32];
+            tmem_ld32(buf, va);
+            tmem_wait_ld();
+            tmem_reg_fence(va);
+            tmem_ld32(buf + 32, vb);
+            ref_slice(va, sb, ks2, acc);
+            tmem_wait_ld();
+            tmem_reg_fence(vb);
+            tmem_ld32(buf + 64, va);
+            ref_slice(vb, sb + 8, ks2, acc);
+            tmem_wait_ld();
+            tmem_reg_fence(va);
+            tmem_ld32(buf + 96, vb);
+            ref_slice(va, sb + 16, ks2, acc);
+            tmem_wait_ld();
+            tmem_reg_fence(vb);
+            // every score of the tile is in registers: re-fill, release
+            fill_buffer(buf, fill);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[grp]);
+            ref_slice(vb, sb + 24, ks2, acc);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bempty[bs]);
+        }
+        float s0, s1, s2, s3, s4, s5, s6, s7;
+        upk(acc[0], s0, s1);
+        upk(acc[1], s2, s3);
+        upk(acc[2], s4, s5);
+        upk(acc[3], s6, s7);
+        const float S = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+        // every group used the same offset M: the row sum is the groups'
+        // sums, added in a fixed order
+        if (grp > 0) sMerge[(grp - 1) * BM + rloc] = S;
+        asm volatile("bar.sync 1, %0;" ::"n"(kRefGroups * kEpiWarps * 32) : "memory");
+        if (grp == 0 && row < a.nr) {
+            float St = S;
+#pragma unroll
+            for (int g = 1; g < kRefGroups; ++g) St += sMerge[(g - 1) * BM + rloc];
+            if (a.splits > 1) {
+                a.partial[(int64_t)blockIdx.y * a.nr + row] = make_float2(M, St);
+            } else {
+                if (!(St >= kTcMinRefSum && St <= kTcMaxRefSum)) {
+                    const unsigned int slot = atomicAdd(&a.fix_count[0], 1u);
+                    if (slot < (unsigned int)a.nr) a.fix_list[slot] = (int)row;
+                }
+                const float lse2 = M + log2f(St);
+                a.pot[row] = a.rnorm[row] - a.eps_ln2 * lse2;
+                a.rbias[row] = a.rlogw2[row] - lse2;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int NCH>
+cudaError_t launch_ref_t(const TcHalfArgs& a, int row_tiles, cudaStream_t s) {
+    constexpr int smem = ref_smem_bytes(NCH);
+    static_assert(smem <= kSmemLimit, "reference kernel does not fit in shared memory");
+    const cudaError_t e =
+        cudaFuncSetAttribute(k_half_ref<NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    k_half_ref<NCH><<<dim3((unsigned)row_tiles, (unsigned)a.splits), kRefThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_half_ref(const TcHalfArgs& a, int row_tiles, cudaStream_t s) {
+    cudaError_t e;
+    if (a.nch == 1)
+        e = launch_ref_t<1>(a, row_tiles, s);
+    else if (a.nch == 2)
+        e = launch_ref_t<2>(a, row_tiles, s);
+    else
+        return cudaErrorInvalidValue;
+    count_launch();
+    return e;
+}
+
+}  // namespace tc
+}  // namespace fs
