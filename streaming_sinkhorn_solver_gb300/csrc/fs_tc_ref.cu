@@ -21,7 +21,15 @@
 //   warp 1     one thread issues the tile's tcgen05.mma (M = 128, N = 128,
 //              K = 16 steps) and one commit;
 //   warps 2-17 four epilogue groups of four warps, group g owning buffer g
-//              and the tiles t = g (mod 4); a thread owns one row.
+//              and the tiles t = g (mod 4).
+// The epilogue reads the scores in the 16x256b shape, in which a thread holds
+// two columns of every eight for two rows of a 16-lane block, so that over its
+// warp's 32 lanes it covers 4 rows x 32 columns of a tile (rather than 1 row
+// x 128 columns).  Every bias value it loads from shared memory then serves
+// four rows: per-thread broadcast loads of a per-column bias would otherwise
+// cost as much shared-memory bandwidth (128 bytes per clock and SM) as the
+// exponentials cost MUFU time.  The four threads sharing a row add their
+// sums once, at the end.
 // The K slots are tied to the TMEM buffers so that the MMA thread, whose
 // serial work per tile bounds the kernel once the epilogue is cheap, waits on
 // a single barrier per tile: tempty[b] completes when the group has re-filled
@@ -48,18 +56,19 @@ __host__ __device__ constexpr int ref_smem_bytes(int nch) {
            8 * (1 + 2 * kTmemBufs + 2 * kRefBiasSlots + 1) + 16;
 }
 
-// One 32-column slice: acc[] += 2^{v kappa' + bias} (the accumulator already
-// holds -M / kappa').
-__device__ __forceinline__ void ref_slice(const float (&v)[32], const float4* __restrict__ sb,
-                                          uint64_t ks2, uint64_t (&acc)[4]) {
+// One 16-lane x 32-column slice (tmem_ld16x32 layout): for each repetition
+// i, the column pair's bias bp[i] serves both rows; lo/hi accumulate the rows
+// t/4 and t/4 + 8 of the block: acc += 2^{v kappa' + bias} (the accumulator
+// already holds -M / kappa').
+__device__ __forceinline__ void ref_slice(const float (&v)[16], const uint64_t (&bp)[4],
+                                          uint64_t ks2, uint64_t& lo, uint64_t& hi) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const float4 bb = sb[q];
+    for (int i = 0; i < 4; ++i) {
         float x0, x1, x2, x3;
-        upk(fma2(pk(v[4 * q], v[4 * q + 1]), ks2, pk(bb.x, bb.y)), x0, x1);
-        upk(fma2(pk(v[4 * q + 2], v[4 * q + 3]), ks2, pk(bb.z, bb.w)), x2, x3);
-        acc[(2 * q) & 3] = add2(acc[(2 * q) & 3], pk(ex2(x0), ex2(x1)));
-        acc[(2 * q + 1) & 3] = add2(acc[(2 * q + 1) & 3], pk(ex2(x2), ex2(x3)));
+        upk(fma2(pk(v[4 * i], v[4 * i + 1]), ks2, bp[i]), x0, x1);
+        upk(fma2(pk(v[4 * i + 2], v[4 * i + 3]), ks2, bp[i]), x2, x3);
+        lo = add2(lo, pk(ex2(x0), ex2(x1)));
+        hi = add2(hi, pk(ex2(x2), ex2(x3)));
     }
 }
 
@@ -193,22 +202,23 @@ __global__ void __launch_bounds__(kRefThreads, 1) k_half_ref(TcHalfArgs a) {
             mbar_wait(drain, 0, a.err, ERR_TIMEOUT_MMA);
         }
     } else {
-        // ---------------- epilogue groups: one thread per row ----------------
+        // ---------------- epilogue groups ----------------
         const int grp = (warp - 2) / kEpiWarps;
         const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
-        const int rloc = quarter * 32 + lane;
-        const int64_t row = rt * BM + rloc;
         const float ks = *a.kscale;
         const uint64_t ks2 = pk(ks, ks);
-        const int64_t rr = row < a.nr ? row : a.nr - 1;
-        const float M = a.rlogw2[rr] - a.rbias[rr];
-        const float fill = -M / ks;
+        // the fill: this thread's own lane, 32*quarter + lane
+        const int64_t rf = min(rt * BM + quarter * 32 + lane, a.nr - 1);
+        const float fill = -(a.rlogw2[rf] - a.rbias[rf]) / ks;
         const uint32_t buf = tmem + (uint32_t)(grp * BN) + ((uint32_t)(quarter * 32) << 16);
         fill_buffer(buf, fill);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[grp]);
 
+        // rows of this thread: 32*quarter + lane/4 + 8k (k = 0..3; acc[k]),
+        // columns 8i + 2(lane%4) + {0, 1} of every 32-column quarter
+        const int cpair = 2 * (lane & 3);
         uint64_t acc[4] = {pk(0.f, 0.f), pk(0.f, 0.f), pk(0.f, 0.f), pk(0.f, 0.f)};
         for (int t = grp; t < ntiles; t += kRefGroups) {
             if (!mbar_wait(&tfull[grp], (uint32_t)((t >> 2) & 1), a.err, ERR_TIMEOUT_EPILOGUE))
@@ -218,38 +228,57 @@ __global__ void __launch_bounds__(kRefThreads, 1) k_half_ref(TcHalfArgs a) {
             if (!mbar_wait(&bfull[bs], (uint32_t)((t / kRefBiasSlots) & 1), a.err,
                            ERR_TIMEOUT_EPILOGUE))
                 break;
-            const float4* sb = reinterpret_cast<const float4*>(sBias + bs * kBiasBytes);
-            float va[32], vb[32];
-            tmem_ld32(buf, va);
-            tmem_wait_ld();
-            tmem_reg_fence(va);
-            tmem_ld32(buf + 32, vb);
-            ref_slice(va, sb, ks2, acc);
-            tmem_wait_ld();
-            tmem_reg_fence(vb);
-            tmem_ld32(buf + 64, va);
-            ref_slice(vb, sb + 8, ks2, acc);
-            tmem_wait_ld();
-            tmem_reg_fence(va);
-            tmem_ld32(buf + 96, vb);
-            ref_slice(va, sb + 16, ks2, acc);
-            tmem_wait_ld();
-            tmem_reg_fence(vb);
-            // every score of the tile is in registers: re-fill, release
-            fill_buffer(buf, fill);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[grp]);
-            ref_slice(vb, sb + 24, ks2, acc);
+            const uint64_t* sb =
+                reinterpret_cast<const uint64_t*>(sBias + bs * kBiasBytes + cpair * 4);
+            // slices s = 2 cq + h: column quarter cq, lane half h; the next
+            // slice's load is in flight while one is summed
+            float va[16], vb[16];
+            uint64_t bp[4];
+            tmem_ld16x32(buf, va);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const int cq = s >> 1, h = s & 1;
+                float(&cur)[16] = (s & 1) ? vb : va;
+                float(&nxt)[16] = (s & 1) ? va : vb;
+                tmem_wait_ld();
+                tmem_reg_fence(cur);
+                if (s < 7) {
+                    const int s1 = s + 1;
+                    tmem_ld16x32(buf + ((uint32_t)(16 * (s1 & 1)) << 16) + (uint32_t)(32 * (s1 >> 1)),
+                                 nxt);
+                } else {
+                    // every score of the tile is in registers: re-fill, release
+                    fill_buffer(buf, fill);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[grp]);
+                }
+                if (h == 0) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) bp[i] = sb[(32 * cq + 8 * i) / 2];
+                }
+                ref_slice(cur, bp, ks2, acc[2 * h], acc[2 * h + 1]);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bempty[bs]);
         }
-        float s0, s1, s2, s3, s4, s5, s6, s7;
-        upk(acc[0], s0, s1);
-        upk(acc[1], s2, s3);
-        upk(acc[2], s4, s5);
-        upk(acc[3], s6, s7);
-        const float S = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+        // row sums: the pair halves, then the four threads sharing the rows
+        float S4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float x, y;
+            upk(acc[k], x, y);
+            S4[k] = x + y;
+            S4[k] += __shfl_xor_sync(0xffffffffu, S4[k], 1);
+            S4[k] += __shfl_xor_sync(0xffffffffu, S4[k], 2);
+        }
+        // from here on a thread owns the row 32*quarter + lane/4 + 8(lane%4)
+        const int kown = lane & 3;
+        const float S = kown == 0 ? S4[0] : kown == 1 ? S4[1] : kown == 2 ? S4[2] : S4[3];
+        const int rloc = quarter * 32 + (lane >> 2) + 8 * kown;
+        const int64_t row = rt * BM + rloc;
+        const int64_t rr = row < a.nr ? row : a.nr - 1;
+        const float M = a.rlogw2[rr] - a.rbias[rr];
         // every group used the same offset M: the row sum is the groups'
         // sums, added in a fixed order
         if (grp > 0) sMerge[(grp - 1) * BM + rloc] = S;
