@@ -48,6 +48,10 @@ def test_capture_refuses_host_arrays_and_growth():
     import torch
     inp = random_cloud(500, 400, 3, seed=950)
     t = to_dev(inp)
+    # earlier tests in the same process may have grown the workspace past
+    # what the large problem below needs: start from an empty one
+    torch.cuda.synchronize()
+    fs.fs_release()
     fs.fs_sinkhorn_solve(t["X"], t["a"], t["Y"], t["b"], 0.1, 2)
     graph = torch.cuda.CUDAGraph()
     with pytest.raises(fs.FlashSinkhornError) as host_err:
