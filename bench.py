@@ -120,18 +120,35 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def _kernel_source_hash():
+# Sources that define and launch the dominant half-update kernel of each path
+# (kernel, host launch code and the headers they share): a committed ncu
+# summary stays valid while none of these files changes.
+KERNEL_SOURCES = {
+    "fma": ["fs_fma.cu", "fs_fma_host.cu", "fs_api.cu", "fs_internal.cuh", "fs_host.cuh"],
+    "tc": ["fs_tc_ref.cu", "fs_tc_half.cu", "fs_tc_host.cu", "fs_tc.cuh", "fs_tc_kernels.cuh",
+           "fs_internal.cuh", "fs_host.cuh"],
+    "pair": ["fs_tc_pair.cu", "fs_tc_host.cu", "fs_tc.cuh", "fs_tc_kernels.cuh", "fs_internal.cuh",
+             "fs_host.cuh"],
+}
+
+
+def kernel_family(d: int, tensor_path: bool) -> str:
+    if not tensor_path:
+        return "fma"
+    return "tc" if d <= 128 else "pair"
+
+
+def _kernel_source_hash(family: str):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "streaming_sinkhorn_solver_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as fh:
-                h.update(name.encode())
-                h.update(fh.read())
+    for name in sorted(KERNEL_SOURCES[family]):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode())
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def _traffic_from_profiles(workload: str):
+def _traffic_from_profiles(workload: str, family: str):
     """DRAM bytes per launch of the half-update kernel from the committed ncu
     summary for this workload, or None if absent or taken on other sources."""
     path = os.path.join(PROFILES, f"half_update_{workload}.md")
@@ -142,7 +159,7 @@ def _traffic_from_profiles(workload: str):
         if line.startswith("- ") and "=" in line:
             k, v = line[2:].split("=", 1)
             vals[k.strip()] = v.strip().strip("`")
-    if vals.get("source_hash") != _kernel_source_hash():
+    if vals.get("source_hash") != _kernel_source_hash(family):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
@@ -374,7 +391,7 @@ def run_gb300(args, w):
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "peak_source": f"{peaks['source']} copy bandwidth"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = _traffic_from_profiles(w.name)
+    roof["traffic"] = _traffic_from_profiles(w.name, kernel_family(d, tensor_path))
     roof["kernel"] = "half_update"
     roof["avg_launch_ms"] = avg_half_ms
     roof["launches"] = half_n
