@@ -208,3 +208,20 @@ def test_reference_offset_path_with_fixups(d, eps, iters):
     fr, gr = orc.sinkhorn(C, inp["a"], inp["b"], eps, iters)
     assert max_abs(f, fr) <= F_TOL_TENSOR * C.max()
     assert max_abs(g, gr) <= F_TOL_TENSOR * C.max()
+
+
+@pytest.mark.parametrize("n,m,d,splits", [(8250, 8300, 40, 0), (8200, 8192, 100, 0),
+                                          (8192, 8192, 128, 0), (8192, 8192, 64, 1),
+                                          (8192, 8192, 64, 4)])
+def test_reference_offset_kernel_shapes(n, m, d, splits):
+    """The reference-offset one-CTA kernel at n*m >= 2^26: one K chunk with
+    zero-padded dimensions (d = 40), two chunks (d = 100, 128), ragged row
+    and column tiles, and forced column splits (1: the guard in the kernel
+    itself; 4: the guard in the split merge)."""
+    inp = make_inputs("c3_n50k_d64", n=n, m=m, d=d, seed=94 + d)
+    C = orc.cost(inp["X"], inp["Y"])
+    f, g, _ = _solve(inp, [(0.05, 6)], path="auto", splits=splits)
+    fr, gr = orc.sinkhorn(C, inp["a"], inp["b"], 0.05, 6)
+    assert max_abs(f, fr) <= F_TOL_TENSOR * C.max()
+    assert max_abs(g, gr) <= F_TOL_TENSOR * C.max()
+
