@@ -220,24 +220,29 @@ __global__ void __launch_bounds__(kHalfThreads, 1) k_half_tc(TcHalfArgs a) {
             mbar_wait(drain, 0, a.err, ERR_TIMEOUT_MMA);
         }
     } else {
-        // ---------------- epilogue groups: one thread per row ----------------
+        // ---------------- epilogue groups ----------------
+        // The scores are read in the 16x256b shape: a thread holds columns
+        // 8i + 2(lane%4) + {0, 1} (i = 0..15) of the four rows
+        // 32*quarter + lane/4 + 8k (k = 0..3), so that each bias value it
+        // loads serves four rows, and keeps a running (max, sum) per row over
+        // its own columns; the four threads sharing a row merge at the end.
         const int grp = (warp - 2) / kEpiWarps;
         const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
-        const int rloc = quarter * 32 + lane;
-        const int64_t row = rt * BM + rloc;
         const float ks = *a.kscale;
         const uint64_t ks2 = pk(ks, ks);
         const uint32_t lofs = (uint32_t)(quarter * 32) << 16;
-        float M = -INFINITY, S = 0.f;
+        const int cpair = 2 * (lane & 3);
+        float Mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        float Sr[4] = {0.f, 0.f, 0.f, 0.f};
         for (int t = grp; t < ntiles; t += GROUPS) {
             const int b = t & (kTmemBufs - 1);
             const uint32_t ph = (uint32_t)((t >> 2) & 1);
             if (!mbar_wait(&tfull[b], ph, a.err, ERR_TIMEOUT_EPILOGUE)) break;
             tc_fence_after();
-            float v[BN];
-#pragma unroll
-            for (int q = 0; q < BN / 32; ++q)
-                tmem_ld32(tmem + (uint32_t)(b * BN) + lofs + q * 32, v + q * 32);
+            // v[64 h + 4i + {0,1}]: row k = 2h, v[64 h + 4i + {2,3}]: row k = 2h + 1
+            float v[2 * 64];
+            tmem_ld16x128(tmem + (uint32_t)(b * BN) + lofs, v);
+            tmem_ld16x128(tmem + (uint32_t)(b * BN) + lofs + (16u << 16), v + 64);
             tmem_wait_ld();
             tmem_reg_fence(v);
             tc_fence_before();
@@ -248,42 +253,75 @@ __global__ void __launch_bounds__(kHalfThreads, 1) k_half_tc(TcHalfArgs a) {
                            ERR_TIMEOUT_EPILOGUE))
                 break;
 
-            // s = acc kappa' + bias, row max (two chains)
-            const float4* sb = reinterpret_cast<const float4*>(sBias + bs * kBiasBytes);
-            float mx0 = -INFINITY, mx1 = -INFINITY;
+            // s = acc kappa' + bias, per-row maxima
+            const uint64_t* sb =
+                reinterpret_cast<const uint64_t*>(sBias + bs * kBiasBytes + cpair * 4);
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int q = 0; q < BN / 4; ++q) {
-                const float4 bb = sb[q];
-                upk(fma2(pk(v[4 * q], v[4 * q + 1]), ks2, pk(bb.x, bb.y)), v[4 * q], v[4 * q + 1]);
-                upk(fma2(pk(v[4 * q + 2], v[4 * q + 3]), ks2, pk(bb.z, bb.w)), v[4 * q + 2],
-                    v[4 * q + 3]);
-                mx0 = max3(mx0, v[4 * q], v[4 * q + 1]);
-                mx1 = max3(mx1, v[4 * q + 2], v[4 * q + 3]);
+            for (int i = 0; i < 16; ++i) {
+                const uint64_t bp = sb[4 * i];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float* w = v + 64 * h + 4 * i;
+                    upk(fma2(pk(w[0], w[1]), ks2, bp), w[0], w[1]);
+                    upk(fma2(pk(w[2], w[3]), ks2, bp), w[2], w[3]);
+                    mx[2 * h] = max3(mx[2 * h], w[0], w[1]);
+                    mx[2 * h + 1] = max3(mx[2 * h + 1], w[2], w[3]);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bempty[bs]);
-            const float mx = fmaxf(mx0, mx1);
-            if (mx > M) {
-                S *= ex2(M - mx);
-                M = mx;
-            }
-            if (M == -INFINITY) continue;   // only padding columns so far: nothing to add
-            // S += sum 2^{s - M}
-            const uint64_t nm = pk(-M, -M);
-            uint64_t acc0 = pk(0.f, 0.f), acc1 = pk(0.f, 0.f);
 #pragma unroll
-            for (int q = 0; q < BN / 4; ++q) {
-                float x0, x1, x2, x3;
-                upk(add2(pk(v[4 * q], v[4 * q + 1]), nm), x0, x1);
-                upk(add2(pk(v[4 * q + 2], v[4 * q + 3]), nm), x2, x3);
-                acc0 = add2(acc0, pk(ex2(x0), ex2(x1)));
-                acc1 = add2(acc1, pk(ex2(x2), ex2(x3)));
+            for (int k = 0; k < 4; ++k) {
+                if (mx[k] > Mr[k]) {
+                    Sr[k] *= ex2(Mr[k] - mx[k]);
+                    Mr[k] = mx[k];
+                }
             }
-            float s0, s1, s2, s3;
-            upk(acc0, s0, s1);
-            upk(acc1, s2, s3);
-            S += (s0 + s1) + (s2 + s3);
+            // S += sum 2^{s - M} (rows still at -inf saw only padding: their
+            // terms are 2^{-inf - (-inf)}, so they are masked to zero)
+            uint64_t acc[4] = {pk(0.f, 0.f), pk(0.f, 0.f), pk(0.f, 0.f), pk(0.f, 0.f)};
+            uint64_t nm[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) nm[k] = pk(-Mr[k], -Mr[k]);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float* w = v + 64 * h + 4 * i;
+                    float x0, x1, x2, x3;
+                    upk(add2(pk(w[0], w[1]), nm[2 * h]), x0, x1);
+                    upk(add2(pk(w[2], w[3]), nm[2 * h + 1]), x2, x3);
+                    acc[2 * h] = add2(acc[2 * h], pk(ex2(x0), ex2(x1)));
+                    acc[2 * h + 1] = add2(acc[2 * h + 1], pk(ex2(x2), ex2(x3)));
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float s0, s1;
+                upk(acc[k], s0, s1);
+                if (Mr[k] != -INFINITY) Sr[k] += s0 + s1;
+            }
         }
+        // the four threads sharing each row merge their (max, sum)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+#pragma unroll
+            for (int o = 1; o <= 2; o <<= 1) {
+                const float Mo = __shfl_xor_sync(0xffffffffu, Mr[k], o);
+                const float So = __shfl_xor_sync(0xffffffffu, Sr[k], o);
+                const float Mn = fmaxf(Mr[k], Mo);
+                Sr[k] = (Mr[k] == -INFINITY ? 0.f : Sr[k] * ex2(Mr[k] - Mn)) +
+                        (Mo == -INFINITY ? 0.f : So * ex2(Mo - Mn));
+                Mr[k] = Mn;
+            }
+        }
+        // from here on a thread owns the row 32*quarter + lane/4 + 8(lane%4)
+        const int kown = lane & 3;
+        const float M = kown == 0 ? Mr[0] : kown == 1 ? Mr[1] : kown == 2 ? Mr[2] : Mr[3];
+        const float S = kown == 0 ? Sr[0] : kown == 1 ? Sr[1] : kown == 2 ? Sr[2] : Sr[3];
+        const int rloc = quarter * 32 + (lane >> 2) + 8 * kown;
+        const int64_t row = rt * BM + rloc;
 
         // merge the groups in a fixed order: group 0 absorbs groups 1, 2, ...
         if (grp > 0) sMerge[(grp - 1) * BM + rloc] = make_float2(M, S);
