@@ -311,6 +311,97 @@ fs_status fs_hvp_x(const float* X, const float* a, int64_t n,
  */
 fs_status fs_unit_rates(double* out, void* stream);
 
+/*
+ * Block-sparse solver for low-dimensional clouds, after the follow-up post
+ * "FlashSinkhorn 2: Block-Sparse Entropic Optimal Transport" (patty.io):
+ * sections on the coarse centroid stage, the Morton ordering, block screening
+ * and the per-row / per-column bound on the skipped tiles.  Readings (the post
+ * gives no formulas):
+ *   - Morton order: coordinates quantised to 2^21 cells per axis over the
+ *     joint bounding box of X and Y, q_k = floor((p_k - lo_k) * (2^21 /
+ *     (hi_k - lo_k))) in float32 (each operation rounded once), clamped to
+ *     [0, 2^21 - 1]; bit b of q_k is bit b*d + k of the code; each cloud is
+ *     sorted stably by its code.  Blocks (and cells) are 128 consecutive
+ *     sorted points.
+ *   - Coarse stage: coarse_iters dense Sinkhorn iterations (the same update)
+ *     between the blocks' weight-averaged centroids with the blocks' weights;
+ *     every point takes its block's potential.
+ *   - Screening, before every half-update: with Delta = c_I - c_J and offsets
+ *     u_i = x_i - c_I, v_j = y_j - c_J from the block centroids, block pair
+ *     (I, J) carries at most 2^U of plan mass,
+ *       U = log2 sum_i a_i 2^{(f_i - 2 Delta.u_i) L/eps}
+ *         + log2 sum_j b_j 2^{(g_j + 2 Delta.v_j) L/eps} - |Delta|^2 L/eps
+ *     (L = log2 e; from C_ij >= |Delta|^2 + 2 Delta.(u_i - v_j)).  An output
+ *     block O keeps input block J iff U + sigma >= log2(tau W_O / N_in) or J
+ *     is the first maximiser of U (sigma = 1/16 + 2^-16 (|max psi_O| +
+ *     |max chi_J| + |Delta|^2 L/eps) with psi = f L/eps + log2 a, chi likewise,
+ *     a slack in favour of keeping), so the skipped blocks of every output
+ *     block carry less than tau times its weight W_O.  tau = 0 keeps all.
+ *   - Fine stage: f-updates over each row block's kept blocks, then g-updates
+ *     over each column block's, until the row residual |P 1 - a|_1 of the
+ *     block-sparse plan (measured every check_every iterations with a fresh
+ *     screening) is <= target, or max_iters iterations.
+ */
+typedef struct fs_sparse_options {
+    int32_t coarse_iters;  /* centroid iterations; 0: start from the caller's f and g */
+    int32_t max_iters;     /* fine iterations, at most (0: coarse stage and report only) */
+    int32_t check_every;   /* residual test period in iterations (0: never, run max_iters) */
+    float tau;             /* omitted-mass bound per block relative to its weight, [0, 1) */
+    float target;          /* stop when the row residual <= target (0: never) */
+    int32_t reserved[4];   /* must be zero */
+} fs_sparse_options;
+
+typedef struct fs_sparse_report {
+    int32_t iters;         /* fine iterations run */
+    int32_t passes;        /* block-sparse passes (2 per iteration + residual measurements) */
+    int32_t blocks_x, blocks_y;
+    double residual;       /* |P 1 - a|_1 of the block-sparse plan at the returned f, g */
+    double kept_blocks;    /* block pairs evaluated, summed over passes */
+    double kept_pairs;     /* score pairs evaluated, summed over passes */
+} fs_sparse_report;
+
+/*
+ * fs_sparse_solve -- the block-sparse solver above, for 1 <= d <= 3.
+ * X, a, Y, b as in fs_sinkhorn_solve (device or host memory).  f (n) and g
+ * (m) are outputs; with coarse_iters == 0 they are also inputs: the first
+ * screening bounds the plan at (f, g), so pass a consistent pair (e.g. the
+ * result of a previous call at a larger eps).  `report` (host, may be NULL)
+ * receives the iteration count, the final residual (one more measurement
+ * pass) and the work done.  The call synchronises `stream` at every residual
+ * test and at the end, and cannot be captured in a CUDA graph.
+ * Workspace: O((n + m) + (n/128)(m/128)) -- the kept-block lists hold one int
+ * per block pair; more than 2^30 block pairs is FS_ERR_UNSUPPORTED.
+ * Errors: FS_ERR_UNSUPPORTED for d > 3; FS_ERR_INVALID_ARG for null pointers,
+ * sizes < 1, eps <= 0, tau outside [0, 1), negative counts or target, or
+ * non-zero reserved fields.
+ */
+fs_status fs_sparse_solve(const float* X, const float* a, int64_t n,
+                          const float* Y, const float* b, int64_t m, int32_t d, float eps,
+                          const fs_sparse_options* opt, float* f, float* g,
+                          fs_sparse_report* report, void* stream);
+
+/*
+ * fs_morton_order -- the Morton order the block-sparse solver uses: perm_x[k]
+ * is the index of the k-th point of X in order (ties keep the input order),
+ * likewise perm_y.  All four arrays are DEVICE memory; perm_* are int64.
+ */
+fs_status fs_morton_order(const float* X, int64_t n, const float* Y, int64_t m, int32_t d,
+                          int64_t* perm_x, int64_t* perm_y, void* stream);
+
+/*
+ * fs_sparse_screen -- one screening of the block-sparse solver at given
+ * potentials f (n) and g (m): side 0 screens for an f-update (output blocks
+ * are X's), side 1 for a g-update.  Blocks are numbered in Morton order.
+ * counts[o] (int32, one per output block) receives the number of kept input
+ * blocks and lists[o * N_in + e], e < counts[o], their indices in increasing
+ * order (int32, N_out x N_in; entries past counts[o] are unspecified).  All
+ * arrays are DEVICE memory.
+ */
+fs_status fs_sparse_screen(const float* X, const float* a, int64_t n,
+                           const float* Y, const float* b, int64_t m, int32_t d, float eps,
+                           const float* f, const float* g, float tau, int32_t side,
+                           int32_t* counts, int32_t* lists, void* stream);
+
 /* Device bytes the library's workspace needs for these sizes (k = 0 for a
  * solve).  The workspace is O((n + m) d): no n x m buffer exists. */
 int64_t fs_workspace_bytes(int64_t n, int64_t m, int32_t d, int32_t k, const fs_options* opt);

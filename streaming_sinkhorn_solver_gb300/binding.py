@@ -32,7 +32,8 @@ EXPORTED = ("fs_sinkhorn_solve", "fs_apply_plan", "fs_barycentric", "fs_grad_x",
             "fs_apply_plan_t", "fs_barycentric_y", "fs_grad_y", "fs_dual_value",
             "fs_marginal_residuals", "fs_workspace_bytes", "fs_check", "fs_release",
             "fs_last_error", "fs_version", "fs_launch_count", "fs_timing_enable",
-            "fs_timing_read", "fs_sinkhorn_solve_noalloc", "fs_unit_rates", "fs_hvp_x")
+            "fs_timing_read", "fs_sinkhorn_solve_noalloc", "fs_unit_rates", "fs_hvp_x",
+            "fs_sparse_solve", "fs_morton_order", "fs_sparse_screen")
 
 
 class FlashSinkhornError(RuntimeError):
@@ -48,6 +49,19 @@ class fs_options(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("splits", ctypes.c_int32),
                 ("check_finite", ctypes.c_int32), ("cost", ctypes.c_int32),
                 ("reserved", ctypes.c_int32 * 4)]
+
+
+class fs_sparse_options(ctypes.Structure):
+    _fields_ = [("coarse_iters", ctypes.c_int32), ("max_iters", ctypes.c_int32),
+                ("check_every", ctypes.c_int32), ("tau", ctypes.c_float),
+                ("target", ctypes.c_float), ("reserved", ctypes.c_int32 * 4)]
+
+
+class fs_sparse_report(ctypes.Structure):
+    _fields_ = [("iters", ctypes.c_int32), ("passes", ctypes.c_int32),
+                ("blocks_x", ctypes.c_int32), ("blocks_y", ctypes.c_int32),
+                ("residual", ctypes.c_double), ("kept_blocks", ctypes.c_double),
+                ("kept_pairs", ctypes.c_double)]
 
 
 _lib = None
@@ -99,6 +113,15 @@ def load_library(path: Optional[str] = None):
         lib.fs_hvp_x.restype = ctypes.c_int
         lib.fs_unit_rates.argtypes = [ctypes.POINTER(ctypes.c_double), vp]
         lib.fs_unit_rates.restype = ctypes.c_int
+        lib.fs_sparse_solve.argtypes = [vp, vp, i64, vp, vp, i64, i32, f32,
+                                        ctypes.POINTER(fs_sparse_options), vp, vp,
+                                        ctypes.POINTER(fs_sparse_report), vp]
+        lib.fs_sparse_solve.restype = ctypes.c_int
+        lib.fs_morton_order.argtypes = [vp, i64, vp, i64, i32, vp, vp, vp]
+        lib.fs_morton_order.restype = ctypes.c_int
+        lib.fs_sparse_screen.argtypes = [vp, vp, i64, vp, vp, i64, i32, f32, vp, vp, f32, i32,
+                                         vp, vp, vp]
+        lib.fs_sparse_screen.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -401,3 +424,72 @@ def fs_sinkhorn_solve_noalloc(X, a, Y, b, eps: float, n_iter: int, f, g, *, stre
         float(eps), int(n_iter), _ptr(f, "f", (n,)), _ptr(g, "g", (m,)), _stream(stream, X))
     _raise(st)
     return f, g
+
+
+# ---------------------------------------------------------------------------
+# block-sparse solver for low dimension (d <= 3)
+
+def fs_sparse_solve(X, a, Y, b, eps: float, *, coarse_iters: int = 0, max_iters: int = 100,
+                    tau: float = 1e-6, target: float = 0.0, check_every: int = 0, f=None, g=None,
+                    stream=None):
+    """The block-sparse solver (see the C header for the method and its
+    readings).  f, g are outputs (and inputs when coarse_iters == 0; zeros if
+    None).  Returns (f, g, report) with report a dict of fs_sparse_report."""
+    n, d = X.shape
+    m = Y.shape[0]
+    if f is None:
+        f = _zeros_like(X, (n,))
+    if g is None:
+        g = _zeros_like(X, (m,))
+    o = fs_sparse_options()
+    o.coarse_iters, o.max_iters, o.check_every = int(coarse_iters), int(max_iters), int(check_every)
+    o.tau, o.target = float(tau), float(target)
+    rep = fs_sparse_report()
+    st = load_library().fs_sparse_solve(
+        _ptr(X, "X", (n, d)), _ptr(a, "a", (n,)), n, _ptr(Y, "Y", (m, d)), _ptr(b, "b", (m,)), m, d,
+        float(eps), ctypes.byref(o), _ptr(f, "f", (n,)), _ptr(g, "g", (m,)), ctypes.byref(rep),
+        _stream(stream, X, f))
+    _raise(st)
+    _host_sync(stream, f, g)
+    return f, g, {k: getattr(rep, k) for k, _ in fs_sparse_report._fields_}
+
+
+def _i_ptr(x, name: str, shape, dtype) -> int:
+    import torch
+    if not (_is_torch(x) and x.is_cuda and x.dtype == dtype and x.is_contiguous()
+            and tuple(x.shape) == tuple(shape)):
+        raise TypeError(f"{name} must be a contiguous CUDA {dtype} tensor of shape {tuple(shape)}")
+    return x.data_ptr()
+
+
+def fs_morton_order(X, Y, *, stream=None):
+    """Morton order of both clouds (CUDA tensors): (perm_x, perm_y) int64."""
+    import torch
+    n, d = X.shape
+    m = Y.shape[0]
+    px = torch.empty(n, dtype=torch.int64, device=X.device)
+    py = torch.empty(m, dtype=torch.int64, device=X.device)
+    st = load_library().fs_morton_order(_ptr(X, "X", (n, d)), n, _ptr(Y, "Y", (m, d)), m, d,
+                                        _i_ptr(px, "perm_x", (n,), torch.int64),
+                                        _i_ptr(py, "perm_y", (m,), torch.int64), _stream(stream, X))
+    _raise(st)
+    return px, py
+
+
+def fs_sparse_screen(X, a, Y, b, eps: float, f, g, tau: float, side: int, *, stream=None):
+    """One screening at (f, g); side 0 for an f-update, 1 for a g-update.
+    Returns (counts, lists) int32 CUDA tensors in Morton block numbering."""
+    import torch
+    n, d = X.shape
+    m = Y.shape[0]
+    nbx, nby = (n + 127) // 128, (m + 127) // 128
+    no, ni = (nbx, nby) if side == 0 else (nby, nbx)
+    counts = torch.empty(no, dtype=torch.int32, device=X.device)
+    lists = torch.empty((no, ni), dtype=torch.int32, device=X.device)
+    st = load_library().fs_sparse_screen(
+        _ptr(X, "X", (n, d)), _ptr(a, "a", (n,)), n, _ptr(Y, "Y", (m, d)), _ptr(b, "b", (m,)), m, d,
+        float(eps), _ptr(f, "f", (n,)), _ptr(g, "g", (m,)), float(tau), int(side),
+        _i_ptr(counts, "counts", (no,), torch.int32), _i_ptr(lists, "lists", (no, ni), torch.int32),
+        _stream(stream, X))
+    _raise(st)
+    return counts, lists

@@ -1,0 +1,1121 @@
+// Block-sparse solver for low-dimensional clouds (d <= 3).
+//
+// "FlashSinkhorn 2: Block-Sparse Entropic Optimal Transport" (patty.io post):
+//   - coarse resolution first: a solve between cell centroids whose
+//     potentials every point of the cell inherits;
+//   - Morton (Z-order) sorting, so that a block of consecutive points is a
+//     compact group in space and a block pair of the plan is the interaction
+//     of two such groups;
+//   - block screening by a bound on every block's plan mass, with a threshold
+//     that bounds what the skipped tiles can change in every row and column;
+//   - fused execution of the kept blocks only.
+//
+// The readings used here (the post gives no formulas):
+//   cells = blocks of 128 consecutive Morton-sorted points; a centroid is the
+//   weight-averaged point of its block, its weight the block's weight; the
+//   coarse problem is the dense log-domain Sinkhorn between centroids.
+//   With Delta = c_I - c_J, u_i = x_i - c_I, v_j = y_j - c_J the cost obeys
+//   C_ij >= |Delta|^2 + 2 Delta.u_i - 2 Delta.v_j, so block pair (I, J)
+//   carries at most 2^U_IJ of plan mass,
+//     U_IJ = log2 sum_i a_i 2^{(f_i - 2 Delta.u_i) L/eps}
+//          + log2 sum_j b_j 2^{(g_j + 2 Delta.v_j) L/eps} - |Delta|^2 L/eps.
+//   Output block O keeps input block In iff U + sigma >= log2(tau W_O / N_In)
+//   (sigma = 1/16 + 2^-16 (|max psi_O| + |max chi_In| + |Delta|^2 L/eps), a
+//   slack in favour of keeping that covers the float32 evaluation) or In is
+//   the first maximiser of U; the omitted mass of every output block is then
+//   below tau W_O.
+//
+// At d <= 3 a score is three fused multiply-adds, so the kept blocks run on
+// the FP32 pipe (packed f32x2) with one ex2 per pair, like the dense FMA path;
+// a tensor-core tile would spend most of its K = 16 on padding.
+#include "fs_host.cuh"
+
+#include <algorithm>
+#include <cmath>
+
+namespace fs {
+namespace {
+
+constexpr int kSB = 128;            // points per block
+constexpr int kMortonBits = 21;     // quantisation cells per axis: 2^21
+constexpr int kSortTile = 2048;     // keys per CTA in a radix pass
+constexpr int kSpMaxDim = 3;
+
+// ---------------------------------------------------------------------------
+// joint bounding box (order-preserving integer encoding of floats, so that
+// atomic min/max are exact and independent of the order)
+
+__device__ __forceinline__ unsigned int f2ord(float f) {
+    const unsigned int u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float ord2f(unsigned int k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+__global__ void k_box_init(unsigned int* box, int d) {
+    const int k = threadIdx.x;
+    if (k < d) {
+        box[k] = 0xffffffffu;
+        box[d + k] = 0u;
+    }
+}
+
+__global__ void k_box(const float* __restrict__ X, int64_t n, const float* __restrict__ Y, int64_t m,
+                      int d, unsigned int* __restrict__ box) {
+    unsigned int lo[kSpMaxDim] = {0xffffffffu, 0xffffffffu, 0xffffffffu};
+    unsigned int hi[kSpMaxDim] = {0u, 0u, 0u};
+    for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < n + m;
+         p += (int64_t)gridDim.x * blockDim.x) {
+        const float* src = p < n ? X + p * d : Y + (p - n) * d;
+        for (int k = 0; k < d; ++k) {
+            const unsigned int o = f2ord(src[k]);
+            lo[k] = min(lo[k], o);
+            hi[k] = max(hi[k], o);
+        }
+    }
+    for (int k = 0; k < d; ++k) {
+        unsigned int l = lo[k], h = hi[k];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            l = min(l, __shfl_xor_sync(0xffffffffu, l, o));
+            h = max(h, __shfl_xor_sync(0xffffffffu, h, o));
+        }
+        if ((threadIdx.x & 31) == 0) {
+            atomicMin(&box[k], l);
+            atomicMax(&box[d + k], h);
+        }
+    }
+}
+
+// Morton code of each point: q_k = floor((p_k - lo_k) * (2^21 / (hi_k - lo_k)))
+// with every float32 operation rounded once (no contraction), clamped to
+// [0, 2^21 - 1]; bit b of q_k goes to bit b*d + k.  vals = the point index.
+__global__ void k_morton(const float* __restrict__ P, int64_t cnt, int d,
+                         const unsigned int* __restrict__ box, uint64_t* __restrict__ keys,
+                         int* __restrict__ vals) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= cnt) return;
+    constexpr unsigned int kMaxQ = (1u << kMortonBits) - 1u;
+    uint64_t key = 0;
+    for (int k = 0; k < d; ++k) {
+        const float lo = ord2f(box[k]), hi = ord2f(box[d + k]);
+        const float span = __fsub_rn(hi, lo);
+        const float scale = span > 0.f ? __fdiv_rn((float)(1u << kMortonBits), span) : 0.f;
+        const float u = __fmul_rn(__fsub_rn(P[i * d + k], lo), scale);
+        float fq = floorf(u);
+        fq = fminf(fmaxf(fq, 0.f), (float)kMaxQ);
+        const unsigned int q = (unsigned int)fq;
+        for (int b = 0; b < kMortonBits; ++b)
+            key |= (uint64_t)((q >> b) & 1u) << (b * d + k);
+    }
+    keys[i] = key;
+    vals[i] = (int)i;
+}
+
+// ---------------------------------------------------------------------------
+// stable LSD radix sort of (key, index) pairs, 8-bit digits
+
+__global__ void k_radix_count(const uint64_t* __restrict__ keys, int64_t cnt, int shift, int ntiles,
+                              unsigned int* __restrict__ hist) {
+    __shared__ unsigned int h[256];
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0u;
+    __syncthreads();
+    const int64_t base = (int64_t)blockIdx.x * kSortTile;
+    for (int i = threadIdx.x; i < kSortTile; i += blockDim.x) {
+        const int64_t e = base + i;
+        if (e < cnt) atomicAdd(&h[(unsigned int)(keys[e] >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[(int64_t)i * ntiles + blockIdx.x] = h[i];
+}
+
+// Exclusive scan of the digit-major histogram, in place, by one block.
+__global__ void __launch_bounds__(1024) k_radix_scan(unsigned int* __restrict__ hist, int64_t total) {
+    __shared__ unsigned int part[1024];
+    const int t = threadIdx.x;
+    const int64_t per = (total + 1023) / 1024;
+    const int64_t b0 = (int64_t)t * per, b1 = min(total, b0 + per);
+    unsigned int s = 0;
+    for (int64_t i = b0; i < b1; ++i) s += hist[i];
+    part[t] = s;
+    __syncthreads();
+    for (int o = 1; o < 1024; o <<= 1) {
+        const unsigned int v = t >= o ? part[t - o] : 0u;
+        __syncthreads();
+        part[t] += v;
+        __syncthreads();
+    }
+    unsigned int run = t ? part[t - 1] : 0u;
+    for (int64_t i = b0; i < b1; ++i) {
+        const unsigned int v = hist[i];
+        hist[i] = run;
+        run += v;
+    }
+}
+
+// Each warp owns 256 consecutive keys of the tile and ranks them in order
+// (32 at a time, peers with the same digit found by match.any), after the
+// per-digit counts of the warps before it: the pass is stable.
+__global__ void __launch_bounds__(256) k_radix_scatter(const uint64_t* __restrict__ kin,
+                                                       const int* __restrict__ vin, int64_t cnt,
+                                                       int shift, int ntiles,
+                                                       const unsigned int* __restrict__ offs,
+                                                       uint64_t* __restrict__ kout,
+                                                       int* __restrict__ vout) {
+    __shared__ unsigned int wh[8][256];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < 8 * 256; i += 256) (&wh[0][0])[i] = 0u;
+    __syncthreads();
+    const int64_t base = (int64_t)blockIdx.x * kSortTile + warp * 256;
+    for (int r = 0; r < 8; ++r) {
+        const int64_t e = base + r * 32 + lane;
+        if (e < cnt) atomicAdd(&wh[warp][(unsigned int)(kin[e] >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    {
+        const int dg = threadIdx.x;   // 256 threads, one digit each
+        unsigned int run = offs[(int64_t)dg * ntiles + blockIdx.x];
+        for (int w = 0; w < 8; ++w) {
+            const unsigned int c = wh[w][dg];
+            wh[w][dg] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    const unsigned int lt = (1u << lane) - 1u;
+    for (int r = 0; r < 8; ++r) {
+        const int64_t e = base + r * 32 + lane;
+        const bool ok = e < cnt;
+        const uint64_t k = ok ? kin[e] : 0ull;
+        const unsigned int dg = ok ? ((unsigned int)(k >> shift) & 255u) : 256u;
+        const unsigned int peers = __match_any_sync(0xffffffffu, dg);
+        const unsigned int below = __popc(peers & lt);
+        unsigned int pos = 0;
+        if (ok) pos = wh[warp][dg] + below;
+        __syncwarp();
+        if (ok) {
+            kout[pos] = k;
+            vout[pos] = vin[e];
+            if (below == 0) wh[warp][dg] += __popc(peers);
+        }
+        __syncwarp();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// sorted copies, records and block statistics
+
+// Sorted raw coordinates (float4, zero-padded), sorted weights, the FMA-path
+// record (centred point padded to D, bias slot at D, stride 4), |p~|^2 and
+// log2 w.  The bias slot is filled later from a potential.
+__global__ void k_sp_gather(const float* __restrict__ P, const float* __restrict__ w,
+                            const int* __restrict__ perm, int64_t cnt, int d,
+                            const float* __restrict__ shift, float4* __restrict__ xs,
+                            float* __restrict__ ws, float4* __restrict__ rec,
+                            float* __restrict__ norm, float* __restrict__ logw2) {
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= cnt) return;
+    const int64_t p = perm[k];
+    float v[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
+    float nrm = 0.f;
+    for (int q = 0; q < d; ++q) {
+        v[q] = P[p * d + q];
+        c[q] = v[q] - shift[q];
+        nrm = fmaf(c[q], c[q], nrm);
+    }
+    const float wk = w[p];
+    xs[k] = make_float4(v[0], v[1], v[2], 0.f);
+    ws[k] = wk;
+    rec[k] = make_float4(c[0], c[1], c[2], 0.f);   // bias slot (index D = 2 or 3) set later
+    norm[k] = nrm;
+    logw2[k] = log2f(wk);
+}
+
+// One thread per block: weight and weighted sum in float64, in point order,
+// with no contraction; centroid = float(S / W), weight = float(W).
+__global__ void k_sp_block_stats(const float4* __restrict__ xs, const float* __restrict__ ws,
+                                 int64_t cnt, int d, int64_t nblk, float4* __restrict__ cen,
+                                 float* __restrict__ cen_flat, float* __restrict__ W,
+                                 float* __restrict__ lw2) {
+    const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= nblk) return;
+    double sw = 0.0, s0 = 0.0, s1 = 0.0, s2 = 0.0;
+    const int64_t e = min(cnt, (b + 1) * kSB);
+    for (int64_t k = b * kSB; k < e; ++k) {
+        const double wk = (double)ws[k];
+        const float4 x = xs[k];
+        sw = __dadd_rn(sw, wk);
+        s0 = __dadd_rn(s0, __dmul_rn(wk, (double)x.x));
+        s1 = __dadd_rn(s1, __dmul_rn(wk, (double)x.y));
+        s2 = __dadd_rn(s2, __dmul_rn(wk, (double)x.z));
+    }
+    const float c0 = (float)__ddiv_rn(s0, sw);
+    const float c1 = d > 1 ? (float)__ddiv_rn(s1, sw) : 0.f;
+    const float c2 = d > 2 ? (float)__ddiv_rn(s2, sw) : 0.f;
+    cen[b] = make_float4(c0, c1, c2, 0.f);
+    cen_flat[b * d] = c0;
+    if (d > 1) cen_flat[b * d + 1] = c1;
+    if (d > 2) cen_flat[b * d + 2] = c2;
+    W[b] = (float)sw;
+    lw2[b] = log2f((float)sw);
+}
+
+// Offsets from the block centroid (xyz of the screening record).
+__global__ void k_sp_offsets(const float4* __restrict__ xs, int64_t cnt,
+                             const float4* __restrict__ cen, float4* __restrict__ scr) {
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= cnt) return;
+    const float4 x = xs[k], c = cen[k / kSB];
+    scr[k] = make_float4(x.x - c.x, x.y - c.y, x.z - c.z, 0.f);
+}
+
+// Lift: every point takes its block's coarse potential.
+__global__ void k_sp_lift(const float* __restrict__ F, int64_t cnt, float* __restrict__ pot) {
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k < cnt) pot[k] = F[k / kSB];
+}
+
+// pot_s[k] = pot[perm[k]]
+__global__ void k_sp_gather_pot(const float* __restrict__ pot, const int* __restrict__ perm,
+                                int64_t cnt, float* __restrict__ pot_s) {
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k < cnt) pot_s[k] = pot[perm[k]];
+}
+
+// pot[perm[k]] = pot_s[k]
+__global__ void k_sp_scatter_pot(const float* __restrict__ pot_s, const int* __restrict__ perm,
+                                 int64_t cnt, float* __restrict__ pot) {
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k < cnt) pot[perm[k]] = pot_s[k];
+}
+
+__global__ void k_sp_perm64(const int* __restrict__ perm, int64_t cnt, int64_t* __restrict__ out) {
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k < cnt) out[k] = perm[k];
+}
+
+// Record bias from a sorted potential: (pot - |p~|^2) L/eps + log2 w.
+__global__ void k_sp_bias(const float* __restrict__ pot_s, const float* __restrict__ norm,
+                          const float* __restrict__ logw2, int64_t cnt, int D, float l_over_eps,
+                          float* __restrict__ rec) {
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k < cnt) rec[k * 4 + D] = (pot_s[k] - norm[k]) * l_over_eps + logw2[k];
+}
+
+// psi_k = pot_k L/eps + log2 w_k for the screening: one 128-thread block per
+// point block stores psi - max into the record's w and the max per block.
+__global__ void __launch_bounds__(kSB) k_sp_psi(const float* __restrict__ pot_s,
+                                                const float* __restrict__ logw2, int64_t cnt,
+                                                float l_over_eps, float4* __restrict__ scr,
+                                                float* __restrict__ pmax) {
+    __shared__ float red[kSB / 32];
+    const int64_t k = (int64_t)blockIdx.x * kSB + threadIdx.x;
+    const bool ok = k < cnt;
+    const float psi = ok ? fmaf(pot_s[k], l_over_eps, logw2[k]) : -INFINITY;
+    float mx = psi;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    if (ok) scr[k].w = psi - mx;
+    if (threadIdx.x == 0) pmax[blockIdx.x] = mx;
+}
+
+// ---------------------------------------------------------------------------
+// screening
+
+struct ScreenArgs {
+    const float4* so;        // output side: (u, psi - max) per sorted point
+    const float4* si;        // input side
+    const float* pmax_o;     // per-block max of psi (output side)
+    const float* pmax_i;
+    const float4* cen_o;     // block centroids
+    const float4* cen_i;
+    const float* lw2_o;      // log2 of the output blocks' weights
+    int64_t cnt_o, cnt_i;
+    int nbo, nbi;
+    float kappa;             // 2 L / eps
+    float l_over_eps;        // L / eps
+    float log2_tau;          // -inf: keep every block
+    int* lists;              // [nbo x nbi]
+    int* counts;             // [nbo]
+};
+
+__device__ __forceinline__ void lse_merge(float& M, float& S, float Mo, float So) {
+    const float Mn = fmaxf(M, Mo);
+    S = (M == -INFINITY ? 0.f : S * ex2(M - Mn)) + (Mo == -INFINITY ? 0.f : So * ex2(Mo - Mn));
+    M = Mn;
+}
+
+__device__ __forceinline__ void lse_add(float& M, float& S, float z) {
+    if (z > M) {
+        S = (M == -INFINITY ? 0.f : S * ex2(M - z)) + 1.f;
+        M = z;
+    } else {
+        S += ex2(z - M);
+    }
+}
+
+__device__ __forceinline__ float warp_lse(float M, float S) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        const float Mo = __shfl_xor_sync(0xffffffffu, M, o);
+        const float So = __shfl_xor_sync(0xffffffffu, S, o);
+        lse_merge(M, S, Mo, So);
+    }
+    return M + log2f(S);
+}
+
+// One 256-thread block per output block.  Phase 1: each warp evaluates the
+// bound U for input blocks warp, warp + 8, ... (the output block's points are
+// held in registers, four per lane) and parks it in the list row.  Phase 2:
+// the first maximiser.  Phase 3: in-order compaction of the kept indices.
+__global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
+    __shared__ float s_val[8];
+    __shared__ int s_idx[8];
+    __shared__ int s_wcnt[8];
+    const int O = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int* row = a.lists + (int64_t)O * a.nbi;
+    const int64_t o0 = (int64_t)O * kSB;
+
+    if (a.log2_tau == -INFINITY) {
+        for (int J = threadIdx.x; J < a.nbi; J += blockDim.x) row[J] = J;
+        if (threadIdx.x == 0) a.counts[O] = a.nbi;
+        return;
+    }
+
+    float4 own[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int64_t k = o0 + lane + 32 * q;
+        own[q] = k < a.cnt_o ? a.so[k] : make_float4(0.f, 0.f, 0.f, -INFINITY);
+    }
+    const float4 co = a.cen_o[O];
+    const float pmo = a.pmax_o[O];
+    for (int J = warp; J < a.nbi; J += 8) {
+        const float4 ci = a.cen_i[J];
+        const float Dx = co.x - ci.x, Dy = co.y - ci.y, Dz = co.z - ci.z;
+        float MA = -INFINITY, SA = 0.f, MB = -INFINITY, SB = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (own[q].w != -INFINITY) {
+                const float z = own[q].w - a.kappa * (Dx * own[q].x + Dy * own[q].y + Dz * own[q].z);
+                lse_add(MA, SA, z);
+            }
+            const int64_t k = (int64_t)J * kSB + lane + 32 * q;
+            if (k < a.cnt_i) {
+                const float4 v = a.si[k];
+                const float z = v.w + a.kappa * (Dx * v.x + Dy * v.y + Dz * v.z);
+                lse_add(MB, SB, z);
+            }
+        }
+        const float A = warp_lse(MA, SA);
+        const float B = warp_lse(MB, SB);
+        const float dd = (Dx * Dx + Dy * Dy + Dz * Dz) * a.l_over_eps;
+        if (lane == 0) row[J] = __float_as_int(pmo + A + a.pmax_i[J] + B - dd);
+    }
+    __syncthreads();
+
+    // first maximiser of U
+    float best = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int J = threadIdx.x; J < a.nbi; J += blockDim.x) {
+        const float u = __int_as_float(row[J]);
+        if (u > best || (u == best && J < bi)) {
+            best = u;
+            bi = J;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ob > best || (ob == best && oi < bi)) {
+            best = ob;
+            bi = oi;
+        }
+    }
+    if (lane == 0) {
+        s_val[warp] = best;
+        s_idx[warp] = bi;
+    }
+    __syncthreads();
+    best = s_val[0];
+    bi = s_idx[0];
+    for (int w = 1; w < 8; ++w)
+        if (s_val[w] > best || (s_val[w] == best && s_idx[w] < bi)) {
+            best = s_val[w];
+            bi = s_idx[w];
+        }
+    const float T = a.log2_tau + a.lw2_o[O] - log2f((float)a.nbi);
+    __syncthreads();
+
+    // compaction in index order, 256 entries per round (reads before writes)
+    int base = 0;
+    for (int c0 = 0; c0 < a.nbi; c0 += 256) {
+        const int J = c0 + threadIdx.x;
+        bool keep = false;
+        if (J < a.nbi) {
+            const float u = __int_as_float(row[J]);
+            const float4 ci = a.cen_i[J];
+            const float Dx = co.x - ci.x, Dy = co.y - ci.y, Dz = co.z - ci.z;
+            const float dd = (Dx * Dx + Dy * Dy + Dz * Dz) * a.l_over_eps;
+            const float sig = 0.0625f + 1.52587890625e-05f * (fabsf(pmo) + fabsf(a.pmax_i[J]) + dd);
+            keep = (u + sig >= T) || J == bi;
+        }
+        const unsigned int bal = __ballot_sync(0xffffffffu, keep);
+        if (lane == 0) s_wcnt[warp] = __popc(bal);
+        __syncthreads();
+        int off = base;
+        int tot = 0;
+        for (int w = 0; w < 8; ++w) {
+            if (w < warp) off += s_wcnt[w];
+            tot += s_wcnt[w];
+        }
+        if (keep) row[off + __popc(bal & ((1u << lane) - 1u))] = J;
+        base += tot;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) a.counts[O] = base;
+}
+
+// ---------------------------------------------------------------------------
+// the block-sparse half-update
+
+struct SpHalfArgs {
+    float* rows;             // packed [nr x 4] records of the updated side (bias slot written)
+    const float* cols;       // packed [nc x 4] records of the other side
+    int64_t nr, nc;
+    int nbi;
+    const int* lists;        // [nbo x nbi]
+    const int* counts;       // [nbo]
+    float kappa;             // 2 L / eps
+    float eps_ln2;
+    const float* rnorm;      // |p~|^2 [nr]
+    const float* rlogw2;     // log2 w [nr]
+    float* pot;              // potentials out [nr] (sorted order)
+    float* rowsum;           // measure mode: row marginal 2^{bias + LSE2} [nr]
+    int measure;             // 1: write rowsum only, no update
+    unsigned long long* work;   // [2] accumulated: block pairs, score pairs evaluated
+};
+
+constexpr int kSpGroups = 4;               // column groups per block
+constexpr int kSpDup = 8;                  // floats per duplicated column record
+constexpr float kSpSlack = 8.f;            // lazy rescale threshold (log2 units)
+
+// One 256-thread block per output block of 128 rows.  Thread t of group
+// h = t / 64 holds rows t % 64 and t % 64 + 64 as packed f32x2 lanes and
+// folds the kept input blocks h, h + 4, ... of the list (staged in its own
+// shared-memory slot, column values duplicated so one packed FMA scores a
+// column against both rows).  The four groups' (max, sum) are merged in
+// group order at the end, so the result does not depend on timing.
+template <int D>
+__global__ void __launch_bounds__(256) k_sp_half(SpHalfArgs a) {
+    __shared__ __align__(16) float sc[kSpGroups][kSB * kSpDup];
+    __shared__ float2 part[kSpGroups][kSB];
+    const int tid = threadIdx.x, grp = tid >> 6, gt = tid & 63;
+    const int O = blockIdx.x;
+    const int64_t r0 = (int64_t)O * kSB;
+    int64_t ra = r0 + gt, rb = r0 + gt + 64;
+    const int64_t ca = ra < a.nr ? ra : a.nr - 1, cb = rb < a.nr ? rb : a.nr - 1;
+    uint64_t q[D];
+#pragma unroll
+    for (int k = 0; k < D; ++k) q[k] = pk(a.rows[ca * 4 + k] * a.kappa, a.rows[cb * 4 + k] * a.kappa);
+    float M[2] = {-INFINITY, -INFINITY}, Mt[2] = {-INFINITY, -INFINITY};
+    uint64_t S = pk(0.f, 0.f), nm = pk(INFINITY, INFINITY);
+
+    const int cnt = a.counts[O];
+    const int* lst = a.lists + (int64_t)O * a.nbi;
+    float* my = sc[grp];
+    int64_t cols_done = 0;
+    for (int e = grp; e < cnt; e += kSpGroups) {
+        const int J = lst[e];
+        const int64_t c0 = (int64_t)J * kSB;
+        const int ncol = (int)min((int64_t)kSB, a.nc - c0);
+        cols_done += ncol;
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(64) : "memory");
+        for (int i = gt; i < ncol * (D + 1); i += 64) {
+            const int jj = i / (D + 1), k = i - jj * (D + 1);
+            const float v = a.cols[(c0 + jj) * 4 + k];
+            my[jj * kSpDup + 2 * k] = v;
+            my[jj * kSpDup + 2 * k + 1] = v;
+        }
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(64) : "memory");
+        const float4* cs = reinterpret_cast<const float4*>(my);
+        int j = 0;
+        for (; j < ncol; j += 8) {
+            const int G = min(8, ncol - j);
+            uint64_t s[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int jj = j + (u < G ? u : 0);
+                const float4 lo = cs[jj * 2], hi = cs[jj * 2 + 1];
+                uint64_t c[4] = {pk(lo.x, lo.y), pk(lo.z, lo.w), pk(hi.x, hi.y), pk(hi.z, hi.w)};
+                uint64_t acc = c[D];
+#pragma unroll
+                for (int k = 0; k < D; ++k) acc = fma2(q[k], c[k], acc);
+                s[u] = u < G ? acc : pk(-INFINITY, -INFINITY);
+            }
+            // online max with a lazy, warp-uniform rescale
+            float m0 = Mt[0], m1 = Mt[1];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                float x0, x1;
+                upk(s[u], x0, x1);
+                m0 = fmaxf(m0, x0);
+                m1 = fmaxf(m1, x1);
+            }
+            const bool grow = (m0 > Mt[0]) | (m1 > Mt[1]);
+            if (__any_sync(0xffffffffu, grow)) {
+                const float n0 = m0 > Mt[0] ? m0 : M[0];
+                const float n1 = m1 > Mt[1] ? m1 : M[1];
+                const float f0 = M[0] == -INFINITY ? 0.f : ex2(M[0] - n0);
+                const float f1 = M[1] == -INFINITY ? 0.f : ex2(M[1] - n1);
+                M[0] = n0;
+                M[1] = n1;
+                Mt[0] = n0 + kSpSlack;
+                Mt[1] = n1 + kSpSlack;
+                S = fma2(S, pk(f0, f1), pk(0.f, 0.f));
+                nm = pk(-M[0], -M[1]);
+            }
+            uint64_t ev[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                float x0, x1;
+                upk(add2(s[u], nm), x0, x1);
+                ev[u] = pk(ex2(x0), ex2(x1));
+            }
+#pragma unroll
+            for (int w = 1; w < 8; w *= 2) {
+#pragma unroll
+                for (int u = 0; u + w < 8; u += 2 * w) ev[u] = add2(ev[u], ev[u + w]);
+            }
+            S = add2(S, ev[0]);
+        }
+    }
+    float S0, S1;
+    upk(S, S0, S1);
+    part[grp][gt] = make_float2(M[0], S0);
+    part[grp][gt + 64] = make_float2(M[1], S1);
+    if (gt == 0) {
+        const int64_t rows_o = min((int64_t)kSB, a.nr - r0);
+        atomicAdd(&a.work[1], (unsigned long long)(rows_o * cols_done));
+        if (grp == 0) atomicAdd(&a.work[0], (unsigned long long)cnt);
+    }
+    __syncthreads();
+    if (tid < kSB) {
+        const int64_t row = r0 + tid;
+        if (row < a.nr) {
+            float Mf = -INFINITY, Sf = 0.f;
+            for (int h = 0; h < kSpGroups; ++h) {
+                const float2 p = part[h][tid];
+                if (p.x != -INFINITY) lse_merge(Mf, Sf, p.x, p.y);
+            }
+            const float lse2 = Mf + log2f(Sf);
+            if (a.measure) {
+                a.rowsum[row] = exp2f(a.rows[row * 4 + D] + lse2);
+            } else {
+                a.pot[row] = a.rnorm[row] - a.eps_ln2 * lse2;
+                a.rows[row * 4 + D] = a.rlogw2[row] - lse2;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+
+inline unsigned grid_for(int64_t cnt, int threads) { return (unsigned)((cnt + threads - 1) / threads); }
+
+struct SpSide {
+    size_t xs, ws, rec, norm, lw, pot, scr, pmax, cen, cenf, W, lW, perm;
+    int64_t cnt, nb;
+};
+
+struct SpBufs {
+    size_t box, keys0, keys1, vals0, vals1, hist;
+    size_t shift_part, shift;
+    SpSide X, Y;
+    size_t lists, counts, rowsum, red_part, red_out, kept;
+    // coarse stage
+    size_t cshift, cPX, cPY, cnx, cny, clx, cly, cpart, F, G;
+    int csplits_f, csplits_g;
+    int64_t ccps_f, ccps_g;
+};
+
+void layout_side(Layout& L, SpSide& s, int64_t cnt, int d) {
+    s.cnt = cnt;
+    s.nb = (cnt + kSB - 1) / kSB;
+    s.perm = L.take(sizeof(int) * cnt);
+    s.xs = L.take(sizeof(float4) * cnt);
+    s.ws = L.take(sizeof(float) * cnt);
+    s.rec = L.take(sizeof(float4) * cnt);
+    s.norm = L.take(sizeof(float) * cnt);
+    s.lw = L.take(sizeof(float) * cnt);
+    s.pot = L.take(sizeof(float) * cnt);
+    s.scr = L.take(sizeof(float4) * cnt);
+    s.pmax = L.take(sizeof(float) * s.nb);
+    s.cen = L.take(sizeof(float4) * s.nb);
+    s.cenf = L.take(sizeof(float) * s.nb * d);
+    s.W = L.take(sizeof(float) * s.nb);
+    s.lW = L.take(sizeof(float) * s.nb);
+}
+
+void layout_sparse(Layout& L, SpBufs& B, int64_t n, int64_t m, int d, int sms, bool coarse) {
+    const int64_t mx = std::max(n, m);
+    const int64_t tiles = (mx + kSortTile - 1) / kSortTile;
+    B.box = L.take(sizeof(unsigned int) * 2 * kSpMaxDim);
+    B.keys0 = L.take(sizeof(uint64_t) * mx);
+    B.keys1 = L.take(sizeof(uint64_t) * mx);
+    B.vals0 = L.take(sizeof(int) * mx);
+    B.vals1 = L.take(sizeof(int) * mx);
+    B.hist = L.take(sizeof(unsigned int) * 256 * tiles);
+    B.shift_part = L.take(sizeof(double) * (size_t)kShiftBlocks * d);
+    B.shift = L.take(sizeof(float) * d);
+    layout_side(L, B.X, n, d);
+    layout_side(L, B.Y, m, d);
+    const int64_t nx = B.X.nb, ny = B.Y.nb;
+    B.lists = L.take(sizeof(int) * (size_t)std::max(nx * ny, (int64_t)1));
+    B.counts = L.take(sizeof(int) * std::max(nx, ny));
+    B.rowsum = L.take(sizeof(float) * n);
+    B.red_part = L.take(sizeof(double) * kRedPartials);
+    B.red_out = L.take(sizeof(double) * 2);
+    B.kept = L.take(sizeof(unsigned long long) * 2);
+    if (coarse) {
+        const int D = fma_pad_dim(d);
+        const int DS = fma_stride(D);
+        const int64_t rpb = fma_rows_per_block(D);
+        const int per_sm = fma_half_blocks_per_sm(D);
+        B.csplits_f = choose_splits((nx + rpb - 1) / rpb, ny, sms, per_sm, 128, nullptr, &B.ccps_f);
+        B.csplits_g = choose_splits((ny + rpb - 1) / rpb, nx, sms, per_sm, 128, nullptr, &B.ccps_g);
+        B.cshift = L.take(sizeof(float) * d);
+        B.cPX = L.take(sizeof(float) * nx * DS);
+        B.cPY = L.take(sizeof(float) * ny * DS);
+        B.cnx = L.take(sizeof(float) * nx);
+        B.cny = L.take(sizeof(float) * ny);
+        B.clx = L.take(sizeof(float) * nx);
+        B.cly = L.take(sizeof(float) * ny);
+        B.cpart = L.take(sizeof(float2) * std::max(nx * B.csplits_f, ny * B.csplits_g));
+        B.F = L.take(sizeof(float) * nx);
+        B.G = L.take(sizeof(float) * ny);
+    }
+}
+
+// Morton order of one cloud into side.perm (the joint box is in B.box).
+fs_status sort_side(Call& c, const SpBufs& B, const float* P, int64_t cnt, int d, int* perm_out) {
+    uint64_t* k0 = c.at<uint64_t>(B.keys0);
+    uint64_t* k1 = c.at<uint64_t>(B.keys1);
+    int* v0 = c.at<int>(B.vals0);
+    int* v1 = c.at<int>(B.vals1);
+    unsigned int* hist = c.at<unsigned int>(B.hist);
+    k_morton<<<grid_for(cnt, 256), 256, 0, c.stream>>>(P, cnt, d, c.at<unsigned int>(B.box), k0, v0);
+    count_launch();
+    FS_CUDA(cudaGetLastError());
+    const int ntiles = (int)((cnt + kSortTile - 1) / kSortTile);
+    const int passes = (kMortonBits * d + 7) / 8;
+    for (int p = 0; p < passes; ++p) {
+        const int shift = 8 * p;
+        k_radix_count<<<ntiles, 256, 0, c.stream>>>(k0, cnt, shift, ntiles, hist);
+        k_radix_scan<<<1, 1024, 0, c.stream>>>(hist, (int64_t)256 * ntiles);
+        k_radix_scatter<<<ntiles, 256, 0, c.stream>>>(k0, v0, cnt, shift, ntiles, hist, k1, v1);
+        count_launch(3);
+        FS_CUDA(cudaGetLastError());
+        std::swap(k0, k1);
+        std::swap(v0, v1);
+    }
+    FS_CUDA(cudaMemcpyAsync(perm_out, v0, sizeof(int) * cnt, cudaMemcpyDeviceToDevice, c.stream));
+    return FS_OK;
+}
+
+// Sorted copies, records, block statistics and centroid offsets of one side.
+fs_status prepare_side(Call& c, const SpBufs& B, const SpSide& s, const float* P, const float* w,
+                       int d) {
+    k_sp_gather<<<grid_for(s.cnt, 256), 256, 0, c.stream>>>(
+        P, w, c.at<int>(s.perm), s.cnt, d, c.at<float>(B.shift), c.at<float4>(s.xs),
+        c.at<float>(s.ws), c.at<float4>(s.rec), c.at<float>(s.norm), c.at<float>(s.lw));
+    k_sp_block_stats<<<grid_for(s.nb, 128), 128, 0, c.stream>>>(
+        c.at<float4>(s.xs), c.at<float>(s.ws), s.cnt, d, s.nb, c.at<float4>(s.cen),
+        c.at<float>(s.cenf), c.at<float>(s.W), c.at<float>(s.lW));
+    k_sp_offsets<<<grid_for(s.cnt, 256), 256, 0, c.stream>>>(c.at<float4>(s.xs), s.cnt,
+                                                             c.at<float4>(s.cen), c.at<float4>(s.scr));
+    count_launch(3);
+    FS_CUDA(cudaGetLastError());
+    return FS_OK;
+}
+
+// Morton sort and per-side preparation shared by the entry points.
+fs_status prepare_sparse(Call& c, const SpBufs& B, const float* X, const float* a, int64_t n,
+                         const float* Y, const float* b, int64_t m, int d) {
+    unsigned int* box = c.at<unsigned int>(B.box);
+    k_box_init<<<1, 32, 0, c.stream>>>(box, d);
+    const int64_t pts = n + m;
+    unsigned blocks = grid_for(pts, 256);
+    if (blocks > 1024) blocks = 1024;
+    k_box<<<blocks, 256, 0, c.stream>>>(X, n, Y, m, d, box);
+    count_launch(2);
+    FS_CUDA(cudaGetLastError());
+    FS_TRY(sort_side(c, B, X, n, d, c.at<int>(B.X.perm)));
+    FS_TRY(sort_side(c, B, Y, m, d, c.at<int>(B.Y.perm)));
+    FS_CUDA(launch_shift(X, n, Y, m, d, c.at<double>(B.shift_part), kShiftBlocks,
+                         c.at<float>(B.shift), c.stream));
+    FS_TRY(prepare_side(c, B, B.X, X, a, d));
+    FS_TRY(prepare_side(c, B, B.Y, Y, b, d));
+    return FS_OK;
+}
+
+fs_status refresh_psi(Call& c, const SpSide& s, float l_over_eps) {
+    k_sp_psi<<<(unsigned)s.nb, kSB, 0, c.stream>>>(c.at<float>(s.pot), c.at<float>(s.lw), s.cnt,
+                                                   l_over_eps, c.at<float4>(s.scr),
+                                                   c.at<float>(s.pmax));
+    count_launch();
+    FS_CUDA(cudaGetLastError());
+    return FS_OK;
+}
+
+fs_status set_bias(Call& c, const SpSide& s, int D, float l_over_eps) {
+    k_sp_bias<<<grid_for(s.cnt, 256), 256, 0, c.stream>>>(c.at<float>(s.pot), c.at<float>(s.norm),
+                                                          c.at<float>(s.lw), s.cnt, D, l_over_eps,
+                                                          c.at<float>(s.rec));
+    count_launch();
+    FS_CUDA(cudaGetLastError());
+    return FS_OK;
+}
+
+fs_status screen(Call& c, const SpBufs& B, const SpSide& o, const SpSide& in, float eps, float tau) {
+    ScreenArgs s;
+    s.so = c.at<float4>(o.scr);
+    s.si = c.at<float4>(in.scr);
+    s.pmax_o = c.at<float>(o.pmax);
+    s.pmax_i = c.at<float>(in.pmax);
+    s.cen_o = c.at<float4>(o.cen);
+    s.cen_i = c.at<float4>(in.cen);
+    s.lw2_o = c.at<float>(o.lW);
+    s.cnt_o = o.cnt;
+    s.cnt_i = in.cnt;
+    s.nbo = (int)o.nb;
+    s.nbi = (int)in.nb;
+    s.kappa = (float)(2.0 * kLog2e / (double)eps);
+    s.l_over_eps = (float)(kLog2e / (double)eps);
+    s.log2_tau = tau > 0.f ? (float)std::log2((double)tau) : -INFINITY;
+    s.lists = c.at<int>(B.lists);
+    s.counts = c.at<int>(B.counts);
+    k_sp_screen<<<(unsigned)o.nb, 256, 0, c.stream>>>(s);
+    count_launch();
+    FS_CUDA(cudaGetLastError());
+    return FS_OK;
+}
+
+fs_status sparse_half(Call& c, const SpBufs& B, const SpSide& o, const SpSide& in, int D,
+                      float eps, bool measure) {
+    SpHalfArgs h;
+    h.rows = c.at<float>(o.rec);
+    h.cols = c.at<float>(in.rec);
+    h.nr = o.cnt;
+    h.nc = in.cnt;
+    h.nbi = (int)in.nb;
+    h.lists = c.at<int>(B.lists);
+    h.counts = c.at<int>(B.counts);
+    h.kappa = (float)(2.0 * kLog2e / (double)eps);
+    h.eps_ln2 = (float)((double)eps * kLn2);
+    h.rnorm = c.at<float>(o.norm);
+    h.rlogw2 = c.at<float>(o.lw);
+    h.pot = c.at<float>(o.pot);
+    h.rowsum = c.at<float>(B.rowsum);
+    h.measure = measure ? 1 : 0;
+    h.work = c.at<unsigned long long>(B.kept);
+    const int ts = measure ? -1 : timing_begin(c.stream);
+    if (D == 2) k_sp_half<2><<<(unsigned)o.nb, 256, 0, c.stream>>>(h);
+    else k_sp_half<3><<<(unsigned)o.nb, 256, 0, c.stream>>>(h);
+    timing_end(ts, TIME_HALF, c.stream);
+    count_launch();
+    FS_CUDA(cudaGetLastError());
+    return FS_OK;
+}
+
+// Row residual |P 1 - a|_1 of the block-sparse plan at the current
+// potentials (screens the f-side first; the lists stay valid for an f-update).
+fs_status measure_residual(Call& c, const SpBufs& B, int D, float eps, float tau, double* out) {
+    FS_TRY(screen(c, B, B.X, B.Y, eps, tau));
+    FS_TRY(sparse_half(c, B, B.X, B.Y, D, eps, true));
+    FS_CUDA(launch_l1_double(c.at<float>(B.rowsum), c.at<float>(B.X.ws), B.X.cnt,
+                             c.at<double>(B.red_part), c.at<double>(B.red_out), 0, c.stream));
+    FS_CUDA(cudaMemcpyAsync(out, c.at<double>(B.red_out), sizeof(double), cudaMemcpyDeviceToHost,
+                            c.stream));
+    FS_CUDA(cudaStreamSynchronize(c.stream));
+    return FS_OK;
+}
+
+// Coarse stage: dense Sinkhorn between the block centroids (FMA path,
+// online offsets), then the lift into the sorted potentials.
+fs_status coarse_stage(Call& c, SpBufs& B, int d, float eps, int iters) {
+    const int D = fma_pad_dim(d);
+    const int DS = fma_stride(D);
+    const int64_t nx = B.X.nb, ny = B.Y.nb;
+    const float l_over_eps = (float)(kLog2e / (double)eps);
+    const float kappa = (float)(2.0 * kLog2e / (double)eps);
+    const float eps_ln2 = (float)((double)eps * kLn2);
+    float* F = c.at<float>(B.F);
+    float* G = c.at<float>(B.G);
+    FS_CUDA(cudaMemsetAsync(G, 0, sizeof(float) * ny, c.stream));
+    const float* cx = c.at<float>(B.X.cenf);
+    const float* cy = c.at<float>(B.Y.cenf);
+    FS_CUDA(launch_shift(cx, nx, cy, ny, d, c.at<double>(B.shift_part), kShiftBlocks,
+                         c.at<float>(B.cshift), c.stream));
+    float* PX = c.at<float>(B.cPX);
+    float* PY = c.at<float>(B.cPY);
+    FS_CUDA(launch_pack_fma(cx, c.at<float>(B.X.W), nullptr, nx, d, D, c.at<float>(B.cshift),
+                            l_over_eps, PX, c.at<float>(B.cnx), c.at<float>(B.clx), c.stream));
+    FS_CUDA(launch_pack_fma(cy, c.at<float>(B.Y.W), G, ny, d, D, c.at<float>(B.cshift), l_over_eps,
+                            PY, c.at<float>(B.cny), c.at<float>(B.cly), c.stream));
+    float2* part = c.at<float2>(B.cpart);
+    HalfArgs hf{PX, PY, nx, ny, kappa, eps_ln2, c.at<float>(B.cnx), c.at<float>(B.clx), F, part,
+                B.csplits_f, B.ccps_f, 0, nullptr, nullptr};
+    HalfArgs hg{PY, PX, ny, nx, kappa, eps_ln2, c.at<float>(B.cny), c.at<float>(B.cly), G, part,
+                B.csplits_g, B.ccps_g, 0, nullptr, nullptr};
+    for (int it = 0; it < iters; ++it) {
+        FS_CUDA(launch_half_fma(D, hf, c.stream));
+        if (hf.splits > 1)
+            FS_CUDA(launch_merge_lse(part, hf.splits, nx, hf.rnorm, hf.rlogw2, eps_ln2, F, PX + D, DS,
+                                     c.stream));
+        FS_CUDA(launch_half_fma(D, hg, c.stream));
+        if (hg.splits > 1)
+            FS_CUDA(launch_merge_lse(part, hg.splits, ny, hg.rnorm, hg.rlogw2, eps_ln2, G, PY + D, DS,
+                                     c.stream));
+    }
+    k_sp_lift<<<grid_for(B.X.cnt, 256), 256, 0, c.stream>>>(F, B.X.cnt, c.at<float>(B.X.pot));
+    k_sp_lift<<<grid_for(B.Y.cnt, 256), 256, 0, c.stream>>>(G, B.Y.cnt, c.at<float>(B.Y.pot));
+    count_launch(2);
+    FS_CUDA(cudaGetLastError());
+    return FS_OK;
+}
+
+constexpr int64_t kMaxListEntries = (int64_t)1 << 30;
+
+fs_status check_sparse_args(const float* X, const float* a, int64_t n, const float* Y, const float* b,
+                            int64_t m, int32_t d, float eps) {
+    if (!X || !a || !Y || !b) return fail(FS_ERR_INVALID_ARG, "null input pointer");
+    if (n < 1 || m < 1 || n > INT32_MAX || m > INT32_MAX)
+        return fail(FS_ERR_INVALID_ARG, "n=%lld m=%lld out of range", (long long)n, (long long)m);
+    if (d < 1 || d > kSpMaxDim)
+        return fail(FS_ERR_UNSUPPORTED, "the block-sparse solver takes 1 <= d <= %d (got %d)",
+                    kSpMaxDim, d);
+    if (!(eps > 0.f) || !std::isfinite(eps))
+        return fail(FS_ERR_INVALID_ARG, "eps must be positive and finite (got %g)", (double)eps);
+    const int64_t nx = (n + kSB - 1) / kSB, ny = (m + kSB - 1) / kSB;
+    if (nx * ny > kMaxListEntries)
+        return fail(FS_ERR_UNSUPPORTED, "%lld x %lld blocks exceed the block-list limit of 2^30",
+                    (long long)nx, (long long)ny);
+    return FS_OK;
+}
+
+fs_status sparse_solve_entry(const float* X, const float* a, int64_t n, const float* Y,
+                             const float* b, int64_t m, int32_t d, float eps,
+                             const fs_sparse_options* opt, float* f, float* g,
+                             fs_sparse_report* rep, void* stream) {
+    FS_TRY(check_sparse_args(X, a, n, Y, b, m, d, eps));
+    if (!f || !g || !opt) return fail(FS_ERR_INVALID_ARG, "null f, g or options");
+    if (opt->coarse_iters < 0 || opt->max_iters < 0 || opt->check_every < 0)
+        return fail(FS_ERR_INVALID_ARG, "negative iteration count in fs_sparse_options");
+    if (!(opt->tau >= 0.f && opt->tau < 1.f))
+        return fail(FS_ERR_INVALID_ARG, "tau=%g must be in [0, 1)", (double)opt->tau);
+    if (!(opt->target >= 0.f) || !std::isfinite(opt->target))
+        return fail(FS_ERR_INVALID_ARG, "target=%g must be finite and >= 0", (double)opt->target);
+    for (int i = 0; i < 4; ++i)
+        if (opt->reserved[i]) return fail(FS_ERR_INVALID_ARG, "fs_sparse_options.reserved must be zero");
+    Call c;
+    FS_TRY(begin_call(c, stream));
+    if (c.capturing)
+        return fail(FS_ERR_UNSUPPORTED, "fs_sparse_solve reads residuals on the host: not inside a "
+                                        "graph capture");
+    Problem P;
+    P.n = n; P.m = m; P.d = d; P.eps = eps;
+    FS_TRY(classify(c, P.X, X, (size_t)n * d));
+    FS_TRY(classify(c, P.a, a, (size_t)n));
+    FS_TRY(classify(c, P.Y, Y, (size_t)m * d));
+    FS_TRY(classify(c, P.b, b, (size_t)m));
+    FS_TRY(classify(c, P.f, f, (size_t)n));
+    FS_TRY(classify(c, P.g, g, (size_t)m));
+    SpBufs B;
+    layout_sparse(c.L, B, n, m, d, c.ws->sms, opt->coarse_iters > 0);
+    FS_TRY(ensure_capacity(c));
+    for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g}) bind(c, *A);
+    for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g}) FS_TRY(upload(c, *A));
+
+    const int D = fma_pad_dim(d);
+    const float l_over_eps = (float)(kLog2e / (double)eps);
+    const int tp = timing_begin(c.stream);
+    FS_TRY(prepare_sparse(c, B, P.X.dev, P.a.dev, n, P.Y.dev, P.b.dev, m, d));
+    if (opt->coarse_iters > 0) {
+        FS_TRY(coarse_stage(c, B, d, eps, opt->coarse_iters));
+    } else {
+        k_sp_gather_pot<<<grid_for(n, 256), 256, 0, c.stream>>>(P.f.dev, c.at<int>(B.X.perm), n,
+                                                                c.at<float>(B.X.pot));
+        k_sp_gather_pot<<<grid_for(m, 256), 256, 0, c.stream>>>(P.g.dev, c.at<int>(B.Y.perm), m,
+                                                                c.at<float>(B.Y.pot));
+        count_launch(2);
+        FS_CUDA(cudaGetLastError());
+    }
+    FS_TRY(set_bias(c, B.X, D, l_over_eps));
+    FS_TRY(set_bias(c, B.Y, D, l_over_eps));
+    timing_end(tp, TIME_PREP, c.stream);
+    FS_CUDA(cudaMemsetAsync(c.at<unsigned long long>(B.kept), 0, 2 * sizeof(unsigned long long),
+                            c.stream));
+
+    const float tau = opt->tau;
+    int it = 0, passes = 0;
+    double resid = -1.0;
+    bool screened = false;   // the lists hold the f-screening of the current state
+    FS_TRY(refresh_psi(c, B.X, l_over_eps));
+    FS_TRY(refresh_psi(c, B.Y, l_over_eps));
+    while (it < opt->max_iters) {
+        if (opt->target > 0.f && opt->check_every > 0 && it > 0 && it % opt->check_every == 0) {
+            FS_TRY(measure_residual(c, B, D, eps, tau, &resid));
+            ++passes;
+            if (resid <= (double)opt->target) break;
+            screened = true;
+        }
+        if (!screened) FS_TRY(screen(c, B, B.X, B.Y, eps, tau));
+        screened = false;
+        FS_TRY(sparse_half(c, B, B.X, B.Y, D, eps, false));
+        FS_TRY(refresh_psi(c, B.X, l_over_eps));
+        FS_TRY(screen(c, B, B.Y, B.X, eps, tau));
+        FS_TRY(sparse_half(c, B, B.Y, B.X, D, eps, false));
+        FS_TRY(refresh_psi(c, B.Y, l_over_eps));
+        passes += 2;
+        ++it;
+    }
+    if (rep) {
+        FS_TRY(measure_residual(c, B, D, eps, tau, &resid));
+        ++passes;
+    }
+    unsigned long long work[2] = {0, 0};
+    FS_CUDA(cudaMemcpyAsync(work, c.at<unsigned long long>(B.kept), sizeof(work),
+                            cudaMemcpyDeviceToHost, c.stream));
+    FS_CUDA(cudaStreamSynchronize(c.stream));
+    k_sp_scatter_pot<<<grid_for(n, 256), 256, 0, c.stream>>>(c.at<float>(B.X.pot),
+                                                             c.at<int>(B.X.perm), n, P.f.dev);
+    k_sp_scatter_pot<<<grid_for(m, 256), 256, 0, c.stream>>>(c.at<float>(B.Y.pot),
+                                                             c.at<int>(B.Y.perm), m, P.g.dev);
+    count_launch(2);
+    FS_CUDA(cudaGetLastError());
+    FS_TRY(download(c, P.f));
+    FS_TRY(download(c, P.g));
+    if (rep) {
+        rep->iters = it;
+        rep->passes = passes;
+        rep->blocks_x = (int32_t)B.X.nb;
+        rep->blocks_y = (int32_t)B.Y.nb;
+        rep->residual = resid;
+        rep->kept_blocks = (double)work[0];
+        rep->kept_pairs = (double)work[1];
+    }
+    return end_call(c);
+}
+
+fs_status morton_entry(const float* X, int64_t n, const float* Y, int64_t m, int32_t d,
+                       int64_t* perm_x, int64_t* perm_y, void* stream) {
+    if (!X || !Y || !perm_x || !perm_y) return fail(FS_ERR_INVALID_ARG, "null pointer");
+    if (n < 1 || m < 1 || n > INT32_MAX || m > INT32_MAX)
+        return fail(FS_ERR_INVALID_ARG, "n=%lld m=%lld out of range", (long long)n, (long long)m);
+    if (d < 1 || d > kSpMaxDim)
+        return fail(FS_ERR_UNSUPPORTED, "Morton order takes 1 <= d <= %d (got %d)", kSpMaxDim, d);
+    if (!is_device_ptr(X) || !is_device_ptr(Y) || !is_device_ptr(perm_x) || !is_device_ptr(perm_y))
+        return fail(FS_ERR_INVALID_ARG, "fs_morton_order takes device arrays only");
+    Call c;
+    FS_TRY(begin_call(c, stream));
+    SpBufs B;
+    layout_sparse(c.L, B, n, m, d, c.ws->sms, false);
+    FS_TRY(ensure_capacity(c));
+    unsigned int* box = c.at<unsigned int>(B.box);
+    k_box_init<<<1, 32, 0, c.stream>>>(box, d);
+    unsigned blocks = grid_for(n + m, 256);
+    if (blocks > 1024) blocks = 1024;
+    k_box<<<blocks, 256, 0, c.stream>>>(X, n, Y, m, d, box);
+    count_launch(2);
+    FS_CUDA(cudaGetLastError());
+    FS_TRY(sort_side(c, B, X, n, d, c.at<int>(B.X.perm)));
+    FS_TRY(sort_side(c, B, Y, m, d, c.at<int>(B.Y.perm)));
+    k_sp_perm64<<<grid_for(n, 256), 256, 0, c.stream>>>(c.at<int>(B.X.perm), n, perm_x);
+    k_sp_perm64<<<grid_for(m, 256), 256, 0, c.stream>>>(c.at<int>(B.Y.perm), m, perm_y);
+    count_launch(2);
+    FS_CUDA(cudaGetLastError());
+    return end_call(c);
+}
+
+fs_status screen_entry(const float* X, const float* a, int64_t n, const float* Y, const float* b,
+                       int64_t m, int32_t d, float eps, const float* f, const float* g, float tau,
+                       int32_t side, int32_t* counts, int32_t* lists, void* stream) {
+    FS_TRY(check_sparse_args(X, a, n, Y, b, m, d, eps));
+    if (!f || !g || !counts || !lists) return fail(FS_ERR_INVALID_ARG, "null f, g, counts or lists");
+    if (side != 0 && side != 1) return fail(FS_ERR_INVALID_ARG, "side=%d must be 0 or 1", side);
+    if (!(tau >= 0.f && tau < 1.f)) return fail(FS_ERR_INVALID_ARG, "tau=%g must be in [0, 1)", (double)tau);
+    for (const void* p : {(const void*)X, (const void*)a, (const void*)Y, (const void*)b,
+                          (const void*)f, (const void*)g, (const void*)counts, (const void*)lists})
+        if (!is_device_ptr(p)) return fail(FS_ERR_INVALID_ARG, "fs_sparse_screen takes device arrays only");
+    Call c;
+    FS_TRY(begin_call(c, stream));
+    SpBufs B;
+    layout_sparse(c.L, B, n, m, d, c.ws->sms, false);
+    FS_TRY(ensure_capacity(c));
+    FS_TRY(prepare_sparse(c, B, X, a, n, Y, b, m, d));
+    k_sp_gather_pot<<<grid_for(n, 256), 256, 0, c.stream>>>(f, c.at<int>(B.X.perm), n,
+                                                            c.at<float>(B.X.pot));
+    k_sp_gather_pot<<<grid_for(m, 256), 256, 0, c.stream>>>(g, c.at<int>(B.Y.perm), m,
+                                                            c.at<float>(B.Y.pot));
+    count_launch(2);
+    FS_CUDA(cudaGetLastError());
+    const float l_over_eps = (float)(kLog2e / (double)eps);
+    FS_TRY(refresh_psi(c, B.X, l_over_eps));
+    FS_TRY(refresh_psi(c, B.Y, l_over_eps));
+    const SpSide& o = side == 0 ? B.X : B.Y;
+    const SpSide& in = side == 0 ? B.Y : B.X;
+    FS_TRY(screen(c, B, o, in, eps, tau));
+    FS_CUDA(cudaMemcpyAsync(counts, c.at<int>(B.counts), sizeof(int) * o.nb,
+                            cudaMemcpyDeviceToDevice, c.stream));
+    FS_CUDA(cudaMemcpyAsync(lists, c.at<int>(B.lists), sizeof(int) * o.nb * in.nb,
+                            cudaMemcpyDeviceToDevice, c.stream));
+    return end_call(c);
+}
+
+}  // namespace
+}  // namespace fs
+
+using namespace fs;
+
+extern "C" {
+
+fs_status fs_sparse_solve(const float* X, const float* a, int64_t n, const float* Y,
+                          const float* b, int64_t m, int32_t d, float eps,
+                          const fs_sparse_options* opt, float* f, float* g,
+                          fs_sparse_report* report, void* stream) {
+    try {
+        return sparse_solve_entry(X, a, n, Y, b, m, d, eps, opt, f, g, report, stream);
+    } catch (...) {
+        return fail(FS_ERR_CUDA, "unexpected host exception");
+    }
+}
+
+fs_status fs_morton_order(const float* X, int64_t n, const float* Y, int64_t m, int32_t d,
+                          int64_t* perm_x, int64_t* perm_y, void* stream) {
+    try {
+        return morton_entry(X, n, Y, m, d, perm_x, perm_y, stream);
+    } catch (...) {
+        return fail(FS_ERR_CUDA, "unexpected host exception");
+    }
+}
+
+fs_status fs_sparse_screen(const float* X, const float* a, int64_t n, const float* Y,
+                           const float* b, int64_t m, int32_t d, float eps, const float* f,
+                           const float* g, float tau, int32_t side, int32_t* counts,
+                           int32_t* lists, void* stream) {
+    try {
+        return screen_entry(X, a, n, Y, b, m, d, eps, f, g, tau, side, counts, lists, stream);
+    } catch (...) {
+        return fail(FS_ERR_CUDA, "unexpected host exception");
+    }
+}
+
+}  // extern "C"

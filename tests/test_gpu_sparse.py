@@ -1,0 +1,243 @@
+"""GPU parity of the block-sparse low-dimensional solver against the float64
+oracle (``oracle/block_sparse.py``), through the C ABI.
+
+Source: "FlashSinkhorn 2: Block-Sparse Entropic Optimal Transport" (patty.io
+post).  Bars:
+* Morton order: integer work, bit-exact.
+* Screening: a decision is compared where the oracle's float64 bound is at
+  least 0.02 log2 units from the threshold (the GPU evaluates it in float32);
+  the kept lists must be strictly increasing.
+* Potentials: within 1e-4 max(C) of the oracle after the same schedule (the
+  FP32-FMA tolerance); a borderline block kept on one side and not the other
+  changes a marginal by less than tau of its block's weight.
+* Full size: dense column marginals at the returned potentials lie in
+  [b_j, b_j + tau W_J] (the screening guarantee), checked on sampled columns.
+"""
+import numpy as np
+import pytest
+
+import oracle as orc
+import oracle.block_sparse as bsp
+from streaming_sinkhorn_solver_gb300 import binding as fs
+from streaming_sinkhorn_solver_gb300.workloads import make_inputs, random_cloud
+from tests.gpu_util import F_TOL_FMA, max_abs, np64, to_dev
+
+pytestmark = pytest.mark.gpu
+
+MARGIN = 0.02
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    assert torch.cuda.is_available()
+    fs.load_library()
+
+
+def _lattice(n, d, seed):
+    rng = np.random.default_rng(seed)
+    P = rng.integers(0, 50, size=(n, d)).astype(np.float32) * np.float32(0.37)
+    P[: n // 3] = P[n // 3: 2 * (n // 3)]          # exact duplicates: ties keep input order
+    return P
+
+
+@pytest.mark.parametrize("n,m,d", [(1, 1, 1), (5, 300, 2), (1000, 777, 3), (5000, 4100, 3),
+                                   (4099, 2048, 1), (3000, 3001, 2)])
+def test_morton_order_bit_exact(n, m, d):
+    c = random_cloud(n, m, d, seed=n + m + d)
+    t = to_dev(c)
+    px, py = fs.fs_morton_order(t["X"], t["Y"])
+    ox, oy = bsp.morton_order(c["X"], c["Y"])
+    np.testing.assert_array_equal(px.cpu().numpy(), ox)
+    np.testing.assert_array_equal(py.cpu().numpy(), oy)
+
+
+@pytest.mark.parametrize("d", [1, 2, 3])
+def test_morton_order_with_ties_bit_exact(d):
+    X, Y = _lattice(3000, d, 1), _lattice(2100, d, 2)
+    import torch
+    px, py = fs.fs_morton_order(torch.from_numpy(X).cuda(), torch.from_numpy(Y).cuda())
+    ox, oy = bsp.morton_order(X, Y)
+    np.testing.assert_array_equal(px.cpu().numpy(), ox)
+    np.testing.assert_array_equal(py.cpu().numpy(), oy)
+
+
+def _screen_case(name, n, m, d, eps, dense_iters):
+    inp = make_inputs(name, n=n, m=m, d=d)
+    C = orc.cost(inp["X"], inp["Y"])
+    f, g = orc.sinkhorn(C, inp["a"], inp["b"], eps, dense_iters)
+    return inp, f.astype(np.float32), g.astype(np.float32)
+
+
+@pytest.mark.parametrize("name,n,m,d,eps,tau,side", [
+    ("c2_n10k_d3", 3000, 2500, 3, 0.003, 1e-4, 0),
+    ("c2_n10k_d3", 3000, 2500, 3, 0.003, 1e-4, 1),
+    ("c2_n10k_d3", 4000, 4000, 2, 0.001, 1e-6, 0),
+    ("c1_n512_d2", 2600, 1900, 2, 0.02, 1e-3, 1),
+    ("c2_n10k_d3", 2000, 2200, 1, 0.0005, 1e-5, 0),
+])
+def test_screening_decisions_match_oracle(name, n, m, d, eps, tau, side):
+    inp, f32, g32 = _screen_case(name, n, m, d, eps, 6)
+    t = to_dev(dict(inp, f=f32, g=g32))
+    counts, lists = fs.fs_sparse_screen(t["X"], t["a"], t["Y"], t["b"], eps, t["f"], t["g"], tau, side)
+    counts, lists = counts.cpu().numpy(), lists.cpu().numpy()
+    px, py = bsp.morton_order(inp["X"], inp["Y"])
+    Xs, as_, Ys, bs = inp["X"][px], inp["a"][px], inp["Y"][py], inp["b"][py]
+    cx, wx = bsp.block_stats(Xs, as_)
+    cy, wy = bsp.block_stats(Ys, bs)
+    U, sig = bsp.block_bounds(Xs, as_, f32.astype(np.float64)[px], Ys, bs,
+                              g32.astype(np.float64)[py], eps, cx, cy)
+    w_out = wx if side == 0 else wy
+    if side == 1:
+        U, sig = U.T, sig.T
+    nO, nIn = U.shape
+    T = np.log2(np.float64(tau)) + np.log2(w_out.astype(np.float64)) - np.log2(nIn)
+    gap = U + sig - T[:, None]
+    near_max = U >= U.max(axis=1, keepdims=True) - MARGIN
+    gpu = np.zeros((nO, nIn), dtype=bool)
+    for o in range(nO):
+        row = lists[o, :counts[o]]
+        assert counts[o] >= 1
+        assert np.all(np.diff(row) > 0) and row.min() >= 0 and row.max() < nIn
+        gpu[o, row] = True
+    must_keep = gap >= MARGIN
+    must_skip = (gap <= -MARGIN) & ~near_max
+    assert np.all(gpu[must_keep]), "a block the bound keeps was skipped"
+    assert not np.any(gpu[must_skip]), "a block the bound skips was kept"
+    # the cases are chosen so that the screening is not trivial
+    assert 0.0 < must_skip.mean() and gpu.mean() < 0.95
+
+
+@pytest.mark.parametrize("n,m,d", [(1, 1, 1), (7, 300, 2), (130, 129, 3), (1000, 1300, 3),
+                                   (2049, 700, 1)])
+def test_without_screening_equals_dense_oracle(n, m, d):
+    inp = random_cloud(n, m, d, seed=50 + n, weights="lognormal")
+    t = to_dev(inp)
+    f, g, rep = fs.fs_sparse_solve(t["X"], t["a"], t["Y"], t["b"], 0.05, coarse_iters=0,
+                                   max_iters=15, tau=0.0)
+    C = orc.cost(inp["X"], inp["Y"])
+    fr, gr = orc.sinkhorn(C, inp["a"], inp["b"], 0.05, 15)
+    tol = F_TOL_FMA * C.max()
+    assert max_abs(np64(f), fr) <= tol
+    assert max_abs(np64(g), gr) <= tol
+    assert rep["iters"] == 15
+    assert rep["kept_pairs"] == rep["passes"] * n * m
+
+
+@pytest.mark.parametrize("name,n,d,eps,tau", [("c2_n10k_d3", 2600, 1, 0.001, 1e-6),
+                                              ("c2_n10k_d3", 3000, 2, 0.002, 1e-4),
+                                              ("c1_n512_d2", 2200, 2, 0.02, 1e-5)])
+def test_screened_solve_matches_oracle(name, n, d, eps, tau):
+    inp = make_inputs(name, n=n, m=n - 300, d=d)
+    t = to_dev(inp)
+    f, g, rep = fs.fs_sparse_solve(t["X"], t["a"], t["Y"], t["b"], eps, coarse_iters=20,
+                                   max_iters=25, tau=tau)
+    fr, gr, orep = bsp.solve(inp["X"], inp["a"], inp["Y"], inp["b"], eps, 20, 25, tau)
+    C = orc.cost(inp["X"], inp["Y"])
+    tol = F_TOL_FMA * C.max()
+    assert max_abs(np64(f), fr) <= tol
+    assert max_abs(np64(g), gr) <= tol
+    assert rep["iters"] == orep["iters"] == 25
+    # work per pass within 2 % (borderline blocks may differ)
+    per_gpu = rep["kept_pairs"] / rep["passes"]
+    per_orc = orep["kept_pairs"] / orep["halves"]
+    assert abs(per_gpu / per_orc - 1.0) < 0.02
+    assert per_gpu < 0.9 * n * (n - 300)
+    assert rep["residual"] == pytest.approx(orep["residual"], rel=1e-2, abs=1e-5)
+
+
+def test_coarse_stage_alone_matches_oracle():
+    inp = make_inputs("c2_n10k_d3", n=3000, m=2700)
+    t = to_dev(inp)
+    f, g, rep = fs.fs_sparse_solve(t["X"], t["a"], t["Y"], t["b"], 0.01, coarse_iters=40,
+                                   max_iters=0, tau=1e-6)
+    px, py = bsp.morton_order(inp["X"], inp["Y"])
+    fs_, gs_, (cx, wx, cy, wy) = bsp.coarse_potentials(inp["X"][px], inp["a"][px], inp["Y"][py],
+                                                       inp["b"][py], 0.01, 40)
+    fr = np.empty(3000)
+    gr = np.empty(2700)
+    fr[px], gr[py] = fs_, gs_
+    Cc = orc.cost(cx, cy)
+    assert max_abs(np64(f), fr) <= F_TOL_FMA * Cc.max()
+    assert max_abs(np64(g), gr) <= F_TOL_FMA * Cc.max()
+    assert rep["iters"] == 0
+
+
+def test_stopping_rule_matches_oracle():
+    inp = make_inputs("c2_n10k_d3", n=1500, m=1500, d=2)
+    t = to_dev(inp)
+    kw = dict(coarse_iters=30, max_iters=300, tau=1e-5, target=5e-3, check_every=5)
+    f, g, rep = fs.fs_sparse_solve(t["X"], t["a"], t["Y"], t["b"], 0.01, **kw)
+    fr, gr, orep = bsp.solve(inp["X"], inp["a"], inp["Y"], inp["b"], 0.01, 30, 300, 1e-5,
+                             target=5e-3, check_every=5)
+    assert rep["residual"] <= 5e-3 and orep["residual"] <= 5e-3
+    assert rep["iters"] % 5 == 0 and abs(rep["iters"] - orep["iters"]) <= 5
+    if rep["iters"] == orep["iters"]:
+        C = orc.cost(inp["X"], inp["Y"])
+        assert max_abs(np64(f), fr) <= F_TOL_FMA * C.max()
+
+
+def test_host_buffers_give_the_same_potentials():
+    inp = make_inputs("c2_n10k_d3", n=1500, m=1400)
+    t = to_dev(inp)
+    fd, gd, _ = fs.fs_sparse_solve(t["X"], t["a"], t["Y"], t["b"], 0.01, coarse_iters=10,
+                                   max_iters=10, tau=1e-6)
+    fh, gh, _ = fs.fs_sparse_solve(inp["X"], inp["a"], inp["Y"], inp["b"], 0.01, coarse_iters=10,
+                                   max_iters=10, tau=1e-6)
+    np.testing.assert_array_equal(fd.cpu().numpy(), fh)
+    np.testing.assert_array_equal(gd.cpu().numpy(), gh)
+
+
+def test_warm_start_continues_the_iteration():
+    """coarse_iters = 0 starts from the caller's (f, g): 10 + 10 iterations
+    equal 20 (up to the float32 rounding of the handed-over potentials)."""
+    inp = make_inputs("c2_n10k_d3", n=2000, m=1800)
+    t = to_dev(inp)
+    f1, g1, _ = fs.fs_sparse_solve(t["X"], t["a"], t["Y"], t["b"], 0.01, coarse_iters=10,
+                                   max_iters=20, tau=0.0)
+    f2, g2, _ = fs.fs_sparse_solve(t["X"], t["a"], t["Y"], t["b"], 0.01, coarse_iters=10,
+                                   max_iters=10, tau=0.0)
+    f3, g3, _ = fs.fs_sparse_solve(t["X"], t["a"], t["Y"], t["b"], 0.01, coarse_iters=0,
+                                   max_iters=10, tau=0.0, f=f2, g=g2)
+    C = orc.cost(inp["X"], inp["Y"])
+    assert max_abs(np64(f3), np64(f1)) <= 1e-5 * C.max()
+    assert max_abs(np64(g3), np64(g1)) <= 1e-5 * C.max()
+
+
+def test_invalid_arguments_are_rejected():
+    inp = to_dev(random_cloud(10, 10, 4, seed=1))
+    with pytest.raises(fs.FlashSinkhornError) as e:
+        fs.fs_sparse_solve(inp["X"], inp["a"], inp["Y"], inp["b"], 0.1)
+    assert e.value.status == fs.FS_ERR_UNSUPPORTED
+    inp = to_dev(random_cloud(10, 10, 2, seed=1))
+    for kw in (dict(tau=1.0), dict(tau=-1e-3), dict(max_iters=-1), dict(target=-1.0)):
+        with pytest.raises(fs.FlashSinkhornError) as e:
+            fs.fs_sparse_solve(inp["X"], inp["a"], inp["Y"], inp["b"], 0.1, **kw)
+        assert e.value.status == fs.FS_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("n,eps,iters", [(400_000, 0.002, 12)])
+def test_full_size_column_marginals_within_the_screening_bound(n, eps, iters):
+    """At the returned potentials (after a g-update) every dense column
+    marginal c_j lies in [b_j, b_j + tau W_J]: the kept blocks carry exactly
+    b_j and the skipped ones at most tau W_J.  Checked on sampled columns
+    with the oracle's dense single-row update."""
+    tau = 1e-4
+    inp = make_inputs("c2_n10k_d3", n=n, m=n)
+    t = to_dev(inp)
+    f, g, rep = fs.fs_sparse_solve(t["X"], t["a"], t["Y"], t["b"], eps, coarse_iters=30,
+                                   max_iters=iters, tau=tau)
+    assert rep["kept_pairs"] < 0.5 * rep["passes"] * n * n
+    f64, g64 = np64(f), np64(g)
+    px, py = bsp.morton_order(inp["X"], inp["Y"])
+    _, wy = bsp.block_stats(inp["Y"][py], inp["b"][py])
+    block_of = np.empty(n, dtype=np.int64)
+    block_of[py] = np.arange(n) // bsp.BLOCK
+    cols = np.linspace(0, n - 1, 48).astype(np.int64)
+    # g-update of column j from f (roles swapped): c_j / b_j = exp((g_j - g_upd_j) / eps)
+    g_upd = orc.f_update_rows(inp["Y"], inp["X"], inp["a"], eps, f64, cols)
+    c = inp["b"][cols].astype(np.float64) * np.exp((g64[cols] - g_upd) / orc.as_eps(eps))
+    b = inp["b"][cols].astype(np.float64)
+    # float32 rounding of g (|g| <= 3, eps = 0.002) moves c_j by < 1e-4 relative
+    assert np.all(c >= b * (1 - 3e-4))
+    assert np.all(c <= b * (1 + 3e-4) + tau * wy[block_of[cols]])
