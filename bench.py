@@ -460,6 +460,141 @@ def run_gb300(args, w):
         print(json.dumps(line), flush=True)
 
 
+def run_sparse(args, w):
+    """The block-sparse solver (workloads with tau > 0): one step is one
+    fs_sparse_solve call from a cold start -- Morton sort, centroid stage,
+    the workload's block-sparse iterations and the final residual pass."""
+    import torch
+    from streaming_sinkhorn_solver_gb300 import binding as fs
+
+    rank, world, local = _rank_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    fs.load_library()
+    n, m, d = w.n, w.m, w.d
+    eps, iters = w.stages[0]
+    inp = make_inputs(w.name, seed=replica_seed(w, rank))
+    t = {k: torch.from_numpy(v).to(dev) for k, v in inp.items()}
+    t["f"] = torch.empty(n, device=dev)
+    t["g"] = torch.empty(m, device=dev)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MB > L2
+    kw = dict(coarse_iters=w.coarse_iters, max_iters=iters, tau=w.tau)
+
+    def step(src):
+        return fs.fs_sparse_solve(src["X"], src["a"], src["Y"], src["b"], eps, f=src["f"],
+                                  g=src["g"], **kw)[2]
+
+    try:
+        rates = fs.fs_unit_rates()
+    except Exception as exc:  # pragma: no cover
+        rates = {"error": str(exc)}
+    for _ in range(args.warmup):
+        step(t)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    fs.fs_timing_read()
+    fs.fs_timing_enable(True)
+    l0 = fs.fs_launch_count()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    reps = []
+    for s_ in range(args.steps):
+        flush.fill_(float(s_))
+        ev[s_][0].record(stream)
+        reps.append(step(t))
+        ev[s_][1].record(stream)
+    torch.cuda.synchronize()
+    launches = fs.fs_launch_count() - l0
+    fs.fs_timing_enable(False)
+    (half_ms, _, prep_ms), (half_n, _, _) = fs.fs_timing_read()
+    clocks = sampler.stop()
+    total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), dev if world > 1 else None)
+    rep = reps[-1]
+    dense_pairs = 2 * n * m * iters                     # pairs a dense solve would evaluate
+    value = aggregate_rate(world, dense_pairs, args.steps, total_ms)
+    kept_per_step = rep["kept_pairs"]
+    # the update passes are the timed half-updates; the residual pass is one more
+    kept_update = kept_per_step * (2 * rep["iters"]) / max(rep["passes"], 1)
+    avg_half_ms = half_ms / max(half_n, 1)
+    pairs_per_launch = kept_update / max(2 * rep["iters"], 1)
+    peaks = _peaks()
+    clk = (clocks or {}).get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ex2_clk = rates.get("ex2_per_clk_sm") or EX2_PER_CLK_SM
+    fp32_clk = rates.get("fma2_lanes_per_clk_sm") or FP32_LANES_PER_CLK_SM
+    rate_src = "measured by fs_unit_rates" if "ex2_per_clk_sm" in rates else "nominal"
+    # per kept pair: d fused multiply-adds, the online max, the offset
+    # subtraction and the accumulation
+    fp32_ops = d + 3
+    ex2_peak = ex2_clk * sms * clk * 1e6
+    fp32_peak = fp32_clk / fp32_ops * sms * clk * 1e6
+    alu_peak = min(ex2_peak, fp32_peak)
+    achieved = pairs_per_launch / (avg_half_ms * 1e-3)
+    roof = {"bound": "alu", "achieved": achieved / 1e9, "peak": alu_peak / 1e9, "unit": "Gpair/s",
+            "frac": achieved / alu_peak,
+            "peak_source": f"derived: min(MUFU {ex2_clk:.1f} ex2/clk/SM, FP32 {fp32_clk:.1f} "
+                           f"lanes/clk/SM / {fp32_ops} lane-ops per kept pair) ({rate_src}) x "
+                           f"{sms} SMs x {clk:.0f} MHz (median SM clock in the timed region)",
+            "mufu_frac": achieved / ex2_peak, "fp32_frac": achieved / fp32_peak,
+            "traffic": None, "kernel": "block_sparse_half_update",
+            "avg_launch_ms": avg_half_ms, "launches": half_n,
+            "kept_pairs_per_launch": pairs_per_launch,
+            "unit_rates": dict(rates, source=rate_src)}
+    step_ms = total_ms / args.steps
+    line = {"metric": METRIC, "value": value, "unit": "score-pairs/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "value_kind": "dense-equivalent score-pairs/s: 2 n m per iteration over the step "
+                          "time; the block-sparse solver evaluates only the kept blocks "
+                          "(omitted mass per block below tau of its weight)",
+            "config": {"workload": w.name, "n": n, "m": m, "d": d, "eps": eps, "iters": iters,
+                       "coarse_iters": w.coarse_iters, "tau": w.tau,
+                       "l2": "256 MB write between timed steps; inputs also > L2"},
+            "iters_per_s": aggregate_rate(world, iters, args.steps, total_ms),
+            "kept_pairs_per_s": aggregate_rate(world, kept_per_step, args.steps, total_ms),
+            "kept_fraction": kept_per_step / (rep["passes"] * n * m),
+            "residual": rep["residual"], "blocks": [rep["blocks_x"], rep["blocks_y"]],
+            "time_split_ms_per_step": {
+                "half_updates": half_ms / args.steps, "prep_sort_coarse": prep_ms / args.steps,
+                "screening_and_residual": step_ms - (half_ms + prep_ms) / args.steps},
+            "roofline": roof, "gpu_launches": int(launches), "clocks": clocks}
+    if not args.no_e2e:
+        host = {k: torch.from_numpy(v).pin_memory() for k, v in inp.items()}
+        host["f"] = torch.empty(n).pin_memory()
+        host["g"] = torch.empty(m).pin_memory()
+        step(host)
+        e2e = []
+        for s_ in range(max(1, min(args.steps, 3))):
+            flush.fill_(float(s_))
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            step(host)
+            torch.cuda.synchronize()
+            e2e.append(1e3 * (time.perf_counter() - t0))
+        e2e_total = max_over_ranks(sum(e2e), dev if world > 1 else None)
+        line["e2e"] = {"value": aggregate_rate(world, dense_pairs, len(e2e), e2e_total),
+                       "unit": "score-pairs/s",
+                       "h2d_bytes_per_step": int(4 * (n * d + n + m * d + m + n + m)),
+                       "d2h_bytes_per_step": int(4 * (n + m)), "ms_per_step": e2e_total / len(e2e),
+                       "timer": "host wall clock around the C-ABI call, stream synchronised"}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = _cpu_baseline(w, inp, args.cpu_seconds)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -477,6 +612,8 @@ def main():
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
+    elif w.tau > 0:
+        run_sparse(args, w)
     else:
         run_gb300(args, w)
 

@@ -37,6 +37,10 @@ class Workload:
     k: int = 0          # columns of V for "pv"
     seed: int = 0
     about: str = ""
+    # block-sparse solver only: coarse centroid iterations and the screening's
+    # omitted-mass bound (0 = the dense solver)
+    coarse_iters: int = 0
+    tau: float = 0.0
 
     @property
     def n_iter(self) -> int:
@@ -78,6 +82,12 @@ WORKLOADS: Dict[str, Workload] = {
         k=64, seed=1005,
         about="X~N(0,I/d), Y~N(0,2I/d), log-normal weights, eps 1.0->0.01 geometric over "
               "10 stages x 20 iterations, final P.V with V~N(0,1) of shape m x 64"),
+    "bs_n1m_d3": Workload(
+        "bs_n1m_d3", 1_000_000, 1_000_000, 3, ((0.001, 50),), None, seed=1007,
+        coarse_iters=50, tau=1e-6,
+        about="block-sparse solver: the c2 recipe (X~U[0,1]^3, Y 4-component GMM sigma 0.1, "
+              "uniform weights) at n=m=1e6, eps=1e-3 (blur 0.03, three mean spacings), 50 "
+              "centroid iterations, then 50 block-sparse iterations with tau=1e-6"),
 }
 
 
@@ -104,7 +114,7 @@ def make_inputs(name: str, n: Optional[int] = None, m: Optional[int] = None,
         Y = 1.0 + 0.5 * rng.standard_normal((m, d))
         a = np.full(n, 1.0 / n)
         b = np.full(m, 1.0 / m)
-    elif name.startswith("c2"):
+    elif name.startswith("c2") or name.startswith("bs"):
         X = rng.uniform(0.0, 1.0, (n, d))
         means = rng.uniform(0.0, 1.0, (4, d))
         comp = rng.integers(0, 4, m)
