@@ -261,13 +261,38 @@ __global__ void k_sp_block_stats(const float4* __restrict__ xs, const float* __r
     lw2[b] = log2f((float)sw);
 }
 
-// Offsets from the block centroid (xyz of the screening record).
-__global__ void k_sp_offsets(const float4* __restrict__ xs, int64_t cnt,
-                             const float4* __restrict__ cen, float4* __restrict__ scr) {
-    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (k >= cnt) return;
-    const float4 x = xs[k], c = cen[k / kSB];
-    scr[k] = make_float4(x.x - c.x, x.y - c.y, x.z - c.z, 0.f);
+// Offsets from the block centroid (xyz of the screening record) and the
+// block's per-axis extent max_i |u_ik|; one 128-thread block per point block.
+__global__ void __launch_bounds__(kSB) k_sp_offsets(const float4* __restrict__ xs, int64_t cnt,
+                                                    const float4* __restrict__ cen,
+                                                    float4* __restrict__ scr,
+                                                    float4* __restrict__ ext) {
+    __shared__ float4 red[kSB / 32];
+    const int64_t k = (int64_t)blockIdx.x * kSB + threadIdx.x;
+    float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (k < cnt) {
+        const float4 x = xs[k], c = cen[blockIdx.x];
+        u = make_float4(x.x - c.x, x.y - c.y, x.z - c.z, 0.f);
+        scr[k] = u;
+    }
+    float e0 = fabsf(u.x), e1 = fabsf(u.y), e2 = fabsf(u.z);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        e0 = fmaxf(e0, __shfl_xor_sync(0xffffffffu, e0, o));
+        e1 = fmaxf(e1, __shfl_xor_sync(0xffffffffu, e1, o));
+        e2 = fmaxf(e2, __shfl_xor_sync(0xffffffffu, e2, o));
+    }
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = make_float4(e0, e1, e2, 0.f);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float4 e = red[0];
+        for (int w = 1; w < kSB / 32; ++w) {
+            e.x = fmaxf(e.x, red[w].x);
+            e.y = fmaxf(e.y, red[w].y);
+            e.z = fmaxf(e.z, red[w].z);
+        }
+        ext[blockIdx.x] = e;
+    }
 }
 
 // Lift: every point takes its block's coarse potential.
@@ -304,12 +329,14 @@ __global__ void k_sp_bias(const float* __restrict__ pot_s, const float* __restri
 }
 
 // psi_k = pot_k L/eps + log2 w_k for the screening: one 128-thread block per
-// point block stores psi - max into the record's w and the max per block.
+// point block stores psi - max into the record's w, the max per block, and
+// a0 = log2 sum_k 2^{psi_k - max} (the block's bound at Delta = 0).
 __global__ void __launch_bounds__(kSB) k_sp_psi(const float* __restrict__ pot_s,
                                                 const float* __restrict__ logw2, int64_t cnt,
                                                 float l_over_eps, float4* __restrict__ scr,
-                                                float* __restrict__ pmax) {
+                                                float* __restrict__ pmax, float* __restrict__ a0) {
     __shared__ float red[kSB / 32];
+    __shared__ float red2[kSB / 32];
     const int64_t k = (int64_t)blockIdx.x * kSB + threadIdx.x;
     const bool ok = k < cnt;
     const float psi = ok ? fmaf(pot_s[k], l_over_eps, logw2[k]) : -INFINITY;
@@ -319,8 +346,16 @@ __global__ void __launch_bounds__(kSB) k_sp_psi(const float* __restrict__ pot_s,
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
     __syncthreads();
     mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    float e = ok ? exp2f(psi - mx) : 0.f;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
+    if ((threadIdx.x & 31) == 0) red2[threadIdx.x >> 5] = e;
     if (ok) scr[k].w = psi - mx;
-    if (threadIdx.x == 0) pmax[blockIdx.x] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        pmax[blockIdx.x] = mx;
+        a0[blockIdx.x] = log2f(((red2[0] + red2[1]) + red2[2]) + red2[3]);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -333,6 +368,10 @@ struct ScreenArgs {
     const float* pmax_i;
     const float4* cen_o;     // block centroids
     const float4* cen_i;
+    const float4* ext_o;     // per-axis extents of the blocks around their centroids
+    const float4* ext_i;
+    const float* a0_o;       // log2 sum 2^{psi - max} per block
+    const float* a0_i;
     const float* lw2_o;      // log2 of the output blocks' weights
     int64_t cnt_o, cnt_i;
     int nbo, nbi;
@@ -368,10 +407,79 @@ __device__ __forceinline__ float warp_lse(float M, float S) {
     return M + log2f(S);
 }
 
-// One 256-thread block per output block.  Phase 1: each warp evaluates the
-// bound U for input blocks warp, warp + 8, ... (the output block's points are
-// held in registers, four per lane) and parks it in the list row.  Phase 2:
-// the first maximiser.  Phase 3: in-order compaction of the kept indices.
+// Full bound U for input block J (a warp; own[] holds the output block's
+// points, four per lane).
+__device__ __forceinline__ float bound_exact(const ScreenArgs& a, const float4 (&own)[4],
+                                             float4 co, float pmo, int J, int lane) {
+    const float4 ci = a.cen_i[J];
+    const float Dx = co.x - ci.x, Dy = co.y - ci.y, Dz = co.z - ci.z;
+    float MA = -INFINITY, SA = 0.f, MB = -INFINITY, SB = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (own[q].w != -INFINITY) {
+            const float z = own[q].w - a.kappa * (Dx * own[q].x + Dy * own[q].y + Dz * own[q].z);
+            lse_add(MA, SA, z);
+        }
+        const int64_t k = (int64_t)J * kSB + lane + 32 * q;
+        if (k < a.cnt_i) {
+            const float4 v = a.si[k];
+            const float z = v.w + a.kappa * (Dx * v.x + Dy * v.y + Dz * v.z);
+            lse_add(MB, SB, z);
+        }
+    }
+    const float A = warp_lse(MA, SA);
+    const float B = warp_lse(MB, SB);
+    const float dd = (Dx * Dx + Dy * Dy + Dz * Dz) * a.l_over_eps;
+    return pmo + A + a.pmax_i[J] + B - dd;
+}
+
+// The slack sigma of the pair and a block-level upper bound of U that needs
+// no per-point work: -kappa Delta.u_i <= kappa sum_k |Delta_k| e_k (e the
+// per-axis extent), so U <= pmax_O + a0_O + pmax_J + a0_J
+//                           + kappa sum_k |Delta_k| (e_Ok + e_Jk) - |Delta|^2 L/eps.
+__device__ __forceinline__ void bound_cheap(const ScreenArgs& a, float4 co, float4 eo, float pmo,
+                                            float a0o, int J, float& ub, float& sig) {
+    const float4 ci = a.cen_i[J], ei = a.ext_i[J];
+    const float Dx = co.x - ci.x, Dy = co.y - ci.y, Dz = co.z - ci.z;
+    const float dd = (Dx * Dx + Dy * Dy + Dz * Dz) * a.l_over_eps;
+    const float pmi = a.pmax_i[J];
+    sig = 0.0625f + 1.52587890625e-05f * (fabsf(pmo) + fabsf(pmi) + dd);
+    ub = pmo + a0o + pmi + a.a0_i[J] +
+         a.kappa * (fabsf(Dx) * (eo.x + ei.x) + fabsf(Dy) * (eo.y + ei.y) + fabsf(Dz) * (eo.z + ei.z)) -
+         dd;
+}
+
+// Margin (log2 units) by which the block-level bound must clear a test before
+// it decides without the per-point bound: covers its float32 rounding.
+constexpr float kCullMargin = 0.25f;
+
+// In-order block-wide compaction helper: returns the write offset of this
+// thread's entry (if keep) and adds the chunk's total to base.
+__device__ __forceinline__ int compact_offset(bool keep, int& base, int* s_wcnt) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const unsigned int bal = __ballot_sync(0xffffffffu, keep);
+    if (lane == 0) s_wcnt[warp] = __popc(bal);
+    __syncthreads();
+    int off = base, tot = 0;
+    for (int w = 0; w < 8; ++w) {
+        if (w < warp) off += s_wcnt[w];
+        tot += s_wcnt[w];
+    }
+    base += tot;
+    return off + __popc(bal & ((1u << lane) - 1u));
+}
+
+// One 256-thread block per output block.
+//   1. Cull: every input block whose block-level bound is below the
+//      threshold (by kCullMargin) is skipped; the others ("survivors") are
+//      compacted, in order, to the front of the list row.
+//   2. If survivors are at most half the row: warps evaluate their exact U
+//      (stored at the back of the row), the first maximiser is found among
+//      them -- unless a culled block's bound reaches it, in which case the
+//      whole row is evaluated -- and the kept survivors are compacted.
+//   3. Otherwise every input block is evaluated exactly.
+// Both routes keep exactly {J : U_J + sigma_J >= T} plus the first
+// maximiser of U, so the result does not depend on the cull.
 __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
     __shared__ float s_val[8];
     __shared__ int s_idx[8];
@@ -393,35 +501,106 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
         const int64_t k = o0 + lane + 32 * q;
         own[q] = k < a.cnt_o ? a.so[k] : make_float4(0.f, 0.f, 0.f, -INFINITY);
     }
-    const float4 co = a.cen_o[O];
-    const float pmo = a.pmax_o[O];
-    for (int J = warp; J < a.nbi; J += 8) {
-        const float4 ci = a.cen_i[J];
-        const float Dx = co.x - ci.x, Dy = co.y - ci.y, Dz = co.z - ci.z;
-        float MA = -INFINITY, SA = 0.f, MB = -INFINITY, SB = 0.f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            if (own[q].w != -INFINITY) {
-                const float z = own[q].w - a.kappa * (Dx * own[q].x + Dy * own[q].y + Dz * own[q].z);
-                lse_add(MA, SA, z);
-            }
-            const int64_t k = (int64_t)J * kSB + lane + 32 * q;
-            if (k < a.cnt_i) {
-                const float4 v = a.si[k];
-                const float z = v.w + a.kappa * (Dx * v.x + Dy * v.y + Dz * v.z);
-                lse_add(MB, SB, z);
-            }
-        }
-        const float A = warp_lse(MA, SA);
-        const float B = warp_lse(MB, SB);
-        const float dd = (Dx * Dx + Dy * Dy + Dz * Dz) * a.l_over_eps;
-        if (lane == 0) row[J] = __float_as_int(pmo + A + a.pmax_i[J] + B - dd);
-    }
-    __syncthreads();
+    const float4 co = a.cen_o[O], eo = a.ext_o[O];
+    const float pmo = a.pmax_o[O], a0o = a.a0_o[O];
+    const float T = a.log2_tau + a.lw2_o[O] - log2f((float)a.nbi);
 
-    // first maximiser of U
+    // 1. cull
+    int S = 0;
+    for (int c0 = 0; c0 < a.nbi; c0 += 256) {
+        const int J = c0 + threadIdx.x;
+        bool surv = false;
+        if (J < a.nbi) {
+            float ub, sig;
+            bound_cheap(a, co, eo, pmo, a0o, J, ub, sig);
+            surv = ub + sig + kCullMargin >= T;
+        }
+        const int pos = compact_offset(surv, S, s_wcnt);
+        if (surv) row[pos] = J;
+        __syncthreads();
+    }
+
+    bool full = 2 * S > a.nbi || S == 0;
     float best = -INFINITY;
     int bi = 0x7fffffff;
+    if (!full) {
+        // 2a. exact bounds of the survivors
+        for (int sv = warp; sv < S; sv += 8) {
+            const int J = row[sv];
+            const float u = bound_exact(a, own, co, pmo, J, lane);
+            if (lane == 0) row[a.nbi - 1 - sv] = __float_as_int(u);
+        }
+        __syncthreads();
+        // 2b. first maximiser among them
+        for (int sv = threadIdx.x; sv < S; sv += blockDim.x) {
+            const float u = __int_as_float(row[a.nbi - 1 - sv]);
+            const int J = row[sv];
+            if (u > best || (u == best && J < bi)) {
+                best = u;
+                bi = J;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ob > best || (ob == best && oi < bi)) {
+                best = ob;
+                bi = oi;
+            }
+        }
+        if (lane == 0) {
+            s_val[warp] = best;
+            s_idx[warp] = bi;
+        }
+        __syncthreads();
+        best = s_val[0];
+        bi = s_idx[0];
+        for (int w = 1; w < 8; ++w)
+            if (s_val[w] > best || (s_val[w] == best && s_idx[w] < bi)) {
+                best = s_val[w];
+                bi = s_idx[w];
+            }
+        // 2c. a culled block could still be the maximiser: evaluate everything
+        bool risk = false;
+        for (int J = threadIdx.x; J < a.nbi; J += blockDim.x) {
+            float ub, sig;
+            bound_cheap(a, co, eo, pmo, a0o, J, ub, sig);
+            if (!(ub + sig + kCullMargin >= T) && ub + kCullMargin >= best) risk = true;
+        }
+        full = __syncthreads_or(risk) != 0;
+        if (!full) {
+            // 2d. compaction of the kept survivors (reads of a round before its writes)
+            int base = 0;
+            for (int c0 = 0; c0 < S; c0 += 256) {
+                const int sv = c0 + threadIdx.x;
+                bool keep = false;
+                int J = 0;
+                if (sv < S) {
+                    J = row[sv];
+                    const float u = __int_as_float(row[a.nbi - 1 - sv]);
+                    float ub, sig;
+                    bound_cheap(a, co, eo, pmo, a0o, J, ub, sig);
+                    keep = (u + sig >= T) || J == bi;
+                }
+                const int pos = compact_offset(keep, base, s_wcnt);
+                if (keep) row[pos] = J;
+                __syncthreads();
+            }
+            if (threadIdx.x == 0) a.counts[O] = base;
+            return;
+        }
+        __syncthreads();
+    }
+
+    // 3. every input block, exactly
+    for (int J = warp; J < a.nbi; J += 8) {
+        const float u = bound_exact(a, own, co, pmo, J, lane);
+        if (lane == 0) row[J] = __float_as_int(u);
+    }
+    __syncthreads();
+    best = -INFINITY;
+    bi = 0x7fffffff;
     for (int J = threadIdx.x; J < a.nbi; J += blockDim.x) {
         const float u = __int_as_float(row[J]);
         if (u > best || (u == best && J < bi)) {
@@ -450,33 +629,19 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
             best = s_val[w];
             bi = s_idx[w];
         }
-    const float T = a.log2_tau + a.lw2_o[O] - log2f((float)a.nbi);
     __syncthreads();
-
-    // compaction in index order, 256 entries per round (reads before writes)
     int base = 0;
     for (int c0 = 0; c0 < a.nbi; c0 += 256) {
         const int J = c0 + threadIdx.x;
         bool keep = false;
         if (J < a.nbi) {
             const float u = __int_as_float(row[J]);
-            const float4 ci = a.cen_i[J];
-            const float Dx = co.x - ci.x, Dy = co.y - ci.y, Dz = co.z - ci.z;
-            const float dd = (Dx * Dx + Dy * Dy + Dz * Dz) * a.l_over_eps;
-            const float sig = 0.0625f + 1.52587890625e-05f * (fabsf(pmo) + fabsf(a.pmax_i[J]) + dd);
+            float ub, sig;
+            bound_cheap(a, co, eo, pmo, a0o, J, ub, sig);
             keep = (u + sig >= T) || J == bi;
         }
-        const unsigned int bal = __ballot_sync(0xffffffffu, keep);
-        if (lane == 0) s_wcnt[warp] = __popc(bal);
-        __syncthreads();
-        int off = base;
-        int tot = 0;
-        for (int w = 0; w < 8; ++w) {
-            if (w < warp) off += s_wcnt[w];
-            tot += s_wcnt[w];
-        }
-        if (keep) row[off + __popc(bal & ((1u << lane) - 1u))] = J;
-        base += tot;
+        const int pos = compact_offset(keep, base, s_wcnt);
+        if (keep) row[pos] = J;
         __syncthreads();
     }
     if (threadIdx.x == 0) a.counts[O] = base;
@@ -502,117 +667,144 @@ struct SpHalfArgs {
     unsigned long long* work;   // [2] accumulated: block pairs, score pairs evaluated
 };
 
-constexpr int kSpGroups = 4;               // column groups per block
-constexpr int kSpDup = 8;                  // floats per duplicated column record
+constexpr int kSpWarps = 8;                 // warps per block, each its own share of the list
 constexpr float kSpSlack = 8.f;            // lazy rescale threshold (log2 units)
 
-// One 256-thread block per output block of 128 rows.  Thread t of group
-// h = t / 64 holds rows t % 64 and t % 64 + 64 as packed f32x2 lanes and
-// folds the kept input blocks h, h + 4, ... of the list (staged in its own
-// shared-memory slot, column values duplicated so one packed FMA scores a
-// column against both rows).  The four groups' (max, sum) are merged in
-// group order at the end, so the result does not depend on timing.
+// One 256-thread block per output block of 128 rows.  Every warp holds all
+// 128 rows (lane l: rows l, l + 32, l + 64, l + 96 as two packed f32x2 row
+// pairs) and folds the kept input blocks w, w + 8, ... of the list, staged
+// by the warp itself into its own shared-memory slot with every value
+// duplicated, so one packed FMA scores a column against two rows.  The
+// eight warps' (max, sum) are merged in warp order at the end, so the result
+// does not depend on timing.
 template <int D>
 __global__ void __launch_bounds__(256) k_sp_half(SpHalfArgs a) {
-    __shared__ __align__(16) float sc[kSpGroups][kSB * kSpDup];
-    __shared__ float2 part[kSpGroups][kSB];
-    const int tid = threadIdx.x, grp = tid >> 6, gt = tid & 63;
+    __shared__ float4 sc[kSpWarps][2 * kSB];
+    __shared__ float2 part[kSpWarps][kSB];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int O = blockIdx.x;
     const int64_t r0 = (int64_t)O * kSB;
-    int64_t ra = r0 + gt, rb = r0 + gt + 64;
-    const int64_t ca = ra < a.nr ? ra : a.nr - 1, cb = rb < a.nr ? rb : a.nr - 1;
-    uint64_t q[D];
+    uint64_t q[2][D];
 #pragma unroll
-    for (int k = 0; k < D; ++k) q[k] = pk(a.rows[ca * 4 + k] * a.kappa, a.rows[cb * 4 + k] * a.kappa);
-    float M[2] = {-INFINITY, -INFINITY}, Mt[2] = {-INFINITY, -INFINITY};
-    uint64_t S = pk(0.f, 0.f), nm = pk(INFINITY, INFINITY);
+    for (int p = 0; p < 2; ++p) {
+        const int64_t ra = min(r0 + lane + 64 * p, a.nr - 1), rb = min(r0 + lane + 64 * p + 32, a.nr - 1);
+#pragma unroll
+        for (int k = 0; k < D; ++k) q[p][k] = pk(a.rows[ra * 4 + k] * a.kappa, a.rows[rb * 4 + k] * a.kappa);
+    }
+    float M[4], Mt[4];
+    uint64_t S[2], nm[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) M[i] = Mt[i] = -INFINITY;
+    S[0] = S[1] = pk(0.f, 0.f);
+    nm[0] = nm[1] = pk(INFINITY, INFINITY);
 
     const int cnt = a.counts[O];
     const int* lst = a.lists + (int64_t)O * a.nbi;
-    float* my = sc[grp];
+    const float4* cols4 = reinterpret_cast<const float4*>(a.cols);
+    float4* my = sc[warp];
     int64_t cols_done = 0;
-    for (int e = grp; e < cnt; e += kSpGroups) {
+    for (int e = warp; e < cnt; e += kSpWarps) {
         const int J = lst[e];
         const int64_t c0 = (int64_t)J * kSB;
         const int ncol = (int)min((int64_t)kSB, a.nc - c0);
         cols_done += ncol;
-        asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(64) : "memory");
-        for (int i = gt; i < ncol * (D + 1); i += 64) {
-            const int jj = i / (D + 1), k = i - jj * (D + 1);
-            const float v = a.cols[(c0 + jj) * 4 + k];
-            my[jj * kSpDup + 2 * k] = v;
-            my[jj * kSpDup + 2 * k + 1] = v;
+        __syncwarp();
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int j = lane + 32 * t;
+            if (j < ncol) {
+                const float4 v = cols4[c0 + j];
+                my[2 * j] = make_float4(v.x, v.x, v.y, v.y);
+                my[2 * j + 1] = make_float4(v.z, v.z, v.w, v.w);
+            }
         }
-        asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(64) : "memory");
-        const float4* cs = reinterpret_cast<const float4*>(my);
-        int j = 0;
-        for (; j < ncol; j += 8) {
+        __syncwarp();
+        for (int j = 0; j < ncol; j += 8) {
             const int G = min(8, ncol - j);
-            uint64_t s[8];
+            uint64_t s[2][8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int jj = j + (u < G ? u : 0);
-                const float4 lo = cs[jj * 2], hi = cs[jj * 2 + 1];
-                uint64_t c[4] = {pk(lo.x, lo.y), pk(lo.z, lo.w), pk(hi.x, hi.y), pk(hi.z, hi.w)};
-                uint64_t acc = c[D];
+                const float4 lo = my[2 * jj], hi = my[2 * jj + 1];
+                const uint64_t c[4] = {pk(lo.x, lo.y), pk(lo.z, lo.w), pk(hi.x, hi.y), pk(hi.z, hi.w)};
 #pragma unroll
-                for (int k = 0; k < D; ++k) acc = fma2(q[k], c[k], acc);
-                s[u] = u < G ? acc : pk(-INFINITY, -INFINITY);
+                for (int p = 0; p < 2; ++p) {
+                    uint64_t acc = c[D];
+#pragma unroll
+                    for (int k = 0; k < D; ++k) acc = fma2(q[p][k], c[k], acc);
+                    s[p][u] = u < G ? acc : pk(-INFINITY, -INFINITY);
+                }
             }
             // online max with a lazy, warp-uniform rescale
-            float m0 = Mt[0], m1 = Mt[1];
+            float m[4] = {Mt[0], Mt[1], Mt[2], Mt[3]};
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                float x0, x1;
-                upk(s[u], x0, x1);
-                m0 = fmaxf(m0, x0);
-                m1 = fmaxf(m1, x1);
+            for (int p = 0; p < 2; ++p) {
+#pragma unroll
+                for (int u = 0; u < 8; u += 2) {
+                    float x0, x1, y0, y1;
+                    upk(s[p][u], x0, x1);
+                    upk(s[p][u + 1], y0, y1);
+                    m[2 * p] = max3(m[2 * p], x0, y0);
+                    m[2 * p + 1] = max3(m[2 * p + 1], x1, y1);
+                }
             }
-            const bool grow = (m0 > Mt[0]) | (m1 > Mt[1]);
+            bool grow = false;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) grow |= m[i] > Mt[i];
             if (__any_sync(0xffffffffu, grow)) {
-                const float n0 = m0 > Mt[0] ? m0 : M[0];
-                const float n1 = m1 > Mt[1] ? m1 : M[1];
-                const float f0 = M[0] == -INFINITY ? 0.f : ex2(M[0] - n0);
-                const float f1 = M[1] == -INFINITY ? 0.f : ex2(M[1] - n1);
-                M[0] = n0;
-                M[1] = n1;
-                Mt[0] = n0 + kSpSlack;
-                Mt[1] = n1 + kSpSlack;
-                S = fma2(S, pk(f0, f1), pk(0.f, 0.f));
-                nm = pk(-M[0], -M[1]);
-            }
-            uint64_t ev[8];
+                float f[4];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                float x0, x1;
-                upk(add2(s[u], nm), x0, x1);
-                ev[u] = pk(ex2(x0), ex2(x1));
+                for (int i = 0; i < 4; ++i) {
+                    const float nM = m[i] > Mt[i] ? m[i] : M[i];
+                    f[i] = M[i] == -INFINITY ? 0.f : ex2(M[i] - nM);
+                    M[i] = nM;
+                    Mt[i] = nM + kSpSlack;
+                }
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    S[p] = fma2(S[p], pk(f[2 * p], f[2 * p + 1]), pk(0.f, 0.f));
+                    nm[p] = pk(-M[2 * p], -M[2 * p + 1]);
+                }
             }
 #pragma unroll
-            for (int w = 1; w < 8; w *= 2) {
+            for (int p = 0; p < 2; ++p) {
+                uint64_t ev[8];
 #pragma unroll
-                for (int u = 0; u + w < 8; u += 2 * w) ev[u] = add2(ev[u], ev[u + w]);
+                for (int u = 0; u < 8; ++u) {
+                    float x0, x1;
+                    upk(add2(s[p][u], nm[p]), x0, x1);
+                    ev[u] = pk(ex2(x0), ex2(x1));
+                }
+#pragma unroll
+                for (int w = 1; w < 8; w *= 2) {
+#pragma unroll
+                    for (int u = 0; u + w < 8; u += 2 * w) ev[u] = add2(ev[u], ev[u + w]);
+                }
+                S[p] = add2(S[p], ev[0]);
             }
-            S = add2(S, ev[0]);
         }
     }
-    float S0, S1;
-    upk(S, S0, S1);
-    part[grp][gt] = make_float2(M[0], S0);
-    part[grp][gt + 64] = make_float2(M[1], S1);
-    if (gt == 0) {
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        float s0, s1;
+        upk(S[p], s0, s1);
+        part[warp][lane + 64 * p] = make_float2(M[2 * p], s0);
+        part[warp][lane + 64 * p + 32] = make_float2(M[2 * p + 1], s1);
+    }
+    if (lane == 0) {
         const int64_t rows_o = min((int64_t)kSB, a.nr - r0);
-        atomicAdd(&a.work[1], (unsigned long long)(rows_o * cols_done));
-        if (grp == 0) atomicAdd(&a.work[0], (unsigned long long)cnt);
+        if (cols_done) atomicAdd(&a.work[1], (unsigned long long)(rows_o * cols_done));
+        if (warp == 0) atomicAdd(&a.work[0], (unsigned long long)cnt);
     }
     __syncthreads();
-    if (tid < kSB) {
-        const int64_t row = r0 + tid;
+    if (threadIdx.x < kSB) {
+        const int t = threadIdx.x;
+        const int64_t row = r0 + t;
         if (row < a.nr) {
             float Mf = -INFINITY, Sf = 0.f;
-            for (int h = 0; h < kSpGroups; ++h) {
-                const float2 p = part[h][tid];
-                if (p.x != -INFINITY) lse_merge(Mf, Sf, p.x, p.y);
+            for (int w = 0; w < kSpWarps; ++w) {
+                const float2 pp = part[w][t];
+                if (pp.x != -INFINITY) lse_merge(Mf, Sf, pp.x, pp.y);
             }
             const float lse2 = Mf + log2f(Sf);
             if (a.measure) {
@@ -631,7 +823,7 @@ __global__ void __launch_bounds__(256) k_sp_half(SpHalfArgs a) {
 inline unsigned grid_for(int64_t cnt, int threads) { return (unsigned)((cnt + threads - 1) / threads); }
 
 struct SpSide {
-    size_t xs, ws, rec, norm, lw, pot, scr, pmax, cen, cenf, W, lW, perm;
+    size_t xs, ws, rec, norm, lw, pot, scr, pmax, a0, ext, cen, cenf, W, lW, perm;
     int64_t cnt, nb;
 };
 
@@ -658,6 +850,8 @@ void layout_side(Layout& L, SpSide& s, int64_t cnt, int d) {
     s.pot = L.take(sizeof(float) * cnt);
     s.scr = L.take(sizeof(float4) * cnt);
     s.pmax = L.take(sizeof(float) * s.nb);
+    s.a0 = L.take(sizeof(float) * s.nb);
+    s.ext = L.take(sizeof(float4) * s.nb);
     s.cen = L.take(sizeof(float4) * s.nb);
     s.cenf = L.take(sizeof(float) * s.nb * d);
     s.W = L.take(sizeof(float) * s.nb);
@@ -739,8 +933,9 @@ fs_status prepare_side(Call& c, const SpBufs& B, const SpSide& s, const float* P
     k_sp_block_stats<<<grid_for(s.nb, 128), 128, 0, c.stream>>>(
         c.at<float4>(s.xs), c.at<float>(s.ws), s.cnt, d, s.nb, c.at<float4>(s.cen),
         c.at<float>(s.cenf), c.at<float>(s.W), c.at<float>(s.lW));
-    k_sp_offsets<<<grid_for(s.cnt, 256), 256, 0, c.stream>>>(c.at<float4>(s.xs), s.cnt,
-                                                             c.at<float4>(s.cen), c.at<float4>(s.scr));
+    k_sp_offsets<<<(unsigned)s.nb, kSB, 0, c.stream>>>(c.at<float4>(s.xs), s.cnt,
+                                                       c.at<float4>(s.cen), c.at<float4>(s.scr),
+                                                       c.at<float4>(s.ext));
     count_launch(3);
     FS_CUDA(cudaGetLastError());
     return FS_OK;
@@ -769,7 +964,7 @@ fs_status prepare_sparse(Call& c, const SpBufs& B, const float* X, const float* 
 fs_status refresh_psi(Call& c, const SpSide& s, float l_over_eps) {
     k_sp_psi<<<(unsigned)s.nb, kSB, 0, c.stream>>>(c.at<float>(s.pot), c.at<float>(s.lw), s.cnt,
                                                    l_over_eps, c.at<float4>(s.scr),
-                                                   c.at<float>(s.pmax));
+                                                   c.at<float>(s.pmax), c.at<float>(s.a0));
     count_launch();
     FS_CUDA(cudaGetLastError());
     return FS_OK;
@@ -792,6 +987,10 @@ fs_status screen(Call& c, const SpBufs& B, const SpSide& o, const SpSide& in, fl
     s.pmax_i = c.at<float>(in.pmax);
     s.cen_o = c.at<float4>(o.cen);
     s.cen_i = c.at<float4>(in.cen);
+    s.ext_o = c.at<float4>(o.ext);
+    s.ext_i = c.at<float4>(in.ext);
+    s.a0_o = c.at<float>(o.a0);
+    s.a0_i = c.at<float>(in.a0);
     s.lw2_o = c.at<float>(o.lW);
     s.cnt_o = o.cnt;
     s.cnt_i = in.cnt;
