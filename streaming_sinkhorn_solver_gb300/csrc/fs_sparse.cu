@@ -388,49 +388,36 @@ __device__ __forceinline__ void lse_merge(float& M, float& S, float Mo, float So
     M = Mn;
 }
 
-__device__ __forceinline__ void lse_add(float& M, float& S, float z) {
-    if (z > M) {
-        S = (M == -INFINITY ? 0.f : S * ex2(M - z)) + 1.f;
-        M = z;
-    } else {
-        S += ex2(z - M);
-    }
-}
-
-__device__ __forceinline__ float warp_lse(float M, float S) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-        const float Mo = __shfl_xor_sync(0xffffffffu, M, o);
-        const float So = __shfl_xor_sync(0xffffffffu, S, o);
-        lse_merge(M, S, Mo, So);
-    }
-    return M + log2f(S);
-}
 
 // Full bound U for input block J (a warp; own[] holds the output block's
 // points, four per lane).
+// log2 sum over the warp of 2^z (four values per lane, -inf for none):
+// the warp max first, then one sum.
+__device__ __forceinline__ float warp_lse4(const float (&z)[4]) {
+    float m = max3(z[0], z[1], fmaxf(z[2], z[3]));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float s = (ex2(z[0] - m) + ex2(z[1] - m)) + (ex2(z[2] - m) + ex2(z[3] - m));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    return m + log2f(s);
+}
+
 __device__ __forceinline__ float bound_exact(const ScreenArgs& a, const float4 (&own)[4],
                                              float4 co, float pmo, int J, int lane) {
     const float4 ci = a.cen_i[J];
     const float Dx = co.x - ci.x, Dy = co.y - ci.y, Dz = co.z - ci.z;
-    float MA = -INFINITY, SA = 0.f, MB = -INFINITY, SB = 0.f;
+    float za[4], zb[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        if (own[q].w != -INFINITY) {
-            const float z = own[q].w - a.kappa * (Dx * own[q].x + Dy * own[q].y + Dz * own[q].z);
-            lse_add(MA, SA, z);
-        }
+        za[q] = own[q].w - a.kappa * (Dx * own[q].x + Dy * own[q].y + Dz * own[q].z);
         const int64_t k = (int64_t)J * kSB + lane + 32 * q;
-        if (k < a.cnt_i) {
-            const float4 v = a.si[k];
-            const float z = v.w + a.kappa * (Dx * v.x + Dy * v.y + Dz * v.z);
-            lse_add(MB, SB, z);
-        }
+        float4 v = make_float4(0.f, 0.f, 0.f, -INFINITY);
+        if (k < a.cnt_i) v = a.si[k];
+        zb[q] = v.w + a.kappa * (Dx * v.x + Dy * v.y + Dz * v.z);
     }
-    const float A = warp_lse(MA, SA);
-    const float B = warp_lse(MB, SB);
     const float dd = (Dx * Dx + Dy * Dy + Dz * Dz) * a.l_over_eps;
-    return pmo + A + a.pmax_i[J] + B - dd;
+    return pmo + warp_lse4(za) + a.pmax_i[J] + warp_lse4(zb) - dd;
 }
 
 // The slack sigma of the pair and a block-level upper bound of U that needs
@@ -657,6 +644,7 @@ struct SpHalfArgs {
     int nbi;
     const int* lists;        // [nbo x nbi]
     const int* counts;       // [nbo]
+    const int* order;        // [nbo] output block of each CTA
     float kappa;             // 2 L / eps
     float eps_ln2;
     const float* rnorm;      // |p~|^2 [nr]
@@ -682,7 +670,7 @@ __global__ void __launch_bounds__(256) k_sp_half(SpHalfArgs a) {
     __shared__ float4 sc[kSpWarps][2 * kSB];
     __shared__ float2 part[kSpWarps][kSB];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int O = blockIdx.x;
+    const int O = a.order[blockIdx.x];
     const int64_t r0 = (int64_t)O * kSB;
     uint64_t q[2][D];
 #pragma unroll
@@ -817,6 +805,31 @@ __global__ void __launch_bounds__(256) k_sp_half(SpHalfArgs a) {
     }
 }
 
+// Output blocks in decreasing order of kept-list length (buckets of
+// 2^shift entries), so the longest blocks start first and the last wave is
+// made of short ones.  One block; the order within a bucket is arbitrary
+// (each output block's result does not depend on when it runs).
+__global__ void __launch_bounds__(1024) k_sp_order(const int* __restrict__ counts, int nbo, int shift,
+                                                   int* __restrict__ order) {
+    __shared__ int h[1024];
+    for (int i = threadIdx.x; i < 1024; i += blockDim.x) h[i] = 0;
+    __syncthreads();
+    for (int o = threadIdx.x; o < nbo; o += blockDim.x)
+        atomicAdd(&h[1023 - min(counts[o] >> shift, 1023)], 1);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int i = 0; i < 1024; ++i) {
+            const int v = h[i];
+            h[i] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    for (int o = threadIdx.x; o < nbo; o += blockDim.x)
+        order[atomicAdd(&h[1023 - min(counts[o] >> shift, 1023)], 1)] = o;
+}
+
 // ---------------------------------------------------------------------------
 // host side
 
@@ -831,7 +844,7 @@ struct SpBufs {
     size_t box, keys0, keys1, vals0, vals1, hist;
     size_t shift_part, shift;
     SpSide X, Y;
-    size_t lists, counts, rowsum, red_part, red_out, kept;
+    size_t lists, counts, order, rowsum, red_part, red_out, kept;
     // coarse stage
     size_t cshift, cPX, cPY, cnx, cny, clx, cly, cpart, F, G;
     int csplits_f, csplits_g;
@@ -874,6 +887,7 @@ void layout_sparse(Layout& L, SpBufs& B, int64_t n, int64_t m, int d, int sms, b
     const int64_t nx = B.X.nb, ny = B.Y.nb;
     B.lists = L.take(sizeof(int) * (size_t)std::max(nx * ny, (int64_t)1));
     B.counts = L.take(sizeof(int) * std::max(nx, ny));
+    B.order = L.take(sizeof(int) * std::max(nx, ny));
     B.rowsum = L.take(sizeof(float) * n);
     B.red_part = L.take(sizeof(double) * kRedPartials);
     B.red_out = L.take(sizeof(double) * 2);
@@ -1025,6 +1039,11 @@ fs_status sparse_half(Call& c, const SpBufs& B, const SpSide& o, const SpSide& i
     h.rowsum = c.at<float>(B.rowsum);
     h.measure = measure ? 1 : 0;
     h.work = c.at<unsigned long long>(B.kept);
+    h.order = c.at<int>(B.order);
+    int shift = 0;
+    while ((in.nb >> shift) >= 1024) ++shift;
+    k_sp_order<<<1, 1024, 0, c.stream>>>(h.counts, (int)o.nb, shift, c.at<int>(B.order));
+    count_launch();
     const int ts = measure ? -1 : timing_begin(c.stream);
     if (D == 2) k_sp_half<2><<<(unsigned)o.nb, 256, 0, c.stream>>>(h);
     else k_sp_half<3><<<(unsigned)o.nb, 256, 0, c.stream>>>(h);
