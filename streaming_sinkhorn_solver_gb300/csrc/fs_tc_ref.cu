@@ -9,10 +9,9 @@
 //
 // Once the potentials have settled, a row's previous LSE is a fixed exponent
 // offset M for the whole pass: no running max, so every score costs one
-// multiply-add, one exp2 and one add.  The accumulator of each score tile is
-// pre-loaded with -M / kappa' (tcgen05.st), the MMAs accumulate onto it, and
-// the epilogue forms 2^{acc kappa' + bias} directly.  The row's sum is
-// range-checked at the end; a row outside the range goes to the fixup list.
+// multiply-add, one subtraction, one exp2 and one add (packed two by two).
+// The row's sum is range-checked at the end; a row outside the range goes to
+// the fixup list.
 //
 // One CTA owns a 128-row tile of Q (resident in shared memory) and a range
 // of 128-column tiles of K; tile t lives in TMEM buffer t mod 4.
@@ -32,7 +31,7 @@
 // sums once, at the end.
 // The K slots are tied to the TMEM buffers so that the MMA thread, whose
 // serial work per tile bounds the kernel once the epilogue is cheap, waits on
-// a single barrier per tile: tempty[b] completes when the group has re-filled
+// a single barrier per tile: tempty[b] completes when the group has released
 // buffer b (four arrivals), the producer has armed it (one arrival with the
 // K tile's byte count) and the K tile has landed.  The producer re-uses slot
 // b once the MMAs of the tile before have completed (tfull[b]), so the MMA
@@ -58,30 +57,19 @@ __host__ __device__ constexpr int ref_smem_bytes(int nch) {
 
 // One 16-lane x 32-column slice (tmem_ld16x32 layout): for each repetition
 // i, the column pair's bias bp[i] serves both rows; lo/hi accumulate the rows
-// t/4 and t/4 + 8 of the block: acc += 2^{v kappa' + bias} (the accumulator
-// already holds -M / kappa').
+// t/4 and t/4 + 8 of the block: acc += 2^{v kappa' + bias - M} (nlo, nhi hold
+// the rows' -M, packed twice).
 __device__ __forceinline__ void ref_slice(const float (&v)[16], const uint64_t (&bp)[4],
-                                          uint64_t ks2, uint64_t& lo, uint64_t& hi) {
+                                          uint64_t ks2, uint64_t nlo, uint64_t nhi, uint64_t& lo,
+                                          uint64_t& hi) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         float x0, x1, x2, x3;
-        upk(fma2(pk(v[4 * i], v[4 * i + 1]), ks2, bp[i]), x0, x1);
-        upk(fma2(pk(v[4 * i + 2], v[4 * i + 3]), ks2, bp[i]), x2, x3);
+        upk(add2(fma2(pk(v[4 * i], v[4 * i + 1]), ks2, bp[i]), nlo), x0, x1);
+        upk(add2(fma2(pk(v[4 * i + 2], v[4 * i + 3]), ks2, bp[i]), nhi), x2, x3);
         lo = add2(lo, pk(ex2(x0), ex2(x1)));
         hi = add2(hi, pk(ex2(x2), ex2(x3)));
     }
-}
-
-// the row offset into 128 accumulator columns, 8 at a time from 8 opaque
-// registers (so that no block of copies of `fill` stays live over a loop)
-__device__ __forceinline__ void fill_buffer(uint32_t buf, float fill) {
-    float f8[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) f8[i] = fill;
-    tmem_reg_fence(f8);
-#pragma unroll
-    for (int q = 0; q < BN / 8; ++q) tmem_st8(buf + q * 8, f8);
-    tmem_wait_st();
 }
 
 template <int NCH>
@@ -102,7 +90,7 @@ __global__ void __launch_bounds__(kRefThreads, 1) k_half_ref(TcHalfArgs a) {
     float* sMerge = reinterpret_cast<float*>(sBias + kRefBiasSlots * kBiasBytes);
     uint64_t* qfull = reinterpret_cast<uint64_t*>(sMerge + BM * (kRefGroups - 1));
     uint64_t* tfull = qfull + 1;                 // MMAs of the buffer's tile complete
-    uint64_t* tempty = tfull + kTmemBufs;        // buffer re-filled and its K tile landed
+    uint64_t* tempty = tfull + kTmemBufs;        // buffer released and its K tile landed
     uint64_t* bfull = tempty + kTmemBufs;
     uint64_t* bempty = bfull + kRefBiasSlots;
     uint64_t* drain = bempty + kRefBiasSlots;
@@ -194,7 +182,7 @@ __global__ void __launch_bounds__(kRefThreads, 1) k_half_ref(TcHalfArgs a) {
                     for (int kk = 0; kk < BK / 16; ++kk)
                         mma_f16(d_tmem, qd[c] + (uint64_t)(2 * kk),
                                 kd + (uint64_t)((c * CHUNK_BYTES) >> 4) + (uint64_t)(2 * kk), idesc,
-                                1u);
+                                (c | kk) != 0);
                 mma_commit(&tfull[b]);
             }
             // every MMA issued has completed once `drain` fires
@@ -207,11 +195,15 @@ __global__ void __launch_bounds__(kRefThreads, 1) k_half_ref(TcHalfArgs a) {
         const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
         const float ks = *a.kscale;
         const uint64_t ks2 = pk(ks, ks);
-        // the fill: this thread's own lane, 32*quarter + lane
-        const int64_t rf = min(rt * BM + quarter * 32 + lane, a.nr - 1);
-        const float fill = -(a.rlogw2[rf] - a.rbias[rf]) / ks;
+        // -M of this thread's four rows, 32*quarter + lane/4 + 8k
+        uint64_t nM[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t rk = min(rt * BM + quarter * 32 + (lane >> 2) + 8 * k, a.nr - 1);
+            const float m = a.rlogw2[rk] - a.rbias[rk];
+            nM[k] = pk(-m, -m);
+        }
         const uint32_t buf = tmem + (uint32_t)(grp * BN) + ((uint32_t)(quarter * 32) << 16);
-        fill_buffer(buf, fill);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[grp]);
@@ -247,8 +239,7 @@ __global__ void __launch_bounds__(kRefThreads, 1) k_half_ref(TcHalfArgs a) {
                     tmem_ld16x32(buf + ((uint32_t)(16 * (s1 & 1)) << 16) + (uint32_t)(32 * (s1 >> 1)),
                                  nxt);
                 } else {
-                    // every score of the tile is in registers: re-fill, release
-                    fill_buffer(buf, fill);
+                    // every score of the tile is in registers: release the buffer
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&tempty[grp]);
@@ -257,7 +248,7 @@ __global__ void __launch_bounds__(kRefThreads, 1) k_half_ref(TcHalfArgs a) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) bp[i] = sb[(32 * cq + 8 * i) / 2];
                 }
-                ref_slice(cur, bp, ks2, acc[2 * h], acc[2 * h + 1]);
+                ref_slice(cur, bp, ks2, nM[2 * h], nM[2 * h + 1], acc[2 * h], acc[2 * h + 1]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bempty[bs]);
