@@ -129,6 +129,7 @@ KERNEL_SOURCES = {
            "fs_internal.cuh", "fs_host.cuh"],
     "pair": ["fs_tc_pair.cu", "fs_tc_host.cu", "fs_tc.cuh", "fs_tc_kernels.cuh", "fs_internal.cuh",
              "fs_host.cuh"],
+    "sparse": ["fs_sparse.cu", "fs_internal.cuh", "fs_host.cuh"],
 }
 
 
@@ -544,7 +545,8 @@ def run_sparse(args, w):
                            f"lanes/clk/SM / {fp32_ops} lane-ops per kept pair) ({rate_src}) x "
                            f"{sms} SMs x {clk:.0f} MHz (median SM clock in the timed region)",
             "mufu_frac": achieved / ex2_peak, "fp32_frac": achieved / fp32_peak,
-            "traffic": None, "kernel": "block_sparse_half_update",
+            "traffic": _traffic_from_profiles(w.name, "sparse"),
+            "kernel": "block_sparse_half_update",
             "avg_launch_ms": avg_half_ms, "launches": half_n,
             "kept_pairs_per_launch": pairs_per_launch,
             "unit_rates": dict(rates, source=rate_src)}
