@@ -143,19 +143,27 @@ cudaError_t launch_merge_apply_tc(const TcApplyArgs& a, cudaStream_t s) {
 
 namespace {
 constexpr int kStageA = 4 * CHUNK_BYTES;          // K hi, K lo, Q hi, Q lo
-constexpr int kVtSlot = kApplyKV * 2 * 128;       // 2 halves x 128 rows x 128 B
 constexpr int kOCol = 2 * BN;                     // TMEM column of the O accumulator
+// value-tile slots: KV output rows x 2 halves x 128 B each
+__host__ __device__ constexpr int vt_slot_bytes(int kv) { return kv * 2 * 128; }
+__host__ __device__ constexpr int vt_slots(int kv) { return kv == 256 ? 1 : 2; }
 }  // namespace
 
+// KV output columns per CTA.  With one value slot (KV = 256) the value tile
+// of tile t is loaded while the scores of tile t + 1 stream (after its first
+// half of chunks), which the MMA thread consumes only after those scores.
+template <int KV>
 __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
+    constexpr int kVtSlot = vt_slot_bytes(KV);
+    constexpr int VS = vt_slots(KV);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int64_t rt = blockIdx.x;
-    const int n0 = blockIdx.y * kApplyKV;
-    const int kvN = min(kApplyKV, a.kpad - n0);       // multiple of 16
+    const int n0 = blockIdx.y * KV;
+    const int kvN = min(KV, a.kpad - n0);             // multiple of 16
     const int j0 = blockIdx.z * a.tiles_per_split;
     const int j1 = min(a.col_tiles, j0 + a.tiles_per_split);
     const int ntiles = j1 - j0;
@@ -163,7 +171,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
 
     uint8_t* sStage = smem;
     uint8_t* sVT = sStage + kApplyStages * kStageA;
-    uint8_t* sP = sVT + 2 * kVtSlot;
+    uint8_t* sP = sVT + VS * kVtSlot;
     uint64_t* full = reinterpret_cast<uint64_t*>(sP + 2 * CHUNK_BYTES);
     uint64_t* empty = full + kApplyStages;
     uint64_t* tfull = empty + kApplyStages;
@@ -208,6 +216,21 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
             int s = 0, issued = 0, vissued = 0;
             uint32_t ph = 0;
             bool ok = true;
+            // value tile of tile t into slot t % VS (its u-th use, u = t / VS)
+            auto load_v = [&](int t) -> bool {
+                const int vb = t % VS;
+                const int u = t / VS;
+                if (!mbar_wait(&vempty[vb], (uint32_t)(u & 1) ^ 1u, a.err, ERR_TIMEOUT_PRODUCER))
+                    return false;
+                const uint32_t vbytes = (uint32_t)kvN * 128u;
+                const int64_t j = j0 + t;
+                mbar_arrive_expect_tx(&vfull[vb], 2 * vbytes);
+                for (int kq = 0; kq < 2; ++kq)
+                    bulk_g2s(sVT + vb * kVtSlot + kq * vbytes,
+                             VTg + ((j * 2 + kq) * a.kpad + n0) * (int64_t)128, vbytes, &vfull[vb]);
+                ++vissued;
+                return true;
+            };
             for (int t = 0; t < ntiles && ok; ++t) {
                 const int64_t j = j0 + t;
                 const int64_t koff = j * nch * (int64_t)CHUNK_BYTES;
@@ -230,21 +253,12 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
                         s = 0;
                         ph ^= 1u;
                     }
+                    if (VS == 1 && c == nch / 2 && t > 0 && !(ok = load_v(t - 1))) break;
                 }
                 if (!ok) break;
-                const int vb = t & 1;
-                if (!mbar_wait(&vempty[vb], (uint32_t)((t >> 1) & 1) ^ 1u, a.err,
-                               ERR_TIMEOUT_PRODUCER)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t vbytes = (uint32_t)kvN * 128u;
-                mbar_arrive_expect_tx(&vfull[vb], 2 * vbytes);
-                for (int kq = 0; kq < 2; ++kq)
-                    bulk_g2s(sVT + vb * kVtSlot + kq * vbytes,
-                             VTg + ((j * 2 + kq) * a.kpad + n0) * (int64_t)128, vbytes, &vfull[vb]);
-                ++vissued;
+                if (VS == 2 && !(ok = load_v(t))) break;
             }
+            if (ok && VS == 1 && ntiles > 0) ok = load_v(ntiles - 1);
             if (!ok) {
                 // let every copy already issued land before the CTA can exit
                 int s2 = 0;
@@ -257,8 +271,8 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
                         ph2 ^= 1u;
                     }
                 }
-                for (int i = vissued > 2 ? vissued - 2 : 0; i < vissued; ++i)
-                    mbar_wait(&vfull[i & 1], (uint32_t)((i >> 1) & 1), a.err, ERR_TIMEOUT_PRODUCER);
+                for (int i = vissued > VS ? vissued - VS : 0; i < vissued; ++i)
+                    mbar_wait(&vfull[i % VS], (uint32_t)((i / VS) & 1), a.err, ERR_TIMEOUT_PRODUCER);
             }
         }
     } else if (warp == 1) {
@@ -299,12 +313,12 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
             for (int t = 0; t < ntiles && ok; ++t) {
                 if (t + 1 < ntiles && !(ok = issue_S(t + 1))) break;
                 if (!mbar_wait(pfull, (uint32_t)(t & 1), a.err, ERR_TIMEOUT_MMA) ||
-                    !mbar_wait(&vfull[t & 1], (uint32_t)((t >> 1) & 1), a.err, ERR_TIMEOUT_MMA)) {
+                    !mbar_wait(&vfull[t % VS], (uint32_t)((t / VS) & 1), a.err, ERR_TIMEOUT_MMA)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint8_t* vslot = sVT + (t & 1) * kVtSlot;
+                const uint8_t* vslot = sVT + (t % VS) * kVtSlot;
 #pragma unroll
                 for (int kq = 0; kq < 2; ++kq)
 #pragma unroll
@@ -314,7 +328,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
                                 sdesc_sw128(smem_u32(vslot + kq * kvN * 128) + kk * 32), idescO,
                                 (t | kq | kk) != 0);
                 mma_commit(pempty);
-                mma_commit(&vempty[t & 1]);
+                mma_commit(&vempty[t % VS]);
             }
             mma_commit(ofull);
             mma_commit(drain);
@@ -414,20 +428,29 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
     }
 }
 
-size_t apply_smem_bytes() {
-    return 1024 + (size_t)kApplyStages * kStageA + 2 * (size_t)kVtSlot + 2 * (size_t)CHUNK_BYTES +
-           8 * (2 * kApplyStages + 8 + 4) + 16;
+constexpr size_t apply_smem_bytes(int kv) {
+    return 1024 + (size_t)kApplyStages * kStageA + (size_t)vt_slots(kv) * vt_slot_bytes(kv) +
+           2 * (size_t)CHUNK_BYTES + 8 * (2 * kApplyStages + 8 + 4) + 16;
+}
+static_assert(apply_smem_bytes(128) <= kSmemLimit && apply_smem_bytes(256) <= kSmemLimit,
+              "plan application does not fit in shared memory");
+
+template <int KV>
+cudaError_t launch_apply_kv(const TcApplyArgs& a, int row_tiles, cudaStream_t s) {
+    constexpr size_t smem = apply_smem_bytes(KV);
+    cudaError_t e = cudaFuncSetAttribute(k_apply_tc<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)row_tiles, (unsigned)((a.kpad + KV - 1) / KV), (unsigned)a.splits);
+    k_apply_tc<KV><<<grid, kApplyThreads, smem, s>>>(a);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_apply_tc(const TcApplyArgs& a, int row_tiles, cudaStream_t s) {
-    const size_t smem = apply_smem_bytes();
-    cudaError_t e = cudaFuncSetAttribute(k_apply_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)row_tiles, (unsigned)((a.kpad + kApplyKV - 1) / kApplyKV), (unsigned)a.splits);
-    k_apply_tc<<<grid, kApplyThreads, smem, s>>>(a);
+    const cudaError_t e = apply_kv(a.nch, a.kpad) == 256 ? launch_apply_kv<256>(a, row_tiles, s)
+                                                         : launch_apply_kv<128>(a, row_tiles, s);
     count_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace tc

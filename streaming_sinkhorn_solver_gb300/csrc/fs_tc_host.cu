@@ -144,7 +144,8 @@ struct TcApplyBufs {
 void layout_apply(Layout& L, TcApplyBufs& A, const TcPlan& p, int64_t n, int32_t k, int sms,
                   const fs_options* opt) {
     A.kpad = (k + 15) / 16 * 16;
-    const int64_t nkv = (A.kpad + kApplyKV - 1) / kApplyKV;
+    const int kv = apply_kv(p.nch, A.kpad);
+    const int64_t nkv = (A.kpad + kv - 1) / kv;
     choose_tc_splits(p.rtx * nkv, p.rty, sms, opt, &A.splits, &A.tps);
     A.lse2 = L.take(sizeof(float) * n);
     A.phi = L.take(sizeof(float) * n);

@@ -120,7 +120,11 @@ cudaError_t launch_half_ref(const TcHalfArgs& a, int row_tiles, cudaStream_t s);
 // output column n) of 64 fp16 values in the K-major 128-byte-swizzled order,
 // i.e. byte ((j*2 + kq)*kpad + n)*128 + swizzled offset of point p.
 constexpr int kApplyStages = 2;         // (K hi, K lo, Q hi, Q lo) chunk sets in flight
-constexpr int kApplyKV = 128;           // output columns per CTA (TMEM columns of O)
+// Output columns per CTA (TMEM columns of O): 256 when the scores of a tile
+// take long enough (d >= 256) to hide the load of the next value tile into a
+// single 64 KB slot, else 128 with two value slots.  Every 256 columns of
+// output recompute the scores once.
+__host__ __device__ constexpr int apply_kv(int nch, int kpad) { return nch >= 4 && kpad > 128 ? 256 : 128; }
 constexpr int kApplyThreads = 32 * (2 + kEpiWarps);   // producer, MMA, one epilogue group
 constexpr int kApplyTmemCols = 512;     // 2 score buffers + O, rounded to a power of two
 
