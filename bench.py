@@ -532,9 +532,10 @@ def run_sparse(args, w):
     ex2_clk = rates.get("ex2_per_clk_sm") or EX2_PER_CLK_SM
     fp32_clk = rates.get("fma2_lanes_per_clk_sm") or FP32_LANES_PER_CLK_SM
     rate_src = "measured by fs_unit_rates" if "ex2_per_clk_sm" in rates else "nominal"
-    # per kept pair: d fused multiply-adds, the online max, the offset
-    # subtraction and the accumulation
-    fp32_ops = d + 3
+    # per kept pair, at the least (reference offsets, as after the first
+    # iterations): d fused multiply-adds, the offset subtraction and the
+    # accumulation -- the same count as the dense FMA path
+    fp32_ops = fp32_ops_per_pair(d, False)
     ex2_peak = ex2_clk * sms * clk * 1e6
     fp32_peak = fp32_clk / fp32_ops * sms * clk * 1e6
     alu_peak = min(ex2_peak, fp32_peak)

@@ -338,7 +338,9 @@ fs_status fs_unit_rates(double* out, void* stream);
  *     a slack in favour of keeping), so the skipped blocks of every output
  *     block carry less than tau times its weight W_O.  tau = 0 keeps all.
  *   - Fine stage: f-updates over each row block's kept blocks, then g-updates
- *     over each column block's, until the row residual |P 1 - a|_1 of the
+ *     over each column block's (the exponent offset of a row is its running max
+ *     for the first online_iters iterations, then its previous LSE with a
+ *     guarded sum), until the row residual |P 1 - a|_1 of the
  *     block-sparse plan (measured every check_every iterations with a fresh
  *     screening) is <= target, or max_iters iterations.
  */
@@ -348,7 +350,10 @@ typedef struct fs_sparse_options {
     int32_t check_every;   /* residual test period in iterations (0: never, run max_iters) */
     float tau;             /* omitted-mass bound per block relative to its weight, [0, 1) */
     float target;          /* stop when the row residual <= target (0: never) */
-    int32_t reserved[4];   /* must be zero */
+    int32_t online_iters;  /* fine iterations that take the running max as the exponent
+                              offset before each row's previous LSE is used (a guarded
+                              sum, rows outside the range recomputed): 0 = 2, -1 = none */
+    int32_t reserved[3];   /* must be zero */
 } fs_sparse_options;
 
 typedef struct fs_sparse_report {

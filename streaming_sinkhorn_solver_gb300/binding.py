@@ -54,7 +54,8 @@ class fs_options(ctypes.Structure):
 class fs_sparse_options(ctypes.Structure):
     _fields_ = [("coarse_iters", ctypes.c_int32), ("max_iters", ctypes.c_int32),
                 ("check_every", ctypes.c_int32), ("tau", ctypes.c_float),
-                ("target", ctypes.c_float), ("reserved", ctypes.c_int32 * 4)]
+                ("target", ctypes.c_float), ("online_iters", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 3)]
 
 
 class fs_sparse_report(ctypes.Structure):
@@ -431,7 +432,7 @@ def fs_sinkhorn_solve_noalloc(X, a, Y, b, eps: float, n_iter: int, f, g, *, stre
 
 def fs_sparse_solve(X, a, Y, b, eps: float, *, coarse_iters: int = 0, max_iters: int = 100,
                     tau: float = 1e-6, target: float = 0.0, check_every: int = 0, f=None, g=None,
-                    stream=None):
+                    online_iters: int = 0, stream=None):
     """The block-sparse solver (see the C header for the method and its
     readings).  f, g are outputs (and inputs when coarse_iters == 0; zeros if
     None).  Returns (f, g, report) with report a dict of fs_sparse_report."""
@@ -444,6 +445,7 @@ def fs_sparse_solve(X, a, Y, b, eps: float, *, coarse_iters: int = 0, max_iters:
     o = fs_sparse_options()
     o.coarse_iters, o.max_iters, o.check_every = int(coarse_iters), int(max_iters), int(check_every)
     o.tau, o.target = float(tau), float(target)
+    o.online_iters = int(online_iters)
     rep = fs_sparse_report()
     st = load_library().fs_sparse_solve(
         _ptr(X, "X", (n, d)), _ptr(a, "a", (n,)), n, _ptr(Y, "Y", (m, d)), _ptr(b, "b", (m,)), m, d,

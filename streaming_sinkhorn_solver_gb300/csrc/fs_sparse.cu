@@ -653,7 +653,16 @@ struct SpHalfArgs {
     float* rowsum;           // measure mode: row marginal 2^{bias + LSE2} [nr]
     int measure;             // 1: write rowsum only, no update
     unsigned long long* work;   // [2] accumulated: block pairs, score pairs evaluated
+    // reference offsets: rows whose guarded sum left the range, for k_sp_fix
+    int* fix_list;            // [nr]
+    unsigned int* fix_count;  // [2], zero before the first guarded half-update
 };
+
+// Guarded range of a row's sum 2^{s - M} when M is the previous LSE: below
+// 2^-64 the terms that underflowed could matter, above 2^126 the sum could
+// overflow; such rows are recomputed with the online max.
+constexpr float kSpMinRefSum = 5.421010862427522e-20f;   // 2^-64
+constexpr float kSpMaxRefSum = 8.507059173023462e+37f;   // 2^126
 
 constexpr int kSpWarps = 8;                 // warps per block, each its own share of the list
 constexpr float kSpSlack = 8.f;            // lazy rescale threshold (log2 units)
@@ -665,8 +674,12 @@ constexpr float kSpSlack = 8.f;            // lazy rescale threshold (log2 units
 // duplicated, so one packed FMA scores a column against two rows.  The
 // eight warps' (max, sum) are merged in warp order at the end, so the result
 // does not depend on timing.
-template <int D>
-__global__ void __launch_bounds__(256) k_sp_half(SpHalfArgs a) {
+// REF = false: online max with a lazy rescale.  REF = true: the offset of a
+// row is its previous LSE, log2 w - (bias slot), so a pair costs the score,
+// one subtraction, one ex2 and one add; the row's sum is range-checked and
+// rows outside the range go to the fixup list.
+template <int D, bool REF>
+__global__ void __launch_bounds__(256, 3) k_sp_half(SpHalfArgs a) {
     __shared__ float4 sc[kSpWarps][2 * kSB];
     __shared__ float2 part[kSpWarps][kSB];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -685,6 +698,15 @@ __global__ void __launch_bounds__(256) k_sp_half(SpHalfArgs a) {
     for (int i = 0; i < 4; ++i) M[i] = Mt[i] = -INFINITY;
     S[0] = S[1] = pk(0.f, 0.f);
     nm[0] = nm[1] = pk(INFINITY, INFINITY);
+    if (REF) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t r = min(r0 + lane + 32 * i, a.nr - 1);
+            M[i] = a.rlogw2[r] - a.rows[r * 4 + D];
+        }
+        nm[0] = pk(-M[0], -M[1]);
+        nm[1] = pk(-M[2], -M[3]);
+    }
 
     const int cnt = a.counts[O];
     const int* lst = a.lists + (int64_t)O * a.nbi;
@@ -723,6 +745,7 @@ __global__ void __launch_bounds__(256) k_sp_half(SpHalfArgs a) {
                     s[p][u] = u < G ? acc : pk(-INFINITY, -INFINITY);
                 }
             }
+            if (!REF) {
             // online max with a lazy, warp-uniform rescale
             float m[4] = {Mt[0], Mt[1], Mt[2], Mt[3]};
 #pragma unroll
@@ -753,6 +776,7 @@ __global__ void __launch_bounds__(256) k_sp_half(SpHalfArgs a) {
                     S[p] = fma2(S[p], pk(f[2 * p], f[2 * p + 1]), pk(0.f, 0.f));
                     nm[p] = pk(-M[2 * p], -M[2 * p + 1]);
                 }
+            }
             }
 #pragma unroll
             for (int p = 0; p < 2; ++p) {
@@ -790,9 +814,19 @@ __global__ void __launch_bounds__(256) k_sp_half(SpHalfArgs a) {
         const int64_t row = r0 + t;
         if (row < a.nr) {
             float Mf = -INFINITY, Sf = 0.f;
-            for (int w = 0; w < kSpWarps; ++w) {
-                const float2 pp = part[w][t];
-                if (pp.x != -INFINITY) lse_merge(Mf, Sf, pp.x, pp.y);
+            if (REF) {
+                // one offset for every warp: the sum of the warps' sums in order
+                Mf = part[0][t].x;
+                for (int w = 0; w < kSpWarps; ++w) Sf += part[w][t].y;
+                if (!(Sf >= kSpMinRefSum && Sf <= kSpMaxRefSum)) {
+                    const unsigned int slot = atomicAdd(&a.fix_count[0], 1u);
+                    if (slot < (unsigned int)a.nr) a.fix_list[slot] = (int)row;
+                }
+            } else {
+                for (int w = 0; w < kSpWarps; ++w) {
+                    const float2 pp = part[w][t];
+                    if (pp.x != -INFINITY) lse_merge(Mf, Sf, pp.x, pp.y);
+                }
             }
             const float lse2 = Mf + log2f(Sf);
             if (a.measure) {
@@ -801,6 +835,67 @@ __global__ void __launch_bounds__(256) k_sp_half(SpHalfArgs a) {
                 a.pot[row] = a.rnorm[row] - a.eps_ln2 * lse2;
                 a.rows[row * 4 + D] = a.rlogw2[row] - lse2;
             }
+        }
+    }
+}
+
+// Recompute, with the online max over the row block's kept blocks, the rows a
+// guarded half-update listed: one warp per row, lanes striding over the
+// kept columns, then a shuffle merge.  The last block to finish resets the
+// list for the next half-update.
+constexpr int kSpFixBlocks = 64;
+
+template <int D>
+__global__ void __launch_bounds__(256) k_sp_fix(SpHalfArgs a) {
+    __shared__ unsigned int s_cnt;
+    if (threadIdx.x == 0) s_cnt = min(*(volatile unsigned int*)&a.fix_count[0], (unsigned int)a.nr);
+    __syncthreads();
+    const unsigned int cnt = s_cnt;
+    const int lane = threadIdx.x & 31;
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    for (unsigned int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < cnt; w += warps) {
+        const int64_t row = a.fix_list[w];
+        const int64_t O = row / kSB;
+        float q[D];
+#pragma unroll
+        for (int k = 0; k < D; ++k) q[k] = a.rows[row * 4 + k] * a.kappa;
+        float M = -INFINITY, S = 0.f;
+        const int* lst = a.lists + O * a.nbi;
+        const int nk = a.counts[O];
+        for (int e = 0; e < nk; ++e) {
+            const int64_t c0 = (int64_t)lst[e] * kSB;
+            const int ncol = (int)min((int64_t)kSB, a.nc - c0);
+            for (int j = lane; j < ncol; j += 32) {
+                const float* c = a.cols + (c0 + j) * 4;
+                float sc = c[D];
+#pragma unroll
+                for (int k = 0; k < D; ++k) sc = fmaf(q[k], c[k], sc);
+                if (sc > M) {
+                    S = (M == -INFINITY ? 0.f : S * ex2(M - sc));
+                    M = sc;
+                }
+                S += ex2(sc - M);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            const float Mo = __shfl_xor_sync(0xffffffffu, M, o);
+            const float So = __shfl_xor_sync(0xffffffffu, S, o);
+            lse_merge(M, S, Mo, So);
+        }
+        if (lane == 0) {
+            const float lse2 = M + log2f(S);
+            a.pot[row] = a.rnorm[row] - a.eps_ln2 * lse2;
+            a.rows[row * 4 + D] = a.rlogw2[row] - lse2;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(&a.fix_count[1], 1u) == gridDim.x - 1) {
+            a.fix_count[0] = 0;
+            a.fix_count[1] = 0;
+            __threadfence();
         }
     }
 }
@@ -844,7 +939,7 @@ struct SpBufs {
     size_t box, keys0, keys1, vals0, vals1, hist;
     size_t shift_part, shift;
     SpSide X, Y;
-    size_t lists, counts, order, rowsum, red_part, red_out, kept;
+    size_t lists, counts, order, rowsum, red_part, red_out, kept, fix_list, fix_count;
     // coarse stage
     size_t cshift, cPX, cPY, cnx, cny, clx, cly, cpart, F, G;
     int csplits_f, csplits_g;
@@ -892,6 +987,8 @@ void layout_sparse(Layout& L, SpBufs& B, int64_t n, int64_t m, int d, int sms, b
     B.red_part = L.take(sizeof(double) * kRedPartials);
     B.red_out = L.take(sizeof(double) * 2);
     B.kept = L.take(sizeof(unsigned long long) * 2);
+    B.fix_list = L.take(sizeof(int) * mx);
+    B.fix_count = L.take(sizeof(unsigned int) * 2);
     if (coarse) {
         const int D = fma_pad_dim(d);
         const int DS = fma_stride(D);
@@ -1022,7 +1119,7 @@ fs_status screen(Call& c, const SpBufs& B, const SpSide& o, const SpSide& in, fl
 }
 
 fs_status sparse_half(Call& c, const SpBufs& B, const SpSide& o, const SpSide& in, int D,
-                      float eps, bool measure) {
+                      float eps, bool measure, bool ref = false) {
     SpHalfArgs h;
     h.rows = c.at<float>(o.rec);
     h.cols = c.at<float>(in.rec);
@@ -1040,16 +1137,30 @@ fs_status sparse_half(Call& c, const SpBufs& B, const SpSide& o, const SpSide& i
     h.measure = measure ? 1 : 0;
     h.work = c.at<unsigned long long>(B.kept);
     h.order = c.at<int>(B.order);
+    h.fix_list = c.at<int>(B.fix_list);
+    h.fix_count = c.at<unsigned int>(B.fix_count);
+    ref = ref && !measure;
     int shift = 0;
     while ((in.nb >> shift) >= 1024) ++shift;
     k_sp_order<<<1, 1024, 0, c.stream>>>(h.counts, (int)o.nb, shift, c.at<int>(B.order));
     count_launch();
     const int ts = measure ? -1 : timing_begin(c.stream);
-    if (D == 2) k_sp_half<2><<<(unsigned)o.nb, 256, 0, c.stream>>>(h);
-    else k_sp_half<3><<<(unsigned)o.nb, 256, 0, c.stream>>>(h);
+    if (D == 2) {
+        if (ref) k_sp_half<2, true><<<(unsigned)o.nb, 256, 0, c.stream>>>(h);
+        else k_sp_half<2, false><<<(unsigned)o.nb, 256, 0, c.stream>>>(h);
+    } else {
+        if (ref) k_sp_half<3, true><<<(unsigned)o.nb, 256, 0, c.stream>>>(h);
+        else k_sp_half<3, false><<<(unsigned)o.nb, 256, 0, c.stream>>>(h);
+    }
     timing_end(ts, TIME_HALF, c.stream);
     count_launch();
     FS_CUDA(cudaGetLastError());
+    if (ref) {
+        if (D == 2) k_sp_fix<2><<<kSpFixBlocks, 256, 0, c.stream>>>(h);
+        else k_sp_fix<3><<<kSpFixBlocks, 256, 0, c.stream>>>(h);
+        count_launch();
+        FS_CUDA(cudaGetLastError());
+    }
     return FS_OK;
 }
 
@@ -1111,6 +1222,7 @@ fs_status coarse_stage(Call& c, SpBufs& B, int d, float eps, int iters) {
 }
 
 constexpr int64_t kMaxListEntries = (int64_t)1 << 30;
+constexpr int kSpOnlineIters = 2;
 
 fs_status check_sparse_args(const float* X, const float* a, int64_t n, const float* Y, const float* b,
                             int64_t m, int32_t d, float eps) {
@@ -1141,8 +1253,12 @@ fs_status sparse_solve_entry(const float* X, const float* a, int64_t n, const fl
         return fail(FS_ERR_INVALID_ARG, "tau=%g must be in [0, 1)", (double)opt->tau);
     if (!(opt->target >= 0.f) || !std::isfinite(opt->target))
         return fail(FS_ERR_INVALID_ARG, "target=%g must be finite and >= 0", (double)opt->target);
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 3; ++i)
         if (opt->reserved[i]) return fail(FS_ERR_INVALID_ARG, "fs_sparse_options.reserved must be zero");
+    if (opt->online_iters < -1)
+        return fail(FS_ERR_INVALID_ARG, "online_iters=%d must be >= -1", opt->online_iters);
+    const int online_iters = opt->online_iters == 0 ? kSpOnlineIters
+                             : opt->online_iters < 0 ? 0 : opt->online_iters;
     Call c;
     FS_TRY(begin_call(c, stream));
     if (c.capturing)
@@ -1181,6 +1297,7 @@ fs_status sparse_solve_entry(const float* X, const float* a, int64_t n, const fl
     timing_end(tp, TIME_PREP, c.stream);
     FS_CUDA(cudaMemsetAsync(c.at<unsigned long long>(B.kept), 0, 2 * sizeof(unsigned long long),
                             c.stream));
+    FS_CUDA(cudaMemsetAsync(c.at<unsigned int>(B.fix_count), 0, 2 * sizeof(unsigned int), c.stream));
 
     const float tau = opt->tau;
     int it = 0, passes = 0;
@@ -1197,10 +1314,13 @@ fs_status sparse_solve_entry(const float* X, const float* a, int64_t n, const fl
         }
         if (!screened) FS_TRY(screen(c, B, B.X, B.Y, eps, tau));
         screened = false;
-        FS_TRY(sparse_half(c, B, B.X, B.Y, D, eps, false));
+        // the first iterations take the online max: the lifted (or given)
+        // potentials may be far from the first updates
+        const bool ref = it >= online_iters;
+        FS_TRY(sparse_half(c, B, B.X, B.Y, D, eps, false, ref));
         FS_TRY(refresh_psi(c, B.X, l_over_eps));
         FS_TRY(screen(c, B, B.Y, B.X, eps, tau));
-        FS_TRY(sparse_half(c, B, B.Y, B.X, D, eps, false));
+        FS_TRY(sparse_half(c, B, B.Y, B.X, D, eps, false, ref));
         FS_TRY(refresh_psi(c, B.Y, l_over_eps));
         passes += 2;
         ++it;

@@ -146,6 +146,34 @@ def test_screened_solve_matches_oracle(name, n, d, eps, tau):
     assert rep["residual"] == pytest.approx(orep["residual"], rel=1e-2, abs=1e-5)
 
 
+@pytest.mark.parametrize("online_iters", [0, -1])
+def test_reference_offsets_with_fixups_match_oracle(online_iters):
+    """After `online_iters` iterations a row's exponent offset is its previous
+    LSE, read from its bias slot.  With -1 that holds from the first update
+    of a cold start, where the offset implied by f = g = 0 is far from the
+    row's LSE (checked on the oracle: more than the guarded 2^-64 below it
+    for some rows), so those rows go through the fixup.  The potentials
+    must match the oracle either way."""
+    inp = make_inputs("c2_n10k_d3", n=2000, m=1900, d=2)
+    eps, tau = 0.002, 1e-6
+    C = orc.cost(inp["X"], inp["Y"])
+    e = orc.as_eps(eps)
+    if online_iters == -1:
+        # offset from f = 0: log2 a_i - ((0 - |x~|^2) L/eps + log2 a_i) = |x~|^2 L/eps;
+        # LSE2 of the first update: (|x~|^2 - f_1) L/eps; gap = -f_1 L/eps
+        f1, _, _ = bsp.solve(inp["X"], inp["a"], inp["Y"], inp["b"], eps, 0, 1, tau)
+        # (f_1 = -eps LSE over the kept blocks; the gap is independent of the centring)
+        gap = -f1 / (e * np.log(2.0))
+        assert gap.min() < -64
+    t = to_dev(inp)
+    f, g, _ = fs.fs_sparse_solve(t["X"], t["a"], t["Y"], t["b"], eps, coarse_iters=0,
+                                 max_iters=8, tau=tau, online_iters=online_iters)
+    fr, gr, _ = bsp.solve(inp["X"], inp["a"], inp["Y"], inp["b"], eps, 0, 8, tau)
+    tol = F_TOL_FMA * C.max()
+    assert max_abs(np64(f), fr) <= tol
+    assert max_abs(np64(g), gr) <= tol
+
+
 def test_coarse_stage_alone_matches_oracle():
     inp = make_inputs("c2_n10k_d3", n=3000, m=2700)
     t = to_dev(inp)

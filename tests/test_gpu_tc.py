@@ -147,6 +147,21 @@ def test_grad_and_barycentric_tensor_match_oracle(d):
 
 
 @pytest.mark.parametrize("splits", [1, 3])
+def test_apply_forced_splits_wide_output_blocks(splits):
+    """d >= 256 and more than 128 value columns: 256-column output blocks with
+    one value slot, a ragged second block (k = 290 -> 256 + 48), several
+    column tiles per CTA and split partials."""
+    inp = random_cloud(300, 900, 300, seed=17, spread=1.0 / np.sqrt(300), weights="lognormal")
+    C, f32, g32 = _potentials(inp, 0.05 * 2.0, 6)
+    V = np.random.default_rng(5).standard_normal((900, 290)).astype(np.float32)
+    t = to_dev(dict(inp, V=V, f=f32, g=g32))
+    out = fs.fs_apply_plan(t["X"], t["a"], t["Y"], t["b"], 0.1, t["f"], t["g"], t["V"],
+                           path="tensor", splits=splits)
+    ref = orc.apply_plan(C, inp["a"], inp["b"], 0.1, f32, g32, V)
+    assert rel_l2(np64(out), ref) <= APPLY_TOL
+
+
+@pytest.mark.parametrize("splits", [1, 3])
 def test_apply_forced_splits(splits):
     inp = random_cloud(500, 650, 64, seed=13, spread=0.125, weights="lognormal")
     C, f32, g32 = _potentials(inp, 0.1, 10)
