@@ -329,32 +329,105 @@ __global__ void k_sp_bias(const float* __restrict__ pot_s, const float* __restri
 }
 
 // psi_k = pot_k L/eps + log2 w_k for the screening: one 128-thread block per
-// point block stores psi - max into the record's w, the max per block, and
-// a0 = log2 sum_k 2^{psi_k - max} (the block's bound at Delta = 0).
+// point block stores psi - max into the record's w, the max per block,
+// a0 = log2 sum_k 2^{psi_k - max} (the block's bound at Delta = 0), and an
+// affine majorant of psi - max over the block's offsets u from its centroid:
+// psi_k - max <= c + g.u_k for every point, with g the least-squares slope
+// (a ridge keeps degenerate axes at zero slope; any g gives a valid bound)
+// and c its intercept plus the largest residual.  lin = (g, c + log2 count).
 __global__ void __launch_bounds__(kSB) k_sp_psi(const float* __restrict__ pot_s,
                                                 const float* __restrict__ logw2, int64_t cnt,
                                                 float l_over_eps, float4* __restrict__ scr,
-                                                float* __restrict__ pmax, float* __restrict__ a0) {
+                                                float* __restrict__ pmax, float* __restrict__ a0,
+                                                float4* __restrict__ lin) {
+    constexpr int NM = 14;   // moments: 1, u (3), p, u u^T (6), u p (3)
     __shared__ float red[kSB / 32];
     __shared__ float red2[kSB / 32];
+    __shared__ double mom[kSB / 32][NM];
+    __shared__ float s_fit[4];
     const int64_t k = (int64_t)blockIdx.x * kSB + threadIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const bool ok = k < cnt;
     const float psi = ok ? fmaf(pot_s[k], l_over_eps, logw2[k]) : -INFINITY;
     float mx = psi;
 #pragma unroll
     for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    if (lane == 0) red[warp] = mx;
     __syncthreads();
     mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
     float e = ok ? exp2f(psi - mx) : 0.f;
 #pragma unroll
     for (int o = 16; o; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
-    if ((threadIdx.x & 31) == 0) red2[threadIdx.x >> 5] = e;
-    if (ok) scr[k].w = psi - mx;
+    if (lane == 0) red2[warp] = e;
+    float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float ps = ok ? psi - mx : 0.f;
+    if (ok) {
+        u = scr[k];
+        scr[k].w = ps;
+    }
+    // moments of the fit, in double
+    double m[NM];
+    const double w1 = ok ? 1.0 : 0.0, x0 = u.x, x1 = u.y, x2 = u.z, pp = ps;
+    m[0] = w1; m[1] = x0; m[2] = x1; m[3] = x2; m[4] = pp;
+    m[5] = x0 * x0; m[6] = x0 * x1; m[7] = x0 * x2; m[8] = x1 * x1; m[9] = x1 * x2; m[10] = x2 * x2;
+    m[11] = x0 * pp; m[12] = x1 * pp; m[13] = x2 * pp;
+#pragma unroll
+    for (int i = 0; i < NM; ++i) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1) m[i] += __shfl_xor_sync(0xffffffffu, m[i], o);
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < NM; ++i) mom[warp][i] = m[i];
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
+        double t[NM];
+        for (int i = 0; i < NM; ++i) t[i] = ((mom[0][i] + mom[1][i]) + mom[2][i]) + mom[3][i];
+        // normal equations of psi - max ~ alpha + g.u, with a small ridge on g
+        const double ridge = 1e-9 * (t[5] + t[8] + t[10]) + 1e-30;
+        double A[4][5] = {{t[0], t[1], t[2], t[3], t[4]},
+                          {t[1], t[5] + ridge, t[6], t[7], t[11]},
+                          {t[2], t[6], t[8] + ridge, t[9], t[12]},
+                          {t[3], t[7], t[9], t[10] + ridge, t[13]}};
+        for (int c = 0; c < 4; ++c) {   // Gaussian elimination, partial pivoting
+            int pv = c;
+            for (int r = c + 1; r < 4; ++r)
+                if (fabs(A[r][c]) > fabs(A[pv][c])) pv = r;
+            if (pv != c)
+                for (int q = 0; q < 5; ++q) {
+                    const double tmp = A[c][q];
+                    A[c][q] = A[pv][q];
+                    A[pv][q] = tmp;
+                }
+            for (int r = c + 1; r < 4; ++r) {
+                const double f = A[r][c] / A[c][c];
+                for (int q = c; q < 5; ++q) A[r][q] -= f * A[c][q];
+            }
+        }
+        double sol[4];
+        for (int r = 3; r >= 0; --r) {
+            double v = A[r][4];
+            for (int q = r + 1; q < 4; ++q) v -= A[r][q] * sol[q];
+            sol[r] = v / A[r][r];
+        }
+        for (int i = 0; i < 4; ++i) s_fit[i] = isfinite(sol[i]) ? (float)sol[i] : 0.f;
+    }
+    __syncthreads();
+    const float al = s_fit[0], g0 = s_fit[1], g1 = s_fit[2], g2 = s_fit[3];
+    float res = ok ? ps - (al + (g0 * u.x + g1 * u.y + g2 * u.z)) : -INFINITY;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) res = fmaxf(res, __shfl_xor_sync(0xffffffffu, res, o));
+    __syncthreads();
+    if (lane == 0) red[warp] = res;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const float r = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+        const int count = (int)min((int64_t)kSB, cnt - (int64_t)blockIdx.x * kSB);
         pmax[blockIdx.x] = mx;
         a0[blockIdx.x] = log2f(((red2[0] + red2[1]) + red2[2]) + red2[3]);
+        // intercept + residual, a 1/64 allowance for the float32 evaluation, log2 count
+        lin[blockIdx.x] = make_float4(g0, g1, g2, al + r + 0.015625f + log2f((float)count));
     }
 }
 
@@ -372,6 +445,8 @@ struct ScreenArgs {
     const float4* ext_i;
     const float* a0_o;       // log2 sum 2^{psi - max} per block
     const float* a0_i;
+    const float4* lin_o;     // affine majorant of psi - max per block: (slope, offset + log2 count)
+    const float4* lin_i;
     const float* lw2_o;      // log2 of the output blocks' weights
     int64_t cnt_o, cnt_i;
     int nbo, nbi;
@@ -421,19 +496,27 @@ __device__ __forceinline__ float bound_exact(const ScreenArgs& a, const float4 (
 }
 
 // The slack sigma of the pair and a block-level upper bound of U that needs
-// no per-point work: -kappa Delta.u_i <= kappa sum_k |Delta_k| e_k (e the
-// per-axis extent), so U <= pmax_O + a0_O + pmax_J + a0_J
-//                           + kappa sum_k |Delta_k| (e_Ok + e_Jk) - |Delta|^2 L/eps.
-__device__ __forceinline__ void bound_cheap(const ScreenArgs& a, float4 co, float4 eo, float pmo,
-                                            float a0o, int J, float& ub, float& sig) {
-    const float4 ci = a.cen_i[J], ei = a.ext_i[J];
+// no per-point work.  Per side, the smaller of two majorants of
+// log2 sum 2^{psi - max -+ kappa Delta.u} (e the per-axis extents):
+//   a0 + kappa sum_k |Delta_k| e_k                      (-+kappa Delta.u <= kappa |Delta_k| e_k)
+//   lin.w + sum_k |g_k -+ kappa Delta_k| e_k            (psi - max <= c + g.u)
+// The second keeps the potentials' slope inside a block, which cancels the
+// linear term for the blocks that exchange mass.
+__device__ __forceinline__ void bound_cheap(const ScreenArgs& a, float4 co, float4 eo, float4 lo,
+                                            float pmo, float a0o, int J, float& ub, float& sig) {
+    const float4 ci = a.cen_i[J], ei = a.ext_i[J], li = a.lin_i[J];
     const float Dx = co.x - ci.x, Dy = co.y - ci.y, Dz = co.z - ci.z;
     const float dd = (Dx * Dx + Dy * Dy + Dz * Dz) * a.l_over_eps;
     const float pmi = a.pmax_i[J];
     sig = 0.0625f + 1.52587890625e-05f * (fabsf(pmo) + fabsf(pmi) + dd);
-    ub = pmo + a0o + pmi + a.a0_i[J] +
-         a.kappa * (fabsf(Dx) * (eo.x + ei.x) + fabsf(Dy) * (eo.y + ei.y) + fabsf(Dz) * (eo.z + ei.z)) -
-         dd;
+    const float kx = a.kappa * Dx, ky = a.kappa * Dy, kz = a.kappa * Dz;
+    const float Ao = fminf(a0o + fabsf(kx) * eo.x + fabsf(ky) * eo.y + fabsf(kz) * eo.z,
+                           lo.w + fabsf(lo.x - kx) * eo.x + fabsf(lo.y - ky) * eo.y +
+                               fabsf(lo.z - kz) * eo.z);
+    const float Bi = fminf(a.a0_i[J] + fabsf(kx) * ei.x + fabsf(ky) * ei.y + fabsf(kz) * ei.z,
+                           li.w + fabsf(li.x + kx) * ei.x + fabsf(li.y + ky) * ei.y +
+                               fabsf(li.z + kz) * ei.z);
+    ub = pmo + Ao + pmi + Bi - dd;
 }
 
 // Margin (log2 units) by which the block-level bound must clear a test before
@@ -488,7 +571,7 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
         const int64_t k = o0 + lane + 32 * q;
         own[q] = k < a.cnt_o ? a.so[k] : make_float4(0.f, 0.f, 0.f, -INFINITY);
     }
-    const float4 co = a.cen_o[O], eo = a.ext_o[O];
+    const float4 co = a.cen_o[O], eo = a.ext_o[O], lo = a.lin_o[O];
     const float pmo = a.pmax_o[O], a0o = a.a0_o[O];
     const float T = a.log2_tau + a.lw2_o[O] - log2f((float)a.nbi);
 
@@ -499,7 +582,7 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
         bool surv = false;
         if (J < a.nbi) {
             float ub, sig;
-            bound_cheap(a, co, eo, pmo, a0o, J, ub, sig);
+            bound_cheap(a, co, eo, lo, pmo, a0o, J, ub, sig);
             surv = ub + sig + kCullMargin >= T;
         }
         const int pos = compact_offset(surv, S, s_wcnt);
@@ -552,7 +635,7 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
         bool risk = false;
         for (int J = threadIdx.x; J < a.nbi; J += blockDim.x) {
             float ub, sig;
-            bound_cheap(a, co, eo, pmo, a0o, J, ub, sig);
+            bound_cheap(a, co, eo, lo, pmo, a0o, J, ub, sig);
             if (!(ub + sig + kCullMargin >= T) && ub + kCullMargin >= best) risk = true;
         }
         full = __syncthreads_or(risk) != 0;
@@ -567,7 +650,7 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
                     J = row[sv];
                     const float u = __int_as_float(row[a.nbi - 1 - sv]);
                     float ub, sig;
-                    bound_cheap(a, co, eo, pmo, a0o, J, ub, sig);
+                    bound_cheap(a, co, eo, lo, pmo, a0o, J, ub, sig);
                     keep = (u + sig >= T) || J == bi;
                 }
                 const int pos = compact_offset(keep, base, s_wcnt);
@@ -624,7 +707,7 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
         if (J < a.nbi) {
             const float u = __int_as_float(row[J]);
             float ub, sig;
-            bound_cheap(a, co, eo, pmo, a0o, J, ub, sig);
+            bound_cheap(a, co, eo, lo, pmo, a0o, J, ub, sig);
             keep = (u + sig >= T) || J == bi;
         }
         const int pos = compact_offset(keep, base, s_wcnt);
@@ -931,7 +1014,7 @@ __global__ void __launch_bounds__(1024) k_sp_order(const int* __restrict__ count
 inline unsigned grid_for(int64_t cnt, int threads) { return (unsigned)((cnt + threads - 1) / threads); }
 
 struct SpSide {
-    size_t xs, ws, rec, norm, lw, pot, scr, pmax, a0, ext, cen, cenf, W, lW, perm;
+    size_t xs, ws, rec, norm, lw, pot, scr, pmax, a0, lin, ext, cen, cenf, W, lW, perm;
     int64_t cnt, nb;
 };
 
@@ -959,6 +1042,7 @@ void layout_side(Layout& L, SpSide& s, int64_t cnt, int d) {
     s.scr = L.take(sizeof(float4) * cnt);
     s.pmax = L.take(sizeof(float) * s.nb);
     s.a0 = L.take(sizeof(float) * s.nb);
+    s.lin = L.take(sizeof(float4) * s.nb);
     s.ext = L.take(sizeof(float4) * s.nb);
     s.cen = L.take(sizeof(float4) * s.nb);
     s.cenf = L.take(sizeof(float) * s.nb * d);
@@ -1075,7 +1159,8 @@ fs_status prepare_sparse(Call& c, const SpBufs& B, const float* X, const float* 
 fs_status refresh_psi(Call& c, const SpSide& s, float l_over_eps) {
     k_sp_psi<<<(unsigned)s.nb, kSB, 0, c.stream>>>(c.at<float>(s.pot), c.at<float>(s.lw), s.cnt,
                                                    l_over_eps, c.at<float4>(s.scr),
-                                                   c.at<float>(s.pmax), c.at<float>(s.a0));
+                                                   c.at<float>(s.pmax), c.at<float>(s.a0),
+                                                   c.at<float4>(s.lin));
     count_launch();
     FS_CUDA(cudaGetLastError());
     return FS_OK;
@@ -1102,6 +1187,8 @@ fs_status screen(Call& c, const SpBufs& B, const SpSide& o, const SpSide& in, fl
     s.ext_i = c.at<float4>(in.ext);
     s.a0_o = c.at<float>(o.a0);
     s.a0_i = c.at<float>(in.a0);
+    s.lin_o = c.at<float4>(o.lin);
+    s.lin_i = c.at<float4>(in.lin);
     s.lw2_o = c.at<float>(o.lW);
     s.cnt_o = o.cnt;
     s.cnt_i = in.cnt;
