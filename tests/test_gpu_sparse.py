@@ -174,6 +174,40 @@ def test_reference_offsets_with_fixups_match_oracle(online_iters):
     assert max_abs(np64(g), gr) <= tol
 
 
+def test_screened_solve_with_lognormal_weights_matches_oracle():
+    """Non-uniform weights: block weights, and with them the per-block
+    thresholds, vary across the blocks."""
+    inp = random_cloud(2600, 2300, 2, seed=77, spread=0.3, weights="lognormal")
+    eps, tau = 0.003, 1e-5
+    t = to_dev(inp)
+    f, g, rep = fs.fs_sparse_solve(t["X"], t["a"], t["Y"], t["b"], eps, coarse_iters=15,
+                                   max_iters=20, tau=tau)
+    fr, gr, orep = bsp.solve(inp["X"], inp["a"], inp["Y"], inp["b"], eps, 15, 20, tau)
+    C = orc.cost(inp["X"], inp["Y"])
+    assert max_abs(np64(f), fr) <= F_TOL_FMA * C.max()
+    assert max_abs(np64(g), gr) <= F_TOL_FMA * C.max()
+    assert rep["kept_pairs"] < 0.9 * rep["passes"] * 2600 * 2300
+
+
+def test_degenerate_clouds():
+    """Every point of X at one place and every point of Y at another: the
+    bounding box has zero extent on every axis (all Morton codes equal, the
+    order is the identity) and the blocks have zero extents."""
+    X = np.tile(np.array([[0.25, -0.5, 1.0]], np.float32), (300, 1))
+    Y = np.tile(np.array([[0.75, 0.5, 0.0]], np.float32), (200, 1))
+    inp = dict(X=X, Y=Y, a=np.full(300, 1 / 300, np.float32), b=np.full(200, 1 / 200, np.float32))
+    t = to_dev(inp)
+    px, py = fs.fs_morton_order(t["X"], t["Y"])
+    np.testing.assert_array_equal(px.cpu().numpy(), np.arange(300))
+    np.testing.assert_array_equal(py.cpu().numpy(), np.arange(200))
+    f, g, rep = fs.fs_sparse_solve(t["X"], t["a"], t["Y"], t["b"], 0.05, coarse_iters=3,
+                                   max_iters=4, tau=1e-6)
+    fr, gr, _ = bsp.solve(X, inp["a"], Y, inp["b"], 0.05, 3, 4, 1e-6)
+    C = orc.cost(X, Y)
+    assert max_abs(np64(f), fr) <= F_TOL_FMA * C.max()
+    assert max_abs(np64(g), gr) <= F_TOL_FMA * C.max()
+
+
 def test_coarse_stage_alone_matches_oracle():
     inp = make_inputs("c2_n10k_d3", n=3000, m=2700)
     t = to_dev(inp)
