@@ -19,7 +19,7 @@ import pytest
 import oracle as orc
 import oracle.block_sparse as bsp
 from streaming_sinkhorn_solver_gb300 import binding as fs
-from streaming_sinkhorn_solver_gb300.workloads import make_inputs, random_cloud
+from streaming_sinkhorn_solver_gb300.workloads import WORKLOADS, make_inputs, random_cloud
 from tests.gpu_util import F_TOL_FMA, max_abs, np64, to_dev
 
 pytestmark = pytest.mark.gpu
@@ -278,28 +278,35 @@ def test_invalid_arguments_are_rejected():
         assert e.value.status == fs.FS_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("n,eps,iters", [(400_000, 0.002, 12)])
-def test_full_size_column_marginals_within_the_screening_bound(n, eps, iters):
-    """At the returned potentials (after a g-update) every dense column
-    marginal c_j lies in [b_j, b_j + tau W_J]: the kept blocks carry exactly
-    b_j and the skipped ones at most tau W_J.  Checked on sampled columns
-    with the oracle's dense single-row update."""
-    tau = 1e-4
-    inp = make_inputs("c2_n10k_d3", n=n, m=n)
+def test_full_size_column_marginals_within_the_screening_bound():
+    """The benchmark's block-sparse workload in its launch configuration
+    (n = m = 10^6, d = 3, the workload's eps, centroid iterations, fine
+    iterations and tau): at the returned potentials (after a g-update) every
+    dense column marginal c_j lies in [b_j, b_j + tau W_J] up to float32
+    rounding -- the kept blocks carry exactly b_j and the skipped ones at
+    most tau W_J.  Checked on sampled columns with the oracle's dense
+    single-row update, which sees every column pair, kept or not."""
+    w = WORKLOADS["bs_n1m_d3"]
+    eps, iters = w.stages[0]
+    tau = w.tau
+    n = w.n
+    inp = make_inputs(w.name)
     t = to_dev(inp)
-    f, g, rep = fs.fs_sparse_solve(t["X"], t["a"], t["Y"], t["b"], eps, coarse_iters=30,
+    f, g, rep = fs.fs_sparse_solve(t["X"], t["a"], t["Y"], t["b"], eps, coarse_iters=w.coarse_iters,
                                    max_iters=iters, tau=tau)
-    assert rep["kept_pairs"] < 0.5 * rep["passes"] * n * n
+    assert rep["iters"] == iters
+    assert rep["kept_pairs"] < 0.2 * rep["passes"] * n * w.m
     f64, g64 = np64(f), np64(g)
     px, py = bsp.morton_order(inp["X"], inp["Y"])
     _, wy = bsp.block_stats(inp["Y"][py], inp["b"][py])
-    block_of = np.empty(n, dtype=np.int64)
-    block_of[py] = np.arange(n) // bsp.BLOCK
-    cols = np.linspace(0, n - 1, 48).astype(np.int64)
+    block_of = np.empty(w.m, dtype=np.int64)
+    block_of[py] = np.arange(w.m) // bsp.BLOCK
+    cols = np.linspace(0, w.m - 1, 48).astype(np.int64)
     # g-update of column j from f (roles swapped): c_j / b_j = exp((g_j - g_upd_j) / eps)
     g_upd = orc.f_update_rows(inp["Y"], inp["X"], inp["a"], eps, f64, cols)
     c = inp["b"][cols].astype(np.float64) * np.exp((g64[cols] - g_upd) / orc.as_eps(eps))
     b = inp["b"][cols].astype(np.float64)
-    # float32 rounding of g (|g| <= 3, eps = 0.002) moves c_j by < 1e-4 relative
-    assert np.all(c >= b * (1 - 3e-4))
-    assert np.all(c <= b * (1 + 3e-4) + tau * wy[block_of[cols]])
+    # float32 rounding of g (|g| <= 3, eps = 1e-3: < 1.2e-4 relative in c_j) and of the
+    # scores (|kappa x~.y~| up to ~2e3 log2 units: ~2e-4) stay below 1e-3
+    assert np.all(c >= b * (1 - 1e-3))
+    assert np.all(c <= b * (1 + 1e-3) + tau * wy[block_of[cols]])
