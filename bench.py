@@ -75,10 +75,10 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, tag: str = ""):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}{tag}.csv")
 
     def start(self):
         try:
@@ -286,6 +286,114 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def _dense_roofline(w, path, half_ms, half_n, rates, clocks, sms):
+    """Roofline of the dense half-update from its own events.  Per launch (one
+    f- or g-update) the algorithmic work is n*m score pairs: 2 n m d tensor
+    flops (tensor path), n m exponentials with d + 2 (FMA path) or 2 (tensor
+    path) FP32 lane-ops each, and the streamed operand bytes; the binding term
+    is the largest of the three times."""
+    n, m, d = w.n, w.m, w.d
+    peaks = _peaks()
+    tensor_path = (path == "tensor") or (path == "auto" and d > 16)
+    avg_half_ms = half_ms / max(half_n, 1)
+    t_launch = avg_half_ms * 1e-3
+    pairs_per_half = n * m
+    clk = (clocks or {}).get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
+    ex2_clk = rates.get("ex2_per_clk_sm") or EX2_PER_CLK_SM
+    fp32_clk = rates.get("fma2_lanes_per_clk_sm") or FP32_LANES_PER_CLK_SM
+    rate_src = "measured by fs_unit_rates" if "ex2_per_clk_sm" in rates else "nominal"
+    ex2_peak = ex2_clk * sms * clk * 1e6                               # ex2 / s
+    fp32_ops = fp32_ops_per_pair(d, tensor_path)
+    fp32_pair_peak = fp32_clk / fp32_ops * sms * clk * 1e6             # pairs / s
+    tflops_peak = float(peaks["bf16_tflops_sustained"])
+    hbm_peak = float(peaks["hbm_gbs"])
+    op_bytes = 2 if tensor_path else 4
+    alg_bytes = op_bytes * (n + m) * d + 4 * 3 * (n + m)                # operands + biases/outputs
+    alu_peak = min(ex2_peak, fp32_pair_peak)                           # pairs / s
+    terms = {"alu_s": pairs_per_half / alu_peak, "hbm_s": alg_bytes / (hbm_peak * 1e9)}
+    if tensor_path:
+        terms["tensor_s"] = 2.0 * pairs_per_half * d / (tflops_peak * 1e12)
+    bound = max(terms, key=terms.get)[:-2]
+    if bound == "tensor":
+        achieved = 2.0 * pairs_per_half * d / t_launch / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tflops_peak, "unit": "TFLOP/s",
+                "peak_source": f"{peaks['source']} bf16 dense sustained; f16 operands have the "
+                               f"same nominal rate"}
+    elif bound == "alu":
+        achieved = pairs_per_half / t_launch / 1e9
+        per_clk = min(ex2_clk, fp32_clk / fp32_ops)
+        roof = {"bound": "alu", "achieved": achieved, "peak": alu_peak / 1e9, "unit": "Gpair/s",
+                "peak_source": f"derived: min(MUFU {ex2_clk:.1f} ex2/clk/SM, FP32 "
+                               f"{fp32_clk:.1f} lanes/clk/SM / {fp32_ops} lane-ops per "
+                               f"pair) = {per_clk:.1f} pairs/clk/SM ({rate_src}) x {sms} SMs x "
+                               f"{clk:.0f} MHz (median SM clock sampled in the timed region)",
+                "mufu_frac": achieved * 1e9 / ex2_peak,
+                "fp32_frac": achieved * 1e9 / fp32_pair_peak}
+    else:
+        achieved = alg_bytes / t_launch / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "peak_source": f"{peaks['source']} copy bandwidth"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = _traffic_from_profiles(w.name, kernel_family(d, tensor_path))
+    roof["kernel"] = "half_update"
+    roof["avg_launch_ms"] = avg_half_ms
+    roof["launches"] = half_n
+    roof["roofline_ms"] = {k[:-2]: v * 1e3 for k, v in terms.items()}
+    roof["algorithmic_bytes_per_launch"] = alg_bytes
+    roof["unit_rates"] = dict(rates, source=rate_src)
+    return roof
+
+
+# The metric's other points (n = m = 50k at d = 3 and d = 64), measured after
+# the timed region of the default workload (d = 512) in the same process.
+METRIC_POINTS = ("c2_n50k_d3", "c3_n50k_d64")
+
+
+def _metric_point(fs, name, dev, rates, path, steps=3, warmup=3):
+    """One more workload of the metric, timed like the main one (warm-up,
+    CUDA events around each step on the launching stream, a 256 MB write
+    between steps, the half-update's own events for the roofline)."""
+    import torch
+    w = WORKLOADS[name]
+    n, m, d = w.n, w.m, w.d
+    inp = make_inputs(w.name)
+    t = {k: torch.from_numpy(v).to(dev) for k, v in inp.items()}
+    t["f"] = torch.empty(n, device=dev)
+    t["g0"] = torch.zeros(m, device=dev)
+    t["out"] = torch.empty(n, w.k if w.apply == "pv" else d, device=dev) if w.apply else None
+    step = _step_fn(fs, w, t, path)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index, tag=f"_{name}")
+    sampler.start()
+    fs.fs_timing_read()
+    fs.fs_timing_enable(True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for s_ in range(steps):
+        flush.fill_(float(s_))
+        ev[s_][0].record(stream)
+        step()
+        ev[s_][1].record(stream)
+    torch.cuda.synchronize()
+    fs.fs_timing_enable(False)
+    (half_ms, _, _), (half_n, _, _) = fs.fs_timing_read()
+    clocks = sampler.stop()
+    total_ms = sum(a.elapsed_time(b) for a, b in ev)
+    iters, pairs = _work(w, n, m, d)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    roof = _dense_roofline(w, path, half_ms, half_n, rates, clocks, sms)
+    keep = ("bound", "achieved", "peak", "unit", "frac", "mufu_frac", "fp32_frac", "traffic",
+            "avg_launch_ms", "launches")
+    return {"workload": name, "n": n, "m": m, "d": d, "steps": steps, "warmup": warmup,
+            "value": pairs * steps / (total_ms * 1e-3), "unit": "score-pairs/s",
+            "iters_per_s": iters * steps / (total_ms * 1e-3), "ms_per_step": total_ms / steps,
+            "roofline": {k: roof[k] for k in keep if k in roof}, "clocks": clocks}
+
+
 def run_gb300(args, w):
     import torch
     from streaming_sinkhorn_solver_gb300 import binding as fs
@@ -346,59 +454,9 @@ def run_gb300(args, w):
     value = aggregate_rate(world, pairs, args.steps, total_ms)
     iters_per_s = aggregate_rate(world, iters, args.steps, total_ms)
 
-    # roofline of the dominant kernel (the half-update), from its own events.
-    # Per launch (one f- or g-update) the algorithmic work is n*m score pairs:
-    # 2 n m d tensor flops (tensor path), n m exponentials, and the streamed
-    # operand bytes; the binding term is the largest of the three times.
-    peaks = _peaks()
-    tensor_path = (path == "tensor") or (path == "auto" and d > 16)
-    avg_half_ms = half_ms / max(half_n, 1)
-    t_launch = avg_half_ms * 1e-3
-    pairs_per_half = n * m
-    clk = (clocks or {}).get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    ex2_clk = rates.get("ex2_per_clk_sm") or EX2_PER_CLK_SM
-    fp32_clk = rates.get("fma2_lanes_per_clk_sm") or FP32_LANES_PER_CLK_SM
-    rate_src = "measured by fs_unit_rates" if "ex2_per_clk_sm" in rates else "nominal"
-    ex2_peak = ex2_clk * sms * clk * 1e6                               # ex2 / s
-    fp32_ops = fp32_ops_per_pair(d, tensor_path)
-    fp32_pair_peak = fp32_clk / fp32_ops * sms * clk * 1e6             # pairs / s
-    tflops_peak = float(peaks["bf16_tflops_sustained"])
-    hbm_peak = float(peaks["hbm_gbs"])
-    op_bytes = 2 if tensor_path else 4
-    alg_bytes = op_bytes * (n + m) * d + 4 * 3 * (n + m)                # operands + biases/outputs
-    alu_peak = min(ex2_peak, fp32_pair_peak)                           # pairs / s
-    terms = {"alu_s": pairs_per_half / alu_peak, "hbm_s": alg_bytes / (hbm_peak * 1e9)}
-    if tensor_path:
-        terms["tensor_s"] = 2.0 * pairs_per_half * d / (tflops_peak * 1e12)
-    bound = max(terms, key=terms.get)[:-2]
-    if bound == "tensor":
-        achieved = 2.0 * pairs_per_half * d / t_launch / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": tflops_peak, "unit": "TFLOP/s",
-                "peak_source": f"{peaks['source']} bf16 dense sustained; f16 operands have the "
-                               f"same nominal rate"}
-    elif bound == "alu":
-        achieved = pairs_per_half / t_launch / 1e9
-        per_clk = min(ex2_clk, fp32_clk / fp32_ops)
-        roof = {"bound": "alu", "achieved": achieved, "peak": alu_peak / 1e9, "unit": "Gpair/s",
-                "peak_source": f"derived: min(MUFU {ex2_clk:.1f} ex2/clk/SM, FP32 "
-                               f"{fp32_clk:.1f} lanes/clk/SM / {fp32_ops} lane-ops per "
-                               f"pair) = {per_clk:.1f} pairs/clk/SM ({rate_src}) x {sms} SMs x "
-                               f"{clk:.0f} MHz (median SM clock sampled in the timed region)",
-                "mufu_frac": achieved * 1e9 / ex2_peak,
-                "fp32_frac": achieved * 1e9 / fp32_pair_peak}
-    else:
-        achieved = alg_bytes / t_launch / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "peak_source": f"{peaks['source']} copy bandwidth"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = _traffic_from_profiles(w.name, kernel_family(d, tensor_path))
-    roof["kernel"] = "half_update"
-    roof["avg_launch_ms"] = avg_half_ms
-    roof["launches"] = half_n
-    roof["roofline_ms"] = {k[:-2]: v * 1e3 for k, v in terms.items()}
-    roof["algorithmic_bytes_per_launch"] = alg_bytes
-    roof["unit_rates"] = dict(rates, source=rate_src)
+    tensor_path = (path == "tensor") or (path == "auto" and d > 16)
+    roof = _dense_roofline(w, path, half_ms, half_n, rates, clocks, sms)
 
     line = {"metric": METRIC, "value": value, "unit": "score-pairs/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
@@ -417,6 +475,17 @@ def run_gb300(args, w):
             "workspace_bytes": int(max(fs.fs_workspace_bytes(n, m, d, 0, path=path),
                                        fs.fs_workspace_bytes(n, m, d, k_out, path=path)
                                        if w.apply else 0))}
+
+    if world == 1 and w.name == DEFAULT_WORKLOAD and not args.no_points:
+        line["metric_points"] = {w.name: {
+            "workload": w.name, "n": n, "m": m, "d": d, "value": line["value"],
+            "unit": "score-pairs/s", "iters_per_s": line["iters_per_s"],
+            "ms_per_step": line["ms_per_step"],
+            "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac",
+                                               "traffic", "avg_launch_ms", "launches")},
+            "note": "the main measurement of this line"}}
+        for name in METRIC_POINTS:
+            line["metric_points"][name] = _metric_point(fs, name, dev, rates, path)
 
     # end to end through the C ABI with pinned host buffers
     if not args.no_e2e:
@@ -609,6 +678,8 @@ def main():
     ap.add_argument("--path", choices=["auto", "fma", "tensor"], default="auto")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-points", action="store_true",
+                    help="skip the metric's d = 3 and d = 64 points after the default workload")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=64)
     args = ap.parse_args()
