@@ -407,6 +407,18 @@ fs_status fs_sparse_screen(const float* X, const float* a, int64_t n,
                            const float* f, const float* g, float tau, int32_t side,
                            int32_t* counts, int32_t* lists, void* stream);
 
+/*
+ * fs_wait_selftest -- failure-detection self-test (no counterpart on the
+ * pages).  Every wait of the tensor-core kernels gives up after a deadline,
+ * sets a bit in the device error word and lets its kernel return, so a lost
+ * arrival surfaces as FS_ERR_TIMEOUT from fs_check() instead of a hung GPU.
+ * This call launches that same bounded wait on an mbarrier that nothing
+ * signals, with a deadline of timeout_ns (1e3 .. 1e9 ns), on `stream`; the
+ * next fs_check() then returns FS_ERR_TIMEOUT (and clears the word), and the
+ * context stays usable.  FS_ERR_INVALID_ARG for a deadline out of range.
+ */
+fs_status fs_wait_selftest(int64_t timeout_ns, void* stream);
+
 /* Device bytes the library's workspace needs for these sizes (k = 0 for a
  * solve).  The workspace is O((n + m) d): no n x m buffer exists. */
 int64_t fs_workspace_bytes(int64_t n, int64_t m, int32_t d, int32_t k, const fs_options* opt);

@@ -33,7 +33,7 @@ EXPORTED = ("fs_sinkhorn_solve", "fs_apply_plan", "fs_barycentric", "fs_grad_x",
             "fs_marginal_residuals", "fs_workspace_bytes", "fs_check", "fs_release",
             "fs_last_error", "fs_version", "fs_launch_count", "fs_timing_enable",
             "fs_timing_read", "fs_sinkhorn_solve_noalloc", "fs_unit_rates", "fs_hvp_x",
-            "fs_sparse_solve", "fs_morton_order", "fs_sparse_screen")
+            "fs_sparse_solve", "fs_morton_order", "fs_sparse_screen", "fs_wait_selftest")
 
 
 class FlashSinkhornError(RuntimeError):
@@ -123,6 +123,8 @@ def load_library(path: Optional[str] = None):
         lib.fs_sparse_screen.argtypes = [vp, vp, i64, vp, vp, i64, i32, f32, vp, vp, f32, i32,
                                          vp, vp, vp]
         lib.fs_sparse_screen.restype = ctypes.c_int
+        lib.fs_wait_selftest.argtypes = [i64, vp]
+        lib.fs_wait_selftest.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -495,3 +497,9 @@ def fs_sparse_screen(X, a, Y, b, eps: float, f, g, tau: float, side: int, *, str
         _stream(stream, X))
     _raise(st)
     return counts, lists
+
+
+def fs_wait_selftest(timeout_ns: int = 1_000_000, *, stream=None) -> None:
+    """Run the library's bounded device wait on a barrier nothing signals
+    (see the C header); the next fs_check() raises FS_ERR_TIMEOUT."""
+    _raise(load_library().fs_wait_selftest(int(timeout_ns), _stream(stream)))

@@ -126,6 +126,7 @@ fs_status solve_fma(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) 
     auto half = [&](HalfArgs& h, int splits, int64_t nr, const float* rnorm, const float* rlogw2,
                     float* pot, float* packed, bool ref) -> fs_status {
         h.use_ref = ref ? 1 : 0;
+        NvtxRange nvtx(h.rows == PX ? "fs f-update (FMA)" : "fs g-update (FMA)");
         const int ts = timing_begin(c.stream);
         FS_CUDA(launch_half_fma(p.D, h, c.stream));
         timing_end(ts, TIME_HALF, c.stream);
@@ -197,6 +198,7 @@ fs_status apply_fma(Call& c, Problem& P, int mode, const fs_options* opt) {
     A.splits = splits;
     A.cols_per_split = cps;
     A.mode = mode;
+    NvtxRange nvtx("fs plan application (FMA)");
     const int ts = timing_begin(c.stream);
     FS_CUDA(launch_apply_fma(p.D, A, c.stream));
     timing_end(ts, TIME_APPLY, c.stream);

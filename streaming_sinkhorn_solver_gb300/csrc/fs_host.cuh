@@ -5,6 +5,8 @@
 #include "flashsinkhorn.h"
 #include "fs_internal.cuh"
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <mutex>
 #include <vector>
 #include <string>
@@ -84,6 +86,16 @@ void bind(Call& c, Arr& a);
 fs_status upload(Call& c, const Arr& a);
 fs_status download(Call& c, const Arr& a);
 fs_status scan_finite(Call& c, const float* v, int64_t len, unsigned int* counter);
+
+// A named NVTX range over the enqueueing of one phase (a half-update, a plan
+// application, a screening...), so profiler timelines show the phases by name;
+// NVTX is header-only and inert unless a profiling tool is attached.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Kernel timing (fs_timing_enable / fs_timing_read).  timing_begin returns a
 // slot (or -1 when timing is off); timing_end closes it.

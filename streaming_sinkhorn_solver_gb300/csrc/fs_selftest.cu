@@ -1,0 +1,59 @@
+// Failure-detection self-test of the bounded device waits.
+//
+// Every wait of the tensor-core kernels (producer, MMA issuer and epilogue
+// roles on their mbarriers) gives up after a deadline, sets a bit in the
+// device error word and unwinds, so a lost arrival becomes FS_ERR_TIMEOUT
+// from fs_check() instead of a hung GPU.  This entry runs that same wait loop
+// on a freshly initialised mbarrier whose phase nothing completes, with a
+// short deadline chosen by the caller, so the path can be tested without
+// faulting or hanging anything: the kernel returns after the deadline and
+// the context stays usable.
+#include "fs_host.cuh"
+#include "fs_tc.cuh"
+
+namespace fs {
+namespace {
+
+// The error word bit this self-test sets (apart from the kernels' own bits).
+constexpr uint32_t ERR_TIMEOUT_SELFTEST = 8u;
+
+__global__ void k_wait_selftest(uint32_t* err, uint64_t timeout_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&bar, 1);
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // phase 0 of a barrier that expects one arrival nobody makes
+        uint32_t ok;
+        asm volatile(FS_MBAR_WAIT_PTX("")
+                     : "=r"(ok)
+                     : "r"(tc::smem_u32(&bar)), "r"(0u), "l"(timeout_ns), "r"(tc::kSuspendHintNs)
+                     : "memory");
+        if (!ok) atomicOr(err, ERR_TIMEOUT_SELFTEST);
+    }
+}
+
+fs_status selftest_entry(int64_t timeout_ns, void* stream) {
+    if (timeout_ns < 1000 || timeout_ns > 1000000000)
+        return fail(FS_ERR_INVALID_ARG, "timeout_ns=%lld must be in [1e3, 1e9]", (long long)timeout_ns);
+    Call c;
+    FS_TRY(begin_call(c, stream));
+    if (c.capturing) return fail(FS_ERR_UNSUPPORTED, "not inside a graph capture");
+    k_wait_selftest<<<1, 32, 0, c.stream>>>(c.ws->err_word, (uint64_t)timeout_ns);
+    count_launch();
+    FS_CUDA(cudaGetLastError());
+    return end_call(c);
+}
+
+}  // namespace
+}  // namespace fs
+
+extern "C" fs_status fs_wait_selftest(int64_t timeout_ns, void* stream) {
+    try {
+        return fs::selftest_entry(timeout_ns, stream);
+    } catch (...) {
+        return fs::fail(FS_ERR_CUDA, "unexpected host exception");
+    }
+}

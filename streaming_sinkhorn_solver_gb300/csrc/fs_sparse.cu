@@ -1199,6 +1199,7 @@ fs_status screen(Call& c, const SpBufs& B, const SpSide& o, const SpSide& in, fl
     s.log2_tau = tau > 0.f ? (float)std::log2((double)tau) : -INFINITY;
     s.lists = c.at<int>(B.lists);
     s.counts = c.at<int>(B.counts);
+    NvtxRange nvtx("fs screening (block-sparse)");
     k_sp_screen<<<(unsigned)o.nb, 256, 0, c.stream>>>(s);
     count_launch();
     FS_CUDA(cudaGetLastError());
@@ -1231,6 +1232,8 @@ fs_status sparse_half(Call& c, const SpBufs& B, const SpSide& o, const SpSide& i
     while ((in.nb >> shift) >= 1024) ++shift;
     k_sp_order<<<1, 1024, 0, c.stream>>>(h.counts, (int)o.nb, shift, c.at<int>(B.order));
     count_launch();
+    NvtxRange nvtx(measure ? "fs residual pass (block-sparse)"
+                         : o.rec == B.X.rec ? "fs f-update (block-sparse)" : "fs g-update (block-sparse)");
     const int ts = measure ? -1 : timing_begin(c.stream);
     if (D == 2) {
         if (ref) k_sp_half<2, true><<<(unsigned)o.nb, 256, 0, c.stream>>>(h);
@@ -1267,6 +1270,7 @@ fs_status measure_residual(Call& c, const SpBufs& B, int D, float eps, float tau
 // Coarse stage: dense Sinkhorn between the block centroids (FMA path,
 // online offsets), then the lift into the sorted potentials.
 fs_status coarse_stage(Call& c, SpBufs& B, int d, float eps, int iters) {
+    NvtxRange nvtx("fs coarse stage (block-sparse)");
     const int D = fma_pad_dim(d);
     const int DS = fma_stride(D);
     const int64_t nx = B.X.nb, ny = B.Y.nb;

@@ -247,6 +247,7 @@ fs_status solve_tc(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) {
                     const TensorMap128& tk, int64_t row_tiles, int splits, int64_t nr, float* pot,
                     bool ref) -> fs_status {
         h.use_ref = ref ? 1 : 0;
+        NvtxRange nvtx(pot == P.f.dev ? "fs f-update (tensor)" : "fs g-update (tensor)");
         const int ts = timing_begin(c.stream);
         FS_CUDA(p.pair ? launch_half_pair(h, tq, tk, (int)row_tiles, p.qres, c.stream)
                        : launch_half_tc(h, (int)row_tiles, p.qres, c.stream));
@@ -361,6 +362,7 @@ fs_status apply_tc(Call& c, Problem& P, int mode, const fs_options* opt) {
     ap.out = P.out.dev;
     ap.partial = A.splits > 1 ? c.at<float>(A.partial) : nullptr;
     ap.err = c.ws->err_word;
+    NvtxRange nvtx("fs plan application (tensor)");
     const int ts = timing_begin(c.stream);
     FS_CUDA(launch_apply_tc(ap, (int)p.rtx, c.stream));
     timing_end(ts, TIME_APPLY, c.stream);
