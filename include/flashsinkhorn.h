@@ -419,6 +419,18 @@ fs_status fs_sparse_screen(const float* X, const float* a, int64_t n,
  */
 fs_status fs_wait_selftest(int64_t timeout_ns, void* stream);
 
+/*
+ * fs_debug_bounds -- bounds-check report (no counterpart on the pages).  A
+ * debug build of the library (built with FS_DEBUG_BOUNDS:
+ * libflashsinkhorn_dbg.so) checks the global-memory indices of its FMA,
+ * preparation and block-sparse kernels; an index outside its buffer is
+ * recorded and the access skipped instead of faulting.  *enabled (host) is 1
+ * in such a build, 0 otherwise; *first_violation (host) receives the first
+ * recorded violation, (site << 48) | index, or 0, and the record is cleared.
+ * Synchronises the device.
+ */
+fs_status fs_debug_bounds(int32_t* enabled, uint64_t* first_violation);
+
 /* Device bytes the library's workspace needs for these sizes (k = 0 for a
  * solve).  The workspace is O((n + m) d): no n x m buffer exists. */
 int64_t fs_workspace_bytes(int64_t n, int64_t m, int32_t d, int32_t k, const fs_options* opt);

@@ -21,6 +21,8 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libflashsinkhorn.so")
+# debug build with global-memory index checks (build(debug_bounds=True))
+DEBUG_LIB_PATH = os.path.join(_HERE, "libflashsinkhorn_dbg.so")
 
 FS_OK, FS_ERR_INVALID_ARG, FS_ERR_CUDA, FS_ERR_OOM = 0, 1, 2, 3
 FS_ERR_NONFINITE, FS_ERR_TIMEOUT, FS_ERR_UNSUPPORTED = 4, 5, 6
@@ -33,7 +35,8 @@ EXPORTED = ("fs_sinkhorn_solve", "fs_apply_plan", "fs_barycentric", "fs_grad_x",
             "fs_marginal_residuals", "fs_workspace_bytes", "fs_check", "fs_release",
             "fs_last_error", "fs_version", "fs_launch_count", "fs_timing_enable",
             "fs_timing_read", "fs_sinkhorn_solve_noalloc", "fs_unit_rates", "fs_hvp_x",
-            "fs_sparse_solve", "fs_morton_order", "fs_sparse_screen", "fs_wait_selftest")
+            "fs_sparse_solve", "fs_morton_order", "fs_sparse_screen", "fs_wait_selftest",
+            "fs_debug_bounds")
 
 
 class FlashSinkhornError(RuntimeError):
@@ -125,6 +128,8 @@ def load_library(path: Optional[str] = None):
         lib.fs_sparse_screen.restype = ctypes.c_int
         lib.fs_wait_selftest.argtypes = [i64, vp]
         lib.fs_wait_selftest.restype = ctypes.c_int
+        lib.fs_debug_bounds.argtypes = [ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_uint64)]
+        lib.fs_debug_bounds.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib

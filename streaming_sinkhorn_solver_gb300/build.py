@@ -5,7 +5,7 @@ parallel, then linked into ``streaming_sinkhorn_solver_gb300/libflashsinkhorn.so
 Objects go to ``streaming_sinkhorn_solver_gb300/_build/``.  A unit is rebuilt
 when it or any header it may include is newer than its object.
 
-    python -m streaming_sinkhorn_solver_gb300.build [--force] [--verbose]
+    python -m streaming_sinkhorn_solver_gb300.build [--force] [--verbose] [--debug-bounds]
 """
 from __future__ import annotations
 
@@ -22,6 +22,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libflashsinkhorn.so")
+# debug build: global-memory index checks of the FMA, prep and block-sparse
+# kernels (-DFS_DEBUG_BOUNDS), reported by fs_debug_bounds()
+OUT_DBG = os.path.join(PKG, "_build_dbg")
+LIB_DBG = os.path.join(PKG, "libflashsinkhorn_dbg.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
@@ -46,15 +50,17 @@ def _stale(src: str, obj: str, newest_header: float) -> bool:
     return os.path.getmtime(src) > t or newest_header > t
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    os.makedirs(OUT, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=None,
+          debug_bounds: bool = False) -> str:
+    out_dir, lib_path = (OUT_DBG, LIB_DBG) if debug_bounds else (OUT, LIB)
+    os.makedirs(out_dir, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     hdrs = _headers()
     newest = max((os.path.getmtime(h) for h in hdrs), default=0.0)
-    flags = NVCC_FLAGS + list(extra_flags or [])
+    flags = NVCC_FLAGS + list(extra_flags or []) + (["-DFS_DEBUG_BOUNDS"] if debug_bounds else [])
     jobs = []
     for src in sources:
-        obj = os.path.join(OUT, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         if force or _stale(src, obj, newest):
             jobs.append((src, obj))
 
@@ -72,16 +78,16 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     if jobs:
         with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
             list(ex.map(compile_one, jobs))
-    objs = [os.path.join(OUT, os.path.basename(s)[:-3] + ".o") for s in sources]
-    if force or jobs or not os.path.exists(LIB) or any(
-            os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    objs = [os.path.join(out_dir, os.path.basename(s)[:-3] + ".o") for s in sources]
+    if force or jobs or not os.path.exists(lib_path) or any(
+            os.path.getmtime(o) > os.path.getmtime(lib_path) for o in objs):
+        tmp = lib_path + f".tmp{os.getpid()}"
         cmd = [nvcc()] + ARCH + ["-shared", "-Xcompiler", "-fPIC", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 def main():
@@ -89,10 +95,12 @@ def main():
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true")
     ap.add_argument("--ptxas-info", action="store_true", help="print register/spill report")
+    ap.add_argument("--debug-bounds", action="store_true",
+                    help="build libflashsinkhorn_dbg.so with global-memory index checks")
     args = ap.parse_args()
     extra = ["-Xptxas", "-v"] if args.ptxas_info else []
     print(build(force=args.force or args.ptxas_info, verbose=args.verbose or args.ptxas_info,
-                extra_flags=extra))
+                extra_flags=extra, debug_bounds=args.debug_bounds))
 
 
 if __name__ == "__main__":

@@ -11,6 +11,7 @@
 // (MUFU ex2) and FP32 issue rate bound this path, not memory or tensor cores.
 // Scores stay in base 2 (the factor 2 log2(e)/eps is folded into the row
 // operand once), so every pair costs exactly one ex2.
+#include "fs_debug.cuh"
 #include "fs_internal.cuh"
 
 namespace fs {
@@ -198,7 +199,8 @@ __global__ void __launch_bounds__(kThreads, D <= 8 ? 3 : 2) k_half_fma(HalfArgs 
         // stage (coordinates, bias) records, each value written twice
         for (int e = tid; e < ncol * (D + 1); e += kThreads) {
             const int jj = e / (D + 1), k = e - jj * (D + 1);
-            const float v = a.cols[(cb + jj) * DS + k];
+            const int64_t src = (cb + jj) * DS + k;
+            const float v = FS_IDX_OK(src, a.nc * DS, 1) ? a.cols[src] : 0.f;
             sf[jj * DD + 2 * k] = v;
             sf[jj * DD + 2 * k + 1] = v;
         }
@@ -226,7 +228,8 @@ __global__ void __launch_bounds__(kThreads, D <= 8 ? 3 : 2) k_half_fma(HalfArgs 
         const int64_t row = row0 + tid + i * kThreads;
         if (row >= a.nr) continue;
         if (a.splits > 1) {
-            a.partial[(int64_t)blockIdx.y * a.nr + row] = make_float2(M[i], Sf[i]);
+            const int64_t pi = (int64_t)blockIdx.y * a.nr + row;
+            if (FS_IDX_OK(pi, (int64_t)a.splits * a.nr, 2)) a.partial[pi] = make_float2(M[i], Sf[i]);
         } else {
             if (REF && !(Sf[i] >= kMinRefSum && Sf[i] <= kMaxRefSum)) push_fix(a, row);
             const float lse2 = M[i] + log2f(Sf[i]);
@@ -256,9 +259,12 @@ __global__ void k_merge_lse(const float2* __restrict__ partial, int splits, int6
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= nr) return;
     float M = -INFINITY;
-    for (int sp = 0; sp < splits; ++sp) M = fmaxf(M, partial[(int64_t)sp * nr + i].x);
+    for (int sp = 0; sp < splits; ++sp)
+        if (FS_IDX_OK((int64_t)sp * nr + i, (int64_t)splits * nr, 3))
+            M = fmaxf(M, partial[(int64_t)sp * nr + i].x);
     float S = 0.f;
     for (int sp = 0; sp < splits; ++sp) {
+        if (!FS_IDX_OK((int64_t)sp * nr + i, (int64_t)splits * nr, 3)) continue;
         const float2 p = partial[(int64_t)sp * nr + i];
         if (p.x != -INFINITY) S += p.y * ex2(p.x - M);   // a padding-only split adds nothing
     }
@@ -292,6 +298,7 @@ __global__ void __launch_bounds__(256) k_fix_fma(HalfArgs a) {
     const int warps = gridDim.x * (blockDim.x >> 5);
     for (unsigned int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < cnt; w += warps) {
         const int64_t row = a.fix_list[w];
+        if (!FS_IDX_OK(row, a.nr, 4)) continue;
         float q[D];
 #pragma unroll
         for (int k = 0; k < D; ++k) q[k] = a.rows[row * DS + k] * a.kappa;
@@ -374,10 +381,12 @@ __global__ void __launch_bounds__(kApplyThreads) k_apply_fma(ApplyArgs a) {
         const int ncol = (int)min((int64_t)kApplyChunk, c1 - cb);
         __syncthreads();
         const float4* src = reinterpret_cast<const float4*>(a.cols + cb * DS);
-        for (int e = tid; e < ncol * (DS / 4); e += kApplyThreads) sc[e] = src[e];
+        for (int e = tid; e < ncol * (DS / 4); e += kApplyThreads)
+            if (FS_IDX_OK(cb * (DS / 4) + e, a.m * (DS / 4), 5)) sc[e] = src[e];
         for (int e = tid; e < ncol * KC; e += kApplyThreads) {
             const int j = e / KC, c = e - j * KC;
-            sv[e] = c < kw ? a.V[(cb + j) * a.k + kc0 + c] : 0.f;
+            const int64_t vi = (cb + j) * a.k + kc0 + c;
+            sv[e] = c < kw && FS_IDX_OK(vi, a.m * (int64_t)a.k, 6) ? a.V[vi] : 0.f;
         }
         __syncthreads();
         for (int j = 0; j < ncol; ++j) {
@@ -400,8 +409,10 @@ __global__ void __launch_bounds__(kApplyThreads) k_apply_fma(ApplyArgs a) {
     if (row >= a.n) return;
     if (a.splits > 1) {
         const int64_t base = ((int64_t)blockIdx.y * a.n + row) * (a.k + 1);
-        if (blockIdx.z == 0) a.partial[base] = M;
-        for (int c = 0; c < kw; ++c) a.partial[base + 1 + kc0 + c] = O[c];
+        const int64_t plen = (int64_t)a.splits * a.n * (a.k + 1);
+        if (blockIdx.z == 0 && FS_IDX_OK(base, plen, 7)) a.partial[base] = M;
+        for (int c = 0; c < kw; ++c)
+            if (FS_IDX_OK(base + 1 + kc0 + c, plen, 7)) a.partial[base + 1 + kc0 + c] = O[c];
         return;
     }
     const float w = exp2f(a.phi[row] + M);
@@ -411,7 +422,7 @@ __global__ void __launch_bounds__(kApplyThreads) k_apply_fma(ApplyArgs a) {
         if (a.mode == APPLY_PV) o = a.a[row] * t;
         else if (a.mode == APPLY_BARY) o = t;
         else o = 2.f * a.a[row] * (a.X[row * a.d + kc0 + c] - t);
-        a.out[row * a.k + kc0 + c] = o;
+        if (FS_IDX_OK(row * a.k + kc0 + c, a.n * (int64_t)a.k, 8)) a.out[row * a.k + kc0 + c] = o;
     }
 }
 
@@ -521,6 +532,8 @@ cudaError_t launch_apply_fma(int D, const ApplyArgs& a, cudaStream_t s) {
         default: return cudaErrorInvalidValue;
     }
 }
+
+FS_BOUNDS_READER(bounds_take_fma)
 
 cudaError_t launch_merge_apply(const ApplyArgs& a, cudaStream_t s) {
     k_merge_apply<<<(unsigned)((a.n + 127) / 128), 128, 0, s>>>(a);

@@ -7,6 +7,7 @@
 // Y, so both clouds are centred on the mean of all n + m points before the
 // dot-product form is used; this keeps |x~|^2 and x~.y~ small and avoids the
 // cancellation the dot form would otherwise suffer for far-off clouds.
+#include "fs_debug.cuh"
 #include "fs_internal.cuh"
 
 namespace fs {
@@ -20,7 +21,8 @@ __global__ void k_colsum(const float* __restrict__ X, int64_t n, const float* __
     for (int k = threadIdx.x; k < d; k += blockDim.x) {
         double s = 0.0;
         for (int64_t r = r0; r < r1; ++r) {
-            const float v = r < n ? X[r * d + k] : Y[(r - n) * d + k];
+            const bool ok = r < n ? FS_IDX_OK(r * d + k, n * d, 20) : FS_IDX_OK((r - n) * d + k, m * d, 21);
+            const float v = !ok ? 0.f : r < n ? X[r * d + k] : Y[(r - n) * d + k];
             s += (double)v;
         }
         partial[(int64_t)blockIdx.x * d + k] = s;
@@ -104,6 +106,8 @@ cudaError_t launch_pack_fma(const float* P, const float* w, const float* pot, in
     count_launch();
     return cudaGetLastError();
 }
+
+FS_BOUNDS_READER(bounds_take_prep)
 
 __global__ void k_phi(const float* __restrict__ f, const float* __restrict__ norm, int64_t n,
                       float l_over_eps, float* __restrict__ phi) {

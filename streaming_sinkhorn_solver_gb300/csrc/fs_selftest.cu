@@ -8,6 +8,7 @@
 // short deadline chosen by the caller, so the path can be tested without
 // faulting or hanging anything: the kernel returns after the deadline and
 // the context stays usable.
+#include "fs_debug.cuh"
 #include "fs_host.cuh"
 #include "fs_tc.cuh"
 
@@ -53,6 +54,28 @@ fs_status selftest_entry(int64_t timeout_ns, void* stream) {
 extern "C" fs_status fs_wait_selftest(int64_t timeout_ns, void* stream) {
     try {
         return fs::selftest_entry(timeout_ns, stream);
+    } catch (...) {
+        return fs::fail(FS_ERR_CUDA, "unexpected host exception");
+    }
+}
+
+// Bounds-check report of a debug build (see fs_debug.cuh): the first
+// recorded violation over the instrumented translation units, then cleared.
+extern "C" fs_status fs_debug_bounds(int32_t* enabled, uint64_t* first_violation) {
+    try {
+        if (!enabled || !first_violation) return fs::fail(FS_ERR_INVALID_ARG, "null pointer");
+        *enabled = fs::kDebugBounds ? 1 : 0;
+        *first_violation = 0;
+        cudaError_t (*take[])(unsigned long long*) = {fs::bounds_take_fma, fs::bounds_take_prep,
+                                                      fs::bounds_take_sparse};
+        for (auto fn : take) {
+            unsigned long long w = 0;
+            const cudaError_t e = fn(&w);
+            if (e != cudaSuccess)
+                return fs::fail(FS_ERR_CUDA, "reading the bounds word: %s", cudaGetErrorString(e));
+            if (w && !*first_violation) *first_violation = w;
+        }
+        return FS_OK;
     } catch (...) {
         return fs::fail(FS_ERR_CUDA, "unexpected host exception");
     }

@@ -28,6 +28,7 @@
 // At d <= 3 a score is three fused multiply-adds, so the kept blocks run on
 // the FP32 pipe (packed f32x2) with one ex2 per pair, like the dense FMA path;
 // a tensor-core tile would spend most of its K = 16 on padding.
+#include "fs_debug.cuh"
 #include "fs_host.cuh"
 
 #include <algorithm>
@@ -195,8 +196,10 @@ __global__ void __launch_bounds__(256) k_radix_scatter(const uint64_t* __restric
         if (ok) pos = wh[warp][dg] + below;
         __syncwarp();
         if (ok) {
-            kout[pos] = k;
-            vout[pos] = vin[e];
+            if (FS_IDX_OK(pos, cnt, 30)) {
+                kout[pos] = k;
+                vout[pos] = vin[e];
+            }
             if (below == 0) wh[warp][dg] += __popc(peers);
         }
         __syncwarp();
@@ -217,6 +220,7 @@ __global__ void k_sp_gather(const float* __restrict__ P, const float* __restrict
     const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (k >= cnt) return;
     const int64_t p = perm[k];
+    if (!FS_IDX_OK(p, cnt, 31)) return;
     float v[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
     float nrm = 0.f;
     for (int q = 0; q < d; ++q) {
@@ -298,21 +302,21 @@ __global__ void __launch_bounds__(kSB) k_sp_offsets(const float4* __restrict__ x
 // Lift: every point takes its block's coarse potential.
 __global__ void k_sp_lift(const float* __restrict__ F, int64_t cnt, float* __restrict__ pot) {
     const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (k < cnt) pot[k] = F[k / kSB];
+    if (k < cnt) pot[k] = F[k / kSB];   // k / 128 < number of blocks
 }
 
 // pot_s[k] = pot[perm[k]]
 __global__ void k_sp_gather_pot(const float* __restrict__ pot, const int* __restrict__ perm,
                                 int64_t cnt, float* __restrict__ pot_s) {
     const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (k < cnt) pot_s[k] = pot[perm[k]];
+    if (k < cnt && FS_IDX_OK(perm[k], cnt, 32)) pot_s[k] = pot[perm[k]];
 }
 
 // pot[perm[k]] = pot_s[k]
 __global__ void k_sp_scatter_pot(const float* __restrict__ pot_s, const int* __restrict__ perm,
                                  int64_t cnt, float* __restrict__ pot) {
     const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (k < cnt) pot[perm[k]] = pot_s[k];
+    if (k < cnt && FS_IDX_OK(perm[k], cnt, 33)) pot[perm[k]] = pot_s[k];
 }
 
 __global__ void k_sp_perm64(const int* __restrict__ perm, int64_t cnt, int64_t* __restrict__ out) {
@@ -586,7 +590,7 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
             surv = ub + sig + kCullMargin >= T;
         }
         const int pos = compact_offset(surv, S, s_wcnt);
-        if (surv) row[pos] = J;
+        if (surv && FS_IDX_OK(pos, a.nbi, 34)) row[pos] = J;
         __syncthreads();
     }
 
@@ -598,7 +602,7 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
         for (int sv = warp; sv < S; sv += 8) {
             const int J = row[sv];
             const float u = bound_exact(a, own, co, pmo, J, lane);
-            if (lane == 0) row[a.nbi - 1 - sv] = __float_as_int(u);
+            if (lane == 0 && FS_IDX_OK(a.nbi - 1 - sv, a.nbi, 35)) row[a.nbi - 1 - sv] = __float_as_int(u);
         }
         __syncthreads();
         // 2b. first maximiser among them
@@ -654,7 +658,7 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
                     keep = (u + sig >= T) || J == bi;
                 }
                 const int pos = compact_offset(keep, base, s_wcnt);
-                if (keep) row[pos] = J;
+                if (keep && FS_IDX_OK(pos, a.nbi, 36)) row[pos] = J;
                 __syncthreads();
             }
             if (threadIdx.x == 0) a.counts[O] = base;
@@ -711,7 +715,7 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
             keep = (u + sig >= T) || J == bi;
         }
         const int pos = compact_offset(keep, base, s_wcnt);
-        if (keep) row[pos] = J;
+        if (keep && FS_IDX_OK(pos, a.nbi, 37)) row[pos] = J;
         __syncthreads();
     }
     if (threadIdx.x == 0) a.counts[O] = base;
@@ -798,6 +802,7 @@ __global__ void __launch_bounds__(256, 3) k_sp_half(SpHalfArgs a) {
     int64_t cols_done = 0;
     for (int e = warp; e < cnt; e += kSpWarps) {
         const int J = lst[e];
+        if (!FS_IDX_OK(J, a.nbi, 38)) continue;
         const int64_t c0 = (int64_t)J * kSB;
         const int ncol = (int)min((int64_t)kSB, a.nc - c0);
         cols_done += ncol;
@@ -805,7 +810,7 @@ __global__ void __launch_bounds__(256, 3) k_sp_half(SpHalfArgs a) {
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
             const int j = lane + 32 * t;
-            if (j < ncol) {
+            if (j < ncol && FS_IDX_OK(c0 + j, a.nc, 39)) {
                 const float4 v = cols4[c0 + j];
                 my[2 * j] = make_float4(v.x, v.x, v.y, v.y);
                 my[2 * j + 1] = make_float4(v.z, v.z, v.w, v.w);
@@ -938,6 +943,7 @@ __global__ void __launch_bounds__(256) k_sp_fix(SpHalfArgs a) {
     const int warps = gridDim.x * (blockDim.x >> 5);
     for (unsigned int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < cnt; w += warps) {
         const int64_t row = a.fix_list[w];
+        if (!FS_IDX_OK(row, a.nr, 40)) continue;
         const int64_t O = row / kSB;
         float q[D];
 #pragma unroll
@@ -946,6 +952,7 @@ __global__ void __launch_bounds__(256) k_sp_fix(SpHalfArgs a) {
         const int* lst = a.lists + O * a.nbi;
         const int nk = a.counts[O];
         for (int e = 0; e < nk; ++e) {
+            if (!FS_IDX_OK(lst[e], a.nbi, 41)) continue;
             const int64_t c0 = (int64_t)lst[e] * kSB;
             const int ncol = (int)min((int64_t)kSB, a.nc - c0);
             for (int j = lane; j < ncol; j += 32) {
@@ -1004,8 +1011,10 @@ __global__ void __launch_bounds__(1024) k_sp_order(const int* __restrict__ count
         }
     }
     __syncthreads();
-    for (int o = threadIdx.x; o < nbo; o += blockDim.x)
-        order[atomicAdd(&h[1023 - min(counts[o] >> shift, 1023)], 1)] = o;
+    for (int o = threadIdx.x; o < nbo; o += blockDim.x) {
+        const int pos = atomicAdd(&h[1023 - min(counts[o] >> shift, 1023)], 1);
+        if (FS_IDX_OK(pos, nbo, 42)) order[pos] = o;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -1510,6 +1519,9 @@ fs_status screen_entry(const float* X, const float* a, int64_t n, const float* Y
 }
 
 }  // namespace
+
+FS_BOUNDS_READER(bounds_take_sparse)
+
 }  // namespace fs
 
 using namespace fs;
