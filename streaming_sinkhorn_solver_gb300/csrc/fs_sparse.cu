@@ -334,11 +334,11 @@ __global__ void k_sp_bias(const float* __restrict__ pot_s, const float* __restri
 
 // psi_k = pot_k L/eps + log2 w_k for the screening: one 128-thread block per
 // point block stores psi - max into the record's w, the max per block,
-// a0 = log2 sum_k 2^{psi_k - max} (the block's bound at Delta = 0), and an
-// affine majorant of psi - max over the block's offsets u from its centroid:
-// psi_k - max <= c + g.u_k for every point, with g the least-squares slope
-// (a ridge keeps degenerate axes at zero slope; any g gives a valid bound)
-// and c its intercept plus the largest residual.  lin = (g, c + log2 count).
+// a0 = log2 sum_k 2^{psi_k - max} (the block's bound at Delta = 0), and,
+// with g the least-squares slope of psi - max over the block's offsets u from
+// its centroid (a ridge keeps degenerate axes at zero slope; any g gives a
+// valid bound), lin = (g, log2 sum_k 2^{psi_k - max - g.u_k}): then
+// log2 sum_k 2^{psi_k - max + h.u_k} <= lin.w + sum_axes |g + h| e for any h.
 __global__ void __launch_bounds__(kSB) k_sp_psi(const float* __restrict__ pot_s,
                                                 const float* __restrict__ logw2, int64_t cnt,
                                                 float l_over_eps, float4* __restrict__ scr,
@@ -418,20 +418,28 @@ __global__ void __launch_bounds__(kSB) k_sp_psi(const float* __restrict__ pot_s,
         for (int i = 0; i < 4; ++i) s_fit[i] = isfinite(sol[i]) ? (float)sol[i] : 0.f;
     }
     __syncthreads();
-    const float al = s_fit[0], g0 = s_fit[1], g1 = s_fit[2], g2 = s_fit[3];
-    float res = ok ? ps - (al + (g0 * u.x + g1 * u.y + g2 * u.z)) : -INFINITY;
+    const float g0 = s_fit[1], g1 = s_fit[2], g2 = s_fit[3];
+    // detrended block mass: log2 sum_k 2^{psi_k - max - g.u_k}
+    const float z = ok ? ps - (g0 * u.x + g1 * u.y + g2 * u.z) : -INFINITY;
+    float zm = z;
 #pragma unroll
-    for (int o = 16; o; o >>= 1) res = fmaxf(res, __shfl_xor_sync(0xffffffffu, res, o));
+    for (int o = 16; o; o >>= 1) zm = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, o));
     __syncthreads();
-    if (lane == 0) red[warp] = res;
+    if (lane == 0) red[warp] = zm;
+    __syncthreads();
+    zm = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    float ze = ok ? exp2f(z - zm) : 0.f;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ze += __shfl_xor_sync(0xffffffffu, ze, o);
+    __shared__ float red3[kSB / 32];
+    if (lane == 0) red3[warp] = ze;
     __syncthreads();
     if (threadIdx.x == 0) {
-        const float r = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-        const int count = (int)min((int64_t)kSB, cnt - (int64_t)blockIdx.x * kSB);
         pmax[blockIdx.x] = mx;
         a0[blockIdx.x] = log2f(((red2[0] + red2[1]) + red2[2]) + red2[3]);
-        // intercept + residual, a 1/64 allowance for the float32 evaluation, log2 count
-        lin[blockIdx.x] = make_float4(g0, g1, g2, al + r + 0.015625f + log2f((float)count));
+        // plus a 1/64 allowance for the float32 evaluation
+        const float lw = zm + log2f(((red3[0] + red3[1]) + red3[2]) + red3[3]) + 0.015625f;
+        lin[blockIdx.x] = make_float4(g0, g1, g2, lw);
     }
 }
 
@@ -502,8 +510,9 @@ __device__ __forceinline__ float bound_exact(const ScreenArgs& a, const float4 (
 // The slack sigma of the pair and a block-level upper bound of U that needs
 // no per-point work.  Per side, the smaller of two majorants of
 // log2 sum 2^{psi - max -+ kappa Delta.u} (e the per-axis extents):
-//   a0 + kappa sum_k |Delta_k| e_k                      (-+kappa Delta.u <= kappa |Delta_k| e_k)
-//   lin.w + sum_k |g_k -+ kappa Delta_k| e_k            (psi - max <= c + g.u)
+//   a0 + kappa sum_k |Delta_k| e_k        (-+kappa Delta.u <= kappa |Delta_k| e_k)
+//   lin.w + sum_k |g_k -+ kappa Delta_k| e_k
+//                                         (the same, after taking the slope g out)
 // The second keeps the potentials' slope inside a block, which cancels the
 // linear term for the blocks that exchange mass.
 __device__ __forceinline__ void bound_cheap(const ScreenArgs& a, float4 co, float4 eo, float4 lo,
