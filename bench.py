@@ -634,6 +634,10 @@ def run_sparse(args, w):
             "iters_per_s": aggregate_rate(world, iters, args.steps, total_ms),
             "kept_pairs_per_s": aggregate_rate(world, kept_per_step, args.steps, total_ms),
             "kept_fraction": kept_per_step / (rep["passes"] * n * m),
+            # block pairs the screenings evaluated point by point (one screening per
+            # pass when there is no in-loop residual check, as here)
+            "exact_bound_fraction": rep["exact_bounds"] / max(
+                rep["passes"] * rep["blocks_x"] * rep["blocks_y"], 1),
             "residual": rep["residual"], "blocks": [rep["blocks_x"], rep["blocks_y"]],
             "time_split_ms_per_step": {
                 "half_updates": half_ms / args.steps, "prep_sort_coarse": prep_ms / args.steps,

@@ -363,6 +363,8 @@ typedef struct fs_sparse_report {
     double residual;       /* |P 1 - a|_1 of the block-sparse plan at the returned f, g */
     double kept_blocks;    /* block pairs evaluated, summed over passes */
     double kept_pairs;     /* score pairs evaluated, summed over passes */
+    double exact_bounds;   /* block pairs given the per-point bound by the screenings
+                              (the rest were decided by the block-level bound) */
 } fs_sparse_report;
 
 /*

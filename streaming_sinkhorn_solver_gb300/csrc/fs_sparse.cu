@@ -467,6 +467,7 @@ struct ScreenArgs {
     float log2_tau;          // -inf: keep every block
     int* lists;              // [nbo x nbi]
     int* counts;             // [nbo]
+    unsigned long long* exact;  // accumulated: block pairs given the per-point bound
 };
 
 __device__ __forceinline__ void lse_merge(float& M, float& S, float Mo, float So) {
@@ -480,31 +481,38 @@ __device__ __forceinline__ void lse_merge(float& M, float& S, float Mo, float So
 // points, four per lane).
 // log2 sum over the warp of 2^z (four values per lane, -inf for none):
 // the warp max first, then one sum.
-__device__ __forceinline__ float warp_lse4(const float (&z)[4]) {
-    float m = max3(z[0], z[1], fmaxf(z[2], z[3]));
+// log2 sum over the 16 lanes of a half-warp of 2^z (eight values per lane,
+// -inf for none): the max first, then one sum.  Both halves of the warp run
+// it together, each on its own block pair.
+__device__ __forceinline__ float half_lse8(const float (&z)[8]) {
+    float m = fmaxf(max3(z[0], z[1], z[2]), max3(z[3], z[4], fmaxf(z[5], fmaxf(z[6], z[7]))));
 #pragma unroll
-    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float s = (ex2(z[0] - m) + ex2(z[1] - m)) + (ex2(z[2] - m) + ex2(z[3] - m));
+    for (int o = 8; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float s = 0.f;
 #pragma unroll
-    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    for (int q = 0; q < 8; ++q) s += ex2(z[q] - m);
+#pragma unroll
+    for (int o = 8; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     return m + log2f(s);
 }
 
-__device__ __forceinline__ float bound_exact(const ScreenArgs& a, const float4 (&own)[4],
-                                             float4 co, float pmo, int J, int lane) {
+// Exact bound U for input block J, by one half-warp (hl = lane % 16); own[]
+// holds the output block's points hl + 16 q, q < 8.
+__device__ __forceinline__ float bound_exact(const ScreenArgs& a, const float4 (&own)[8],
+                                             float4 co, float pmo, int J, int hl) {
     const float4 ci = a.cen_i[J];
     const float Dx = co.x - ci.x, Dy = co.y - ci.y, Dz = co.z - ci.z;
-    float za[4], zb[4];
+    float za[8], zb[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 8; ++q) {
         za[q] = own[q].w - a.kappa * (Dx * own[q].x + Dy * own[q].y + Dz * own[q].z);
-        const int64_t k = (int64_t)J * kSB + lane + 32 * q;
+        const int64_t k = (int64_t)J * kSB + hl + 16 * q;
         float4 v = make_float4(0.f, 0.f, 0.f, -INFINITY);
         if (k < a.cnt_i) v = a.si[k];
         zb[q] = v.w + a.kappa * (Dx * v.x + Dy * v.y + Dz * v.z);
     }
     const float dd = (Dx * Dx + Dy * Dy + Dz * Dz) * a.l_over_eps;
-    return pmo + warp_lse4(za) + a.pmax_i[J] + warp_lse4(zb) - dd;
+    return pmo + half_lse8(za) + a.pmax_i[J] + half_lse8(zb) - dd;
 }
 
 // The slack sigma of the pair and a block-level upper bound of U that needs
@@ -578,18 +586,20 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
         return;
     }
 
-    float4 own[4];
+    const int hl = lane & 15, half = lane >> 4;
+    float4 own[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int64_t k = o0 + lane + 32 * q;
+    for (int q = 0; q < 8; ++q) {
+        const int64_t k = o0 + hl + 16 * q;
         own[q] = k < a.cnt_o ? a.so[k] : make_float4(0.f, 0.f, 0.f, -INFINITY);
     }
     const float4 co = a.cen_o[O], eo = a.ext_o[O], lo = a.lin_o[O];
     const float pmo = a.pmax_o[O], a0o = a.a0_o[O];
     const float T = a.log2_tau + a.lw2_o[O] - log2f((float)a.nbi);
 
-    // 1. cull
+    // 1. cull (and the largest block-level bound among the culled blocks)
     int S = 0;
+    float culled_ub = -INFINITY;
     for (int c0 = 0; c0 < a.nbi; c0 += 256) {
         const int J = c0 + threadIdx.x;
         bool surv = false;
@@ -597,21 +607,31 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
             float ub, sig;
             bound_cheap(a, co, eo, lo, pmo, a0o, J, ub, sig);
             surv = ub + sig + kCullMargin >= T;
+            if (!surv) culled_ub = fmaxf(culled_ub, ub);
         }
         const int pos = compact_offset(surv, S, s_wcnt);
         if (surv && FS_IDX_OK(pos, a.nbi, 34)) row[pos] = J;
         __syncthreads();
     }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) culled_ub = fmaxf(culled_ub, __shfl_xor_sync(0xffffffffu, culled_ub, o));
+    if (lane == 0) s_val[warp] = culled_ub;
+    __syncthreads();
+    culled_ub = s_val[0];
+    for (int w = 1; w < 8; ++w) culled_ub = fmaxf(culled_ub, s_val[w]);
+    __syncthreads();
 
     bool full = 2 * S > a.nbi || S == 0;
     float best = -INFINITY;
     int bi = 0x7fffffff;
     if (!full) {
-        // 2a. exact bounds of the survivors
-        for (int sv = warp; sv < S; sv += 8) {
-            const int J = row[sv];
-            const float u = bound_exact(a, own, co, pmo, J, lane);
-            if (lane == 0 && FS_IDX_OK(a.nbi - 1 - sv, a.nbi, 35)) row[a.nbi - 1 - sv] = __float_as_int(u);
+        // 2a. exact bounds of the survivors, two per warp
+        for (int s0 = 2 * warp; s0 < S; s0 += 16) {
+            const int sv = s0 + half;
+            const int J = row[sv < S ? sv : s0];
+            const float u = bound_exact(a, own, co, pmo, J, hl);
+            if (hl == 0 && sv < S && FS_IDX_OK(a.nbi - 1 - sv, a.nbi, 35))
+                row[a.nbi - 1 - sv] = __float_as_int(u);
         }
         __syncthreads();
         // 2b. first maximiser among them
@@ -645,13 +665,8 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
                 bi = s_idx[w];
             }
         // 2c. a culled block could still be the maximiser: evaluate everything
-        bool risk = false;
-        for (int J = threadIdx.x; J < a.nbi; J += blockDim.x) {
-            float ub, sig;
-            bound_cheap(a, co, eo, lo, pmo, a0o, J, ub, sig);
-            if (!(ub + sig + kCullMargin >= T) && ub + kCullMargin >= best) risk = true;
-        }
-        full = __syncthreads_or(risk) != 0;
+        full = culled_ub + kCullMargin >= best;
+        __syncthreads();
         if (!full) {
             // 2d. compaction of the kept survivors (reads of a round before its writes)
             int base = 0;
@@ -670,16 +685,20 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
                 if (keep && FS_IDX_OK(pos, a.nbi, 36)) row[pos] = J;
                 __syncthreads();
             }
-            if (threadIdx.x == 0) a.counts[O] = base;
+            if (threadIdx.x == 0) {
+                a.counts[O] = base;
+                atomicAdd(a.exact, (unsigned long long)S);
+            }
             return;
         }
         __syncthreads();
     }
 
-    // 3. every input block, exactly
-    for (int J = warp; J < a.nbi; J += 8) {
-        const float u = bound_exact(a, own, co, pmo, J, lane);
-        if (lane == 0) row[J] = __float_as_int(u);
+    // 3. every input block, exactly, two per warp
+    for (int J0 = 2 * warp; J0 < a.nbi; J0 += 16) {
+        const int J = J0 + half;
+        const float u = bound_exact(a, own, co, pmo, J < a.nbi ? J : J0, hl);
+        if (hl == 0 && J < a.nbi) row[J] = __float_as_int(u);
     }
     __syncthreads();
     best = -INFINITY;
@@ -727,7 +746,10 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
         if (keep && FS_IDX_OK(pos, a.nbi, 37)) row[pos] = J;
         __syncthreads();
     }
-    if (threadIdx.x == 0) a.counts[O] = base;
+    if (threadIdx.x == 0) {
+        a.counts[O] = base;
+        atomicAdd(a.exact, (unsigned long long)(a.nbi + (S > 0 && 2 * S <= a.nbi ? S : 0)));
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -1088,7 +1110,7 @@ void layout_sparse(Layout& L, SpBufs& B, int64_t n, int64_t m, int d, int sms, b
     B.rowsum = L.take(sizeof(float) * n);
     B.red_part = L.take(sizeof(double) * kRedPartials);
     B.red_out = L.take(sizeof(double) * 2);
-    B.kept = L.take(sizeof(unsigned long long) * 2);
+    B.kept = L.take(sizeof(unsigned long long) * 3);
     B.fix_list = L.take(sizeof(int) * mx);
     B.fix_count = L.take(sizeof(unsigned int) * 2);
     if (coarse) {
@@ -1217,6 +1239,7 @@ fs_status screen(Call& c, const SpBufs& B, const SpSide& o, const SpSide& in, fl
     s.log2_tau = tau > 0.f ? (float)std::log2((double)tau) : -INFINITY;
     s.lists = c.at<int>(B.lists);
     s.counts = c.at<int>(B.counts);
+    s.exact = c.at<unsigned long long>(B.kept) + 2;
     NvtxRange nvtx("fs screening (block-sparse)");
     k_sp_screen<<<(unsigned)o.nb, 256, 0, c.stream>>>(s);
     count_launch();
@@ -1404,7 +1427,7 @@ fs_status sparse_solve_entry(const float* X, const float* a, int64_t n, const fl
     FS_TRY(set_bias(c, B.X, D, l_over_eps));
     FS_TRY(set_bias(c, B.Y, D, l_over_eps));
     timing_end(tp, TIME_PREP, c.stream);
-    FS_CUDA(cudaMemsetAsync(c.at<unsigned long long>(B.kept), 0, 2 * sizeof(unsigned long long),
+    FS_CUDA(cudaMemsetAsync(c.at<unsigned long long>(B.kept), 0, 3 * sizeof(unsigned long long),
                             c.stream));
     FS_CUDA(cudaMemsetAsync(c.at<unsigned int>(B.fix_count), 0, 2 * sizeof(unsigned int), c.stream));
 
@@ -1438,7 +1461,7 @@ fs_status sparse_solve_entry(const float* X, const float* a, int64_t n, const fl
         FS_TRY(measure_residual(c, B, D, eps, tau, &resid));
         ++passes;
     }
-    unsigned long long work[2] = {0, 0};
+    unsigned long long work[3] = {0, 0, 0};
     FS_CUDA(cudaMemcpyAsync(work, c.at<unsigned long long>(B.kept), sizeof(work),
                             cudaMemcpyDeviceToHost, c.stream));
     FS_CUDA(cudaStreamSynchronize(c.stream));
@@ -1458,6 +1481,7 @@ fs_status sparse_solve_entry(const float* X, const float* a, int64_t n, const fl
         rep->residual = resid;
         rep->kept_blocks = (double)work[0];
         rep->kept_pairs = (double)work[1];
+        rep->exact_bounds = (double)work[2];
     }
     return end_call(c);
 }
