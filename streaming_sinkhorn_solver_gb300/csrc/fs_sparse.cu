@@ -797,7 +797,7 @@ constexpr float kSpSlack = 8.f;            // lazy rescale threshold (log2 units
 // one subtraction, one ex2 and one add; the row's sum is range-checked and
 // rows outside the range go to the fixup list.
 template <int D, bool REF>
-__global__ void __launch_bounds__(256, 3) k_sp_half(SpHalfArgs a) {
+__global__ void __launch_bounds__(256, REF ? 4 : 3) k_sp_half(SpHalfArgs a) {
     __shared__ float4 sc[kSpWarps][2 * kSB];
     __shared__ float2 part[kSpWarps][kSB];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
