@@ -41,8 +41,10 @@ def test_cosine_potentials_match_oracle(n, m, d, tol):
     assert max_abs(np64(g), gr) <= tol * C.max()
 
 
-@pytest.mark.parametrize("d", [3, 64])
+@pytest.mark.parametrize("d", [3, 64, 300])
 def test_cosine_plan_operators_match_oracle(d):
+    """d = 300: the barycentric map and the gradient (k = d > 128) go through
+    the 256-column output blocks of the tensor plan application."""
     inp = random_cloud(600, 500, d, seed=450 + d, weights="lognormal")
     inp["X"] *= np.linspace(0.2, 3.0, 600, dtype=np.float32)[:, None]
     eps = 0.1
