@@ -124,11 +124,12 @@ class ClockSampler:
 # (kernel, host launch code and the headers they share): a committed ncu
 # summary stays valid while none of these files changes.
 KERNEL_SOURCES = {
-    "fma": ["fs_fma.cu", "fs_fma_host.cu", "fs_api.cu", "fs_internal.cuh", "fs_host.cuh"],
+    "fma": ["fs_fma.cu", "fs_fma_host.cu", "fs_api.cu", "fs_internal.cuh", "fs_host.cuh",
+            "fs_shard.cuh"],
     "tc": ["fs_tc_ref.cu", "fs_tc_half.cu", "fs_tc_host.cu", "fs_tc.cuh", "fs_tc_kernels.cuh",
-           "fs_internal.cuh", "fs_host.cuh"],
+           "fs_internal.cuh", "fs_host.cuh", "fs_shard.cuh"],
     "pair": ["fs_tc_pair.cu", "fs_tc_host.cu", "fs_tc.cuh", "fs_tc_kernels.cuh", "fs_internal.cuh",
-             "fs_host.cuh"],
+             "fs_host.cuh", "fs_shard.cuh"],
     "sparse": ["fs_sparse.cu", "fs_internal.cuh", "fs_host.cuh"],
 }
 

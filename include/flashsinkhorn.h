@@ -98,8 +98,39 @@ typedef struct fs_options {
     int32_t check_finite;  /* nonzero: after the call, scan the outputs and return
                               FS_ERR_NONFINITE if any is NaN/Inf (synchronises) */
     int32_t cost;          /* fs_cost; 0 = squared Euclidean */
-    int32_t reserved[4];   /* must be zero */
+    int32_t row_shards;    /* fs_sinkhorn_solve: 0 or 1 = one launch per half-update;
+                              G >= 2 = row shards (below); the other calls, whose
+                              rows need no exchange, ignore it */
+    int32_t reserved[3];   /* must be zero */
 } fs_options;
+
+/*
+ * Row shards.  A half-update partitions by rows of the updated side with no
+ * exchange inside it (Method 1: the update of row i needs only that row and
+ * the whole other side), so a G-GPU run would give each GPU a contiguous range
+ * of rows, have it update them against the full other side, and all-gather
+ * the potential before the next half.  With row_shards = G >= 2,
+ * fs_sinkhorn_solve runs every half-update as those G shards, one after the
+ * other on the call's stream: each launch (half-update, split merge, fixup)
+ * sees only its shard's rows, through offset pointers and sizes, and the next
+ * half reads the potential they wrote together.  Shards are cut on whole row
+ * blocks of the kernels (fs_shard_unit) and keep the unsharded column split,
+ * so every row takes the same arithmetic and the result is bitwise equal to
+ * row_shards = 1.  It is the per-GPU decomposition of a multi-GPU solve on
+ * one GPU; it is slower than one launch (G times the launches, smaller grids).
+ */
+
+/* Rows per shard unit for the path the options select at dimension d (the
+ * row block of the half-update kernels), or -1 for an invalid d or path. */
+int64_t fs_shard_unit(int32_t d, const fs_options* opt);
+
+/* Row range [*r0, *r1) of shard s of G over `rows` rows cut in units of
+ * `unit`: units [s U / G, (s + 1) U / G) of U = ceil(rows / unit), clipped to
+ * the rows (empty when G > U).  Host only, no device work.  FS_ERR_INVALID_ARG
+ * for rows or unit outside [0, 2^31 - 1] and [1, 2^31 - 1], G < 1, s outside
+ * [0, G) or null outputs. */
+fs_status fs_shard_range(int64_t rows, int64_t unit, int32_t shards, int32_t s, int64_t* r0,
+                         int64_t* r1);
 
 /*
  * CUDA graphs.  fs_sinkhorn_solve, fs_apply_plan, fs_barycentric, fs_grad_x
@@ -136,7 +167,7 @@ typedef struct fs_options {
  *
  * Limits: 1 <= n, m <= 2^31 - 1; 1 <= d <= 4096.
  * Errors: FS_ERR_INVALID_ARG for sizes out of range, null pointers,
- * eps <= 0 or not finite, n_iter < 1, nonzero reserved options;
+ * eps <= 0 or not finite, n_iter < 1, row_shards < 0, nonzero reserved options;
  * FS_ERR_OOM, FS_ERR_CUDA, FS_ERR_TIMEOUT, FS_ERR_NONFINITE as above.
  * On error f and g are unspecified.
  */

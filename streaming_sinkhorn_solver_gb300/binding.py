@@ -36,7 +36,7 @@ EXPORTED = ("fs_sinkhorn_solve", "fs_apply_plan", "fs_barycentric", "fs_grad_x",
             "fs_last_error", "fs_version", "fs_launch_count", "fs_timing_enable",
             "fs_timing_read", "fs_sinkhorn_solve_noalloc", "fs_unit_rates", "fs_hvp_x",
             "fs_sparse_solve", "fs_morton_order", "fs_sparse_screen", "fs_wait_selftest",
-            "fs_debug_bounds")
+            "fs_debug_bounds", "fs_shard_unit", "fs_shard_range")
 
 
 class FlashSinkhornError(RuntimeError):
@@ -51,7 +51,7 @@ COSTS = {"sqeuclidean": 0, "cosine": 1}
 class fs_options(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("splits", ctypes.c_int32),
                 ("check_finite", ctypes.c_int32), ("cost", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 4)]
+                ("row_shards", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
 
 class fs_sparse_options(ctypes.Structure):
@@ -130,6 +130,10 @@ def load_library(path: Optional[str] = None):
         lib.fs_wait_selftest.restype = ctypes.c_int
         lib.fs_debug_bounds.argtypes = [ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_uint64)]
         lib.fs_debug_bounds.restype = ctypes.c_int
+        lib.fs_shard_unit.argtypes = [i32, opt]
+        lib.fs_shard_unit.restype = i64
+        lib.fs_shard_range.argtypes = [i64, i64, i32, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+        lib.fs_shard_range.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -181,12 +185,14 @@ def _stream(stream, *xs):
     return ctypes.c_void_p(0)
 
 
-def _opts(path: str, splits: int, check_finite: bool, cost: str = "sqeuclidean"):
+def _opts(path: str, splits: int, check_finite: bool, cost: str = "sqeuclidean",
+          row_shards: int = 0):
     o = fs_options()
     o.path = PATHS[path]
     o.splits = int(splits)
     o.check_finite = 1 if check_finite else 0
     o.cost = COSTS[cost]
+    o.row_shards = int(row_shards)
     return ctypes.byref(o)
 
 
@@ -225,9 +231,12 @@ def _zeros_like(ref, shape):
 # the C ABI, one function each
 
 def fs_sinkhorn_solve(X, a, Y, b, eps: float, n_iter: int, f=None, g=None, *, path: str = "auto", cost: str = "sqeuclidean",
-                      splits: int = 0, check_finite: bool = False, stream=None) -> Tuple:
+                      splits: int = 0, check_finite: bool = False, row_shards: int = 0,
+                      stream=None) -> Tuple:
     """n_iter log-domain Sinkhorn iterations; f, g are in/out (g seeds the first
-    f-update, zeros if None).  Returns (f, g)."""
+    f-update, zeros if None).  Returns (f, g).  row_shards = G >= 2 runs every
+    half-update as G row shards, one after the other (the per-GPU launches of
+    a G-way row partition); the result is bitwise that of one launch."""
     n, d = X.shape
     m = Y.shape[0]
     f = _new_like(X, (n,)) if f is None else f
@@ -235,10 +244,28 @@ def fs_sinkhorn_solve(X, a, Y, b, eps: float, n_iter: int, f=None, g=None, *, pa
     st = load_library().fs_sinkhorn_solve(
         _ptr(X, "X", (n, d)), _ptr(a, "a", (n,)), n, _ptr(Y, "Y", (m, d)), _ptr(b, "b", (m,)), m, d,
         float(eps), int(n_iter), _ptr(f, "f", (n,)), _ptr(g, "g", (m,)),
-        _opts(path, splits, check_finite, cost), _stream(stream, X))
+        _opts(path, splits, check_finite, cost, row_shards), _stream(stream, X))
     _raise(st)
     _host_sync(stream, X, f, g)
     return f, g
+
+
+def fs_shard_unit(d: int, path: str = "auto") -> int:
+    """Rows per shard unit (the half-update's row block) for dimension d."""
+    o = fs_options()
+    o.path = PATHS[path]
+    u = load_library().fs_shard_unit(int(d), ctypes.byref(o))
+    if u < 1:
+        raise FlashSinkhornError(1, f"no shard unit for d={d}, path={path}")
+    return int(u)
+
+
+def fs_shard_range(rows: int, unit: int, shards: int, s: int) -> Tuple[int, int]:
+    """Row range [r0, r1) of shard s of `shards` (host only)."""
+    r0, r1 = ctypes.c_int64(), ctypes.c_int64()
+    _raise(load_library().fs_shard_range(int(rows), int(unit), int(shards), int(s),
+                                         ctypes.byref(r0), ctypes.byref(r1)))
+    return r0.value, r1.value
 
 
 def fs_apply_plan(X, a, Y, b, eps: float, f, g, V, out=None, *, path: str = "auto", cost: str = "sqeuclidean",

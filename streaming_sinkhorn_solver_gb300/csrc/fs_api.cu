@@ -6,6 +6,7 @@
 // Method 1 (log-domain f-update, Proposition 1), Method 2 (streaming fused
 // kernels, O((n+m)d) memory) and Method 3 (plan application).
 #include "fs_host.cuh"
+#include "fs_shard.cuh"
 
 #include <algorithm>
 #include <cmath>
@@ -254,8 +255,10 @@ fs_status check_common(const float* X, const float* a, int64_t n, const float* Y
     if (!(eps > 0.f) || !std::isfinite(eps))
         return fail(FS_ERR_INVALID_ARG, "eps must be positive and finite (got %g)", (double)eps);
     if (opt) {
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 3; ++i)
             if (opt->reserved[i]) return fail(FS_ERR_INVALID_ARG, "fs_options.reserved must be zero");
+        if (opt->row_shards < 0)
+            return fail(FS_ERR_INVALID_ARG, "fs_options.row_shards=%d", opt->row_shards);
         if (opt->cost < FS_COST_SQEUCLIDEAN || opt->cost > FS_COST_COSINE)
             return fail(FS_ERR_INVALID_ARG, "fs_options.cost=%d", opt->cost);
         if (opt->path < FS_PATH_AUTO || opt->path > FS_PATH_TENSOR)
@@ -411,6 +414,24 @@ fs_status fs_grad_y(const float* X, const float* a, int64_t n, const float* Y, c
     } catch (...) {
         return fail(FS_ERR_CUDA, "unexpected host exception");
     }
+}
+
+int64_t fs_shard_unit(int32_t d, const fs_options* opt) {
+    if (d < 1 || d > kMaxDim) return -1;
+    if (opt && (opt->path < FS_PATH_AUTO || opt->path > FS_PATH_TENSOR)) return -1;
+    const int path = choose_path(d, opt);
+    if (path == FS_PATH_FMA && d > kFmaMaxDim) return -1;
+    return path == FS_PATH_FMA ? shard_unit_fma(d) : shard_unit_tc();
+}
+
+fs_status fs_shard_range(int64_t rows, int64_t unit, int32_t shards, int32_t s, int64_t* r0,
+                         int64_t* r1) {
+    if (rows < 0 || rows > INT32_MAX || unit < 1 || unit > INT32_MAX || shards < 1 || s < 0 ||
+        s >= shards || !r0 || !r1)
+        return fail(FS_ERR_INVALID_ARG, "fs_shard_range(rows=%lld, unit=%lld, shards=%d, s=%d)",
+                    (long long)rows, (long long)unit, shards, s);
+    shard_range(rows, unit, shards, s, r0, r1);
+    return FS_OK;
 }
 
 int64_t fs_workspace_bytes(int64_t n, int64_t m, int32_t d, int32_t k, const fs_options* opt) {

@@ -1,6 +1,7 @@
 // Host orchestration of the FP32-FMA path (d <= 16): buffer layout,
 // preparation, the alternating half-update loop and plan application.
 #include "fs_host.cuh"
+#include "fs_shard.cuh"
 
 #include <algorithm>
 
@@ -65,6 +66,8 @@ int apply_splits_for(int64_t n, int64_t m, int32_t k, int sms, const fs_options*
 
 }  // namespace
 
+int64_t shard_unit_fma(int32_t d) { return fma_rows_per_block(fma_pad_dim(d)); }
+
 int64_t workspace_bytes_fma(int64_t n, int64_t m, int32_t d, int32_t k, int sms,
                             const fs_options* opt) {
     const FmaPlan p = plan_fma(n, m, d, sms, opt);
@@ -123,24 +126,38 @@ fs_status solve_fma(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) 
     // ones use reference offsets, with a guarded sum and a fixup of the rows
     // that fail it.
     const bool ref_ok = (double)n * (double)m >= kRefMinPairs;
-    auto half = [&](HalfArgs& h, int splits, int64_t nr, const float* rnorm, const float* rlogw2,
-                    float* pot, float* packed, bool ref) -> fs_status {
-        h.use_ref = ref ? 1 : 0;
+    // With row shards, each shard's launches see only its rows (offset row
+    // pointers, its row count); the column side and the split stay whole.
+    const int shards = opt && opt->row_shards > 1 ? opt->row_shards : 1;
+    const int64_t unit = fma_rows_per_block(p.D);
+    auto half = [&](const HalfArgs& h, int splits, bool ref) -> fs_status {
         NvtxRange nvtx(h.rows == PX ? "fs f-update (FMA)" : "fs g-update (FMA)");
-        const int ts = timing_begin(c.stream);
-        FS_CUDA(launch_half_fma(p.D, h, c.stream));
-        timing_end(ts, TIME_HALF, c.stream);
-        if (splits > 1)
-            FS_CUDA(launch_merge_lse(part, splits, nr, rnorm, rlogw2, eps_ln2, pot, packed + p.D,
-                                     p.DS, c.stream, ref ? fix_list : nullptr,
-                                     ref ? fix_count : nullptr));
-        if (ref) FS_CUDA(launch_fix_fma(p.D, h, c.stream));
+        for (int s = 0; s < shards; ++s) {
+            int64_t r0, r1;
+            shard_range(h.nr, unit, shards, s, &r0, &r1);
+            if (r1 <= r0) continue;
+            HalfArgs hs = h;
+            hs.use_ref = ref ? 1 : 0;
+            hs.rows = h.rows + r0 * p.DS;
+            hs.nr = r1 - r0;
+            hs.rnorm = h.rnorm + r0;
+            hs.rlogw2 = h.rlogw2 + r0;
+            hs.pot = h.pot + r0;
+            const int ts = timing_begin(c.stream);
+            FS_CUDA(launch_half_fma(p.D, hs, c.stream));
+            timing_end(ts, TIME_HALF, c.stream);
+            if (splits > 1)
+                FS_CUDA(launch_merge_lse(part, splits, hs.nr, hs.rnorm, hs.rlogw2, eps_ln2, hs.pot,
+                                         hs.rows + p.D, p.DS, c.stream, ref ? fix_list : nullptr,
+                                         ref ? fix_count : nullptr));
+            if (ref) FS_CUDA(launch_fix_fma(p.D, hs, c.stream));
+        }
         return FS_OK;
     };
     for (int32_t it = 0; it < n_iter; ++it) {
         const bool ref = ref_ok && it >= kOnlineIters;
-        FS_TRY(half(hf, p.splits_f, n, nx, lax, P.f.dev, PX, ref));
-        FS_TRY(half(hg, p.splits_g, m, ny, lby, P.g.dev, PY, ref));
+        FS_TRY(half(hf, p.splits_f, ref));
+        FS_TRY(half(hg, p.splits_g, ref));
     }
     if (opt && opt->check_finite) {
         FS_TRY(scan_finite(c, P.f.dev, n, c.at<unsigned int>(B.counter)));

@@ -2,8 +2,10 @@
 // layout, preparation, the alternating half-update loop, plan application.
 #include "fs_host.cuh"
 #include "fs_tc_kernels.cuh"
+#include "fs_shard.cuh"
 
 #include <algorithm>
+#include <vector>
 
 namespace fs {
 
@@ -161,6 +163,8 @@ void layout_apply(Layout& L, TcApplyBufs& A, const TcPlan& p, int64_t n, int32_t
 
 }  // namespace
 
+int64_t shard_unit_tc() { return 2 * BM; }
+
 int64_t workspace_bytes_tc(int64_t n, int64_t m, int32_t d, int32_t k, int sms,
                            const fs_options* opt) {
     const TcPlan p = plan_tc(n, m, d, sms, opt);
@@ -243,25 +247,74 @@ fs_status solve_tc(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) {
                  hg.rnorm, hg.rlogw2, P.g.dev, hg.rbias, fix_list, fix_count};
     const bool ref_ok = d <= kFixMaxDim && (double)n * (double)m >= kTcRefMinPairs;
 
-    auto half = [&](TcHalfArgs& h, const TcFixArgs& fx, const TensorMap128& tq,
-                    const TensorMap128& tk, int64_t row_tiles, int splits, int64_t nr, float* pot,
-                    bool ref) -> fs_status {
-        h.use_ref = ref ? 1 : 0;
-        NvtxRange nvtx(pot == P.f.dev ? "fs f-update (tensor)" : "fs g-update (tensor)");
-        const int ts = timing_begin(c.stream);
-        FS_CUDA(p.pair ? launch_half_pair(h, tq, tk, (int)row_tiles, p.qres, c.stream)
-                       : launch_half_tc(h, (int)row_tiles, p.qres, c.stream));
-        timing_end(ts, TIME_HALF, c.stream);
-        if (splits > 1)
-            FS_CUDA(launch_merge_lse(part, splits, nr, h.rnorm, h.rlogw2, eps_ln2, pot, h.rbias, 1,
-                                     c.stream, ref ? fix_list : nullptr, ref ? fix_count : nullptr));
-        if (ref) FS_CUDA(launch_fix_tc(fx, c.stream));
+    // With row shards, each shard's launches see only its rows: the row
+    // operand from its first tile on (a tensor map over its tiles for the
+    // pair kernel), offset row arrays and its row count; the column side and
+    // the split stay whole.  Shards are cut on tile pairs.
+    const int shards = opt && opt->row_shards > 1 ? opt->row_shards : 1;
+    std::vector<TensorMap128> shard_maps;
+    if (shards > 1 && p.pair) {
+        shard_maps.resize((size_t)2 * shards);
+        for (int side = 0; side < 2; ++side) {
+            const int64_t nr = side == 0 ? n : m;
+            const char* Q = static_cast<const char*>(side == 0 ? hf.Q : hg.Q);
+            for (int s = 0; s < shards; ++s) {
+                int64_t r0, r1;
+                shard_range(nr, shard_unit_tc(), shards, s, &r0, &r1);
+                if (r1 <= r0) continue;
+                const int64_t t0 = r0 / BM, t1 = (r1 + 2 * BM - 1) / (2 * BM) * 2;
+                FS_TRY(make_chunk_tmap(&shard_maps[(size_t)side * shards + s],
+                                       Q + t0 * p.nch * (int64_t)CHUNK_BYTES,
+                                       (uint64_t)(t1 - t0) * p.nch * BM));
+            }
+        }
+    }
+    auto half = [&](const TcHalfArgs& h, const TcFixArgs& fx, const TensorMap128& tq,
+                    const TensorMap128& tk, int64_t row_tiles, int side, bool ref) -> fs_status {
+        NvtxRange nvtx(side == 0 ? "fs f-update (tensor)" : "fs g-update (tensor)");
+        for (int s = 0; s < shards; ++s) {
+            int64_t r0 = 0, r1 = h.nr;
+            int64_t t0 = 0, t1 = row_tiles;
+            if (shards > 1) {
+                shard_range(h.nr, shard_unit_tc(), shards, s, &r0, &r1);
+                if (r1 <= r0) continue;
+                t0 = r0 / BM;
+                t1 = (r1 + 2 * BM - 1) / (2 * BM) * 2;
+            }
+            TcHalfArgs hs = h;
+            hs.use_ref = ref ? 1 : 0;
+            hs.Q = static_cast<const char*>(h.Q) + t0 * p.nch * (int64_t)CHUNK_BYTES;
+            hs.nr = r1 - r0;
+            hs.rnorm = h.rnorm + r0;
+            hs.rlogw2 = h.rlogw2 + r0;
+            hs.pot = h.pot + r0;
+            hs.rbias = h.rbias + r0;
+            const TensorMap128& tqs = shards > 1 && p.pair ? shard_maps[(size_t)side * shards + s] : tq;
+            const int ts = timing_begin(c.stream);
+            FS_CUDA(p.pair ? launch_half_pair(hs, tqs, tk, (int)(t1 - t0), p.qres, c.stream)
+                           : launch_half_tc(hs, (int)(t1 - t0), p.qres, c.stream));
+            timing_end(ts, TIME_HALF, c.stream);
+            if (h.splits > 1)
+                FS_CUDA(launch_merge_lse(part, h.splits, hs.nr, hs.rnorm, hs.rlogw2, eps_ln2, hs.pot,
+                                         hs.rbias, 1, c.stream, ref ? fix_list : nullptr,
+                                         ref ? fix_count : nullptr));
+            if (ref) {
+                TcFixArgs fxs = fx;
+                fxs.R = fx.R + r0 * (int64_t)d;
+                fxs.nr = hs.nr;
+                fxs.rnorm = hs.rnorm;
+                fxs.rlogw2 = hs.rlogw2;
+                fxs.pot = hs.pot;
+                fxs.rbias = hs.rbias;
+                FS_CUDA(launch_fix_tc(fxs, c.stream));
+            }
+        }
         return FS_OK;
     };
     for (int32_t it = 0; it < n_iter; ++it) {
         const bool ref = ref_ok && it >= kTcOnlineIters;
-        FS_TRY(half(hf, ff, tmX, tmY, p.rtx, p.splits_f, n, P.f.dev, ref));
-        FS_TRY(half(hg, fg, tmY, tmX, p.rty, p.splits_g, m, P.g.dev, ref));
+        FS_TRY(half(hf, ff, tmX, tmY, p.rtx, 0, ref));
+        FS_TRY(half(hg, fg, tmY, tmX, p.rty, 1, ref));
     }
     if (opt && opt->check_finite) {
         unsigned int* counter = c.at<unsigned int>(B.absmax);

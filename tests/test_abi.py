@@ -57,7 +57,8 @@ def _small():
     return X, a, Y, b
 
 
-@pytest.mark.parametrize("bad", ["eps0", "epsnan", "iters0", "path", "reserved", "splits"])
+@pytest.mark.parametrize("bad", ["eps0", "epsnan", "iters0", "path", "reserved", "splits",
+                                 "row_shards"])
 def test_invalid_arguments_rejected_on_host(lib, bad):
     X, a, Y, b = _small()
     f = np.zeros(4, np.float32)
@@ -76,6 +77,8 @@ def test_invalid_arguments_rejected_on_host(lib, bad):
         opt.reserved[2] = 1
     elif bad == "splits":
         opt.splits = -1
+    elif bad == "row_shards":
+        opt.row_shards = -2
     st = lib.fs_sinkhorn_solve(X.ctypes.data, a.ctypes.data, 4, Y.ctypes.data, b.ctypes.data, 5, 2,
                                eps, iters, f.ctypes.data, g.ctypes.data, ctypes.byref(opt), None)
     assert st == fs.FS_ERR_INVALID_ARG
