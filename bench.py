@@ -44,10 +44,11 @@ FP32_LANES_PER_CLK_SM = 128
 
 def fp32_ops_per_pair(d: int, tensor_path: bool) -> int:
     """FP32 lane-ops one score pair needs at the least: on the FMA path d
-    fused multiply-adds (the bias is the chain's first addend), one offset
-    subtraction and one accumulation; on the tensor path the dot product is
-    on the tensor pipe and the epilogue keeps the subtraction and the sum."""
-    return 2 if tensor_path else d + 2
+    fused multiply-adds (the column bias, with the row's exponent offset
+    folded into it, is the chain's first addend) and one accumulation; on the
+    tensor path the dot product and the offset are on the tensor pipe and the
+    epilogue keeps the scale-and-bias multiply-add and the sum."""
+    return 2 if tensor_path else d + 1
 
 
 def _rank_info():
@@ -290,7 +291,7 @@ def run_reference(args, w):
 def _dense_roofline(w, path, half_ms, half_n, rates, clocks, sms):
     """Roofline of the dense half-update from its own events.  Per launch (one
     f- or g-update) the algorithmic work is n*m score pairs: 2 n m d tensor
-    flops (tensor path), n m exponentials with d + 2 (FMA path) or 2 (tensor
+    flops (tensor path), n m exponentials with d + 1 (FMA path) or 2 (tensor
     path) FP32 lane-ops each, and the streamed operand bytes; the binding term
     is the largest of the three times."""
     n, m, d = w.n, w.m, w.d
@@ -603,8 +604,8 @@ def run_sparse(args, w):
     fp32_clk = rates.get("fma2_lanes_per_clk_sm") or FP32_LANES_PER_CLK_SM
     rate_src = "measured by fs_unit_rates" if "ex2_per_clk_sm" in rates else "nominal"
     # per kept pair, at the least (reference offsets, as after the first
-    # iterations): d fused multiply-adds, the offset subtraction and the
-    # accumulation -- the same count as the dense FMA path
+    # iterations, folded into the column records): d fused multiply-adds and
+    # the accumulation -- the same count as the dense FMA path
     fp32_ops = fp32_ops_per_pair(d, False)
     ex2_peak = ex2_clk * sms * clk * 1e6
     fp32_peak = fp32_clk / fp32_ops * sms * clk * 1e6
@@ -639,10 +640,12 @@ def run_sparse(args, w):
             # pass when there is no in-loop residual check, as here)
             "exact_bound_fraction": rep["exact_bounds"] / max(
                 rep["passes"] * rep["blocks_x"] * rep["blocks_y"], 1),
+            # rows whose guarded sum left its range and were recomputed
+            "fixed_row_fraction": rep["fixed_rows"] / max(rep["passes"] * (n + m) / 2, 1),
             "residual": rep["residual"], "blocks": [rep["blocks_x"], rep["blocks_y"]],
             "time_split_ms_per_step": {
                 "half_updates": half_ms / args.steps, "prep_sort_coarse": prep_ms / args.steps,
-                "screening_and_residual": step_ms - (half_ms + prep_ms) / args.steps},
+                "screening_fixups_and_residual": step_ms - (half_ms + prep_ms) / args.steps},
             "roofline": roof, "gpu_launches": int(launches), "clocks": clocks}
     if not args.no_e2e:
         host = {k: torch.from_numpy(v).pin_memory() for k, v in inp.items()}

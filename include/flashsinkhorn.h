@@ -396,6 +396,8 @@ typedef struct fs_sparse_report {
     double kept_pairs;     /* score pairs evaluated, summed over passes */
     double exact_bounds;   /* block pairs given the per-point bound by the screenings
                               (the rest were decided by the block-level bound) */
+    double fixed_rows;     /* rows whose guarded sum left its range and were
+                              recomputed with the online max, summed over passes */
 } fs_sparse_report;
 
 /*

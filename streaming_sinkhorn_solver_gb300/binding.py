@@ -65,7 +65,8 @@ class fs_sparse_report(ctypes.Structure):
     _fields_ = [("iters", ctypes.c_int32), ("passes", ctypes.c_int32),
                 ("blocks_x", ctypes.c_int32), ("blocks_y", ctypes.c_int32),
                 ("residual", ctypes.c_double), ("kept_blocks", ctypes.c_double),
-                ("kept_pairs", ctypes.c_double), ("exact_bounds", ctypes.c_double)]
+                ("kept_pairs", ctypes.c_double), ("exact_bounds", ctypes.c_double),
+                ("fixed_rows", ctypes.c_double)]
 
 
 _lib = None

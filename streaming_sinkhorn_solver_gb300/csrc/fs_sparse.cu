@@ -770,16 +770,18 @@ struct SpHalfArgs {
     float* pot;              // potentials out [nr] (sorted order)
     float* rowsum;           // measure mode: row marginal 2^{bias + LSE2} [nr]
     int measure;             // 1: write rowsum only, no update
-    unsigned long long* work;   // [2] accumulated: block pairs, score pairs evaluated
+    unsigned long long* work;   // [4] accumulated: block pairs, score pairs evaluated,
+                                //     (screening: exact bounds), rows fixed up
     // reference offsets: rows whose guarded sum left the range, for k_sp_fix
     int* fix_list;            // [nr]
     unsigned int* fix_count;  // [2], zero before the first guarded half-update
 };
 
-// Guarded range of a row's sum 2^{s - M} when M is the previous LSE: below
-// 2^-64 the terms that underflowed could matter, above 2^126 the sum could
-// overflow; such rows are recomputed with the online max.
-constexpr float kSpMinRefSum = 5.421010862427522e-20f;   // 2^-64
+// Guarded range of a row's sum 2^{s - M} relative to its offset M: below
+// 2^-96 the terms that flushed to zero (under 2^-126, i.e. 2^-30 of the sum)
+// could matter, above 2^126 the sum could overflow; such rows are recomputed
+// with the online max.
+constexpr float kSpMinRefSum = 1.2621774483536189e-29f;  // 2^-96
 constexpr float kSpMaxRefSum = 8.507059173023462e+37f;   // 2^126
 
 constexpr int kSpWarps = 8;                 // warps per block, each its own share of the list
@@ -792,14 +794,135 @@ constexpr float kSpSlack = 8.f;            // lazy rescale threshold (log2 units
 // duplicated, so one packed FMA scores a column against two rows.  The
 // eight warps' (max, sum) are merged in warp order at the end, so the result
 // does not depend on timing.
-// REF = false: online max with a lazy rescale.  REF = true: the offset of a
-// row is its previous LSE, log2 w - (bias slot), so a pair costs the score,
-// one subtraction, one ex2 and one add; the row's sum is range-checked and
-// rows outside the range go to the fixup list.
+// REF = false: online max with a lazy rescale.  REF = true: the offsets are
+// the rows' previous LSEs M_i = log2 w_i - (bias slot), through an affine fit
+// over the block (block_offset_fit): A_i = mu + h . q_i, with q_i the row's
+// kappa-scaled coordinates.  Folded into the staged column records
+// (y_j - h, bias_j - mu), it makes the score chain itself produce s_ij - A_i,
+// so a pair costs the score, one ex2 and one add; the row's sum, relative to
+// A_i, is range-checked and rows outside the range go to the fixup list.
+
+// Warp sum over a butterfly: every lane ends with the same bits.
+__device__ __forceinline__ float warp_sum_all(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Least-squares affine fit M ~ Mbar + h . (q - qbar) over the block's rows
+// (lane holds rows lane + 32 i, i < 4; valid[i] false for padding), computed
+// identically by every lane of every warp.  Returns h and mu, shifted so the
+// largest residual M_i - A_i is kSpFitTop: every row's sum relative to A_i
+// then stays below 2^kSpFitTop times its sum relative to M_i (which is about
+// 1 once the LSEs settle, and far from 2^126), and only a row whose residual
+// lies more than kSpFitTop + 96 below the largest leaves the guarded range.
+// A singular or non-finite fit gives h = 0 (a constant offset).
+constexpr float kSpFitTop = 100.f;
+
+template <int D>
+__device__ __forceinline__ void block_offset_fit(const float (&q)[4][D], const float (&M)[4],
+                                                 const bool (&valid)[4], float (&h)[D], float& mu) {
+    float n = 0.f, qs[D], ms = 0.f;
+#pragma unroll
+    for (int k = 0; k < D; ++k) qs[k] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (!valid[i]) continue;
+        n += 1.f;
+        ms += M[i];
+#pragma unroll
+        for (int k = 0; k < D; ++k) qs[k] += q[i][k];
+    }
+    n = warp_sum_all(n);
+    const float mbar = warp_sum_all(ms) / n;
+    float qbar[D];
+#pragma unroll
+    for (int k = 0; k < D; ++k) qbar[k] = warp_sum_all(qs[k]) / n;
+    float C[D][D], c[D];
+#pragma unroll
+    for (int k = 0; k < D; ++k) {
+        c[k] = 0.f;
+#pragma unroll
+        for (int l = 0; l < D; ++l) C[k][l] = 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (!valid[i]) continue;
+        const float dm = M[i] - mbar;
+#pragma unroll
+        for (int k = 0; k < D; ++k) {
+            const float dk = q[i][k] - qbar[k];
+            c[k] += dk * dm;
+#pragma unroll
+            for (int l = k; l < D; ++l) C[k][l] += dk * (q[i][l] - qbar[l]);
+        }
+    }
+    float tr = 0.f;
+#pragma unroll
+    for (int k = 0; k < D; ++k) {
+        c[k] = warp_sum_all(c[k]);
+#pragma unroll
+        for (int l = k; l < D; ++l) C[l][k] = C[k][l] = warp_sum_all(C[k][l]);
+        tr += C[k][k];
+    }
+    const float lam = 1e-4f * tr / D + 1e-30f;
+#pragma unroll
+    for (int k = 0; k < D; ++k) C[k][k] += lam;
+    // Cholesky solve of the D x D system
+    bool ok = true;
+#pragma unroll
+    for (int k = 0; k < D; ++k) {
+#pragma unroll
+        for (int l = 0; l < k; ++l) C[k][k] -= C[k][l] * C[k][l];
+        ok = ok && C[k][k] > 0.f;
+        C[k][k] = sqrtf(fmaxf(C[k][k], 1e-30f));
+#pragma unroll
+        for (int r = k + 1; r < D; ++r) {
+#pragma unroll
+            for (int l = 0; l < k; ++l) C[r][k] -= C[r][l] * C[k][l];
+            C[r][k] /= C[k][k];
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < D; ++k) {
+#pragma unroll
+        for (int l = 0; l < k; ++l) c[k] -= C[k][l] * c[l];
+        c[k] /= C[k][k];
+    }
+#pragma unroll
+    for (int k = D - 1; k >= 0; --k) {
+#pragma unroll
+        for (int l = k + 1; l < D; ++l) c[k] -= C[l][k] * h[l];
+        h[k] = c[k] / C[k][k];
+        ok = ok && isfinite(h[k]);
+    }
+    if (!ok) {
+#pragma unroll
+        for (int k = 0; k < D; ++k) h[k] = 0.f;
+    }
+    // the largest residual sets the level
+    mu = mbar;
+#pragma unroll
+    for (int k = 0; k < D; ++k) mu -= h[k] * qbar[k];
+    float rmax = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (!valid[i]) continue;
+        float a = mu;
+#pragma unroll
+        for (int k = 0; k < D; ++k) a = fmaf(h[k], q[i][k], a);
+        rmax = fmaxf(rmax, M[i] - a);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) rmax = fmaxf(rmax, __shfl_xor_sync(0xffffffffu, rmax, o));
+    if (isfinite(rmax)) mu += rmax - kSpFitTop;
+}
+
 template <int D, bool REF>
 __global__ void __launch_bounds__(256, REF ? 4 : 3) k_sp_half(SpHalfArgs a) {
     __shared__ float4 sc[kSpWarps][2 * kSB];
     __shared__ float2 part[kSpWarps][kSB];
+    __shared__ float4 sfit[kSpWarps];       // REF: the warp's column shift (h, mu)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int O = a.order[blockIdx.x];
     const int64_t r0 = (int64_t)O * kSB;
@@ -816,14 +939,37 @@ __global__ void __launch_bounds__(256, REF ? 4 : 3) k_sp_half(SpHalfArgs a) {
     for (int i = 0; i < 4; ++i) M[i] = Mt[i] = -INFINITY;
     S[0] = S[1] = pk(0.f, 0.f);
     nm[0] = nm[1] = pk(INFINITY, INFINITY);
+    // REF: the column shift (h, mu) of the block's affine offset (kept in
+    // shared memory for the staging), and each row's offset A_i = mu + h . q_i
+    // in M[i]
     if (REF) {
+        float hc[D], mu;
+        float qi[4][D];
+        bool valid[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
+            valid[i] = r0 + lane + 32 * i < a.nr;
             const int64_t r = min(r0 + lane + 32 * i, a.nr - 1);
             M[i] = a.rlogw2[r] - a.rows[r * 4 + D];
+#pragma unroll
+            for (int k = 0; k < D; ++k) qi[i][k] = a.rows[r * 4 + k] * a.kappa;
         }
-        nm[0] = pk(-M[0], -M[1]);
-        nm[1] = pk(-M[2], -M[3]);
+        block_offset_fit<D>(qi, M, valid, hc, mu);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float A = mu;
+#pragma unroll
+            for (int k = 0; k < D; ++k) A = fmaf(hc[k], qi[i][k], A);
+            M[i] = A;
+        }
+        if (lane == 0) {
+            float f[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < D; ++k) f[k] = hc[k];
+            f[D] = mu;
+            sfit[warp] = make_float4(f[0], f[1], f[2], f[3]);
+        }
+        __syncwarp();
     }
 
     const int cnt = a.counts[O];
@@ -841,19 +987,36 @@ __global__ void __launch_bounds__(256, REF ? 4 : 3) k_sp_half(SpHalfArgs a) {
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
             const int j = lane + 32 * t;
-            if (j < ncol && FS_IDX_OK(c0 + j, a.nc, 39)) {
-                const float4 v = cols4[c0 + j];
-                my[2 * j] = make_float4(v.x, v.x, v.y, v.y);
-                my[2 * j + 1] = make_float4(v.z, v.z, v.w, v.w);
+            if (j < ((ncol + 7) & ~7)) {
+                // past ncol (the rest of the last group): zero coordinates
+                // and a -inf bias, so those columns score -inf
+                float e[4] = {0.f, 0.f, 0.f, 0.f};
+                e[D] = -INFINITY;
+                if (j < ncol && FS_IDX_OK(c0 + j, a.nc, 39)) {
+                    const float4 v = cols4[c0 + j];
+                    e[0] = v.x;
+                    e[1] = v.y;
+                    e[2] = v.z;
+                    e[3] = v.w;
+                    if (REF) {
+                        const float4 sh = sfit[warp];
+                        e[0] -= sh.x;
+                        e[1] -= sh.y;
+                        e[2] -= sh.z;
+                        e[3] -= sh.w;   // the bias slot's shift is mu; a slot past it is unused
+                    }
+                }
+                my[2 * j] = make_float4(e[0], e[0], e[1], e[1]);
+                my[2 * j + 1] = make_float4(e[2], e[2], e[3], e[3]);
             }
         }
         __syncwarp();
+        // every group of 8 is full: the staged tail past ncol scores -inf
         for (int j = 0; j < ncol; j += 8) {
-            const int G = min(8, ncol - j);
             uint64_t s[2][8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const int jj = j + (u < G ? u : 0);
+                const int jj = j + u;
                 const float4 lo = my[2 * jj], hi = my[2 * jj + 1];
                 const uint64_t c[4] = {pk(lo.x, lo.y), pk(lo.z, lo.w), pk(hi.x, hi.y), pk(hi.z, hi.w)};
 #pragma unroll
@@ -861,7 +1024,7 @@ __global__ void __launch_bounds__(256, REF ? 4 : 3) k_sp_half(SpHalfArgs a) {
                     uint64_t acc = c[D];
 #pragma unroll
                     for (int k = 0; k < D; ++k) acc = fma2(q[p][k], c[k], acc);
-                    s[p][u] = u < G ? acc : pk(-INFINITY, -INFINITY);
+                    s[p][u] = acc;
                 }
             }
             if (!REF) {
@@ -903,7 +1066,7 @@ __global__ void __launch_bounds__(256, REF ? 4 : 3) k_sp_half(SpHalfArgs a) {
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     float x0, x1;
-                    upk(add2(s[p][u], nm[p]), x0, x1);
+                    upk(REF ? s[p][u] : add2(s[p][u], nm[p]), x0, x1);
                     ev[u] = pk(ex2(x0), ex2(x1));
                 }
 #pragma unroll
@@ -959,44 +1122,47 @@ __global__ void __launch_bounds__(256, REF ? 4 : 3) k_sp_half(SpHalfArgs a) {
 }
 
 // Recompute, with the online max over the row block's kept blocks, the rows a
-// guarded half-update listed: one warp per row, lanes striding over the
-// kept columns, then a shuffle merge.  The last block to finish resets the
-// list for the next half-update.
-constexpr int kSpFixBlocks = 64;
+// guarded half-update listed: one 256-thread block per row (a row's kept
+// list can hold hundreds of blocks of 128 columns), threads striding over
+// the kept columns, then a fixed-order merge (warp butterflies, then the
+// warps in order), so the result does not depend on timing.  The grid
+// strides over the list; the last block to finish resets it for the next
+// half-update.
+constexpr int kSpFixBlocks = 1216;   // 8 per SM on 152 SMs; idle blocks exit at once
 
 template <int D>
 __global__ void __launch_bounds__(256) k_sp_fix(SpHalfArgs a) {
     __shared__ unsigned int s_cnt;
+    __shared__ float2 s_part[8];
     if (threadIdx.x == 0) s_cnt = min(*(volatile unsigned int*)&a.fix_count[0], (unsigned int)a.nr);
     __syncthreads();
     const unsigned int cnt = s_cnt;
-    const int lane = threadIdx.x & 31;
-    const int warps = gridDim.x * (blockDim.x >> 5);
-    for (unsigned int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < cnt; w += warps) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (unsigned int w = blockIdx.x; w < cnt; w += gridDim.x) {
         const int64_t row = a.fix_list[w];
-        if (!FS_IDX_OK(row, a.nr, 40)) continue;
+        if (!FS_IDX_OK(row, a.nr, 40)) continue;     // block-uniform
         const int64_t O = row / kSB;
         float q[D];
 #pragma unroll
         for (int k = 0; k < D; ++k) q[k] = a.rows[row * 4 + k] * a.kappa;
         float M = -INFINITY, S = 0.f;
         const int* lst = a.lists + O * a.nbi;
-        const int nk = a.counts[O];
-        for (int e = 0; e < nk; ++e) {
-            if (!FS_IDX_OK(lst[e], a.nbi, 41)) continue;
-            const int64_t c0 = (int64_t)lst[e] * kSB;
-            const int ncol = (int)min((int64_t)kSB, a.nc - c0);
-            for (int j = lane; j < ncol; j += 32) {
-                const float* c = a.cols + (c0 + j) * 4;
-                float sc = c[D];
+        const int64_t total = (int64_t)a.counts[O] * kSB;
+        for (int64_t idx = threadIdx.x; idx < total; idx += blockDim.x) {
+            const int J = lst[idx / kSB];
+            if (!FS_IDX_OK(J, a.nbi, 41)) continue;
+            const int64_t col = (int64_t)J * kSB + idx % kSB;
+            if (col >= a.nc) continue;
+            const float4 c = reinterpret_cast<const float4*>(a.cols)[col];
+            const float cv[4] = {c.x, c.y, c.z, c.w};
+            float sc = cv[D];
 #pragma unroll
-                for (int k = 0; k < D; ++k) sc = fmaf(q[k], c[k], sc);
-                if (sc > M) {
-                    S = (M == -INFINITY ? 0.f : S * ex2(M - sc));
-                    M = sc;
-                }
-                S += ex2(sc - M);
+            for (int k = 0; k < D; ++k) sc = fmaf(q[k], cv[k], sc);
+            if (sc > M) {
+                S = (M == -INFINITY ? 0.f : S * ex2(M - sc));
+                M = sc;
             }
+            S += ex2(sc - M);
         }
 #pragma unroll
         for (int o = 16; o; o >>= 1) {
@@ -1004,16 +1170,23 @@ __global__ void __launch_bounds__(256) k_sp_fix(SpHalfArgs a) {
             const float So = __shfl_xor_sync(0xffffffffu, S, o);
             lse_merge(M, S, Mo, So);
         }
-        if (lane == 0) {
-            const float lse2 = M + log2f(S);
+        if (lane == 0) s_part[warp] = make_float2(M, S);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float Mf = -INFINITY, Sf = 0.f;
+            for (int v = 0; v < 8; ++v)
+                if (s_part[v].x != -INFINITY) lse_merge(Mf, Sf, s_part[v].x, s_part[v].y);
+            const float lse2 = Mf + log2f(Sf);
             a.pot[row] = a.rnorm[row] - a.eps_ln2 * lse2;
             a.rows[row * 4 + D] = a.rlogw2[row] - lse2;
         }
+        __syncthreads();
     }
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
         if (atomicAdd(&a.fix_count[1], 1u) == gridDim.x - 1) {
+            atomicAdd(&a.work[3], (unsigned long long)cnt);
             a.fix_count[0] = 0;
             a.fix_count[1] = 0;
             __threadfence();
@@ -1110,7 +1283,7 @@ void layout_sparse(Layout& L, SpBufs& B, int64_t n, int64_t m, int d, int sms, b
     B.rowsum = L.take(sizeof(float) * n);
     B.red_part = L.take(sizeof(double) * kRedPartials);
     B.red_out = L.take(sizeof(double) * 2);
-    B.kept = L.take(sizeof(unsigned long long) * 3);
+    B.kept = L.take(sizeof(unsigned long long) * 4);
     B.fix_list = L.take(sizeof(int) * mx);
     B.fix_count = L.take(sizeof(unsigned int) * 2);
     if (coarse) {
@@ -1427,7 +1600,7 @@ fs_status sparse_solve_entry(const float* X, const float* a, int64_t n, const fl
     FS_TRY(set_bias(c, B.X, D, l_over_eps));
     FS_TRY(set_bias(c, B.Y, D, l_over_eps));
     timing_end(tp, TIME_PREP, c.stream);
-    FS_CUDA(cudaMemsetAsync(c.at<unsigned long long>(B.kept), 0, 3 * sizeof(unsigned long long),
+    FS_CUDA(cudaMemsetAsync(c.at<unsigned long long>(B.kept), 0, 4 * sizeof(unsigned long long),
                             c.stream));
     FS_CUDA(cudaMemsetAsync(c.at<unsigned int>(B.fix_count), 0, 2 * sizeof(unsigned int), c.stream));
 
@@ -1461,7 +1634,7 @@ fs_status sparse_solve_entry(const float* X, const float* a, int64_t n, const fl
         FS_TRY(measure_residual(c, B, D, eps, tau, &resid));
         ++passes;
     }
-    unsigned long long work[3] = {0, 0, 0};
+    unsigned long long work[4] = {0, 0, 0, 0};
     FS_CUDA(cudaMemcpyAsync(work, c.at<unsigned long long>(B.kept), sizeof(work),
                             cudaMemcpyDeviceToHost, c.stream));
     FS_CUDA(cudaStreamSynchronize(c.stream));
@@ -1482,6 +1655,7 @@ fs_status sparse_solve_entry(const float* X, const float* a, int64_t n, const fl
         rep->kept_blocks = (double)work[0];
         rep->kept_pairs = (double)work[1];
         rep->exact_bounds = (double)work[2];
+        rep->fixed_rows = (double)work[3];
     }
     return end_call(c);
 }

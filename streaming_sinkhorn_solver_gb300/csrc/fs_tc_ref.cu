@@ -8,10 +8,16 @@
 // exponent, sum and potential write-back fused in one pass).
 //
 // Once the potentials have settled, a row's previous LSE is a fixed exponent
-// offset M for the whole pass: no running max, so every score costs one
-// multiply-add, one subtraction, one exp2 and one add (packed two by two).
-// The row's sum is range-checked at the end; a row outside the range goes to
-// the fixup list.
+// offset M for the whole pass: no running max.  The offset enters the
+// accumulator through the tensor core: one more K = 16 step per tile
+// multiplies an offset column block of the resident Q tile, whose first two
+// columns hold the fp16 split (hi, lo) of -M / (ks 2^p) for each row, by a
+// constant column block whose first two columns hold 2^p, so the
+// accumulator is Q K^T - M / ks and every score costs one multiply-add, one
+// exp2 and one add (packed two by two).  The offset actually applied is
+// M' = -(hi + lo) 2^p ks, which the write-back uses; 2^p puts the CTA's
+// largest |M| / ks near 2^14, inside fp16.  The row's sum is range-checked at
+// the end; a row outside the range goes to the fixup list.
 //
 // One CTA owns a 128-row tile of Q (resident in shared memory) and a range
 // of 128-column tiles of K; tile t lives in TMEM buffer t mod 4.
@@ -51,22 +57,36 @@ static_assert(kRefGroups == kTmemBufs, "one epilogue group per TMEM buffer");
 
 __host__ __device__ constexpr int ref_smem_bytes(int nch) {
     return 1024 /* alignment slack */ + (1 + kTmemBufs) * nch * CHUNK_BYTES +
-           kRefBiasSlots * kBiasBytes + BM * 4 * (kRefGroups - 1) /* group merge */ +
-           8 * (1 + 2 * kTmemBufs + 2 * kRefBiasSlots + 1) + 16;
+           2 * CHUNK_BYTES /* offset column blocks */ + kRefBiasSlots * kBiasBytes +
+           BM * 4 * (kRefGroups - 1) /* group merge */ +
+           8 * (1 + 2 * kTmemBufs + 2 * kRefBiasSlots + 2) + 16;
+}
+
+// fp16 split of the scaled row offset: hi + lo = -M / (ks 2^p) to about 22
+// bits (clamped inside the fp16 range: a row clamped here leaves the guarded
+// range and is recomputed by the fixup)
+__device__ __forceinline__ void offset_split(float M, float inv_scale, __half& hi, __half& lo) {
+    const float t = fminf(fmaxf(-M * inv_scale, -60000.f), 60000.f);
+    hi = __float2half_rn(t);
+    lo = __float2half_rn(t - __half2float(hi));
+}
+
+// the offset the accumulator received: -(hi + lo) 2^p ks
+__device__ __forceinline__ float offset_applied(__half hi, __half lo, float scale) {
+    return -(__half2float(hi) + __half2float(lo)) * scale;
 }
 
 // One 16-lane x 32-column slice (tmem_ld16x32 layout): for each repetition
 // i, the column pair's bias bp[i] serves both rows; lo/hi accumulate the rows
-// t/4 and t/4 + 8 of the block: acc += 2^{v kappa' + bias - M} (nlo, nhi hold
-// the rows' -M, packed twice).
+// t/4 and t/4 + 8 of the block: acc += 2^{v kappa' + bias} (v already holds
+// the row's -M' / kappa').
 __device__ __forceinline__ void ref_slice(const float (&v)[16], const uint64_t (&bp)[4],
-                                          uint64_t ks2, uint64_t nlo, uint64_t nhi, uint64_t& lo,
-                                          uint64_t& hi) {
+                                          uint64_t ks2, uint64_t& lo, uint64_t& hi) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         float x0, x1, x2, x3;
-        upk(add2(fma2(pk(v[4 * i], v[4 * i + 1]), ks2, bp[i]), nlo), x0, x1);
-        upk(add2(fma2(pk(v[4 * i + 2], v[4 * i + 3]), ks2, bp[i]), nhi), x2, x3);
+        upk(fma2(pk(v[4 * i], v[4 * i + 1]), ks2, bp[i]), x0, x1);
+        upk(fma2(pk(v[4 * i + 2], v[4 * i + 3]), ks2, bp[i]), x2, x3);
         lo = add2(lo, pk(ex2(x0), ex2(x1)));
         hi = add2(hi, pk(ex2(x2), ex2(x3)));
     }
@@ -86,7 +106,9 @@ __global__ void __launch_bounds__(kRefThreads, 1) k_half_ref(TcHalfArgs a) {
 
     uint8_t* sQ = smem;
     uint8_t* sK = smem + TILE_BYTES;                       // slot b at sK + b * TILE_BYTES
-    uint8_t* sBias = sK + kTmemBufs * TILE_BYTES;
+    uint8_t* sQx = sK + kTmemBufs * TILE_BYTES;            // offset column block of Q
+    uint8_t* sKx = sQx + CHUNK_BYTES;                      // constant column block of K
+    uint8_t* sBias = sKx + CHUNK_BYTES;
     float* sMerge = reinterpret_cast<float*>(sBias + kRefBiasSlots * kBiasBytes);
     uint64_t* qfull = reinterpret_cast<uint64_t*>(sMerge + BM * (kRefGroups - 1));
     uint64_t* tfull = qfull + 1;                 // MMAs of the buffer's tile complete
@@ -94,7 +116,9 @@ __global__ void __launch_bounds__(kRefThreads, 1) k_half_ref(TcHalfArgs a) {
     uint64_t* bfull = tempty + kTmemBufs;
     uint64_t* bempty = bfull + kRefBiasSlots;
     uint64_t* drain = bempty + kRefBiasSlots;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* xfull = drain + 1;                 // offset column blocks written
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xfull + 1);
+    uint32_t* sMmax = tmem_slot + 1;             // largest |M| of the tile's rows (float bits)
 
     if (threadIdx.x == 0) {
         mbar_init(qfull, 1);
@@ -107,6 +131,8 @@ __global__ void __launch_bounds__(kRefThreads, 1) k_half_ref(TcHalfArgs a) {
             mbar_init(&bempty[s], kEpiWarps);
         }
         mbar_init(drain, 1);
+        mbar_init(xfull, kRefGroups * kEpiWarps);
+        *sMmax = 0u;
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
@@ -169,7 +195,10 @@ __global__ void __launch_bounds__(kRefThreads, 1) k_half_ref(TcHalfArgs a) {
 #pragma unroll
             for (int c = 0; c < NCH; ++c) qd[c] = sdesc_sw128(smem_u32(sQ + c * CHUNK_BYTES));
             const uint64_t kd0 = sdesc_sw128(smem_u32(sK));
-            bool ok = mbar_wait(qfull, 0, a.err, ERR_TIMEOUT_MMA);
+            const uint64_t qxd = sdesc_sw128(smem_u32(sQx));
+            const uint64_t kxd = sdesc_sw128(smem_u32(sKx));
+            bool ok = mbar_wait(qfull, 0, a.err, ERR_TIMEOUT_MMA) &&
+                      mbar_wait(xfull, 0, a.err, ERR_TIMEOUT_MMA);
             for (int t = 0; t < ntiles && ok; ++t) {
                 const int b = t & (kTmemBufs - 1);
                 if (!mbar_wait(&tempty[b], (uint32_t)((t >> 2) & 1), a.err, ERR_TIMEOUT_MMA)) break;
@@ -183,6 +212,7 @@ __global__ void __launch_bounds__(kRefThreads, 1) k_half_ref(TcHalfArgs a) {
                         mma_f16(d_tmem, qd[c] + (uint64_t)(2 * kk),
                                 kd + (uint64_t)((c * CHUNK_BYTES) >> 4) + (uint64_t)(2 * kk), idesc,
                                 (c | kk) != 0);
+                mma_f16(d_tmem, qxd, kxd, idesc, 1);      // + (-M / ks) for every row
                 mma_commit(&tfull[b]);
             }
             // every MMA issued has completed once `drain` fires
@@ -195,14 +225,49 @@ __global__ void __launch_bounds__(kRefThreads, 1) k_half_ref(TcHalfArgs a) {
         const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
         const float ks = *a.kscale;
         const uint64_t ks2 = pk(ks, ks);
-        // -M of this thread's four rows, 32*quarter + lane/4 + 8k
-        uint64_t nM[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int64_t rk = min(rt * BM + quarter * 32 + (lane >> 2) + 8 * k, a.nr - 1);
-            const float m = a.rlogw2[rk] - a.rbias[rk];
-            nM[k] = pk(-m, -m);
+        // The offset column blocks.  The tile's largest |M| (the warps of
+        // group 0 cover its 128 rows) sets 2^p; then the 16 warps write the
+        // 2 x 128 rows x 8 16-byte units of the two blocks.
+        const int ew = warp - 2;                    // epilogue warp 0..15
+        if (grp == 0) {
+            float mabs = 0.f;
+            const int64_t rk = min(rt * BM + quarter * 32 + lane, a.nr - 1);
+            mabs = fabsf(a.rlogw2[rk] - a.rbias[rk]);
+            if (!(mabs <= 3.0e38f)) mabs = 3.0e38f;   // NaN and inf: the largest finite
+            const unsigned int mb = __reduce_max_sync(0xffffffffu, __float_as_uint(mabs));
+            if (lane == 0) atomicMax(sMmax, mb);
         }
+        asm volatile("bar.sync 1, %0;" ::"n"(kRefGroups * kEpiWarps * 32) : "memory");
+        float scale, inv_scale;
+        __half two_p;
+        {
+            const float q = __uint_as_float(*sMmax) / ks;
+            int p = 0;
+            if (q > 0.f && q <= 3.0e38f) p = min(max(ilogbf(q) - 13, -14), 15);
+            two_p = __float2half_rn(ldexpf(1.f, p));
+            scale = ldexpf(ks, p);
+            inv_scale = 1.f / scale;
+        }
+        for (int idx = ew * 32 + lane; idx < 2 * BM * 8; idx += kRefGroups * kEpiWarps * 32) {
+            const int blk = idx >> 10, r = (idx >> 3) & (BM - 1), u = idx & 7;
+            __align__(16) __half h[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) h[q] = __float2half_rn(0.f);
+            if (u == 0) {
+                if (blk == 0) {
+                    const int64_t rr = min(rt * BM + r, a.nr - 1);
+                    offset_split(a.rlogw2[rr] - a.rbias[rr], inv_scale, h[0], h[1]);
+                } else {
+                    h[0] = two_p;
+                    h[1] = two_p;
+                }
+            }
+            *reinterpret_cast<uint4*>((blk ? sKx : sQx) + swz_offset(r, u * 8)) =
+                *reinterpret_cast<const uint4*>(h);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xfull);
         const uint32_t buf = tmem + (uint32_t)(grp * BN) + ((uint32_t)(quarter * 32) << 16);
         tc_fence_before();
         __syncwarp();
@@ -248,7 +313,7 @@ __global__ void __launch_bounds__(kRefThreads, 1) k_half_ref(TcHalfArgs a) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) bp[i] = sb[(32 * cq + 8 * i) / 2];
                 }
-                ref_slice(cur, bp, ks2, nM[2 * h], nM[2 * h + 1], acc[2 * h], acc[2 * h + 1]);
+                ref_slice(cur, bp, ks2, acc[2 * h], acc[2 * h + 1]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bempty[bs]);
@@ -269,7 +334,9 @@ __global__ void __launch_bounds__(kRefThreads, 1) k_half_ref(TcHalfArgs a) {
         const int rloc = quarter * 32 + (lane >> 2) + 8 * kown;
         const int64_t row = rt * BM + rloc;
         const int64_t rr = row < a.nr ? row : a.nr - 1;
-        const float M = a.rlogw2[rr] - a.rbias[rr];
+        __half mhi, mlo;
+        offset_split(a.rlogw2[rr] - a.rbias[rr], inv_scale, mhi, mlo);
+        const float M = offset_applied(mhi, mlo, scale);
         // every group used the same offset M: the row sum is the groups'
         // sums, added in a fixed order
         if (grp > 0) sMerge[(grp - 1) * BM + rloc] = S;
