@@ -14,6 +14,8 @@
 #include "fs_debug.cuh"
 #include "fs_internal.cuh"
 
+#include <type_traits>
+
 namespace fs {
 
 namespace {
@@ -110,6 +112,193 @@ __device__ __forceinline__ void fma_sum_exp(const uint64_t (&s)[RP][G], const ui
     }
 }
 
+// S[r] += sum_u 2^{s[r][u]}: the scores already carry the row offset (folded
+// into the staged column records).
+template <int RP, int G>
+__device__ __forceinline__ void fma_sum_exp_noff(const uint64_t (&s)[RP][G], uint64_t (&S)[RP]) {
+#pragma unroll
+    for (int r = 0; r < RP; ++r) {
+        uint64_t e[G];
+#pragma unroll
+        for (int u = 0; u < G; ++u) {
+            float x0, x1;
+            upk(s[r][u], x0, x1);
+            e[u] = pk(ex2(x0), ex2(x1));
+        }
+#pragma unroll
+        for (int w = 1; w < G; w *= 2) {
+#pragma unroll
+            for (int u = 0; u + w < G; u += 2 * w) e[u] = add2(e[u], e[u + w]);
+        }
+        S[r] = add2(S[r], e[0]);
+    }
+}
+
+// Sum of NV values over the CTA, the same bits in every thread: warp
+// butterflies, then the warps' sums in warp order (red: NV * (warps + 1)).
+template <int NV>
+__device__ __forceinline__ void cta_sum(float (&v)[NV], float* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int W = kThreads / 32;
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+#pragma unroll
+        for (int o = 16; o; o >>= 1) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
+    if (lane == 0)
+#pragma unroll
+        for (int k = 0; k < NV; ++k) red[warp * NV + k] = v[k];
+    __syncthreads();
+    if (threadIdx.x < NV) {
+        float t = 0.f;
+        for (int w = 0; w < W; ++w) t += red[w * NV + threadIdx.x];
+        red[W * NV + threadIdx.x] = t;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < NV; ++k) v[k] = red[W * NV + k];
+    __syncthreads();
+}
+
+// Folded offsets (rows in Morton order).  The CTA fits its rows' previous
+// LSEs M_i by an affine function of their kappa-scaled coordinates q_i,
+// A_i = mu + h . q_i (least squares; a D x D Cholesky solve, h = 0 when
+// singular), with mu raised so the largest residual M_i - A_i is kFoldTop.
+// Staging the columns as (y - h, bias - mu) makes the score chain yield
+// s_ij - A_i.  Sums relative to A_i stay in the guarded range while the
+// residuals spread less than kFoldSpread; a CTA whose rows spread more keeps
+// the per-row offsets (fold = false).  fit[0 .. D-1] = h, fit[D] = mu.
+constexpr float kFoldTop = 80.f;
+constexpr float kFoldSpread = 130.f;
+
+template <int D, int RPT>
+__device__ __forceinline__ bool cta_offset_fit(const float (&qv)[RPT][D], const float (&M)[RPT],
+                                               const bool (&valid)[RPT], float* red, float* fit) {
+    float m1[D + 2];
+#pragma unroll
+    for (int k = 0; k < D + 2; ++k) m1[k] = 0.f;
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+        if (!valid[i]) continue;
+        m1[0] += 1.f;
+        m1[1] += M[i];
+#pragma unroll
+        for (int k = 0; k < D; ++k) m1[2 + k] += qv[i][k];
+    }
+    cta_sum<D + 2>(m1, red);
+    const float inv_n = 1.f / m1[0];
+    const float mbar = m1[1] * inv_n;
+    float qbar[D];
+#pragma unroll
+    for (int k = 0; k < D; ++k) qbar[k] = m1[2 + k] * inv_n;
+    constexpr int NC = D * (D + 1) / 2;
+    float m2[NC + D];
+#pragma unroll
+    for (int k = 0; k < NC + D; ++k) m2[k] = 0.f;
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+        if (!valid[i]) continue;
+        const float dm = M[i] - mbar;
+        int t = 0;
+#pragma unroll
+        for (int k = 0; k < D; ++k) {
+            const float dk = qv[i][k] - qbar[k];
+            m2[NC + k] += dk * dm;
+#pragma unroll
+            for (int l = k; l < D; ++l) m2[t++] += dk * (qv[i][l] - qbar[l]);
+        }
+    }
+    cta_sum<NC + D>(m2, red);
+    float C[D][D], c[D], h[D];
+    {
+        int t = 0;
+        float tr = 0.f;
+#pragma unroll
+        for (int k = 0; k < D; ++k) {
+            c[k] = m2[NC + k];
+#pragma unroll
+            for (int l = k; l < D; ++l) {
+                C[k][l] = C[l][k] = m2[t++];
+            }
+            tr += C[k][k];
+        }
+        const float lam = 1e-4f * tr / D + 1e-30f;
+#pragma unroll
+        for (int k = 0; k < D; ++k) C[k][k] += lam;
+    }
+    bool ok = true;
+#pragma unroll
+    for (int k = 0; k < D; ++k) {
+#pragma unroll
+        for (int l = 0; l < k; ++l) C[k][k] -= C[k][l] * C[k][l];
+        ok = ok && C[k][k] > 0.f;
+        C[k][k] = sqrtf(fmaxf(C[k][k], 1e-30f));
+#pragma unroll
+        for (int r = k + 1; r < D; ++r) {
+#pragma unroll
+            for (int l = 0; l < k; ++l) C[r][k] -= C[r][l] * C[k][l];
+            C[r][k] /= C[k][k];
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < D; ++k) {
+#pragma unroll
+        for (int l = 0; l < k; ++l) c[k] -= C[k][l] * c[l];
+        c[k] /= C[k][k];
+    }
+#pragma unroll
+    for (int k = D - 1; k >= 0; --k) {
+#pragma unroll
+        for (int l = k + 1; l < D; ++l) c[k] -= C[l][k] * h[l];
+        h[k] = c[k] / C[k][k];
+        ok = ok && isfinite(h[k]);
+    }
+    if (!ok) {
+#pragma unroll
+        for (int k = 0; k < D; ++k) h[k] = 0.f;
+    }
+    float mu = mbar;
+#pragma unroll
+    for (int k = 0; k < D; ++k) mu -= h[k] * qbar[k];
+    // residual range over the CTA (max of r and of -r)
+    float rr[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+        if (!valid[i]) continue;
+        float a = mu;
+#pragma unroll
+        for (int k = 0; k < D; ++k) a = fmaf(h[k], qv[i][k], a);
+        rr[0] = fmaxf(rr[0], M[i] - a);
+        rr[1] = fmaxf(rr[1], a - M[i]);
+    }
+    {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        constexpr int W = kThreads / 32;
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+            for (int o = 16; o; o >>= 1) rr[k] = fmaxf(rr[k], __shfl_xor_sync(0xffffffffu, rr[k], o));
+        if (lane == 0) {
+            red[2 * warp] = rr[0];
+            red[2 * warp + 1] = rr[1];
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float a = -INFINITY, b = -INFINITY;
+            for (int w = 0; w < W; ++w) {
+                a = fmaxf(a, red[2 * w]);
+                b = fmaxf(b, red[2 * w + 1]);
+            }
+            const bool fold = a + b <= kFoldSpread && isfinite(a + b);
+#pragma unroll
+            for (int k = 0; k < D; ++k) fit[k] = h[k];
+            fit[D] = mu + a - kFoldTop;
+            fit[D + 1] = fold ? 1.f : 0.f;
+        }
+        __syncthreads();
+    }
+    return fit[D + 1] != 0.f;
+}
+
 // Online fold of G scores per row into (M, S): S = sum 2^{s - M}.  Mt = M +
 // slack is the threshold a new max must pass to move M; nm holds the packed
 // -M of each row pair.  The check is warp-uniform, so the rescale branch
@@ -153,17 +342,20 @@ __device__ __forceinline__ void push_fix(const HalfArgs& a, int64_t row) {
 }
 
 // Half-update, RP row pairs per thread (rows row0 + tid + i * kThreads,
-// i < 2 RP).  REF = false: online max.  REF = true: each row's offset is the
-// LSE of its previous half-update, log2 w_i - (bias slot), so no max is
-// tracked; the sum is range-checked at the end (here when the split is the
-// whole row, else in the merge).
-template <int D, int RP, bool REF>
+// i < 2 RP).  MODE 0: online max.  MODE 1: each row's offset is the LSE of
+// its previous half-update, log2 w_i - (bias slot), so no max is tracked;
+// the sum is range-checked at the end (here when the split is the whole row,
+// else in the merge).  MODE 2: as 1, through the CTA's affine fit of those
+// LSEs folded into the staged columns (cta_offset_fit; rows in Morton order).
+template <int D, int RP, int MODE>
 __global__ void __launch_bounds__(kThreads, D <= 8 ? 3 : 2) k_half_fma(HalfArgs a) {
+    constexpr bool REF = MODE >= 1;
     constexpr int DS = fma_stride(D);
     constexpr int DD = fma_dup_stride(D);
     constexpr int CH = fma_chunk(D);
     constexpr int RPT = 2 * RP;
     __shared__ float4 sc[CH * DD / 4];
+    __shared__ float fit[D + 1];
 
     const int tid = threadIdx.x;
     const int64_t row0 = (int64_t)blockIdx.x * (kThreads * RPT);
@@ -191,34 +383,67 @@ __global__ void __launch_bounds__(kThreads, D <= 8 ? 3 : 2) k_half_fma(HalfArgs 
         S[r] = pk(0.f, 0.f);
         nm[r] = REF ? pk(-M[2 * r], -M[2 * r + 1]) : pk(INFINITY, INFINITY);
     }
-
-    float* sf = reinterpret_cast<float*>(sc);
-    for (int64_t cb = c0; cb < c1; cb += CH) {
-        const int ncol = (int)min((int64_t)CH, c1 - cb);
-        __syncthreads();
-        // stage (coordinates, bias) records, each value written twice
-        for (int e = tid; e < ncol * (D + 1); e += kThreads) {
-            const int jj = e / (D + 1), k = e - jj * (D + 1);
-            const int64_t src = (cb + jj) * DS + k;
-            const float v = FS_IDX_OK(src, a.nc * DS, 1) ? a.cols[src] : 0.f;
-            sf[jj * DD + 2 * k] = v;
-            sf[jj * DD + 2 * k + 1] = v;
-        }
-        __syncthreads();
-        int j = 0;
-        for (; j + kGroup <= ncol; j += kGroup) {
-            uint64_t s[RP][kGroup];
-            fma_scores<D, RP, kGroup>(sc, j, q, s);
-            if (REF) fma_sum_exp<RP, kGroup>(s, nm, S);
-            else fma_fold<RP, kGroup>(s, M, Mt, nm, S);
-        }
-        for (; j < ncol; ++j) {
-            uint64_t s[RP][1];
-            fma_scores<D, RP, 1>(sc, j, q, s);
-            if (REF) fma_sum_exp<RP, 1>(s, nm, S);
-            else fma_fold<RP, 1>(s, M, Mt, nm, S);
+    // MODE 2: this CTA's fit (k_fma_fit): h, mu and whether it holds
+    bool fold = false;
+    if constexpr (MODE == 2) {
+        const float* fg = a.fit + (int64_t)blockIdx.x * (D + 2);
+        fold = fg[D + 1] != 0.f;
+        if (tid <= D) fit[tid] = fg[tid];    // read by the staging after its barrier
+        if (fold) {
+#pragma unroll
+            for (int r = 0; r < RP; ++r) {
+                float A0 = fg[D], A1 = fg[D];
+#pragma unroll
+                for (int k = 0; k < D; ++k) {
+                    float x0, x1;
+                    upk(q[r][k], x0, x1);
+                    A0 = fmaf(fg[k], x0, A0);
+                    A1 = fmaf(fg[k], x1, A1);
+                }
+                M[2 * r] = A0;
+                M[2 * r + 1] = A1;
+            }
         }
     }
+
+    float* sf = reinterpret_cast<float*>(sc);
+    // the column sweep; FOLD: the staged records carry the CTA's fit and the
+    // scores the row offsets (two copies of the loop, so that the folded one
+    // keeps no per-row offsets live)
+    auto sweep = [&](auto fold_tag) {
+        constexpr bool FOLD = decltype(fold_tag)::value;
+        for (int64_t cb = c0; cb < c1; cb += CH) {
+            const int ncol = (int)min((int64_t)CH, c1 - cb);
+            __syncthreads();
+            // stage (coordinates, bias) records, each value written twice
+            for (int e = tid; e < ncol * (D + 1); e += kThreads) {
+                const int jj = e / (D + 1), k = e - jj * (D + 1);
+                const int64_t src = (cb + jj) * DS + k;
+                float v = FS_IDX_OK(src, a.nc * DS, 1) ? a.cols[src] : 0.f;
+                if (FOLD) v -= fit[k];   // coordinates minus h, bias minus mu
+                sf[jj * DD + 2 * k] = v;
+                sf[jj * DD + 2 * k + 1] = v;
+            }
+            __syncthreads();
+            int j = 0;
+            for (; j + kGroup <= ncol; j += kGroup) {
+                uint64_t s[RP][kGroup];
+                fma_scores<D, RP, kGroup>(sc, j, q, s);
+                if (FOLD) fma_sum_exp_noff<RP, kGroup>(s, S);
+                else if (REF) fma_sum_exp<RP, kGroup>(s, nm, S);
+                else fma_fold<RP, kGroup>(s, M, Mt, nm, S);
+            }
+            for (; j < ncol; ++j) {
+                uint64_t s[RP][1];
+                fma_scores<D, RP, 1>(sc, j, q, s);
+                if (FOLD) fma_sum_exp_noff<RP, 1>(s, S);
+                else if (REF) fma_sum_exp<RP, 1>(s, nm, S);
+                else fma_fold<RP, 1>(s, M, Mt, nm, S);
+            }
+        }
+    };
+    if (MODE == 2 && fold) sweep(std::true_type{});
+    else sweep(std::false_type{});
 
     float Sf[RPT];
 #pragma unroll
@@ -239,14 +464,51 @@ __global__ void __launch_bounds__(kThreads, D <= 8 ? 3 : 2) k_half_fma(HalfArgs 
     }
 }
 
+// The per-CTA offset fits of a mode-2 half-update: the same CTA grid over
+// the rows, one fit per row block into a.fit.
+template <int D, int RP>
+__global__ void __launch_bounds__(kThreads) k_fma_fit(HalfArgs a) {
+    constexpr int DS = fma_stride(D);
+    constexpr int RPT = 2 * RP;
+    __shared__ float red[(D * (D + 1) / 2 + D) * (kThreads / 32 + 1)];
+    __shared__ float fit[D + 2];
+    const int tid = threadIdx.x;
+    const int64_t row0 = (int64_t)blockIdx.x * (kThreads * RPT);
+    float qv[RPT][D], M[RPT];
+    bool valid[RPT];
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+        const int64_t r = row0 + tid + i * kThreads;
+        valid[i] = r < a.nr;
+        const int64_t rc = r < a.nr ? r : a.nr - 1;
+#pragma unroll
+        for (int k = 0; k < D; ++k) qv[i][k] = a.rows[rc * DS + k] * a.kappa;
+        M[i] = a.rlogw2[rc] - a.rows[rc * DS + D];
+    }
+    cta_offset_fit<D, RPT>(qv, M, valid, red, fit);
+    if (tid < D + 2) a.fit[(int64_t)blockIdx.x * (D + 2) + tid] = fit[tid];
+}
+
 template <int D>
 cudaError_t launch_half_fma_t(const HalfArgs& a, cudaStream_t s) {
     constexpr int RP = fma_row_pairs(D);
     const int64_t rows_per_block = (int64_t)kThreads * 2 * RP;
     static_assert(kThreads * 2 * RP == fma_rows_per_block(D), "row blocking");
     dim3 grid((unsigned)((a.nr + rows_per_block - 1) / rows_per_block), (unsigned)a.splits);
-    if (a.use_ref) k_half_fma<D, RP, true><<<grid, kThreads, 0, s>>>(a);
-    else k_half_fma<D, RP, false><<<grid, kThreads, 0, s>>>(a);
+    bool launched = false;
+    if constexpr (D <= 4) {
+        if (a.use_ref == 2) {
+            if (a.fit == nullptr) return cudaErrorInvalidValue;
+            k_fma_fit<D, RP><<<grid.x, kThreads, 0, s>>>(a);
+            count_launch();
+            k_half_fma<D, RP, 2><<<grid, kThreads, 0, s>>>(a);
+            launched = true;
+        }
+    }
+    if (!launched) {
+        if (a.use_ref) k_half_fma<D, RP, 1><<<grid, kThreads, 0, s>>>(a);
+        else k_half_fma<D, RP, 0><<<grid, kThreads, 0, s>>>(a);
+    }
     count_launch();
     return cudaGetLastError();
 }
@@ -482,7 +744,7 @@ int half_fma_residency() {
     static std::atomic<int> cached{0};
     int v = cached.load(std::memory_order_relaxed);
     if (v == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, k_half_fma<D, fma_row_pairs(D), true>,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, k_half_fma<D, fma_row_pairs(D), 1>,
                                                           kThreads, 0) != cudaSuccess || v < 1)
             v = 1;
         cached.store(v, std::memory_order_relaxed);

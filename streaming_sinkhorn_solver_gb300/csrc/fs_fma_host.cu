@@ -1,6 +1,7 @@
 // Host orchestration of the FP32-FMA path (d <= 16): buffer layout,
 // preparation, the alternating half-update loop and plan application.
 #include "fs_host.cuh"
+#include "fs_morton.cuh"
 #include "fs_shard.cuh"
 
 #include <algorithm>
@@ -31,12 +32,23 @@ FmaPlan plan_fma(int64_t n, int64_t m, int32_t d, int sms, const fs_options* opt
 struct FmaBufs {
     size_t shift_part, shift, PX, PY, nx, ny, lax, lby, partial, phi, apply_part, counter, fix_list,
         fix_count;
+    // Morton order of the solve (fold_offsets): permutations, sort buffers and
+    // the potentials in that order
+    MortonBufs srt;
+    size_t perm_x, perm_y, fs, gs, fit;
 };
 
 // Problems from this many score pairs up use reference offsets after the
 // first iteration: below it the fixup launch costs more than the online max.
 constexpr double kRefMinPairs = 67108864.0;   // 2^26
 constexpr int kOnlineIters = 2;
+
+// Solves that use reference offsets at d <= 3 run in Morton order, where the
+// rows of a CTA are close in space and their offsets fold into the staged
+// columns (k_half_fma mode 2): a pair then costs d FMAs, one ex2 and one add.
+bool fold_offsets(int64_t n, int64_t m, int32_t d) {
+    return d <= kMortonMaxDim && (double)n * (double)m >= kRefMinPairs;
+}
 
 void layout_fma(Layout& L, FmaBufs& B, int64_t n, int64_t m, int32_t d, const FmaPlan& p,
                 int apply_k, int apply_splits) {
@@ -56,6 +68,17 @@ void layout_fma(Layout& L, FmaBufs& B, int64_t n, int64_t m, int32_t d, const Fm
     B.counter = L.take(sizeof(unsigned int) * 4);
     B.fix_list = L.take(sizeof(int) * (size_t)std::max(n, m));
     B.fix_count = L.take(sizeof(unsigned int) * 2);
+    B.perm_x = B.perm_y = B.fs = B.gs = B.fit = 0;
+}
+
+void layout_fold(Layout& L, FmaBufs& B, int64_t n, int64_t m, int32_t d, const FmaPlan& p) {
+    layout_morton(L, B.srt, n, m, d);
+    const int64_t rpb = fma_rows_per_block(p.D);
+    B.fit = L.take(sizeof(float) * (size_t)((std::max(n, m) + rpb - 1) / rpb) * (p.D + 2));
+    B.perm_x = L.take(sizeof(int) * (size_t)n);
+    B.perm_y = L.take(sizeof(int) * (size_t)m);
+    B.fs = L.take(sizeof(float) * (size_t)n);
+    B.gs = L.take(sizeof(float) * (size_t)m);
 }
 
 int apply_splits_for(int64_t n, int64_t m, int32_t k, int sms, const fs_options* opt, int64_t* cps) {
@@ -76,6 +99,7 @@ int64_t workspace_bytes_fma(int64_t n, int64_t m, int32_t d, int32_t k, int sms,
     Layout L;
     FmaBufs B;
     layout_fma(L, B, n, m, d, p, k, splits);
+    if (k == 0 && fold_offsets(n, m, d)) layout_fold(L, B, n, m, d, p);
     return (int64_t)L.off;
 }
 
@@ -85,12 +109,20 @@ fs_status solve_fma(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) 
     const FmaPlan p = plan_fma(n, m, d, c.ws->sms, opt);
     FmaBufs B;
     layout_fma(c.L, B, n, m, d, p, 0, 1);
+    const bool fold = fold_offsets(n, m, d);
+    if (fold) layout_fold(c.L, B, n, m, d, p);
     CosBufs cb;
     layout_cos(c.L, cb, P);
     FS_TRY(ensure_capacity(c));
     for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g}) bind(c, *A);
     for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.g}) FS_TRY(upload(c, *A));
     FS_TRY(prepare_cos(c, P, cb));
+    // Morton order: rows are packed in it and the potentials computed in it
+    // (pot_f, pot_g), then scattered back to the caller's order
+    const int* perm_x = fold ? c.at<int>(B.perm_x) : nullptr;
+    const int* perm_y = fold ? c.at<int>(B.perm_y) : nullptr;
+    float* pot_f = fold ? c.at<float>(B.fs) : P.f.dev;
+    float* pot_g = fold ? c.at<float>(B.gs) : P.g.dev;
 
     const double eps = (double)P.eps;
     const float l_over_eps = (float)(kLog2e / eps);
@@ -106,21 +138,25 @@ fs_status solve_fma(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) 
     float2* part = c.at<float2>(B.partial);
 
     const int tp = timing_begin(c.stream);
+    if (fold)
+        FS_TRY(morton_permutation(c, B.srt, P.X.dev, n, P.Y.dev, m, d, c.at<int>(B.perm_x),
+                                  c.at<int>(B.perm_y)));
     FS_CUDA(launch_shift(P.X.dev, n, P.Y.dev, m, d, c.at<double>(B.shift_part), kShiftBlocks, shift,
                          c.stream));
     FS_CUDA(launch_pack_fma(P.X.dev, P.a.dev, nullptr, n, d, p.D, shift, l_over_eps, PX, nx, lax,
-                            c.stream));
+                            c.stream, perm_x));
     FS_CUDA(launch_pack_fma(P.Y.dev, P.b.dev, P.g.dev, m, d, p.D, shift, l_over_eps, PY, ny, lby,
-                            c.stream));
+                            c.stream, perm_y));
     timing_end(tp, TIME_PREP, c.stream);
 
     int* fix_list = c.at<int>(B.fix_list);
     unsigned int* fix_count = c.at<unsigned int>(B.fix_count);
     FS_CUDA(cudaMemsetAsync(fix_count, 0, 2 * sizeof(unsigned int), c.stream));
-    HalfArgs hf{PX, PY, n, m, kappa, eps_ln2, nx, lax, P.f.dev, part, p.splits_f, p.cps_f,
+    HalfArgs hf{PX, PY, n, m, kappa, eps_ln2, nx, lax, pot_f, part, p.splits_f, p.cps_f,
                 0, fix_list, fix_count};
-    HalfArgs hg{PY, PX, m, n, kappa, eps_ln2, ny, lby, P.g.dev, part, p.splits_g, p.cps_g,
+    HalfArgs hg{PY, PX, m, n, kappa, eps_ln2, ny, lby, pot_g, part, p.splits_g, p.cps_g,
                 0, fix_list, fix_count};
+    hf.fit = hg.fit = fold ? c.at<float>(B.fit) : nullptr;
     // The first iterations take the online max: the initial potentials may be
     // arbitrary and the first updates move the LSEs by large amounts.  Later
     // ones use reference offsets, with a guarded sum and a fixup of the rows
@@ -137,7 +173,7 @@ fs_status solve_fma(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) 
             shard_range(h.nr, unit, shards, s, &r0, &r1);
             if (r1 <= r0) continue;
             HalfArgs hs = h;
-            hs.use_ref = ref ? 1 : 0;
+            hs.use_ref = ref ? (fold ? 2 : 1) : 0;
             hs.rows = h.rows + r0 * p.DS;
             hs.nr = r1 - r0;
             hs.rnorm = h.rnorm + r0;
@@ -158,6 +194,10 @@ fs_status solve_fma(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) 
         const bool ref = ref_ok && it >= kOnlineIters;
         FS_TRY(half(hf, p.splits_f, ref));
         FS_TRY(half(hg, p.splits_g, ref));
+    }
+    if (fold) {
+        FS_CUDA(launch_scatter_rows(pot_f, perm_x, n, P.f.dev, c.stream));
+        FS_CUDA(launch_scatter_rows(pot_g, perm_y, m, P.g.dev, c.stream));
     }
     if (opt && opt->check_finite) {
         FS_TRY(scan_finite(c, P.f.dev, n, c.at<unsigned int>(B.counter)));

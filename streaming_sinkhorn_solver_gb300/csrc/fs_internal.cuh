@@ -105,9 +105,11 @@ struct HalfArgs {
     // LSE of its previous half-update (log2 w_i minus its bias slot) instead
     // of an online max; rows whose sum leaves the guarded range are appended
     // to fix_list (fix_count[0] entries) for launch_fix_fma.
-    int use_ref;
+    int use_ref;              // 0 online max, 1 reference offsets, 2 reference offsets
+                              // folded per CTA (rows in Morton order; d <= 4)
     int* fix_list;            // [nr]
     unsigned int* fix_count;  // [2], zero before the first guarded half-update
+    float* fit;               // use_ref 2: [row blocks x (D + 2)] per-CTA offset fits
 };
 cudaError_t launch_half_fma(int D, const HalfArgs& a, cudaStream_t s);
 // Recompute the listed rows with the online max; resets the list.
@@ -156,9 +158,15 @@ cudaError_t launch_shift(const float* X, int64_t n, const float* Y, int64_t m, i
 
 // FMA path: centre, pack, norms and log2-weights of one side.  If `pot` is
 // non-null the bias slot is filled from it: bias = (pot - |p~|^2) L/eps + log2 w.
+// With `perm`, packed row i is the caller's row perm[i] (P, w and pot are read
+// there); outputs are in the permuted order.
 cudaError_t launch_pack_fma(const float* P, const float* w, const float* pot, int64_t rows, int d,
                             int D, const float* shift, float l_over_eps, float* packed,
-                            float* norm, float* logw2, cudaStream_t s);
+                            float* norm, float* logw2, cudaStream_t s, const int* perm = nullptr);
+
+// dst[perm[i]] = src[i], i < rows (back from a permuted order).
+cudaError_t launch_scatter_rows(const float* src, const int* perm, int64_t rows, float* dst,
+                                cudaStream_t s);
 
 // phi_i = (f_i - |x~_i|^2) L/eps (apply).
 cudaError_t launch_phi(const float* f, const float* norm, int64_t n, float l_over_eps, float* phi,

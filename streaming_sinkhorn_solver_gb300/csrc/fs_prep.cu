@@ -58,10 +58,12 @@ __global__ void k_pack_fma(const float* __restrict__ P, const float* __restrict_
                            const float* __restrict__ pot, int64_t rows, int d,
                            const float* __restrict__ shift, float l_over_eps,
                            float* __restrict__ packed, float* __restrict__ norm,
-                           float* __restrict__ logw2) {
+                           float* __restrict__ logw2, const int* __restrict__ perm) {
     constexpr int DS = fma_stride(D);
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= rows) return;
+    const int64_t si = perm != nullptr ? (int64_t)perm[i] : i;
+    if (!FS_IDX_OK(si, rows, 22)) return;
     float v[DS];
     float nrm = 0.f;
 #pragma unroll
@@ -69,13 +71,13 @@ __global__ void k_pack_fma(const float* __restrict__ P, const float* __restrict_
 #pragma unroll
     for (int k = 0; k < D; ++k) {
         if (k < d) {
-            const float c = P[i * d + k] - shift[k];
+            const float c = P[si * d + k] - shift[k];
             v[k] = c;
             nrm = fmaf(c, c, nrm);
         }
     }
-    const float lw = log2f(w[i]);
-    if (pot != nullptr) v[D] = (pot[i] - nrm) * l_over_eps + lw;
+    const float lw = log2f(w[si]);
+    if (pot != nullptr) v[D] = (pot[si] - nrm) * l_over_eps + lw;
     float4* dst = reinterpret_cast<float4*>(packed + i * DS);
 #pragma unroll
     for (int q = 0; q < DS / 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
@@ -85,14 +87,14 @@ __global__ void k_pack_fma(const float* __restrict__ P, const float* __restrict_
 
 cudaError_t launch_pack_fma(const float* P, const float* w, const float* pot, int64_t rows, int d,
                             int D, const float* shift, float l_over_eps, float* packed,
-                            float* norm, float* logw2, cudaStream_t s) {
+                            float* norm, float* logw2, cudaStream_t s, const int* perm) {
     const int threads = 256;
     const int64_t blocks = (rows + threads - 1) / threads;
     switch (D) {
 #define FS_PACK_CASE(DD)                                                                           \
     case DD:                                                                                       \
         k_pack_fma<DD><<<(unsigned)blocks, threads, 0, s>>>(P, w, pot, rows, d, shift, l_over_eps, \
-                                                            packed, norm, logw2);                  \
+                                                            packed, norm, logw2, perm);            \
         break;
         FS_PACK_CASE(2)
         FS_PACK_CASE(3)
@@ -103,6 +105,21 @@ cudaError_t launch_pack_fma(const float* P, const float* w, const float* pot, in
         default:
             return cudaErrorInvalidValue;
     }
+    count_launch();
+    return cudaGetLastError();
+}
+
+__global__ void k_scatter_rows(const float* __restrict__ src, const int* __restrict__ perm,
+                               int64_t rows, float* __restrict__ dst) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= rows) return;
+    const int64_t di = perm[i];
+    if (FS_IDX_OK(di, rows, 23)) dst[di] = src[i];
+}
+
+cudaError_t launch_scatter_rows(const float* src, const int* perm, int64_t rows, float* dst,
+                                cudaStream_t s) {
+    k_scatter_rows<<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(src, perm, rows, dst);
     count_launch();
     return cudaGetLastError();
 }

@@ -30,6 +30,7 @@
 // a tensor-core tile would spend most of its K = 16 on padding.
 #include "fs_debug.cuh"
 #include "fs_host.cuh"
+#include "fs_morton.cuh"
 
 #include <algorithm>
 #include <cmath>
@@ -40,7 +41,7 @@ namespace {
 constexpr int kSB = 128;            // points per block
 constexpr int kMortonBits = 21;     // quantisation cells per axis: 2^21
 constexpr int kSortTile = 2048;     // keys per CTA in a radix pass
-constexpr int kSpMaxDim = 3;
+constexpr int kSpMaxDim = kMortonMaxDim;
 
 // ---------------------------------------------------------------------------
 // joint bounding box (order-preserving integer encoding of floats, so that
@@ -1232,7 +1233,7 @@ struct SpSide {
 };
 
 struct SpBufs {
-    size_t box, keys0, keys1, vals0, vals1, hist;
+    MortonBufs srt;
     size_t shift_part, shift;
     SpSide X, Y;
     size_t lists, counts, order, rowsum, red_part, red_out, kept, fix_list, fix_count;
@@ -1265,13 +1266,7 @@ void layout_side(Layout& L, SpSide& s, int64_t cnt, int d) {
 
 void layout_sparse(Layout& L, SpBufs& B, int64_t n, int64_t m, int d, int sms, bool coarse) {
     const int64_t mx = std::max(n, m);
-    const int64_t tiles = (mx + kSortTile - 1) / kSortTile;
-    B.box = L.take(sizeof(unsigned int) * 2 * kSpMaxDim);
-    B.keys0 = L.take(sizeof(uint64_t) * mx);
-    B.keys1 = L.take(sizeof(uint64_t) * mx);
-    B.vals0 = L.take(sizeof(int) * mx);
-    B.vals1 = L.take(sizeof(int) * mx);
-    B.hist = L.take(sizeof(unsigned int) * 256 * tiles);
+    layout_morton(L, B.srt, n, m, d);
     B.shift_part = L.take(sizeof(double) * (size_t)kShiftBlocks * d);
     B.shift = L.take(sizeof(float) * d);
     layout_side(L, B.X, n, d);
@@ -1306,8 +1301,8 @@ void layout_sparse(Layout& L, SpBufs& B, int64_t n, int64_t m, int d, int sms, b
     }
 }
 
-// Morton order of one cloud into side.perm (the joint box is in B.box).
-fs_status sort_side(Call& c, const SpBufs& B, const float* P, int64_t cnt, int d, int* perm_out) {
+// Morton order of one cloud into perm_out (the joint box is in M.box).
+fs_status sort_side(Call& c, const MortonBufs& B, const float* P, int64_t cnt, int d, int* perm_out) {
     uint64_t* k0 = c.at<uint64_t>(B.keys0);
     uint64_t* k1 = c.at<uint64_t>(B.keys1);
     int* v0 = c.at<int>(B.vals0);
@@ -1352,16 +1347,7 @@ fs_status prepare_side(Call& c, const SpBufs& B, const SpSide& s, const float* P
 // Morton sort and per-side preparation shared by the entry points.
 fs_status prepare_sparse(Call& c, const SpBufs& B, const float* X, const float* a, int64_t n,
                          const float* Y, const float* b, int64_t m, int d) {
-    unsigned int* box = c.at<unsigned int>(B.box);
-    k_box_init<<<1, 32, 0, c.stream>>>(box, d);
-    const int64_t pts = n + m;
-    unsigned blocks = grid_for(pts, 256);
-    if (blocks > 1024) blocks = 1024;
-    k_box<<<blocks, 256, 0, c.stream>>>(X, n, Y, m, d, box);
-    count_launch(2);
-    FS_CUDA(cudaGetLastError());
-    FS_TRY(sort_side(c, B, X, n, d, c.at<int>(B.X.perm)));
-    FS_TRY(sort_side(c, B, Y, m, d, c.at<int>(B.Y.perm)));
+    FS_TRY(morton_permutation(c, B.srt, X, n, Y, m, d, c.at<int>(B.X.perm), c.at<int>(B.Y.perm)));
     FS_CUDA(launch_shift(X, n, Y, m, d, c.at<double>(B.shift_part), kShiftBlocks,
                          c.at<float>(B.shift), c.stream));
     FS_TRY(prepare_side(c, B, B.X, X, a, d));
@@ -1674,15 +1660,7 @@ fs_status morton_entry(const float* X, int64_t n, const float* Y, int64_t m, int
     SpBufs B;
     layout_sparse(c.L, B, n, m, d, c.ws->sms, false);
     FS_TRY(ensure_capacity(c));
-    unsigned int* box = c.at<unsigned int>(B.box);
-    k_box_init<<<1, 32, 0, c.stream>>>(box, d);
-    unsigned blocks = grid_for(n + m, 256);
-    if (blocks > 1024) blocks = 1024;
-    k_box<<<blocks, 256, 0, c.stream>>>(X, n, Y, m, d, box);
-    count_launch(2);
-    FS_CUDA(cudaGetLastError());
-    FS_TRY(sort_side(c, B, X, n, d, c.at<int>(B.X.perm)));
-    FS_TRY(sort_side(c, B, Y, m, d, c.at<int>(B.Y.perm)));
+    FS_TRY(morton_permutation(c, B.srt, X, n, Y, m, d, c.at<int>(B.X.perm), c.at<int>(B.Y.perm)));
     k_sp_perm64<<<grid_for(n, 256), 256, 0, c.stream>>>(c.at<int>(B.X.perm), n, perm_x);
     k_sp_perm64<<<grid_for(m, 256), 256, 0, c.stream>>>(c.at<int>(B.Y.perm), m, perm_y);
     count_launch(2);
@@ -1726,6 +1704,33 @@ fs_status screen_entry(const float* X, const float* a, int64_t n, const float* Y
 }
 
 }  // namespace
+
+void layout_morton(Layout& L, MortonBufs& M, int64_t n, int64_t m, int d) {
+    (void)d;
+    const int64_t mx = std::max(n, m);
+    const int64_t tiles = (mx + kSortTile - 1) / kSortTile;
+    M.box = L.take(sizeof(unsigned int) * 2 * kSpMaxDim);
+    M.keys0 = L.take(sizeof(uint64_t) * mx);
+    M.keys1 = L.take(sizeof(uint64_t) * mx);
+    M.vals0 = L.take(sizeof(int) * mx);
+    M.vals1 = L.take(sizeof(int) * mx);
+    M.hist = L.take(sizeof(unsigned int) * 256 * tiles);
+}
+
+fs_status morton_permutation(Call& c, const MortonBufs& M, const float* X, int64_t n,
+                             const float* Y, int64_t m, int d, int* perm_x, int* perm_y) {
+    if (d < 1 || d > kSpMaxDim) return fail(FS_ERR_UNSUPPORTED, "Morton order takes 1 <= d <= %d", kSpMaxDim);
+    unsigned int* box = c.at<unsigned int>(M.box);
+    k_box_init<<<1, 32, 0, c.stream>>>(box, d);
+    unsigned blocks = grid_for(n + m, 256);
+    if (blocks > 1024) blocks = 1024;
+    k_box<<<blocks, 256, 0, c.stream>>>(X, n, Y, m, d, box);
+    count_launch(2);
+    FS_CUDA(cudaGetLastError());
+    FS_TRY(sort_side(c, M, X, n, d, perm_x));
+    FS_TRY(sort_side(c, M, Y, m, d, perm_y));
+    return FS_OK;
+}
 
 FS_BOUNDS_READER(bounds_take_sparse)
 

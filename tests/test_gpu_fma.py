@@ -221,3 +221,23 @@ def test_reference_offset_path_with_fixups(eps, iters):
     f, g, fr, gr, C, _ = _solve_both(inp, eps, iters, path="auto")
     assert max_abs(f, fr) <= F_TOL_FMA * C.max()
     assert max_abs(g, gr) <= F_TOL_FMA * C.max()
+
+
+def test_folded_offsets_do_not_depend_on_the_row_order():
+    """From 2^26 score pairs on, a d <= 3 solve runs in Morton order with the
+    row offsets folded into the staged columns (one affine fit per block of
+    rows).  Shuffling the caller's rows must give the same potentials,
+    shuffled the same way, up to rounding (the Morton order breaks ties of
+    equal codes by the caller's order, so a block's rows, and its fit, can
+    differ slightly), and both must match the oracle."""
+    inp = make_inputs("c2_n10k_d3", n=8300, m=8200, seed=404)
+    eps, iters = 0.01, 6
+    perm = np.random.default_rng(5).permutation(8300)
+    sh = dict(inp, X=np.ascontiguousarray(inp["X"][perm]), a=np.ascontiguousarray(inp["a"][perm]))
+    f, g, fr, gr, C, _ = _solve_both(inp, eps, iters, path="auto")
+    t = to_dev(sh)
+    fs_, gs_ = fs.fs_sinkhorn_solve(t["X"], t["a"], t["Y"], t["b"], eps, iters)
+    tol = F_TOL_FMA * C.max()
+    assert max_abs(np64(fs_), f[perm]) <= tol
+    assert max_abs(np64(gs_), g) <= tol
+    assert max_abs(f, fr) <= tol and max_abs(g, gr) <= tol
