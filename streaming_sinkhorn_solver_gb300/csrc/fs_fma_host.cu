@@ -43,11 +43,15 @@ struct FmaBufs {
 constexpr double kRefMinPairs = 67108864.0;   // 2^26
 constexpr int kOnlineIters = 2;
 
-// Solves that use reference offsets at d <= 3 run in Morton order, where the
-// rows of a CTA are close in space and their offsets fold into the staged
+// Solves from this many score pairs up at d <= 3 run in Morton order, where
+// the rows of a CTA are close in space and their offsets fold into the staged
 // columns (k_half_fma mode 2): a pair then costs d FMAs, one ex2 and one add.
+// Below it the fit launch per half-update costs more than the fold saves
+// (measured: +6 % per half-update at 10^8 pairs, -13 % at 2.5 * 10^9).
+constexpr double kFoldMinPairs = 268435456.0;   // 2^28
+
 bool fold_offsets(int64_t n, int64_t m, int32_t d) {
-    return d <= kMortonMaxDim && (double)n * (double)m >= kRefMinPairs;
+    return d <= kMortonMaxDim && (double)n * (double)m >= kFoldMinPairs;
 }
 
 void layout_fma(Layout& L, FmaBufs& B, int64_t n, int64_t m, int32_t d, const FmaPlan& p,

@@ -27,6 +27,8 @@ def _lib():
 def _inputs(kind):
     if kind == "fma_ref":          # n m = 7.4e7 > 2^26: reference offsets from iteration 3
         return make_inputs("c2_n10k_d3", n=9000, m=8200, seed=301), 0.005, 6, "fma"
+    if kind == "fma_fold":         # n m = 2.7e8 >= 2^28: Morton order, offsets folded per CTA
+        return make_inputs("c2_n10k_d3", n=16400, m=16400, seed=306), 0.01, 5, "fma"
     if kind == "fma_small":        # online maxima only
         return random_cloud(1500, 1000, 8, seed=302, spread=0.5, weights="lognormal"), 0.05, 4, "fma"
     if kind == "tc_ref":           # one-CTA tensor kernels, reference offsets
@@ -45,7 +47,8 @@ def _solve(t, eps, iters, path, splits, shards):
     return f.cpu().numpy(), g.cpu().numpy()
 
 
-@pytest.mark.parametrize("kind", ["fma_ref", "fma_small", "tc_ref", "pair_ref", "tc_small"])
+@pytest.mark.parametrize("kind", ["fma_ref", "fma_fold", "fma_small", "tc_ref", "pair_ref",
+                                  "tc_small"])
 @pytest.mark.parametrize("splits", [0, 1])
 def test_row_shards_are_bitwise_the_unsharded_solve(kind, splits):
     import torch
