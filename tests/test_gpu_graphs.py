@@ -18,10 +18,11 @@ def _lib():
     fs.load_library()
 
 
-@pytest.mark.parametrize("d", [3, 64])
-def test_solve_and_apply_replay_bitwise(d):
+@pytest.mark.parametrize("d,n,m", [(3, 3000, 2800), (64, 3000, 2800), (3, 16400, 16400)])
+def test_solve_and_apply_replay_bitwise(d, n, m):
+    """(3, 16400, 16400): 2.7e8 score pairs, so the captured solve includes
+    the Morton sort, the per-CTA offset fits and the scatter back."""
     import torch
-    n, m = 3000, 2800
     inp = random_cloud(n, m, d, seed=900 + d, spread=1.0 / np.sqrt(d), weights="lognormal")
     t = to_dev(inp)
     eps, iters = 0.05, 12
