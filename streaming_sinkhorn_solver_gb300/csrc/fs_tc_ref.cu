@@ -288,9 +288,12 @@ __global__ void __launch_bounds__(kRefThreads, 1) k_half_ref(TcHalfArgs a) {
             const uint64_t* sb =
                 reinterpret_cast<const uint64_t*>(sBias + bs * kBiasBytes + cpair * 4);
             // slices s = 2 cq + h: column quarter cq, lane half h; the next
-            // slice's load is in flight while one is summed
+            // slice's load is in flight while one is summed, and the next
+            // quarter's bias pairs while its second slice is
             float va[16], vb[16];
-            uint64_t bp[4];
+            uint64_t bp[4], bn[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) bp[i] = sb[(8 * i) / 2];
             tmem_ld16x32(buf, va);
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
@@ -309,11 +312,15 @@ __global__ void __launch_bounds__(kRefThreads, 1) k_half_ref(TcHalfArgs a) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&tempty[grp]);
                 }
-                if (h == 0) {
+                if (h == 1 && cq < 3) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) bp[i] = sb[(32 * cq + 8 * i) / 2];
+                    for (int i = 0; i < 4; ++i) bn[i] = sb[(32 * (cq + 1) + 8 * i) / 2];
                 }
                 ref_slice(cur, bp, ks2, acc[2 * h], acc[2 * h + 1]);
+                if (h == 1 && cq < 3) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) bp[i] = bn[i];
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bempty[bs]);
