@@ -513,23 +513,40 @@ cudaError_t launch_half_fma_t(const HalfArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// (M, S) := the (max, sum) pair of the union: S 2^M + So 2^Mo = S' 2^M'.
+__device__ __forceinline__ void merge_pair(float& M, float& S, float Mo, float So) {
+    const float Mn = fmaxf(M, Mo);
+    S = (M == -INFINITY ? 0.f : S * ex2(M - Mn)) + (Mo == -INFINITY ? 0.f : So * ex2(Mo - Mn));
+    M = Mn;
+}
+
+// Merge of the column splits' (max, sum) pairs of each row: `lanes` threads
+// per row (a power of two up to 32, about the split count), each folding
+// the splits l, l + lanes, ... in order, then a butterfly over the row's
+// lanes; fixed assignment and order, so the result does not depend on
+// timing.  Whole warps run, so that every lane takes part in the shuffles.
 __global__ void k_merge_lse(const float2* __restrict__ partial, int splits, int64_t nr,
                             const float* __restrict__ rnorm, const float* __restrict__ rlogw2,
                             float eps_ln2, float* __restrict__ pot, float* __restrict__ bias,
                             int64_t bias_stride, int* __restrict__ fix_list,
-                            unsigned int* __restrict__ fix_count) {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= nr) return;
-    float M = -INFINITY;
-    for (int sp = 0; sp < splits; ++sp)
-        if (FS_IDX_OK((int64_t)sp * nr + i, (int64_t)splits * nr, 3))
-            M = fmaxf(M, partial[(int64_t)sp * nr + i].x);
-    float S = 0.f;
-    for (int sp = 0; sp < splits; ++sp) {
-        if (!FS_IDX_OK((int64_t)sp * nr + i, (int64_t)splits * nr, 3)) continue;
-        const float2 p = partial[(int64_t)sp * nr + i];
-        if (p.x != -INFINITY) S += p.y * ex2(p.x - M);   // a padding-only split adds nothing
+                            unsigned int* __restrict__ fix_count, int lanes) {
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t i = t / lanes;
+    const int l = (int)(t % lanes);
+    float M = -INFINITY, S = 0.f;
+    if (i < nr) {
+        for (int sp = l; sp < splits; sp += lanes) {
+            if (!FS_IDX_OK((int64_t)sp * nr + i, (int64_t)splits * nr, 3)) continue;
+            const float2 p = partial[(int64_t)sp * nr + i];
+            if (p.x != -INFINITY) merge_pair(M, S, p.x, p.y);   // a padding-only split adds nothing
+        }
     }
+    for (int o = lanes >> 1; o; o >>= 1) {
+        const float Mo = __shfl_xor_sync(0xffffffffu, M, o);
+        const float So = __shfl_xor_sync(0xffffffffu, S, o);
+        merge_pair(M, S, Mo, So);
+    }
+    if (i >= nr || l != 0) return;
     if (fix_list != nullptr && !(S >= kMinRefSum && S <= kMaxRefSum)) {
         const unsigned int slot = atomicAdd(&fix_count[0], 1u);
         if (slot < (unsigned int)nr) fix_list[slot] = (int)i;
@@ -767,8 +784,12 @@ cudaError_t launch_merge_lse(const float2* partial, int splits, int64_t nr, cons
                              const float* rlogw2, float eps_ln2, float* pot, float* bias,
                              int64_t bias_stride, cudaStream_t s, int* fix_list,
                              unsigned int* fix_count) {
-    k_merge_lse<<<(unsigned)((nr + 255) / 256), 256, 0, s>>>(
-        partial, splits, nr, rnorm, rlogw2, eps_ln2, pot, bias, bias_stride, fix_list, fix_count);
+    int lanes = 1;
+    while (lanes < splits && lanes < 32) lanes *= 2;
+    const int64_t threads = nr * lanes;
+    k_merge_lse<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
+        partial, splits, nr, rnorm, rlogw2, eps_ln2, pot, bias, bias_stride, fix_list, fix_count,
+        lanes);
     count_launch();
     return cudaGetLastError();
 }
