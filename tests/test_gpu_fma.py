@@ -223,7 +223,8 @@ def test_reference_offset_path_with_fixups(eps, iters):
     assert max_abs(g, gr) <= F_TOL_FMA * C.max()
 
 
-def test_folded_offsets_match_the_oracle_and_do_not_depend_on_the_row_order():
+@pytest.mark.parametrize("d", [1, 2, 3])
+def test_folded_offsets_match_the_oracle_and_do_not_depend_on_the_row_order(d):
     """From 2^28 score pairs on, a d <= 3 solve runs in Morton order with the
     row offsets folded into the staged columns (one affine fit per block of
     rows).  The last f-update of the solve equals the oracle's point-by-point
@@ -231,9 +232,10 @@ def test_folded_offsets_match_the_oracle_and_do_not_depend_on_the_row_order():
     sampled rows; shuffling the caller's rows gives the same potentials,
     shuffled the same way, up to rounding (the Morton order breaks ties of
     equal codes by the caller's order, so a block's rows, and its fit, can
-    differ slightly)."""
+    differ slightly).  d = 1 pads a zero coordinate, whose row of the fit's
+    normal equations is zero but for the regularisation."""
     n = m = 16400                                    # n m = 2.69e8 >= 2^28
-    inp = make_inputs("c2_n10k_d3", n=n, m=m, seed=404)
+    inp = make_inputs("c2_n10k_d3", n=n, m=m, d=d, seed=404)
     eps, iters = 0.01, 8
     t = to_dev(inp)
     f, g = fs.fs_sinkhorn_solve(t["X"], t["a"], t["Y"], t["b"], eps, iters)
