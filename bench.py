@@ -23,6 +23,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -79,7 +80,10 @@ class ClockSampler:
     def __init__(self, gpu_index: int, tag: str = ""):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}{tag}.csv")
+        # the raw samples go to FS_CLOCK_LOG_DIR when set (to keep them), else
+        # to the temporary directory; the JSON line carries their summary
+        log_dir = os.environ.get("FS_CLOCK_LOG_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(log_dir, f"clocks_gpu{gpu_index}{tag}_{os.getpid()}.csv")
 
     def start(self):
         try:
