@@ -175,3 +175,42 @@ def test_hvp_rejects_bad_arguments(lib):
                       f.ctypes.data, g.ctypes.data, V.ctypes.data, out.ctypes.data, 0, 0.0, None,
                       None)
     assert st == fs.FS_ERR_UNSUPPORTED
+
+
+_CTYPE = {"int32_t": ctypes.c_int32, "int64_t": ctypes.c_int64, "float": ctypes.c_float,
+          "double": ctypes.c_double}
+
+
+def _header_structs():
+    """{struct name: [(field, C type, array length or 0), ...]} from include/*.h."""
+    out = {}
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for mt in re.finditer(r"typedef\s+struct\s+(\w+)\s*\{(.*?)\}\s*(\w+)\s*;", text, flags=re.S):
+            fields = []
+            for decl in mt.group(2).split(";"):
+                decl = decl.strip()
+                if not decl:
+                    continue
+                ctype, names = decl.split(None, 1)
+                for name in names.split(","):
+                    name = name.strip()
+                    arr = re.match(r"(\w+)\[(\d+)\]", name)
+                    fields.append((arr.group(1), ctype, int(arr.group(2))) if arr else (name, ctype, 0))
+            out[mt.group(3)] = fields
+    return out
+
+
+@pytest.mark.parametrize("name", ["fs_options", "fs_sparse_options", "fs_sparse_report"])
+def test_binding_structs_mirror_the_header(name):
+    """The ctypes structures of the binding have the header's fields, in
+    order, with the same types and array lengths, so they have its layout."""
+    want = _header_structs()[name]
+    got = getattr(fs, name)._fields_
+    assert [f for f, _ in got] == [f for f, _, _ in want]
+    for (fname, ctype_b), (_, ctype_h, n) in zip(got, want):
+        ref = _CTYPE[ctype_h] * n if n else _CTYPE[ctype_h]
+        assert ctypes.sizeof(ctype_b) == ctypes.sizeof(ref), fname
+        base = ctype_b._type_ if hasattr(ctype_b, "_length_") else ctype_b
+        assert base == _CTYPE[ctype_h], fname
+        assert getattr(ctype_b, "_length_", 0) == n, fname
