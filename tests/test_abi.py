@@ -214,3 +214,35 @@ def test_binding_structs_mirror_the_header(name):
         base = ctype_b._type_ if hasattr(ctype_b, "_length_") else ctype_b
         assert base == _CTYPE[ctype_h], fname
         assert getattr(ctype_b, "_length_", 0) == n, fname
+
+
+def _header_functions():
+    """{name: (return type, parameter count)} of the functions include/*.h declares."""
+    out = {}
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for mt in re.finditer(r"([A-Za-z_][\w\s\*]*?)\b(fs_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+            ret = " ".join(mt.group(1).split())
+            params = " ".join(mt.group(3).split())
+            n = 0 if params in ("", "void") else params.count(",") + 1
+            out[mt.group(2)] = (ret, n)
+    return out
+
+
+def test_binding_declares_every_signature(lib):
+    """Every declared function has ctypes argtypes of the header's arity and
+    a restype of the header's width (an unset argtypes would pass 64-bit
+    pointers and sizes as C ints)."""
+    funcs = _header_functions()
+    assert "fs_sinkhorn_solve" in funcs and "fs_shard_range" in funcs
+    for name, (ret, n) in funcs.items():
+        fn = getattr(lib, name)
+        if n:
+            assert fn.argtypes is not None and len(fn.argtypes) == n, name
+        if ret.endswith("fs_status"):
+            assert fn.restype in (ctypes.c_int, ctypes.c_int32), name
+        elif ret.endswith("int64_t"):
+            assert fn.restype == ctypes.c_int64, name
+        elif ret.endswith("char*") or ret.endswith("char *"):
+            assert fn.restype == ctypes.c_char_p, name
