@@ -256,6 +256,21 @@ def _cpu_baseline(w, inp, seconds: float):
                       f"columns (d={d}), {dt:.1f} s; the full step is {_work(w, n, m, d)[1]:.3e} pairs"}
 
 
+def arm_config(w) -> dict:
+    """The workload's `config` object, the same for both arms."""
+    n, m, d = w.n, w.m, w.d
+    big = (n + m) * d * 4 > 129e6
+    if w.tau > 0:
+        eps, iters = w.stages[0]
+        return {"workload": w.name, "n": n, "m": m, "d": d, "eps": eps, "iters": iters,
+                "coarse_iters": w.coarse_iters, "tau": w.tau,
+                "l2": "256 MB write between timed steps; inputs also > L2"}
+    return {"workload": w.name, "n": n, "m": m, "d": d,
+            "stages": [list(st) for st in w.stages], "apply": w.apply,
+            "l2": "256 MB write between timed steps; inputs also > L2" if big
+                  else "256 MB write between timed steps"}
+
+
 def run_reference(args, w):
     """The reference arm: the oracle, timed on the host cores."""
     rank, world, _ = _rank_info()
@@ -282,7 +297,7 @@ def run_reference(args, w):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "n": n, "m": m, "d": d, "eps": eps},
+            "config": arm_config(w),
             "cpu_baseline": {"value": value, "unit": "score-pairs/s", "cores": orc.num_threads(),
                              "kind": "oracle",
                              "sample": f"per step: float64 f-update of {rows_per_step} rows "
@@ -468,10 +483,7 @@ def run_gb300(args, w):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16xf16->f32" if tensor_path else "f32", "data": "synthetic",
-            "config": {"workload": w.name, "n": n, "m": m, "d": d,
-                       "stages": [list(s) for s in w.stages], "apply": w.apply,
-                       "l2": "256 MB write between timed steps; inputs also > L2"
-                             if (n + m) * d * 4 > 129e6 else "256 MB write between timed steps"},
+            "config": arm_config(w),
             "iters_per_s": iters_per_s, "roofline": roof, "gpu_launches": int(launches),
             "clocks": clocks,
             "apply_ms": apply_ms / max(apply_n, 1) if apply_n else None,
@@ -634,9 +646,7 @@ def run_sparse(args, w):
             "value_kind": "dense-equivalent score-pairs/s: 2 n m per iteration over the step "
                           "time; the block-sparse solver evaluates only the kept blocks "
                           "(omitted mass per block below tau of its weight)",
-            "config": {"workload": w.name, "n": n, "m": m, "d": d, "eps": eps, "iters": iters,
-                       "coarse_iters": w.coarse_iters, "tau": w.tau,
-                       "l2": "256 MB write between timed steps; inputs also > L2"},
+            "config": arm_config(w),
             "iters_per_s": aggregate_rate(world, iters, args.steps, total_ms),
             "kept_pairs_per_s": aggregate_rate(world, kept_per_step, args.steps, total_ms),
             "kept_fraction": kept_per_step / (rep["passes"] * n * m),
