@@ -1,0 +1,46 @@
+"""The benchmark's reference arm on the CPU: one JSON line with the
+contract's keys, timed on the float64 oracle, and the same `config` object
+the GPU arm reports for the workload (no GPU needed)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_prints_one_contract_line():
+    out = subprocess.run(
+        [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+         "--workload", "c1_n512_d2", "--steps", "2", "--warmup", "1"],
+        capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 1
+    assert line["value"] > 0 and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["value"] == line["value"] and line["e2e"]["h2d_bytes_per_step"] == 0
+    sys.path.insert(0, ROOT)
+    import bench
+    from streaming_sinkhorn_solver_gb300.workloads import WORKLOADS
+    assert line["config"] == json.loads(json.dumps(bench.arm_config(WORKLOADS["c1_n512_d2"])))
+    assert line["metric"] == bench.METRIC
+
+
+@pytest.mark.parametrize("name", ["c1_n512_d2", "c4_n50k_d512", "bs_n1m_d3"])
+def test_arm_config_names_the_workload(name):
+    import bench
+    from streaming_sinkhorn_solver_gb300.workloads import WORKLOADS
+    w = WORKLOADS[name]
+    cfg = bench.arm_config(w)
+    assert cfg["workload"] == name and (cfg["n"], cfg["m"], cfg["d"]) == (w.n, w.m, w.d)
+    assert "model" not in cfg
+    assert ("tau" in cfg) == (w.tau > 0)
