@@ -43,7 +43,10 @@
  *     not race, but they do not overlap either.
  *   - Results are bitwise deterministic for the same inputs, sizes and
  *     options: partial reductions are merged in a fixed order, with no
- *     floating-point atomics.
+ *     floating-point atomics.  Large solves at d <= 3 (from 2^28 score
+ *     pairs) run in Morton order with per-block exponent offsets, so
+ *     reordering the caller's points changes the potentials (reordered the
+ *     same way) only by rounding.
  *   - Errors are returned as fs_status codes, never as C++ exceptions.  A
  *     human-readable message for the last non-OK status of the calling
  *     thread is available from fs_last_error().
