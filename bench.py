@@ -52,6 +52,25 @@ def fp32_ops_per_pair(d: int, tensor_path: bool) -> int:
     return 2 if tensor_path else d + 1
 
 
+def tensor_peak(peaks: dict, sm_mhz: float):
+    """Dense f16/bf16 tensor peak for a kernel that ran at median SM clock
+    `sm_mhz`: the measured sustained cuBLAS rate, scaled from the median SM
+    clock it was measured at to the run's clock (the tensor pipe's work per
+    clock is fixed, so a run at a higher clock than the power-capped
+    measurement has a proportionally higher ceiling).  Without a recorded
+    clock the burst rate is used.  Returns (TFLOP/s, description)."""
+    sustained = float(peaks["bf16_tflops_sustained"])
+    at = ((peaks.get("clocks_under_load") or {}).get("sm_mhz_median"))
+    if at and sm_mhz:
+        peak = sustained * float(sm_mhz) / float(at)
+        return peak, (f"{peaks['source']} bf16 dense sustained {sustained:.1f} TFLOP/s at a median "
+                      f"{float(at):.0f} MHz, scaled to the run's median {float(sm_mhz):.0f} MHz; "
+                      f"f16 operands have the same nominal rate")
+    burst = float(peaks["bf16_tflops"])
+    return burst, (f"{peaks['source']} bf16 dense burst (no clock recorded for the sustained "
+                   f"figure); f16 operands have the same nominal rate")
+
+
 def _rank_info():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -326,7 +345,7 @@ def _dense_roofline(w, path, half_ms, half_n, rates, clocks, sms):
     ex2_peak = ex2_clk * sms * clk * 1e6                               # ex2 / s
     fp32_ops = fp32_ops_per_pair(d, tensor_path)
     fp32_pair_peak = fp32_clk / fp32_ops * sms * clk * 1e6             # pairs / s
-    tflops_peak = float(peaks["bf16_tflops_sustained"])
+    tflops_peak, tflops_src = tensor_peak(peaks, clk)
     hbm_peak = float(peaks["hbm_gbs"])
     op_bytes = 2 if tensor_path else 4
     alg_bytes = op_bytes * (n + m) * d + 4 * 3 * (n + m)                # operands + biases/outputs
@@ -338,8 +357,8 @@ def _dense_roofline(w, path, half_ms, half_n, rates, clocks, sms):
     if bound == "tensor":
         achieved = 2.0 * pairs_per_half * d / t_launch / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tflops_peak, "unit": "TFLOP/s",
-                "peak_source": f"{peaks['source']} bf16 dense sustained; f16 operands have the "
-                               f"same nominal rate"}
+                "peak_source": tflops_src,
+                "frac_of_burst": achieved / float(peaks["bf16_tflops"])}
     elif bound == "alu":
         achieved = pairs_per_half / t_launch / 1e9
         per_clk = min(ex2_clk, fp32_clk / fp32_ops)
@@ -365,15 +384,29 @@ def _dense_roofline(w, path, half_ms, half_n, rates, clocks, sms):
     return roof
 
 
-# The metric's other points (n = m = 50k at d = 3 and d = 64), measured after
-# the timed region of the default workload (d = 512) in the same process.
-METRIC_POINTS = ("c2_n50k_d3", "c3_n50k_d64")
+# The metric's other points (n = m = 50k at d = 3 and d = 64) and the other
+# configurations of the workload set (c5 at d = 1024, c2 at 10k, c1), each
+# measured after the timed region of the default workload (d = 512) in the
+# same process.
+METRIC_POINTS = ("c2_n50k_d3", "c3_n50k_d64", "c5_n20k_m30k_d1024", "c2_n10k_d3", "c1_n512_d2")
+# every point is timed over at least this many steps and about this long, so
+# that its clock record holds several samples (nvidia-smi samples every 200 ms)
+POINT_MIN_STEPS = 10
+POINT_MIN_MS = 2500.0
+POINT_MAX_STEPS = 5000
 
 
-def _metric_point(fs, name, dev, rates, path, steps=3, warmup=3):
-    """One more workload of the metric, timed like the main one (warm-up,
-    CUDA events around each step on the launching stream, a 256 MB write
-    between steps, the half-update's own events for the roofline)."""
+def point_steps(warm_ms_per_step: float) -> int:
+    """Timed steps of a metric point from its warm-up step time."""
+    want = int(POINT_MIN_MS / max(warm_ms_per_step, 1e-3)) + 1
+    return max(POINT_MIN_STEPS, min(POINT_MAX_STEPS, want))
+
+
+def _metric_point(fs, name, dev, rates, path, warmup=3):
+    """One more workload, timed like the main one (warm-up, CUDA events
+    around each step on the launching stream, a 256 MB write between steps,
+    the half-update's own events for the roofline), over point_steps()
+    steps."""
     import torch
     w = WORKLOADS[name]
     n, m, d = w.n, w.m, w.d
@@ -385,9 +418,14 @@ def _metric_point(fs, name, dev, rates, path, steps=3, warmup=3):
     step = _step_fn(fs, w, t, path)
     flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-    for _ in range(warmup):
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(warmup):
+        if i == warmup - 1:
+            w0.record(stream)
         step()
+    w1.record(stream)
     torch.cuda.synchronize()
+    steps = point_steps(w0.elapsed_time(w1))
     sampler = ClockSampler(dev.index, tag=f"_{name}")
     sampler.start()
     fs.fs_timing_read()
@@ -407,8 +445,8 @@ def _metric_point(fs, name, dev, rates, path, steps=3, warmup=3):
     iters, pairs = _work(w, n, m, d)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     roof = _dense_roofline(w, path, half_ms, half_n, rates, clocks, sms)
-    keep = ("bound", "achieved", "peak", "unit", "frac", "mufu_frac", "fp32_frac", "traffic",
-            "avg_launch_ms", "launches")
+    keep = ("bound", "achieved", "peak", "unit", "frac", "mufu_frac", "fp32_frac", "frac_of_burst",
+            "traffic", "avg_launch_ms", "launches")
     return {"workload": name, "n": n, "m": m, "d": d, "steps": steps, "warmup": warmup,
             "value": pairs * steps / (total_ms * 1e-3), "unit": "score-pairs/s",
             "iters_per_s": iters * steps / (total_ms * 1e-3), "ms_per_step": total_ms / steps,
@@ -500,7 +538,8 @@ def run_gb300(args, w):
             "unit": "score-pairs/s", "iters_per_s": line["iters_per_s"],
             "ms_per_step": line["ms_per_step"],
             "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac",
-                                               "traffic", "avg_launch_ms", "launches")},
+                                               "frac_of_burst", "traffic", "avg_launch_ms",
+                                               "launches") if k in roof},
             "note": "the main measurement of this line"}}
         for name in METRIC_POINTS:
             line["metric_points"][name] = _metric_point(fs, name, dev, rates, path)
@@ -515,7 +554,7 @@ def run_gb300(args, w):
         estep(host)
         torch.cuda.synchronize()
         e2e_ms = []
-        for s in range(max(1, min(args.steps, 3))):
+        for s in range(max(1, min(args.steps, 10))):
             host["g0"].zero_()
             flush.fill_(float(s))
             torch.cuda.synchronize()
@@ -667,7 +706,7 @@ def run_sparse(args, w):
         host["g"] = torch.empty(m).pin_memory()
         step(host)
         e2e = []
-        for s_ in range(max(1, min(args.steps, 3))):
+        for s_ in range(max(1, min(args.steps, 10))):
             flush.fill_(float(s_))
             torch.cuda.synchronize()
             t0 = time.perf_counter()
@@ -701,7 +740,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-points", action="store_true",
-                    help="skip the metric's d = 3 and d = 64 points after the default workload")
+                    help="skip the other workloads' points after the default workload")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=64)
     args = ap.parse_args()

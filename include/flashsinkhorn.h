@@ -274,7 +274,11 @@ fs_status fs_marginal_residuals(const float* X, const float* a, int64_t n,
 
 /*
  * fs_sinkhorn_solve_noalloc -- the same iterations as fs_sinkhorn_solve on the
- * FP32-FMA path, for callers that cannot allocate device memory.
+ * FP32-FMA path, for callers that cannot allocate device memory.  It always
+ * takes the online row max as the exponent offset (fs_sinkhorn_solve uses
+ * reference offsets from 2^26 score pairs on) and caps its column split at
+ * 16, so the two agree within the FMA-path tolerance (1e-4 max C), and bit
+ * for bit only below 2^26 pairs where both choose the same split.
  *
  * The pages have no counterpart: this entry point exists for callers that
  * must not call cudaMalloc (a process whose device memory is budgeted by
@@ -468,6 +472,20 @@ fs_status fs_wait_selftest(int64_t timeout_ns, void* stream);
  * Synchronises the device.
  */
 fs_status fs_debug_bounds(int32_t* enabled, uint64_t* first_violation);
+
+/*
+ * fs_fixup_stats -- reference-offset diagnostics (no counterpart on the
+ * pages).  After its first iterations a large solve (from 2^26 score pairs;
+ * tensor path up to d = 512) takes each row's exponent offset from the row's
+ * previous LogSumExp instead of a running max, range-checks the resulting
+ * sum once per row and recomputes the rows that fail with an FP32 fixup
+ * kernel.  The library counts, per device, the fixup passes that ran (one
+ * per reference-offset half-update) and the rows they recomputed.
+ * *launches and *rows (host, either may be NULL) receive those counts for
+ * the current device since the last reset; reset != 0 then zeroes them.
+ * Synchronises the device.  FS_OK with zeros before the first call.
+ */
+fs_status fs_fixup_stats(uint64_t* launches, uint64_t* rows, int32_t reset);
 
 /* Device bytes the library's workspace needs for these sizes (k = 0 for a
  * solve).  The workspace is O((n + m) d): no n x m buffer exists. */

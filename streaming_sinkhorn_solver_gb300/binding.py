@@ -36,7 +36,7 @@ EXPORTED = ("fs_sinkhorn_solve", "fs_apply_plan", "fs_barycentric", "fs_grad_x",
             "fs_last_error", "fs_version", "fs_launch_count", "fs_timing_enable",
             "fs_timing_read", "fs_sinkhorn_solve_noalloc", "fs_unit_rates", "fs_hvp_x",
             "fs_sparse_solve", "fs_morton_order", "fs_sparse_screen", "fs_wait_selftest",
-            "fs_debug_bounds", "fs_shard_unit", "fs_shard_range")
+            "fs_debug_bounds", "fs_shard_unit", "fs_shard_range", "fs_fixup_stats")
 
 
 class FlashSinkhornError(RuntimeError):
@@ -135,6 +135,9 @@ def load_library(path: Optional[str] = None):
         lib.fs_shard_unit.restype = i64
         lib.fs_shard_range.argtypes = [i64, i64, i32, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
         lib.fs_shard_range.restype = ctypes.c_int
+        lib.fs_fixup_stats.argtypes = [ctypes.POINTER(ctypes.c_uint64),
+                                       ctypes.POINTER(ctypes.c_uint64), i32]
+        lib.fs_fixup_stats.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -435,6 +438,15 @@ def fs_version() -> str:
 
 def fs_launch_count() -> int:
     return int(load_library().fs_launch_count())
+
+
+def fs_fixup_stats(reset: bool = False):
+    """(fixup launches, rows recomputed) of the reference-offset half-updates
+    on the current device since the last reset (synchronises the device)."""
+    launches, rows = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    _raise(load_library().fs_fixup_stats(ctypes.byref(launches), ctypes.byref(rows),
+                                         1 if reset else 0))
+    return int(launches.value), int(rows.value)
 
 
 def fs_timing_enable(on: bool = True) -> None:

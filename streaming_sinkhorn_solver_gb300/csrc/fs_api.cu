@@ -50,8 +50,8 @@ fs_status begin_call(Call& c, void* stream) {
         return fail(FS_ERR_UNSUPPORTED, "make one call on this device before capturing a graph");
     if (w.done == nullptr) {
         FS_CUDA(cudaDeviceGetAttribute(&w.sms, cudaDevAttrMultiProcessorCount, c.dev));
-        FS_CUDA(cudaMalloc(&w.err_word, sizeof(uint32_t)));
-        FS_CUDA(cudaMemset(w.err_word, 0, sizeof(uint32_t)));
+        FS_CUDA(cudaMalloc(&w.err_word, kErrWordBytes));
+        FS_CUDA(cudaMemset(w.err_word, 0, kErrWordBytes));
         FS_CUDA(cudaDeviceSynchronize());
         FS_CUDA(cudaEventCreateWithFlags(&w.done, cudaEventDisableTiming));
     }
@@ -461,6 +461,27 @@ fs_status fs_check(void* stream) {
             FS_CUDA(cudaMemset(w.err_word, 0, sizeof(uint32_t)));
             return fail(FS_ERR_TIMEOUT, "device error word 0x%x (bounded wait gave up)", h);
         }
+        return FS_OK;
+    } catch (...) {
+        return fail(FS_ERR_CUDA, "unexpected host exception");
+    }
+}
+
+fs_status fs_fixup_stats(uint64_t* launches, uint64_t* rows, int32_t reset) {
+    try {
+        int dev = 0;
+        FS_CUDA(cudaGetDevice(&dev));
+        if (dev < 0 || dev >= kMaxDevices) return fail(FS_ERR_UNSUPPORTED, "device index %d", dev);
+        Workspace& w = g_ws[dev];
+        std::lock_guard<std::mutex> lk(w.mu);
+        unsigned long long h[2] = {0ull, 0ull};
+        if (w.err_word) {
+            FS_CUDA(cudaDeviceSynchronize());
+            FS_CUDA(cudaMemcpy(h, fix_stats_of(w.err_word), sizeof(h), cudaMemcpyDeviceToHost));
+            if (reset) FS_CUDA(cudaMemset(fix_stats_of(w.err_word), 0, sizeof(h)));
+        }
+        if (launches) *launches = (uint64_t)h[0];
+        if (rows) *rows = (uint64_t)h[1];
         return FS_OK;
     } catch (...) {
         return fail(FS_ERR_CUDA, "unexpected host exception");

@@ -610,6 +610,10 @@ __global__ void __launch_bounds__(256) k_fix_fma(HalfArgs a) {
     if (threadIdx.x == 0) {
         __threadfence();
         if (atomicAdd(&a.fix_count[1], 1u) == gridDim.x - 1) {
+            if (a.fix_stats) {
+                a.fix_stats[0] += 1ull;
+                a.fix_stats[1] += cnt;
+            }
             a.fix_count[0] = 0;
             a.fix_count[1] = 0;
             __threadfence();

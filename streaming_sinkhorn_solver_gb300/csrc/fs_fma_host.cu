@@ -161,6 +161,7 @@ fs_status solve_fma(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) 
     HalfArgs hg{PY, PX, m, n, kappa, eps_ln2, ny, lby, pot_g, part, p.splits_g, p.cps_g,
                 0, fix_list, fix_count};
     hf.fit = hg.fit = fold ? c.at<float>(B.fit) : nullptr;
+    hf.fix_stats = hg.fix_stats = fix_stats_of(c.ws->err_word);
     // The first iterations take the online max: the initial potentials may be
     // arbitrary and the first updates move the LSEs by large amounts.  Later
     // ones use reference offsets, with a guarded sum and a fixup of the rows

@@ -34,6 +34,11 @@ constexpr int kMaxDevices = 64;
 constexpr int kShiftBlocks = 1024;
 
 // One workspace per device: a single cudaMalloc'd arena carved per call.
+constexpr size_t kErrWordBytes = 32;
+inline unsigned long long* fix_stats_of(uint32_t* err_word) {
+    return reinterpret_cast<unsigned long long*>(err_word + 2);
+}
+
 struct Workspace {
     std::mutex mu;
     char* base = nullptr;
@@ -41,7 +46,10 @@ struct Workspace {
     cudaEvent_t done = nullptr;        // recorded at the end of every call
     cudaStream_t last_stream = nullptr;
     bool used = false;
-    uint32_t* err_word = nullptr;      // device error word (own allocation)
+    // device error word (own allocation of kErrWordBytes): word 0 is the
+    // error bits; bytes 8..23 hold the cumulative fixup statistics (two
+    // 64-bit counters: fixup launches, rows recomputed)
+    uint32_t* err_word = nullptr;
     int sms = 0;
 };
 

@@ -110,6 +110,9 @@ struct HalfArgs {
     int* fix_list;            // [nr]
     unsigned int* fix_count;  // [2], zero before the first guarded half-update
     float* fit;               // use_ref 2: [row blocks x (D + 2)] per-CTA offset fits
+    // Cumulative fixup statistics [2] (fixup launches, rows recomputed), or
+    // nullptr; the fixup kernel's last block adds to them.
+    unsigned long long* fix_stats;
 };
 cudaError_t launch_half_fma(int D, const HalfArgs& a, cudaStream_t s);
 // Recompute the listed rows with the online max; resets the list.

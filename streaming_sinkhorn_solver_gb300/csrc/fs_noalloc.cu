@@ -22,8 +22,14 @@
 //     results; calls on one stream are ordered and safe.  Every scratch byte
 //     a call reads is written earlier in the same call, so nothing has to be
 //     cleared between calls.
-// It runs exactly the kernels fs_sinkhorn_solve runs on the FMA path and
-// returns the same potentials.
+// It runs the FMA-path half-update kernels of fs_sinkhorn_solve for the same
+// iterations, but always with the online row max as the exponent offset:
+// fs_sinkhorn_solve switches to reference offsets (each row's previous LSE,
+// with a guarded sum and a fixup) from 2^26 score pairs on, and at d <= 3 to
+// Morton-ordered folded offsets from 2^28; and it caps the column split at
+// 16.  The potentials of the two entry points agree within the FMA-path
+// tolerance (1e-4 max C); they are equal bit for bit only below 2^26 pairs
+// and where both choose the same column split.
 #include "fs_host.cuh"
 
 #include <cmath>

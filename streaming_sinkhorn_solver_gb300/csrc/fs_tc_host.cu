@@ -242,9 +242,10 @@ fs_status solve_tc(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) {
     hf.fix_count = hg.fix_count = fix_count;
     TcFixArgs ff{P.X.dev, P.Y.dev, c.at<float>(B.shift), d, (float)(2.0 * kLog2e / (double)P.eps),
                  hf.cbias, n, m, eps_ln2, hf.rnorm, hf.rlogw2, P.f.dev, hf.rbias, fix_list,
-                 fix_count};
+                 fix_count, fix_stats_of(c.ws->err_word)};
     TcFixArgs fg{P.Y.dev, P.X.dev, c.at<float>(B.shift), d, ff.kappa, hg.cbias, m, n, eps_ln2,
-                 hg.rnorm, hg.rlogw2, P.g.dev, hg.rbias, fix_list, fix_count};
+                 hg.rnorm, hg.rlogw2, P.g.dev, hg.rbias, fix_list, fix_count,
+                 fix_stats_of(c.ws->err_word)};
     const bool ref_ok = d <= kFixMaxDim && (double)n * (double)m >= kTcRefMinPairs;
 
     // With row shards, each shard's launches see only its rows: the row

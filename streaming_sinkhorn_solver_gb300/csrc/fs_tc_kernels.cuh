@@ -78,6 +78,7 @@ struct TcFixArgs {
     float* rbias;
     int* fix_list;
     unsigned int* fix_count;
+    unsigned long long* fix_stats;   // [2] launches, rows recomputed (or nullptr)
 };
 constexpr int kFixMaxDim = 512;
 cudaError_t launch_fix_tc(const TcFixArgs& a, cudaStream_t s);

@@ -44,3 +44,32 @@ def test_arm_config_names_the_workload(name):
     assert cfg["workload"] == name and (cfg["n"], cfg["m"], cfg["d"]) == (w.n, w.m, w.d)
     assert "model" not in cfg
     assert ("tau" in cfg) == (w.tau > 0)
+
+
+def test_tensor_peak_scales_with_the_run_clock():
+    """The tensor roofline's denominator is the measured sustained rate scaled
+    from the clock it was measured at to the run's clock: a kernel that ran
+    at 1800 MHz doing 1750 TFLOP/s against a 1745.7 TFLOP/s measurement at
+    1500 MHz is at 0.83 of it, not above 1 (a fraction above 1 would be an
+    accounting error, not a result)."""
+    import bench
+    peaks = {"bf16_tflops": 1925.9, "bf16_tflops_sustained": 1745.7, "source": "measured",
+             "clocks_under_load": {"sm_mhz_median": 1500.0}}
+    peak, src = bench.tensor_peak(peaks, 1800.0)
+    assert abs(peak - 1745.7 * 1.2) < 1e-9 and "1800" in src
+    assert 1750.0 / peak < 1.0
+    same, _ = bench.tensor_peak(peaks, 1500.0)
+    assert same == 1745.7
+    burst, src = bench.tensor_peak({"bf16_tflops": 1925.9, "bf16_tflops_sustained": 1700.0,
+                                    "source": "fallback"}, 1800.0)
+    assert burst == 1925.9 and "burst" in src
+
+
+def test_metric_points_cover_every_configuration_with_long_regions():
+    import bench
+    from streaming_sinkhorn_solver_gb300.workloads import WORKLOADS
+    dense = {n for n, w in WORKLOADS.items() if w.tau == 0}
+    assert dense == set(bench.METRIC_POINTS) | {bench.DEFAULT_WORKLOAD}
+    assert bench.point_steps(300.0) == bench.POINT_MIN_STEPS
+    assert bench.point_steps(1.0) * 1.0 >= bench.POINT_MIN_MS
+    assert bench.point_steps(1e-6) == bench.POINT_MAX_STEPS

@@ -6,7 +6,9 @@ a process whose device memory budget belongs to someone else or a loop where
 the synchronisation of cudaMalloc/cudaFree is not allowed: its scratch is
 one static array in the library's device image.  Two calls in a row must
 each give the regular solve's potentials (the array is shared and reused),
-within the FMA-path tolerance of 1e-4 max(C).  The file sorts last so that
+within the FMA-path tolerance of 1e-4 max(C); at 2^26 score pairs, where the
+regular solve takes reference offsets and the allocation-free one keeps the
+online max, both are also checked against the float64 oracle.  The file sorts last so that
 a run stopping at the first failure has run every other test first; it
 also passes on its own in a fresh process.
 """
@@ -48,6 +50,27 @@ def test_noalloc_matches_regular_solve_on_two_calls_in_a_row():
         tol = F_TOL_FMA * _cmax(inp)
         assert max_abs(f, fr) <= tol
         assert max_abs(g, gr) <= tol
+
+
+def test_noalloc_at_2_26_pairs_matches_the_oracle_and_the_regular_solve():
+    """n = m = 8192, d = 3 (2^26 score pairs): here the regular solve switches
+    to reference offsets with fixups after two iterations, while the
+    allocation-free one keeps the online max throughout, so the two run
+    different kernels.  Both must match the float64 oracle element by element
+    within 1e-4 max(C), on two allocation-free calls in a row."""
+    import oracle as orc
+    fs.load_library()
+    inp = make_inputs("c2_n10k_d3", n=8192, m=8192, seed=405)
+    eps, iters = 0.01, 12
+    C = orc.cost(inp["X"], inp["Y"])
+    fr, gr = orc.sinkhorn(C, inp["a"], inp["b"], eps, iters)
+    tol = F_TOL_FMA * C.max()
+    del C
+    for _ in range(2):
+        f, g, f_reg, g_reg = _both(inp, eps, iters)
+        assert max_abs(f, fr) <= tol and max_abs(g, gr) <= tol
+        assert max_abs(f_reg, fr) <= tol and max_abs(g_reg, gr) <= tol
+        assert max_abs(f, f_reg) <= tol and max_abs(g, g_reg) <= tol
 
 
 def test_noalloc_rejects_sizes_beyond_its_static_scratch():
