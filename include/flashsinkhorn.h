@@ -316,22 +316,31 @@ fs_status fs_sinkhorn_solve_noalloc(const float* X, const float* a, int64_t n,
  * (solved by conjugate gradients in the complement of the gauge direction 1),
  * fdot = (r - P gdot) / a, and
  *     (H V)_i = 2 a_i v_i - (2/eps) sum_j P_ij (fdot_i + gdot_j - Cdot_ij) y_j.
- * Every product with P is a plan application (never stored); the last term
- * applies P to the d^2 products y_j y_j^T.
+ * Every product with P is a streamed plan application (never stored); the
+ * term sum_j P_ij Cdot_ij y_j (and r) comes from one tangent application: the
+ * plan entries weighted by Cdot_ij, whose dot products v_i . y_j are formed
+ * tile by tile beside the scores (a second tensor-core tile on the tensor
+ * path), so no n x m or n d^2 array exists.
  *   f, g          converged potentials (from fs_sinkhorn_solve); the formula
  *                 assumes both marginals hold, so its accuracy follows the
  *                 marginal residuals (fs_marginal_residuals)
  *   V [n*d], out [n*d]   direction and result (host or device)
  *   cg_max_iter   CG iteration limit, 0 = 200;  cg_tol  relative residual, 0 = 1e-6
- * Squared-Euclidean cost, 1 <= d <= 64 (FS_ERR_UNSUPPORTED otherwise).
- * Stream-ordered scratch of O((n + m) d^2) floats; synchronises `stream`
- * (each CG step reads two dot products on the host).
+ * Squared-Euclidean cost (FS_ERR_UNSUPPORTED otherwise), 1 <= d <= 4096.
+ * Stream-ordered scratch of O((n + m) d) floats (fs_hvp_workspace_bytes);
+ * synchronises `stream` (each CG step reads two dot products on the host).
  */
 fs_status fs_hvp_x(const float* X, const float* a, int64_t n,
                    const float* Y, const float* b, int64_t m, int32_t d,
                    float eps, const float* f, const float* g,
                    const float* V, float* out, int32_t cg_max_iter, float cg_tol,
                    const fs_options* opt, void* stream);
+
+/* Device bytes fs_hvp_x uses for these sizes with device inputs: its own
+ * scratch vectors plus the largest library workspace its plan applications
+ * grow to; O((n + m) d).  -1 for sizes out of range or a cost other than the
+ * squared-Euclidean one.  Host only. */
+int64_t fs_hvp_workspace_bytes(int64_t n, int64_t m, int32_t d, const fs_options* opt);
 
 /*
  * fs_unit_rates -- measure, on the current GPU, the per-SM issue rates that

@@ -36,7 +36,8 @@ EXPORTED = ("fs_sinkhorn_solve", "fs_apply_plan", "fs_barycentric", "fs_grad_x",
             "fs_last_error", "fs_version", "fs_launch_count", "fs_timing_enable",
             "fs_timing_read", "fs_sinkhorn_solve_noalloc", "fs_unit_rates", "fs_hvp_x",
             "fs_sparse_solve", "fs_morton_order", "fs_sparse_screen", "fs_wait_selftest",
-            "fs_debug_bounds", "fs_shard_unit", "fs_shard_range", "fs_fixup_stats")
+            "fs_debug_bounds", "fs_shard_unit", "fs_shard_range", "fs_fixup_stats",
+            "fs_hvp_workspace_bytes")
 
 
 class FlashSinkhornError(RuntimeError):
@@ -138,6 +139,8 @@ def load_library(path: Optional[str] = None):
         lib.fs_fixup_stats.argtypes = [ctypes.POINTER(ctypes.c_uint64),
                                        ctypes.POINTER(ctypes.c_uint64), i32]
         lib.fs_fixup_stats.restype = ctypes.c_int
+        lib.fs_hvp_workspace_bytes.argtypes = [i64, i64, i32, opt]
+        lib.fs_hvp_workspace_bytes.restype = i64
         if path is None:
             _lib = lib
         return lib
@@ -405,6 +408,11 @@ def fs_hvp_x(X, a, Y, b, eps: float, f, g, V, out=None, *, cg_max_iter: int = 0,
         _stream(stream, X))
     _raise(st)
     return out
+
+
+def fs_hvp_workspace_bytes(n: int, m: int, d: int, *, path: str = "auto") -> int:
+    """Device bytes fs_hvp_x uses for these sizes (host only)."""
+    return int(load_library().fs_hvp_workspace_bytes(n, m, d, _opts(path, 0, False)))
 
 
 def fs_unit_rates(stream=None) -> dict:

@@ -22,8 +22,6 @@ std::atomic<int64_t> g_launches{0};
 namespace {
 thread_local std::string t_err;
 Workspace g_ws[kMaxDevices];
-constexpr int kMaxDim = 4096;
-constexpr int kMaxK = 4096;
 }  // namespace
 
 fs_status fail(fs_status st, const char* fmt, ...) {
@@ -306,9 +304,14 @@ fs_status solve_entry(const float* X, const float* a, int64_t n, const float* Y,
 fs_status apply_entry(int mode, const float* X, const float* a, int64_t n, const float* Y,
                       const float* b, int64_t m, int32_t d, float eps, const float* f,
                       const float* g, const float* V, int32_t k, float* out,
-                      const fs_options* opt, void* stream) {
+                      const fs_options* opt, void* stream, const float* U = nullptr,
+                      float* out2 = nullptr) {
     FS_TRY(check_common(X, a, n, Y, b, m, d, eps, opt));
     if (!f || !g || !V || !out) return fail(FS_ERR_INVALID_ARG, "null f, g, V or out");
+    if (mode == APPLY_TAN && (!U || !out2))
+        return fail(FS_ERR_INVALID_ARG, "null direction or second output");
+    if (mode == APPLY_TAN && opt && opt->cost != FS_COST_SQEUCLIDEAN)
+        return fail(FS_ERR_UNSUPPORTED, "the tangent application takes the squared-Euclidean cost");
     if (k < 1 || k > kMaxK) return fail(FS_ERR_INVALID_ARG, "k=%d out of range [1, %d]", k, kMaxK);
     const int path = choose_path(d, opt);
     FS_TRY(check_path(path, d));
@@ -331,11 +334,36 @@ fs_status apply_entry(int mode, const float* X, const float* a, int64_t n, const
         FS_TRY(classify(c, P.V, V, (size_t)m * k));
     }
     FS_TRY(classify(c, P.out, out, (size_t)n * k));
+    if (mode == APPLY_TAN) {
+        FS_TRY(classify(c, P.U, U, (size_t)n * d));
+        FS_TRY(classify(c, P.out2, out2, (size_t)n));
+    }
     FS_TRY(path == FS_PATH_FMA ? apply_fma(c, P, mode, opt) : apply_tc(c, P, mode, opt));
     return end_call(c);
 }
 
 }  // namespace
+
+int64_t workspace_bytes_any(int64_t n, int64_t m, int32_t d, int32_t k, const fs_options* opt,
+                            bool tan) {
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaGetLastError();
+    const int path = choose_path(d, opt);
+    if (path == FS_PATH_FMA && d > kFmaMaxDim) return -1;
+    return (path == FS_PATH_FMA ? workspace_bytes_fma(n, m, d, k, sms, opt, tan)
+                                : workspace_bytes_tc(n, m, d, k, sms, opt, tan)) +
+           cos_workspace_bytes(n, m, d, opt);
+}
+
+fs_status apply_tangent(const float* X, const float* a, int64_t n, const float* Y, const float* b,
+                        int64_t m, int32_t d, float eps, const float* f, const float* g,
+                        const float* U, const float* V, int32_t k, float* out, float* out2,
+                        const fs_options* opt, void* stream) {
+    return apply_entry(APPLY_TAN, X, a, n, Y, b, m, d, eps, f, g, V, k, out, opt, stream, U, out2);
+}
+
 }  // namespace fs
 
 using namespace fs;
@@ -436,15 +464,7 @@ fs_status fs_shard_range(int64_t rows, int64_t unit, int32_t shards, int32_t s, 
 
 int64_t fs_workspace_bytes(int64_t n, int64_t m, int32_t d, int32_t k, const fs_options* opt) {
     if (n < 1 || m < 1 || d < 1 || d > kMaxDim || k < 0 || k > kMaxK) return -1;
-    int dev = 0, sms = 152;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaGetLastError();
-    const int path = choose_path(d, opt);
-    if (path == FS_PATH_FMA && d > kFmaMaxDim) return -1;
-    return (path == FS_PATH_FMA ? workspace_bytes_fma(n, m, d, k, sms, opt)
-                                : workspace_bytes_tc(n, m, d, k, sms, opt)) +
-           cos_workspace_bytes(n, m, d, opt);
+    return workspace_bytes_any(n, m, d, k, opt, false);
 }
 
 fs_status fs_check(void* stream) {

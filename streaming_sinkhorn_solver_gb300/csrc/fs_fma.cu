@@ -347,15 +347,17 @@ __device__ __forceinline__ void push_fix(const HalfArgs& a, int64_t row) {
 // the sum is range-checked at the end (here when the split is the whole row,
 // else in the merge).  MODE 2: as 1, through the CTA's affine fit of those
 // LSEs folded into the staged columns (cta_offset_fit; rows in Morton order).
+// Four CTAs per SM in the folded mode (64 registers; measured 1.4 % faster
+// than three at d = 3), three (d <= 8) or two otherwise.
 template <int D, int RP, int MODE>
-__global__ void __launch_bounds__(kThreads, D <= 8 ? 3 : 2) k_half_fma(HalfArgs a) {
+__global__ void __launch_bounds__(kThreads, MODE == 2 ? 4 : D <= 8 ? 3 : 2) k_half_fma(HalfArgs a) {
     constexpr bool REF = MODE >= 1;
     constexpr int DS = fma_stride(D);
     constexpr int DD = fma_dup_stride(D);
     constexpr int CH = fma_chunk(D);
     constexpr int RPT = 2 * RP;
     __shared__ float4 sc[CH * DD / 4];
-    __shared__ float fit[D + 1];
+    __shared__ float fit[D + 2];
 
     const int tid = threadIdx.x;
     const int64_t row0 = (int64_t)blockIdx.x * (kThreads * RPT);
@@ -383,25 +385,28 @@ __global__ void __launch_bounds__(kThreads, D <= 8 ? 3 : 2) k_half_fma(HalfArgs 
         S[r] = pk(0.f, 0.f);
         nm[r] = REF ? pk(-M[2 * r], -M[2 * r + 1]) : pk(INFINITY, INFINITY);
     }
-    // MODE 2: this CTA's fit (k_fma_fit): h, mu and whether it holds
+    // MODE 2: the CTA fits its rows' previous LSEs (every column split of a
+    // row block computes the same fit from the same values): h, mu and
+    // whether the fit holds, in fit[]; the rows' offsets become the fitted A_i
     bool fold = false;
     if constexpr (MODE == 2) {
-        const float* fg = a.fit + (int64_t)blockIdx.x * (D + 2);
-        fold = fg[D + 1] != 0.f;
-        if (tid <= D) fit[tid] = fg[tid];    // read by the staging after its barrier
+        __shared__ float red[(D * (D + 1) / 2 + D) * (kThreads / 32 + 1)];
+        float qv[RPT][D];
+        bool valid[RPT];
+#pragma unroll
+        for (int r = 0; r < RP; ++r)
+#pragma unroll
+            for (int k = 0; k < D; ++k) upk(q[r][k], qv[2 * r][k], qv[2 * r + 1][k]);
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) valid[i] = row0 + tid + i * kThreads < a.nr;
+        fold = cta_offset_fit<D, RPT>(qv, M, valid, red, fit);
         if (fold) {
 #pragma unroll
-            for (int r = 0; r < RP; ++r) {
-                float A0 = fg[D], A1 = fg[D];
+            for (int i = 0; i < RPT; ++i) {
+                float A = fit[D];
 #pragma unroll
-                for (int k = 0; k < D; ++k) {
-                    float x0, x1;
-                    upk(q[r][k], x0, x1);
-                    A0 = fmaf(fg[k], x0, A0);
-                    A1 = fmaf(fg[k], x1, A1);
-                }
-                M[2 * r] = A0;
-                M[2 * r + 1] = A1;
+                for (int k = 0; k < D; ++k) A = fmaf(fit[k], qv[i][k], A);
+                M[i] = A;
             }
         }
     }
@@ -464,31 +469,6 @@ __global__ void __launch_bounds__(kThreads, D <= 8 ? 3 : 2) k_half_fma(HalfArgs 
     }
 }
 
-// The per-CTA offset fits of a mode-2 half-update: the same CTA grid over
-// the rows, one fit per row block into a.fit.
-template <int D, int RP>
-__global__ void __launch_bounds__(kThreads) k_fma_fit(HalfArgs a) {
-    constexpr int DS = fma_stride(D);
-    constexpr int RPT = 2 * RP;
-    __shared__ float red[(D * (D + 1) / 2 + D) * (kThreads / 32 + 1)];
-    __shared__ float fit[D + 2];
-    const int tid = threadIdx.x;
-    const int64_t row0 = (int64_t)blockIdx.x * (kThreads * RPT);
-    float qv[RPT][D], M[RPT];
-    bool valid[RPT];
-#pragma unroll
-    for (int i = 0; i < RPT; ++i) {
-        const int64_t r = row0 + tid + i * kThreads;
-        valid[i] = r < a.nr;
-        const int64_t rc = r < a.nr ? r : a.nr - 1;
-#pragma unroll
-        for (int k = 0; k < D; ++k) qv[i][k] = a.rows[rc * DS + k] * a.kappa;
-        M[i] = a.rlogw2[rc] - a.rows[rc * DS + D];
-    }
-    cta_offset_fit<D, RPT>(qv, M, valid, red, fit);
-    if (tid < D + 2) a.fit[(int64_t)blockIdx.x * (D + 2) + tid] = fit[tid];
-}
-
 template <int D>
 cudaError_t launch_half_fma_t(const HalfArgs& a, cudaStream_t s) {
     constexpr int RP = fma_row_pairs(D);
@@ -498,9 +478,6 @@ cudaError_t launch_half_fma_t(const HalfArgs& a, cudaStream_t s) {
     bool launched = false;
     if constexpr (D <= 4) {
         if (a.use_ref == 2) {
-            if (a.fit == nullptr) return cudaErrorInvalidValue;
-            k_fma_fit<D, RP><<<grid.x, kThreads, 0, s>>>(a);
-            count_launch();
             k_half_fma<D, RP, 2><<<grid, kThreads, 0, s>>>(a);
             launched = true;
         }
@@ -638,7 +615,7 @@ cudaError_t launch_fix_fma_t(const HalfArgs& a, cudaStream_t s) {
 constexpr int kApplyThreads = 128;
 constexpr int kApplyChunk = 256;
 
-template <int D, int KC>
+template <int D, int KC, bool TAN>
 __global__ void __launch_bounds__(kApplyThreads) k_apply_fma(ApplyArgs a) {
     constexpr int DS = fma_stride(D);
     __shared__ float4 sc[kApplyChunk * DS / 4];
@@ -655,6 +632,16 @@ __global__ void __launch_bounds__(kApplyThreads) k_apply_fma(ApplyArgs a) {
     float q[D];
 #pragma unroll
     for (int k = 0; k < D; ++k) q[k] = a.rows[rr * DS + k] * a.kappa;
+    // APPLY_TAN: t_ij = u_i . (y~_j - x~_i) = u_i . y~_j - c_i (the centring cancels)
+    float u[D];
+    float ci = 0.f, sig = 0.f;
+    if (TAN) {
+#pragma unroll
+        for (int k = 0; k < D; ++k) {
+            u[k] = k < a.d ? a.U[rr * a.d + k] : 0.f;
+            ci = fmaf(u[k], a.rows[rr * DS + k], ci);
+        }
+    }
     float M = -INFINITY;
     float O[KC];
 #pragma unroll
@@ -682,27 +669,38 @@ __global__ void __launch_bounds__(kApplyThreads) k_apply_fma(ApplyArgs a) {
                 const float r = ex2(M - sij);
 #pragma unroll
                 for (int c = 0; c < KC; ++c) O[c] *= r;
+                if (TAN) sig *= r;
                 M = sij;
             }
-            const float p = ex2(sij - M);
+            float p = ex2(sij - M);
+            if (TAN) {
+                float t = -ci;
+#pragma unroll
+                for (int k = 0; k < D; ++k) t = fmaf(u[k], cv[k], t);
+                p *= t;
+                sig += p;
+            }
 #pragma unroll
             for (int c = 0; c < KC; ++c) O[c] = fmaf(p, sv[j * KC + c], O[c]);
         }
     }
     if (row >= a.n) return;
+    const int pk_stride = a.k + 1 + (TAN ? 1 : 0);
     if (a.splits > 1) {
-        const int64_t base = ((int64_t)blockIdx.y * a.n + row) * (a.k + 1);
-        const int64_t plen = (int64_t)a.splits * a.n * (a.k + 1);
+        const int64_t base = ((int64_t)blockIdx.y * a.n + row) * pk_stride;
+        const int64_t plen = (int64_t)a.splits * a.n * pk_stride;
         if (blockIdx.z == 0 && FS_IDX_OK(base, plen, 7)) a.partial[base] = M;
+        if (TAN && blockIdx.z == 0 && FS_IDX_OK(base + 1 + a.k, plen, 7)) a.partial[base + 1 + a.k] = sig;
         for (int c = 0; c < kw; ++c)
             if (FS_IDX_OK(base + 1 + kc0 + c, plen, 7)) a.partial[base + 1 + kc0 + c] = O[c];
         return;
     }
     const float w = exp2f(a.phi[row] + M);
+    if (TAN && blockIdx.z == 0) a.out2[row] = a.a[row] * (w * sig);
     for (int c = 0; c < kw; ++c) {
         const float t = w * O[c];
         float o;
-        if (a.mode == APPLY_PV) o = a.a[row] * t;
+        if (a.mode == APPLY_PV || a.mode == APPLY_TAN) o = a.a[row] * t;
         else if (a.mode == APPLY_BARY) o = t;
         else o = 2.f * a.a[row] * (a.X[row * a.d + kc0 + c] - t);
         if (FS_IDX_OK(row * a.k + kc0 + c, a.n * (int64_t)a.k, 8)) a.out[row * a.k + kc0 + c] = o;
@@ -713,12 +711,15 @@ template <int D>
 cudaError_t launch_apply_fma_t(const ApplyArgs& a, cudaStream_t s) {
     const unsigned kchunks16 = (unsigned)((a.k + 15) / 16);
     dim3 grid((unsigned)((a.n + kApplyThreads - 1) / kApplyThreads), (unsigned)a.splits);
+    const bool tan = a.mode == APPLY_TAN;
     if (a.k <= 4) {
         grid.z = 1;
-        k_apply_fma<D, 4><<<grid, kApplyThreads, 0, s>>>(a);
+        if (tan) k_apply_fma<D, 4, true><<<grid, kApplyThreads, 0, s>>>(a);
+        else k_apply_fma<D, 4, false><<<grid, kApplyThreads, 0, s>>>(a);
     } else {
         grid.z = kchunks16;
-        k_apply_fma<D, 16><<<grid, kApplyThreads, 0, s>>>(a);
+        if (tan) k_apply_fma<D, 16, true><<<grid, kApplyThreads, 0, s>>>(a);
+        else k_apply_fma<D, 16, false><<<grid, kApplyThreads, 0, s>>>(a);
     }
     count_launch();
     return cudaGetLastError();
@@ -727,19 +728,28 @@ cudaError_t launch_apply_fma_t(const ApplyArgs& a, cudaStream_t s) {
 __global__ void k_merge_apply(ApplyArgs a) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= a.n) return;
-    const int64_t stride = (int64_t)a.n * (a.k + 1);
+    const int pk_stride = a.k + 1 + (a.mode == APPLY_TAN ? 1 : 0);
+    const int64_t stride = (int64_t)a.n * pk_stride;
     float M = -INFINITY;
-    for (int sp = 0; sp < a.splits; ++sp) M = fmaxf(M, a.partial[sp * stride + i * (a.k + 1)]);
+    for (int sp = 0; sp < a.splits; ++sp) M = fmaxf(M, a.partial[sp * stride + i * pk_stride]);
     const float w = exp2f(a.phi[i] + M);
+    if (a.mode == APPLY_TAN) {
+        float sig = 0.f;
+        for (int sp = 0; sp < a.splits; ++sp) {
+            const float* p = a.partial + sp * stride + i * pk_stride;
+            sig += p[1 + a.k] * ex2(p[0] - M);
+        }
+        a.out2[i] = a.a[i] * (w * sig);
+    }
     for (int c = 0; c < a.k; ++c) {
         float O = 0.f;
         for (int sp = 0; sp < a.splits; ++sp) {
-            const float* p = a.partial + sp * stride + i * (a.k + 1);
+            const float* p = a.partial + sp * stride + i * pk_stride;
             O += p[1 + c] * ex2(p[0] - M);
         }
         const float t = w * O;
         float o;
-        if (a.mode == APPLY_PV) o = a.a[i] * t;
+        if (a.mode == APPLY_PV || a.mode == APPLY_TAN) o = a.a[i] * t;
         else if (a.mode == APPLY_BARY) o = t;
         else o = 2.f * a.a[i] * (a.X[i * a.d + c] - t);
         a.out[i * a.k + c] = o;
@@ -760,12 +770,12 @@ cudaError_t launch_half_fma(int D, const HalfArgs& a, cudaStream_t s) {
 }
 
 namespace {
-template <int D>
+template <int D, int MODE>
 int half_fma_residency() {
     static std::atomic<int> cached{0};
     int v = cached.load(std::memory_order_relaxed);
     if (v == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, k_half_fma<D, fma_row_pairs(D), 1>,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, k_half_fma<D, fma_row_pairs(D), MODE>,
                                                           kThreads, 0) != cudaSuccess || v < 1)
             v = 1;
         cached.store(v, std::memory_order_relaxed);
@@ -774,13 +784,21 @@ int half_fma_residency() {
 }
 }  // namespace
 
-int fma_half_blocks_per_sm(int D) {
+int fma_half_blocks_per_sm(int D, bool folded) {
+    if (folded) {
+        switch (D) {
+            case 2: return half_fma_residency<2, 2>();
+            case 3: return half_fma_residency<3, 2>();
+            case 4: return half_fma_residency<4, 2>();
+            default: break;
+        }
+    }
     switch (D) {
-        case 2: return half_fma_residency<2>();
-        case 3: return half_fma_residency<3>();
-        case 4: return half_fma_residency<4>();
-        case 8: return half_fma_residency<8>();
-        default: return half_fma_residency<16>();
+        case 2: return half_fma_residency<2, 1>();
+        case 3: return half_fma_residency<3, 1>();
+        case 4: return half_fma_residency<4, 1>();
+        case 8: return half_fma_residency<8, 1>();
+        default: return half_fma_residency<16, 1>();
     }
 }
 

@@ -16,12 +16,22 @@ struct FmaPlan {
     int64_t cps_f, cps_g;
 };
 
+// Solves from this many score pairs up at d <= 3 run in Morton order, where
+// the rows of a CTA are close in space and their offsets fold into the staged
+// columns (k_half_fma mode 2): a pair then costs d FMAs, one ex2 and one add.
+// Below it the Morton sort and the per-CTA fit cost more than the fold saves.
+constexpr double kFoldMinPairs = 268435456.0;   // 2^28
+
+bool fold_offsets(int64_t n, int64_t m, int32_t d) {
+    return d <= kMortonMaxDim && (double)n * (double)m >= kFoldMinPairs;
+}
+
 FmaPlan plan_fma(int64_t n, int64_t m, int32_t d, int sms, const fs_options* opt) {
     FmaPlan p;
     p.D = fma_pad_dim(d);
     p.DS = fma_stride(p.D);
     const int64_t rows_per_block = fma_rows_per_block(p.D);
-    const int per_sm = fma_half_blocks_per_sm(p.D);
+    const int per_sm = fma_half_blocks_per_sm(p.D, fold_offsets(n, m, d));
     p.splits_f = choose_splits((n + rows_per_block - 1) / rows_per_block, m, sms, per_sm, 128, opt,
                                &p.cps_f);
     p.splits_g = choose_splits((m + rows_per_block - 1) / rows_per_block, n, sms, per_sm, 128, opt,
@@ -35,24 +45,13 @@ struct FmaBufs {
     // Morton order of the solve (fold_offsets): permutations, sort buffers and
     // the potentials in that order
     MortonBufs srt;
-    size_t perm_x, perm_y, fs, gs, fit;
+    size_t perm_x, perm_y, fs, gs;
 };
 
 // Problems from this many score pairs up use reference offsets after the
 // first iteration: below it the fixup launch costs more than the online max.
 constexpr double kRefMinPairs = 67108864.0;   // 2^26
 constexpr int kOnlineIters = 2;
-
-// Solves from this many score pairs up at d <= 3 run in Morton order, where
-// the rows of a CTA are close in space and their offsets fold into the staged
-// columns (k_half_fma mode 2): a pair then costs d FMAs, one ex2 and one add.
-// Below it the fit launch per half-update costs more than the fold saves
-// (measured: +6 % per half-update at 10^8 pairs, -13 % at 2.5 * 10^9).
-constexpr double kFoldMinPairs = 268435456.0;   // 2^28
-
-bool fold_offsets(int64_t n, int64_t m, int32_t d) {
-    return d <= kMortonMaxDim && (double)n * (double)m >= kFoldMinPairs;
-}
 
 void layout_fma(Layout& L, FmaBufs& B, int64_t n, int64_t m, int32_t d, const FmaPlan& p,
                 int apply_k, int apply_splits) {
@@ -72,13 +71,11 @@ void layout_fma(Layout& L, FmaBufs& B, int64_t n, int64_t m, int32_t d, const Fm
     B.counter = L.take(sizeof(unsigned int) * 4);
     B.fix_list = L.take(sizeof(int) * (size_t)std::max(n, m));
     B.fix_count = L.take(sizeof(unsigned int) * 2);
-    B.perm_x = B.perm_y = B.fs = B.gs = B.fit = 0;
+    B.perm_x = B.perm_y = B.fs = B.gs = 0;
 }
 
 void layout_fold(Layout& L, FmaBufs& B, int64_t n, int64_t m, int32_t d, const FmaPlan& p) {
     layout_morton(L, B.srt, n, m, d);
-    const int64_t rpb = fma_rows_per_block(p.D);
-    B.fit = L.take(sizeof(float) * (size_t)((std::max(n, m) + rpb - 1) / rpb) * (p.D + 2));
     B.perm_x = L.take(sizeof(int) * (size_t)n);
     B.perm_y = L.take(sizeof(int) * (size_t)m);
     B.fs = L.take(sizeof(float) * (size_t)n);
@@ -96,13 +93,13 @@ int apply_splits_for(int64_t n, int64_t m, int32_t k, int sms, const fs_options*
 int64_t shard_unit_fma(int32_t d) { return fma_rows_per_block(fma_pad_dim(d)); }
 
 int64_t workspace_bytes_fma(int64_t n, int64_t m, int32_t d, int32_t k, int sms,
-                            const fs_options* opt) {
+                            const fs_options* opt, bool tan) {
     const FmaPlan p = plan_fma(n, m, d, sms, opt);
     int64_t cps;
     const int splits = k > 0 ? apply_splits_for(n, m, k, sms, opt, &cps) : 1;
     Layout L;
     FmaBufs B;
-    layout_fma(L, B, n, m, d, p, k, splits);
+    layout_fma(L, B, n, m, d, p, tan ? k + 1 : k, splits);
     if (k == 0 && fold_offsets(n, m, d)) layout_fold(L, B, n, m, d, p);
     return (int64_t)L.off;
 }
@@ -160,7 +157,6 @@ fs_status solve_fma(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) 
                 0, fix_list, fix_count};
     HalfArgs hg{PY, PX, m, n, kappa, eps_ln2, ny, lby, pot_g, part, p.splits_g, p.cps_g,
                 0, fix_list, fix_count};
-    hf.fit = hg.fit = fold ? c.at<float>(B.fit) : nullptr;
     hf.fix_stats = hg.fix_stats = fix_stats_of(c.ws->err_word);
     // The first iterations take the online max: the initial potentials may be
     // arbitrary and the first updates move the LSEs by large amounts.  Later
@@ -220,12 +216,13 @@ fs_status apply_fma(Call& c, Problem& P, int mode, const fs_options* opt) {
     int64_t cps;
     const int splits = apply_splits_for(n, m, k, c.ws->sms, opt, &cps);
     FmaBufs B;
-    layout_fma(c.L, B, n, m, d, p, k, splits);
+    const bool tan = mode == APPLY_TAN;
+    layout_fma(c.L, B, n, m, d, p, tan ? k + 1 : k, splits);   // APPLY_TAN: one more partial
     CosBufs cb;
     layout_cos(c.L, cb, P);
     FS_TRY(ensure_capacity(c));
-    for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g, &P.V, &P.out}) bind(c, *A);
-    for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g, &P.V}) FS_TRY(upload(c, *A));
+    for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g, &P.V, &P.out, &P.U, &P.out2}) bind(c, *A);
+    for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g, &P.V, &P.U}) FS_TRY(upload(c, *A));
     FS_TRY(prepare_cos(c, P, cb, mode != APPLY_PV));
 
     const double eps = (double)P.eps;
@@ -260,6 +257,8 @@ fs_status apply_fma(Call& c, Problem& P, int mode, const fs_options* opt) {
     A.splits = splits;
     A.cols_per_split = cps;
     A.mode = mode;
+    A.U = P.U.dev;
+    A.out2 = P.out2.dev;
     NvtxRange nvtx("fs plan application (FMA)");
     const int ts = timing_begin(c.stream);
     FS_CUDA(launch_apply_fma(p.D, A, c.stream));
@@ -269,6 +268,7 @@ fs_status apply_fma(Call& c, Problem& P, int mode, const fs_options* opt) {
     if (opt && opt->check_finite)
         FS_TRY(scan_finite(c, P.out.dev, n * (int64_t)k, c.at<unsigned int>(B.counter)));
     FS_TRY(download(c, P.out));
+    FS_TRY(download(c, P.out2));
     return FS_OK;
 }
 

@@ -117,9 +117,14 @@ fs_status make_chunk_tmap(void* map128, const void* base, uint64_t rows);
 int choose_splits(int64_t row_blocks, int64_t nc, int sms, int per_sm, int64_t min_cols,
                   const fs_options* opt, int64_t* cols_per_split);
 
+// Largest dimension d and value width k the entry points accept.
+constexpr int kMaxDim = 4096;
+constexpr int kMaxK = 4096;
+
 // The arrays of one call, staged.
 struct Problem {
     Arr X, a, Y, b, f, g, V, out;
+    Arr U, out2;            // APPLY_TAN: row directions (n x d), sum_j P_ij t_ij (n)
     int64_t n = 0, m = 0;
     int32_t d = 0, k = 0;
     float eps = 0.f;
@@ -199,7 +204,21 @@ fs_status solve_fma(Call& c, Problem& P, int32_t n_iter, const fs_options* opt);
 fs_status apply_fma(Call& c, Problem& P, int mode, const fs_options* opt);
 fs_status solve_tc(Call& c, Problem& P, int32_t n_iter, const fs_options* opt);
 fs_status apply_tc(Call& c, Problem& P, int mode, const fs_options* opt);
-int64_t workspace_bytes_fma(int64_t n, int64_t m, int32_t d, int32_t k, int sms, const fs_options* opt);
-int64_t workspace_bytes_tc(int64_t n, int64_t m, int32_t d, int32_t k, int sms, const fs_options* opt);
+// (tan: the tangent application's extra buffers)
+int64_t workspace_bytes_fma(int64_t n, int64_t m, int32_t d, int32_t k, int sms, const fs_options* opt,
+                            bool tan = false);
+int64_t workspace_bytes_tc(int64_t n, int64_t m, int32_t d, int32_t k, int sms, const fs_options* opt,
+                           bool tan = false);
+// library workspace of one call: path choice plus the cosine copies
+int64_t workspace_bytes_any(int64_t n, int64_t m, int32_t d, int32_t k, const fs_options* opt,
+                            bool tan = false);
+
+// Tangent application (squared-Euclidean cost): out = sum_j P_ij t_ij V_j
+// (n x k) and out2_i = sum_j P_ij t_ij with t_ij = u_i . (y_j - x_i), for row
+// directions U (n x d).  Arguments and memory as fs_apply_plan.
+fs_status apply_tangent(const float* X, const float* a, int64_t n, const float* Y, const float* b,
+                        int64_t m, int32_t d, float eps, const float* f, const float* g,
+                        const float* U, const float* V, int32_t k, float* out, float* out2,
+                        const fs_options* opt, void* stream);
 
 }  // namespace fs

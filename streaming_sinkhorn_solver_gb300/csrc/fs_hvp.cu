@@ -8,21 +8,24 @@
 //
 //   F(X) = <a, f*> + <b, g*>,   grad_i = 2 (a_i x_i - (P Y)_i)
 //   along X + t V:  d/dt P_ij = P_ij (fdot_i + gdot_j - Cdot_ij) / eps,
-//                   Cdot_ij = 2 (x_i - y_j) . v_i
+//                   Cdot_ij = 2 (x_i - y_j) . v_i = -2 t_ij,  t_ij = v_i . (y_j - x_i)
 //   P 1 = a and P^T 1 = b differentiated:
-//      a_i fdot_i + (P gdot)_i   = r_i = sum_j P_ij Cdot_ij = 2 a_i w_i - 2 v_i.(P Y)_i
+//      a_i fdot_i + (P gdot)_i   = r_i = sum_j P_ij Cdot_ij = -2 sum_j P_ij t_ij
 //      (P^T fdot)_j + b_j gdot_j = c_j = sum_i P_ij Cdot_ij = 2 (P^T w)_j - 2 y_j.(P^T V)_j
 //   (w_i = x_i . v_i).  Eliminating fdot = (r - P gdot) / a leaves
 //      S gdot = c - P^T (r / a),   S = diag(b) - P^T diag(1/a) P,
 //   symmetric positive semi-definite with null space 1 (the gauge), solved by
 //   conjugate gradients in the complement of 1.  Then
-//   (H V)_i = 2 a_i v_i - (2/eps) [fdot_i (P Y)_i + (P (gdot . Y))_i
-//                                  - 2 w_i (P Y)_i + 2 (P (Y (x) Y))_i v_i].
-// Every product with P or P^T is one plan application of this library
-// (streamed, never stored); the last term applies P to the d^2 products
-// y_j y_j^T, so d <= 64.
+//   (H V)_i = 2 a_i v_i - (2/eps) [fdot_i (P Y)_i + (P (gdot . Y))_i + 2 T_i],
+//   T_i = sum_j P_ij t_ij y_j.
+// Every product with P or P^T is one streamed plan application of this
+// library; T and sum_j P_ij t_ij come from one tangent application (the plan
+// entries weighted by t_ij, a second dot-product tile U K^T beside the score
+// tile on the tensor path, d more FMAs per pair on the FMA path).  Nothing
+// of size n x m or n d^2 is stored: the scratch is O((n + m) d).
 #include "fs_host.cuh"
 
+#include <algorithm>
 #include <cmath>
 
 namespace fs {
@@ -43,13 +46,12 @@ __global__ void k_rowdot(const float* __restrict__ A, const float* __restrict__ 
     out[i] = (float)(scale * s);
 }
 
-// r_i = 2 a_i w_i - 2 vPY_i;  q_i = r_i / a_i
-__global__ void k_hvp_r(const float* __restrict__ a, const float* __restrict__ w,
-                        const float* __restrict__ vpy, int64_t n, float* __restrict__ r,
-                        float* __restrict__ q) {
+// r_i = -2 sum_j P_ij t_ij;  q_i = r_i / a_i
+__global__ void k_hvp_r(const float* __restrict__ a, const float* __restrict__ pt, int64_t n,
+                        float* __restrict__ r, float* __restrict__ q) {
     const int64_t i = (int64_t)blockIdx.x * kT + threadIdx.x;
     if (i >= n) return;
-    const float ri = 2.f * a[i] * w[i] - 2.f * vpy[i];
+    const float ri = -2.f * pt[i];
     r[i] = ri;
     q[i] = ri / a[i];
 }
@@ -116,35 +118,24 @@ __global__ void k_fdot(const float* __restrict__ r, const float* __restrict__ pg
     if (i < n) fdot[i] = (r[i] - pg[i]) / a[i];
 }
 
-// Z_j = gdot_j y_j;  YY_j = y_j (x) y_j (row-major d x d)
-__global__ void k_gy_and_outer(const float* __restrict__ Y, const float* __restrict__ gdot,
-                               int64_t m, int d, float* __restrict__ Z, float* __restrict__ YY) {
-    const int64_t j = (int64_t)blockIdx.x * kT + threadIdx.x;
-    if (j >= m) return;
-    const float gj = gdot[j];
-    for (int k = 0; k < d; ++k) {
-        const float yk = Y[j * d + k];
-        Z[j * d + k] = gj * yk;
-        for (int l = 0; l < d; ++l) YY[(j * d + k) * d + l] = yk * Y[j * d + l];
-    }
+// Z_j = gdot_j y_j, one thread per element
+__global__ void k_gy(const float* __restrict__ Y, const float* __restrict__ gdot, int64_t m, int d,
+                     float* __restrict__ Z) {
+    const int64_t e = (int64_t)blockIdx.x * kT + threadIdx.x;
+    if (e >= m * d) return;
+    Z[e] = gdot[e / d] * Y[e];
 }
 
-// out_i = 2 a_i v_i - (2/eps) [fdot_i PY_i + PZ_i - 2 w_i PY_i + 2 PYY_i v_i]
+// out_i = 2 a_i v_i - (2/eps) [fdot_i PY_i + PZ_i + 2 T_i], one thread per element
 __global__ void k_hvp_final(const float* __restrict__ a, const float* __restrict__ V,
                             const float* __restrict__ fdot, const float* __restrict__ PY,
-                            const float* __restrict__ PZ, const float* __restrict__ w,
-                            const float* __restrict__ PYY, int64_t n, int d, float two_over_eps,
-                            float* __restrict__ out) {
-    const int64_t i = (int64_t)blockIdx.x * kT + threadIdx.x;
-    if (i >= n) return;
-    for (int k = 0; k < d; ++k) {
-        double q = 0.0;
-        for (int l = 0; l < d; ++l)
-            q += (double)PYY[(i * d + k) * d + l] * (double)V[i * d + l];
-        const double bracket = (double)fdot[i] * PY[i * d + k] + PZ[i * d + k] -
-                               2.0 * (double)w[i] * PY[i * d + k] + 2.0 * q;
-        out[i * d + k] = (float)(2.0 * (double)a[i] * V[i * d + k] - (double)two_over_eps * bracket);
-    }
+                            const float* __restrict__ PZ, const float* __restrict__ T, int64_t n,
+                            int d, float two_over_eps, float* __restrict__ out) {
+    const int64_t e = (int64_t)blockIdx.x * kT + threadIdx.x;
+    if (e >= n * d) return;
+    const int64_t i = e / d;
+    const double bracket = (double)fdot[i] * PY[e] + (double)PZ[e] + 2.0 * (double)T[e];
+    out[e] = (float)(2.0 * (double)a[i] * V[e] - (double)two_over_eps * bracket);
 }
 
 struct Hvp {
@@ -181,9 +172,8 @@ fs_status hvp_entry(const float* X, const float* a, int64_t n, const float* Y, c
     if (!X || !a || !Y || !b || !f || !g || !V || !out)
         return fail(FS_ERR_INVALID_ARG, "null pointer");
     if (n < 1 || m < 1) return fail(FS_ERR_INVALID_ARG, "n=%lld m=%lld", (long long)n, (long long)m);
-    if (d < 1 || d > 64)
-        return fail(FS_ERR_UNSUPPORTED, "fs_hvp_x takes 1 <= d <= 64 (got %d): it applies the plan "
-                                        "to the d^2 products y_j y_j^T", d);
+    if (d < 1 || d > kMaxDim)
+        return fail(FS_ERR_INVALID_ARG, "d=%d out of range [1, %d]", d, kMaxDim);
     if (!(eps > 0.f) || !std::isfinite(eps)) return fail(FS_ERR_INVALID_ARG, "eps must be positive");
     if (cg_max_iter < 0 || !(cg_tol >= 0.f)) return fail(FS_ERR_INVALID_ARG, "cg_max_iter/cg_tol");
     if (opt && opt->cost != FS_COST_SQEUCLIDEAN)
@@ -206,13 +196,13 @@ fs_status hvp_entry(const float* X, const float* a, int64_t n, const float* Y, c
     float* out_d = out;
     if (!out_dev) FS_CUDA(sc.get(&out_d, (size_t)n * d));
 
-    float *PY, *w, *vpy, *r, *q, *U, *PtU, *t, *rhs, *x, *res, *p, *Sp, *tn, *tn2, *fdot, *Z, *PZ,
-        *YY, *PYY;
+    float *PY, *T, *pt, *w, *r, *q, *U, *PtU, *t, *rhs, *x, *res, *p, *Sp, *tn, *tn2, *fdot, *Z,
+        *PZ;
     double *partial, *dres;
-    const int d2 = d * d;
     FS_CUDA(sc.get(&PY, (size_t)n * d));
+    FS_CUDA(sc.get(&T, (size_t)n * d));
+    FS_CUDA(sc.get(&pt, (size_t)n));
     FS_CUDA(sc.get(&w, (size_t)n));
-    FS_CUDA(sc.get(&vpy, (size_t)n));
     FS_CUDA(sc.get(&r, (size_t)n));
     FS_CUDA(sc.get(&q, (size_t)n));
     FS_CUDA(sc.get(&U, (size_t)n * (d + 1)));
@@ -228,20 +218,18 @@ fs_status hvp_entry(const float* X, const float* a, int64_t n, const float* Y, c
     FS_CUDA(sc.get(&fdot, (size_t)n));
     FS_CUDA(sc.get(&Z, (size_t)m * d));
     FS_CUDA(sc.get(&PZ, (size_t)n * d));
-    FS_CUDA(sc.get(&YY, (size_t)m * d2));
-    FS_CUDA(sc.get(&PYY, (size_t)n * d2));
     FS_CUDA(sc.get(&partial, kRedPartials));
     FS_CUDA(sc.get(&dres, 1));
     float* ones = nullptr;
     FS_CUDA(sc.get(&ones, (size_t)m));
 
-    // r and the right-hand side
+    // P Y, the tangent terms (T, sum_j P_ij t_ij), r and the right-hand side
     FS_TRY(apply_p(h, h.Y, d, PY));
+    FS_TRY(apply_tangent(h.X, h.a, n, h.Y, h.b, m, d, eps, h.f, h.g, V_d, h.Y, d, T, pt, opt, s));
+    k_hvp_r<<<blocks_for(n), kT, 0, s>>>(h.a, pt, n, r, q);
     k_rowdot<<<blocks_for(n), kT, 0, s>>>(h.X, V_d, n, d, 1.f, w);
-    k_rowdot<<<blocks_for(n), kT, 0, s>>>(V_d, PY, n, d, 1.f, vpy);
-    k_hvp_r<<<blocks_for(n), kT, 0, s>>>(h.a, w, vpy, n, r, q);
     k_pack_u<<<blocks_for(n), kT, 0, s>>>(w, V_d, n, d, U);
-    count_launch(4);
+    count_launch(3);
     FS_CUDA(cudaGetLastError());
     FS_TRY(apply_pt(h, U, d + 1, PtU));
     FS_TRY(apply_pt(h, q, 1, t));
@@ -296,13 +284,12 @@ fs_status hvp_entry(const float* X, const float* a, int64_t n, const float* Y, c
     // fdot, then the Hessian-vector product
     FS_TRY(apply_p(h, x, 1, tn));
     k_fdot<<<blocks_for(n), kT, 0, s>>>(r, tn, h.a, n, fdot);
-    k_gy_and_outer<<<blocks_for(m), kT, 0, s>>>(h.Y, x, m, d, Z, YY);
+    k_gy<<<blocks_for(m * (int64_t)d), kT, 0, s>>>(h.Y, x, m, d, Z);
     count_launch(2);
     FS_CUDA(cudaGetLastError());
     FS_TRY(apply_p(h, Z, d, PZ));
-    FS_TRY(apply_p(h, YY, d2, PYY));
-    k_hvp_final<<<blocks_for(n), kT, 0, s>>>(h.a, V_d, fdot, PY, PZ, w, PYY, n, d,
-                                             (float)(2.0 / (double)eps), out_d);
+    k_hvp_final<<<blocks_for(n * (int64_t)d), kT, 0, s>>>(h.a, V_d, fdot, PY, PZ, T, n, d,
+                                                          (float)(2.0 / (double)eps), out_d);
     count_launch();
     FS_CUDA(cudaGetLastError());
     if (!out_dev)
@@ -312,7 +299,26 @@ fs_status hvp_entry(const float* X, const float* a, int64_t n, const float* Y, c
 }
 
 }  // namespace
+
+// Device bytes of fs_hvp_x with device inputs: its stream-ordered scratch
+// (the vectors allocated above) plus the largest library workspace its plan
+// applications grow to (P with k = d, P^T with k = d + 1, the tangent).
+int64_t hvp_workspace_bytes(int64_t n, int64_t m, int32_t d, const fs_options* opt) {
+    const int64_t floats = n * (4 * (int64_t)d + 8) + m * (2 * (int64_t)d + 8);
+    const int64_t own = 4 * floats + 8 * (kRedPartials + 1);
+    int64_t ws = workspace_bytes_any(n, m, d, d, opt, false);
+    ws = std::max(ws, workspace_bytes_any(m, n, d, d + 1, opt, false));
+    ws = std::max(ws, workspace_bytes_any(n, m, d, d, opt, true));
+    return ws < 0 ? -1 : own + ws;
+}
+
 }  // namespace fs
+
+extern "C" int64_t fs_hvp_workspace_bytes(int64_t n, int64_t m, int32_t d, const fs_options* opt) {
+    if (n < 1 || m < 1 || d < 1 || d > fs::kMaxDim) return -1;
+    if (opt && opt->cost != FS_COST_SQEUCLIDEAN) return -1;
+    return fs::hvp_workspace_bytes(n, m, d, opt);
+}
 
 extern "C" fs_status fs_hvp_x(const float* X, const float* a, int64_t n, const float* Y,
                               const float* b, int64_t m, int32_t d, float eps, const float* f,

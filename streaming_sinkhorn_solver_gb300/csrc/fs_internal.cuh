@@ -109,7 +109,6 @@ struct HalfArgs {
                               // folded per CTA (rows in Morton order; d <= 4)
     int* fix_list;            // [nr]
     unsigned int* fix_count;  // [2], zero before the first guarded half-update
-    float* fit;               // use_ref 2: [row blocks x (D + 2)] per-CTA offset fits
     // Cumulative fixup statistics [2] (fixup launches, rows recomputed), or
     // nullptr; the fixup kernel's last block adds to them.
     unsigned long long* fix_stats;
@@ -117,8 +116,9 @@ struct HalfArgs {
 cudaError_t launch_half_fma(int D, const HalfArgs& a, cudaStream_t s);
 // Recompute the listed rows with the online max; resets the list.
 cudaError_t launch_fix_fma(int D, const HalfArgs& a, cudaStream_t s);
-// Blocks of the half-update kernel for padded dimension D resident per SM.
-int fma_half_blocks_per_sm(int D);
+// Blocks of the half-update kernel for padded dimension D resident per SM
+// (folded: the kernel of the folded-offset mode, d <= 4).
+int fma_half_blocks_per_sm(int D, bool folded = false);
 
 // Merge of split partials: LSE2 = M + log2 sum_s S_s 2^{M_s - M} in split
 // order, then pot = rnorm - eps ln2 LSE2 and bias = rlogw2 - LSE2.
@@ -130,7 +130,10 @@ cudaError_t launch_merge_lse(const float2* partial, int splits, int64_t nr, cons
                              unsigned int* fix_count = nullptr);
 
 // Plan application on the FMA path.
-enum ApplyMode : int { APPLY_PV = 0, APPLY_BARY = 1, APPLY_GRAD = 2 };
+// APPLY_TAN weights each plan entry by t_ij = u_i . (y_j - x_i) for row
+// directions U (n x d): out_i = sum_j P_ij t_ij V_j and out2_i = sum_j P_ij t_ij
+// (the plan's tangent along X + tU at fixed potentials, up to -2/eps).
+enum ApplyMode : int { APPLY_PV = 0, APPLY_BARY = 1, APPLY_GRAD = 2, APPLY_TAN = 3 };
 struct ApplyArgs {
     const float* rows;      // packed [n x DS] (centred x~)
     const float* cols;      // packed [m x DS] with beta from the given g
@@ -143,10 +146,12 @@ struct ApplyArgs {
     const float* X;         // raw X [n x d] (grad mode)
     int d;
     float* out;             // [n x k]
-    float* partial;         // [splits x n x (k+1)] or nullptr
+    float* partial;         // [splits x n x (k+1)] ([.. x (k+2)] in APPLY_TAN) or nullptr
     int splits;
     int64_t cols_per_split;
     int mode;
+    const float* U;         // APPLY_TAN: row directions [n x d]
+    float* out2;            // APPLY_TAN: sum_j P_ij t_ij [n]
 };
 cudaError_t launch_apply_fma(int D, const ApplyArgs& a, cudaStream_t s);
 cudaError_t launch_merge_apply(const ApplyArgs& a, cudaStream_t s);

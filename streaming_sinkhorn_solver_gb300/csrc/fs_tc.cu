@@ -87,7 +87,7 @@ __global__ void k_to_tiles(const float* __restrict__ P, int64_t rows, int d,
     for (int q = 0; q < 8; ++q) {
         const int k = k0 + q;
         float v = 0.f;
-        if (row < rows && k < d) v = (P[row * d + k] - shift[k]) * scale;
+        if (row < rows && k < d) v = (P[row * d + k] - (shift != nullptr ? shift[k] : 0.f)) * scale;
         h[q] = __float2half_rn(v);
         l[q] = __float2half_rn(v - __half2float(h[q]));
     }
@@ -107,6 +107,72 @@ __global__ void k_bias_init(const float* __restrict__ pot, const float* __restri
     if (j >= rows_pad) return;
     if (j >= rows) bias[j] = -INFINITY;
     else if (pot != nullptr) bias[j] = (pot[j] - norm[j]) * l_over_eps + logw2[j];
+}
+
+// Tangent application: one warp per row, crow_i = u_i . x~_i, and the running
+// maxima of |u_i|^2 (bits[0]) and of |u_ik| (bits[1]) as ordered bits.
+__global__ void k_tan_rows(const float* __restrict__ U, const float* __restrict__ X, int64_t rows,
+                           int d, const float* __restrict__ shift, float* __restrict__ crow,
+                           unsigned int* __restrict__ bits) {
+    const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    float c = 0.f, s = 0.f, mx = 0.f;
+    for (int k = lane; k < d; k += 32) {
+        const float u = U[row * d + k];
+        c = fmaf(u, X[row * d + k] - shift[k], c);
+        s = fmaf(u, u, s);
+        mx = fmaxf(mx, fabsf(u));
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        c += __shfl_xor_sync(0xffffffffu, c, o);
+        s += __shfl_xor_sync(0xffffffffu, s, o);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if (lane == 0) {
+        crow[row] = c;
+        atomicMax(bits, __float_as_uint(s));
+        atomicMax(bits + 1, __float_as_uint(mx));
+    }
+}
+
+// tparams from bits = (max |u|^2, max |u_k|, max |x~|^2, max |y~|^2) and the
+// column cloud's tile scale 2^ey (yscale): |t_ij| <= |u_i| (|y~_j| + |x~_i|)
+// = B, and the plan entries p t (|p| <= 1) are carried as p t 2^et with
+// B 2^et <= 2^14 in the fp16 plan tile.
+//   [0] = 2^-(eu + ey) 2^et   (U K^T accumulator -> t 2^et)
+//   [1] = 2^et,  [2] = 2^-et,  [3] = 2^eu (tile scale of U)
+__global__ void k_tan_params(const unsigned int* __restrict__ bits, const float* __restrict__ yscale,
+                             float* __restrict__ tparams) {
+    const int eu = scale_exp(bits[1]);
+    const float bound = sqrtf(__uint_as_float(bits[0])) *
+                        (sqrtf(__uint_as_float(bits[2])) + sqrtf(__uint_as_float(bits[3])));
+    int et = 0;
+    if (bound > 0.f && isfinite(bound)) {
+        int E;
+        frexpf(bound, &E);                 // bound < 2^E
+        et = min(max(14 - E, -120), 120);
+    }
+    tparams[0] = ldexpf(1.f / *yscale, et - eu);
+    tparams[1] = ldexpf(1.f, et);
+    tparams[2] = ldexpf(1.f, -et);
+    tparams[3] = ldexpf(1.f, eu);
+}
+
+cudaError_t launch_tan_rows(const float* U, const float* X, int64_t rows, int d, const float* shift,
+                            float* crow, unsigned int* bits, cudaStream_t s) {
+    const int64_t threads = rows * 32;
+    k_tan_rows<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(U, X, rows, d, shift, crow, bits);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tan_params(const unsigned int* bits, const float* yscale, float* tparams,
+                              cudaStream_t s) {
+    k_tan_params<<<1, 1, 0, s>>>(bits, yscale, tparams);
+    count_launch();
+    return cudaGetLastError();
 }
 
 cudaError_t launch_prep_side(const float* P, const float* w, int64_t rows, int d,

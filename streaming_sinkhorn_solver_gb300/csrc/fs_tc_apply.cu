@@ -104,7 +104,7 @@ cudaError_t launch_vt_tiles(const float* V, int64_t m, int k, int kpad, const fl
 
 __device__ __forceinline__ float apply_out(const TcApplyArgs& a, int64_t row, int col, float W,
                                            float o, float sigma) {
-    if (a.mode == APPLY_PV) return a.a[row] * W * o;
+    if (a.mode == APPLY_PV || a.mode == APPLY_TAN) return a.a[row] * W * o;
     const float py = o + a.shift[col] * sigma;     // sum_j p_ij y_j
     if (a.mode == APPLY_BARY) return W * py;
     return 2.f * a.a[row] * (a.X[row * (int64_t)a.k + col] - W * py);
@@ -124,6 +124,7 @@ __global__ void k_merge_apply_tc(TcApplyArgs a) {
     }
     const float W = exp2f(a.phi[row] + a.lse2[row]);
     a.out[idx] = apply_out(a, row, col, W, o, sigma);
+    if (a.mode == APPLY_TAN && col == 0) a.out2[row] = a.a[row] * W * sigma;
 }
 
 cudaError_t launch_merge_apply_tc(const TcApplyArgs& a, cudaStream_t s) {
@@ -140,6 +141,9 @@ cudaError_t launch_merge_apply_tc(const TcApplyArgs& a, cudaStream_t s) {
 // warp 0: producer (K/Q chunk pairs into a 3-deep ring, value tiles into 2 slots)
 // warp 1: MMA issuer (S_{t+1} = Q K_{t+1}^T is issued before O += P_t V_t)
 // warps 2-5: epilogue, one thread per row
+// TAN (APPLY_TAN): every tile also forms T = U K^T in TMEM columns 128..255
+// (the ring carries, per tile, the nch (K, Q) chunk sets and then nch (K, U)
+// sets); S and T are single-buffered, and p_ij t_ij replaces p_ij.
 
 namespace {
 constexpr int kStageA = 4 * CHUNK_BYTES;          // K hi, K lo, Q hi, Q lo
@@ -152,7 +156,7 @@ __host__ __device__ constexpr int vt_slots(int kv) { return kv == 256 ? 1 : 2; }
 // KV output columns per CTA.  With one value slot (KV = 256) the value tile
 // of tile t is loaded while the scores of tile t + 1 stream (after its first
 // half of chunks), which the MMA thread consumes only after those scores.
-template <int KV>
+template <int KV, bool TAN>
 __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
     constexpr int kVtSlot = vt_slot_bytes(KV);
     constexpr int VS = vt_slots(KV);
@@ -168,6 +172,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
     const int j1 = min(a.col_tiles, j0 + a.tiles_per_split);
     const int ntiles = j1 - j0;
     const int nch = a.nch;
+    const int nent = TAN ? 2 * nch : nch;   // ring entries per tile
 
     uint8_t* sStage = smem;
     uint8_t* sVT = sStage + kApplyStages * kStageA;
@@ -212,6 +217,8 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
             const int64_t qoff = rt * nch * (int64_t)CHUNK_BYTES;
             const char* Qg = reinterpret_cast<const char*>(a.Q) + qoff;
             const char* Qlg = reinterpret_cast<const char*>(a.Qlo) + qoff;
+            const char* Ug = TAN ? reinterpret_cast<const char*>(a.U) + qoff : nullptr;
+            const char* Ulg = TAN ? reinterpret_cast<const char*>(a.Ulo) + qoff : nullptr;
             const char* VTg = reinterpret_cast<const char*>(a.VT);
             int s = 0, issued = 0, vissued = 0;
             uint32_t ph = 0;
@@ -236,24 +243,26 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
                 const int64_t koff = j * nch * (int64_t)CHUNK_BYTES;
                 const char* Kg = reinterpret_cast<const char*>(a.K) + koff;
                 const char* Klg = reinterpret_cast<const char*>(a.Klo) + koff;
-                for (int c = 0; c < nch; ++c) {
+                for (int e = 0; e < nent; ++e) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, a.err, ERR_TIMEOUT_PRODUCER)) {
                         ok = false;
                         break;
                     }
+                    const int c = e < nch ? e : e - nch;
+                    const bool tpart = TAN && e >= nch;     // (K, U) instead of (K, Q)
                     uint8_t* st = sStage + s * kStageA;
                     const int64_t co = c * (int64_t)CHUNK_BYTES;
                     mbar_arrive_expect_tx(&full[s], kStageA);
                     bulk_g2s(st, Kg + co, CHUNK_BYTES, &full[s]);
                     bulk_g2s(st + CHUNK_BYTES, Klg + co, CHUNK_BYTES, &full[s]);
-                    bulk_g2s(st + 2 * CHUNK_BYTES, Qg + co, CHUNK_BYTES, &full[s]);
-                    bulk_g2s(st + 3 * CHUNK_BYTES, Qlg + co, CHUNK_BYTES, &full[s]);
+                    bulk_g2s(st + 2 * CHUNK_BYTES, (tpart ? Ug : Qg) + co, CHUNK_BYTES, &full[s]);
+                    bulk_g2s(st + 3 * CHUNK_BYTES, (tpart ? Ulg : Qlg) + co, CHUNK_BYTES, &full[s]);
                     ++issued;
                     if (++s == kApplyStages) {
                         s = 0;
                         ph ^= 1u;
                     }
-                    if (VS == 1 && c == nch / 2 && t > 0 && !(ok = load_v(t - 1))) break;
+                    if (VS == 1 && e == nch / 2 && t > 0 && !(ok = load_v(t - 1))) break;
                 }
                 if (!ok) break;
                 if (VS == 2 && !(ok = load_v(t))) break;
@@ -282,12 +291,15 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
             int s = 0;
             uint32_t ph = 0;
             auto issue_S = [&](int t) -> bool {
-                const int b = t & 1;
-                if (!mbar_wait(&tempty[b], (uint32_t)((t >> 1) & 1) ^ 1u, a.err, ERR_TIMEOUT_MMA))
+                // TAN: one S buffer (columns 0..127) and one T buffer (128..255)
+                const int b = TAN ? 0 : (t & 1);
+                const uint32_t tph = TAN ? (uint32_t)(t & 1) : (uint32_t)((t >> 1) & 1);
+                if (!mbar_wait(&tempty[b], tph ^ 1u, a.err, ERR_TIMEOUT_MMA))
                     return false;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem + (uint32_t)(b * BN);
-                for (int c = 0; c < nch; ++c) {
+                for (int e = 0; e < nent; ++e) {
+                    const int c = e < nch ? e : e - nch;
+                    const uint32_t d_tmem = tmem + (uint32_t)((e < nch ? b : 1) * BN);
                     if (!mbar_wait(&full[s], ph, a.err, ERR_TIMEOUT_MMA)) return false;
                     tc_fence_after();
                     const uint8_t* st = sStage + s * kStageA;
@@ -345,7 +357,60 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
         const uint32_t lofs = (uint32_t)(quarter * 32) << 16;
         float sigma = 0.f;
         bool ok = true;
-        for (int t = 0; t < ntiles; ++t) {
+        float tmul = 0.f, tc = 0.f;
+        if (TAN) {
+            tmul = a.tparams[0];
+            tc = -a.crow[rowc] * a.tparams[1];
+        }
+        for (int t = 0; t < ntiles && TAN; ++t) {
+            // S and T of tile t (single buffer), a 32-column quarter at a time
+            if (!mbar_wait(&tfull[0], (uint32_t)(t & 1), a.err, ERR_TIMEOUT_EPILOGUE) ||
+                !mbar_wait(pempty, (uint32_t)(t & 1) ^ 1u, a.err, ERR_TIMEOUT_EPILOGUE)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float4* bp = reinterpret_cast<const float4*>(a.cbias + (int64_t)(j0 + t) * BN);
+#pragma unroll 1
+            for (int qq = 0; qq < BN / 32; ++qq) {
+                float v[32], tv[32];
+                tmem_ld32(tmem + lofs + qq * 32, v);
+                tmem_ld32(tmem + (uint32_t)BN + lofs + qq * 32, tv);
+                tmem_wait_ld();
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    const int u16 = qq * 4 + g8;
+                    const float4 b0 = __ldg(bp + 2 * u16);
+                    const float4 b1 = __ldg(bp + 2 * u16 + 1);
+                    const float* w = v + 8 * g8;
+                    const float* tw = tv + 8 * g8;
+                    const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                    float p[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        p[e] = ex2(fmaf(w[e], ks, bb[e]) - L) * fmaf(tw[e], tmul, tc);
+                    __align__(16) __half2 h[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        h[q] = live ? __floats2half2_rn(p[2 * q], p[2 * q + 1])
+                                    : __floats2half2_rn(0.f, 0.f);
+                        const float2 r = __half22float2(h[q]);
+                        sigma += r.x + r.y;
+                    }
+                    const int kq = u16 >> 3, u = u16 & 7;
+                    *reinterpret_cast<uint4*>(sP + kq * CHUNK_BYTES + swz_offset(rloc, u * 8)) =
+                        *reinterpret_cast<const uint4*>(h);
+                }
+            }
+            tc_fence_before();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&tempty[0]);
+                mbar_arrive(pfull);
+            }
+        }
+        for (int t = 0; t < ntiles && !TAN; ++t) {
             const int b = t & 1;
             if (!mbar_wait(&tfull[b], (uint32_t)((t >> 1) & 1), a.err, ERR_TIMEOUT_EPILOGUE)) {
                 ok = false;
@@ -396,12 +461,16 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
         }
         if (mbar_wait(ofull, 0, a.err, ERR_TIMEOUT_EPILOGUE) && ok) {
             tc_fence_after();
-            const float vinv = *a.vinv;
+            // TAN: the plan entries carried a factor 2^et
+            const float unt = TAN ? a.tparams[2] : 1.f;
+            const float vinv = *a.vinv * unt;
+            sigma *= unt;
             const float W = exp2f(a.phi[rowc] + L);
             float* prow = a.splits > 1
                               ? a.partial + ((int64_t)blockIdx.z * a.nr + row) * (a.k + 1)
                               : nullptr;
             if (live && a.splits > 1 && blockIdx.y == 0) prow[a.k] = sigma;
+            if (TAN && live && a.splits == 1 && blockIdx.y == 0) a.out2[row] = a.a[row] * W * sigma;
             for (int q = 0; q < (kvN + 31) / 32; ++q) {
                 float o[32];
                 tmem_ld32(tmem + kOCol + lofs + q * 32, o);
@@ -435,20 +504,24 @@ constexpr size_t apply_smem_bytes(int kv) {
 static_assert(apply_smem_bytes(128) <= kSmemLimit && apply_smem_bytes(256) <= kSmemLimit,
               "plan application does not fit in shared memory");
 
-template <int KV>
+template <int KV, bool TAN>
 cudaError_t launch_apply_kv(const TcApplyArgs& a, int row_tiles, cudaStream_t s) {
     constexpr size_t smem = apply_smem_bytes(KV);
-    cudaError_t e = cudaFuncSetAttribute(k_apply_tc<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k_apply_tc<KV, TAN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)row_tiles, (unsigned)((a.kpad + KV - 1) / KV), (unsigned)a.splits);
-    k_apply_tc<KV><<<grid, kApplyThreads, smem, s>>>(a);
+    k_apply_tc<KV, TAN><<<grid, kApplyThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_apply_tc(const TcApplyArgs& a, int row_tiles, cudaStream_t s) {
-    const cudaError_t e = apply_kv(a.nch, a.kpad) == 256 ? launch_apply_kv<256>(a, row_tiles, s)
-                                                         : launch_apply_kv<128>(a, row_tiles, s);
+    const bool wide = apply_kv(a.nch, a.kpad) == 256;
+    cudaError_t e;
+    if (a.mode == APPLY_TAN)
+        e = wide ? launch_apply_kv<256, true>(a, row_tiles, s) : launch_apply_kv<128, true>(a, row_tiles, s);
+    else
+        e = wide ? launch_apply_kv<256, false>(a, row_tiles, s) : launch_apply_kv<128, false>(a, row_tiles, s);
     count_launch();
     return e;
 }

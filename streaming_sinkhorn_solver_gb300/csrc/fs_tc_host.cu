@@ -139,12 +139,13 @@ fs_status prep_tc(Call& c, Problem& P, const TcPlan& p, const TcBufs& B, bool be
 
 struct TcApplyBufs {
     size_t lse2, phi, VT, vabs, vparams, partial, Xlo, Ylo, lse_partial;
+    size_t U16, Ulo, crow, tbits, tparams;     // APPLY_TAN only
     int splits, tps, kpad;
     int lse_splits, lse_tps;    // the log2-sum-exp pre-pass (one-CTA kernel, 128-column tiles)
 };
 
 void layout_apply(Layout& L, TcApplyBufs& A, const TcPlan& p, int64_t n, int32_t k, int sms,
-                  const fs_options* opt) {
+                  const fs_options* opt, bool tan = false) {
     A.kpad = (k + 15) / 16 * 16;
     const int kv = apply_kv(p.nch, A.kpad);
     const int64_t nkv = (A.kpad + kv - 1) / kv;
@@ -159,6 +160,14 @@ void layout_apply(Layout& L, TcApplyBufs& A, const TcPlan& p, int64_t n, int32_t
     A.Ylo = L.take((size_t)p.rty * p.nch * CHUNK_BYTES);
     choose_tc_splits(p.rtx, p.rty, sms, opt, &A.lse_splits, &A.lse_tps);
     A.lse_partial = L.take(sizeof(float2) * (size_t)n * A.lse_splits);
+    A.U16 = A.Ulo = A.crow = A.tbits = A.tparams = 0;
+    if (tan) {
+        A.U16 = L.take((size_t)p.rtx * p.nch * CHUNK_BYTES);
+        A.Ulo = L.take((size_t)p.rtx * p.nch * CHUNK_BYTES);
+        A.crow = L.take(sizeof(float) * n);
+        A.tbits = L.take(sizeof(unsigned int) * 4);
+        A.tparams = L.take(sizeof(float) * 4);
+    }
 }
 
 }  // namespace
@@ -166,14 +175,14 @@ void layout_apply(Layout& L, TcApplyBufs& A, const TcPlan& p, int64_t n, int32_t
 int64_t shard_unit_tc() { return 2 * BM; }
 
 int64_t workspace_bytes_tc(int64_t n, int64_t m, int32_t d, int32_t k, int sms,
-                           const fs_options* opt) {
+                           const fs_options* opt, bool tan) {
     const TcPlan p = plan_tc(n, m, d, sms, opt);
     Layout L;
     TcBufs B;
     layout_tc(L, B, n, m, d, p);
     if (k > 0) {
         TcApplyBufs A;
-        layout_apply(L, A, p, n, k, sms, opt);
+        layout_apply(L, A, p, n, k, sms, opt, tan);
     }
     return (int64_t)L.off;
 }
@@ -334,12 +343,13 @@ fs_status apply_tc(Call& c, Problem& P, int mode, const fs_options* opt) {
     TcBufs B;
     layout_tc(c.L, B, n, m, d, p);
     TcApplyBufs A;
-    layout_apply(c.L, A, p, n, k, c.ws->sms, opt);
+    const bool tan = mode == APPLY_TAN;
+    layout_apply(c.L, A, p, n, k, c.ws->sms, opt, tan);
     CosBufs cb;
     layout_cos(c.L, cb, P);
     FS_TRY(ensure_capacity(c));
-    for (Arr* X : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g, &P.V, &P.out}) bind(c, *X);
-    for (Arr* X : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g, &P.V}) FS_TRY(upload(c, *X));
+    for (Arr* X : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g, &P.V, &P.out, &P.U, &P.out2}) bind(c, *X);
+    for (Arr* X : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g, &P.V, &P.U}) FS_TRY(upload(c, *X));
     FS_TRY(prepare_cos(c, P, cb, mode != APPLY_PV));
     FS_TRY(prep_tc(c, P, p, B, true, c.at<void>(A.Xlo), c.at<void>(A.Ylo)));
 
@@ -376,7 +386,7 @@ fs_status apply_tc(Call& c, Problem& P, int mode, const fs_options* opt) {
     unsigned int* vabs = c.at<unsigned int>(A.vabs);
     float* vparams = c.at<float>(A.vparams);
     float* shift = c.at<float>(B.shift);
-    if (mode == APPLY_PV) {
+    if (mode == APPLY_PV || mode == APPLY_TAN) {
         FS_CUDA(cudaMemsetAsync(vabs, 0, sizeof(unsigned int), c.stream));
         FS_CUDA(launch_absmax(P.V.dev, m * (int64_t)k, vabs, c.stream));
         FS_CUDA(launch_value_scale(vabs, vparams, c.stream));
@@ -416,6 +426,24 @@ fs_status apply_tc(Call& c, Problem& P, int mode, const fs_options* opt) {
     ap.out = P.out.dev;
     ap.partial = A.splits > 1 ? c.at<float>(A.partial) : nullptr;
     ap.err = c.ws->err_word;
+    if (tan) {
+        // direction tiles (split fp16, own power-of-two scale), u_i . x~_i and
+        // the scales of the tangent weights
+        unsigned int* tbits = c.at<unsigned int>(A.tbits);
+        float* tparams = c.at<float>(A.tparams);
+        FS_CUDA(cudaMemsetAsync(tbits, 0, 4 * sizeof(unsigned int), c.stream));
+        FS_CUDA(launch_tan_rows(P.U.dev, P.X.dev, n, d, shift, c.at<float>(A.crow), tbits, c.stream));
+        FS_CUDA(launch_absmax(c.at<float>(B.nx), n, tbits + 2, c.stream));
+        FS_CUDA(launch_absmax(c.at<float>(B.ny), m, tbits + 3, c.stream));
+        FS_CUDA(launch_tan_params(tbits, c.at<float>(B.params) + 1, tparams, c.stream));
+        FS_CUDA(launch_to_tiles(P.U.dev, n, d, nullptr, tparams + 3, p.nch, p.rtx,
+                                c.at<void>(A.U16), c.at<void>(A.Ulo), c.stream));
+        ap.U = c.at<void>(A.U16);
+        ap.Ulo = c.at<void>(A.Ulo);
+        ap.tparams = tparams;
+        ap.crow = c.at<float>(A.crow);
+        ap.out2 = P.out2.dev;
+    }
     NvtxRange nvtx("fs plan application (tensor)");
     const int ts = timing_begin(c.stream);
     FS_CUDA(launch_apply_tc(ap, (int)p.rtx, c.stream));
@@ -425,6 +453,7 @@ fs_status apply_tc(Call& c, Problem& P, int mode, const fs_options* opt) {
     if (opt && opt->check_finite)
         FS_TRY(scan_finite(c, P.out.dev, n * (int64_t)k, c.at<unsigned int>(A.vabs) + 1));
     FS_TRY(download(c, P.out));
+    FS_TRY(download(c, P.out2));
     return FS_OK;
 }
 

@@ -149,10 +149,18 @@ struct TcApplyArgs {
     int64_t nr, nc;
     int nch, col_tiles, tiles_per_split, splits;
     int k, kpad;
-    int mode;               // APPLY_PV / APPLY_BARY / APPLY_GRAD
+    int mode;               // APPLY_PV / APPLY_BARY / APPLY_GRAD / APPLY_TAN
     float* out;             // n x k
     float* partial;         // splits x n x (k+1): unscaled sums, then sum_j p_ij
     uint32_t* err;
+    // APPLY_TAN: each p_ij is weighted by t_ij = u_i . (y_j - x_i), formed on
+    // the tensor cores as U K^T (split precision, a second TMEM buffer) minus
+    // the row constant u_i . x~_i; out2_i = a_i W_i sum_j p_ij t_ij.
+    const void* U;          // row-direction tiles (hi), same layout as Q
+    const void* Ulo;        // row-direction remainders
+    const float* tparams;   // [0] scale of U K^T to t 2^et, [1] 2^et, [2] 2^-et
+    const float* crow;      // u_i . x~_i per row
+    float* out2;            // n
 };
 
 size_t apply_smem_bytes();
@@ -162,6 +170,13 @@ cudaError_t launch_merge_apply_tc(const TcApplyArgs& a, cudaStream_t s);
 cudaError_t launch_vt_tiles(const float* V, int64_t m, int k, int kpad, const float* shift,
                             const float* scale_ptr, int64_t col_tiles, void* out,
                             cudaStream_t s);
+// tangent application: crow_i = u_i . x~_i and maxima of |u_i|^2, |u_ik| into
+// bits[0..1]; then the scales of the tangent weights from bits[0..3] (bits[2..3]:
+// max |x~_i|^2, max |y~_j|^2) and the column cloud's tile scale
+cudaError_t launch_tan_rows(const float* U, const float* X, int64_t rows, int d, const float* shift,
+                            float* crow, unsigned int* bits, cudaStream_t s);
+cudaError_t launch_tan_params(const unsigned int* bits, const float* yscale, float* tparams,
+                              cudaStream_t s);
 // max |V| as ordered float bits (atomicMax)
 cudaError_t launch_absmax(const float* V, int64_t len, unsigned int* bits, cudaStream_t s);
 // params[0] = 2^e with max|V| 2^e in [2^14, 2^15), params[1] = 2^-e

@@ -171,9 +171,15 @@ def test_hvp_rejects_bad_arguments(lib):
     st = lib.fs_hvp_x(X.ctypes.data, a.ctypes.data, 4, Y.ctypes.data, b.ctypes.data, 5, 2, 0.1,
                       f.ctypes.data, g.ctypes.data, None, out.ctypes.data, 0, 0.0, None, None)
     assert st == fs.FS_ERR_INVALID_ARG
-    st = lib.fs_hvp_x(X.ctypes.data, a.ctypes.data, 4, Y.ctypes.data, b.ctypes.data, 5, 100, 0.1,
+    st = lib.fs_hvp_x(X.ctypes.data, a.ctypes.data, 4, Y.ctypes.data, b.ctypes.data, 5, 5000, 0.1,
                       f.ctypes.data, g.ctypes.data, V.ctypes.data, out.ctypes.data, 0, 0.0, None,
                       None)
+    assert st == fs.FS_ERR_INVALID_ARG
+    opt = fs.fs_options()
+    opt.cost = fs.COSTS["cosine"]
+    st = lib.fs_hvp_x(X.ctypes.data, a.ctypes.data, 4, Y.ctypes.data, b.ctypes.data, 5, 2, 0.1,
+                      f.ctypes.data, g.ctypes.data, V.ctypes.data, out.ctypes.data, 0, 0.0,
+                      ctypes.byref(opt), None)
     assert st == fs.FS_ERR_UNSUPPORTED
 
 
@@ -246,3 +252,17 @@ def test_binding_declares_every_signature(lib):
             assert fn.restype == ctypes.c_int64, name
         elif ret.endswith("char*") or ret.endswith("char *"):
             assert fn.restype == ctypes.c_char_p, name
+
+
+def test_hvp_workspace_is_linear_in_the_dimension(lib):
+    """fs_hvp_x keeps O((n + m) d) device memory: no n x m array and no
+    n d^2 products (doubling d at most doubles it, doubling n and m at most
+    doubles it)."""
+    for d in (64, 512, 1024):
+        b1 = fs.fs_hvp_workspace_bytes(20000, 30000, d)
+        assert b1 > 0
+        assert fs.fs_hvp_workspace_bytes(20000, 30000, 2 * d) <= 2.05 * b1
+        assert fs.fs_hvp_workspace_bytes(40000, 60000, d) <= 2.5 * b1
+    # far below n d^2 floats at d = 1024
+    assert fs.fs_hvp_workspace_bytes(50000, 50000, 1024) < 4 * 50000 * 1024 * 64
+    assert fs.fs_hvp_workspace_bytes(100, 100, 8, path="fma") > 0
