@@ -471,6 +471,17 @@ fs_status fs_sparse_screen(const float* X, const float* a, int64_t n,
 fs_status fs_wait_selftest(int64_t timeout_ns, void* stream);
 
 /*
+ * fs_barrier_selftest -- the same check for the grid barrier of the one-launch
+ * solve (no counterpart on the pages).  Small FMA-path solves run every
+ * iteration in one cooperative kernel whose phases are separated by a grid
+ * barrier; each barrier wait gives up after a deadline (2 s in a solve), sets
+ * a bit in the device error word and ends the kernel.  This call launches two
+ * co-resident blocks of which only one arrives, with a deadline of
+ * timeout_ns (1e3 .. 1e9 ns); the next fs_check() returns FS_ERR_TIMEOUT.
+ */
+fs_status fs_barrier_selftest(int64_t timeout_ns, void* stream);
+
+/*
  * fs_debug_bounds -- bounds-check report (no counterpart on the pages).  A
  * debug build of the library (built with FS_DEBUG_BOUNDS:
  * libflashsinkhorn_dbg.so) checks the global-memory indices of its FMA,
@@ -523,9 +534,11 @@ int64_t fs_launch_count(void);
  * and the preparation of a call (kind 2: centring, norms, operand packing or
  * tiling, initial biases).  fs_timing_read synchronises those events and
  * returns, per kind, the summed elapsed milliseconds and the number of timed
- * regions since the previous read, then starts a new count.  Either output
- * pointer may be NULL.  Enabling adds two event records per timed region and
- * nothing else. */
+ * units since the previous read, then starts a new count: a unit is one
+ * launch, except that a small FMA-path solve run as one launch (every
+ * iteration in one cooperative kernel) counts as its 2 n_iter half-updates.
+ * Either output pointer may be NULL.  Enabling adds two event records per
+ * timed region and nothing else. */
 fs_status fs_timing_enable(int32_t on);
 fs_status fs_timing_read(double* ms_by_kind /* [3] */, int64_t* launches_by_kind /* [3] */);
 

@@ -37,7 +37,7 @@ EXPORTED = ("fs_sinkhorn_solve", "fs_apply_plan", "fs_barycentric", "fs_grad_x",
             "fs_timing_read", "fs_sinkhorn_solve_noalloc", "fs_unit_rates", "fs_hvp_x",
             "fs_sparse_solve", "fs_morton_order", "fs_sparse_screen", "fs_wait_selftest",
             "fs_debug_bounds", "fs_shard_unit", "fs_shard_range", "fs_fixup_stats",
-            "fs_hvp_workspace_bytes")
+            "fs_hvp_workspace_bytes", "fs_barrier_selftest")
 
 
 class FlashSinkhornError(RuntimeError):
@@ -141,6 +141,8 @@ def load_library(path: Optional[str] = None):
         lib.fs_fixup_stats.restype = ctypes.c_int
         lib.fs_hvp_workspace_bytes.argtypes = [i64, i64, i32, opt]
         lib.fs_hvp_workspace_bytes.restype = i64
+        lib.fs_barrier_selftest.argtypes = [i64, vp]
+        lib.fs_barrier_selftest.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -556,3 +558,9 @@ def fs_wait_selftest(timeout_ns: int = 1_000_000, *, stream=None) -> None:
     """Run the library's bounded device wait on a barrier nothing signals
     (see the C header); the next fs_check() raises FS_ERR_TIMEOUT."""
     _raise(load_library().fs_wait_selftest(int(timeout_ns), _stream(stream)))
+
+
+def fs_barrier_selftest(timeout_ns: int = 1_000_000, *, stream=None) -> None:
+    """Run the one-launch solve's grid barrier with a block that never
+    arrives (see the C header); the next fs_check() raises FS_ERR_TIMEOUT."""
+    _raise(load_library().fs_barrier_selftest(int(timeout_ns), _stream(stream)))

@@ -165,6 +165,7 @@ struct TimingState {
     bool on = false;
     std::vector<cudaEvent_t> pool;   // pairs: 2*slot (start), 2*slot+1 (end)
     std::vector<int> kind;           // kind of each used slot (-1 = open)
+    std::vector<int> units;          // timed units of each slot
     size_t used = 0;
 };
 TimingState g_timing;
@@ -189,6 +190,7 @@ int timing_begin(cudaStream_t s) {
             g_timing.pool.push_back(e);
         }
         g_timing.kind.push_back(-1);
+        g_timing.units.push_back(1);
     }
     g_timing.kind[slot] = -1;
     g_timing.used = slot + 1;
@@ -196,11 +198,12 @@ int timing_begin(cudaStream_t s) {
     return (int)slot;
 }
 
-void timing_end(int slot, int kind, cudaStream_t s) {
+void timing_end(int slot, int kind, cudaStream_t s, int units) {
     if (slot < 0) return;
     std::lock_guard<std::mutex> lk(g_timing.mu);
     cudaEventRecord(g_timing.pool[2 * slot + 1], s);
     g_timing.kind[slot] = kind;
+    g_timing.units[slot] = units;
 }
 
 // Column splits for a grid of row_blocks x splits blocks, per_sm of which
@@ -209,7 +212,7 @@ void timing_end(int slot, int kind, cudaStream_t s) {
 // columns; the split count minimising (waves x per-block cost) wins, so a
 // grid that would spill a thin last wave takes fewer, longer blocks.
 int choose_splits(int64_t row_blocks, int64_t nc, int sms, int per_sm, int64_t min_cols,
-                  const fs_options* opt, int64_t* cols_per_split) {
+                  const fs_options* opt, int64_t* cols_per_split, bool sm_balance) {
     constexpr double kBlockOverheadCols = 64.0;
     int64_t sp;
     if (opt && opt->splits > 0) {
@@ -225,7 +228,16 @@ int choose_splits(int64_t row_blocks, int64_t nc, int sms, int per_sm, int64_t m
             const int64_t cps = (nc + s - 1) / s;
             const int64_t used = (nc + cps - 1) / cps;
             const int64_t waves = (row_blocks * used + slots - 1) / slots;
-            const double cost = (double)waves * ((double)cps + kBlockOverheadCols);
+            double cost = (double)waves * ((double)cps + kBlockOverheadCols);
+            if (sm_balance) {
+                // blocks per SM, taken dynamically as slots free up: the SM with
+                // the most blocks sets the time; a grid of one wave starts every
+                // block at once and runs its barrier phases in step (measured 3-4 %
+                // slower at n = m = 50,000, d = 3, than 2.5 waves balanced per SM)
+                const int64_t per_sm_blocks = (row_blocks * used + sms - 1) / sms;
+                cost = (double)per_sm_blocks * ((double)cps + kBlockOverheadCols) *
+                       (waves < 2 ? 1.04 : 1.0);
+            }
             if (s == 1 || cost < best * (1.0 - 1e-9)) {
                 best = cost;
                 sp = used;
@@ -547,7 +559,7 @@ fs_status fs_timing_read(double* ms_by_kind, int64_t* launches_by_kind) {
         float t = 0.f;
         FS_CUDA(cudaEventElapsedTime(&t, g_timing.pool[2 * i], g_timing.pool[2 * i + 1]));
         ms[k] += (double)t;
-        cnt[k] += 1;
+        cnt[k] += g_timing.units[i];
     }
     g_timing.used = 0;
     for (int k = 0; k < TIME_KINDS; ++k) {

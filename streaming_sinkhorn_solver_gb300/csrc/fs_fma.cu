@@ -14,6 +14,7 @@
 #include "fs_debug.cuh"
 #include "fs_internal.cuh"
 
+#include <algorithm>
 #include <type_traits>
 
 namespace fs {
@@ -347,10 +348,10 @@ __device__ __forceinline__ void push_fix(const HalfArgs& a, int64_t row) {
 // the sum is range-checked at the end (here when the split is the whole row,
 // else in the merge).  MODE 2: as 1, through the CTA's affine fit of those
 // LSEs folded into the staged columns (cta_offset_fit; rows in Morton order).
-// Four CTAs per SM in the folded mode (64 registers; measured 1.4 % faster
-// than three at d = 3), three (d <= 8) or two otherwise.
+// The work of one CTA: row block rb (rows rb * 512 RP + ...) against the
+// columns of split sp.
 template <int D, int RP, int MODE>
-__global__ void __launch_bounds__(kThreads, MODE == 2 ? 4 : D <= 8 ? 3 : 2) k_half_fma(HalfArgs a) {
+__device__ __forceinline__ void half_body(const HalfArgs& a, int64_t rb, int64_t sp) {
     constexpr bool REF = MODE >= 1;
     constexpr int DS = fma_stride(D);
     constexpr int DD = fma_dup_stride(D);
@@ -360,8 +361,8 @@ __global__ void __launch_bounds__(kThreads, MODE == 2 ? 4 : D <= 8 ? 3 : 2) k_ha
     __shared__ float fit[D + 2];
 
     const int tid = threadIdx.x;
-    const int64_t row0 = (int64_t)blockIdx.x * (kThreads * RPT);
-    const int64_t c0 = (int64_t)blockIdx.y * a.cols_per_split;
+    const int64_t row0 = rb * (kThreads * RPT);
+    const int64_t c0 = sp * a.cols_per_split;
     const int64_t c1 = min(a.nc, c0 + a.cols_per_split);
 
     uint64_t q[RP][D];
@@ -458,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, MODE == 2 ? 4 : D <= 8 ? 3 : 2) k_ha
         const int64_t row = row0 + tid + i * kThreads;
         if (row >= a.nr) continue;
         if (a.splits > 1) {
-            const int64_t pi = (int64_t)blockIdx.y * a.nr + row;
+            const int64_t pi = sp * a.nr + row;
             if (FS_IDX_OK(pi, (int64_t)a.splits * a.nr, 2)) a.partial[pi] = make_float2(M[i], Sf[i]);
         } else {
             if (REF && !(Sf[i] >= kMinRefSum && Sf[i] <= kMaxRefSum)) push_fix(a, row);
@@ -467,6 +468,13 @@ __global__ void __launch_bounds__(kThreads, MODE == 2 ? 4 : D <= 8 ? 3 : 2) k_ha
             a.rows[row * DS + D] = a.rlogw2[row] - lse2;
         }
     }
+}
+
+// Four CTAs per SM in the folded mode (64 registers; measured 1.4 % faster
+// than three at d = 3), three (d <= 8) or two otherwise.
+template <int D, int RP, int MODE>
+__global__ void __launch_bounds__(kThreads, MODE == 2 ? 4 : D <= 8 ? 3 : 2) k_half_fma(HalfArgs a) {
+    half_body<D, RP, MODE>(a, blockIdx.x, blockIdx.y);
 }
 
 template <int D>
@@ -502,12 +510,12 @@ __device__ __forceinline__ void merge_pair(float& M, float& S, float Mo, float S
 // the splits l, l + lanes, ... in order, then a butterfly over the row's
 // lanes; fixed assignment and order, so the result does not depend on
 // timing.  Whole warps run, so that every lane takes part in the shuffles.
-__global__ void k_merge_lse(const float2* __restrict__ partial, int splits, int64_t nr,
-                            const float* __restrict__ rnorm, const float* __restrict__ rlogw2,
-                            float eps_ln2, float* __restrict__ pot, float* __restrict__ bias,
-                            int64_t bias_stride, int* __restrict__ fix_list,
-                            unsigned int* __restrict__ fix_count, int lanes) {
-    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+__device__ __forceinline__ void merge_slot(int64_t t, const float2* __restrict__ partial, int splits,
+                                           int64_t nr, const float* __restrict__ rnorm,
+                                           const float* __restrict__ rlogw2, float eps_ln2,
+                                           float* __restrict__ pot, float* __restrict__ bias,
+                                           int64_t bias_stride, int* __restrict__ fix_list,
+                                           unsigned int* __restrict__ fix_count, int lanes) {
     const int64_t i = t / lanes;
     const int l = (int)(t % lanes);
     float M = -INFINITY, S = 0.f;
@@ -537,24 +545,26 @@ __global__ void k_merge_lse(const float2* __restrict__ partial, int splits, int6
     bias[i * bias_stride] = rlogw2[i] - lse2;
 }
 
+__global__ void k_merge_lse(const float2* __restrict__ partial, int splits, int64_t nr,
+                            const float* __restrict__ rnorm, const float* __restrict__ rlogw2,
+                            float eps_ln2, float* __restrict__ pot, float* __restrict__ bias,
+                            int64_t bias_stride, int* __restrict__ fix_list,
+                            unsigned int* __restrict__ fix_count, int lanes) {
+    merge_slot((int64_t)blockIdx.x * blockDim.x + threadIdx.x, partial, splits, nr, rnorm, rlogw2,
+               eps_ln2, pot, bias, bias_stride, fix_list, fix_count, lanes);
+}
+
 // Recompute, with the online max, the rows listed by a guarded half-update:
 // one warp per listed row, lanes striding over all columns, then a shuffle
 // merge of the lanes' (max, sum).  The list length is read once per block;
 // the last block to finish resets the list for the next half-update.
 constexpr int kFixBlocks = 64;
 
+// One listed row, by one warp (lane = its lane).
 template <int D>
-__global__ void __launch_bounds__(256) k_fix_fma(HalfArgs a) {
+__device__ __forceinline__ void fix_row(const HalfArgs& a, int64_t row, int lane) {
     constexpr int DS = fma_stride(D);
-    __shared__ unsigned int s_cnt;
-    if (threadIdx.x == 0) s_cnt = min(*(volatile unsigned int*)&a.fix_count[0], (unsigned int)a.nr);
-    __syncthreads();
-    const unsigned int cnt = s_cnt;
-    const int lane = threadIdx.x & 31;
-    const int warps = gridDim.x * (blockDim.x >> 5);
-    for (unsigned int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < cnt; w += warps) {
-        const int64_t row = a.fix_list[w];
-        if (!FS_IDX_OK(row, a.nr, 4)) continue;
+    {
         float q[D];
 #pragma unroll
         for (int k = 0; k < D; ++k) q[k] = a.rows[row * DS + k] * a.kappa;
@@ -583,6 +593,21 @@ __global__ void __launch_bounds__(256) k_fix_fma(HalfArgs a) {
             a.rows[row * DS + D] = a.rlogw2[row] - lse2;
         }
     }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) k_fix_fma(HalfArgs a) {
+    __shared__ unsigned int s_cnt;
+    if (threadIdx.x == 0) s_cnt = min(*(volatile unsigned int*)&a.fix_count[0], (unsigned int)a.nr);
+    __syncthreads();
+    const unsigned int cnt = s_cnt;
+    const int lane = threadIdx.x & 31;
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    for (unsigned int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < cnt; w += warps) {
+        const int64_t row = a.fix_list[w];
+        if (!FS_IDX_OK(row, a.nr, 4)) continue;
+        fix_row<D>(a, row, lane);
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
@@ -603,6 +628,157 @@ cudaError_t launch_fix_fma_t(const HalfArgs& a, cudaStream_t s) {
     k_fix_fma<D><<<kFixBlocks, 256, 0, s>>>(a);
     count_launch();
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Whole solve in one cooperative launch, for problems small enough that
+// launches dominate (c1, c2 at 10^4 points).  Every half-update runs the same
+// three phases as the multi-launch path -- the half-update work items (row
+// block, column split), the split merge, the fixup of guarded rows -- with
+// the same per-row arithmetic, the same merge order (merge_slot) and the same
+// fixup (fix_row), so the potentials are bitwise those of separate launches.
+// The phases are separated by a grid barrier (all blocks are co-resident:
+// cudaLaunchCooperativeKernel) whose waits give up after SmallArgs::timeout_ns,
+// set ERR_TIMEOUT_BARRIER in the error word and end the kernel.
+//
+// The two sides use separate fixup lists: the f-half's list is reset (and
+// counted) by block 0 during the g-half and vice versa, when every block has
+// read it and before it is written again.
+
+__device__ __forceinline__ uint64_t fma_globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// bar[0] counts arrivals over the whole launch (zeroed before it): barrier k
+// is passed once it reaches k * gridDim.x.  Each block adds one with release
+// semantics (after its threads' writes, ordered by the block barrier) and
+// polls with acquire loads, so the critical path is the last arrival and one
+// poll.  gen counts the barriers this block has passed.  Returns false (in
+// every thread) when the wait gave up.
+__device__ __forceinline__ bool grid_barrier(unsigned int* bar, unsigned int& gen, uint32_t* err,
+                                             uint64_t timeout_ns) {
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned int target = (gen + 1u) * gridDim.x;
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(bar) : "memory");
+        int ok = 1;
+        const uint64_t deadline = fma_globaltimer() + timeout_ns;
+        for (;;) {
+            unsigned int v;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(bar) : "memory");
+            if ((int)(v - target) >= 0) break;
+            if (fma_globaltimer() > deadline) {
+                atomicOr(err, ERR_TIMEOUT_BARRIER);
+                ok = 0;
+                break;
+            }
+            __nanosleep(32);
+        }
+        s_ok = ok;
+    }
+    __syncthreads();
+    ++gen;
+    return s_ok != 0;
+}
+
+template <int D, int RP>
+__global__ void __launch_bounds__(kThreads, 3) k_solve_small(SmallArgs s) {
+    unsigned int gen = 0;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    for (int it = 0; it < s.n_iter; ++it) {
+        const bool ref = it >= s.ref_from;
+        for (int side = 0; side < 2; ++side) {
+            const HalfArgs& a = s.h[side];
+            const int64_t items = s.row_blocks[side] * a.splits;
+            for (int64_t w = blockIdx.x; w < items; w += gridDim.x) {
+                const int64_t rb = w % s.row_blocks[side], sp = w / s.row_blocks[side];
+                if (ref) half_body<D, RP, 1>(a, rb, sp);
+                else half_body<D, RP, 0>(a, rb, sp);
+            }
+            if (a.splits > 1) {
+                if (!grid_barrier(s.bar, gen, s.err, s.timeout_ns)) return;
+                const int64_t slots = a.nr * s.lanes[side];
+                for (int64_t t0 = (int64_t)blockIdx.x * kThreads; t0 < slots;
+                     t0 += (int64_t)gridDim.x * kThreads)
+                    merge_slot(t0 + tid, a.partial, a.splits, a.nr, a.rnorm, a.rlogw2, a.eps_ln2,
+                               a.pot, a.rows + D, fma_stride(D), ref ? a.fix_list : nullptr,
+                               ref ? a.fix_count : nullptr, s.lanes[side]);
+            }
+            if (!grid_barrier(s.bar, gen, s.err, s.timeout_ns)) return;
+            if (ref) {
+                // the other side's list was read completely before this point
+                if (blockIdx.x == 0 && tid == 0) {
+                    const HalfArgs& o = s.h[side ^ 1];
+                    const unsigned int oc = min(o.fix_count[0], (unsigned int)o.nr);
+                    if (o.fix_stats != nullptr && it - (side == 0 ? 1 : 0) >= s.ref_from) {
+                        o.fix_stats[0] += 1ull;
+                        o.fix_stats[1] += oc;
+                    }
+                    o.fix_count[0] = 0u;
+                }
+                const unsigned int cnt =
+                    min(*(volatile unsigned int*)&a.fix_count[0], (unsigned int)a.nr);
+                if (cnt > 0) {   // every block read the same count (the list is complete)
+                    const unsigned int warps = gridDim.x * (kThreads / 32);
+                    for (unsigned int w = blockIdx.x * (kThreads / 32) + (tid >> 5); w < cnt;
+                         w += warps) {
+                        const int64_t row = a.fix_list[w];
+                        if (!FS_IDX_OK(row, a.nr, 4)) continue;
+                        fix_row<D>(a, row, lane);
+                    }
+                    if (!grid_barrier(s.bar, gen, s.err, s.timeout_ns)) return;
+                }
+            }
+        }
+    }
+    // the last half's list: counted and reset by block 0 after the final barrier
+    if (blockIdx.x == 0 && tid == 0 && s.n_iter > s.ref_from) {
+        const HalfArgs& o = s.h[1];
+        if (o.fix_stats != nullptr) {
+            o.fix_stats[0] += 1ull;
+            o.fix_stats[1] += min(o.fix_count[0], (unsigned int)o.nr);
+        }
+        o.fix_count[0] = 0u;
+    }
+}
+
+// One block arrives, the other never does (a wait that must run out).
+__global__ void k_barrier_selftest(unsigned int* bar, uint32_t* err, uint64_t timeout_ns) {
+    if (blockIdx.x != 0) return;
+    unsigned int gen = 0;
+    grid_barrier(bar, gen, err, timeout_ns);
+}
+
+template <int D>
+int solve_small_blocks_t() {
+    static std::atomic<int> cached{0};
+    int v = cached.load(std::memory_order_relaxed);
+    if (v == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, k_solve_small<D, fma_row_pairs(D)>,
+                                                          kThreads, 0) != cudaSuccess || v < 1)
+            v = 1;
+        cached.store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+template <int D>
+cudaError_t launch_solve_small_t(const SmallArgs& a, int sms, cudaStream_t s) {
+    // no more blocks than work items of the larger half-update: every block
+    // takes part in every barrier
+    const int64_t items = std::max(a.row_blocks[0] * a.h[0].splits, a.row_blocks[1] * a.h[1].splits);
+    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(items, (int64_t)solve_small_blocks_t<D>() * sms));
+    SmallArgs args = a;
+    void* params[] = {&args};
+    const cudaError_t e = cudaLaunchCooperativeKernel(
+        (const void*)k_solve_small<D, fma_row_pairs(D)>, dim3((unsigned)blocks), dim3(kThreads),
+        params, 0, s);
+    count_launch();
+    return e;
 }
 
 // ---------------------------------------------------------------------------
@@ -802,12 +978,37 @@ int fma_half_blocks_per_sm(int D, bool folded) {
     }
 }
 
+cudaError_t launch_barrier_selftest(unsigned int* bar, uint32_t* err, uint64_t timeout_ns,
+                                    cudaStream_t s) {
+    void* params[] = {&bar, &err, &timeout_ns};
+    const cudaError_t e = cudaLaunchCooperativeKernel((const void*)k_barrier_selftest, dim3(2),
+                                                      dim3(32), params, 0, s);
+    count_launch();
+    return e;
+}
+
+int merge_lanes(int splits) {
+    int lanes = 1;
+    while (lanes < splits && lanes < 32) lanes *= 2;
+    return lanes;
+}
+
+cudaError_t launch_solve_small(int D, const SmallArgs& a, int sms, cudaStream_t s) {
+    switch (D) {
+        case 2: return launch_solve_small_t<2>(a, sms, s);
+        case 3: return launch_solve_small_t<3>(a, sms, s);
+        case 4: return launch_solve_small_t<4>(a, sms, s);
+        case 8: return launch_solve_small_t<8>(a, sms, s);
+        case 16: return launch_solve_small_t<16>(a, sms, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 cudaError_t launch_merge_lse(const float2* partial, int splits, int64_t nr, const float* rnorm,
                              const float* rlogw2, float eps_ln2, float* pot, float* bias,
                              int64_t bias_stride, cudaStream_t s, int* fix_list,
                              unsigned int* fix_count) {
-    int lanes = 1;
-    while (lanes < splits && lanes < 32) lanes *= 2;
+    const int lanes = merge_lanes(splits);
     const int64_t threads = nr * lanes;
     k_merge_lse<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
         partial, splits, nr, rnorm, rlogw2, eps_ln2, pot, bias, bias_stride, fix_list, fix_count,

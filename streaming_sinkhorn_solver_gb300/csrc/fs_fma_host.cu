@@ -26,22 +26,35 @@ bool fold_offsets(int64_t n, int64_t m, int32_t d) {
     return d <= kMortonMaxDim && (double)n * (double)m >= kFoldMinPairs;
 }
 
+
+// Solves below this many score pairs run as one cooperative launch
+// (k_solve_small): there a half-update's kernels take microseconds and the
+// launches between them would dominate.
+constexpr double kSmallMaxPairs = 268435456.0;   // 2^28
+
 FmaPlan plan_fma(int64_t n, int64_t m, int32_t d, int sms, const fs_options* opt) {
     FmaPlan p;
     p.D = fma_pad_dim(d);
     p.DS = fma_stride(p.D);
     const int64_t rows_per_block = fma_rows_per_block(p.D);
     const int per_sm = fma_half_blocks_per_sm(p.D, fold_offsets(n, m, d));
-    p.splits_f = choose_splits((n + rows_per_block - 1) / rows_per_block, m, sms, per_sm, 128, opt,
-                               &p.cps_f);
-    p.splits_g = choose_splits((m + rows_per_block - 1) / rows_per_block, n, sms, per_sm, 128, opt,
-                               &p.cps_g);
+    // separate launches per half-update (large problems): balance the blocks
+    // per SM; one-launch solves (small problems): down to 32 columns per block,
+    // so that a small problem still spreads over the SMs
+    const bool many = (double)n * (double)m >= kSmallMaxPairs;
+    const int64_t min_cols = many ? 128 : 32;
+    p.splits_f = choose_splits((n + rows_per_block - 1) / rows_per_block, m, sms, per_sm, min_cols,
+                               opt, &p.cps_f, many);
+    p.splits_g = choose_splits((m + rows_per_block - 1) / rows_per_block, n, sms, per_sm, min_cols,
+                               opt, &p.cps_g, many);
     return p;
 }
 
 struct FmaBufs {
     size_t shift_part, shift, PX, PY, nx, ny, lax, lby, partial, phi, apply_part, counter, fix_list,
         fix_count;
+    // one-launch solve: the g-half's own fixup list and count, the grid barrier
+    size_t fix_list2, fix_count2, bar;
     // Morton order of the solve (fold_offsets): permutations, sort buffers and
     // the potentials in that order
     MortonBufs srt;
@@ -71,6 +84,9 @@ void layout_fma(Layout& L, FmaBufs& B, int64_t n, int64_t m, int32_t d, const Fm
     B.counter = L.take(sizeof(unsigned int) * 4);
     B.fix_list = L.take(sizeof(int) * (size_t)std::max(n, m));
     B.fix_count = L.take(sizeof(unsigned int) * 2);
+    B.fix_list2 = L.take(sizeof(int) * (size_t)std::max(n, m));
+    B.fix_count2 = L.take(sizeof(unsigned int) * 2);
+    B.bar = L.take(sizeof(unsigned int) * 2);
     B.perm_x = B.perm_y = B.fs = B.gs = 0;
 }
 
@@ -191,10 +207,36 @@ fs_status solve_fma(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) 
         }
         return FS_OK;
     };
-    for (int32_t it = 0; it < n_iter; ++it) {
-        const bool ref = ref_ok && it >= kOnlineIters;
-        FS_TRY(half(hf, p.splits_f, ref));
-        FS_TRY(half(hg, p.splits_g, ref));
+    const bool one_launch = !fold && shards == 1 && !c.capturing &&
+                            (double)n * (double)m < kSmallMaxPairs;
+    if (one_launch) {
+        // the same half-updates, merges and fixups in one cooperative launch
+        NvtxRange nvtx("fs solve, one launch (FMA)");
+        SmallArgs sa{};
+        sa.h[0] = hf;
+        sa.h[1] = hg;
+        sa.h[1].fix_list = c.at<int>(B.fix_list2);
+        sa.h[1].fix_count = c.at<unsigned int>(B.fix_count2);
+        sa.row_blocks[0] = (n + unit - 1) / unit;
+        sa.row_blocks[1] = (m + unit - 1) / unit;
+        sa.lanes[0] = merge_lanes(p.splits_f);
+        sa.lanes[1] = merge_lanes(p.splits_g);
+        sa.n_iter = n_iter;
+        sa.ref_from = ref_ok ? kOnlineIters : n_iter;
+        sa.bar = c.at<unsigned int>(B.bar);
+        sa.err = c.ws->err_word;
+        sa.timeout_ns = 2000000000ull;
+        FS_CUDA(cudaMemsetAsync(sa.h[1].fix_count, 0, 2 * sizeof(unsigned int), c.stream));
+        FS_CUDA(cudaMemsetAsync(sa.bar, 0, 2 * sizeof(unsigned int), c.stream));
+        const int ts = timing_begin(c.stream);
+        FS_CUDA(launch_solve_small(p.D, sa, c.ws->sms, c.stream));
+        timing_end(ts, TIME_HALF, c.stream, 2 * n_iter);
+    } else {
+        for (int32_t it = 0; it < n_iter; ++it) {
+            const bool ref = ref_ok && it >= kOnlineIters;
+            FS_TRY(half(hf, p.splits_f, ref));
+            FS_TRY(half(hg, p.splits_g, ref));
+        }
     }
     if (fold) {
         FS_CUDA(launch_scatter_rows(pot_f, perm_x, n, P.f.dev, c.stream));

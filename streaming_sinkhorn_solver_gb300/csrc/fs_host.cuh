@@ -106,16 +106,19 @@ struct NvtxRange {
 };
 
 // Kernel timing (fs_timing_enable / fs_timing_read).  timing_begin returns a
-// slot (or -1 when timing is off); timing_end closes it.
+// slot (or -1 when timing is off); timing_end closes it, counting the region
+// as `units` timed units (one launch's several half-updates, for instance).
 enum TimingKind : int { TIME_HALF = 0, TIME_APPLY = 1, TIME_PREP = 2, TIME_KINDS = 3 };
 int timing_begin(cudaStream_t s);
-void timing_end(int slot, int kind, cudaStream_t s);
+void timing_end(int slot, int kind, cudaStream_t s, int units = 1);
 
 // TMA tensor map (128 bytes) over `rows` rows of 64 fp16 at `base`, box 64 x 128.
 fs_status make_chunk_tmap(void* map128, const void* base, uint64_t rows);
 
+// sm_balance: cost by the blocks per SM (dynamic scheduling over several
+// waves) instead of full waves.
 int choose_splits(int64_t row_blocks, int64_t nc, int sms, int per_sm, int64_t min_cols,
-                  const fs_options* opt, int64_t* cols_per_split);
+                  const fs_options* opt, int64_t* cols_per_split, bool sm_balance = false);
 
 // Largest dimension d and value width k the entry points accept.
 constexpr int kMaxDim = 4096;

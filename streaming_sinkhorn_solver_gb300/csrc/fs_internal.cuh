@@ -30,7 +30,12 @@ extern std::atomic<int64_t> g_launches;
 inline void count_launch(int64_t k = 1) { g_launches.fetch_add(k, std::memory_order_relaxed); }
 
 // Device error word bits (set by bounded waits; read by fs_check).
-enum : uint32_t { ERR_TIMEOUT_PRODUCER = 1u, ERR_TIMEOUT_MMA = 2u, ERR_TIMEOUT_EPILOGUE = 4u };
+enum : uint32_t {
+    ERR_TIMEOUT_PRODUCER = 1u,
+    ERR_TIMEOUT_MMA = 2u,
+    ERR_TIMEOUT_EPILOGUE = 4u,
+    ERR_TIMEOUT_BARRIER = 16u    // a grid barrier of the one-launch solve gave up
+};
 
 // ---------------------------------------------------------------------------
 // device helpers
@@ -114,6 +119,29 @@ struct HalfArgs {
     unsigned long long* fix_stats;
 };
 cudaError_t launch_half_fma(int D, const HalfArgs& a, cudaStream_t s);
+
+// The whole solve as one cooperative launch (small problems): n_iter
+// iterations of (f-half, g-half), each half-update's work items, split merge
+// and fixups separated by bounded grid barriers.  h[0] / h[1] are the two
+// halves' arguments as for launch_half_fma (with their own fixup lists).
+struct SmallArgs {
+    HalfArgs h[2];
+    int64_t row_blocks[2];
+    int lanes[2];             // merge lanes per row (as launch_merge_lse chooses)
+    int n_iter;
+    int ref_from;             // first iteration with reference offsets (n_iter: none)
+    unsigned int* bar;        // [2] grid barrier (arrivals, generation), zero before first use
+    uint32_t* err;            // device error word
+    uint64_t timeout_ns;      // a barrier wait gives up after this long
+};
+cudaError_t launch_solve_small(int D, const SmallArgs& a, int sms, cudaStream_t s);
+// Failure-detection self-test of that grid barrier: two co-resident blocks,
+// one of which never arrives; the other's wait gives up after timeout_ns and
+// sets ERR_TIMEOUT_BARRIER.  bar: [2] zeroed device words.
+cudaError_t launch_barrier_selftest(unsigned int* bar, uint32_t* err, uint64_t timeout_ns,
+                                    cudaStream_t s);
+// lanes per row of the split merge for `splits` partials
+int merge_lanes(int splits);
 // Recompute the listed rows with the online max; resets the list.
 cudaError_t launch_fix_fma(int D, const HalfArgs& a, cudaStream_t s);
 // Blocks of the half-update kernel for padded dimension D resident per SM

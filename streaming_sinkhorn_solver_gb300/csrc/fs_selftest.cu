@@ -48,8 +48,30 @@ fs_status selftest_entry(int64_t timeout_ns, void* stream) {
     return end_call(c);
 }
 
+fs_status barrier_selftest_entry(int64_t timeout_ns, void* stream) {
+    if (timeout_ns < 1000 || timeout_ns > 1000000000)
+        return fail(FS_ERR_INVALID_ARG, "timeout_ns=%lld must be in [1e3, 1e9]", (long long)timeout_ns);
+    Call c;
+    FS_TRY(begin_call(c, stream));
+    if (c.capturing) return fail(FS_ERR_UNSUPPORTED, "not inside a graph capture");
+    const size_t off = c.L.take(2 * sizeof(unsigned int));
+    FS_TRY(ensure_capacity(c));
+    unsigned int* bar = c.at<unsigned int>(off);
+    FS_CUDA(cudaMemsetAsync(bar, 0, 2 * sizeof(unsigned int), c.stream));
+    FS_CUDA(launch_barrier_selftest(bar, c.ws->err_word, (uint64_t)timeout_ns, c.stream));
+    return end_call(c);
+}
+
 }  // namespace
 }  // namespace fs
+
+extern "C" fs_status fs_barrier_selftest(int64_t timeout_ns, void* stream) {
+    try {
+        return fs::barrier_selftest_entry(timeout_ns, stream);
+    } catch (...) {
+        return fs::fail(FS_ERR_CUDA, "unexpected host exception");
+    }
+}
 
 extern "C" fs_status fs_wait_selftest(int64_t timeout_ns, void* stream) {
     try {

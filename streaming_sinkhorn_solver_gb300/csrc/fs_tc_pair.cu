@@ -134,7 +134,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(half_threads(REF), 1
     const uint32_t rank = cluster_rank();
     const bool leader = rank == 0;
     const int64_t rt = blockIdx.x;
-    const int j0 = blockIdx.y * a.tiles_per_split;
+    const int split = blockIdx.y;
+    const int j0 = split * a.tiles_per_split;
     const int j1 = min(a.col_tiles, j0 + a.tiles_per_split);
     const int ntiles = j1 - j0;
     const int nch = a.nch;
@@ -412,7 +413,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(half_threads(REF), 1
             }
             if (row < a.nr) {
                 if (a.splits > 1) {
-                    a.partial[(int64_t)blockIdx.y * a.nr + row] = make_float2(Mt, St);
+                    a.partial[(int64_t)split * a.nr + row] = make_float2(Mt, St);
                 } else {
                     if (REF && !(St >= kTcMinRefSum && St <= kTcMaxRefSum)) {
                         const unsigned int slot = atomicAdd(&a.fix_count[0], 1u);
@@ -447,7 +448,8 @@ cudaError_t launch_half_pair_t(const TcHalfArgs& a, const TensorMap128& tmQ, con
     const cudaError_t e = cudaFuncSetAttribute(
         k_half_pair<QRES, REF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_half_pair<QRES, REF><<<dim3((unsigned)row_tiles, (unsigned)a.splits), half_threads(REF), smem,
+    const dim3 grid((unsigned)row_tiles, (unsigned)a.splits);
+    k_half_pair<QRES, REF><<<grid, half_threads(REF), smem,
                              s>>>(tmQ, tmK, a);
     return cudaGetLastError();
 }

@@ -218,9 +218,14 @@ def test_reference_offset_path_with_fixups(eps, iters):
     iterations, so many rows fail the guarded range and are recomputed by the
     fixup kernel.  The potentials must still match the oracle."""
     inp = make_inputs("c2_n10k_d3", n=8192, m=8192, seed=91)
+    fs.fs_fixup_stats(reset=True)
     f, g, fr, gr, C, _ = _solve_both(inp, eps, iters, path="auto")
+    launches, fixed = fs.fs_fixup_stats(reset=True)
     assert max_abs(f, fr) <= F_TOL_FMA * C.max()
     assert max_abs(g, gr) <= F_TOL_FMA * C.max()
+    # one fixup pass per reference-offset half-update (this size runs as one launch)
+    assert launches == 2 * (iters - 2)
+    print(f"eps={eps}: {fixed} rows recomputed over {launches} fixup passes")
 
 
 @pytest.mark.parametrize("d", [1, 2, 3])
