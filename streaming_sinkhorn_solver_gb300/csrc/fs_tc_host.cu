@@ -158,7 +158,13 @@ void layout_apply(Layout& L, TcApplyBufs& A, const TcPlan& p, int64_t n, int32_t
     A.partial = A.splits > 1 ? L.take(sizeof(float) * (size_t)A.splits * n * (k + 1)) : 0;
     A.Xlo = L.take((size_t)p.rtx * p.nch * CHUNK_BYTES);
     A.Ylo = L.take((size_t)p.rty * p.nch * CHUNK_BYTES);
-    choose_tc_splits(p.rtx, p.rty, sms, opt, &A.lse_splits, &A.lse_tps);
+    // the pre-pass runs the solve's f-half kernel: CTA pairs for d > 128
+    if (p.pair) {
+        A.lse_splits = p.splits_f;
+        A.lse_tps = p.tps_f;
+    } else {
+        choose_tc_splits(p.rtx, p.rty, sms, opt, &A.lse_splits, &A.lse_tps);
+    }
     A.lse_partial = L.take(sizeof(float2) * (size_t)n * A.lse_splits);
     A.U16 = A.Ulo = A.crow = A.tbits = A.tparams = 0;
     if (tan) {
@@ -368,16 +374,23 @@ fs_status apply_tc(Call& c, Problem& P, int mode, const fs_options* opt) {
     h.nr = n;
     h.nc = m;
     h.nch = p.nch;
-    h.col_tiles = (int)p.rty;
+    h.col_tiles = (int)(p.pair ? p.rty / 2 : p.rty);
     h.tiles_per_split = A.lse_tps;
     h.splits = A.lse_splits;
-    h.stages = half_stages(p.nch, p.qres);
+    h.stages = p.pair ? pair_stages(p.nch, p.qres) : half_stages(p.nch, p.qres);
     h.eps_ln2 = (float)(eps * kLn2);
     h.rnorm = nullptr;
     h.pot = lse2;
     h.partial = c.at<float2>(A.lse_partial);
     h.err = c.ws->err_word;
-    FS_CUDA(launch_half_tc(h, (int)p.rtx, p.qres, c.stream));
+    if (p.pair) {
+        TensorMap128 tmX, tmY;
+        FS_TRY(make_chunk_tmap(&tmX, h.Q, (uint64_t)p.rtx * p.nch * BM));
+        FS_TRY(make_chunk_tmap(&tmY, h.K, (uint64_t)p.rty * p.nch * BM));
+        FS_CUDA(launch_half_pair(h, tmX, tmY, (int)p.rtx, p.qres, c.stream));
+    } else {
+        FS_CUDA(launch_half_tc(h, (int)p.rtx, p.qres, c.stream));
+    }
     if (A.lse_splits > 1)
         FS_CUDA(launch_merge_lse(h.partial, A.lse_splits, n, nullptr, nullptr, 0.f, lse2, nullptr, 1,
                                  c.stream));
