@@ -39,6 +39,8 @@ namespace fs {
 namespace {
 
 constexpr int kSB = 128;            // points per block
+constexpr int kSuper = 16;          // blocks per super-block of the two-level cull
+constexpr int64_t kSuperMinBlocks = 32;   // input blocks from which the super-block cull runs
 constexpr int kMortonBits = 21;     // quantisation cells per axis: 2^21
 constexpr int kSortTile = 2048;     // keys per CTA in a radix pass
 constexpr int kSpMaxDim = kMortonMaxDim;
@@ -469,6 +471,13 @@ struct ScreenArgs {
     int* lists;              // [nbo x nbi]
     int* counts;             // [nbo]
     unsigned long long* exact;  // accumulated: block pairs given the per-point bound
+    // super-block cull (nullptr: every input block is a candidate): per output
+    // super-block, the surviving input super-blocks in order, their count, and
+    // the largest bound among the culled ones
+    const int* slist;        // [nsbo x nsbi]
+    const int* scount;       // [nsbo]
+    const float* sculled;    // [nsbo]
+    int nsbi;
 };
 
 __device__ __forceinline__ void lse_merge(float& M, float& S, float Mo, float So) {
@@ -561,6 +570,115 @@ __device__ __forceinline__ int compact_offset(bool keep, int& base, int* s_wcnt)
     return off + __popc(bal & ((1u << lane) - 1u));
 }
 
+// ---------------------------------------------------------------------------
+// two-level cull: super-blocks of kSuper consecutive blocks
+//
+// With Delta = c_I - c_J between block centroids and r_B = |e_B| (e the
+// per-axis extents), the block-level bound's first majorant gives, by
+// Cauchy-Schwarz,  U_IJ <= m_I + m_J + (L/eps)(2 |Delta| (r_I + r_J) - |Delta|^2)
+// with m_B = max_B + log2 sum_B 2^{psi - max} the block's log2 mass.  Over
+// super-blocks I', J' whose centroid boxes are D apart (D <= |Delta|) and
+// R = max r_I + max r_J, 2 d R - d^2 <= 2 D R - D^2 (D >= R) or R^2, so
+//   U_IJ <= M_I' + M_J' + (L/eps) H,   M = max over the blocks of m.
+// The slack sigma of any contained pair is below 1/16 + 2^-16 (P_I' + P_J' +
+// Dmax^2 L/eps) (P the largest |max|, Dmax the largest centroid distance).
+// A super pair whose bound plus slack misses the smallest threshold of the
+// output super-block's blocks by kCullMargin holds no block the block-level
+// cull would keep, so the kept lists are those of the one-level cull.
+
+// per super-block: (centroid box lo, R) and (box hi, M), max |max psi|, min
+// log2 block weight
+__global__ void k_sp_super_stats(const float4* __restrict__ cen, const float4* __restrict__ ext,
+                                 const float* __restrict__ pmax, const float* __restrict__ a0,
+                                 const float* __restrict__ lW, int64_t nb, int64_t nsb,
+                                 float4* __restrict__ slo, float4* __restrict__ shi,
+                                 float* __restrict__ sp, float* __restrict__ slw) {
+    const int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (s >= nsb) return;
+    float4 lo = make_float4(INFINITY, INFINITY, INFINITY, 0.f);
+    float4 hi = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    float pm = 0.f, lw = INFINITY;
+    const int64_t b1 = min(nb, (s + 1) * kSuper);
+    for (int64_t b = s * kSuper; b < b1; ++b) {
+        const float4 c = cen[b], e = ext[b];
+        lo.x = fminf(lo.x, c.x);
+        lo.y = fminf(lo.y, c.y);
+        lo.z = fminf(lo.z, c.z);
+        hi.x = fmaxf(hi.x, c.x);
+        hi.y = fmaxf(hi.y, c.y);
+        hi.z = fmaxf(hi.z, c.z);
+        lo.w = fmaxf(lo.w, sqrtf(e.x * e.x + e.y * e.y + e.z * e.z));
+        hi.w = fmaxf(hi.w, pmax[b] + a0[b]);
+        pm = fmaxf(pm, fabsf(pmax[b]));
+        lw = fminf(lw, lW[b]);
+    }
+    slo[s] = lo;
+    shi[s] = hi;
+    sp[s] = pm;
+    slw[s] = lw;
+}
+
+struct SuperArgs {
+    const float4 *slo_o, *shi_o, *slo_i, *shi_i;
+    const float *sp_o, *sp_i, *slw_o;
+    int64_t nsbo, nsbi;
+    float l_over_eps;
+    float log2_tau;
+    float log2_nbi;
+    int* slist;               // [nsbo x nsbi]
+    int* scount;              // [nsbo]
+    float* sculled;           // [nsbo]
+};
+
+// One 256-thread block per output super-block: the input super-blocks whose
+// bound reaches the threshold, compacted in order, and the largest culled
+// bound.
+__global__ void __launch_bounds__(256) k_sp_super_screen(SuperArgs a) {
+    __shared__ int s_wcnt[8];
+    __shared__ float s_val[8];
+    const int64_t so = blockIdx.x;
+    const float4 lo = a.slo_o[so], hi = a.shi_o[so];
+    const float po = a.sp_o[so];
+    const float T = a.log2_tau + a.slw_o[so] - a.log2_nbi;
+    int* row = a.slist + so * a.nsbi;
+    int base = 0;
+    float culled = -INFINITY;
+    for (int64_t c0 = 0; c0 < a.nsbi; c0 += 256) {
+        const int64_t si = c0 + threadIdx.x;
+        bool surv = false;
+        if (si < a.nsbi) {
+            const float4 li = a.slo_i[si], hii = a.shi_i[si];
+            const float gx = fmaxf(0.f, fmaxf(lo.x - hii.x, li.x - hi.x));
+            const float gy = fmaxf(0.f, fmaxf(lo.y - hii.y, li.y - hi.y));
+            const float gz = fmaxf(0.f, fmaxf(lo.z - hii.z, li.z - hi.z));
+            const float fx = fmaxf(fabsf(hi.x - li.x), fabsf(hii.x - lo.x));
+            const float fy = fmaxf(fabsf(hi.y - li.y), fabsf(hii.y - lo.y));
+            const float fz = fmaxf(fabsf(hi.z - li.z), fabsf(hii.z - lo.z));
+            const float D = sqrtf(gx * gx + gy * gy + gz * gz);
+            const float R = lo.w + li.w;
+            const float H = D >= R ? (2.f * R - D) * D : R * R;
+            const float ub = hi.w + hii.w + a.l_over_eps * H;
+            const float sig = 0.0625f + 1.52587890625e-05f *
+                                            (po + a.sp_i[si] + (fx * fx + fy * fy + fz * fz) * a.l_over_eps);
+            surv = !(ub + sig + kCullMargin < T);   // a NaN bound survives
+            if (!surv) culled = fmaxf(culled, ub);
+        }
+        const int pos = compact_offset(surv, base, s_wcnt);
+        if (surv && FS_IDX_OK(pos, a.nsbi, 38)) row[pos] = (int)si;
+        __syncthreads();
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) culled = fmaxf(culled, __shfl_xor_sync(0xffffffffu, culled, o));
+    if ((threadIdx.x & 31) == 0) s_val[threadIdx.x >> 5] = culled;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float c = s_val[0];
+        for (int w = 1; w < 8; ++w) c = fmaxf(c, s_val[w]);
+        a.scount[so] = base;
+        a.sculled[so] = c;
+    }
+}
+
 // One 256-thread block per output block.
 //   1. Cull: every input block whose block-level bound is below the
 //      threshold (by kCullMargin) is skipped; the others ("survivors") are
@@ -598,13 +716,25 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
     const float pmo = a.pmax_o[O], a0o = a.a0_o[O];
     const float T = a.log2_tau + a.lw2_o[O] - log2f((float)a.nbi);
 
-    // 1. cull (and the largest block-level bound among the culled blocks)
+    // 1. cull (and the largest block-level bound among the culled blocks).
+    // The candidates are every input block, or the blocks of the input
+    // super-blocks that survived the super-block cull of this output block's
+    // super-block (culled_ub then starts from the largest culled super bound).
     int S = 0;
     float culled_ub = -INFINITY;
-    for (int c0 = 0; c0 < a.nbi; c0 += 256) {
-        const int J = c0 + threadIdx.x;
+    int ncand = a.nbi;
+    const int* sl = nullptr;
+    if (a.slist != nullptr) {
+        const int so = O / kSuper;
+        sl = a.slist + (int64_t)so * a.nsbi;
+        ncand = a.scount[so] * kSuper;
+        culled_ub = a.sculled[so];
+    }
+    for (int c0 = 0; c0 < ncand; c0 += 256) {
+        const int k = c0 + threadIdx.x;
+        const int J = sl == nullptr ? k : (k < ncand ? sl[k / kSuper] * kSuper + k % kSuper : a.nbi);
         bool surv = false;
-        if (J < a.nbi) {
+        if (k < ncand && J < a.nbi) {
             float ub, sig;
             bound_cheap(a, co, eo, lo, pmo, a0o, J, ub, sig);
             surv = ub + sig + kCullMargin >= T;
@@ -1229,7 +1359,8 @@ inline unsigned grid_for(int64_t cnt, int threads) { return (unsigned)((cnt + th
 
 struct SpSide {
     size_t xs, ws, rec, norm, lw, pot, scr, pmax, a0, lin, ext, cen, cenf, W, lW, perm;
-    int64_t cnt, nb;
+    size_t slo, shi, sp, slw;      // super-block statistics
+    int64_t cnt, nb, nsb;
 };
 
 struct SpBufs {
@@ -1237,6 +1368,7 @@ struct SpBufs {
     size_t shift_part, shift;
     SpSide X, Y;
     size_t lists, counts, order, rowsum, red_part, red_out, kept, fix_list, fix_count;
+    size_t slist, scount, sculled;   // super-block cull
     // coarse stage
     size_t cshift, cPX, cPY, cnx, cny, clx, cly, cpart, F, G;
     int csplits_f, csplits_g;
@@ -1262,6 +1394,11 @@ void layout_side(Layout& L, SpSide& s, int64_t cnt, int d) {
     s.cenf = L.take(sizeof(float) * s.nb * d);
     s.W = L.take(sizeof(float) * s.nb);
     s.lW = L.take(sizeof(float) * s.nb);
+    s.nsb = (s.nb + kSuper - 1) / kSuper;
+    s.slo = L.take(sizeof(float4) * s.nsb);
+    s.shi = L.take(sizeof(float4) * s.nsb);
+    s.sp = L.take(sizeof(float) * s.nsb);
+    s.slw = L.take(sizeof(float) * s.nsb);
 }
 
 void layout_sparse(Layout& L, SpBufs& B, int64_t n, int64_t m, int d, int sms, bool coarse) {
@@ -1281,6 +1418,9 @@ void layout_sparse(Layout& L, SpBufs& B, int64_t n, int64_t m, int d, int sms, b
     B.kept = L.take(sizeof(unsigned long long) * 4);
     B.fix_list = L.take(sizeof(int) * mx);
     B.fix_count = L.take(sizeof(unsigned int) * 2);
+    B.slist = L.take(sizeof(int) * (size_t)std::max(B.X.nsb * B.Y.nsb, (int64_t)1));
+    B.scount = L.take(sizeof(int) * std::max(B.X.nsb, B.Y.nsb));
+    B.sculled = L.take(sizeof(float) * std::max(B.X.nsb, B.Y.nsb));
     if (coarse) {
         const int D = fma_pad_dim(d);
         const int DS = fma_stride(D);
@@ -1399,7 +1539,42 @@ fs_status screen(Call& c, const SpBufs& B, const SpSide& o, const SpSide& in, fl
     s.lists = c.at<int>(B.lists);
     s.counts = c.at<int>(B.counts);
     s.exact = c.at<unsigned long long>(B.kept) + 2;
+    s.slist = nullptr;
+    s.scount = nullptr;
+    s.sculled = nullptr;
+    s.nsbi = (int)in.nsb;
     NvtxRange nvtx("fs screening (block-sparse)");
+    if (in.nb >= kSuperMinBlocks && tau > 0.f) {
+        // two-level cull: super-block statistics of both sides (the masses change
+        // with every potential), then the super pairs
+        for (const SpSide* sd : {&o, &in})
+            k_sp_super_stats<<<grid_for(sd->nsb, 128), 128, 0, c.stream>>>(
+                c.at<float4>(sd->cen), c.at<float4>(sd->ext), c.at<float>(sd->pmax),
+                c.at<float>(sd->a0), c.at<float>(sd->lW), sd->nb, sd->nsb, c.at<float4>(sd->slo),
+                c.at<float4>(sd->shi), c.at<float>(sd->sp), c.at<float>(sd->slw));
+        SuperArgs sa;
+        sa.slo_o = c.at<float4>(o.slo);
+        sa.shi_o = c.at<float4>(o.shi);
+        sa.slo_i = c.at<float4>(in.slo);
+        sa.shi_i = c.at<float4>(in.shi);
+        sa.sp_o = c.at<float>(o.sp);
+        sa.sp_i = c.at<float>(in.sp);
+        sa.slw_o = c.at<float>(o.slw);
+        sa.nsbo = o.nsb;
+        sa.nsbi = in.nsb;
+        sa.l_over_eps = s.l_over_eps;
+        sa.log2_tau = s.log2_tau;
+        sa.log2_nbi = log2f((float)in.nb);
+        sa.slist = c.at<int>(B.slist);
+        sa.scount = c.at<int>(B.scount);
+        sa.sculled = c.at<float>(B.sculled);
+        k_sp_super_screen<<<(unsigned)o.nsb, 256, 0, c.stream>>>(sa);
+        count_launch(3);
+        FS_CUDA(cudaGetLastError());
+        s.slist = sa.slist;
+        s.scount = sa.scount;
+        s.sculled = sa.sculled;
+    }
     k_sp_screen<<<(unsigned)o.nb, 256, 0, c.stream>>>(s);
     count_launch();
     FS_CUDA(cudaGetLastError());

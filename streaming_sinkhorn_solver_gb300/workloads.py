@@ -88,6 +88,14 @@ WORKLOADS: Dict[str, Workload] = {
         about="block-sparse solver: the c2 recipe (X~U[0,1]^3, Y 4-component GMM sigma 0.1, "
               "uniform weights) at n=m=1e6, eps=1e-3 (blur 0.03, three mean spacings), 50 "
               "centroid iterations, then 50 block-sparse iterations with tau=1e-6"),
+    # the same recipe at four times the points, eps scaled with the squared mean
+    # spacing (4^(2/3)) so that a point still interacts with as many neighbours
+    "bs_n4m_d3": Workload(
+        "bs_n4m_d3", 4_000_000, 4_000_000, 3, ((0.00036, 20),), None, seed=1008,
+        coarse_iters=50, tau=1e-6,
+        about="block-sparse solver at n=m=4e6: the c2 recipe, eps=3.6e-4 (blur 0.019, three "
+              "mean spacings), 50 centroid iterations, then 20 block-sparse iterations with "
+              "tau=1e-6"),
 }
 
 

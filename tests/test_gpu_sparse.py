@@ -64,6 +64,11 @@ def test_morton_order_with_ties_bit_exact(d):
 
 def _screen_case(name, n, m, d, eps, dense_iters):
     inp = make_inputs(name, n=n, m=m, d=d)
+    if n * m > 5e7:
+        # one iteration from g = 0, row by row (no n x m cost matrix)
+        f = orc.f_update_rows(inp["X"], inp["Y"], inp["b"], eps, np.zeros(m), np.arange(n))
+        g = orc.f_update_rows(inp["Y"], inp["X"], inp["a"], eps, f, np.arange(m))
+        return inp, f.astype(np.float32), g.astype(np.float32)
     C = orc.cost(inp["X"], inp["Y"])
     f, g = orc.sinkhorn(C, inp["a"], inp["b"], eps, dense_iters)
     return inp, f.astype(np.float32), g.astype(np.float32)
@@ -75,6 +80,10 @@ def _screen_case(name, n, m, d, eps, dense_iters):
     ("c2_n10k_d3", 4000, 4000, 2, 0.001, 1e-6, 0),
     ("c1_n512_d2", 2600, 1900, 2, 0.02, 1e-3, 1),
     ("c2_n10k_d3", 2000, 2200, 1, 0.0005, 1e-5, 0),
+    # 157 x 141 blocks: the two-level cull (super-blocks of 16 blocks) runs
+    ("c2_n10k_d3", 20000, 18000, 3, 0.002, 1e-6, 0),
+    ("c2_n10k_d3", 20000, 18000, 3, 0.002, 1e-6, 1),
+    ("c2_n10k_d3", 16000, 17000, 2, 0.0005, 1e-5, 0),
 ])
 def test_screening_decisions_match_oracle(name, n, m, d, eps, tau, side):
     inp, f32, g32 = _screen_case(name, n, m, d, eps, 6)
