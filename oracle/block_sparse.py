@@ -18,10 +18,12 @@ the plainest reading of its sections, written out in float64 numpy:
 * *How to cut space so that skipping is safe*: points are put in Morton
   (Z-order) so that a block of consecutive points is spatially compact, and
   a block pair of the plan is the interaction of two such groups.
-  Reading: coordinates are quantised to 2^21 cells per axis over the joint
-  bounding box of both clouds (float32 arithmetic, as the kernels do), the
-  bits are interleaved (bit b of axis k at position b*d + k), points are
-  sorted stably by that code, and cut into blocks of 128 consecutive points.
+  Reading: coordinates are quantised to 2^B cells per axis over the joint
+  bounding box of both clouds (float32 arithmetic, as the kernels do), with
+  B = min(21, floor(63 / d)) so that the interleaved code fits 64 bits (21
+  for d <= 3; 15, 12, 10, 9 and 7 for d = 4 .. 8), the bits are interleaved
+  (bit b of axis k at position b*d + k), points are sorted stably by that
+  code, and cut into blocks of 128 consecutive points.
 * *How to guarantee that skipping is safe*: every block's contribution is
   bounded, blocks below a threshold set by block mass are skipped, and the
   threshold bounds the error the skipped tiles can make in every row and
@@ -57,7 +59,7 @@ import numpy as np
 
 from . import as_eps, cost, sinkhorn
 
-MORTON_BITS = 21
+MORTON_BITS = 21            # cells per axis 2^21 for d <= 3 (morton_bits for larger d)
 BLOCK = 128
 L2E = 1.4426950408889634074   # log2(e)
 
@@ -71,13 +73,20 @@ def morton_box(X, Y) -> Tuple[np.ndarray, np.ndarray]:
     return P.min(axis=0), P.max(axis=0)
 
 
-def morton_codes(P, lo, hi, bits: int = MORTON_BITS) -> np.ndarray:
+def morton_bits(d: int) -> int:
+    """Quantisation bits per axis: the d-axis code fits 64 bits."""
+    return min(MORTON_BITS, 63 // d)
+
+
+def morton_codes(P, lo, hi, bits: Optional[int] = None) -> np.ndarray:
     """Z-order codes: q_k = floor((p_k - lo_k) * (2^bits / (hi_k - lo_k))) in
     float32 arithmetic (each operation rounded once), clamped to
     [0, 2^bits - 1] (q = 0 on an axis of zero extent); bit b of q_k goes to
-    bit b*d + k of the code."""
+    bit b*d + k of the code.  bits defaults to morton_bits(d)."""
     P = np.asarray(P, np.float32)
     n, d = P.shape
+    if bits is None:
+        bits = morton_bits(d)
     lo = np.asarray(lo, np.float32)
     hi = np.asarray(hi, np.float32)
     span = (hi - lo).astype(np.float32)

@@ -72,6 +72,24 @@ def test_morton_order_is_recursive_ztree_order(d):
     np.testing.assert_array_equal(order, _ztree_order(q, 21))
 
 
+@pytest.mark.parametrize("d,bits", [(4, 15), (5, 12), (8, 7)])
+def test_morton_order_is_recursive_ztree_order_in_more_dimensions(d, bits):
+    """The same pin for d = 4, 5 and 8, whose codes quantise each axis to
+    2^floor(63 / d) cells (15, 12 and 7 bits) so that they fit 64 bits."""
+    assert bsp.morton_bits(d) == bits
+    rng = np.random.default_rng(20 + d)
+    G = 2 ** bits
+    pts = rng.integers(0, G, size=(400, d))
+    pts[:50] = rng.integers(0, 2, size=(50, d))           # dense corner, many ties
+    pts[50:70] = pts[200:220]                             # exact duplicates
+    X = pts.astype(np.float32)
+    Y = np.vstack([np.zeros((1, d)), np.full((1, d), G)]).astype(np.float32)
+    lo, hi = bsp.morton_box(X, Y)
+    order = np.argsort(bsp.morton_codes(X, lo, hi), kind="stable")
+    q = np.clip(pts, 0, G - 1).astype(np.int64)
+    np.testing.assert_array_equal(order, _ztree_order(q, bits))
+
+
 def test_morton_codes_small_grid_by_hand():
     """The four cells of a 2 x 2 grid in two dimensions come in Z order
     (0,0), (1,0), (0,1), (1,1): codes 0, 1, 2, 3 at the top level."""
@@ -120,8 +138,8 @@ def test_coarse_stage_with_one_point_per_cell_is_the_dense_solve():
 
 # --- the block bound and the screening -----------------------------------------
 
-def _sorted_problem(name="c2_n10k_d3", n=900, m=700, eps=0.005, iters=8, block=32):
-    inp = make_inputs(name, n=n, m=m)
+def _sorted_problem(name="c2_n10k_d3", n=900, m=700, eps=0.005, iters=8, block=32, d=None):
+    inp = make_inputs(name, n=n, m=m, d=d)
     px, py = bsp.morton_order(inp["X"], inp["Y"])
     Xs, as_, Ys, bs = inp["X"][px], inp["a"][px], inp["Y"][py], inp["b"][py]
     C = orc.cost(Xs, Ys)
@@ -143,9 +161,9 @@ def _true_block_mass(p):
     return M
 
 
-@pytest.mark.parametrize("eps", [0.05, 0.005])
-def test_block_bound_is_never_below_the_block_mass(eps):
-    p = _sorted_problem(eps=eps)
+@pytest.mark.parametrize("eps,d", [(0.05, None), (0.005, None), (0.02, 6), (0.05, 8)])
+def test_block_bound_is_never_below_the_block_mass(eps, d):
+    p = _sorted_problem(eps=eps, d=d)
     U, sig = bsp.block_bounds(p["Xs"], p["as_"], p["fs"], p["Ys"], p["bs"], p["gs"], eps,
                               p["cx"], p["cy"], p["block"])
     M = _true_block_mass(p)
@@ -190,8 +208,9 @@ def test_screening_bounds_the_omitted_mass_per_block(tau):
 
 # --- the block-sparse iteration --------------------------------------------------
 
-def test_iteration_without_screening_is_the_dense_solve():
-    inp = make_inputs("c2_n10k_d3", n=600, m=500)
+@pytest.mark.parametrize("d", [3, 5, 8])
+def test_iteration_without_screening_is_the_dense_solve(d):
+    inp = make_inputs("c2_n10k_d3", n=600, m=500, d=d)
     f, g, rep = bsp.solve(inp["X"], inp["a"], inp["Y"], inp["b"], 0.01, 0, 7, 0.0, block=64)
     fr, gr = orc.sinkhorn(orc.cost(inp["X"], inp["Y"]), inp["a"], inp["b"], 0.01, 7)
     cmax = orc.cost(inp["X"], inp["Y"]).max()
@@ -229,17 +248,20 @@ def test_masked_updates_make_the_kept_marginals_exact():
     np.testing.assert_allclose(cols, p["bs"], rtol=1e-10)
 
 
-def test_screened_iteration_converges_to_the_dense_fixed_point():
+@pytest.mark.parametrize("d,eps,n,kept", [(2, 0.01, 800, 0.9), (5, 0.02, 1500, 0.97)])
+def test_screened_iteration_converges_to_the_dense_fixed_point(d, eps, n, kept):
     """At the returned potentials the dense plan differs from the block-sparse
     one only by the omitted blocks, whose mass the screening bounds by tau in
     each marginal: |P_dense 1 - a|_1 <= residual + tau, |P_dense^T 1 - b|_1 <= tau."""
-    inp = make_inputs("c2_n10k_d3", n=800, m=800, d=2)
-    eps, tau = 0.01, 1e-4
+    inp = make_inputs("c2_n10k_d3", n=n, m=n, d=d)
+    tau = 1e-4
     C = orc.cost(inp["X"], inp["Y"])
     f, g, rep = bsp.solve(inp["X"], inp["a"], inp["Y"], inp["b"], eps, 30, 400, tau,
                           target=1e-5, check_every=10, block=32)
     assert rep["residual"] <= 1e-5 and rep["iters"] < 400
-    assert rep["kept_pairs"] < 0.9 * 2 * rep["iters"] * 800 * 800
+    # in five dimensions blocks of 32 uniform points are far from compact:
+    # the screening still skips some
+    assert rep["kept_pairs"] < kept * 2 * rep["iters"] * n * n
     r, c = orc.marginals(C, inp["a"], inp["b"], eps, f, g)
     assert np.abs(r - inp["a"]).sum() <= rep["residual"] + tau
     assert np.abs(c - inp["b"]).sum() <= tau
@@ -268,7 +290,7 @@ PINS = [
     lambda: test_morton_codes_small_grid_by_hand(),
     lambda: test_block_stats_of_single_points_are_the_points(),
     lambda: test_block_stats_weighted_mean(),
-    lambda: test_block_bound_is_never_below_the_block_mass(0.005),
+    lambda: test_block_bound_is_never_below_the_block_mass(0.005, None),
     lambda: test_block_bound_of_single_points_is_the_plan_entry(),
     lambda: test_screening_bounds_the_omitted_mass_per_block(1e-2),
     lambda: test_masked_updates_make_the_kept_marginals_exact(),
