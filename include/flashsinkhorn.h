@@ -364,12 +364,13 @@ fs_status fs_unit_rates(double* out, void* stream);
  * sections on the coarse centroid stage, the Morton ordering, block screening
  * and the per-row / per-column bound on the skipped tiles.  Readings (the post
  * gives no formulas):
- *   - Morton order: coordinates quantised to 2^21 cells per axis over the
- *     joint bounding box of X and Y, q_k = floor((p_k - lo_k) * (2^21 /
- *     (hi_k - lo_k))) in float32 (each operation rounded once), clamped to
- *     [0, 2^21 - 1]; bit b of q_k is bit b*d + k of the code; each cloud is
- *     sorted stably by its code.  Blocks (and cells) are 128 consecutive
- *     sorted points.
+ *   - Morton order: coordinates quantised to 2^B cells per axis over the
+ *     joint bounding box of X and Y, B = 21 for d <= 3 and floor(63 / d)
+ *     above (so the d*B-bit code fits 64 bits), q_k = floor((p_k - lo_k) *
+ *     (2^B / (hi_k - lo_k))) in float32 (each operation rounded once),
+ *     clamped to [0, 2^B - 1]; bit b of q_k is bit b*d + k of the code; each
+ *     cloud is sorted stably by its code.  Blocks (and cells) are 128
+ *     consecutive sorted points.
  *   - Coarse stage: coarse_iters dense Sinkhorn iterations (the same update)
  *     between the blocks' weight-averaged centroids with the blocks' weights;
  *     every point takes its block's potential.
@@ -417,7 +418,7 @@ typedef struct fs_sparse_report {
 } fs_sparse_report;
 
 /*
- * fs_sparse_solve -- the block-sparse solver above, for 1 <= d <= 3.
+ * fs_sparse_solve -- the block-sparse solver above, for 1 <= d <= 8.
  * X, a, Y, b as in fs_sinkhorn_solve (device or host memory).  f (n) and g
  * (m) are outputs; with coarse_iters == 0 they are also inputs: the first
  * screening bounds the plan at (f, g), so pass a consistent pair (e.g. the
@@ -427,7 +428,7 @@ typedef struct fs_sparse_report {
  * test and at the end, and cannot be captured in a CUDA graph.
  * Workspace: O((n + m) + (n/128)(m/128)) -- the kept-block lists hold one int
  * per block pair; more than 2^30 block pairs is FS_ERR_UNSUPPORTED.
- * Errors: FS_ERR_UNSUPPORTED for d > 3; FS_ERR_INVALID_ARG for null pointers,
+ * Errors: FS_ERR_UNSUPPORTED for d > 8; FS_ERR_INVALID_ARG for null pointers,
  * sizes < 1, eps <= 0, tau outside [0, 1), negative counts or target, or
  * non-zero reserved fields.
  */

@@ -485,7 +485,7 @@ def fs_sinkhorn_solve_noalloc(X, a, Y, b, eps: float, n_iter: int, f, g, *, stre
 
 
 # ---------------------------------------------------------------------------
-# block-sparse solver for low dimension (d <= 3)
+# block-sparse solver for low dimension (d <= 8)
 
 def fs_sparse_solve(X, a, Y, b, eps: float, *, coarse_iters: int = 0, max_iters: int = 100,
                     tau: float = 1e-6, target: float = 0.0, check_every: int = 0, f=None, g=None,

@@ -23,7 +23,7 @@ struct FmaPlan {
 constexpr double kFoldMinPairs = 268435456.0;   // 2^28
 
 bool fold_offsets(int64_t n, int64_t m, int32_t d) {
-    return d <= kMortonMaxDim && (double)n * (double)m >= kFoldMinPairs;
+    return d <= 3 && (double)n * (double)m >= kFoldMinPairs;
 }
 
 

@@ -1,9 +1,10 @@
 // Morton (Z-order) permutation of two low-dimensional clouds, shared by the
 // block-sparse solver and the dense FMA path.
 //
-// Both clouds are quantised on one joint bounding box (2^21 cells per axis)
-// and sorted by their interleaved codes with a stable radix sort, so equal
-// codes keep the caller's order.  Consecutive points of the result form
+// Both clouds are quantised on one joint bounding box (2^B cells per axis,
+// B = min(21, floor(63 / d)): the interleaved code fits 64 bits) and sorted
+// by their interleaved codes with a stable radix sort, so equal codes keep
+// the caller's order.  Consecutive points of the result form
 // compact groups in space ("FlashSinkhorn 2: Block-Sparse Entropic Optimal
 // Transport", Morton sorting).
 #pragma once
@@ -12,7 +13,9 @@
 
 namespace fs {
 
-constexpr int kMortonMaxDim = 3;
+constexpr int kMortonMaxDim = 8;
+// quantisation bits per axis of a d-dimensional Morton code
+__host__ __device__ constexpr int morton_bits(int d) { return d <= 3 ? 21 : 63 / d; }
 
 // Workspace offsets of the sort's buffers (box, keys, values, histograms).
 struct MortonBufs {

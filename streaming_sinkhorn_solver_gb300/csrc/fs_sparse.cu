@@ -1,4 +1,4 @@
-// Block-sparse solver for low-dimensional clouds (d <= 3).
+// Block-sparse solver for low-dimensional clouds (d <= 8).
 //
 // "FlashSinkhorn 2: Block-Sparse Entropic Optimal Transport" (patty.io post):
 //   - coarse resolution first: a solve between cell centroids whose
@@ -25,15 +25,16 @@
 //   the first maximiser of U; the omitted mass of every output block is then
 //   below tau W_O.
 //
-// At d <= 3 a score is three fused multiply-adds, so the kept blocks run on
-// the FP32 pipe (packed f32x2) with one ex2 per pair, like the dense FMA path;
-// a tensor-core tile would spend most of its K = 16 on padding.
+// At d <= 8 a score is at most eight fused multiply-adds, so the kept blocks
+// run on the FP32 pipe (packed f32x2) with one ex2 per pair, like the dense
+// FMA path; a tensor-core tile would spend most of its K = 16 on padding.
 #include "fs_debug.cuh"
 #include "fs_host.cuh"
 #include "fs_morton.cuh"
 
 #include <algorithm>
 #include <cmath>
+#include <type_traits>
 
 namespace fs {
 namespace {
@@ -41,7 +42,6 @@ namespace {
 constexpr int kSB = 128;            // points per block
 constexpr int kSuper = 16;          // blocks per super-block of the two-level cull
 constexpr int64_t kSuperMinBlocks = 32;   // input blocks from which the super-block cull runs
-constexpr int kMortonBits = 21;     // quantisation cells per axis: 2^21
 constexpr int kSortTile = 2048;     // keys per CTA in a radix pass
 constexpr int kSpMaxDim = kMortonMaxDim;
 
@@ -67,8 +67,12 @@ __global__ void k_box_init(unsigned int* box, int d) {
 
 __global__ void k_box(const float* __restrict__ X, int64_t n, const float* __restrict__ Y, int64_t m,
                       int d, unsigned int* __restrict__ box) {
-    unsigned int lo[kSpMaxDim] = {0xffffffffu, 0xffffffffu, 0xffffffffu};
-    unsigned int hi[kSpMaxDim] = {0u, 0u, 0u};
+    unsigned int lo[kSpMaxDim], hi[kSpMaxDim];
+#pragma unroll
+    for (int k = 0; k < kSpMaxDim; ++k) {
+        lo[k] = 0xffffffffu;
+        hi[k] = 0u;
+    }
     for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < n + m;
          p += (int64_t)gridDim.x * blockDim.x) {
         const float* src = p < n ? X + p * d : Y + (p - n) * d;
@@ -92,25 +96,27 @@ __global__ void k_box(const float* __restrict__ X, int64_t n, const float* __res
     }
 }
 
-// Morton code of each point: q_k = floor((p_k - lo_k) * (2^21 / (hi_k - lo_k)))
-// with every float32 operation rounded once (no contraction), clamped to
-// [0, 2^21 - 1]; bit b of q_k goes to bit b*d + k.  vals = the point index.
+// Morton code of each point: q_k = floor((p_k - lo_k) * (2^B / (hi_k - lo_k)))
+// (B = morton_bits(d)) with every float32 operation rounded once (no
+// contraction), clamped to [0, 2^B - 1]; bit b of q_k goes to bit b*d + k.
+// vals = the point index.
 __global__ void k_morton(const float* __restrict__ P, int64_t cnt, int d,
                          const unsigned int* __restrict__ box, uint64_t* __restrict__ keys,
                          int* __restrict__ vals) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= cnt) return;
-    constexpr unsigned int kMaxQ = (1u << kMortonBits) - 1u;
+    const int bits = morton_bits(d);
+    const unsigned int kMaxQ = (1u << bits) - 1u;
     uint64_t key = 0;
     for (int k = 0; k < d; ++k) {
         const float lo = ord2f(box[k]), hi = ord2f(box[d + k]);
         const float span = __fsub_rn(hi, lo);
-        const float scale = span > 0.f ? __fdiv_rn((float)(1u << kMortonBits), span) : 0.f;
+        const float scale = span > 0.f ? __fdiv_rn((float)(1u << bits), span) : 0.f;
         const float u = __fmul_rn(__fsub_rn(P[i * d + k], lo), scale);
         float fq = floorf(u);
         fq = fminf(fmaxf(fq, 0.f), (float)kMaxQ);
         const unsigned int q = (unsigned int)fq;
-        for (int b = 0; b < kMortonBits; ++b)
+        for (int b = 0; b < bits; ++b)
             key |= (uint64_t)((q >> b) & 1u) << (b * d + k);
     }
     keys[i] = key;
@@ -212,93 +218,146 @@ __global__ void __launch_bounds__(256) k_radix_scatter(const uint64_t* __restric
 // ---------------------------------------------------------------------------
 // sorted copies, records and block statistics
 
-// Sorted raw coordinates (float4, zero-padded), sorted weights, the FMA-path
-// record (centred point padded to D, bias slot at D, stride 4), |p~|^2 and
-// log2 w.  The bias slot is filled later from a potential.
+// Records.  The block-sparse path runs at geometry dimension DS = 3 (d <= 3),
+// 4 or 8 (d <= 8) and keeps its per-point and per-block records with a
+// stride RS of 4, 8 or 12 floats: the DS coordinates zero-padded, and one
+// extra value in the last slot (RS - 1): psi - max for the screening record,
+// the offset of the affine majorant, the radius or the log2 mass of a
+// super-block.  The FMA record of the kept-block half-update has the same
+// stride with its bias at index D (the FMA path's padded dimension).
+__host__ __device__ constexpr int sp_ds(int d) { return d <= 3 ? 3 : d <= 4 ? 4 : 8; }
+__host__ __device__ constexpr int sp_rs(int DS) { return DS <= 3 ? 4 : DS <= 4 ? 8 : 12; }
+
+template <int RS>
+__device__ __forceinline__ void ld_rec(const float* __restrict__ p, float (&v)[RS]) {
+#pragma unroll
+    for (int q = 0; q < RS / 4; ++q) {
+        const float4 t = reinterpret_cast<const float4*>(p)[q];
+        v[4 * q] = t.x;
+        v[4 * q + 1] = t.y;
+        v[4 * q + 2] = t.z;
+        v[4 * q + 3] = t.w;
+    }
+}
+template <int RS>
+__device__ __forceinline__ void st_rec(float* __restrict__ p, const float (&v)[RS]) {
+#pragma unroll
+    for (int q = 0; q < RS / 4; ++q)
+        reinterpret_cast<float4*>(p)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
+
+// Sorted raw coordinates (zero-padded, stride RS), sorted weights, the FMA
+// record (centred point, bias slot at D set later from a potential), |p~|^2
+// and log2 w.
+template <int DS>
 __global__ void k_sp_gather(const float* __restrict__ P, const float* __restrict__ w,
                             const int* __restrict__ perm, int64_t cnt, int d,
-                            const float* __restrict__ shift, float4* __restrict__ xs,
-                            float* __restrict__ ws, float4* __restrict__ rec,
+                            const float* __restrict__ shift, float* __restrict__ xs,
+                            float* __restrict__ ws, float* __restrict__ rec,
                             float* __restrict__ norm, float* __restrict__ logw2) {
+    constexpr int RS = sp_rs(DS);
     const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (k >= cnt) return;
     const int64_t p = perm[k];
     if (!FS_IDX_OK(p, cnt, 31)) return;
-    float v[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
+    float v[RS], c[RS];
+#pragma unroll
+    for (int q = 0; q < RS; ++q) v[q] = c[q] = 0.f;
     float nrm = 0.f;
-    for (int q = 0; q < d; ++q) {
+#pragma unroll
+    for (int q = 0; q < DS; ++q) {
+        if (q >= d) break;
         v[q] = P[p * d + q];
         c[q] = v[q] - shift[q];
         nrm = fmaf(c[q], c[q], nrm);
     }
     const float wk = w[p];
-    xs[k] = make_float4(v[0], v[1], v[2], 0.f);
+    st_rec<RS>(xs + k * RS, v);
     ws[k] = wk;
-    rec[k] = make_float4(c[0], c[1], c[2], 0.f);   // bias slot (index D = 2 or 3) set later
+    st_rec<RS>(rec + k * RS, c);
     norm[k] = nrm;
     logw2[k] = log2f(wk);
 }
 
 // One thread per block: weight and weighted sum in float64, in point order,
 // with no contraction; centroid = float(S / W), weight = float(W).
-__global__ void k_sp_block_stats(const float4* __restrict__ xs, const float* __restrict__ ws,
-                                 int64_t cnt, int d, int64_t nblk, float4* __restrict__ cen,
+template <int DS>
+__global__ void k_sp_block_stats(const float* __restrict__ xs, const float* __restrict__ ws,
+                                 int64_t cnt, int d, int64_t nblk, float* __restrict__ cen,
                                  float* __restrict__ cen_flat, float* __restrict__ W,
                                  float* __restrict__ lw2) {
+    constexpr int RS = sp_rs(DS);
     const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= nblk) return;
-    double sw = 0.0, s0 = 0.0, s1 = 0.0, s2 = 0.0;
+    double sw = 0.0, sk[DS];
+#pragma unroll
+    for (int q = 0; q < DS; ++q) sk[q] = 0.0;
     const int64_t e = min(cnt, (b + 1) * kSB);
     for (int64_t k = b * kSB; k < e; ++k) {
         const double wk = (double)ws[k];
-        const float4 x = xs[k];
+        float x[RS];
+        ld_rec<RS>(xs + k * RS, x);
         sw = __dadd_rn(sw, wk);
-        s0 = __dadd_rn(s0, __dmul_rn(wk, (double)x.x));
-        s1 = __dadd_rn(s1, __dmul_rn(wk, (double)x.y));
-        s2 = __dadd_rn(s2, __dmul_rn(wk, (double)x.z));
+#pragma unroll
+        for (int q = 0; q < DS; ++q) sk[q] = __dadd_rn(sk[q], __dmul_rn(wk, (double)x[q]));
     }
-    const float c0 = (float)__ddiv_rn(s0, sw);
-    const float c1 = d > 1 ? (float)__ddiv_rn(s1, sw) : 0.f;
-    const float c2 = d > 2 ? (float)__ddiv_rn(s2, sw) : 0.f;
-    cen[b] = make_float4(c0, c1, c2, 0.f);
-    cen_flat[b * d] = c0;
-    if (d > 1) cen_flat[b * d + 1] = c1;
-    if (d > 2) cen_flat[b * d + 2] = c2;
+    float c[RS];
+#pragma unroll
+    for (int q = 0; q < RS; ++q) c[q] = 0.f;
+#pragma unroll
+    for (int q = 0; q < DS; ++q) {
+        if (q >= d) break;
+        c[q] = (float)__ddiv_rn(sk[q], sw);
+        cen_flat[b * d + q] = c[q];
+    }
+    st_rec<RS>(cen + b * RS, c);
     W[b] = (float)sw;
     lw2[b] = log2f((float)sw);
 }
 
-// Offsets from the block centroid (xyz of the screening record) and the
-// block's per-axis extent max_i |u_ik|; one 128-thread block per point block.
-__global__ void __launch_bounds__(kSB) k_sp_offsets(const float4* __restrict__ xs, int64_t cnt,
-                                                    const float4* __restrict__ cen,
-                                                    float4* __restrict__ scr,
-                                                    float4* __restrict__ ext) {
-    __shared__ float4 red[kSB / 32];
+// Offsets from the block centroid (the screening record's coordinates) and
+// the block's per-axis extent max_i |u_ik|; one 128-thread block per point
+// block.
+template <int DS>
+__global__ void __launch_bounds__(kSB) k_sp_offsets(const float* __restrict__ xs, int64_t cnt,
+                                                    const float* __restrict__ cen,
+                                                    float* __restrict__ scr,
+                                                    float* __restrict__ ext) {
+    constexpr int RS = sp_rs(DS);
+    __shared__ float red[kSB / 32][DS];
     const int64_t k = (int64_t)blockIdx.x * kSB + threadIdx.x;
-    float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (k < cnt) {
-        const float4 x = xs[k], c = cen[blockIdx.x];
-        u = make_float4(x.x - c.x, x.y - c.y, x.z - c.z, 0.f);
-        scr[k] = u;
-    }
-    float e0 = fabsf(u.x), e1 = fabsf(u.y), e2 = fabsf(u.z);
+    float u[RS];
 #pragma unroll
-    for (int o = 16; o; o >>= 1) {
-        e0 = fmaxf(e0, __shfl_xor_sync(0xffffffffu, e0, o));
-        e1 = fmaxf(e1, __shfl_xor_sync(0xffffffffu, e1, o));
-        e2 = fmaxf(e2, __shfl_xor_sync(0xffffffffu, e2, o));
+    for (int q = 0; q < RS; ++q) u[q] = 0.f;
+    if (k < cnt) {
+        float x[RS], c[RS];
+        ld_rec<RS>(xs + k * RS, x);
+        ld_rec<RS>(cen + (int64_t)blockIdx.x * RS, c);
+#pragma unroll
+        for (int q = 0; q < DS; ++q) u[q] = x[q] - c[q];
+        st_rec<RS>(scr + k * RS, u);
     }
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = make_float4(e0, e1, e2, 0.f);
+    float e[DS];
+#pragma unroll
+    for (int q = 0; q < DS; ++q) {
+        e[q] = fabsf(u[q]);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) e[q] = fmaxf(e[q], __shfl_xor_sync(0xffffffffu, e[q], o));
+    }
+    if ((threadIdx.x & 31) == 0)
+#pragma unroll
+        for (int q = 0; q < DS; ++q) red[threadIdx.x >> 5][q] = e[q];
     __syncthreads();
     if (threadIdx.x == 0) {
-        float4 e = red[0];
-        for (int w = 1; w < kSB / 32; ++w) {
-            e.x = fmaxf(e.x, red[w].x);
-            e.y = fmaxf(e.y, red[w].y);
-            e.z = fmaxf(e.z, red[w].z);
+        float r[RS];
+#pragma unroll
+        for (int q = 0; q < RS; ++q) r[q] = 0.f;
+#pragma unroll
+        for (int q = 0; q < DS; ++q) {
+            r[q] = red[0][q];
+            for (int w = 1; w < kSB / 32; ++w) r[q] = fmaxf(r[q], red[w][q]);
         }
-        ext[blockIdx.x] = e;
+        st_rec<RS>(ext + (int64_t)blockIdx.x * RS, r);
     }
 }
 
@@ -329,29 +388,35 @@ __global__ void k_sp_perm64(const int* __restrict__ perm, int64_t cnt, int64_t* 
 
 // Record bias from a sorted potential: (pot - |p~|^2) L/eps + log2 w.
 __global__ void k_sp_bias(const float* __restrict__ pot_s, const float* __restrict__ norm,
-                          const float* __restrict__ logw2, int64_t cnt, int D, float l_over_eps,
-                          float* __restrict__ rec) {
+                          const float* __restrict__ logw2, int64_t cnt, int D, int RS,
+                          float l_over_eps, float* __restrict__ rec) {
     const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (k < cnt) rec[k * 4 + D] = (pot_s[k] - norm[k]) * l_over_eps + logw2[k];
+    if (k < cnt) rec[k * RS + D] = (pot_s[k] - norm[k]) * l_over_eps + logw2[k];
 }
 
 // psi_k = pot_k L/eps + log2 w_k for the screening: one 128-thread block per
-// point block stores psi - max into the record's w, the max per block,
-// a0 = log2 sum_k 2^{psi_k - max} (the block's bound at Delta = 0), and,
-// with g the least-squares slope of psi - max over the block's offsets u from
-// its centroid (a ridge keeps degenerate axes at zero slope; any g gives a
-// valid bound), lin = (g, log2 sum_k 2^{psi_k - max - g.u_k}): then
-// log2 sum_k 2^{psi_k - max + h.u_k} <= lin.w + sum_axes |g + h| e for any h.
+// point block stores psi - max into the record's last slot, the max per
+// block, a0 = log2 sum_k 2^{psi_k - max} (the block's bound at Delta = 0),
+// and, with g the least-squares slope of psi - max over the block's offsets
+// u from its centroid (a ridge keeps degenerate axes at zero slope; any g
+// gives a valid bound), lin = (g, log2 sum_k 2^{psi_k - max - g.u_k}) (the
+// offset in the last slot): then
+// log2 sum_k 2^{psi_k - max + h.u_k} <= lin.offset + sum_axes |g + h| e for any h.
+template <int DS>
 __global__ void __launch_bounds__(kSB) k_sp_psi(const float* __restrict__ pot_s,
                                                 const float* __restrict__ logw2, int64_t cnt,
-                                                float l_over_eps, float4* __restrict__ scr,
+                                                float l_over_eps, float* __restrict__ scr,
                                                 float* __restrict__ pmax, float* __restrict__ a0,
-                                                float4* __restrict__ lin) {
-    constexpr int NM = 14;   // moments: 1, u (3), p, u u^T (6), u p (3)
+                                                float* __restrict__ lin) {
+    constexpr int RS = sp_rs(DS);
+    // moments: 1, u (DS), p, u u^T (upper triangle, row by row), u p (DS)
+    constexpr int NUU = DS * (DS + 1) / 2;
+    constexpr int NM = 2 + 2 * DS + NUU;
+    constexpr int MP = 1 + DS, MUU = 2 + DS, MUP = 2 + DS + NUU;
     __shared__ float red[kSB / 32];
     __shared__ float red2[kSB / 32];
     __shared__ double mom[kSB / 32][NM];
-    __shared__ float s_fit[4];
+    __shared__ float s_fit[DS + 1];
     const int64_t k = (int64_t)blockIdx.x * kSB + threadIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const bool ok = k < cnt;
@@ -366,18 +431,30 @@ __global__ void __launch_bounds__(kSB) k_sp_psi(const float* __restrict__ pot_s,
 #pragma unroll
     for (int o = 16; o; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
     if (lane == 0) red2[warp] = e;
-    float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+    float u[RS];
+#pragma unroll
+    for (int q = 0; q < RS; ++q) u[q] = 0.f;
     const float ps = ok ? psi - mx : 0.f;
     if (ok) {
-        u = scr[k];
-        scr[k].w = ps;
+        ld_rec<RS>(scr + k * RS, u);
+        scr[k * RS + RS - 1] = ps;
     }
     // moments of the fit, in double
     double m[NM];
-    const double w1 = ok ? 1.0 : 0.0, x0 = u.x, x1 = u.y, x2 = u.z, pp = ps;
-    m[0] = w1; m[1] = x0; m[2] = x1; m[3] = x2; m[4] = pp;
-    m[5] = x0 * x0; m[6] = x0 * x1; m[7] = x0 * x2; m[8] = x1 * x1; m[9] = x1 * x2; m[10] = x2 * x2;
-    m[11] = x0 * pp; m[12] = x1 * pp; m[13] = x2 * pp;
+    const double w1 = ok ? 1.0 : 0.0, pp = ps;
+    m[0] = w1;
+#pragma unroll
+    for (int q = 0; q < DS; ++q) m[1 + q] = (double)u[q];
+    m[MP] = pp;
+    {
+        int t = MUU;
+#pragma unroll
+        for (int q = 0; q < DS; ++q)
+#pragma unroll
+            for (int r = q; r < DS; ++r) m[t++] = (double)u[q] * (double)u[r];
+    }
+#pragma unroll
+    for (int q = 0; q < DS; ++q) m[MUP + q] = (double)u[q] * pp;
 #pragma unroll
     for (int i = 0; i < NM; ++i) {
 #pragma unroll
@@ -392,38 +469,53 @@ __global__ void __launch_bounds__(kSB) k_sp_psi(const float* __restrict__ pot_s,
         double t[NM];
         for (int i = 0; i < NM; ++i) t[i] = ((mom[0][i] + mom[1][i]) + mom[2][i]) + mom[3][i];
         // normal equations of psi - max ~ alpha + g.u, with a small ridge on g
-        const double ridge = 1e-9 * (t[5] + t[8] + t[10]) + 1e-30;
-        double A[4][5] = {{t[0], t[1], t[2], t[3], t[4]},
-                          {t[1], t[5] + ridge, t[6], t[7], t[11]},
-                          {t[2], t[6], t[8] + ridge, t[9], t[12]},
-                          {t[3], t[7], t[9], t[10] + ridge, t[13]}};
-        for (int c = 0; c < 4; ++c) {   // Gaussian elimination, partial pivoting
+        auto uu = [&](int q, int r) {   // index of u_q u_r (q <= r) in the upper triangle
+            return MUU + q * DS - q * (q - 1) / 2 + (r - q);
+        };
+        double tr = 0.0;
+        for (int q = 0; q < DS; ++q) tr += t[uu(q, q)];
+        const double ridge = 1e-9 * tr + 1e-30;
+        double A[DS + 1][DS + 2];
+        A[0][0] = t[0];
+        for (int q = 0; q < DS; ++q) A[0][1 + q] = A[1 + q][0] = t[1 + q];
+        A[0][DS + 1] = t[MP];
+        for (int q = 0; q < DS; ++q) {
+            for (int r = 0; r < DS; ++r)
+                A[1 + q][1 + r] = t[q <= r ? uu(q, r) : uu(r, q)] + (q == r ? ridge : 0.0);
+            A[1 + q][DS + 1] = t[MUP + q];
+        }
+        for (int c = 0; c < DS + 1; ++c) {   // Gaussian elimination, partial pivoting
             int pv = c;
-            for (int r = c + 1; r < 4; ++r)
+            for (int r = c + 1; r < DS + 1; ++r)
                 if (fabs(A[r][c]) > fabs(A[pv][c])) pv = r;
             if (pv != c)
-                for (int q = 0; q < 5; ++q) {
+                for (int q = 0; q < DS + 2; ++q) {
                     const double tmp = A[c][q];
                     A[c][q] = A[pv][q];
                     A[pv][q] = tmp;
                 }
-            for (int r = c + 1; r < 4; ++r) {
+            for (int r = c + 1; r < DS + 1; ++r) {
                 const double f = A[r][c] / A[c][c];
-                for (int q = c; q < 5; ++q) A[r][q] -= f * A[c][q];
+                for (int q = c; q < DS + 2; ++q) A[r][q] -= f * A[c][q];
             }
         }
-        double sol[4];
-        for (int r = 3; r >= 0; --r) {
-            double v = A[r][4];
-            for (int q = r + 1; q < 4; ++q) v -= A[r][q] * sol[q];
+        double sol[DS + 1];
+        for (int r = DS; r >= 0; --r) {
+            double v = A[r][DS + 1];
+            for (int q = r + 1; q < DS + 1; ++q) v -= A[r][q] * sol[q];
             sol[r] = v / A[r][r];
         }
-        for (int i = 0; i < 4; ++i) s_fit[i] = isfinite(sol[i]) ? (float)sol[i] : 0.f;
+        for (int i = 0; i < DS + 1; ++i) s_fit[i] = isfinite(sol[i]) ? (float)sol[i] : 0.f;
     }
     __syncthreads();
-    const float g0 = s_fit[1], g1 = s_fit[2], g2 = s_fit[3];
+    float g[DS];
+#pragma unroll
+    for (int q = 0; q < DS; ++q) g[q] = s_fit[1 + q];
     // detrended block mass: log2 sum_k 2^{psi_k - max - g.u_k}
-    const float z = ok ? ps - (g0 * u.x + g1 * u.y + g2 * u.z) : -INFINITY;
+    float gu = 0.f;
+#pragma unroll
+    for (int q = 0; q < DS; ++q) gu = fmaf(g[q], u[q], gu);
+    const float z = ok ? ps - gu : -INFINITY;
     float zm = z;
 #pragma unroll
     for (int o = 16; o; o >>= 1) zm = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, o));
@@ -441,8 +533,13 @@ __global__ void __launch_bounds__(kSB) k_sp_psi(const float* __restrict__ pot_s,
         pmax[blockIdx.x] = mx;
         a0[blockIdx.x] = log2f(((red2[0] + red2[1]) + red2[2]) + red2[3]);
         // plus a 1/64 allowance for the float32 evaluation
-        const float lw = zm + log2f(((red3[0] + red3[1]) + red3[2]) + red3[3]) + 0.015625f;
-        lin[blockIdx.x] = make_float4(g0, g1, g2, lw);
+        float l[RS];
+#pragma unroll
+        for (int q = 0; q < RS; ++q) l[q] = 0.f;
+#pragma unroll
+        for (int q = 0; q < DS; ++q) l[q] = g[q];
+        l[RS - 1] = zm + log2f(((red3[0] + red3[1]) + red3[2]) + red3[3]) + 0.015625f;
+        st_rec<RS>(lin + (int64_t)blockIdx.x * RS, l);
     }
 }
 
@@ -450,18 +547,18 @@ __global__ void __launch_bounds__(kSB) k_sp_psi(const float* __restrict__ pot_s,
 // screening
 
 struct ScreenArgs {
-    const float4* so;        // output side: (u, psi - max) per sorted point
-    const float4* si;        // input side
+    const float* so;         // output side: (u, psi - max) per sorted point, stride RS
+    const float* si;         // input side
     const float* pmax_o;     // per-block max of psi (output side)
     const float* pmax_i;
-    const float4* cen_o;     // block centroids
-    const float4* cen_i;
-    const float4* ext_o;     // per-axis extents of the blocks around their centroids
-    const float4* ext_i;
+    const float* cen_o;      // block centroids (stride RS)
+    const float* cen_i;
+    const float* ext_o;      // per-axis extents of the blocks around their centroids (stride RS)
+    const float* ext_i;
     const float* a0_o;       // log2 sum 2^{psi - max} per block
     const float* a0_i;
-    const float4* lin_o;     // affine majorant of psi - max per block: (slope, offset + log2 count)
-    const float4* lin_i;
+    const float* lin_o;      // affine majorant of psi - max per block: (slope, offset + log2 count)
+    const float* lin_i;
     const float* lw2_o;      // log2 of the output blocks' weights
     int64_t cnt_o, cnt_i;
     int nbo, nbi;
@@ -507,21 +604,40 @@ __device__ __forceinline__ float half_lse8(const float (&z)[8]) {
 }
 
 // Exact bound U for input block J, by one half-warp (hl = lane % 16); own[]
-// holds the output block's points hl + 16 q, q < 8.
-__device__ __forceinline__ float bound_exact(const ScreenArgs& a, const float4 (&own)[8],
-                                             float4 co, float pmo, int J, int hl) {
-    const float4 ci = a.cen_i[J];
-    const float Dx = co.x - ci.x, Dy = co.y - ci.y, Dz = co.z - ci.z;
+// holds the output block's points hl + 16 q, q < 8 (records of stride RS).
+template <int DS>
+__device__ __forceinline__ float bound_exact(const ScreenArgs& a, const float (&own)[8][sp_rs(DS)],
+                                             const float (&co)[sp_rs(DS)], float pmo, int J, int hl) {
+    constexpr int RS = sp_rs(DS);
+    float ci[RS];
+    ld_rec<RS>(a.cen_i + (int64_t)J * RS, ci);
+    float Dl[DS];
+    float dd = 0.f;
+#pragma unroll
+    for (int k = 0; k < DS; ++k) {
+        Dl[k] = co[k] - ci[k];
+    }
     float za[8], zb[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-        za[q] = own[q].w - a.kappa * (Dx * own[q].x + Dy * own[q].y + Dz * own[q].z);
-        const int64_t k = (int64_t)J * kSB + hl + 16 * q;
-        float4 v = make_float4(0.f, 0.f, 0.f, -INFINITY);
-        if (k < a.cnt_i) v = a.si[k];
-        zb[q] = v.w + a.kappa * (Dx * v.x + Dy * v.y + Dz * v.z);
+        float da = 0.f;
+#pragma unroll
+        for (int k = 0; k < DS; ++k) da = fmaf(Dl[k], own[q][k], da);
+        za[q] = own[q][RS - 1] - a.kappa * da;
+        const int64_t kk = (int64_t)J * kSB + hl + 16 * q;
+        float v[RS];
+#pragma unroll
+        for (int t = 0; t < RS; ++t) v[t] = 0.f;
+        v[RS - 1] = -INFINITY;
+        if (kk < a.cnt_i) ld_rec<RS>(a.si + kk * RS, v);
+        float db = 0.f;
+#pragma unroll
+        for (int k = 0; k < DS; ++k) db = fmaf(Dl[k], v[k], db);
+        zb[q] = v[RS - 1] + a.kappa * db;
     }
-    const float dd = (Dx * Dx + Dy * Dy + Dz * Dz) * a.l_over_eps;
+#pragma unroll
+    for (int k = 0; k < DS; ++k) dd = fmaf(Dl[k], Dl[k], dd);
+    dd *= a.l_over_eps;
     return pmo + half_lse8(za) + a.pmax_i[J] + half_lse8(zb) - dd;
 }
 
@@ -533,21 +649,35 @@ __device__ __forceinline__ float bound_exact(const ScreenArgs& a, const float4 (
 //                                         (the same, after taking the slope g out)
 // The second keeps the potentials' slope inside a block, which cancels the
 // linear term for the blocks that exchange mass.
-__device__ __forceinline__ void bound_cheap(const ScreenArgs& a, float4 co, float4 eo, float4 lo,
+template <int DS>
+__device__ __forceinline__ void bound_cheap(const ScreenArgs& a, const float (&co)[sp_rs(DS)],
+                                            const float (&eo)[sp_rs(DS)], const float (&lo)[sp_rs(DS)],
                                             float pmo, float a0o, int J, float& ub, float& sig) {
-    const float4 ci = a.cen_i[J], ei = a.ext_i[J], li = a.lin_i[J];
-    const float Dx = co.x - ci.x, Dy = co.y - ci.y, Dz = co.z - ci.z;
-    const float dd = (Dx * Dx + Dy * Dy + Dz * Dz) * a.l_over_eps;
+    constexpr int RS = sp_rs(DS);
+    float ci[RS], ei[RS], li[RS];
+    ld_rec<RS>(a.cen_i + (int64_t)J * RS, ci);
+    ld_rec<RS>(a.ext_i + (int64_t)J * RS, ei);
+    ld_rec<RS>(a.lin_i + (int64_t)J * RS, li);
+    float dd = 0.f;
+    float kD[DS];
+#pragma unroll
+    for (int k = 0; k < DS; ++k) {
+        const float Dk = co[k] - ci[k];
+        dd = fmaf(Dk, Dk, dd);
+        kD[k] = a.kappa * Dk;
+    }
+    dd *= a.l_over_eps;
     const float pmi = a.pmax_i[J];
     sig = 0.0625f + 1.52587890625e-05f * (fabsf(pmo) + fabsf(pmi) + dd);
-    const float kx = a.kappa * Dx, ky = a.kappa * Dy, kz = a.kappa * Dz;
-    const float Ao = fminf(a0o + fabsf(kx) * eo.x + fabsf(ky) * eo.y + fabsf(kz) * eo.z,
-                           lo.w + fabsf(lo.x - kx) * eo.x + fabsf(lo.y - ky) * eo.y +
-                               fabsf(lo.z - kz) * eo.z);
-    const float Bi = fminf(a.a0_i[J] + fabsf(kx) * ei.x + fabsf(ky) * ei.y + fabsf(kz) * ei.z,
-                           li.w + fabsf(li.x + kx) * ei.x + fabsf(li.y + ky) * ei.y +
-                               fabsf(li.z + kz) * ei.z);
-    ub = pmo + Ao + pmi + Bi - dd;
+    float ao1 = a0o, ao2 = lo[RS - 1], bi1 = a.a0_i[J], bi2 = li[RS - 1];
+#pragma unroll
+    for (int k = 0; k < DS; ++k) {
+        ao1 += fabsf(kD[k]) * eo[k];
+        ao2 += fabsf(lo[k] - kD[k]) * eo[k];
+        bi1 += fabsf(kD[k]) * ei[k];
+        bi2 += fabsf(li[k] + kD[k]) * ei[k];
+    }
+    ub = pmo + fminf(ao1, ao2) + pmi + fminf(bi1, bi2) - dd;
 }
 
 // Margin (log2 units) by which the block-level bound must clear a test before
@@ -586,40 +716,50 @@ __device__ __forceinline__ int compact_offset(bool keep, int& base, int* s_wcnt)
 // output super-block's blocks by kCullMargin holds no block the block-level
 // cull would keep, so the kept lists are those of the one-level cull.
 
-// per super-block: (centroid box lo, R) and (box hi, M), max |max psi|, min
-// log2 block weight
-__global__ void k_sp_super_stats(const float4* __restrict__ cen, const float4* __restrict__ ext,
+// per super-block: (centroid box lo, R) and (box hi, M) as records of stride
+// RS (R and M in the last slot), max |max psi|, min log2 block weight
+template <int DS>
+__global__ void k_sp_super_stats(const float* __restrict__ cen, const float* __restrict__ ext,
                                  const float* __restrict__ pmax, const float* __restrict__ a0,
                                  const float* __restrict__ lW, int64_t nb, int64_t nsb,
-                                 float4* __restrict__ slo, float4* __restrict__ shi,
+                                 float* __restrict__ slo, float* __restrict__ shi,
                                  float* __restrict__ sp, float* __restrict__ slw) {
+    constexpr int RS = sp_rs(DS);
     const int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (s >= nsb) return;
-    float4 lo = make_float4(INFINITY, INFINITY, INFINITY, 0.f);
-    float4 hi = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    float lo[RS], hi[RS];
+#pragma unroll
+    for (int k = 0; k < RS; ++k) {
+        lo[k] = k < DS ? INFINITY : 0.f;
+        hi[k] = k < DS ? -INFINITY : 0.f;
+    }
+    hi[RS - 1] = -INFINITY;
     float pm = 0.f, lw = INFINITY;
     const int64_t b1 = min(nb, (s + 1) * kSuper);
     for (int64_t b = s * kSuper; b < b1; ++b) {
-        const float4 c = cen[b], e = ext[b];
-        lo.x = fminf(lo.x, c.x);
-        lo.y = fminf(lo.y, c.y);
-        lo.z = fminf(lo.z, c.z);
-        hi.x = fmaxf(hi.x, c.x);
-        hi.y = fmaxf(hi.y, c.y);
-        hi.z = fmaxf(hi.z, c.z);
-        lo.w = fmaxf(lo.w, sqrtf(e.x * e.x + e.y * e.y + e.z * e.z));
-        hi.w = fmaxf(hi.w, pmax[b] + a0[b]);
+        float c[RS], e[RS];
+        ld_rec<RS>(cen + b * RS, c);
+        ld_rec<RS>(ext + b * RS, e);
+        float r2 = 0.f;
+#pragma unroll
+        for (int k = 0; k < DS; ++k) {
+            lo[k] = fminf(lo[k], c[k]);
+            hi[k] = fmaxf(hi[k], c[k]);
+            r2 = fmaf(e[k], e[k], r2);
+        }
+        lo[RS - 1] = fmaxf(lo[RS - 1], sqrtf(r2));
+        hi[RS - 1] = fmaxf(hi[RS - 1], pmax[b] + a0[b]);
         pm = fmaxf(pm, fabsf(pmax[b]));
         lw = fminf(lw, lW[b]);
     }
-    slo[s] = lo;
-    shi[s] = hi;
+    st_rec<RS>(slo + s * RS, lo);
+    st_rec<RS>(shi + s * RS, hi);
     sp[s] = pm;
     slw[s] = lw;
 }
 
 struct SuperArgs {
-    const float4 *slo_o, *shi_o, *slo_i, *shi_i;
+    const float *slo_o, *shi_o, *slo_i, *shi_i;   // stride RS
     const float *sp_o, *sp_i, *slw_o;
     int64_t nsbo, nsbi;
     float l_over_eps;
@@ -633,11 +773,15 @@ struct SuperArgs {
 // One 256-thread block per output super-block: the input super-blocks whose
 // bound reaches the threshold, compacted in order, and the largest culled
 // bound.
+template <int DS>
 __global__ void __launch_bounds__(256) k_sp_super_screen(SuperArgs a) {
+    constexpr int RS = sp_rs(DS);
     __shared__ int s_wcnt[8];
     __shared__ float s_val[8];
     const int64_t so = blockIdx.x;
-    const float4 lo = a.slo_o[so], hi = a.shi_o[so];
+    float lo[RS], hi[RS];
+    ld_rec<RS>(a.slo_o + so * RS, lo);
+    ld_rec<RS>(a.shi_o + so * RS, hi);
     const float po = a.sp_o[so];
     const float T = a.log2_tau + a.slw_o[so] - a.log2_nbi;
     int* row = a.slist + so * a.nsbi;
@@ -647,19 +791,22 @@ __global__ void __launch_bounds__(256) k_sp_super_screen(SuperArgs a) {
         const int64_t si = c0 + threadIdx.x;
         bool surv = false;
         if (si < a.nsbi) {
-            const float4 li = a.slo_i[si], hii = a.shi_i[si];
-            const float gx = fmaxf(0.f, fmaxf(lo.x - hii.x, li.x - hi.x));
-            const float gy = fmaxf(0.f, fmaxf(lo.y - hii.y, li.y - hi.y));
-            const float gz = fmaxf(0.f, fmaxf(lo.z - hii.z, li.z - hi.z));
-            const float fx = fmaxf(fabsf(hi.x - li.x), fabsf(hii.x - lo.x));
-            const float fy = fmaxf(fabsf(hi.y - li.y), fabsf(hii.y - lo.y));
-            const float fz = fmaxf(fabsf(hi.z - li.z), fabsf(hii.z - lo.z));
-            const float D = sqrtf(gx * gx + gy * gy + gz * gz);
-            const float R = lo.w + li.w;
+            float li[RS], hii[RS];
+            ld_rec<RS>(a.slo_i + si * RS, li);
+            ld_rec<RS>(a.shi_i + si * RS, hii);
+            float g2 = 0.f, f2 = 0.f;
+#pragma unroll
+            for (int k = 0; k < DS; ++k) {
+                const float gk = fmaxf(0.f, fmaxf(lo[k] - hii[k], li[k] - hi[k]));
+                const float fk = fmaxf(fabsf(hi[k] - li[k]), fabsf(hii[k] - lo[k]));
+                g2 = fmaf(gk, gk, g2);
+                f2 = fmaf(fk, fk, f2);
+            }
+            const float D = sqrtf(g2);
+            const float R = lo[RS - 1] + li[RS - 1];
             const float H = D >= R ? (2.f * R - D) * D : R * R;
-            const float ub = hi.w + hii.w + a.l_over_eps * H;
-            const float sig = 0.0625f + 1.52587890625e-05f *
-                                            (po + a.sp_i[si] + (fx * fx + fy * fy + fz * fz) * a.l_over_eps);
+            const float ub = hi[RS - 1] + hii[RS - 1] + a.l_over_eps * H;
+            const float sig = 0.0625f + 1.52587890625e-05f * (po + a.sp_i[si] + f2 * a.l_over_eps);
             surv = !(ub + sig + kCullMargin < T);   // a NaN bound survives
             if (!surv) culled = fmaxf(culled, ub);
         }
@@ -690,7 +837,9 @@ __global__ void __launch_bounds__(256) k_sp_super_screen(SuperArgs a) {
 //   3. Otherwise every input block is evaluated exactly.
 // Both routes keep exactly {J : U_J + sigma_J >= T} plus the first
 // maximiser of U, so the result does not depend on the cull.
+template <int DS>
 __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
+    constexpr int RS = sp_rs(DS);
     __shared__ float s_val[8];
     __shared__ int s_idx[8];
     __shared__ int s_wcnt[8];
@@ -706,13 +855,19 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
     }
 
     const int hl = lane & 15, half = lane >> 4;
-    float4 own[8];
+    float own[8][RS];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
         const int64_t k = o0 + hl + 16 * q;
-        own[q] = k < a.cnt_o ? a.so[k] : make_float4(0.f, 0.f, 0.f, -INFINITY);
+#pragma unroll
+        for (int t = 0; t < RS; ++t) own[q][t] = 0.f;
+        own[q][RS - 1] = -INFINITY;
+        if (k < a.cnt_o) ld_rec<RS>(a.so + k * RS, own[q]);
     }
-    const float4 co = a.cen_o[O], eo = a.ext_o[O], lo = a.lin_o[O];
+    float co[RS], eo[RS], lo[RS];
+    ld_rec<RS>(a.cen_o + (int64_t)O * RS, co);
+    ld_rec<RS>(a.ext_o + (int64_t)O * RS, eo);
+    ld_rec<RS>(a.lin_o + (int64_t)O * RS, lo);
     const float pmo = a.pmax_o[O], a0o = a.a0_o[O];
     const float T = a.log2_tau + a.lw2_o[O] - log2f((float)a.nbi);
 
@@ -736,7 +891,7 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
         bool surv = false;
         if (k < ncand && J < a.nbi) {
             float ub, sig;
-            bound_cheap(a, co, eo, lo, pmo, a0o, J, ub, sig);
+            bound_cheap<DS>(a, co, eo, lo, pmo, a0o, J, ub, sig);
             surv = ub + sig + kCullMargin >= T;
             if (!surv) culled_ub = fmaxf(culled_ub, ub);
         }
@@ -760,7 +915,7 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
         for (int s0 = 2 * warp; s0 < S; s0 += 16) {
             const int sv = s0 + half;
             const int J = row[sv < S ? sv : s0];
-            const float u = bound_exact(a, own, co, pmo, J, hl);
+            const float u = bound_exact<DS>(a, own, co, pmo, J, hl);
             if (hl == 0 && sv < S && FS_IDX_OK(a.nbi - 1 - sv, a.nbi, 35))
                 row[a.nbi - 1 - sv] = __float_as_int(u);
         }
@@ -809,7 +964,7 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
                     J = row[sv];
                     const float u = __int_as_float(row[a.nbi - 1 - sv]);
                     float ub, sig;
-                    bound_cheap(a, co, eo, lo, pmo, a0o, J, ub, sig);
+                    bound_cheap<DS>(a, co, eo, lo, pmo, a0o, J, ub, sig);
                     keep = (u + sig >= T) || J == bi;
                 }
                 const int pos = compact_offset(keep, base, s_wcnt);
@@ -828,7 +983,7 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
     // 3. every input block, exactly, two per warp
     for (int J0 = 2 * warp; J0 < a.nbi; J0 += 16) {
         const int J = J0 + half;
-        const float u = bound_exact(a, own, co, pmo, J < a.nbi ? J : J0, hl);
+        const float u = bound_exact<DS>(a, own, co, pmo, J < a.nbi ? J : J0, hl);
         if (hl == 0 && J < a.nbi) row[J] = __float_as_int(u);
     }
     __syncthreads();
@@ -870,7 +1025,7 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
         if (J < a.nbi) {
             const float u = __int_as_float(row[J]);
             float ub, sig;
-            bound_cheap(a, co, eo, lo, pmo, a0o, J, ub, sig);
+            bound_cheap<DS>(a, co, eo, lo, pmo, a0o, J, ub, sig);
             keep = (u + sig >= T) || J == bi;
         }
         const int pos = compact_offset(keep, base, s_wcnt);
@@ -887,8 +1042,8 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
 // the block-sparse half-update
 
 struct SpHalfArgs {
-    float* rows;             // packed [nr x 4] records of the updated side (bias slot written)
-    const float* cols;       // packed [nc x 4] records of the other side
+    float* rows;             // packed [nr x RS] records of the updated side (bias slot D written)
+    const float* cols;       // packed [nc x RS] records of the other side
     int64_t nr, nc;
     int nbi;
     const int* lists;        // [nbo x nbi]
@@ -1049,11 +1204,22 @@ __device__ __forceinline__ void block_offset_fit(const float (&q)[4][D], const f
     if (isfinite(rmax)) mu += rmax - kSpFitTop;
 }
 
+// Staging geometry of the kept-block half-update at padded dimension D: a
+// column's D + 1 values (coordinates, bias) are staged duplicated, in sp_np(D)
+// float4, and a warp stages sp_cw(D) columns of an input block at a time.
+__host__ __device__ constexpr int sp_np(int D) { return (2 * (D + 1) + 3) / 4; }
+__host__ __device__ constexpr int sp_cw(int D) { return D <= 3 ? 128 : D <= 4 ? 64 : 32; }
+__host__ __device__ constexpr int sp_min_blocks(int D, bool ref) {
+    return D <= 3 ? (ref ? 4 : 3) : D <= 4 ? 3 : 2;
+}
+
 template <int D, bool REF>
-__global__ void __launch_bounds__(256, REF ? 4 : 3) k_sp_half(SpHalfArgs a) {
-    __shared__ float4 sc[kSpWarps][2 * kSB];
+__global__ void __launch_bounds__(256, sp_min_blocks(D, REF)) k_sp_half(SpHalfArgs a) {
+    constexpr int RS = fma_stride(D), NP = sp_np(D), CW = sp_cw(D);
+    static_assert(kSB % CW == 0 && CW % 32 == 0, "staging chunk");
+    __shared__ float4 sc[kSpWarps][CW * NP];
     __shared__ float2 part[kSpWarps][kSB];
-    __shared__ float4 sfit[kSpWarps];       // REF: the warp's column shift (h, mu)
+    __shared__ float sfit[kSpWarps][D + 1];   // REF: the warp's column shift (h, mu)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int O = a.order[blockIdx.x];
     const int64_t r0 = (int64_t)O * kSB;
@@ -1062,7 +1228,7 @@ __global__ void __launch_bounds__(256, REF ? 4 : 3) k_sp_half(SpHalfArgs a) {
     for (int p = 0; p < 2; ++p) {
         const int64_t ra = min(r0 + lane + 64 * p, a.nr - 1), rb = min(r0 + lane + 64 * p + 32, a.nr - 1);
 #pragma unroll
-        for (int k = 0; k < D; ++k) q[p][k] = pk(a.rows[ra * 4 + k] * a.kappa, a.rows[rb * 4 + k] * a.kappa);
+        for (int k = 0; k < D; ++k) q[p][k] = pk(a.rows[ra * RS + k] * a.kappa, a.rows[rb * RS + k] * a.kappa);
     }
     float M[4], Mt[4];
     uint64_t S[2], nm[2];
@@ -1081,9 +1247,9 @@ __global__ void __launch_bounds__(256, REF ? 4 : 3) k_sp_half(SpHalfArgs a) {
         for (int i = 0; i < 4; ++i) {
             valid[i] = r0 + lane + 32 * i < a.nr;
             const int64_t r = min(r0 + lane + 32 * i, a.nr - 1);
-            M[i] = a.rlogw2[r] - a.rows[r * 4 + D];
+            M[i] = a.rlogw2[r] - a.rows[r * RS + D];
 #pragma unroll
-            for (int k = 0; k < D; ++k) qi[i][k] = a.rows[r * 4 + k] * a.kappa;
+            for (int k = 0; k < D; ++k) qi[i][k] = a.rows[r * RS + k] * a.kappa;
         }
         block_offset_fit<D>(qi, M, valid, hc, mu);
 #pragma unroll
@@ -1094,18 +1260,15 @@ __global__ void __launch_bounds__(256, REF ? 4 : 3) k_sp_half(SpHalfArgs a) {
             M[i] = A;
         }
         if (lane == 0) {
-            float f[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int k = 0; k < D; ++k) f[k] = hc[k];
-            f[D] = mu;
-            sfit[warp] = make_float4(f[0], f[1], f[2], f[3]);
+            for (int k = 0; k < D; ++k) sfit[warp][k] = hc[k];
+            sfit[warp][D] = mu;
         }
         __syncwarp();
     }
 
     const int cnt = a.counts[O];
     const int* lst = a.lists + (int64_t)O * a.nbi;
-    const float4* cols4 = reinterpret_cast<const float4*>(a.cols);
     float4* my = sc[warp];
     int64_t cols_done = 0;
     for (int e = warp; e < cnt; e += kSpWarps) {
@@ -1114,98 +1277,105 @@ __global__ void __launch_bounds__(256, REF ? 4 : 3) k_sp_half(SpHalfArgs a) {
         const int64_t c0 = (int64_t)J * kSB;
         const int ncol = (int)min((int64_t)kSB, a.nc - c0);
         cols_done += ncol;
-        __syncwarp();
+        for (int cc = 0; cc < ncol; cc += CW) {
+            const int nch = min(CW, ncol - cc);
+            __syncwarp();
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const int j = lane + 32 * t;
-            if (j < ((ncol + 7) & ~7)) {
-                // past ncol (the rest of the last group): zero coordinates
-                // and a -inf bias, so those columns score -inf
-                float e[4] = {0.f, 0.f, 0.f, 0.f};
-                e[D] = -INFINITY;
-                if (j < ncol && FS_IDX_OK(c0 + j, a.nc, 39)) {
-                    const float4 v = cols4[c0 + j];
-                    e[0] = v.x;
-                    e[1] = v.y;
-                    e[2] = v.z;
-                    e[3] = v.w;
-                    if (REF) {
-                        const float4 sh = sfit[warp];
-                        e[0] -= sh.x;
-                        e[1] -= sh.y;
-                        e[2] -= sh.z;
-                        e[3] -= sh.w;   // the bias slot's shift is mu; a slot past it is unused
+            for (int t = 0; t < CW / 32; ++t) {
+                const int j = lane + 32 * t;
+                if (j < ((nch + 7) & ~7)) {
+                    // past nch (the rest of the last group): zero coordinates
+                    // and a -inf bias, so those columns score -inf
+                    float v[RS];
+#pragma unroll
+                    for (int k = 0; k < RS; ++k) v[k] = 0.f;
+                    v[D] = -INFINITY;
+                    if (j < nch && FS_IDX_OK(c0 + cc + j, a.nc, 39)) {
+                        ld_rec<RS>(a.cols + (c0 + cc + j) * RS, v);
+                        if (REF) {
+#pragma unroll
+                            for (int k = 0; k <= D; ++k) v[k] -= sfit[warp][k];
+                        }
                     }
-                }
-                my[2 * j] = make_float4(e[0], e[0], e[1], e[1]);
-                my[2 * j + 1] = make_float4(e[2], e[2], e[3], e[3]);
-            }
-        }
-        __syncwarp();
-        // every group of 8 is full: the staged tail past ncol scores -inf
-        for (int j = 0; j < ncol; j += 8) {
-            uint64_t s[2][8];
+                    float w[4 * NP];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int jj = j + u;
-                const float4 lo = my[2 * jj], hi = my[2 * jj + 1];
-                const uint64_t c[4] = {pk(lo.x, lo.y), pk(lo.z, lo.w), pk(hi.x, hi.y), pk(hi.z, hi.w)};
+                    for (int k = 0; k < 4 * NP; ++k) w[k] = k / 2 <= D ? v[k / 2] : 0.f;
 #pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    uint64_t acc = c[D];
-#pragma unroll
-                    for (int k = 0; k < D; ++k) acc = fma2(q[p][k], c[k], acc);
-                    s[p][u] = acc;
+                    for (int u = 0; u < NP; ++u)
+                        my[NP * j + u] = make_float4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
                 }
             }
-            if (!REF) {
-            // online max with a lazy, warp-uniform rescale
-            float m[4] = {Mt[0], Mt[1], Mt[2], Mt[3]};
-#pragma unroll
-            for (int p = 0; p < 2; ++p) {
-#pragma unroll
-                for (int u = 0; u < 8; u += 2) {
-                    float x0, x1, y0, y1;
-                    upk(s[p][u], x0, x1);
-                    upk(s[p][u + 1], y0, y1);
-                    m[2 * p] = max3(m[2 * p], x0, y0);
-                    m[2 * p + 1] = max3(m[2 * p + 1], x1, y1);
-                }
-            }
-            bool grow = false;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) grow |= m[i] > Mt[i];
-            if (__any_sync(0xffffffffu, grow)) {
-                float f[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float nM = m[i] > Mt[i] ? m[i] : M[i];
-                    f[i] = M[i] == -INFINITY ? 0.f : ex2(M[i] - nM);
-                    M[i] = nM;
-                    Mt[i] = nM + kSpSlack;
-                }
-#pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    S[p] = fma2(S[p], pk(f[2 * p], f[2 * p + 1]), pk(0.f, 0.f));
-                    nm[p] = pk(-M[2 * p], -M[2 * p + 1]);
-                }
-            }
-            }
-#pragma unroll
-            for (int p = 0; p < 2; ++p) {
-                uint64_t ev[8];
+            __syncwarp();
+            // every group of 8 is full: the staged tail past nch scores -inf
+            for (int j = 0; j < nch; j += 8) {
+                uint64_t s[2][8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    float x0, x1;
-                    upk(REF ? s[p][u] : add2(s[p][u], nm[p]), x0, x1);
-                    ev[u] = pk(ex2(x0), ex2(x1));
+                    const int jj = j + u;
+                    uint64_t c[D + 1];
+#pragma unroll
+                    for (int h = 0; h < NP; ++h) {
+                        const float4 t4 = my[NP * jj + h];
+                        if (2 * h <= D) c[2 * h] = pk(t4.x, t4.y);
+                        if (2 * h + 1 <= D) c[2 * h + 1] = pk(t4.z, t4.w);
+                    }
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+                        uint64_t acc = c[D];
+#pragma unroll
+                        for (int k = 0; k < D; ++k) acc = fma2(q[p][k], c[k], acc);
+                        s[p][u] = acc;
+                    }
+                }
+                if (!REF) {
+                    // online max with a lazy, warp-uniform rescale
+                    float m[4] = {Mt[0], Mt[1], Mt[2], Mt[3]};
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+#pragma unroll
+                        for (int u = 0; u < 8; u += 2) {
+                            float x0, x1, y0, y1;
+                            upk(s[p][u], x0, x1);
+                            upk(s[p][u + 1], y0, y1);
+                            m[2 * p] = max3(m[2 * p], x0, y0);
+                            m[2 * p + 1] = max3(m[2 * p + 1], x1, y1);
+                        }
+                    }
+                    bool grow = false;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) grow |= m[i] > Mt[i];
+                    if (__any_sync(0xffffffffu, grow)) {
+                        float f[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float nM = m[i] > Mt[i] ? m[i] : M[i];
+                            f[i] = M[i] == -INFINITY ? 0.f : ex2(M[i] - nM);
+                            M[i] = nM;
+                            Mt[i] = nM + kSpSlack;
+                        }
+#pragma unroll
+                        for (int p = 0; p < 2; ++p) {
+                            S[p] = fma2(S[p], pk(f[2 * p], f[2 * p + 1]), pk(0.f, 0.f));
+                            nm[p] = pk(-M[2 * p], -M[2 * p + 1]);
+                        }
+                    }
                 }
 #pragma unroll
-                for (int w = 1; w < 8; w *= 2) {
+                for (int p = 0; p < 2; ++p) {
+                    uint64_t ev[8];
 #pragma unroll
-                    for (int u = 0; u + w < 8; u += 2 * w) ev[u] = add2(ev[u], ev[u + w]);
+                    for (int u = 0; u < 8; ++u) {
+                        float x0, x1;
+                        upk(REF ? s[p][u] : add2(s[p][u], nm[p]), x0, x1);
+                        ev[u] = pk(ex2(x0), ex2(x1));
+                    }
+#pragma unroll
+                    for (int w = 1; w < 8; w *= 2) {
+#pragma unroll
+                        for (int u = 0; u + w < 8; u += 2 * w) ev[u] = add2(ev[u], ev[u + w]);
+                    }
+                    S[p] = add2(S[p], ev[0]);
                 }
-                S[p] = add2(S[p], ev[0]);
             }
         }
     }
@@ -1243,10 +1413,10 @@ __global__ void __launch_bounds__(256, REF ? 4 : 3) k_sp_half(SpHalfArgs a) {
             }
             const float lse2 = Mf + log2f(Sf);
             if (a.measure) {
-                a.rowsum[row] = exp2f(a.rows[row * 4 + D] + lse2);
+                a.rowsum[row] = exp2f(a.rows[row * RS + D] + lse2);
             } else {
                 a.pot[row] = a.rnorm[row] - a.eps_ln2 * lse2;
-                a.rows[row * 4 + D] = a.rlogw2[row] - lse2;
+                a.rows[row * RS + D] = a.rlogw2[row] - lse2;
             }
         }
     }
@@ -1263,6 +1433,7 @@ constexpr int kSpFixBlocks = 1216;   // 8 per SM on 152 SMs; idle blocks exit at
 
 template <int D>
 __global__ void __launch_bounds__(256) k_sp_fix(SpHalfArgs a) {
+    constexpr int RS = fma_stride(D);
     __shared__ unsigned int s_cnt;
     __shared__ float2 s_part[8];
     if (threadIdx.x == 0) s_cnt = min(*(volatile unsigned int*)&a.fix_count[0], (unsigned int)a.nr);
@@ -1275,7 +1446,7 @@ __global__ void __launch_bounds__(256) k_sp_fix(SpHalfArgs a) {
         const int64_t O = row / kSB;
         float q[D];
 #pragma unroll
-        for (int k = 0; k < D; ++k) q[k] = a.rows[row * 4 + k] * a.kappa;
+        for (int k = 0; k < D; ++k) q[k] = a.rows[row * RS + k] * a.kappa;
         float M = -INFINITY, S = 0.f;
         const int* lst = a.lists + O * a.nbi;
         const int64_t total = (int64_t)a.counts[O] * kSB;
@@ -1284,8 +1455,8 @@ __global__ void __launch_bounds__(256) k_sp_fix(SpHalfArgs a) {
             if (!FS_IDX_OK(J, a.nbi, 41)) continue;
             const int64_t col = (int64_t)J * kSB + idx % kSB;
             if (col >= a.nc) continue;
-            const float4 c = reinterpret_cast<const float4*>(a.cols)[col];
-            const float cv[4] = {c.x, c.y, c.z, c.w};
+            float cv[RS];
+            ld_rec<RS>(a.cols + col * RS, cv);
             float sc = cv[D];
 #pragma unroll
             for (int k = 0; k < D; ++k) sc = fmaf(q[k], cv[k], sc);
@@ -1309,7 +1480,7 @@ __global__ void __launch_bounds__(256) k_sp_fix(SpHalfArgs a) {
                 if (s_part[v].x != -INFINITY) lse_merge(Mf, Sf, s_part[v].x, s_part[v].y);
             const float lse2 = Mf + log2f(Sf);
             a.pot[row] = a.rnorm[row] - a.eps_ln2 * lse2;
-            a.rows[row * 4 + D] = a.rlogw2[row] - lse2;
+            a.rows[row * RS + D] = a.rlogw2[row] - lse2;
         }
         __syncthreads();
     }
@@ -1357,10 +1528,33 @@ __global__ void __launch_bounds__(1024) k_sp_order(const int* __restrict__ count
 
 inline unsigned grid_for(int64_t cnt, int threads) { return (unsigned)((cnt + threads - 1) / threads); }
 
+// Calls f with the padded dimension D (2, 3, 4 or 8) of the kept-block
+// half-update as a compile-time constant.
+template <class F>
+void with_pad_dim(int D, F&& f) {
+    switch (D) {
+    case 2: f(std::integral_constant<int, 2>{}); break;
+    case 3: f(std::integral_constant<int, 3>{}); break;
+    case 4: f(std::integral_constant<int, 4>{}); break;
+    default: f(std::integral_constant<int, 8>{}); break;
+    }
+}
+
+// Calls f with the geometry dimension DS of d as a compile-time constant.
+template <class F>
+void with_ds(int d, F&& f) {
+    switch (sp_ds(d)) {
+    case 3: f(std::integral_constant<int, 3>{}); break;
+    case 4: f(std::integral_constant<int, 4>{}); break;
+    default: f(std::integral_constant<int, 8>{}); break;
+    }
+}
+
 struct SpSide {
     size_t xs, ws, rec, norm, lw, pot, scr, pmax, a0, lin, ext, cen, cenf, W, lW, perm;
     size_t slo, shi, sp, slw;      // super-block statistics
     int64_t cnt, nb, nsb;
+    int d, rs;                     // dimension, record stride
 };
 
 struct SpBufs {
@@ -1377,26 +1571,29 @@ struct SpBufs {
 
 void layout_side(Layout& L, SpSide& s, int64_t cnt, int d) {
     s.cnt = cnt;
+    s.d = d;
+    s.rs = sp_rs(sp_ds(d));
+    const size_t rec = sizeof(float) * s.rs;   // one record
     s.nb = (cnt + kSB - 1) / kSB;
     s.perm = L.take(sizeof(int) * cnt);
-    s.xs = L.take(sizeof(float4) * cnt);
+    s.xs = L.take(rec * cnt);
     s.ws = L.take(sizeof(float) * cnt);
-    s.rec = L.take(sizeof(float4) * cnt);
+    s.rec = L.take(rec * cnt);
     s.norm = L.take(sizeof(float) * cnt);
     s.lw = L.take(sizeof(float) * cnt);
     s.pot = L.take(sizeof(float) * cnt);
-    s.scr = L.take(sizeof(float4) * cnt);
+    s.scr = L.take(rec * cnt);
     s.pmax = L.take(sizeof(float) * s.nb);
     s.a0 = L.take(sizeof(float) * s.nb);
-    s.lin = L.take(sizeof(float4) * s.nb);
-    s.ext = L.take(sizeof(float4) * s.nb);
-    s.cen = L.take(sizeof(float4) * s.nb);
+    s.lin = L.take(rec * s.nb);
+    s.ext = L.take(rec * s.nb);
+    s.cen = L.take(rec * s.nb);
     s.cenf = L.take(sizeof(float) * s.nb * d);
     s.W = L.take(sizeof(float) * s.nb);
     s.lW = L.take(sizeof(float) * s.nb);
     s.nsb = (s.nb + kSuper - 1) / kSuper;
-    s.slo = L.take(sizeof(float4) * s.nsb);
-    s.shi = L.take(sizeof(float4) * s.nsb);
+    s.slo = L.take(rec * s.nsb);
+    s.shi = L.take(rec * s.nsb);
     s.sp = L.take(sizeof(float) * s.nsb);
     s.slw = L.take(sizeof(float) * s.nsb);
 }
@@ -1452,7 +1649,7 @@ fs_status sort_side(Call& c, const MortonBufs& B, const float* P, int64_t cnt, i
     count_launch();
     FS_CUDA(cudaGetLastError());
     const int ntiles = (int)((cnt + kSortTile - 1) / kSortTile);
-    const int passes = (kMortonBits * d + 7) / 8;
+    const int passes = (morton_bits(d) * d + 7) / 8;
     for (int p = 0; p < passes; ++p) {
         const int shift = 8 * p;
         k_radix_count<<<ntiles, 256, 0, c.stream>>>(k0, cnt, shift, ntiles, hist);
@@ -1470,15 +1667,18 @@ fs_status sort_side(Call& c, const MortonBufs& B, const float* P, int64_t cnt, i
 // Sorted copies, records, block statistics and centroid offsets of one side.
 fs_status prepare_side(Call& c, const SpBufs& B, const SpSide& s, const float* P, const float* w,
                        int d) {
-    k_sp_gather<<<grid_for(s.cnt, 256), 256, 0, c.stream>>>(
-        P, w, c.at<int>(s.perm), s.cnt, d, c.at<float>(B.shift), c.at<float4>(s.xs),
-        c.at<float>(s.ws), c.at<float4>(s.rec), c.at<float>(s.norm), c.at<float>(s.lw));
-    k_sp_block_stats<<<grid_for(s.nb, 128), 128, 0, c.stream>>>(
-        c.at<float4>(s.xs), c.at<float>(s.ws), s.cnt, d, s.nb, c.at<float4>(s.cen),
-        c.at<float>(s.cenf), c.at<float>(s.W), c.at<float>(s.lW));
-    k_sp_offsets<<<(unsigned)s.nb, kSB, 0, c.stream>>>(c.at<float4>(s.xs), s.cnt,
-                                                       c.at<float4>(s.cen), c.at<float4>(s.scr),
-                                                       c.at<float4>(s.ext));
+    with_ds(d, [&](auto ds) {
+        constexpr int DS = decltype(ds)::value;
+        k_sp_gather<DS><<<grid_for(s.cnt, 256), 256, 0, c.stream>>>(
+            P, w, c.at<int>(s.perm), s.cnt, d, c.at<float>(B.shift), c.at<float>(s.xs),
+            c.at<float>(s.ws), c.at<float>(s.rec), c.at<float>(s.norm), c.at<float>(s.lw));
+        k_sp_block_stats<DS><<<grid_for(s.nb, 128), 128, 0, c.stream>>>(
+            c.at<float>(s.xs), c.at<float>(s.ws), s.cnt, d, s.nb, c.at<float>(s.cen),
+            c.at<float>(s.cenf), c.at<float>(s.W), c.at<float>(s.lW));
+        k_sp_offsets<DS><<<(unsigned)s.nb, kSB, 0, c.stream>>>(c.at<float>(s.xs), s.cnt,
+                                                               c.at<float>(s.cen), c.at<float>(s.scr),
+                                                               c.at<float>(s.ext));
+    });
     count_launch(3);
     FS_CUDA(cudaGetLastError());
     return FS_OK;
@@ -1496,10 +1696,13 @@ fs_status prepare_sparse(Call& c, const SpBufs& B, const float* X, const float* 
 }
 
 fs_status refresh_psi(Call& c, const SpSide& s, float l_over_eps) {
-    k_sp_psi<<<(unsigned)s.nb, kSB, 0, c.stream>>>(c.at<float>(s.pot), c.at<float>(s.lw), s.cnt,
-                                                   l_over_eps, c.at<float4>(s.scr),
-                                                   c.at<float>(s.pmax), c.at<float>(s.a0),
-                                                   c.at<float4>(s.lin));
+    with_ds(s.d, [&](auto ds) {
+        constexpr int DS = decltype(ds)::value;
+        k_sp_psi<DS><<<(unsigned)s.nb, kSB, 0, c.stream>>>(c.at<float>(s.pot), c.at<float>(s.lw),
+                                                           s.cnt, l_over_eps, c.at<float>(s.scr),
+                                                           c.at<float>(s.pmax), c.at<float>(s.a0),
+                                                           c.at<float>(s.lin));
+    });
     count_launch();
     FS_CUDA(cudaGetLastError());
     return FS_OK;
@@ -1507,8 +1710,8 @@ fs_status refresh_psi(Call& c, const SpSide& s, float l_over_eps) {
 
 fs_status set_bias(Call& c, const SpSide& s, int D, float l_over_eps) {
     k_sp_bias<<<grid_for(s.cnt, 256), 256, 0, c.stream>>>(c.at<float>(s.pot), c.at<float>(s.norm),
-                                                          c.at<float>(s.lw), s.cnt, D, l_over_eps,
-                                                          c.at<float>(s.rec));
+                                                          c.at<float>(s.lw), s.cnt, D, s.rs,
+                                                          l_over_eps, c.at<float>(s.rec));
     count_launch();
     FS_CUDA(cudaGetLastError());
     return FS_OK;
@@ -1516,18 +1719,18 @@ fs_status set_bias(Call& c, const SpSide& s, int D, float l_over_eps) {
 
 fs_status screen(Call& c, const SpBufs& B, const SpSide& o, const SpSide& in, float eps, float tau) {
     ScreenArgs s;
-    s.so = c.at<float4>(o.scr);
-    s.si = c.at<float4>(in.scr);
+    s.so = c.at<float>(o.scr);
+    s.si = c.at<float>(in.scr);
     s.pmax_o = c.at<float>(o.pmax);
     s.pmax_i = c.at<float>(in.pmax);
-    s.cen_o = c.at<float4>(o.cen);
-    s.cen_i = c.at<float4>(in.cen);
-    s.ext_o = c.at<float4>(o.ext);
-    s.ext_i = c.at<float4>(in.ext);
+    s.cen_o = c.at<float>(o.cen);
+    s.cen_i = c.at<float>(in.cen);
+    s.ext_o = c.at<float>(o.ext);
+    s.ext_i = c.at<float>(in.ext);
     s.a0_o = c.at<float>(o.a0);
     s.a0_i = c.at<float>(in.a0);
-    s.lin_o = c.at<float4>(o.lin);
-    s.lin_i = c.at<float4>(in.lin);
+    s.lin_o = c.at<float>(o.lin);
+    s.lin_i = c.at<float>(in.lin);
     s.lw2_o = c.at<float>(o.lW);
     s.cnt_o = o.cnt;
     s.cnt_i = in.cnt;
@@ -1548,15 +1751,18 @@ fs_status screen(Call& c, const SpBufs& B, const SpSide& o, const SpSide& in, fl
         // two-level cull: super-block statistics of both sides (the masses change
         // with every potential), then the super pairs
         for (const SpSide* sd : {&o, &in})
-            k_sp_super_stats<<<grid_for(sd->nsb, 128), 128, 0, c.stream>>>(
-                c.at<float4>(sd->cen), c.at<float4>(sd->ext), c.at<float>(sd->pmax),
-                c.at<float>(sd->a0), c.at<float>(sd->lW), sd->nb, sd->nsb, c.at<float4>(sd->slo),
-                c.at<float4>(sd->shi), c.at<float>(sd->sp), c.at<float>(sd->slw));
+            with_ds(o.d, [&](auto ds) {
+                constexpr int DS = decltype(ds)::value;
+                k_sp_super_stats<DS><<<grid_for(sd->nsb, 128), 128, 0, c.stream>>>(
+                    c.at<float>(sd->cen), c.at<float>(sd->ext), c.at<float>(sd->pmax),
+                    c.at<float>(sd->a0), c.at<float>(sd->lW), sd->nb, sd->nsb, c.at<float>(sd->slo),
+                    c.at<float>(sd->shi), c.at<float>(sd->sp), c.at<float>(sd->slw));
+            });
         SuperArgs sa;
-        sa.slo_o = c.at<float4>(o.slo);
-        sa.shi_o = c.at<float4>(o.shi);
-        sa.slo_i = c.at<float4>(in.slo);
-        sa.shi_i = c.at<float4>(in.shi);
+        sa.slo_o = c.at<float>(o.slo);
+        sa.shi_o = c.at<float>(o.shi);
+        sa.slo_i = c.at<float>(in.slo);
+        sa.shi_i = c.at<float>(in.shi);
         sa.sp_o = c.at<float>(o.sp);
         sa.sp_i = c.at<float>(in.sp);
         sa.slw_o = c.at<float>(o.slw);
@@ -1568,14 +1774,18 @@ fs_status screen(Call& c, const SpBufs& B, const SpSide& o, const SpSide& in, fl
         sa.slist = c.at<int>(B.slist);
         sa.scount = c.at<int>(B.scount);
         sa.sculled = c.at<float>(B.sculled);
-        k_sp_super_screen<<<(unsigned)o.nsb, 256, 0, c.stream>>>(sa);
+        with_ds(o.d, [&](auto ds) {
+            k_sp_super_screen<decltype(ds)::value><<<(unsigned)o.nsb, 256, 0, c.stream>>>(sa);
+        });
         count_launch(3);
         FS_CUDA(cudaGetLastError());
         s.slist = sa.slist;
         s.scount = sa.scount;
         s.sculled = sa.sculled;
     }
-    k_sp_screen<<<(unsigned)o.nb, 256, 0, c.stream>>>(s);
+    with_ds(o.d, [&](auto ds) {
+        k_sp_screen<decltype(ds)::value><<<(unsigned)o.nb, 256, 0, c.stream>>>(s);
+    });
     count_launch();
     FS_CUDA(cudaGetLastError());
     return FS_OK;
@@ -1610,19 +1820,18 @@ fs_status sparse_half(Call& c, const SpBufs& B, const SpSide& o, const SpSide& i
     NvtxRange nvtx(measure ? "fs residual pass (block-sparse)"
                          : o.rec == B.X.rec ? "fs f-update (block-sparse)" : "fs g-update (block-sparse)");
     const int ts = measure ? -1 : timing_begin(c.stream);
-    if (D == 2) {
-        if (ref) k_sp_half<2, true><<<(unsigned)o.nb, 256, 0, c.stream>>>(h);
-        else k_sp_half<2, false><<<(unsigned)o.nb, 256, 0, c.stream>>>(h);
-    } else {
-        if (ref) k_sp_half<3, true><<<(unsigned)o.nb, 256, 0, c.stream>>>(h);
-        else k_sp_half<3, false><<<(unsigned)o.nb, 256, 0, c.stream>>>(h);
-    }
+    with_pad_dim(D, [&](auto dd) {
+        constexpr int DD = decltype(dd)::value;
+        if (ref) k_sp_half<DD, true><<<(unsigned)o.nb, 256, 0, c.stream>>>(h);
+        else k_sp_half<DD, false><<<(unsigned)o.nb, 256, 0, c.stream>>>(h);
+    });
     timing_end(ts, TIME_HALF, c.stream);
     count_launch();
     FS_CUDA(cudaGetLastError());
     if (ref) {
-        if (D == 2) k_sp_fix<2><<<kSpFixBlocks, 256, 0, c.stream>>>(h);
-        else k_sp_fix<3><<<kSpFixBlocks, 256, 0, c.stream>>>(h);
+        with_pad_dim(D, [&](auto dd) {
+            k_sp_fix<decltype(dd)::value><<<kSpFixBlocks, 256, 0, c.stream>>>(h);
+        });
         count_launch();
         FS_CUDA(cudaGetLastError());
     }

@@ -19,7 +19,8 @@ import pytest
 import oracle as orc
 import oracle.block_sparse as bsp
 from streaming_sinkhorn_solver_gb300 import binding as fs
-from streaming_sinkhorn_solver_gb300.workloads import WORKLOADS, make_inputs, random_cloud
+from streaming_sinkhorn_solver_gb300.workloads import (WORKLOADS, clustered_cloud, make_inputs,
+                                                       random_cloud)
 from tests.gpu_util import F_TOL_FMA, max_abs, np64, to_dev
 
 pytestmark = pytest.mark.gpu
@@ -42,7 +43,9 @@ def _lattice(n, d, seed):
 
 
 @pytest.mark.parametrize("n,m,d", [(1, 1, 1), (5, 300, 2), (1000, 777, 3), (5000, 4100, 3),
-                                   (4099, 2048, 1), (3000, 3001, 2)])
+                                   (4099, 2048, 1), (3000, 3001, 2),
+                                   # above d = 3: floor(63 / d) bits per axis
+                                   (1000, 900, 4), (3000, 2000, 5), (7, 1, 6), (2000, 2100, 8)])
 def test_morton_order_bit_exact(n, m, d):
     c = random_cloud(n, m, d, seed=n + m + d)
     t = to_dev(c)
@@ -52,7 +55,7 @@ def test_morton_order_bit_exact(n, m, d):
     np.testing.assert_array_equal(py.cpu().numpy(), oy)
 
 
-@pytest.mark.parametrize("d", [1, 2, 3])
+@pytest.mark.parametrize("d", [1, 2, 3, 4, 8])
 def test_morton_order_with_ties_bit_exact(d):
     X, Y = _lattice(3000, d, 1), _lattice(2100, d, 2)
     import torch
@@ -63,7 +66,11 @@ def test_morton_order_with_ties_bit_exact(d):
 
 
 def _screen_case(name, n, m, d, eps, dense_iters):
-    inp = make_inputs(name, n=n, m=m, d=d)
+    if name == "clustered":
+        # 12 clusters of standard deviation 0.03 in [0, 1]^d
+        inp = clustered_cloud(n, m, d, 12, 0.03, seed=n + d)
+    else:
+        inp = make_inputs(name, n=n, m=m, d=d)
     if n * m > 5e7:
         # one iteration from g = 0, row by row (no n x m cost matrix)
         f = orc.f_update_rows(inp["X"], inp["Y"], inp["b"], eps, np.zeros(m), np.arange(n))
@@ -84,6 +91,14 @@ def _screen_case(name, n, m, d, eps, dense_iters):
     ("c2_n10k_d3", 20000, 18000, 3, 0.002, 1e-6, 0),
     ("c2_n10k_d3", 20000, 18000, 3, 0.002, 1e-6, 1),
     ("c2_n10k_d3", 16000, 17000, 2, 0.0005, 1e-5, 0),
+    # d = 4..8: records of 8 and 12 floats; clustered clouds, so that whole
+    # cluster pairs are skipped
+    ("clustered", 3000, 2600, 4, 0.003, 1e-4, 0),
+    ("clustered", 3000, 2500, 5, 0.003, 1e-4, 1),
+    ("clustered", 3000, 2600, 8, 0.003, 1e-5, 0),
+    ("clustered", 2900, 2700, 7, 0.002, 1e-6, 1),
+    # 36 x 32 blocks at d = 8: the two-level cull runs
+    ("clustered", 4600, 4100, 8, 0.002, 1e-6, 0),
 ])
 def test_screening_decisions_match_oracle(name, n, m, d, eps, tau, side):
     inp, f32, g32 = _screen_case(name, n, m, d, eps, 6)
@@ -118,7 +133,8 @@ def test_screening_decisions_match_oracle(name, n, m, d, eps, tau, side):
 
 
 @pytest.mark.parametrize("n,m,d", [(1, 1, 1), (7, 300, 2), (130, 129, 3), (1000, 1300, 3),
-                                   (2049, 700, 1)])
+                                   (2049, 700, 1), (1000, 1300, 4), (700, 900, 5), (129, 130, 6),
+                                   (300, 257, 7), (513, 1100, 8)])
 def test_without_screening_equals_dense_oracle(n, m, d):
     inp = random_cloud(n, m, d, seed=50 + n, weights="lognormal")
     t = to_dev(inp)
@@ -190,6 +206,52 @@ def test_reference_offsets_with_fixups_match_oracle(online_iters, eps):
     if online_iters == 0:
         # settled offsets: a fixup is the exception
         assert rep["fixed_rows"] <= 0.01 * rep["passes"] * 2000
+
+
+@pytest.mark.parametrize("n,m,d,eps,tau", [(2000, 1900, 4, 0.002, 1e-6), (2200, 2000, 5, 0.003, 1e-5),
+                                           (2600, 2300, 8, 0.003, 1e-5)])
+def test_screened_solve_above_three_dimensions_matches_oracle(n, m, d, eps, tau):
+    """d = 4..8 (records of 8 and 12 floats, the kept blocks staged in 64- and
+    32-column chunks) on clustered clouds: the coarse stage, the screenings
+    and the reference-offset updates after two online iterations."""
+    inp = clustered_cloud(n, m, d, 12 if d > 4 else 10, 0.03 if d > 4 else 0.04, seed=400 + d)
+    t = to_dev(inp)
+    f, g, rep = fs.fs_sparse_solve(t["X"], t["a"], t["Y"], t["b"], eps, coarse_iters=20,
+                                   max_iters=25, tau=tau)
+    fr, gr, orep = bsp.solve(inp["X"], inp["a"], inp["Y"], inp["b"], eps, 20, 25, tau)
+    C = orc.cost(inp["X"], inp["Y"])
+    tol = F_TOL_FMA * C.max()
+    assert max_abs(np64(f), fr) <= tol
+    assert max_abs(np64(g), gr) <= tol
+    per_gpu = rep["kept_pairs"] / rep["passes"]
+    per_orc = orep["kept_pairs"] / orep["halves"]
+    assert abs(per_gpu / per_orc - 1.0) < 0.02
+    assert per_gpu < 0.9 * n * m
+    assert rep["residual"] == pytest.approx(orep["residual"], rel=1e-2, abs=1e-5)
+
+
+@pytest.mark.parametrize("d,eps", [(8, 0.003), (8, 0.00004), (5, 0.00004)])
+def test_reference_offsets_above_three_dimensions_match_oracle(d, eps):
+    """Reference offsets from the first update (online_iters = -1) at d = 5
+    and 8: the block's affine fit of the previous LSEs has 5 or 8 slopes.  At
+    eps = 4e-5 the cold-start gap passes 200 log2 units (checked on the
+    oracle), so rows go through the fixup at D = 8."""
+    inp = clustered_cloud(2000, 1800, d, 12, 0.03, seed=500 + d)
+    tau = 1e-6
+    if eps < 0.001:
+        f1, _, _ = bsp.solve(inp["X"], inp["a"], inp["Y"], inp["b"], eps, 0, 1, tau)
+        gap = -f1 / (orc.as_eps(eps) * np.log(2.0))
+        assert gap.min() < -200
+    t = to_dev(inp)
+    f, g, rep = fs.fs_sparse_solve(t["X"], t["a"], t["Y"], t["b"], eps, coarse_iters=0,
+                                   max_iters=8, tau=tau, online_iters=-1)
+    fr, gr, _ = bsp.solve(inp["X"], inp["a"], inp["Y"], inp["b"], eps, 0, 8, tau)
+    C = orc.cost(inp["X"], inp["Y"])
+    tol = F_TOL_FMA * C.max()
+    assert max_abs(np64(f), fr) <= tol
+    assert max_abs(np64(g), gr) <= tol
+    if eps < 0.001:
+        assert rep["fixed_rows"] > 0
 
 
 def test_screened_solve_with_lognormal_weights_matches_oracle():
@@ -285,7 +347,7 @@ def test_warm_start_continues_the_iteration():
 
 
 def test_invalid_arguments_are_rejected():
-    inp = to_dev(random_cloud(10, 10, 4, seed=1))
+    inp = to_dev(random_cloud(10, 10, 9, seed=1))
     with pytest.raises(fs.FlashSinkhornError) as e:
         fs.fs_sparse_solve(inp["X"], inp["a"], inp["Y"], inp["b"], 0.1)
     assert e.value.status == fs.FS_ERR_UNSUPPORTED
