@@ -426,11 +426,18 @@ typedef struct fs_sparse_report {
  * receives the iteration count, the final residual (one more measurement
  * pass) and the work done.  The call synchronises `stream` at every residual
  * test and at the end, and cannot be captured in a CUDA graph.
- * Workspace: O((n + m) + (n/128)(m/128)) -- the kept-block lists hold one int
- * per block pair; more than 2^30 block pairs is FS_ERR_UNSUPPORTED.
- * Errors: FS_ERR_UNSUPPORTED for d > 8; FS_ERR_INVALID_ARG for null pointers,
- * sizes < 1, eps <= 0, tau outside [0, 1), negative counts or target, or
- * non-zero reserved fields.
+ * Memory: O(n + m) per point, one int per pair of super-blocks (16 blocks
+ * of 128 points; at most 2^32 pairs, about 1.3e8 points per side), and the
+ * kept lists: a row per output block with room for twice the blocks of the
+ * input super-blocks its super-block keeps.  Up to 2^30 block pairs the
+ * lists live in the workspace (one int per block pair at most); above, in a
+ * device buffer the call allocates, sizes at every screening (one more
+ * synchronisation of `stream` each) and frees before it returns.
+ * Errors: FS_ERR_UNSUPPORTED for d > 8, more than 2^32 super-block pairs,
+ * or tau = 0 (every block kept) above 2^30 block pairs; FS_ERR_OOM when the
+ * kept lists do not fit; FS_ERR_INVALID_ARG for null pointers, sizes < 1,
+ * eps <= 0, tau outside [0, 1), negative counts or target, or non-zero
+ * reserved fields.
  */
 fs_status fs_sparse_solve(const float* X, const float* a, int64_t n,
                           const float* Y, const float* b, int64_t m, int32_t d, float eps,

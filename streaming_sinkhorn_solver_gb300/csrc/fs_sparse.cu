@@ -44,6 +44,13 @@ constexpr int kSuper = 16;          // blocks per super-block of the two-level c
 constexpr int64_t kSuperMinBlocks = 32;   // input blocks from which the super-block cull runs
 constexpr int kSortTile = 2048;     // keys per CTA in a radix pass
 constexpr int kSpMaxDim = kMortonMaxDim;
+// kept-list entries the workspace holds as one row of nbi per output block
+constexpr int64_t kRoomyListEntries = (int64_t)1 << 30;
+// super-block pairs of the two-level cull (one int each)
+constexpr int64_t kMaxSuperEntries = (int64_t)1 << 32;
+// device counters of a solve: block pairs, score pairs, exact bounds, rows
+// fixed up, kept-list overflows
+constexpr int kWorkCounters = 5;
 
 // ---------------------------------------------------------------------------
 // joint bounding box (order-preserving integer encoding of floats, so that
@@ -565,9 +572,15 @@ struct ScreenArgs {
     float kappa;             // 2 L / eps
     float l_over_eps;        // L / eps
     float log2_tau;          // -inf: keep every block
-    int* lists;              // [nbo x nbi]
+    // kept lists: output block o's row is lists[row_off[o] .. row_off[o + 1]);
+    // a row of nbi entries ("roomy") doubles as scratch for every block's
+    // bound, a shorter one (capacity 2 x candidates + 1 under the super-block
+    // cull) for the survivors' bounds only
+    int* lists;
+    const int64_t* row_off;  // [nbo + 1]
     int* counts;             // [nbo]
     unsigned long long* exact;  // accumulated: block pairs given the per-point bound
+    unsigned long long* overflow;   // accumulated: kept entries that found no room (never)
     // super-block cull (nullptr: every input block is a candidate): per output
     // super-block, the surviving input super-blocks in order, their count, and
     // the largest bound among the culled ones
@@ -698,6 +711,34 @@ __device__ __forceinline__ int compact_offset(bool keep, int& base, int* s_wcnt)
     }
     base += tot;
     return off + __popc(bal & ((1u << lane) - 1u));
+}
+
+// First maximiser: the larger value, the smaller index on ties.
+__device__ __forceinline__ void arg_update(float& best, int& bi, float u, int J) {
+    if (u > best || (u == best && J < bi)) {
+        best = u;
+        bi = J;
+    }
+}
+
+// CTA-wide first maximiser of the threads' (best, bi); every thread gets it.
+__device__ __forceinline__ void block_argmax(float& best, int& bi, float* s_val, int* s_idx) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        arg_update(best, bi, ob, oi);
+    }
+    if (lane == 0) {
+        s_val[warp] = best;
+        s_idx[warp] = bi;
+    }
+    __syncthreads();
+    best = s_val[0];
+    bi = s_idx[0];
+    for (int w = 1; w < 8; ++w) arg_update(best, bi, s_val[w], s_idx[w]);
+    __syncthreads();
 }
 
 // ---------------------------------------------------------------------------
@@ -837,25 +878,14 @@ __global__ void __launch_bounds__(256) k_sp_super_screen(SuperArgs a) {
 //   3. Otherwise every input block is evaluated exactly.
 // Both routes keep exactly {J : U_J + sigma_J >= T} plus the first
 // maximiser of U, so the result does not depend on the cull.
+// The output block's screening records: its points hl + 16 q (q < 8) for a
+// half-warp lane hl, and its centroid, extents and affine majorant.
 template <int DS>
-__global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
+__device__ __forceinline__ void load_out_block(const ScreenArgs& a, int O, int hl,
+                                               float (&own)[8][sp_rs(DS)], float (&co)[sp_rs(DS)],
+                                               float (&eo)[sp_rs(DS)], float (&lo)[sp_rs(DS)]) {
     constexpr int RS = sp_rs(DS);
-    __shared__ float s_val[8];
-    __shared__ int s_idx[8];
-    __shared__ int s_wcnt[8];
-    const int O = blockIdx.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int* row = a.lists + (int64_t)O * a.nbi;
     const int64_t o0 = (int64_t)O * kSB;
-
-    if (a.log2_tau == -INFINITY) {
-        for (int J = threadIdx.x; J < a.nbi; J += blockDim.x) row[J] = J;
-        if (threadIdx.x == 0) a.counts[O] = a.nbi;
-        return;
-    }
-
-    const int hl = lane & 15, half = lane >> 4;
-    float own[8][RS];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
         const int64_t k = o0 + hl + 16 * q;
@@ -864,10 +894,86 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
         own[q][RS - 1] = -INFINITY;
         if (k < a.cnt_o) ld_rec<RS>(a.so + k * RS, own[q]);
     }
-    float co[RS], eo[RS], lo[RS];
     ld_rec<RS>(a.cen_o + (int64_t)O * RS, co);
     ld_rec<RS>(a.ext_o + (int64_t)O * RS, eo);
     ld_rec<RS>(a.lin_o + (int64_t)O * RS, lo);
+}
+
+struct ArgMax {
+    float best;
+    int bi;
+    int evaluated;   // exact bounds computed
+};
+
+// The first maximiser of U when a culled block could still reach the best
+// survivor (best, bi) and the row has no room for every block's bound:
+// evaluate exactly the culled blocks whose block-level bound reaches the
+// best so far -- among the candidates (the blocks of the surviving
+// super-blocks sl[0 .. ncand / 16)), or among all blocks -- 256 at a time.
+// It reloads the output block rather than keep the caller's copy live.
+template <int DS>
+__device__ __forceinline__ ArgMax culled_max_search(const ScreenArgs& a, int O, const int* sl, int ncand,
+                                                 bool all, float best, int bi, int* s_need,
+                                                 int* s_wcnt, float* s_val, int* s_idx) {
+    constexpr int RS = sp_rs(DS);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int hl = lane & 15, half = lane >> 4;
+    float own[8][RS], co[RS], eo[RS], lo[RS];
+    load_out_block<DS>(a, O, hl, own, co, eo, lo);
+    const float pmo = a.pmax_o[O], a0o = a.a0_o[O];
+    const int total = all ? a.nbi : ncand;
+    int evaluated = 0;
+    for (int c0 = 0; c0 < total; c0 += 256) {
+        const int k = c0 + threadIdx.x;
+        const int J = all ? k : (k < ncand ? sl[k / kSuper] * kSuper + k % kSuper : a.nbi);
+        bool need = false;
+        if (k < total && J < a.nbi) {
+            float ub, sig;
+            bound_cheap<DS>(a, co, eo, lo, pmo, a0o, J, ub, sig);
+            need = ub + kCullMargin >= best;
+        }
+        int nneed = 0;
+        const int pos = compact_offset(need, nneed, s_wcnt);
+        if (need) s_need[pos] = J;
+        __syncthreads();
+        for (int s0 = 2 * warp; s0 < nneed; s0 += 16) {
+            const int e = s0 + half;
+            const int Jn = s_need[e < nneed ? e : s0];
+            const float u = bound_exact<DS>(a, own, co, pmo, Jn, hl);
+            if (hl == 0 && e < nneed) arg_update(best, bi, u, Jn);
+        }
+        evaluated += nneed;
+        block_argmax(best, bi, s_val, s_idx);
+    }
+    return ArgMax{best, bi, evaluated};
+}
+
+// Three CTAs per SM at DS = 3 (80 registers; the common path's working set
+// fits, and 90 registers at two CTAs per SM measured 13 % slower), two above.
+template <int DS>
+__global__ void __launch_bounds__(256, DS <= 3 ? 3 : 2) k_sp_screen(const __grid_constant__ ScreenArgs a) {
+    constexpr int RS = sp_rs(DS);
+    __shared__ float s_val[8];
+    __shared__ int s_idx[8];
+    __shared__ int s_wcnt[8];
+    __shared__ int s_need[256];
+    __shared__ int s_flag;
+    const int O = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t rbeg = a.row_off[O];
+    const int cap = (int)min(a.row_off[O + 1] - rbeg, (int64_t)a.nbi);
+    int* row = a.lists + rbeg;
+    const bool roomy = cap >= a.nbi;
+
+    if (a.log2_tau == -INFINITY) {   // every block kept (the row is roomy)
+        for (int J = threadIdx.x; J < cap; J += blockDim.x) row[J] = J;
+        if (threadIdx.x == 0) a.counts[O] = cap;
+        return;
+    }
+
+    const int hl = lane & 15, half = lane >> 4;
+    float own[8][RS], co[RS], eo[RS], lo[RS];
+    load_out_block<DS>(a, O, hl, own, co, eo, lo);
     const float pmo = a.pmax_o[O], a0o = a.a0_o[O];
     const float T = a.log2_tau + a.lw2_o[O] - log2f((float)a.nbi);
 
@@ -876,14 +982,14 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
     // super-blocks that survived the super-block cull of this output block's
     // super-block (culled_ub then starts from the largest culled super bound).
     int S = 0;
-    float culled_ub = -INFINITY;
+    float culled_ub = -INFINITY, super_ub = -INFINITY;
     int ncand = a.nbi;
     const int* sl = nullptr;
     if (a.slist != nullptr) {
         const int so = O / kSuper;
         sl = a.slist + (int64_t)so * a.nsbi;
         ncand = a.scount[so] * kSuper;
-        culled_ub = a.sculled[so];
+        super_ub = a.sculled[so];
     }
     for (int c0 = 0; c0 < ncand; c0 += 256) {
         const int k = c0 + threadIdx.x;
@@ -896,7 +1002,7 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
             if (!surv) culled_ub = fmaxf(culled_ub, ub);
         }
         const int pos = compact_offset(surv, S, s_wcnt);
-        if (surv && FS_IDX_OK(pos, a.nbi, 34)) row[pos] = J;
+        if (surv && FS_IDX_OK(pos, cap, 34)) row[pos] = J;
         __syncthreads();
     }
 #pragma unroll
@@ -905,56 +1011,45 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
     __syncthreads();
     culled_ub = s_val[0];
     for (int w = 1; w < 8; ++w) culled_ub = fmaxf(culled_ub, s_val[w]);
+    culled_ub = fmaxf(culled_ub, super_ub);
     __syncthreads();
 
-    bool full = 2 * S > a.nbi || S == 0;
+    // a roomy row takes the whole-row route when most candidates survive, or none
+    bool full = roomy && (2 * S > a.nbi || S == 0);
     float best = -INFINITY;
     int bi = 0x7fffffff;
     if (!full) {
-        // 2a. exact bounds of the survivors, two per warp
+        // 2a. exact bounds of the survivors, two per warp, stored from the row's end
         for (int s0 = 2 * warp; s0 < S; s0 += 16) {
             const int sv = s0 + half;
             const int J = row[sv < S ? sv : s0];
             const float u = bound_exact<DS>(a, own, co, pmo, J, hl);
-            if (hl == 0 && sv < S && FS_IDX_OK(a.nbi - 1 - sv, a.nbi, 35))
-                row[a.nbi - 1 - sv] = __float_as_int(u);
+            if (hl == 0 && sv < S && FS_IDX_OK(cap - 1 - sv, cap, 35))
+                row[cap - 1 - sv] = __float_as_int(u);
         }
         __syncthreads();
         // 2b. first maximiser among them
-        for (int sv = threadIdx.x; sv < S; sv += blockDim.x) {
-            const float u = __int_as_float(row[a.nbi - 1 - sv]);
-            const int J = row[sv];
-            if (u > best || (u == best && J < bi)) {
-                best = u;
-                bi = J;
+        for (int sv = threadIdx.x; sv < S; sv += blockDim.x)
+            arg_update(best, bi, __int_as_float(row[cap - 1 - sv]), row[sv]);
+        block_argmax(best, bi, s_val, s_idx);
+        // 2c. a culled block could still be the maximiser
+        unsigned long long extra = 0;
+        if (culled_ub + kCullMargin >= best) {
+            if (roomy) {
+                full = true;
+            } else {
+                const ArgMax r = culled_max_search<DS>(a, O, sl, ncand,
+                                                       sl == nullptr || super_ub + kCullMargin >= best,
+                                                       best, bi, s_need, s_wcnt, s_val, s_idx);
+                best = r.best;
+                bi = r.bi;
+                extra = (unsigned long long)r.evaluated;
             }
         }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ob > best || (ob == best && oi < bi)) {
-                best = ob;
-                bi = oi;
-            }
-        }
-        if (lane == 0) {
-            s_val[warp] = best;
-            s_idx[warp] = bi;
-        }
-        __syncthreads();
-        best = s_val[0];
-        bi = s_idx[0];
-        for (int w = 1; w < 8; ++w)
-            if (s_val[w] > best || (s_val[w] == best && s_idx[w] < bi)) {
-                best = s_val[w];
-                bi = s_idx[w];
-            }
-        // 2c. a culled block could still be the maximiser: evaluate everything
-        full = culled_ub + kCullMargin >= best;
-        __syncthreads();
         if (!full) {
             // 2d. compaction of the kept survivors (reads of a round before its writes)
+            if (threadIdx.x == 0) s_flag = 0;
+            __syncthreads();
             int base = 0;
             for (int c0 = 0; c0 < S; c0 += 256) {
                 const int sv = c0 + threadIdx.x;
@@ -962,18 +1057,33 @@ __global__ void __launch_bounds__(256) k_sp_screen(ScreenArgs a) {
                 int J = 0;
                 if (sv < S) {
                     J = row[sv];
-                    const float u = __int_as_float(row[a.nbi - 1 - sv]);
+                    const float u = __int_as_float(row[cap - 1 - sv]);
                     float ub, sig;
                     bound_cheap<DS>(a, co, eo, lo, pmo, a0o, J, ub, sig);
                     keep = (u + sig >= T) || J == bi;
+                    if (J == bi) s_flag = 1;
                 }
                 const int pos = compact_offset(keep, base, s_wcnt);
-                if (keep && FS_IDX_OK(pos, a.nbi, 36)) row[pos] = J;
+                if (keep && FS_IDX_OK(pos, cap, 36)) row[pos] = J;
                 __syncthreads();
             }
             if (threadIdx.x == 0) {
+                // a maximiser found among the culled blocks joins the list in order
+                if (!s_flag && bi < a.nbi) {
+                    if (base < cap) {
+                        int q = base;
+                        while (q > 0 && row[q - 1] > bi) {
+                            row[q] = row[q - 1];
+                            --q;
+                        }
+                        row[q] = bi;
+                        ++base;
+                    } else {
+                        atomicAdd(a.overflow, 1ull);
+                    }
+                }
                 a.counts[O] = base;
-                atomicAdd(a.exact, (unsigned long long)S);
+                atomicAdd(a.exact, (unsigned long long)S + extra);
             }
             return;
         }
@@ -1046,7 +1156,8 @@ struct SpHalfArgs {
     const float* cols;       // packed [nc x RS] records of the other side
     int64_t nr, nc;
     int nbi;
-    const int* lists;        // [nbo x nbi]
+    const int* lists;        // kept lists: row o at lists + row_off[o]
+    const int64_t* row_off;  // [nbo + 1]
     const int* counts;       // [nbo]
     const int* order;        // [nbo] output block of each CTA
     float kappa;             // 2 L / eps
@@ -1056,7 +1167,7 @@ struct SpHalfArgs {
     float* pot;              // potentials out [nr] (sorted order)
     float* rowsum;           // measure mode: row marginal 2^{bias + LSE2} [nr]
     int measure;             // 1: write rowsum only, no update
-    unsigned long long* work;   // [4] accumulated: block pairs, score pairs evaluated,
+    unsigned long long* work;   // accumulated: block pairs, score pairs evaluated,
                                 //     (screening: exact bounds), rows fixed up
     // reference offsets: rows whose guarded sum left the range, for k_sp_fix
     int* fix_list;            // [nr]
@@ -1268,7 +1379,7 @@ __global__ void __launch_bounds__(256, sp_min_blocks(D, REF)) k_sp_half(SpHalfAr
     }
 
     const int cnt = a.counts[O];
-    const int* lst = a.lists + (int64_t)O * a.nbi;
+    const int* lst = a.lists + a.row_off[O];
     float4* my = sc[warp];
     int64_t cols_done = 0;
     for (int e = warp; e < cnt; e += kSpWarps) {
@@ -1448,7 +1559,7 @@ __global__ void __launch_bounds__(256) k_sp_fix(SpHalfArgs a) {
 #pragma unroll
         for (int k = 0; k < D; ++k) q[k] = a.rows[row * RS + k] * a.kappa;
         float M = -INFINITY, S = 0.f;
-        const int* lst = a.lists + O * a.nbi;
+        const int* lst = a.lists + a.row_off[O];
         const int64_t total = (int64_t)a.counts[O] * kSB;
         for (int64_t idx = threadIdx.x; idx < total; idx += blockDim.x) {
             const int J = lst[idx / kSB];
@@ -1494,6 +1605,50 @@ __global__ void __launch_bounds__(256) k_sp_fix(SpHalfArgs a) {
             __threadfence();
         }
     }
+}
+
+// Capacities of the kept-list rows and their offsets (one block, 1024
+// threads, each summing a contiguous range, then a scan of the 1024 sums):
+// nbi entries per row without the super-block cull; with it, room for the
+// candidates' survivors, their bounds and the first maximiser,
+// 2 x 16 x (surviving super-blocks) + 1, at most nbi.
+__global__ void __launch_bounds__(1024) k_sp_row_offsets(const int* __restrict__ scount, int64_t nbo,
+                                                         int nbi, int64_t* __restrict__ off) {
+    __shared__ int64_t part[1024];
+    const int t = threadIdx.x;
+    const int64_t per = (nbo + 1023) / 1024;
+    const int64_t b0 = min(nbo, t * per), b1 = min(nbo, b0 + per);
+    auto capacity = [&](int64_t o) -> int64_t {
+        if (scount == nullptr) return nbi;
+        return min((int64_t)nbi, 2 * (int64_t)kSuper * scount[o / kSuper] + 1);
+    };
+    int64_t sum = 0;
+    for (int64_t o = b0; o < b1; ++o) sum += capacity(o);
+    part[t] = sum;
+    __syncthreads();
+    if (t == 0) {
+        int64_t run = 0;
+        for (int i = 0; i < 1024; ++i) {
+            const int64_t v = part[i];
+            part[i] = run;
+            run += v;
+        }
+        off[nbo] = run;
+    }
+    __syncthreads();
+    int64_t run = part[t];
+    for (int64_t o = b0; o < b1; ++o) {
+        off[o] = run;
+        run += capacity(o);
+    }
+}
+
+// Kept lists into the dense layout of fs_sparse_screen: row o at out + o nbi.
+__global__ void k_sp_expand_lists(const int* __restrict__ lists, const int64_t* __restrict__ row_off,
+                                  const int* __restrict__ counts, int64_t nbi, int* __restrict__ out) {
+    const int64_t o = blockIdx.x;
+    const int cnt = counts[o];
+    for (int e = threadIdx.x; e < cnt; e += blockDim.x) out[o * nbi + e] = lists[row_off[o] + e];
 }
 
 // Output blocks in decreasing order of kept-list length (buckets of
@@ -1561,12 +1716,29 @@ struct SpBufs {
     MortonBufs srt;
     size_t shift_part, shift;
     SpSide X, Y;
-    size_t lists, counts, order, rowsum, red_part, red_out, kept, fix_list, fix_count;
+    size_t lists, row_off, counts, order, rowsum, red_part, red_out, kept, fix_list, fix_count;
+    int64_t list_entries;          // kept-list entries the workspace holds (0: none)
     size_t slist, scount, sculled;   // super-block cull
     // coarse stage
     size_t cshift, cPX, cPY, cnx, cny, clx, cly, cpart, F, G;
     int csplits_f, csplits_g;
     int64_t ccps_f, ccps_g;
+};
+
+// Where the kept lists of the current screening live: the workspace region,
+// or (above kRoomyListEntries block pairs) a device buffer owned by the call,
+// grown to the offsets' total at each screening and freed with the call.
+struct SpLists {
+    int* p = nullptr;
+    int64_t* off = nullptr;
+    int* own = nullptr;
+    size_t own_cap = 0;
+    SpLists() = default;
+    SpLists(const SpLists&) = delete;
+    SpLists& operator=(const SpLists&) = delete;
+    ~SpLists() {
+        if (own) cudaFree(own);
+    }
 };
 
 void layout_side(Layout& L, SpSide& s, int64_t cnt, int d) {
@@ -1606,13 +1778,17 @@ void layout_sparse(Layout& L, SpBufs& B, int64_t n, int64_t m, int d, int sms, b
     layout_side(L, B.X, n, d);
     layout_side(L, B.Y, m, d);
     const int64_t nx = B.X.nb, ny = B.Y.nb;
-    B.lists = L.take(sizeof(int) * (size_t)std::max(nx * ny, (int64_t)1));
+    // the kept lists fit in nx ny entries; above kRoomyListEntries they go to a
+    // buffer of the call sized at each screening
+    B.list_entries = nx * ny <= kRoomyListEntries ? std::max(nx * ny, (int64_t)1) : 0;
+    B.lists = L.take(sizeof(int) * (size_t)std::max(B.list_entries, (int64_t)1));
+    B.row_off = L.take(sizeof(int64_t) * (size_t)(std::max(nx, ny) + 1));
     B.counts = L.take(sizeof(int) * std::max(nx, ny));
     B.order = L.take(sizeof(int) * std::max(nx, ny));
     B.rowsum = L.take(sizeof(float) * n);
     B.red_part = L.take(sizeof(double) * kRedPartials);
     B.red_out = L.take(sizeof(double) * 2);
-    B.kept = L.take(sizeof(unsigned long long) * 4);
+    B.kept = L.take(sizeof(unsigned long long) * kWorkCounters);
     B.fix_list = L.take(sizeof(int) * mx);
     B.fix_count = L.take(sizeof(unsigned int) * 2);
     B.slist = L.take(sizeof(int) * (size_t)std::max(B.X.nsb * B.Y.nsb, (int64_t)1));
@@ -1717,7 +1893,8 @@ fs_status set_bias(Call& c, const SpSide& s, int D, float l_over_eps) {
     return FS_OK;
 }
 
-fs_status screen(Call& c, const SpBufs& B, const SpSide& o, const SpSide& in, float eps, float tau) {
+fs_status screen(Call& c, const SpBufs& B, SpLists& LS, const SpSide& o, const SpSide& in, float eps,
+                 float tau) {
     ScreenArgs s;
     s.so = c.at<float>(o.scr);
     s.si = c.at<float>(in.scr);
@@ -1739,9 +1916,9 @@ fs_status screen(Call& c, const SpBufs& B, const SpSide& o, const SpSide& in, fl
     s.kappa = (float)(2.0 * kLog2e / (double)eps);
     s.l_over_eps = (float)(kLog2e / (double)eps);
     s.log2_tau = tau > 0.f ? (float)std::log2((double)tau) : -INFINITY;
-    s.lists = c.at<int>(B.lists);
     s.counts = c.at<int>(B.counts);
     s.exact = c.at<unsigned long long>(B.kept) + 2;
+    s.overflow = c.at<unsigned long long>(B.kept) + 4;
     s.slist = nullptr;
     s.scount = nullptr;
     s.sculled = nullptr;
@@ -1783,6 +1960,33 @@ fs_status screen(Call& c, const SpBufs& B, const SpSide& o, const SpSide& in, fl
         s.scount = sa.scount;
         s.sculled = sa.sculled;
     }
+    // row capacities and offsets of the kept lists, then their storage
+    LS.off = c.at<int64_t>(B.row_off);
+    k_sp_row_offsets<<<1, 1024, 0, c.stream>>>(s.scount, o.nb, (int)in.nb, LS.off);
+    count_launch();
+    FS_CUDA(cudaGetLastError());
+    if (o.nb * in.nb <= B.list_entries) {
+        LS.p = c.at<int>(B.lists);
+    } else {
+        int64_t total = 0;
+        FS_CUDA(cudaMemcpyAsync(&total, LS.off + o.nb, sizeof(total), cudaMemcpyDeviceToHost, c.stream));
+        FS_CUDA(cudaStreamSynchronize(c.stream));
+        if ((size_t)total > LS.own_cap) {
+            if (LS.own) FS_CUDA(cudaFree(LS.own));
+            LS.own = nullptr;
+            LS.own_cap = 0;
+            const size_t want = (size_t)total + (size_t)total / 4 + 1;
+            if (cudaMalloc(&LS.own, sizeof(int) * want) != cudaSuccess) {
+                (void)cudaGetLastError();
+                LS.own = nullptr;
+                return fail(FS_ERR_OOM, "kept lists: %zu entries do not fit on the device", want);
+            }
+            LS.own_cap = want;
+        }
+        LS.p = LS.own;
+    }
+    s.lists = LS.p;
+    s.row_off = LS.off;
     with_ds(o.d, [&](auto ds) {
         k_sp_screen<decltype(ds)::value><<<(unsigned)o.nb, 256, 0, c.stream>>>(s);
     });
@@ -1791,15 +1995,16 @@ fs_status screen(Call& c, const SpBufs& B, const SpSide& o, const SpSide& in, fl
     return FS_OK;
 }
 
-fs_status sparse_half(Call& c, const SpBufs& B, const SpSide& o, const SpSide& in, int D,
-                      float eps, bool measure, bool ref = false) {
+fs_status sparse_half(Call& c, const SpBufs& B, const SpLists& LS, const SpSide& o,
+                      const SpSide& in, int D, float eps, bool measure, bool ref = false) {
     SpHalfArgs h;
     h.rows = c.at<float>(o.rec);
     h.cols = c.at<float>(in.rec);
     h.nr = o.cnt;
     h.nc = in.cnt;
     h.nbi = (int)in.nb;
-    h.lists = c.at<int>(B.lists);
+    h.lists = LS.p;
+    h.row_off = LS.off;
     h.counts = c.at<int>(B.counts);
     h.kappa = (float)(2.0 * kLog2e / (double)eps);
     h.eps_ln2 = (float)((double)eps * kLn2);
@@ -1840,9 +2045,10 @@ fs_status sparse_half(Call& c, const SpBufs& B, const SpSide& o, const SpSide& i
 
 // Row residual |P 1 - a|_1 of the block-sparse plan at the current
 // potentials (screens the f-side first; the lists stay valid for an f-update).
-fs_status measure_residual(Call& c, const SpBufs& B, int D, float eps, float tau, double* out) {
-    FS_TRY(screen(c, B, B.X, B.Y, eps, tau));
-    FS_TRY(sparse_half(c, B, B.X, B.Y, D, eps, true));
+fs_status measure_residual(Call& c, const SpBufs& B, SpLists& LS, int D, float eps, float tau,
+                           double* out) {
+    FS_TRY(screen(c, B, LS, B.X, B.Y, eps, tau));
+    FS_TRY(sparse_half(c, B, LS, B.X, B.Y, D, eps, true));
     FS_CUDA(launch_l1_double(c.at<float>(B.rowsum), c.at<float>(B.X.ws), B.X.cnt,
                              c.at<double>(B.red_part), c.at<double>(B.red_out), 0, c.stream));
     FS_CUDA(cudaMemcpyAsync(out, c.at<double>(B.red_out), sizeof(double), cudaMemcpyDeviceToHost,
@@ -1896,7 +2102,6 @@ fs_status coarse_stage(Call& c, SpBufs& B, int d, float eps, int iters) {
     return FS_OK;
 }
 
-constexpr int64_t kMaxListEntries = (int64_t)1 << 30;
 constexpr int kSpOnlineIters = 2;
 
 fs_status check_sparse_args(const float* X, const float* a, int64_t n, const float* Y, const float* b,
@@ -1910,8 +2115,18 @@ fs_status check_sparse_args(const float* X, const float* a, int64_t n, const flo
     if (!(eps > 0.f) || !std::isfinite(eps))
         return fail(FS_ERR_INVALID_ARG, "eps must be positive and finite (got %g)", (double)eps);
     const int64_t nx = (n + kSB - 1) / kSB, ny = (m + kSB - 1) / kSB;
-    if (nx * ny > kMaxListEntries)
-        return fail(FS_ERR_UNSUPPORTED, "%lld x %lld blocks exceed the block-list limit of 2^30",
+    const int64_t sx = (nx + kSuper - 1) / kSuper, sy = (ny + kSuper - 1) / kSuper;
+    if (sx * sy > kMaxSuperEntries)
+        return fail(FS_ERR_UNSUPPORTED, "%lld x %lld super-blocks exceed the limit of 2^32 pairs",
+                    (long long)sx, (long long)sy);
+    return FS_OK;
+}
+
+// tau = 0 keeps every block pair: the lists then hold nx ny entries.
+fs_status check_keep_all(int64_t n, int64_t m, float tau) {
+    const int64_t nx = (n + kSB - 1) / kSB, ny = (m + kSB - 1) / kSB;
+    if (tau == 0.f && nx * ny > kRoomyListEntries)
+        return fail(FS_ERR_UNSUPPORTED, "tau = 0 keeps all %lld x %lld block pairs (at most 2^30)",
                     (long long)nx, (long long)ny);
     return FS_OK;
 }
@@ -1926,6 +2141,7 @@ fs_status sparse_solve_entry(const float* X, const float* a, int64_t n, const fl
         return fail(FS_ERR_INVALID_ARG, "negative iteration count in fs_sparse_options");
     if (!(opt->tau >= 0.f && opt->tau < 1.f))
         return fail(FS_ERR_INVALID_ARG, "tau=%g must be in [0, 1)", (double)opt->tau);
+    FS_TRY(check_keep_all(n, m, opt->tau));
     if (!(opt->target >= 0.f) || !std::isfinite(opt->target))
         return fail(FS_ERR_INVALID_ARG, "target=%g must be finite and >= 0", (double)opt->target);
     for (int i = 0; i < 3; ++i)
@@ -1948,6 +2164,7 @@ fs_status sparse_solve_entry(const float* X, const float* a, int64_t n, const fl
     FS_TRY(classify(c, P.f, f, (size_t)n));
     FS_TRY(classify(c, P.g, g, (size_t)m));
     SpBufs B;
+    SpLists LS;
     layout_sparse(c.L, B, n, m, d, c.ws->sms, opt->coarse_iters > 0);
     FS_TRY(ensure_capacity(c));
     for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g}) bind(c, *A);
@@ -1970,7 +2187,7 @@ fs_status sparse_solve_entry(const float* X, const float* a, int64_t n, const fl
     FS_TRY(set_bias(c, B.X, D, l_over_eps));
     FS_TRY(set_bias(c, B.Y, D, l_over_eps));
     timing_end(tp, TIME_PREP, c.stream);
-    FS_CUDA(cudaMemsetAsync(c.at<unsigned long long>(B.kept), 0, 4 * sizeof(unsigned long long),
+    FS_CUDA(cudaMemsetAsync(c.at<unsigned long long>(B.kept), 0, kWorkCounters * sizeof(unsigned long long),
                             c.stream));
     FS_CUDA(cudaMemsetAsync(c.at<unsigned int>(B.fix_count), 0, 2 * sizeof(unsigned int), c.stream));
 
@@ -1982,32 +2199,35 @@ fs_status sparse_solve_entry(const float* X, const float* a, int64_t n, const fl
     FS_TRY(refresh_psi(c, B.Y, l_over_eps));
     while (it < opt->max_iters) {
         if (opt->target > 0.f && opt->check_every > 0 && it > 0 && it % opt->check_every == 0) {
-            FS_TRY(measure_residual(c, B, D, eps, tau, &resid));
+            FS_TRY(measure_residual(c, B, LS, D, eps, tau, &resid));
             ++passes;
             if (resid <= (double)opt->target) break;
             screened = true;
         }
-        if (!screened) FS_TRY(screen(c, B, B.X, B.Y, eps, tau));
+        if (!screened) FS_TRY(screen(c, B, LS, B.X, B.Y, eps, tau));
         screened = false;
         // the first iterations take the online max: the lifted (or given)
         // potentials may be far from the first updates
         const bool ref = it >= online_iters;
-        FS_TRY(sparse_half(c, B, B.X, B.Y, D, eps, false, ref));
+        FS_TRY(sparse_half(c, B, LS, B.X, B.Y, D, eps, false, ref));
         FS_TRY(refresh_psi(c, B.X, l_over_eps));
-        FS_TRY(screen(c, B, B.Y, B.X, eps, tau));
-        FS_TRY(sparse_half(c, B, B.Y, B.X, D, eps, false, ref));
+        FS_TRY(screen(c, B, LS, B.Y, B.X, eps, tau));
+        FS_TRY(sparse_half(c, B, LS, B.Y, B.X, D, eps, false, ref));
         FS_TRY(refresh_psi(c, B.Y, l_over_eps));
         passes += 2;
         ++it;
     }
     if (rep) {
-        FS_TRY(measure_residual(c, B, D, eps, tau, &resid));
+        FS_TRY(measure_residual(c, B, LS, D, eps, tau, &resid));
         ++passes;
     }
-    unsigned long long work[4] = {0, 0, 0, 0};
+    unsigned long long work[kWorkCounters] = {0, 0, 0, 0, 0};
     FS_CUDA(cudaMemcpyAsync(work, c.at<unsigned long long>(B.kept), sizeof(work),
                             cudaMemcpyDeviceToHost, c.stream));
     FS_CUDA(cudaStreamSynchronize(c.stream));
+    if (work[4])
+        return fail(FS_ERR_CUDA, "internal: %llu kept blocks found no room in their list",
+                    (unsigned long long)work[4]);
     k_sp_scatter_pot<<<grid_for(n, 256), 256, 0, c.stream>>>(c.at<float>(B.X.pot),
                                                              c.at<int>(B.X.perm), n, P.f.dev);
     k_sp_scatter_pot<<<grid_for(m, 256), 256, 0, c.stream>>>(c.at<float>(B.Y.pot),
@@ -2059,15 +2279,22 @@ fs_status screen_entry(const float* X, const float* a, int64_t n, const float* Y
     if (!f || !g || !counts || !lists) return fail(FS_ERR_INVALID_ARG, "null f, g, counts or lists");
     if (side != 0 && side != 1) return fail(FS_ERR_INVALID_ARG, "side=%d must be 0 or 1", side);
     if (!(tau >= 0.f && tau < 1.f)) return fail(FS_ERR_INVALID_ARG, "tau=%g must be in [0, 1)", (double)tau);
+    FS_TRY(check_keep_all(n, m, tau));
     for (const void* p : {(const void*)X, (const void*)a, (const void*)Y, (const void*)b,
                           (const void*)f, (const void*)g, (const void*)counts, (const void*)lists})
         if (!is_device_ptr(p)) return fail(FS_ERR_INVALID_ARG, "fs_sparse_screen takes device arrays only");
     Call c;
     FS_TRY(begin_call(c, stream));
     SpBufs B;
+    SpLists LS;
     layout_sparse(c.L, B, n, m, d, c.ws->sms, false);
+    if (c.capturing && B.list_entries == 0)
+        return fail(FS_ERR_UNSUPPORTED, "above 2^30 block pairs fs_sparse_screen sizes its lists on "
+                                        "the host: not inside a graph capture");
     FS_TRY(ensure_capacity(c));
     FS_TRY(prepare_sparse(c, B, X, a, n, Y, b, m, d));
+    FS_CUDA(cudaMemsetAsync(c.at<unsigned long long>(B.kept), 0, kWorkCounters * sizeof(unsigned long long),
+                            c.stream));
     k_sp_gather_pot<<<grid_for(n, 256), 256, 0, c.stream>>>(f, c.at<int>(B.X.perm), n,
                                                             c.at<float>(B.X.pot));
     k_sp_gather_pot<<<grid_for(m, 256), 256, 0, c.stream>>>(g, c.at<int>(B.Y.perm), m,
@@ -2079,11 +2306,13 @@ fs_status screen_entry(const float* X, const float* a, int64_t n, const float* Y
     FS_TRY(refresh_psi(c, B.Y, l_over_eps));
     const SpSide& o = side == 0 ? B.X : B.Y;
     const SpSide& in = side == 0 ? B.Y : B.X;
-    FS_TRY(screen(c, B, o, in, eps, tau));
+    FS_TRY(screen(c, B, LS, o, in, eps, tau));
     FS_CUDA(cudaMemcpyAsync(counts, c.at<int>(B.counts), sizeof(int) * o.nb,
                             cudaMemcpyDeviceToDevice, c.stream));
-    FS_CUDA(cudaMemcpyAsync(lists, c.at<int>(B.lists), sizeof(int) * o.nb * in.nb,
-                            cudaMemcpyDeviceToDevice, c.stream));
+    k_sp_expand_lists<<<(unsigned)o.nb, 256, 0, c.stream>>>(LS.p, LS.off, c.at<int>(B.counts), in.nb,
+                                                            lists);
+    count_launch();
+    FS_CUDA(cudaGetLastError());
     return end_call(c);
 }
 

@@ -96,6 +96,14 @@ WORKLOADS: Dict[str, Workload] = {
         about="block-sparse solver at n=m=4e6: the c2 recipe, eps=3.6e-4 (blur 0.019, three "
               "mean spacings), 50 centroid iterations, then 20 block-sparse iterations with "
               "tau=1e-6"),
+    # sixteen times the points of bs_n1m_d3 (125,000^2 block pairs: the kept lists
+    # no longer fit one row of every block per output block)
+    "bs_n16m_d3": Workload(
+        "bs_n16m_d3", 16_000_000, 16_000_000, 3, ((0.000142, 20),), None, seed=1009,
+        coarse_iters=50, tau=1e-6,
+        about="block-sparse solver at n=m=1.6e7: the c2 recipe, eps=1.42e-4 (blur 0.012, three "
+              "mean spacings), 50 centroid iterations, then 20 block-sparse iterations with "
+              "tau=1e-6"),
 }
 
 

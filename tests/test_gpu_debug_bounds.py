@@ -80,7 +80,10 @@ def test_fma_solve_and_apply_record_no_bad_index(dbg, n, m, d, splits):
 @pytest.mark.parametrize("n,m,d,tau,online", [(1, 1, 1, 1e-6, 0), (300, 129, 2, 1e-5, -1),
                                               (2049, 1900, 3, 1e-6, -1), (3000, 2600, 2, 1e-4, 0),
                                               (700, 513, 4, 1e-5, -1), (1100, 900, 5, 1e-6, 0),
-                                              (1300, 1029, 8, 1e-5, -1), (1, 2, 8, 1e-6, 0)])
+                                              (1300, 1029, 8, 1e-5, -1), (1, 2, 8, 1e-6, 0),
+                                              # >= 32 input blocks: the super-block cull and
+                                              # kept-list rows sized by its survivors
+                                              (6000, 5200, 3, 1e-6, -1), (5000, 4600, 5, 1e-5, 0)])
 def test_block_sparse_solve_records_no_bad_index(dbg, n, m, d, tau, online):
     import torch
     inp = make_inputs("c2_n10k_d3", n=n, m=m, d=d)

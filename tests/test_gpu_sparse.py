@@ -358,6 +358,68 @@ def test_invalid_arguments_are_rejected():
         assert e.value.status == fs.FS_ERR_INVALID_ARG
 
 
+def test_screening_without_survivors_keeps_the_first_maximiser():
+    """Output blocks whose potentials sit far below their marginals: every
+    bound misses the threshold, so the list holds the first maximiser of U
+    alone.  With 157 x 141 blocks the super-block cull runs and the rows are
+    sized by its survivors (fewer entries than input blocks), so the maximiser
+    is searched among the culled blocks without a whole-row scratch."""
+    name, n, m, d, eps, tau = "c2_n10k_d3", 20000, 18000, 3, 0.002, 1e-6
+    inp, f32, g32 = _screen_case(name, n, m, d, eps, 6)
+    px, py = bsp.morton_order(inp["X"], inp["Y"])
+    low = [3, 40, 77, 155]
+    for o in low:
+        f32[px[o * bsp.BLOCK:(o + 1) * bsp.BLOCK]] -= np.float32(400 * eps)
+    t = to_dev(dict(inp, f=f32, g=g32))
+    counts, lists = fs.fs_sparse_screen(t["X"], t["a"], t["Y"], t["b"], eps, t["f"], t["g"], tau, 0)
+    counts, lists = counts.cpu().numpy(), lists.cpu().numpy()
+    Xs, as_, Ys, bs = inp["X"][px], inp["a"][px], inp["Y"][py], inp["b"][py]
+    cx, wx = bsp.block_stats(Xs, as_)
+    cy, wy = bsp.block_stats(Ys, bs)
+    U, sig = bsp.block_bounds(Xs, as_, f32.astype(np.float64)[px], Ys, bs,
+                              g32.astype(np.float64)[py], eps, cx, cy)
+    T = np.log2(np.float64(tau)) + np.log2(wx.astype(np.float64)) - np.log2(U.shape[1])
+    for o in low:
+        assert np.all(U[o] + sig[o] < T[o] - MARGIN)   # nothing passes the threshold
+        assert counts[o] == 1
+        top2 = np.sort(U[o])[-2:]
+        if top2[1] - top2[0] > MARGIN:
+            assert lists[o, 0] == int(np.argmax(U[o]))
+    others = np.setdiff1d(np.arange(U.shape[0]), low)
+    assert np.all(counts[others] >= 1)
+
+
+def test_beyond_2_30_block_pairs_column_marginals():
+    """n = m = 1.6e7 (125,000^2 > 2^30 block pairs): the kept lists live in a
+    buffer sized at each screening from the super-block cull's survivors.
+    The workload in its launch configuration; at the returned potentials the
+    dense column marginals on sampled columns lie in [b_j, b_j + tau W_J]."""
+    w = WORKLOADS["bs_n16m_d3"]
+    eps, iters = w.stages[0]
+    tau = w.tau
+    inp = make_inputs(w.name)
+    t = to_dev(inp)
+    f, g, rep = fs.fs_sparse_solve(t["X"], t["a"], t["Y"], t["b"], eps, coarse_iters=w.coarse_iters,
+                                   max_iters=iters, tau=tau)
+    assert rep["iters"] == iters
+    assert rep["blocks_x"] * rep["blocks_y"] > 2 ** 30
+    assert rep["kept_pairs"] < 0.01 * rep["passes"] * w.n * w.m
+    f64, g64 = np64(f), np64(g)
+    del t, f, g
+    _, py = bsp.morton_order(inp["X"], inp["Y"])
+    _, wy = bsp.block_stats(inp["Y"][py], inp["b"][py])
+    block_of = np.empty(w.m, dtype=np.int64)
+    block_of[py] = np.arange(w.m) // bsp.BLOCK
+    cols = np.linspace(0, w.m - 1, 24).astype(np.int64)
+    g_upd = orc.f_update_rows(inp["Y"], inp["X"], inp["a"], eps, f64, cols)
+    c = inp["b"][cols].astype(np.float64) * np.exp((g64[cols] - g_upd) / orc.as_eps(eps))
+    b = inp["b"][cols].astype(np.float64)
+    # float32 rounding at eps = 1.42e-4: half an ulp of |g_j| <= 3 is 8.4e-4 of eps,
+    # and the scores reach ~1.5e4 log2 units (~1e-3 each, averaging over the rows)
+    assert np.all(c >= b * (1 - 3e-3))
+    assert np.all(c <= b * (1 + 3e-3) + tau * wy[block_of[cols]])
+
+
 def test_full_size_column_marginals_within_the_screening_bound():
     """The benchmark's block-sparse workload in its launch configuration
     (n = m = 10^6, d = 3, the workload's eps, centroid iterations, fine
