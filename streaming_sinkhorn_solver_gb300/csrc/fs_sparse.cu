@@ -32,12 +32,16 @@
 #include "fs_host.cuh"
 #include "fs_morton.cuh"
 
+#include <cooperative_groups.h>
+
 #include <algorithm>
 #include <cmath>
 #include <type_traits>
 
 namespace fs {
 namespace {
+
+namespace cg = cooperative_groups;
 
 constexpr int kSB = 128;            // points per block
 constexpr int kSuper = 16;          // blocks per super-block of the two-level cull
@@ -1534,77 +1538,155 @@ __global__ void __launch_bounds__(256, sp_min_blocks(D, REF)) k_sp_half(SpHalfAr
 }
 
 // Recompute, with the online max over the row block's kept blocks, the rows a
-// guarded half-update listed: one 256-thread block per row (a row's kept
-// list can hold hundreds of blocks of 128 columns), threads striding over
-// the kept columns, then a fixed-order merge (warp butterflies, then the
-// warps in order), so the result does not depend on timing.  The grid
-// strides over the list; the last block to finish resets it for the next
-// half-update.
-constexpr int kSpFixBlocks = 1216;   // 8 per SM on 152 SMs; idle blocks exit at once
+// guarded half-update listed.  Two launches share the work by the number of
+// listed rows, each leaving it to the other when it is not its case:
+//   - many rows (at least kSpFixRowsWide): one 256-thread CTA per row, the
+//     CTAs striding over the list;
+//   - few rows: a cluster of eight CTAs per row, CTA r folding the r-th
+//     eighth of the row's kept list (which can hold thousands of blocks),
+//     merged in rank order through distributed shared memory.
+// Inside a CTA, half a CTA takes a kept block (a thread per column), four
+// blocks in flight per thread, with an online max; the warps' (max, sum)
+// merge in order, so no result depends on timing.  The last CTA of the two
+// launches to finish resets the list for the next half-update.
+constexpr int kSpFixCluster = 8;
+constexpr int kSpFixBlocks = 1216;          // one CTA per row: 8 per SM on 152 SMs
+constexpr int kSpFixClusterBlocks = 608;    // 76 clusters of 8, all resident at once
+constexpr unsigned int kSpFixRowsWide = kSpFixBlocks;
+
+// (max, sum) of one row's scores over the kept-list entries [eb, ee), in the
+// calling CTA's fixed order.
+template <int D>
+__device__ __forceinline__ float2 fix_fold(const SpHalfArgs& a, int64_t row, const int* lst, int eb,
+                                           int ee, float2* s_part) {
+    constexpr int RS = fma_stride(D);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int hc = threadIdx.x >> 7, col_in = threadIdx.x & (kSB - 1);
+    float q[D];
+#pragma unroll
+    for (int k = 0; k < D; ++k) q[k] = a.rows[row * RS + k] * a.kappa;
+    float M = -INFINITY, S = 0.f;
+    for (int e0 = eb + hc; e0 < ee; e0 += 8) {
+        // this half-CTA's entries e0, e0 + 2, e0 + 4, e0 + 6
+        float sc[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            sc[u] = -INFINITY;
+            const int e = e0 + 2 * u;
+            if (e < ee) {
+                const int J = lst[e];
+                const int64_t col = (int64_t)J * kSB + col_in;
+                if (FS_IDX_OK(J, a.nbi, 41) && col < a.nc) {
+                    float cv[RS];
+                    ld_rec<RS>(a.cols + col * RS, cv);
+                    float v = cv[D];
+#pragma unroll
+                    for (int k = 0; k < D; ++k) v = fmaf(q[k], cv[k], v);
+                    sc[u] = v;
+                }
+            }
+        }
+        const float m = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+        if (m > M) {
+            S = (M == -INFINITY ? 0.f : S * ex2(M - m));
+            M = m;
+        }
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) S += ex2(sc[u] - M);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        const float Mo = __shfl_xor_sync(0xffffffffu, M, o);
+        const float So = __shfl_xor_sync(0xffffffffu, S, o);
+        lse_merge(M, S, Mo, So);
+    }
+    if (lane == 0) s_part[warp] = make_float2(M, S);
+    __syncthreads();
+    float Mc = -INFINITY, Sc = 0.f;
+    for (int v = 0; v < 8; ++v)
+        if (s_part[v].x != -INFINITY) lse_merge(Mc, Sc, s_part[v].x, s_part[v].y);
+    __syncthreads();   // s_part is free again
+    return make_float2(Mc, Sc);
+}
 
 template <int D>
-__global__ void __launch_bounds__(256) k_sp_fix(SpHalfArgs a) {
+__device__ __forceinline__ void fix_write(const SpHalfArgs& a, int64_t row, float Mf, float Sf) {
     constexpr int RS = fma_stride(D);
-    __shared__ unsigned int s_cnt;
-    __shared__ float2 s_part[8];
-    if (threadIdx.x == 0) s_cnt = min(*(volatile unsigned int*)&a.fix_count[0], (unsigned int)a.nr);
-    __syncthreads();
-    const unsigned int cnt = s_cnt;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (unsigned int w = blockIdx.x; w < cnt; w += gridDim.x) {
-        const int64_t row = a.fix_list[w];
-        if (!FS_IDX_OK(row, a.nr, 40)) continue;     // block-uniform
-        const int64_t O = row / kSB;
-        float q[D];
-#pragma unroll
-        for (int k = 0; k < D; ++k) q[k] = a.rows[row * RS + k] * a.kappa;
-        float M = -INFINITY, S = 0.f;
-        const int* lst = a.lists + a.row_off[O];
-        const int64_t total = (int64_t)a.counts[O] * kSB;
-        for (int64_t idx = threadIdx.x; idx < total; idx += blockDim.x) {
-            const int J = lst[idx / kSB];
-            if (!FS_IDX_OK(J, a.nbi, 41)) continue;
-            const int64_t col = (int64_t)J * kSB + idx % kSB;
-            if (col >= a.nc) continue;
-            float cv[RS];
-            ld_rec<RS>(a.cols + col * RS, cv);
-            float sc = cv[D];
-#pragma unroll
-            for (int k = 0; k < D; ++k) sc = fmaf(q[k], cv[k], sc);
-            if (sc > M) {
-                S = (M == -INFINITY ? 0.f : S * ex2(M - sc));
-                M = sc;
-            }
-            S += ex2(sc - M);
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            const float Mo = __shfl_xor_sync(0xffffffffu, M, o);
-            const float So = __shfl_xor_sync(0xffffffffu, S, o);
-            lse_merge(M, S, Mo, So);
-        }
-        if (lane == 0) s_part[warp] = make_float2(M, S);
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            float Mf = -INFINITY, Sf = 0.f;
-            for (int v = 0; v < 8; ++v)
-                if (s_part[v].x != -INFINITY) lse_merge(Mf, Sf, s_part[v].x, s_part[v].y);
-            const float lse2 = Mf + log2f(Sf);
-            a.pot[row] = a.rnorm[row] - a.eps_ln2 * lse2;
-            a.rows[row * RS + D] = a.rlogw2[row] - lse2;
-        }
-        __syncthreads();
-    }
+    const float lse2 = Mf + log2f(Sf);
+    a.pot[row] = a.rnorm[row] - a.eps_ln2 * lse2;
+    a.rows[row * RS + D] = a.rlogw2[row] - lse2;
+}
+
+// The last CTA of both fixup launches to finish empties the list.
+__device__ __forceinline__ void fix_done(const SpHalfArgs& a, unsigned int cnt) {
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
-        if (atomicAdd(&a.fix_count[1], 1u) == gridDim.x - 1) {
+        if (atomicAdd(&a.fix_count[1], 1u) == (unsigned int)(kSpFixBlocks + kSpFixClusterBlocks) - 1u) {
             atomicAdd(&a.work[3], (unsigned long long)cnt);
             a.fix_count[0] = 0;
             a.fix_count[1] = 0;
             __threadfence();
         }
     }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) k_sp_fix_rows(const __grid_constant__ SpHalfArgs a) {
+    __shared__ unsigned int s_cnt;
+    __shared__ float2 s_part[8];
+    if (threadIdx.x == 0) s_cnt = min(*(volatile unsigned int*)&a.fix_count[0], (unsigned int)a.nr);
+    __syncthreads();
+    const unsigned int cnt = s_cnt;
+    if (cnt >= kSpFixRowsWide) {
+        for (unsigned int w = blockIdx.x; w < cnt; w += gridDim.x) {
+            const int64_t row = a.fix_list[w];
+            if (!FS_IDX_OK(row, a.nr, 40)) continue;     // block-uniform
+            const int64_t O = row / kSB;
+            const float2 r = fix_fold<D>(a, row, a.lists + a.row_off[O], 0, a.counts[O], s_part);
+            if (threadIdx.x == 0) fix_write<D>(a, row, r.x, r.y);
+        }
+    }
+    fix_done(a, cnt);
+}
+
+template <int D>
+__global__ void __cluster_dims__(kSpFixCluster, 1, 1) __launch_bounds__(256)
+    k_sp_fix_split(const __grid_constant__ SpHalfArgs a) {
+    __shared__ unsigned int s_cnt;
+    __shared__ float2 s_part[8];
+    __shared__ float2 s_cta;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const unsigned int cid = blockIdx.x / kSpFixCluster, ncl = gridDim.x / kSpFixCluster;
+    if (threadIdx.x == 0) s_cnt = min(*(volatile unsigned int*)&a.fix_count[0], (unsigned int)a.nr);
+    __syncthreads();
+    const unsigned int cnt = s_cnt;   // the same in every CTA: written by an earlier launch
+    if (cnt < kSpFixRowsWide) {
+        for (unsigned int w = cid; w < cnt; w += ncl) {
+            const int64_t row = a.fix_list[w];
+            if (!FS_IDX_OK(row, a.nr, 40)) continue;     // cluster-uniform
+            const int64_t O = row / kSB;
+            const int L = a.counts[O];
+            const int eb = (int)((int64_t)L * rank / kSpFixCluster);
+            const int ee = (int)((int64_t)L * (rank + 1) / kSpFixCluster);
+            const float2 r = fix_fold<D>(a, row, a.lists + a.row_off[O], eb, ee, s_part);
+            if (threadIdx.x == 0) s_cta = r;
+            cluster.sync();   // every CTA's s_cta is written
+            if (rank == 0 && threadIdx.x == 0) {
+                float Mf = -INFINITY, Sf = 0.f;
+                for (int q = 0; q < kSpFixCluster; ++q) {
+                    const float2 pr = *cluster.map_shared_rank(&s_cta, q);
+                    if (pr.x != -INFINITY) lse_merge(Mf, Sf, pr.x, pr.y);
+                }
+                fix_write<D>(a, row, Mf, Sf);
+            }
+            cluster.sync();   // s_cta is free again
+        }
+    }
+    fix_done(a, cnt);
 }
 
 // Capacities of the kept-list rows and their offsets (one block, 1024
@@ -2035,9 +2117,10 @@ fs_status sparse_half(Call& c, const SpBufs& B, const SpLists& LS, const SpSide&
     FS_CUDA(cudaGetLastError());
     if (ref) {
         with_pad_dim(D, [&](auto dd) {
-            k_sp_fix<decltype(dd)::value><<<kSpFixBlocks, 256, 0, c.stream>>>(h);
+            k_sp_fix_rows<decltype(dd)::value><<<kSpFixBlocks, 256, 0, c.stream>>>(h);
+            k_sp_fix_split<decltype(dd)::value><<<kSpFixClusterBlocks, 256, 0, c.stream>>>(h);
         });
-        count_launch();
+        count_launch(2);
         FS_CUDA(cudaGetLastError());
     }
     return FS_OK;
