@@ -254,6 +254,26 @@ def test_reference_offsets_above_three_dimensions_match_oracle(d, eps):
         assert rep["fixed_rows"] > 0
 
 
+def test_reference_offsets_with_many_fixups_match_oracle():
+    """A cold start with reference offsets (online_iters = -1) at eps = 5e-5:
+    more than 2000 of the 8000 rows start over 250 log2 units from their LSE
+    (checked on the oracle), so the first update lists more than 1216 rows
+    and the fixup runs one CTA per row instead of a cluster per row."""
+    eps, tau = 5e-5, 1e-6
+    inp = make_inputs("c2_n10k_d3", n=8000, m=7600, d=2)
+    f1, _, _ = bsp.solve(inp["X"], inp["a"], inp["Y"], inp["b"], eps, 0, 1, tau)
+    gap = -f1 / (orc.as_eps(eps) * np.log(2.0))
+    assert (gap < -250).sum() > 2000
+    t = to_dev(inp)
+    f, g, rep = fs.fs_sparse_solve(t["X"], t["a"], t["Y"], t["b"], eps, coarse_iters=0,
+                                   max_iters=4, tau=tau, online_iters=-1)
+    fr, gr, _ = bsp.solve(inp["X"], inp["a"], inp["Y"], inp["b"], eps, 0, 4, tau)
+    C = orc.cost(inp["X"], inp["Y"])
+    assert max_abs(np64(f), fr) <= F_TOL_FMA * C.max()
+    assert max_abs(np64(g), gr) <= F_TOL_FMA * C.max()
+    assert rep["fixed_rows"] > 1216
+
+
 def test_screened_solve_with_lognormal_weights_matches_oracle():
     """Non-uniform weights: block weights, and with them the per-block
     thresholds, vary across the blocks."""
