@@ -14,6 +14,8 @@
 #include "fs_debug.cuh"
 #include "fs_internal.cuh"
 
+#include <cooperative_groups.h>
+
 #include <algorithm>
 #include <type_traits>
 
@@ -684,8 +686,22 @@ __device__ __forceinline__ bool grid_barrier(unsigned int* bar, unsigned int& ge
     return s_ok != 0;
 }
 
-template <int D, int RP>
-__global__ void __launch_bounds__(kThreads, 3) k_solve_small(SmallArgs s) {
+// The barrier between phases: the grid barrier above, or, when the whole
+// grid is one thread-block cluster (at most 16 blocks), the cluster's
+// hardware barrier, whose release/acquire orders the blocks' global writes
+// and reads like the grid barrier's.
+template <bool CLUSTER>
+__device__ __forceinline__ bool phase_barrier(const SmallArgs& s, unsigned int& gen) {
+    if (CLUSTER) {
+        cooperative_groups::this_cluster().sync();
+        ++gen;
+        return true;
+    }
+    return grid_barrier(s.bar, gen, s.err, s.timeout_ns);
+}
+
+template <int D, int RP, bool CLUSTER>
+__global__ void __launch_bounds__(kThreads, 3) k_solve_small(const __grid_constant__ SmallArgs s) {
     unsigned int gen = 0;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -700,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_solve_small(SmallArgs s) {
                 else half_body<D, RP, 0>(a, rb, sp);
             }
             if (a.splits > 1) {
-                if (!grid_barrier(s.bar, gen, s.err, s.timeout_ns)) return;
+                if (!phase_barrier<CLUSTER>(s, gen)) return;
                 const int64_t slots = a.nr * s.lanes[side];
                 for (int64_t t0 = (int64_t)blockIdx.x * kThreads; t0 < slots;
                      t0 += (int64_t)gridDim.x * kThreads)
@@ -708,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_solve_small(SmallArgs s) {
                                a.pot, a.rows + D, fma_stride(D), ref ? a.fix_list : nullptr,
                                ref ? a.fix_count : nullptr, s.lanes[side]);
             }
-            if (!grid_barrier(s.bar, gen, s.err, s.timeout_ns)) return;
+            if (!phase_barrier<CLUSTER>(s, gen)) return;
             if (ref) {
                 // the other side's list was read completely before this point
                 if (blockIdx.x == 0 && tid == 0) {
@@ -730,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_solve_small(SmallArgs s) {
                         if (!FS_IDX_OK(row, a.nr, 4)) continue;
                         fix_row<D>(a, row, lane);
                     }
-                    if (!grid_barrier(s.bar, gen, s.err, s.timeout_ns)) return;
+                    if (!phase_barrier<CLUSTER>(s, gen)) return;
                 }
             }
         }
@@ -758,9 +774,41 @@ int solve_small_blocks_t() {
     static std::atomic<int> cached{0};
     int v = cached.load(std::memory_order_relaxed);
     if (v == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, k_solve_small<D, fma_row_pairs(D)>,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, k_solve_small<D, fma_row_pairs(D), false>,
                                                           kThreads, 0) != cudaSuccess || v < 1)
             v = 1;
+        cached.store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+constexpr int kClusterSolveMax = 16;   // blocks of a one-cluster solve (non-portable above 8)
+
+// Largest one-cluster grid the device schedules for the solve kernel (0: none).
+template <int D>
+int cluster_solve_max_t() {
+    static std::atomic<int> cached{-1};
+    int v = cached.load(std::memory_order_relaxed);
+    if (v < 0) {
+        v = 0;
+        const void* fn = (const void*)k_solve_small<D, fma_row_pairs(D), true>;
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+            (void)cudaGetLastError();
+        for (int c = kClusterSolveMax; c >= 2 && v == 0; c /= 2) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)c);
+            cfg.blockDim = dim3(kThreads);
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = (unsigned)c;
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) == cudaSuccess && clusters >= 1) v = c;
+            else (void)cudaGetLastError();
+        }
         cached.store(v, std::memory_order_relaxed);
     }
     return v;
@@ -773,10 +821,27 @@ cudaError_t launch_solve_small_t(const SmallArgs& a, int sms, cudaStream_t s) {
     const int64_t items = std::max(a.row_blocks[0] * a.h[0].splits, a.row_blocks[1] * a.h[1].splits);
     const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(items, (int64_t)solve_small_blocks_t<D>() * sms));
     SmallArgs args = a;
-    void* params[] = {&args};
-    const cudaError_t e = cudaLaunchCooperativeKernel(
-        (const void*)k_solve_small<D, fma_row_pairs(D)>, dim3((unsigned)blocks), dim3(kThreads),
-        params, 0, s);
+    cudaError_t e;
+    if (blocks <= cluster_solve_max_t<D>()) {
+        // the whole grid as one cluster: the same blocks and work items, the
+        // hardware cluster barrier between phases
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)blocks);
+        cfg.blockDim = dim3(kThreads);
+        cfg.stream = s;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = (unsigned)blocks;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, k_solve_small<D, fma_row_pairs(D), true>, args);
+    } else {
+        void* params[] = {&args};
+        e = cudaLaunchCooperativeKernel((const void*)k_solve_small<D, fma_row_pairs(D), false>,
+                                        dim3((unsigned)blocks), dim3(kThreads), params, 0, s);
+    }
     count_launch();
     return e;
 }
