@@ -287,6 +287,9 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idescS = idesc_f16_f32(BM, BN);
+            const uint64_t stage_desc0 = sdesc_sw128(smem_u32(sStage));
+            const uint64_t p_desc0 = sdesc_sw128(smem_u32(sP));
+            const uint64_t vt_desc0 = sdesc_sw128(smem_u32(sVT));
             const uint32_t idescO = idesc_f16_f32(BM, kvN);
             int s = 0;
             uint32_t ph = 0;
@@ -302,15 +305,17 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
                     const uint32_t d_tmem = tmem + (uint32_t)((e < nch ? b : 1) * BN);
                     if (!mbar_wait(&full[s], ph, a.err, ERR_TIMEOUT_MMA)) return false;
                     tc_fence_after();
-                    const uint8_t* st = sStage + s * kStageA;
-                    const uint32_t kh = smem_u32(st), kl = kh + CHUNK_BYTES;
-                    const uint32_t qh = kh + 2 * CHUNK_BYTES, ql = kh + 3 * CHUNK_BYTES;
+                    // descriptors: the start-address field counts 16-byte units, so a
+                    // 32-byte K step is + 2 and a chunk + CHUNK_BYTES / 16
+                    const uint64_t kh = stage_desc0 + (uint64_t)(s * (kStageA >> 4));
+                    const uint64_t kl = kh + (CHUNK_BYTES >> 4);
+                    const uint64_t qh = kh + 2 * (CHUNK_BYTES >> 4), ql = kh + 3 * (CHUNK_BYTES >> 4);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint32_t o = kk * 32;
-                        mma_f16(d_tmem, sdesc_sw128(qh + o), sdesc_sw128(kh + o), idescS, (c | kk) != 0);
-                        mma_f16(d_tmem, sdesc_sw128(qh + o), sdesc_sw128(kl + o), idescS, 1);
-                        mma_f16(d_tmem, sdesc_sw128(ql + o), sdesc_sw128(kh + o), idescS, 1);
+                        const uint64_t o = 2 * kk;
+                        mma_f16(d_tmem, qh + o, kh + o, idescS, (c | kk) != 0);
+                        mma_f16(d_tmem, qh + o, kl + o, idescS, 1);
+                        mma_f16(d_tmem, ql + o, kh + o, idescS, 1);
                     }
                     mma_commit(&empty[s]);
                     if (++s == kApplyStages) {
@@ -330,15 +335,13 @@ __global__ void __launch_bounds__(kApplyThreads, 1) k_apply_tc(TcApplyArgs a) {
                     break;
                 }
                 tc_fence_after();
-                const uint8_t* vslot = sVT + (t % VS) * kVtSlot;
+                const uint64_t vd = vt_desc0 + (uint64_t)((t % VS) * (kVtSlot >> 4));
 #pragma unroll
                 for (int kq = 0; kq < 2; ++kq)
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        mma_f16(tmem + kOCol,
-                                sdesc_sw128(smem_u32(sP + kq * CHUNK_BYTES) + kk * 32),
-                                sdesc_sw128(smem_u32(vslot + kq * kvN * 128) + kk * 32), idescO,
-                                (t | kq | kk) != 0);
+                        mma_f16(tmem + kOCol, p_desc0 + (uint64_t)(kq * (CHUNK_BYTES >> 4) + 2 * kk),
+                                vd + (uint64_t)(kq * kvN * 8 + 2 * kk), idescO, (t | kq | kk) != 0);
                 mma_commit(pempty);
                 mma_commit(&vempty[t % VS]);
             }

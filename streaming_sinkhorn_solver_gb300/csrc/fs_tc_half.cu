@@ -202,10 +202,11 @@ __global__ void __launch_bounds__(kHalfThreads, 1) k_half_tc(TcHalfArgs a) {
                     const uint8_t* st = sStage + s * STAGE_BYTES;
                     const uint32_t aaddr = smem_u32(QRES ? sQ + c * CHUNK_BYTES : st + CHUNK_BYTES);
                     const uint32_t baddr = smem_u32(st);
+                    // the start-address field counts 16-byte units: a 32-byte step is + 2
+                    const uint64_t ad0 = sdesc_sw128(aaddr), bd0 = sdesc_sw128(baddr);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        mma_f16(d_tmem, sdesc_sw128(aaddr + kk * 32), sdesc_sw128(baddr + kk * 32),
-                                idesc, (c | kk) != 0);
+                        mma_f16(d_tmem, ad0 + 2 * kk, bd0 + 2 * kk, idesc, (c | kk) != 0);
                     mma_commit(&empty[s]);
                     if (++s == stages) {
                         s = 0;

@@ -281,10 +281,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(half_threads(REF), 1
                     const uint8_t* st = sStage + s * STAGE_BYTES;
                     const uint32_t aaddr = smem_u32(QRES ? sQ + c * CHUNK_BYTES : st + CHUNK_BYTES);
                     const uint32_t baddr = smem_u32(st);
+                    // the start-address field counts 16-byte units: a 32-byte step is + 2
+                    const uint64_t ad0 = sdesc_sw128(aaddr), bd0 = sdesc_sw128(baddr);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        mma_f16_pair(d_tmem, sdesc_sw128(aaddr + kk * 32),
-                                     sdesc_sw128(baddr + kk * 32), idesc, REF || (c | kk) != 0);
+                        mma_f16_pair(d_tmem, ad0 + 2 * kk, bd0 + 2 * kk, idesc, REF || (c | kk) != 0);
                     mma_commit_pair(&empty[s], 3);
                     if (++s == stages) {
                         s = 0;
