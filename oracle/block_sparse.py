@@ -45,6 +45,16 @@ the plainest reading of its sections, written out in float64 numpy:
   = 1/16 + 2^-16 (|max_I psi| + |max_J chi| + |Delta|^2 L/eps) is a slack in
   favour of keeping, so the float32 evaluation on the GPU never omits a block
   the exact bound keeps.  tau = 0 keeps every block.
+* *Can the lifted solution be trusted*: a sample of points is checked
+  against its marginal; if the lifted potentials pass, the fine stage
+  starts, else the centroid stage runs more iterations.
+  Reading: the sample is ``lift_samples`` points of X evenly spaced in
+  Morton order (position floor(s n / S)); the statistic is the mean over
+  the sample of |(P 1)_i / a_i - 1| for the dense plan at the lifted (f, g),
+  i.e. |2^{(f_i - f'_i) L/eps} - 1| with f'_i the dense f-update of point
+  i (every column); the lift passes when it is at most ``lift_tol``, and
+  otherwise another ``coarse_iters`` centroid iterations run from the
+  centroid potentials reached, at most ``lift_rounds`` times.
 * The kept blocks are then iterated: the f-update over the kept blocks of its
   row block, then the g-update over the kept blocks of its column block.  The
   row residual |P 1 - a|_1 of the block-sparse plan (measured with a fresh
@@ -57,7 +67,7 @@ from typing import Dict, Optional, Tuple
 
 import numpy as np
 
-from . import as_eps, cost, sinkhorn
+from . import as_eps, cost, f_update_rows, sinkhorn
 
 MORTON_BITS = 21            # cells per axis 2^21 for d <= 3 (morton_bits for larger d)
 BLOCK = 128
@@ -139,13 +149,30 @@ def block_stats(Ps, ws, block: int = BLOCK) -> Tuple[np.ndarray, np.ndarray]:
     return (S / W[:, None]).astype(np.float32), W.astype(np.float32)
 
 
-def coarse_potentials(Xs, as_, Ys, bs, eps, iters, block: int = BLOCK):
+def coarse_potentials(Xs, as_, Ys, bs, eps, iters, block: int = BLOCK, F0=None, G0=None):
     """Coarse stage: Sinkhorn between the block centroids (weights = block
-    weights), then every point inherits its block's potential."""
+    weights), from (F0, G0) (zeros by default), then every point inherits its
+    block's potential.  Returns (f, g, (cx, wx, cy, wy), (F, G))."""
     cx, wx = block_stats(Xs, as_, block)
     cy, wy = block_stats(Ys, bs, block)
-    F, G = sinkhorn(cost(cx, cy), wx, wy, eps, iters)
-    return F[block_ids(len(Xs), block)], G[block_ids(len(Ys), block)], (cx, wx, cy, wy)
+    F, G = sinkhorn(cost(cx, cy), wx, wy, eps, iters, F0, G0)
+    return (F[block_ids(len(Xs), block)], G[block_ids(len(Ys), block)], (cx, wx, cy, wy),
+            (F, G))
+
+
+def lift_sample(n: int, samples: int) -> np.ndarray:
+    """Positions (in Morton order) of the points the lift check samples."""
+    s = min(int(samples), n)
+    return (np.arange(s, dtype=np.int64) * n) // s
+
+
+def lift_error(Xs, Ys, bs, eps, fs, gs, rows) -> float:
+    """Mean over the sampled rows of |(P 1)_i / a_i - 1| for the dense plan
+    at (fs, gs): (P 1)_i / a_i = exp((f_i - f'_i) / eps), f' the dense
+    f-update (every column) from gs."""
+    f_new = f_update_rows(Xs, Ys, bs, eps, gs, rows)
+    r = np.exp((np.asarray(fs, np.float64)[rows] - f_new) / as_eps(eps))
+    return float(np.mean(np.abs(r - 1.0)))
 
 
 # ---------------------------------------------------------------------------
@@ -249,10 +276,12 @@ def row_residual(C, as_, bs, eps, fs, gs, keep_x, block: int = BLOCK) -> float:
 
 def solve(X, a, Y, b, eps, coarse_iters: int, max_iters: int, tau: float,
           target: float = 0.0, check_every: int = 0, f0=None, g0=None,
-          block: int = BLOCK) -> Tuple[np.ndarray, np.ndarray, Dict]:
+          block: int = BLOCK, lift_samples: int = 0, lift_tol: float = 0.0,
+          lift_rounds: int = 0) -> Tuple[np.ndarray, np.ndarray, Dict]:
     """The whole solver: Morton order, coarse stage (or the caller's f0, g0
-    when coarse_iters == 0), block-sparse iterations with the stopping test,
-    and the final residual.  Returns (f, g, report) in the caller's order."""
+    when coarse_iters == 0) with the lift check (lift_samples > 0), block-
+    sparse iterations with the stopping test, and the final residual.
+    Returns (f, g, report) in the caller's order."""
     X = np.asarray(X, np.float32)
     Y = np.asarray(Y, np.float32)
     a = np.asarray(a, np.float32)
@@ -261,15 +290,25 @@ def solve(X, a, Y, b, eps, coarse_iters: int, max_iters: int, tau: float,
     Xs, as_, Ys, bs = X[px], a[px], Y[py], b[py]
     cx, wx = block_stats(Xs, as_, block)
     cy, wy = block_stats(Ys, bs, block)
+    lift_checks, lift_err = 0, -1.0
     if coarse_iters > 0:
-        fs, gs, _ = coarse_potentials(Xs, as_, Ys, bs, eps, coarse_iters, block)
+        fs, gs, _, (F, G) = coarse_potentials(Xs, as_, Ys, bs, eps, coarse_iters, block)
+        if lift_samples > 0:
+            rows = lift_sample(len(Xs), lift_samples)
+            lift_err = lift_error(Xs, Ys, bs, eps, fs, gs, rows)
+            lift_checks = 1
+            while lift_err > lift_tol and lift_checks <= lift_rounds:
+                fs, gs, _, (F, G) = coarse_potentials(Xs, as_, Ys, bs, eps, coarse_iters, block,
+                                                      F, G)
+                lift_err = lift_error(Xs, Ys, bs, eps, fs, gs, rows)
+                lift_checks += 1
     else:
         fs = np.zeros(len(X)) if f0 is None else np.asarray(f0, np.float64)[px]
         gs = np.zeros(len(Y)) if g0 is None else np.asarray(g0, np.float64)[py]
     C = cost(Xs, Ys)
     nI, nJ = len(cx), len(cy)
     rep = {"iters": 0, "kept_blocks": 0, "kept_pairs": 0, "halves": 0,
-           "blocks_x": nI, "blocks_y": nJ}
+           "blocks_x": nI, "blocks_y": nJ, "lift_checks": lift_checks, "lift_error": lift_err}
     sx = np.minimum(block, len(X) - np.arange(nI) * block)
     sy = np.minimum(block, len(Y) - np.arange(nJ) * block)
 

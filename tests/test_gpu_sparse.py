@@ -314,8 +314,8 @@ def test_coarse_stage_alone_matches_oracle():
     f, g, rep = fs.fs_sparse_solve(t["X"], t["a"], t["Y"], t["b"], 0.01, coarse_iters=40,
                                    max_iters=0, tau=1e-6)
     px, py = bsp.morton_order(inp["X"], inp["Y"])
-    fs_, gs_, (cx, wx, cy, wy) = bsp.coarse_potentials(inp["X"][px], inp["a"][px], inp["Y"][py],
-                                                       inp["b"][py], 0.01, 40)
+    fs_, gs_, (cx, wx, cy, wy), _ = bsp.coarse_potentials(inp["X"][px], inp["a"][px],
+                                                          inp["Y"][py], inp["b"][py], 0.01, 40)
     fr = np.empty(3000)
     gr = np.empty(2700)
     fr[px], gr[py] = fs_, gs_

@@ -130,10 +130,66 @@ def test_block_stats_weighted_mean():
 
 def test_coarse_stage_with_one_point_per_cell_is_the_dense_solve():
     c = random_cloud(40, 33, 2, 6, weights="random")
-    f, g, _ = bsp.coarse_potentials(c["X"], c["a"], c["Y"], c["b"], 0.1, 15, block=1)
+    f, g, _, _ = bsp.coarse_potentials(c["X"], c["a"], c["Y"], c["b"], 0.1, 15, block=1)
     fr, gr = orc.sinkhorn(orc.cost(c["X"], c["Y"]), c["a"], c["b"], 0.1, 15)
     np.testing.assert_allclose(f, fr, rtol=0, atol=1e-12)
     np.testing.assert_allclose(g, gr, rtol=0, atol=1e-12)
+
+
+# --- the lift check --------------------------------------------------------------
+
+def test_lift_sample_positions_are_evenly_spaced_and_distinct():
+    assert list(bsp.lift_sample(10, 4)) == [0, 2, 5, 7]
+    assert list(bsp.lift_sample(3, 8)) == [0, 1, 2]
+    r = bsp.lift_sample(1000, 64)
+    assert len(np.unique(r)) == 64 and r.min() == 0 and r.max() < 1000
+
+
+def test_lift_error_is_the_sampled_relative_row_marginal_error():
+    """Against the dense oracle's plan marginals (P 1 summed from the plan
+    entries), not the f-update identity the check uses."""
+    c = random_cloud(300, 260, 3, 12, weights="random")
+    C = orc.cost(c["X"], c["Y"])
+    f, g = orc.sinkhorn(C, c["a"], c["b"], 0.1, 3)
+    f = f + 0.01 * np.sin(np.arange(300))          # away from an f-update's exact rows
+    rows = bsp.lift_sample(300, 37)
+    r, _ = orc.marginals(C, c["a"], c["b"], 0.1, f, g)
+    want = np.mean(np.abs(r[rows] / c["a"][rows].astype(np.float64) - 1.0))
+    got = bsp.lift_error(c["X"], c["Y"], c["b"], 0.1, f, g, rows)
+    assert got == pytest.approx(want, rel=1e-10)
+    # after an f-update the rows are exact
+    f1 = orc.f_update(C, c["b"], 0.1, g)
+    assert bsp.lift_error(c["X"], c["Y"], c["b"], 0.1, f1, g, rows) < 1e-12
+
+
+def test_coarse_stage_continues_like_one_longer_solve():
+    """Two rounds of k centroid iterations, the second from where the first
+    stopped, are 2k iterations from zero: the lift check's extra rounds."""
+    inp = make_inputs("c2_n10k_d3", n=1500, m=1300)
+    px, py = bsp.morton_order(inp["X"], inp["Y"])
+    args = (inp["X"][px], inp["a"][px], inp["Y"][py], inp["b"][py], 0.01)
+    _, _, _, (F1, G1) = bsp.coarse_potentials(*args, 7)
+    f2, g2, _, _ = bsp.coarse_potentials(*args, 7, F0=F1, G0=G1)
+    f14, g14, _, _ = bsp.coarse_potentials(*args, 14)
+    np.testing.assert_allclose(f2, f14, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(g2, g14, rtol=0, atol=1e-12)
+
+
+def test_lift_check_rounds():
+    """A loose tolerance passes the first check and changes nothing; a zero
+    tolerance runs every extra round, which is the longer centroid solve."""
+    inp = make_inputs("c2_n10k_d3", n=1500, m=1300)
+    args = (inp["X"], inp["a"], inp["Y"], inp["b"], 0.01)
+    f0, g0, r0 = bsp.solve(*args, 5, 3, 1e-6)
+    f1, g1, r1 = bsp.solve(*args, 5, 3, 1e-6, lift_samples=200, lift_tol=1e9, lift_rounds=4)
+    assert r1["lift_checks"] == 1 and r0["lift_checks"] == 0
+    np.testing.assert_array_equal(f1, f0)
+    f2, g2, r2 = bsp.solve(*args, 5, 3, 1e-6, lift_samples=200, lift_tol=0.0, lift_rounds=2)
+    f3, g3, _ = bsp.solve(*args, 15, 3, 1e-6)
+    assert r2["lift_checks"] == 3
+    np.testing.assert_allclose(f2, f3, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(g2, g3, rtol=0, atol=1e-12)
+    assert r2["lift_error"] > 0.0
 
 
 # --- the block bound and the screening -----------------------------------------
@@ -283,6 +339,10 @@ MUTANTS = [
      "mask = keep_y[block_ids(C.shape[1], block)][:, block_ids(C.shape[0], block)]",
      "mask = keep_y[block_ids(C.shape[1], block)][:, block_ids(C.shape[0], block)[::-1]]"),
     ("screen_y_not_transposed", 'if side == "y":', "if False:"),
+    ("lift_error_sign", "r = np.exp((np.asarray(fs, np.float64)[rows] - f_new) / as_eps(eps))",
+     "r = np.exp((f_new - np.asarray(fs, np.float64)[rows]) / as_eps(eps))"),
+    ("lift_restarts_from_zero", "F, G = sinkhorn(cost(cx, cy), wx, wy, eps, iters, F0, G0)",
+     "F, G = sinkhorn(cost(cx, cy), wx, wy, eps, iters)"),
 ]
 
 PINS = [
@@ -294,6 +354,8 @@ PINS = [
     lambda: test_block_bound_of_single_points_is_the_plan_entry(),
     lambda: test_screening_bounds_the_omitted_mass_per_block(1e-2),
     lambda: test_masked_updates_make_the_kept_marginals_exact(),
+    lambda: test_lift_error_is_the_sampled_relative_row_marginal_error(),
+    lambda: test_coarse_stage_continues_like_one_longer_solve(),
 ]
 
 
