@@ -374,6 +374,13 @@ fs_status fs_unit_rates(double* out, void* stream);
  *   - Coarse stage: coarse_iters dense Sinkhorn iterations (the same update)
  *     between the blocks' weight-averaged centroids with the blocks' weights;
  *     every point takes its block's potential.
+ *   - Lift check (lift_samples > 0): lift_samples points of X evenly spaced
+ *     in Morton order (position floor(s n / S)); the error is the mean over
+ *     them of |(P 1)_i / a_i - 1| for the dense plan at the lifted (f, g)
+ *     (every column), i.e. |2^{(f_i - f'_i) L/eps} - 1| with f' the dense
+ *     f-update; while it exceeds lift_tol, another coarse_iters centroid
+ *     iterations run from the centroid potentials reached and the lift is
+ *     checked again, at most lift_rounds times.
  *   - Screening, before every half-update: with Delta = c_I - c_J and offsets
  *     u_i = x_i - c_I, v_j = y_j - c_J from the block centroids, block pair
  *     (I, J) carries at most 2^U of plan mass,
@@ -401,7 +408,9 @@ typedef struct fs_sparse_options {
     int32_t online_iters;  /* fine iterations that take the running max as the exponent
                               offset before each row's previous LSE is used (a guarded
                               sum, rows outside the range recomputed): 0 = 2, -1 = none */
-    int32_t reserved[3];   /* must be zero */
+    int32_t lift_samples;  /* points of the lift check (0: no check) */
+    int32_t lift_rounds;   /* further centroid rounds the check may ask for */
+    float lift_tol;        /* the lift passes when its sampled error is at most this */
 } fs_sparse_options;
 
 typedef struct fs_sparse_report {
@@ -415,6 +424,9 @@ typedef struct fs_sparse_report {
                               (the rest were decided by the block-level bound) */
     double fixed_rows;     /* rows whose guarded sum left its range and were
                               recomputed with the online max, summed over passes */
+    int32_t lift_checks;   /* lift checks run (0 without the check) */
+    int32_t reserved;
+    double lift_error;     /* the last check's sampled error (-1 without the check) */
 } fs_sparse_report;
 
 /*
@@ -436,8 +448,8 @@ typedef struct fs_sparse_report {
  * Errors: FS_ERR_UNSUPPORTED for d > 8, more than 2^32 super-block pairs,
  * or tau = 0 (every block kept) above 2^30 block pairs; FS_ERR_OOM when the
  * kept lists do not fit; FS_ERR_INVALID_ARG for null pointers, sizes < 1,
- * eps <= 0, tau outside [0, 1), negative counts or target, or non-zero
- * reserved fields.
+ * eps <= 0, tau outside [0, 1), negative counts or target, a negative or
+ * non-finite lift_tol, or a lift check without a coarse stage.
  */
 fs_status fs_sparse_solve(const float* X, const float* a, int64_t n,
                           const float* Y, const float* b, int64_t m, int32_t d, float eps,

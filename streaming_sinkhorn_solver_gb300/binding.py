@@ -59,7 +59,8 @@ class fs_sparse_options(ctypes.Structure):
     _fields_ = [("coarse_iters", ctypes.c_int32), ("max_iters", ctypes.c_int32),
                 ("check_every", ctypes.c_int32), ("tau", ctypes.c_float),
                 ("target", ctypes.c_float), ("online_iters", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 3)]
+                ("lift_samples", ctypes.c_int32), ("lift_rounds", ctypes.c_int32),
+                ("lift_tol", ctypes.c_float)]
 
 
 class fs_sparse_report(ctypes.Structure):
@@ -67,7 +68,8 @@ class fs_sparse_report(ctypes.Structure):
                 ("blocks_x", ctypes.c_int32), ("blocks_y", ctypes.c_int32),
                 ("residual", ctypes.c_double), ("kept_blocks", ctypes.c_double),
                 ("kept_pairs", ctypes.c_double), ("exact_bounds", ctypes.c_double),
-                ("fixed_rows", ctypes.c_double)]
+                ("fixed_rows", ctypes.c_double), ("lift_checks", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("lift_error", ctypes.c_double)]
 
 
 _lib = None
@@ -489,7 +491,8 @@ def fs_sinkhorn_solve_noalloc(X, a, Y, b, eps: float, n_iter: int, f, g, *, stre
 
 def fs_sparse_solve(X, a, Y, b, eps: float, *, coarse_iters: int = 0, max_iters: int = 100,
                     tau: float = 1e-6, target: float = 0.0, check_every: int = 0, f=None, g=None,
-                    online_iters: int = 0, stream=None):
+                    online_iters: int = 0, lift_samples: int = 0, lift_tol: float = 0.0,
+                    lift_rounds: int = 0, stream=None):
     """The block-sparse solver (see the C header for the method and its
     readings).  f, g are outputs (and inputs when coarse_iters == 0; zeros if
     None).  Returns (f, g, report) with report a dict of fs_sparse_report."""
@@ -503,6 +506,7 @@ def fs_sparse_solve(X, a, Y, b, eps: float, *, coarse_iters: int = 0, max_iters:
     o.coarse_iters, o.max_iters, o.check_every = int(coarse_iters), int(max_iters), int(check_every)
     o.tau, o.target = float(tau), float(target)
     o.online_iters = int(online_iters)
+    o.lift_samples, o.lift_rounds, o.lift_tol = int(lift_samples), int(lift_rounds), float(lift_tol)
     rep = fs_sparse_report()
     st = load_library().fs_sparse_solve(
         _ptr(X, "X", (n, d)), _ptr(a, "a", (n,)), n, _ptr(Y, "Y", (m, d)), _ptr(b, "b", (m,)), m, d,

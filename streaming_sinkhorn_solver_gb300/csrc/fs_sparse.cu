@@ -1803,6 +1803,11 @@ struct SpBufs {
     size_t slist, scount, sculled;   // super-block cull
     // coarse stage
     size_t cshift, cPX, cPY, cnx, cny, clx, cly, cpart, F, G;
+    // lift check: sampled records, norms, log2-weights, lifted and updated
+    // potentials, split partials
+    size_t lift_rec, lift_norm, lift_lw, lift_pot, lift_new, lift_part;
+    int64_t lift_S = 0, lift_cps = 0;
+    int lift_splits = 1;
     int csplits_f, csplits_g;
     int64_t ccps_f, ccps_g;
 };
@@ -1852,7 +1857,8 @@ void layout_side(Layout& L, SpSide& s, int64_t cnt, int d) {
     s.slw = L.take(sizeof(float) * s.nsb);
 }
 
-void layout_sparse(Layout& L, SpBufs& B, int64_t n, int64_t m, int d, int sms, bool coarse) {
+void layout_sparse(Layout& L, SpBufs& B, int64_t n, int64_t m, int d, int sms, bool coarse,
+                   int64_t lift_samples = 0) {
     const int64_t mx = std::max(n, m);
     layout_morton(L, B.srt, n, m, d);
     B.shift_part = L.take(sizeof(double) * (size_t)kShiftBlocks * d);
@@ -1893,6 +1899,18 @@ void layout_sparse(Layout& L, SpBufs& B, int64_t n, int64_t m, int d, int sms, b
         B.cpart = L.take(sizeof(float2) * std::max(nx * B.csplits_f, ny * B.csplits_g));
         B.F = L.take(sizeof(float) * nx);
         B.G = L.take(sizeof(float) * ny);
+        if (lift_samples > 0) {
+            const int64_t S = std::min<int64_t>(lift_samples, n);
+            B.lift_S = S;
+            B.lift_splits = choose_splits((S + rpb - 1) / rpb, m, sms, per_sm, 128, nullptr,
+                                          &B.lift_cps);
+            B.lift_rec = L.take(sizeof(float) * (size_t)S * B.X.rs);
+            B.lift_norm = L.take(sizeof(float) * S);
+            B.lift_lw = L.take(sizeof(float) * S);
+            B.lift_pot = L.take(sizeof(float) * S);
+            B.lift_new = L.take(sizeof(float) * S);
+            B.lift_part = L.take(sizeof(float2) * (size_t)S * B.lift_splits);
+        }
     }
 }
 
@@ -2142,7 +2160,9 @@ fs_status measure_residual(Call& c, const SpBufs& B, SpLists& LS, int D, float e
 
 // Coarse stage: dense Sinkhorn between the block centroids (FMA path,
 // online offsets), then the lift into the sorted potentials.
-fs_status coarse_stage(Call& c, SpBufs& B, int d, float eps, int iters) {
+// resume: continue from the centroid potentials (and packed biases) the last
+// call left, instead of from zero.
+fs_status coarse_stage(Call& c, SpBufs& B, int d, float eps, int iters, bool resume = false) {
     NvtxRange nvtx("fs coarse stage (block-sparse)");
     const int D = fma_pad_dim(d);
     const int DS = fma_stride(D);
@@ -2152,17 +2172,19 @@ fs_status coarse_stage(Call& c, SpBufs& B, int d, float eps, int iters) {
     const float eps_ln2 = (float)((double)eps * kLn2);
     float* F = c.at<float>(B.F);
     float* G = c.at<float>(B.G);
-    FS_CUDA(cudaMemsetAsync(G, 0, sizeof(float) * ny, c.stream));
-    const float* cx = c.at<float>(B.X.cenf);
-    const float* cy = c.at<float>(B.Y.cenf);
-    FS_CUDA(launch_shift(cx, nx, cy, ny, d, c.at<double>(B.shift_part), kShiftBlocks,
-                         c.at<float>(B.cshift), c.stream));
     float* PX = c.at<float>(B.cPX);
     float* PY = c.at<float>(B.cPY);
-    FS_CUDA(launch_pack_fma(cx, c.at<float>(B.X.W), nullptr, nx, d, D, c.at<float>(B.cshift),
-                            l_over_eps, PX, c.at<float>(B.cnx), c.at<float>(B.clx), c.stream));
-    FS_CUDA(launch_pack_fma(cy, c.at<float>(B.Y.W), G, ny, d, D, c.at<float>(B.cshift), l_over_eps,
-                            PY, c.at<float>(B.cny), c.at<float>(B.cly), c.stream));
+    if (!resume) {
+        FS_CUDA(cudaMemsetAsync(G, 0, sizeof(float) * ny, c.stream));
+        const float* cx = c.at<float>(B.X.cenf);
+        const float* cy = c.at<float>(B.Y.cenf);
+        FS_CUDA(launch_shift(cx, nx, cy, ny, d, c.at<double>(B.shift_part), kShiftBlocks,
+                             c.at<float>(B.cshift), c.stream));
+        FS_CUDA(launch_pack_fma(cx, c.at<float>(B.X.W), nullptr, nx, d, D, c.at<float>(B.cshift),
+                                l_over_eps, PX, c.at<float>(B.cnx), c.at<float>(B.clx), c.stream));
+        FS_CUDA(launch_pack_fma(cy, c.at<float>(B.Y.W), G, ny, d, D, c.at<float>(B.cshift),
+                                l_over_eps, PY, c.at<float>(B.cny), c.at<float>(B.cly), c.stream));
+    }
     float2* part = c.at<float2>(B.cpart);
     HalfArgs hf{PX, PY, nx, ny, kappa, eps_ln2, c.at<float>(B.cnx), c.at<float>(B.clx), F, part,
                 B.csplits_f, B.ccps_f, 0, nullptr, nullptr};
@@ -2186,6 +2208,81 @@ fs_status coarse_stage(Call& c, SpBufs& B, int d, float eps, int iters) {
 }
 
 constexpr int kSpOnlineIters = 2;
+
+// Lift check: the sampled points' FMA records, norms, log2-weights and
+// lifted potentials, gathered from their positions floor(s n / S) in Morton
+// order.
+__global__ void k_sp_lift_gather(const float* __restrict__ rec, const float* __restrict__ norm,
+                                 const float* __restrict__ logw2, const float* __restrict__ pot,
+                                 int64_t n, int64_t S, int RS, float* __restrict__ srec,
+                                 float* __restrict__ snorm, float* __restrict__ slogw2,
+                                 float* __restrict__ spot) {
+    const int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (s >= S) return;
+    const int64_t k = s * n / S;
+    if (!FS_IDX_OK(k, n, 43)) return;
+    for (int q = 0; q < RS; ++q) srec[s * RS + q] = rec[k * RS + q];
+    snorm[s] = norm[k];
+    slogw2[s] = logw2[k];
+    spot[s] = pot[k];
+}
+
+// Mean over the samples of |2^{(f - f') L/eps} - 1| (f the lifted potential,
+// f' its dense f-update), accumulated in double in a fixed order by one
+// block.
+__global__ void __launch_bounds__(1024) k_sp_lift_error(const float* __restrict__ f,
+                                                        const float* __restrict__ fnew, int64_t S,
+                                                        float l_over_eps, double* __restrict__ out) {
+    __shared__ double part[1024];
+    double acc = 0.0;
+    for (int64_t s = threadIdx.x; s < S; s += blockDim.x) {
+        const double r = exp2((double)(f[s] - fnew[s]) * (double)l_over_eps);
+        acc += fabs(r - 1.0);
+    }
+    part[threadIdx.x] = acc;
+    __syncthreads();
+    for (int w = 512; w; w >>= 1) {
+        if ((int)threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) out[0] = part[0] / (double)S;
+}
+
+// The lift check's sampled error at the current (lifted) potentials: the
+// sampled X records against every column record of Y (whose biases hold the
+// lifted g) through the dense half-update kernel.
+fs_status lift_check(Call& c, const SpBufs& B, int d, float eps, double* err) {
+    NvtxRange nvtx("fs lift check (block-sparse)");
+    const int D = fma_pad_dim(d);
+    const int RS = B.X.rs;
+    const int64_t S = B.lift_S;
+    const float l_over_eps = (float)(kLog2e / (double)eps);
+    float* srec = c.at<float>(B.lift_rec);
+    float* snorm = c.at<float>(B.lift_norm);
+    float* slw = c.at<float>(B.lift_lw);
+    float* spot = c.at<float>(B.lift_pot);
+    float* fnew = c.at<float>(B.lift_new);
+    k_sp_lift_gather<<<grid_for(S, 256), 256, 0, c.stream>>>(
+        c.at<float>(B.X.rec), c.at<float>(B.X.norm), c.at<float>(B.X.lw), c.at<float>(B.X.pot),
+        B.X.cnt, S, RS, srec, snorm, slw, spot);
+    count_launch();
+    FS_CUDA(cudaGetLastError());
+    float2* part = c.at<float2>(B.lift_part);
+    HalfArgs h{srec, c.at<float>(B.Y.rec), S, B.Y.cnt, (float)(2.0 * kLog2e / (double)eps),
+               (float)((double)eps * kLn2), snorm, slw, fnew, part, B.lift_splits, B.lift_cps, 0,
+               nullptr, nullptr};
+    FS_CUDA(launch_half_fma(D, h, c.stream));
+    if (h.splits > 1)
+        FS_CUDA(launch_merge_lse(part, h.splits, S, snorm, slw, h.eps_ln2, fnew, srec + D, RS,
+                                 c.stream));
+    k_sp_lift_error<<<1, 1024, 0, c.stream>>>(spot, fnew, S, l_over_eps, c.at<double>(B.red_out));
+    count_launch();
+    FS_CUDA(cudaGetLastError());
+    FS_CUDA(cudaMemcpyAsync(err, c.at<double>(B.red_out), sizeof(double), cudaMemcpyDeviceToHost,
+                            c.stream));
+    FS_CUDA(cudaStreamSynchronize(c.stream));
+    return FS_OK;
+}
 
 fs_status check_sparse_args(const float* X, const float* a, int64_t n, const float* Y, const float* b,
                             int64_t m, int32_t d, float eps) {
@@ -2227,8 +2324,12 @@ fs_status sparse_solve_entry(const float* X, const float* a, int64_t n, const fl
     FS_TRY(check_keep_all(n, m, opt->tau));
     if (!(opt->target >= 0.f) || !std::isfinite(opt->target))
         return fail(FS_ERR_INVALID_ARG, "target=%g must be finite and >= 0", (double)opt->target);
-    for (int i = 0; i < 3; ++i)
-        if (opt->reserved[i]) return fail(FS_ERR_INVALID_ARG, "fs_sparse_options.reserved must be zero");
+    if (opt->lift_samples < 0 || opt->lift_rounds < 0)
+        return fail(FS_ERR_INVALID_ARG, "lift_samples and lift_rounds must be >= 0");
+    if (!(opt->lift_tol >= 0.f) || !std::isfinite(opt->lift_tol))
+        return fail(FS_ERR_INVALID_ARG, "lift_tol=%g must be finite and >= 0", (double)opt->lift_tol);
+    if (opt->lift_samples > 0 && opt->coarse_iters == 0)
+        return fail(FS_ERR_INVALID_ARG, "the lift check needs a coarse stage (coarse_iters > 0)");
     if (opt->online_iters < -1)
         return fail(FS_ERR_INVALID_ARG, "online_iters=%d must be >= -1", opt->online_iters);
     const int online_iters = opt->online_iters == 0 ? kSpOnlineIters
@@ -2248,7 +2349,7 @@ fs_status sparse_solve_entry(const float* X, const float* a, int64_t n, const fl
     FS_TRY(classify(c, P.g, g, (size_t)m));
     SpBufs B;
     SpLists LS;
-    layout_sparse(c.L, B, n, m, d, c.ws->sms, opt->coarse_iters > 0);
+    layout_sparse(c.L, B, n, m, d, c.ws->sms, opt->coarse_iters > 0, opt->lift_samples);
     FS_TRY(ensure_capacity(c));
     for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g}) bind(c, *A);
     for (Arr* A : {&P.X, &P.a, &P.Y, &P.b, &P.f, &P.g}) FS_TRY(upload(c, *A));
@@ -2269,6 +2370,20 @@ fs_status sparse_solve_entry(const float* X, const float* a, int64_t n, const fl
     }
     FS_TRY(set_bias(c, B.X, D, l_over_eps));
     FS_TRY(set_bias(c, B.Y, D, l_over_eps));
+    // lift check: more centroid rounds while the sampled error is too large
+    int lift_checks = 0;
+    double lift_err = -1.0;
+    if (opt->coarse_iters > 0 && opt->lift_samples > 0) {
+        FS_TRY(lift_check(c, B, d, eps, &lift_err));
+        lift_checks = 1;
+        while (lift_err > (double)opt->lift_tol && lift_checks <= opt->lift_rounds) {
+            FS_TRY(coarse_stage(c, B, d, eps, opt->coarse_iters, true));
+            FS_TRY(set_bias(c, B.X, D, l_over_eps));
+            FS_TRY(set_bias(c, B.Y, D, l_over_eps));
+            FS_TRY(lift_check(c, B, d, eps, &lift_err));
+            ++lift_checks;
+        }
+    }
     timing_end(tp, TIME_PREP, c.stream);
     FS_CUDA(cudaMemsetAsync(c.at<unsigned long long>(B.kept), 0, kWorkCounters * sizeof(unsigned long long),
                             c.stream));
@@ -2329,6 +2444,9 @@ fs_status sparse_solve_entry(const float* X, const float* a, int64_t n, const fl
         rep->kept_pairs = (double)work[1];
         rep->exact_bounds = (double)work[2];
         rep->fixed_rows = (double)work[3];
+        rep->lift_checks = lift_checks;
+        rep->reserved = 0;
+        rep->lift_error = lift_err;
     }
     return end_call(c);
 }

@@ -93,6 +93,7 @@ def test_block_sparse_solve_records_no_bad_index(dbg, n, m, d, tau, online):
     o = fs.fs_sparse_options()
     o.coarse_iters, o.max_iters, o.tau, o.online_iters = 3, 6, tau, online
     o.target, o.check_every = 1e-9, 2
+    o.lift_samples, o.lift_rounds, o.lift_tol = 77, 1, 0.0     # one extra centroid round
     rep = fs.fs_sparse_report()
     st = dbg.fs_sparse_solve(_p(t["X"]), _p(t["a"]), n, _p(t["Y"]), _p(t["b"]), m, d,
                              ctypes.c_float(0.005), ctypes.byref(o), _p(f), _p(g),
@@ -100,6 +101,7 @@ def test_block_sparse_solve_records_no_bad_index(dbg, n, m, d, tau, online):
     assert st == 0, dbg.fs_last_error()
     assert _report(dbg) == 0
     fr, gr, _ = bsp.solve(inp["X"], inp["a"], inp["Y"], inp["b"], 0.005, 3, 6, tau,
-                          target=1e-9, check_every=2)
+                          target=1e-9, check_every=2, lift_samples=77, lift_tol=0.0,
+                          lift_rounds=1)
     C = orc.cost(inp["X"], inp["Y"])
     assert max_abs(f.cpu().numpy(), fr) <= F_TOL_FMA * C.max()

@@ -325,6 +325,33 @@ def test_coarse_stage_alone_matches_oracle():
     assert rep["iters"] == 0
 
 
+@pytest.mark.parametrize("tol,rounds,checks", [(0.0, 2, 3), (1e12, 4, 1)])
+def test_lift_check_matches_oracle(tol, rounds, checks):
+    """The lift check: lift_samples points evenly spaced in Morton order, the
+    mean relative row-marginal error of the dense plan at the lifted
+    potentials; a zero tolerance runs every extra centroid round, a loose one
+    passes at once.  Rounds, error and the potentials after the fine
+    iterations against the oracle."""
+    inp = make_inputs("c2_n10k_d3", n=1500, m=1300)
+    t = to_dev(inp)
+    kw = dict(coarse_iters=5, max_iters=3, tau=1e-6, lift_samples=200, lift_tol=tol,
+              lift_rounds=rounds)
+    f, g, rep = fs.fs_sparse_solve(t["X"], t["a"], t["Y"], t["b"], 0.01, **kw)
+    fr, gr, orep = bsp.solve(inp["X"], inp["a"], inp["Y"], inp["b"], 0.01, 5, 3, 1e-6,
+                             lift_samples=200, lift_tol=tol, lift_rounds=rounds)
+    assert rep["lift_checks"] == orep["lift_checks"] == checks
+    assert rep["lift_error"] == pytest.approx(orep["lift_error"], rel=1e-2)
+    C = orc.cost(inp["X"], inp["Y"])
+    assert max_abs(np64(f), fr) <= F_TOL_FMA * C.max()
+    assert max_abs(np64(g), gr) <= F_TOL_FMA * C.max()
+    if checks == 1:
+        # a check that passes changes nothing
+        f0, g0, rep0 = fs.fs_sparse_solve(t["X"], t["a"], t["Y"], t["b"], 0.01, coarse_iters=5,
+                                          max_iters=3, tau=1e-6)
+        assert rep0["lift_checks"] == 0 and rep0["lift_error"] == -1.0
+        np.testing.assert_array_equal(f.cpu().numpy(), f0.cpu().numpy())
+
+
 def test_stopping_rule_matches_oracle():
     inp = make_inputs("c2_n10k_d3", n=1500, m=1500, d=2)
     t = to_dev(inp)
@@ -372,7 +399,10 @@ def test_invalid_arguments_are_rejected():
         fs.fs_sparse_solve(inp["X"], inp["a"], inp["Y"], inp["b"], 0.1)
     assert e.value.status == fs.FS_ERR_UNSUPPORTED
     inp = to_dev(random_cloud(10, 10, 2, seed=1))
-    for kw in (dict(tau=1.0), dict(tau=-1e-3), dict(max_iters=-1), dict(target=-1.0)):
+    for kw in (dict(tau=1.0), dict(tau=-1e-3), dict(max_iters=-1), dict(target=-1.0),
+               dict(lift_samples=10, coarse_iters=0), dict(lift_samples=10, coarse_iters=2,
+                                                           lift_tol=-1.0),
+               dict(lift_samples=-1, coarse_iters=2)):
         with pytest.raises(fs.FlashSinkhornError) as e:
             fs.fs_sparse_solve(inp["X"], inp["a"], inp["Y"], inp["b"], 0.1, **kw)
         assert e.value.status == fs.FS_ERR_INVALID_ARG
