@@ -929,7 +929,7 @@ __global__ void __launch_bounds__(kApplyThreads) k_apply_fma(ApplyArgs a) {
     const int pk_stride = a.k + 1 + (TAN ? 1 : 0);
     if (a.splits > 1) {
         const int64_t base = ((int64_t)blockIdx.y * a.n + row) * pk_stride;
-        const int64_t plen = (int64_t)a.splits * a.n * pk_stride;
+        [[maybe_unused]] const int64_t plen = (int64_t)a.splits * a.n * pk_stride;   // index checks
         if (blockIdx.z == 0 && FS_IDX_OK(base, plen, 7)) a.partial[base] = M;
         if (TAN && blockIdx.z == 0 && FS_IDX_OK(base + 1 + a.k, plen, 7)) a.partial[base + 1 + a.k] = sig;
         for (int c = 0; c < kw; ++c)
