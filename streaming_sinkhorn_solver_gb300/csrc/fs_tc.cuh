@@ -314,6 +314,28 @@ __device__ __forceinline__ void tma_chunk_pair(void* dst_smem, const void* tmap,
         : "memory");
 }
 
+// L2 eviction-priority policies for the bulk tensor copies' cache hints
+__device__ __forceinline__ uint64_t l2_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// tma_chunk_pair with an L2 cache policy
+__device__ __forceinline__ void tma_chunk_pair_hint(void* dst_smem, const void* tmap, uint32_t row,
+                                                    uint32_t bar_cluster, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst_smem)),
+        "l"(tmap), "r"(0), "r"(row), "r"(bar_cluster), "l"(policy)
+        : "memory");
+}
+
 // one warp in each CTA of the pair, collectively
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(

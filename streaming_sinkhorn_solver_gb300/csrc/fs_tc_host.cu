@@ -20,6 +20,7 @@ struct TcPlan {
     int64_t rtx, rty;           // row tiles of X and Y
     int splits_f, splits_g;
     int tps_f, tps_g;           // column tiles per split
+    int raster_pairs;           // launch-order group of the pair kernel
 };
 
 // Pick the split count that best fills whole waves of one CTA per SM, charging
@@ -71,6 +72,13 @@ TcPlan plan_tc(int64_t n, int64_t m, int32_t d, int sms, const fs_options* opt) 
     // buffers keep both epilogue groups busier.
     p.pair = p.nch > 2;
     const int64_t ct = p.pair ? 2 : 1;   // 128-row tiles per column tile
+    // one group of the pair kernel's launch order.  With resident Q: a quarter
+    // of the pairs resident at once (one CTA per SM), so that a group's Q
+    // tiles stay in L2 beside the K tiles while its column splits run.  A
+    // streamed Q is re-read from L2 for every column tile; there the splits
+    // run one after another (one group), so that the K tiles in use at once
+    // are one split's share.
+    p.raster_pairs = p.qres ? std::max(1, sms / 8) : 0;
     choose_tc_splits(p.rtx, p.rty / ct, sms, opt, &p.splits_f, &p.tps_f);
     choose_tc_splits(p.rty, p.rtx / ct, sms, opt, &p.splits_g, &p.tps_g);
     return p;
@@ -222,6 +230,7 @@ fs_status solve_tc(Call& c, Problem& P, int32_t n_iter, const fs_options* opt) {
     hf.col_tiles = (int)(p.pair ? p.rty / 2 : p.rty);
     hf.tiles_per_split = p.tps_f;
     hf.splits = p.splits_f;
+    hf.raster_pairs = p.raster_pairs;
     hf.stages = p.pair ? pair_stages(p.nch, p.qres) : half_stages(p.nch, p.qres);
     hf.eps_ln2 = eps_ln2;
     hf.rnorm = c.at<float>(B.nx);
@@ -377,6 +386,7 @@ fs_status apply_tc(Call& c, Problem& P, int mode, const fs_options* opt) {
     h.col_tiles = (int)(p.pair ? p.rty / 2 : p.rty);
     h.tiles_per_split = A.lse_tps;
     h.splits = A.lse_splits;
+    h.raster_pairs = p.raster_pairs;
     h.stages = p.pair ? pair_stages(p.nch, p.qres) : half_stages(p.nch, p.qres);
     h.eps_ln2 = (float)(eps * kLn2);
     h.rnorm = nullptr;

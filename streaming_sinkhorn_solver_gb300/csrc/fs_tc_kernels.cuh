@@ -34,6 +34,7 @@ struct TcHalfArgs {
     int tiles_per_split;
     int splits;
     int stages;             // ring depth (from half_stages)
+    int raster_pairs;       // CTA-pair kernel: pairs per launch-order group (0 = all)
     float eps_ln2;
     const float* rnorm;     // |x~|^2 of the rows; nullptr = write log2-sum-exp only
     const float* rlogw2;    // log2 of the row weights

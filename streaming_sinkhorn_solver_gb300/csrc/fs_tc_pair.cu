@@ -105,6 +105,24 @@ __device__ __forceinline__ void fold128(float* v, const float4* sb, uint64_t ks2
     S += (s0 + s1) + (s2 + s3);
 }
 
+// Launch order.  The grid is one-dimensional, row_tiles * splits CTAs, and
+// blocks start roughly in index order.  Consecutive pairs are taken in groups
+// of raster_pairs row-tile pairs (the last group may be shorter); a group runs
+// every column split of its pairs before the next group starts, so its Q tiles
+// are reused from L2 by the later splits instead of being read again from
+// DRAM once every row tile of a split has streamed past.
+__device__ __forceinline__ void pair_tile(int splits, int raster_pairs, int64_t& rt, int& split) {
+    const int64_t pairs = gridDim.x / (2 * (int64_t)splits);
+    const int64_t grp = raster_pairs > 0 ? min((int64_t)raster_pairs, pairs) : pairs;
+    const int64_t L = blockIdx.x >> 1;
+    const int64_t g = L / (grp * splits);
+    const int64_t base = g * grp;
+    const int64_t in_group = min(grp, pairs - base);
+    const int64_t w = L - g * grp * splits;
+    split = (int)(w / in_group);
+    rt = 2 * (base + (w - (int64_t)split * in_group)) + (blockIdx.x & 1);
+}
+
 }  // namespace
 
 int pair_stages(int nch, bool qres) {
@@ -133,8 +151,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(half_threads(REF), 1
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
     const bool leader = rank == 0;
-    const int64_t rt = blockIdx.x;
-    const int split = blockIdx.y;
+    int64_t rt;
+    int split;
+    pair_tile(a.splits, a.raster_pairs, rt, split);
     const int j0 = split * a.tiles_per_split;
     const int j1 = min(a.col_tiles, j0 + a.tiles_per_split);
     const int ntiles = j1 - j0;
@@ -192,10 +211,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(half_threads(REF), 1
             // both CTAs' copies complete their bytes on the even CTA's barriers
             const uint32_t qfull_lead = mapa_shared(smem_u32(qfull), 0);
             const uint32_t qrow0 = (uint32_t)(rt * nch) * BM;
+            // L2 priorities with resident Q: the pairs running at once stream
+            // the same K tiles, which are kept, while a Q tile is read once per
+            // pair and goes first.  A streamed Q tile is re-read for every
+            // column tile, so without resident Q neither operand is hinted.
+            const uint64_t keep = l2_evict_last();
             if (QRES) {
+                const uint64_t once = l2_evict_first();
                 if (leader) mbar_arrive_expect_tx(qfull, (uint32_t)(2 * nch * CHUNK_BYTES));
                 for (int c = 0; c < nch; ++c)
-                    tma_chunk_pair(sQ + c * CHUNK_BYTES, &tmQ, qrow0 + c * BM, qfull_lead);
+                    tma_chunk_pair_hint(sQ + c * CHUNK_BYTES, &tmQ, qrow0 + c * BM, qfull_lead, once);
             }
             int s = 0, issued = 0, bissued = 0;
             uint32_t ph = 0;
@@ -220,7 +245,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(half_threads(REF), 1
                     uint8_t* st = sStage + s * STAGE_BYTES;
                     const uint32_t full_lead = mapa_shared(smem_u32(&full[s]), 0);
                     if (leader) mbar_arrive_expect_tx(&full[s], 2 * STAGE_BYTES);
-                    tma_chunk_pair(st, &tmK, krow0 + c * BM, full_lead);
+                    if (QRES) tma_chunk_pair_hint(st, &tmK, krow0 + c * BM, full_lead, keep);
+                    else tma_chunk_pair(st, &tmK, krow0 + c * BM, full_lead);
                     if (!QRES) tma_chunk_pair(st + CHUNK_BYTES, &tmQ, qrow0 + c * BM, full_lead);
                     ++issued;
                     if (++s == stages) {
@@ -449,7 +475,7 @@ cudaError_t launch_half_pair_t(const TcHalfArgs& a, const TensorMap128& tmQ, con
     const cudaError_t e = cudaFuncSetAttribute(
         k_half_pair<QRES, REF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)row_tiles, (unsigned)a.splits);
+    const dim3 grid((unsigned)((int64_t)row_tiles * a.splits));
     k_half_pair<QRES, REF><<<grid, half_threads(REF), smem,
                              s>>>(tmQ, tmK, a);
     return cudaGetLastError();
@@ -457,7 +483,8 @@ cudaError_t launch_half_pair_t(const TcHalfArgs& a, const TensorMap128& tmQ, con
 
 cudaError_t launch_half_pair(const TcHalfArgs& a, const TensorMap128& tmQ,
                              const TensorMap128& tmK, int row_tiles, bool qres, cudaStream_t s) {
-    if (row_tiles % 2 != 0) return cudaErrorInvalidValue;
+    if (row_tiles % 2 != 0 || a.splits < 1 || (int64_t)row_tiles * a.splits > 0x7fffffff)
+        return cudaErrorInvalidValue;
     const size_t smem = pair_smem_bytes(a.nch, qres, a.stages);
     cudaError_t e;
     if (a.use_ref)
