@@ -231,14 +231,14 @@ __device__ __forceinline__ void tmem_reg_fence(float (&v)[N]) {
                      "+f"(v[i + 5]), "+f"(v[i + 6]), "+f"(v[i + 7]));
 }
 
-// warp: the same value x into 32 consecutive columns of the warp's 32 lanes
-__device__ __forceinline__ void tmem_fill32(uint32_t taddr, float x) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, "
-        "%1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1};" ::"r"(taddr),
-        "f"(x)
-        : "memory");
+// warp: the same value x into 8 consecutive columns of the warp's 32 lanes
+// (a store names one source register per column, so the 32-column form keeps
+// 32 registers live where this one keeps 8)
+__device__ __forceinline__ void tmem_fill8(uint32_t taddr, float x) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %1, %1, %1, %1, %1, %1, %1};" ::"r"(
+                     taddr),
+                 "f"(x)
+                 : "memory");
 }
 // warp: 8 registers into 8 consecutive columns of the warp's 32 lanes
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {

@@ -54,9 +54,15 @@ struct TcHalfArgs {
 // Groups of the reference-offset half-update (fs_tc_ref.cu): four groups of
 // four warps, one per TMEM buffer, each issuing its own copies and MMAs.
 constexpr int kRefGroups = 4;
-// Threads of the CTA-pair half-update: producer, MMA warp and two (online)
-// or four (reference offsets) epilogue groups.
-constexpr int half_threads(bool ref) { return 32 * (2 + (ref ? kRefGroups : kHalfGroups) * kEpiWarps); }
+// Epilogue groups of the CTA-pair half-update with reference offsets: two
+// per TMEM buffer, each owning half of its columns (one group per buffer,
+// with the registers of 10 warps instead of 18, ran 2 % slower at d = 512).
+constexpr int kPairRefGroups = 4;
+// Threads of the CTA-pair half-update: producer, MMA warp and the epilogue
+// groups (two with online maxima).
+constexpr int half_threads(bool ref) {
+    return 32 * (2 + (ref ? kPairRefGroups : kHalfGroups) * kEpiWarps);
+}
 
 // Guarded range of a reference-offset sum (see the FMA path).
 constexpr float kTcMinRefSum = 5.421010862427522e-20f;   // 2^-64

@@ -26,10 +26,11 @@
 //              online mode: two groups, tile t going to group t mod 2, a
 //              thread reading its 256 scores in two halves and folding them
 //              into a running max and sum;
-//              reference mode: four groups, two per TMEM buffer, each owning
-//              one 128-column half: the group pre-loads its accumulators
-//              with -M / kappa' (M = the row's previous LSE), then streams its
-//              half in 32-column slices and only sums 2^{acc kappa' + bias}.
+//              reference mode: kPairRefGroups groups spread over the two
+//              TMEM buffers, each owning an equal share of a buffer's
+//              columns: the group pre-loads its accumulators with
+//              -M / kappa' (M = the row's previous LSE), then streams its
+//              share in 32-column slices and only sums 2^{acc kappa' + bias}.
 // Bias slices go through a ring of 8, so the producer never waits on them
 // before issuing K chunks.
 #include "fs_tc.cuh"
@@ -44,7 +45,7 @@ constexpr int kPairBufs = 2;                // TMEM buffers of BNP columns
 constexpr int kPairTmemCols = kPairBufs * BNP;
 constexpr int kPairBiasBytes = BNP * 4;
 constexpr int kPairBiasSlots = 8;
-constexpr int kPairMaxGroups = kRefGroups;
+constexpr int kPairMaxGroups = kPairRefGroups > kHalfGroups ? kPairRefGroups : kHalfGroups;
 
 __host__ __device__ constexpr int pair_fixed_bytes(int nch, bool qres) {
     return 1024 + (qres ? nch * CHUNK_BYTES : 0) + kPairBiasSlots * kPairBiasBytes +
@@ -112,15 +113,16 @@ __device__ __forceinline__ void fold128(float* v, const float4* sb, uint64_t ks2
 // are reused from L2 by the later splits instead of being read again from
 // DRAM once every row tile of a split has streamed past.
 __device__ __forceinline__ void pair_tile(int splits, int raster_pairs, int64_t& rt, int& split) {
-    const int64_t pairs = gridDim.x / (2 * (int64_t)splits);
-    const int64_t grp = raster_pairs > 0 ? min((int64_t)raster_pairs, pairs) : pairs;
-    const int64_t L = blockIdx.x >> 1;
-    const int64_t g = L / (grp * splits);
-    const int64_t base = g * grp;
-    const int64_t in_group = min(grp, pairs - base);
-    const int64_t w = L - g * grp * splits;
+    // gridDim.x < 2^31 (checked at launch), so every quantity fits 32 bits
+    const uint32_t pairs = gridDim.x / (2u * (uint32_t)splits);
+    const uint32_t grp = raster_pairs > 0 ? min((uint32_t)raster_pairs, pairs) : pairs;
+    const uint32_t L = blockIdx.x >> 1;
+    const uint32_t g = L / (grp * (uint32_t)splits);
+    const uint32_t base = g * grp;
+    const uint32_t in_group = min(grp, pairs - base);
+    const uint32_t w = L - g * grp * (uint32_t)splits;
     split = (int)(w / in_group);
-    rt = 2 * (base + (w - (int64_t)split * in_group)) + (blockIdx.x & 1);
+    rt = 2 * (int64_t)(base + (w - (uint32_t)split * in_group)) + (blockIdx.x & 1);
 }
 
 }  // namespace
@@ -142,8 +144,12 @@ template <bool QRES, bool REF>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(half_threads(REF), 1)
     k_half_pair(const __grid_constant__ TensorMap128 tmQ, const __grid_constant__ TensorMap128 tmK,
                 TcHalfArgs a) {
-    constexpr int GROUPS = REF ? kRefGroups : kHalfGroups;
-    static_assert(!REF || GROUPS == 2 * kPairBufs, "reference mode: two groups per TMEM buffer");
+    constexpr int GROUPS = REF ? kPairRefGroups : kHalfGroups;
+    static_assert(!REF || GROUPS % kPairBufs == 0, "reference mode: equal groups per TMEM buffer");
+    // reference mode: groups per TMEM buffer, columns of one group's share
+    constexpr int SHARES = REF ? GROUPS / kPairBufs : 1;
+    constexpr int SHARE_COLS = BNP / SHARES;
+    static_assert(SHARE_COLS % 64 == 0, "a share is an even number of 32-column slices");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -184,8 +190,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(half_threads(REF), 1
             mbar_init(&empty[s], 1);
         }
         // a TMEM buffer is released by every epilogue warp that reads it, in
-        // both CTAs: one group per CTA (online), two (reference)
-        constexpr int readers = (REF ? 2 : 1) * kEpiWarps;
+        // both CTAs: one group per CTA (online), SHARES (reference)
+        constexpr int readers = SHARES * kEpiWarps;
         for (int b = 0; b < kPairBufs; ++b) {
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], 2 * readers);
@@ -335,15 +341,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(half_threads(REF), 1
         const uint32_t lofs = (uint32_t)(quarter * 32) << 16;
         float M = -INFINITY, S = 0.f;
         if constexpr (REF) {
-            // group g: TMEM buffer g / 2 (tiles t = g / 2 mod 2), column half g % 2
-            const int b = grp >> 1, h = grp & 1;
+            // group g: TMEM buffer g / SHARES (tiles t = that mod 2), column
+            // share g % SHARES
+            constexpr int SLICES = SHARE_COLS / 32;
+            const int b = grp / SHARES, h = grp % SHARES;
             const int64_t rr = row < a.nr ? row : a.nr - 1;
             M = a.rlogw2[rr] - a.rbias[rr];
-            const float fill = -M / ks;
-            const uint32_t buf = tmem + (uint32_t)(b * BNP + h * 128) + lofs;
+            const float fill = __fdividef(-M, ks);   // the offset only has to be M up to rounding
+            const uint32_t buf = tmem + (uint32_t)(b * BNP + h * SHARE_COLS) + lofs;
             const uint32_t tempty_lead = mapa_shared(smem_u32(&tempty[b]), 0);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_fill32(buf + q * 32, fill);
+            for (int q = 0; q < 4 * SLICES; ++q) tmem_fill8(buf + q * 8, fill);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -357,32 +365,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(half_threads(REF), 1
                 if (!mbar_wait(&bfull[bs], (uint32_t)((t / kPairBiasSlots) & 1), a.err,
                                ERR_TIMEOUT_EPILOGUE))
                     break;
-                const float4* sb =
-                    reinterpret_cast<const float4*>(sBias + bs * kPairBiasBytes) + h * 32;
+                const float4* sb = reinterpret_cast<const float4*>(sBias + bs * kPairBiasBytes) +
+                                   h * (SHARE_COLS / 4);
+                // slice q + 1 loads while slice q is summed; va holds the even
+                // slices, vb the odd ones.  The loop stays rolled: unrolled,
+                // the bias loads of later slices move up and spill registers.
                 float va[32], vb[32];
                 tmem_ld32(buf, va);
                 tmem_wait_ld();
                 tmem_reg_fence(va);
-                tmem_ld32(buf + 32, vb);
-                ref_slice(va, sb, ks2, acc);
-                tmem_wait_ld();
-                tmem_reg_fence(vb);
-                tmem_ld32(buf + 64, va);
-                ref_slice(vb, sb + 8, ks2, acc);
-                tmem_wait_ld();
-                tmem_reg_fence(va);
-                tmem_ld32(buf + 96, vb);
-                ref_slice(va, sb + 16, ks2, acc);
-                tmem_wait_ld();
-                tmem_reg_fence(vb);
-                // the half is in registers: pre-load it again, hand it back
+#pragma unroll 1
+                for (int q = 0; q < SLICES; q += 2) {
+                    tmem_ld32(buf + (q + 1) * 32, vb);
+                    ref_slice(va, sb + q * 8, ks2, acc);
+                    tmem_wait_ld();
+                    tmem_reg_fence(vb);
+                    if (q + 2 < SLICES) {
+                        tmem_ld32(buf + (q + 2) * 32, va);
+                        ref_slice(vb, sb + (q + 1) * 8, ks2, acc);
+                        tmem_wait_ld();
+                        tmem_reg_fence(va);
+                    }
+                }
+                // the share is in registers: pre-load it again, hand it back
 #pragma unroll
-                for (int q = 0; q < 4; ++q) tmem_fill32(buf + q * 32, fill);
+                for (int q = 0; q < 4 * SLICES; ++q) tmem_fill8(buf + q * 8, fill);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_remote(tempty_lead);
-                ref_slice(vb, sb + 24, ks2, acc);
+                ref_slice(vb, sb + (SLICES - 1) * 8, ks2, acc);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bempty[bs]);
             }
