@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -164,13 +165,21 @@ def kernel_family(d: int, tensor_path: bool) -> str:
     return "tc" if d <= 128 else "pair"
 
 
+def _code_only(text: str) -> str:
+    """C++ source without its comments and blank lines, each line stripped:
+    a change to a comment alone leaves the hash below unchanged."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.strip() for line in text.splitlines() if line.strip())
+
+
 def _kernel_source_hash(family: str):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "streaming_sinkhorn_solver_gb300", "csrc")
     for name in sorted(KERNEL_SOURCES[family]):
-        with open(os.path.join(csrc, name), "rb") as fh:
+        with open(os.path.join(csrc, name), encoding="utf-8") as fh:
             h.update(name.encode())
-            h.update(fh.read())
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -14,13 +14,15 @@
 // read and 4 KB of B written per 128 clocks (~96 B/clk), and its copy ring
 // covers twice the latency for the same bytes.
 //
-// Roles (320 threads per CTA, clusters of 2 along x):
+// Roles (320 threads per CTA with online maxima, 576 with reference offsets;
+// clusters of 2 along x):
 //   warp 0     producer, both CTAs: own Q tile once, then per 256-column tile
-//              the 1 KB bias slice and its own 128-row half of every K chunk;
+//              the 1 KB bias slice and its own 128-row half of every K chunk,
+//              the Q and K copies completing their bytes on the even CTA's
+//              barriers (the even producer's expect_tx covers both halves);
 //   warp 1     even CTA: issues the pair MMAs into TMEM buffer t mod 2 and
-//              commits with multicast to both CTAs' barriers;
-//              odd CTA: relays "my half of this stage has landed" (and "my Q
-//              has landed") to the even CTA's barriers with remote arrives;
+//              commits with multicast to both CTAs' barriers; odd CTA: only
+//              allocates and frees the pair's TMEM with the even one;
 //   warps 2-   epilogue groups, one thread per row, releasing TMEM buffers
 //              to the even CTA's barrier (local and remote arrivals):
 //              online mode: two groups, tile t going to group t mod 2, a

@@ -73,3 +73,14 @@ def test_metric_points_cover_every_configuration_with_long_regions():
     assert bench.point_steps(300.0) == bench.POINT_MIN_STEPS
     assert bench.point_steps(1.0) * 1.0 >= bench.POINT_MIN_MS
     assert bench.point_steps(1e-6) == bench.POINT_MAX_STEPS
+
+
+def test_kernel_source_hash_ignores_comments_only():
+    """The committed ncu summaries stay attached to their kernels through
+    comment edits, and detach on any code change."""
+    import bench
+    code = "int f(int x) {\n  return x + 1;  // one more\n}\n/* block\n comment */\n"
+    assert bench._code_only(code) == bench._code_only(
+        "int f(int x) {\n\n    return x + 1;   // another comment\n}\n")
+    assert bench._code_only(code) != bench._code_only("int f(int x) {\n  return x + 2;\n}\n")
+
