@@ -516,7 +516,7 @@ fs_status fs_debug_bounds(int32_t* enabled, uint64_t* first_violation);
 /*
  * fs_fixup_stats -- reference-offset diagnostics (no counterpart on the
  * pages).  After its first iterations a large solve (from 2^26 score pairs;
- * tensor path up to d = 512) takes each row's exponent offset from the row's
+ * tensor path up to d = 1024) takes each row's exponent offset from the row's
  * previous LogSumExp instead of a running max, range-checks the resulting
  * sum once per row and recomputes the rows that fail with an FP32 fixup
  * kernel.  The library counts, per device, the fixup passes that ran (one

@@ -87,7 +87,7 @@ struct TcFixArgs {
     unsigned int* fix_count;
     unsigned long long* fix_stats;   // [2] launches, rows recomputed (or nullptr)
 };
-constexpr int kFixMaxDim = 512;
+constexpr int kFixMaxDim = 1024;   // reference offsets on the tensor path up to this d
 cudaError_t launch_fix_tc(const TcFixArgs& a, cudaStream_t s);
 
 cudaError_t launch_prep_side(const float* P, const float* w, int64_t rows, int d,

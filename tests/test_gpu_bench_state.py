@@ -2,7 +2,7 @@
 
 The throughput workloads run their whole iteration count from a cold start:
 two iterations with the online row max, then (from 2^26 score pairs, tensor
-path up to d = 512) reference offsets -- each row's previous LSE as its
+path up to d = 1024) reference offsets -- each row's previous LSE as its
 exponent offset, a guarded sum and an FP32 fixup of the rows that fail it.
 "FlashSinkhorn" (gist.science, Method 1) reaches the same iterates as the
 plain log-domain update, so parity has to hold at that iteration count, in
@@ -60,8 +60,8 @@ def _cmax_rows(P, Q, idx):
 
 def _ref_iterations(w):
     """Reference-offset half-update pairs a solve of workload w runs (two
-    online iterations per call; tensor path only up to d = 512)."""
-    if w.n * w.m < 2 ** 26 or w.d > 512:
+    online iterations per call; tensor path only up to d = 1024)."""
+    if w.n * w.m < 2 ** 26 or w.d > 1024:
         return 0
     return sum(max(it - 2, 0) for _, it in w.stages)
 
@@ -117,5 +117,25 @@ def test_recipe_at_2_26_pairs_full_iterations_element_wise(name, d):
     print(f"{name} d={d} at 8192^2: {fixed} rows recomputed over {launches} fixup passes")
     C = orc.cost(inp["X"], inp["Y"])
     fr, gr = orc.sinkhorn(C, inp["a"], inp["b"], eps, iters)
+    assert max_abs(np64(f), fr) <= F_TOL_TENSOR * C.max()
+    assert max_abs(np64(g), gr) <= F_TOL_TENSOR * C.max()
+
+
+def test_annealed_d1024_recipe_at_2_26_pairs_element_wise():
+    """The c5 recipe (d = 1024: CTA pairs with Q streamed through the ring)
+    at n = m = 8192, its whole schedule of ten eps stages of 20 warm-started
+    iterations: every call runs two online iterations, then reference offsets
+    with fixups; f and g element-wise against the float64 solve of the same
+    schedule."""
+    w = WORKLOADS["c5_n20k_m30k_d1024"]
+    inp = make_inputs("c5_n20k_m30k_d1024", n=8192, m=8192, seed=w.seed + 77)
+    t = to_dev(inp)
+    fs.fs_fixup_stats(reset=True)
+    f, g = _solve(t, w.stages)
+    launches, fixed = fs.fs_fixup_stats(reset=True)
+    assert launches == 2 * sum(it - 2 for _, it in w.stages)
+    print(f"c5 recipe at 8192^2: {fixed} rows recomputed over {launches} fixup passes")
+    C = orc.cost(inp["X"], inp["Y"])
+    fr, gr = orc.sinkhorn_stages(C, inp["a"], inp["b"], w.stages)
     assert max_abs(np64(f), fr) <= F_TOL_TENSOR * C.max()
     assert max_abs(np64(g), gr) <= F_TOL_TENSOR * C.max()

@@ -211,10 +211,12 @@ def test_full_size_plan_application_on_sampled_rows(name):
     assert rel_l2(np64(out)[rows], ref) <= APPLY_TOL
 
 
-@pytest.mark.parametrize("d,eps,iters", [(64, 0.01, 6), (64, 0.1, 10), (256, 0.02, 6)])
+@pytest.mark.parametrize("d,eps,iters", [(64, 0.01, 6), (64, 0.1, 10), (256, 0.02, 6),
+                                         (1024, 0.02, 6)])
 def test_reference_offset_path_with_fixups(d, eps, iters):
     """n*m = 2^26 takes reference offsets after the first iterations (one-CTA
-    kernel at d = 64, CTA pairs at d = 256).  A cold start at small eps moves
+    kernel at d = 64, CTA pairs at d = 256, CTA pairs with Q streamed through
+    the ring at d = 1024).  A cold start at small eps moves
     the LSEs far between iterations, so many rows fail the guarded range and
     are recomputed by the FP32 fixup; the potentials must still match."""
     inp = make_inputs("c3_n50k_d64", n=8192, m=8192, d=d, seed=93)
