@@ -84,3 +84,26 @@ def test_marginal_residuals(d, iters):
     assert abs(c - ref_c) <= APPLY_TOL * mass
     if iters >= 40:
         assert r < 1e-3 * mass
+
+
+@pytest.mark.parametrize("d,iters", [(3, 3), (3, 40), (64, 3)])
+def test_marginals_element_wise(d, iters):
+    """The marginals themselves: P1 (the plan application with V = 1) and
+    P^T 1 (the transposed application with U = 1), row by row and column by
+    column against the oracle's plan sums, each within 1e-3 relative (sums of
+    positive plan entries); the residuals the library reports are the L1
+    distances of those vectors to a and b, up to the rounding of the sums."""
+    eps = 0.1
+    n, m = 900, 800
+    inp, C, f32, g32 = _state(n, m, d, 41 + d + iters, eps, iters)
+    row, col = orc.marginals(C, inp["a"], inp["b"], eps, f32, g32)
+    t = to_dev(dict(inp, f=f32, g=g32, V=np.ones((m, 1), np.float32),
+                    U=np.ones((n, 1), np.float32)))
+    P1 = np64(fs.fs_apply_plan(t["X"], t["a"], t["Y"], t["b"], eps, t["f"], t["g"], t["V"]))[:, 0]
+    PT1 = np64(fs.fs_apply_plan_t(t["X"], t["a"], t["Y"], t["b"], eps, t["f"], t["g"], t["U"]))[:, 0]
+    assert np.max(np.abs(P1 - row) / row) <= APPLY_TOL
+    assert np.max(np.abs(PT1 - col) / col) <= APPLY_TOL
+    r, c = fs.fs_marginal_residuals(t["X"], t["a"], t["Y"], t["b"], eps, t["f"], t["g"])
+    mass = float(inp["a"].sum())
+    assert abs(r - float(np.abs(P1 - inp["a"]).sum())) <= 1e-5 * mass
+    assert abs(c - float(np.abs(PT1 - inp["b"]).sum())) <= 1e-5 * mass
