@@ -1555,45 +1555,60 @@ constexpr int kSpFixClusterBlocks = 608;    // 76 clusters of 8, all resident at
 constexpr unsigned int kSpFixRowsWide = kSpFixBlocks;
 
 // (max, sum) of one row's scores over the kept-list entries [eb, ee), in the
-// calling CTA's fixed order.
+// calling CTA's fixed order.  A half-CTA folds kSpFixInFlight of its entries
+// per step (every other entry of the range), and the list entries of the
+// next step load while the records of this one do, so each step waits on one
+// memory latency, not two.
+constexpr int kSpFixInFlight = 4;
 template <int D>
 __device__ __forceinline__ float2 fix_fold(const SpHalfArgs& a, int64_t row, const int* lst, int eb,
                                            int ee, float2* s_part) {
     constexpr int RS = fma_stride(D);
+    constexpr int U = kSpFixInFlight;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int hc = threadIdx.x >> 7, col_in = threadIdx.x & (kSB - 1);
     float q[D];
 #pragma unroll
     for (int k = 0; k < D; ++k) q[k] = a.rows[row * RS + k] * a.kappa;
     float M = -INFINITY, S = 0.f;
-    for (int e0 = eb + hc; e0 < ee; e0 += 8) {
-        // this half-CTA's entries e0, e0 + 2, e0 + 4, e0 + 6
-        float sc[4];
+    int Jn[U];   // the next step's kept blocks (-1: past the range)
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < U; ++u) {
+        const int e = eb + hc + 2 * u;
+        Jn[u] = e < ee ? lst[e] : -1;
+    }
+    for (int e0 = eb + hc; e0 < ee; e0 += 2 * U) {
+        int J[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            J[u] = Jn[u];
+            const int e = e0 + 2 * U + 2 * u;
+            Jn[u] = e < ee ? lst[e] : -1;
+        }
+        float sc[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
             sc[u] = -INFINITY;
-            const int e = e0 + 2 * u;
-            if (e < ee) {
-                const int J = lst[e];
-                const int64_t col = (int64_t)J * kSB + col_in;
-                if (FS_IDX_OK(J, a.nbi, 41) && col < a.nc) {
-                    float cv[RS];
-                    ld_rec<RS>(a.cols + col * RS, cv);
-                    float v = cv[D];
+            const int64_t col = (int64_t)J[u] * kSB + col_in;
+            if (J[u] >= 0 && FS_IDX_OK(J[u], a.nbi, 41) && col < a.nc) {
+                float cv[RS];
+                ld_rec<RS>(a.cols + col * RS, cv);
+                float v = cv[D];
 #pragma unroll
-                    for (int k = 0; k < D; ++k) v = fmaf(q[k], cv[k], v);
-                    sc[u] = v;
-                }
+                for (int k = 0; k < D; ++k) v = fmaf(q[k], cv[k], v);
+                sc[u] = v;
             }
         }
-        const float m = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+        float m = sc[0];
+#pragma unroll
+        for (int u = 1; u < U; ++u) m = fmaxf(m, sc[u]);
         if (m > M) {
             S = (M == -INFINITY ? 0.f : S * ex2(M - m));
             M = m;
         }
         if (M != -INFINITY) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) S += ex2(sc[u] - M);
+            for (int u = 0; u < U; ++u) S += ex2(sc[u] - M);
         }
     }
 #pragma unroll
@@ -1634,7 +1649,7 @@ __device__ __forceinline__ void fix_done(const SpHalfArgs& a, unsigned int cnt) 
 }
 
 template <int D>
-__global__ void __launch_bounds__(256) k_sp_fix_rows(const __grid_constant__ SpHalfArgs a) {
+__global__ void __launch_bounds__(256, 8) k_sp_fix_rows(const __grid_constant__ SpHalfArgs a) {
     __shared__ unsigned int s_cnt;
     __shared__ float2 s_part[8];
     if (threadIdx.x == 0) s_cnt = min(*(volatile unsigned int*)&a.fix_count[0], (unsigned int)a.nr);
@@ -1653,7 +1668,7 @@ __global__ void __launch_bounds__(256) k_sp_fix_rows(const __grid_constant__ SpH
 }
 
 template <int D>
-__global__ void __cluster_dims__(kSpFixCluster, 1, 1) __launch_bounds__(256)
+__global__ void __cluster_dims__(kSpFixCluster, 1, 1) __launch_bounds__(256, 8)
     k_sp_fix_split(const __grid_constant__ SpHalfArgs a) {
     __shared__ unsigned int s_cnt;
     __shared__ float2 s_part[8];
