@@ -229,12 +229,15 @@ def test_reference_offset_path_with_fixups(d, eps, iters):
 
 @pytest.mark.parametrize("n,m,d,splits", [(8250, 8300, 40, 0), (8200, 8192, 100, 0),
                                           (8192, 8192, 128, 0), (8192, 8192, 64, 1),
-                                          (8192, 8192, 64, 4)])
+                                          (8192, 8192, 64, 4), (8200, 8300, 1000, 1),
+                                          (8300, 8200, 1000, 0)])
 def test_reference_offset_kernel_shapes(n, m, d, splits):
-    """The reference-offset one-CTA kernel at n*m >= 2^26: one K chunk with
-    zero-padded dimensions (d = 40), two chunks (d = 100, 128), ragged row
-    and column tiles, and forced column splits (1: the guard in the kernel
-    itself; 4: the guard in the split merge)."""
+    """The reference-offset kernels at n*m >= 2^26: the one-CTA kernel with
+    one K chunk and zero-padded dimensions (d = 40), two chunks (d = 100,
+    128), ragged row and column tiles, and forced column splits (1: the guard
+    in the kernel itself; 4: the guard in the split merge); the CTA-pair
+    kernel with Q streamed through the ring (d = 1000: 16 chunks, the last
+    zero-padded) with ragged tiles, unsplit and split."""
     inp = make_inputs("c3_n50k_d64", n=n, m=m, d=d, seed=94 + d)
     C = orc.cost(inp["X"], inp["Y"])
     f, g, _ = _solve(inp, [(0.05, 6)], path="auto", splits=splits)
