@@ -177,6 +177,43 @@ def test_marginal_residuals_vanish_at_convergence():
     assert np.abs(col - c["b"]).sum() < 1e-13
 
 
+def test_entropic_duality_links_dual_value_transport_cost_and_marginals():
+    """For any potentials the plan's form gives log(P_ij / (a_i b_j)) =
+    (f_i + g_j - C_ij)/eps, hence sum_ij P_ij log(P_ij / (a_i b_j)) =
+    (<f, P1> + <g, P^T 1> - <P, C>)/eps.  At the Sinkhorn fixed point P1 = a
+    and P^T 1 = b, and this is strong duality of entropic OT:
+    <a, f> + <b, g> = <P, C> + eps KL(P | a x b).  The entropy term is
+    evaluated here from the plan's definition on a scipy cost matrix, so
+    the identity ties the oracle's marginals, transport cost and dual value
+    to each other and to the plan."""
+    c = _cloud(40, 35, 3, 12, weights="lognormal")
+    a = c["a"].astype(np.float64)
+    b = c["b"].astype(np.float64)
+    Cs = cdist(c["X"].astype(np.float64), c["Y"].astype(np.float64), "sqeuclidean")
+    C = orc.cost(c["X"], c["Y"])
+    eps = orc.as_eps(0.3)
+
+    def entropy_term(f, g):
+        logr = (f[:, None] + g[None, :] - Cs) / eps        # log(P / (a x b))
+        P = a[:, None] * b[None, :] * np.exp(logr)
+        return float((P * logr).sum())
+
+    # any potentials: the identity with the realised marginals
+    f, g = orc.sinkhorn(C, c["a"], c["b"], eps, 3)
+    g = g + 0.05                                           # off the last g-update
+    row, col = orc.marginals(C, c["a"], c["b"], eps, f, g)
+    tc = orc.transport_cost(C, c["a"], c["b"], eps, f, g)
+    lhs = float(f @ row + g @ col)
+    assert abs(lhs - (tc + eps * entropy_term(f, g))) <= 1e-12 * max(1.0, abs(lhs))
+    # the fixed point: strong duality with the dual value
+    f, g = orc.sinkhorn(C, c["a"], c["b"], eps, 500)
+    tc = orc.transport_cost(C, c["a"], c["b"], eps, f, g)
+    gap = abs(float(a.sum() - b.sum()))                    # float32 weights: masses differ slightly
+    dual = orc.dual(c["a"], c["b"], f, g)
+    scale = float(np.abs(f).max() + np.abs(g).max())
+    assert abs(dual - (tc + eps * entropy_term(f, g))) <= 1e-10 + 4 * gap * scale
+
+
 # --- invariances ------------------------------------------------------------
 
 def test_gauge_invariance_of_plan_and_update_equivariance():

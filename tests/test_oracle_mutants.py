@@ -31,6 +31,10 @@ MUTANTS = [
     ("prop1_no_ynorm", "orc_f_update_prop1", "double ghat = g[j] - yy;", "double ghat = g[j];"),
     ("cosine_no_factor2", "orc_cost_cosine", "- 2.0 * cosv;", "- cosv;"),
     ("cosine_no_ynorm", "orc_cost_cosine", "dot / (nx * ny[j])", "dot / nx"),
+    ("tc_no_a", "orc_transport_cost", "(double)a[i] * (double)b[j] * exp", "(double)b[j] * exp"),
+    ("tc_g_sign", "orc_transport_cost", "exp((f[i] + g[j] - C[i * m + j]) / eps)",
+     "exp((f[i] - g[j] - C[i * m + j]) / eps)"),
+    ("marg_col_no_b", "orc_marginals", "col[j] = s;", "col[j] = s / (double)b[j];"),
 ]
 
 PINS = [
@@ -47,6 +51,7 @@ PINS = [
     lambda: pins.test_grad_x_matches_finite_differences(),
     lambda: pins.test_cosine_cost_special_values(),
     lambda: pins.test_cosine_cost_equals_squared_euclidean_on_unit_rows(),
+    lambda: pins.test_entropic_duality_links_dual_value_transport_cost_and_marginals(),
 ]
 
 
@@ -69,7 +74,8 @@ def _function_span(src: str, fname: str):
 def test_pins_catch_planted_mistakes(tmp_path, name, fname, old, new):
     src = orc.source_text()
     # the definition of fname (skip forward declarations and calls)
-    key = {"lse": "static double lse(", "sqdist": "static double sqdist("}.get(fname, "void " + fname + "(")
+    key = {"lse": "static double lse(", "sqdist": "static double sqdist(",
+           "orc_transport_cost": "double orc_transport_cost("}.get(fname, "void " + fname + "(")
     s0 = src.index(key)
     _, s1 = _function_span(src, key[:-1])
     body = src[s0:s1]
